@@ -1,0 +1,234 @@
+"""Independent fp64 forms used to pin the oracle (test helpers, CPU only).
+
+1. ``ogd_steps``: each step is literally "one normalized gradient step on the
+   instantaneous objective" (agihunt explainer, Method; paperlayer §3.1, §4.4),
+   with the gradient taken by torch autograd and the smoothness scale taken as
+   the top eigenvalue (numpy ``eigvalsh``) of the data term's curvature
+   (paperlayer §3.1: "L_t = ||x_t||^2 + lambda_t"; §C.6 / sungsoo post: Falcon-3
+   uses lambda_max of the window covariance). It shares no arithmetic with the
+   oracle's hand-written update. Valid only while the decay clamp is inactive.
+
+2. ``chunk_forward``: the chunk-parallel form (paperlayer Figure 2, §D.1, §E.2,
+   §F.2, §H.3): per chunk, one unit-lower-triangular solve whose right-hand side
+   merges the value path and the projected-history path, log-prefix decay reset
+   to zero at every chunk start, a read-after-write masked output and a carried
+   state. With ``C >= T`` it is the masked-parallel form (one dense solve over
+   the whole sequence, paperlayer Figure 2 "Masked-parallel form"). Its algebra
+   comes from unrolling the recurrence inside a chunk; only exp(L_a - L_b) with
+   a >= b is ever formed, so nothing overflows when the clamp binds.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+F1, F1A, F2, F3 = 1, 2, 3, 5
+
+
+def _np(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().double().numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+def _global_pairs(k, v, pos, tail, W):
+    """Key/value lookup by global 1-based index (0 for indices <= 0)."""
+    T, dk = k.shape
+    dv = v.shape[1]
+
+    def key(i):
+        if i <= 0:
+            return np.zeros(dk)
+        if i <= pos:
+            return tail[0][i - (pos - W + 1)]
+        return k[i - pos - 1]
+
+    def val(i):
+        if i <= 0:
+            return np.zeros(dv)
+        if i <= pos:
+            return tail[1][i - (pos - W + 2)]
+        return v[i - pos - 1]
+
+    return key, val
+
+
+# --------------------------------------------------------------------------------------
+# 1. autograd gradient steps
+# --------------------------------------------------------------------------------------
+
+def ogd_steps(variant, q, k, v, beta, lam, S0=None, *, pos=0, tail=None, W=1, eps=1e-6, eps_gamma=1e-6):
+    """One sequence: q,k [T,dk], v [T,dv], beta [T] or [T,dv], lam [T]."""
+    q, k, v, beta, lam, S0 = (_np(a) for a in (q, k, v, beta, lam, S0))
+    T, dk = q.shape
+    dv = v.shape[1]
+    key, val = _global_pairs(k, v, pos, tail, W)
+    S = np.zeros((dk, dv)) if S0 is None else S0.copy()
+    out = np.zeros((T, dv))
+    for t in range(T):
+        tau = pos + t + 1
+        win = W if variant == F3 else 1
+        js = [j for j in range(tau - win + 1, tau + 1) if j >= 2]
+        if js:
+            xs = [key(j - 1) for j in js]
+            ys = [val(j) for j in js]
+            nb = len(js)
+            Sv = torch.tensor(S, requires_grad=True)
+            lt = float(lam[t])
+            if variant == F1A:
+                x, y = torch.tensor(xs[0]), torch.tensor(ys[0])
+                data = -(y @ (Sv.T @ x))
+            else:
+                data = sum(0.5 * torch.sum((torch.tensor(y) - Sv.T @ torch.tensor(x)) ** 2)
+                           for x, y in zip(xs, ys)) / nb
+            loss = data + 0.5 * lt * torch.sum(Sv ** 2)
+            (grad,) = torch.autograd.grad(loss, Sv)
+            grad = grad.numpy()
+            if variant == F1A:
+                smooth = float(np.dot(xs[0], xs[0]))  # write-energy normaliser (paperlayer "inner-product variants")
+            else:
+                cov = sum(np.outer(x, x) for x in xs) / nb  # curvature of the data term, per column
+                smooth = float(np.linalg.eigvalsh(cov).max())
+            den = smooth + lt + eps
+            if variant == F2:
+                eta = np.where(den == 0, 0.0, beta[t] / den)  # [dv]
+                assert np.all(eta * lt < 1 - eps_gamma), "clamp active: autograd form does not apply"
+                S = S - grad * eta[None, :]
+            else:
+                eta = 0.0 if den == 0 else float(beta[t]) / den
+                assert eta * lt < 1 - eps_gamma, "clamp active: autograd form does not apply"
+                S = S - eta * grad
+        out[t] = S.T @ q[t]
+    return out, S
+
+
+# --------------------------------------------------------------------------------------
+# 2. chunk-parallel (and, with C >= T, masked-parallel) form
+# --------------------------------------------------------------------------------------
+
+def _scalars(betas, lams, den, first_mask, eps_gamma):
+    eta = np.where(den == 0, 0.0, betas / np.where(den == 0, 1.0, den))
+    eta = np.where(first_mask, 0.0, eta)
+    alpha = np.minimum(eta * lams, 1.0 - eps_gamma)
+    alpha = np.where(first_mask, 0.0, alpha)
+    return eta, alpha
+
+
+def _lambda_max_small(g):
+    return float(np.linalg.eigvalsh(g).max()) if g.size else 0.0
+
+
+def chunk_forward(variant, q, k, v, beta, lam, S0=None, *, C, pos=0, tail=None, W=1, eps=1e-6,
+                  eps_gamma=1e-6):
+    """One sequence, fp64. Returns (out [T,dv], S_final [dk,dv])."""
+    q, k, v, beta, lam, S0 = (_np(a) for a in (q, k, v, beta, lam, S0))
+    T, dk = q.shape
+    dv = v.shape[1]
+    key, val = _global_pairs(k, v, pos, tail, W)
+    S = np.zeros((dk, dv)) if S0 is None else S0.copy()
+    out = np.zeros((T, dv))
+    for t0 in range(0, T, C):
+        t1 = min(T, t0 + C)
+        n = t1 - t0
+        taus = np.arange(pos + t0 + 1, pos + t1 + 1)
+        Q = q[t0:t1]
+        lm = lam[t0:t1]
+        if variant in (F1, F1A, F2):
+            X = np.stack([key(int(tau) - 1) for tau in taus])
+            Y = v[t0:t1]
+            first = taus == 1
+            den = np.sum(X * X, axis=1) + lm + eps
+            G = X @ X.T
+            Sc = Q @ X.T
+            if variant == F2:
+                eta, alpha = _scalars(beta[t0:t1], lm[:, None], den[:, None], first[:, None], eps_gamma)
+            else:
+                eta, alpha = _scalars(beta[t0:t1], lm, den, first, eps_gamma)
+            Lc = np.cumsum(np.log1p(-alpha), axis=0)            # inclusive prefix, reset per chunk
+            Lx = np.concatenate([np.zeros_like(Lc[:1]), Lc[:-1]], axis=0)  # exclusive prefix
+            LC = Lc[-1]
+            lower = np.tril(np.ones((n, n)), -1)
+            incl = np.tril(np.ones((n, n)), 0)
+            if variant == F2:
+                R = np.zeros((n, dv))
+                O = np.zeros((n, dv))
+                Snew = np.zeros_like(S)
+                for c in range(dv):
+                    Ec = np.exp(np.minimum(Lx[:, c][:, None] - Lc[:, c][None, :], 0.0)) * lower
+                    A = eta[None, :, c] * Ec * G
+                    rhs = Y[:, c] - np.exp(Lx[:, c]) * (X @ S[:, c])
+                    r = np.linalg.solve(np.eye(n) + A, rhs)
+                    Pc = eta[None, :, c] * np.exp(np.minimum(Lc[:, c][:, None] - Lc[:, c][None, :], 0.0)) * incl * Sc
+                    O[:, c] = np.exp(Lc[:, c]) * (Q @ S[:, c]) + Pc @ r
+                    w = eta[:, c] * np.exp(LC[c] - Lc[:, c])
+                    Snew[:, c] = np.exp(LC[c]) * S[:, c] + X.T @ (w * r)
+                out[t0:t1] = O
+                S = Snew
+                continue
+            E = np.exp(np.minimum(Lx[:, None] - Lc[None, :], 0.0)) * lower
+            A = eta[None, :] * E * G
+            P = eta[None, :] * np.exp(np.minimum(Lc[:, None] - Lc[None, :], 0.0)) * incl * Sc
+            if variant == F1:
+                R = np.linalg.solve(np.eye(n) + A, Y - np.exp(Lx)[:, None] * (X @ S))
+            else:
+                R = Y
+            out[t0:t1] = np.exp(Lc)[:, None] * (Q @ S) + P @ R
+            w = eta * np.exp(LC - Lc)
+            S = np.exp(LC) * S + X.T @ (w[:, None] * R)
+        else:  # Falcon-3: rank-W system over (token, window slot) unknowns
+            ne = n + W - 1
+            js = np.arange(int(taus[0]) - W + 1, int(taus[-1]) + 1)     # global pair indices
+            valid_e = js >= 2
+            Xe = np.stack([key(int(j) - 1) if j >= 2 else np.zeros(dk) for j in js])
+            Ye = np.stack([val(int(j)) if j >= 2 else np.zeros(dv) for j in js])
+            Ge = Xe @ Xe.T
+            Sce = Q @ Xe.T
+            eta = np.zeros(n)
+            alpha = np.zeros(n)
+            kap = np.zeros(n)
+            for i in range(n):
+                ps = [i - a + W - 1 for a in range(W) if valid_e[i - a + W - 1]]
+                if not ps:
+                    continue
+                nb = len(ps)
+                mu = _lambda_max_small(Ge[np.ix_(ps, ps)] / nb)
+                den = mu + lm[i] + eps
+                eta[i] = 0.0 if den == 0 else beta[t0 + i] / den
+                alpha[i] = min(eta[i] * lm[i], 1.0 - eps_gamma)
+                kap[i] = eta[i] / nb
+            Lc = np.cumsum(np.log1p(-alpha))
+            Lx = np.concatenate([[0.0], Lc[:-1]])
+            LC = Lc[-1]
+            m = n * W
+            A = np.zeros((m, m))
+            rhs = np.zeros((m, dv))
+            XeS = Xe @ S
+            for i in range(n):
+                for a in range(W):
+                    pa = i - a + W - 1
+                    if not valid_e[pa]:
+                        continue
+                    rhs[i * W + a] = Ye[pa] - np.exp(Lx[i]) * XeS[pa]
+                    for l in range(i):
+                        f = kap[l] * np.exp(Lx[i] - Lc[l])
+                        for b in range(W):
+                            pb = l - b + W - 1
+                            if valid_e[pb]:
+                                A[i * W + a, l * W + b] = f * Ge[pa, pb]
+            R = np.linalg.solve(np.eye(m) + A, rhs)
+            Ps = np.zeros((n, m))
+            Xw = np.zeros((m, dk))
+            for l in range(n):
+                for b in range(W):
+                    pb = l - b + W - 1
+                    if not valid_e[pb]:
+                        continue
+                    Xw[l * W + b] = kap[l] * np.exp(LC - Lc[l]) * Xe[pb]
+                    for i in range(l, n):
+                        Ps[i, l * W + b] = kap[l] * np.exp(Lc[i] - Lc[l]) * Sce[i, pb]
+            out[t0:t1] = np.exp(Lc)[:, None] * (Q @ S) + Ps @ R
+            S = np.exp(LC) * S + Xw.T @ R
+    return out, S
