@@ -1,0 +1,382 @@
+"""Falcon forward throughput on GB300: tokens/s through the C ABI, roofline, oracle baseline.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one full forward pass of the workload (all its segments) over one
+batch of synthetic input already resident in HBM. Rank 0 prints one JSON line.
+Under torchrun each rank runs the whole workload on its own GPU (sequences are
+independent, so there is no data-path collective: weak scaling); the value is
+all ranks' tokens over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def _algorithmic_bytes(w, es):
+    """Bytes every step must move at least once: inputs read, outputs written."""
+    BH = w.batch * w.heads
+    tok = BH * w.seqlen
+    per_seg = tok * (2 * w.dk + w.dv) * es + tok * w.dv * es + tok * 4 * (w.dv if w.variant == "falcon2" else 1) \
+        + tok * 4 + BH * w.dk * w.dv * 4
+    tail = BH * (w.window * w.dk + (w.window - 1) * w.dv) * es
+    total = w.segments * (per_seg + tail)
+    total += (w.segments - 1) * (BH * w.dk * w.dv * 4 + tail)  # S0 and tail read by later segments
+    return total
+
+
+def _kernel_digest():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "weight_linear_attention_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload, kernel_id):
+    """DRAM bytes per launch from a committed ncu summary, only if taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(f"{workload}:{kernel_id}")
+    if not e or e.get("kernel_digest") != _kernel_digest():
+        return None
+    return e.get("dram_bytes_per_step")
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ".",
+                                 f".clocks_{os.getpid()}.csv")
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+        return dist, rank, world, local
+    return None, rank, world, local
+
+
+def _barrier_max(dist, value):
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, w):
+    """The oracle (fp64 C recurrence) as it stands, timed on the host cores."""
+    import oracle
+    from weight_linear_attention_gb300 import inputs as I
+
+    dist, rank, world, _ = _dist_setup()
+    if rank != 0:
+        return
+    oracle.build()
+    inp = I.make_inputs(w, seed=0)
+    cores = os.cpu_count() or 1
+    # Bounded sample: the first `bs` batch rows of every segment, all heads, all tokens.
+    bs = max(1, min(w.batch, args.ref_batch))
+    segs = []
+    for s in range(w.segments):
+        sl = slice(s * w.seqlen, (s + 1) * w.seqlen)
+        segs.append({n: inp[n][:bs, :, sl] for n in ("q", "k", "v", "beta", "lam")})
+
+    def step():
+        S, tail = None, None
+        for s, x in enumerate(segs):
+            _, S, tail = oracle.falcon_ref_fwd(w.variant_id, x["q"], x["k"], x["v"], x["beta"], x["lam"], S, tail,
+                                               pos=s * w.seqlen, window=w.window, eps=w.eps,
+                                               eps_gamma=w.eps_gamma, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    tokens = bs * w.seqlen * w.segments * args.steps
+    value = tokens / el
+    sample = f"batch rows 0..{bs - 1} of {w.batch}, all {w.heads} heads, all {w.seqlen * w.segments} tokens"
+    line = {
+        "impl": "reference", "metric": "falcon_fwd_tokens_per_s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "seq_len": w.seqlen * w.segments,
+                   "d": w.dk, "chunk": w.chunk, "variant": w.variant, "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, budget_s=12.0):
+    import oracle
+    from weight_linear_attention_gb300 import inputs as I
+
+    oracle.build()
+    cores = os.cpu_count() or 1
+    inp = I.make_inputs(w, seed=0)
+    bs = 1
+    x = {n: inp[n][:bs, :, :w.seqlen] for n in ("q", "k", "v", "beta", "lam")}
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        oracle.falcon_ref_fwd(w.variant_id, x["q"], x["k"], x["v"], x["beta"], x["lam"], window=w.window,
+                              eps=w.eps, eps_gamma=w.eps_gamma, nthreads=cores)
+        runs += 1
+        if time.perf_counter() - t0 > budget_s or runs >= 200:
+            break
+    el = time.perf_counter() - t0
+    return {"value": runs * bs * w.seqlen / el, "unit": "tokens/s", "cores": min(cores, bs * w.heads),
+            "kind": "oracle",
+            "sample": f"{runs} runs of batch row 0 ({w.heads} heads x {w.seqlen} tokens, first segment), "
+                      f"{el:.1f} s"}
+
+
+def run_ours(args, w):
+    import torch
+
+    from weight_linear_attention_gb300 import build as fbuild
+    from weight_linear_attention_gb300 import falcon as F
+    from weight_linear_attention_gb300 import inputs as I
+
+    dist, rank, world, local = _dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fbuild.build()
+    F.load()
+    es = 4 if w.dtype == "f32" else 2
+    inp = I.make_inputs(w, seed=0)
+    B, H, Ts, dk, dv, W = w.batch, w.heads, w.seqlen, w.dk, w.dv, w.window
+    dims = [F.make_dims(B, H, Ts, dk, dv, window=W, dtype=F.FALCON_F32 if w.dtype == "f32" else F.FALCON_BF16,
+                        pos=s * Ts, eps=w.eps, eps_gamma=w.eps_gamma) for s in range(w.segments)]
+    kernel_id = F.falcon_kernel_for(w.variant_id, dims[0], w.chunk)
+    step_bytes = _algorithmic_bytes(w, es)
+    nsets = max(2, -(-3 * L2_BYTES // step_bytes) + 1)  # rotating sets: > 3x L2 between reuses
+    stream = torch.cuda.Stream(device=dev)
+    tail_n = F.falcon_tail_bytes(dims[0]) // es
+
+    def seg_inputs(s):
+        sl = slice(s * Ts, (s + 1) * Ts)
+        return {n: inp[n][:, :, sl].contiguous() for n in ("q", "k", "v", "beta", "lam")}
+
+    host_segs = [seg_inputs(s) for s in range(w.segments)]
+    sets = []
+    for _ in range(nsets):
+        segs = []
+        for s in range(w.segments):
+            d = {n: host_segs[s][n].to(dev) for n in host_segs[s]}
+            d["out"] = torch.empty((B, H, Ts, dv), dtype=w.torch_dtype, device=dev)
+            d["S"] = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+            d["tail_out"] = torch.empty(tail_n, dtype=w.torch_dtype, device=dev)
+            segs.append(d)
+        sets.append(segs)
+
+    def launch(segs, strm):
+        for s, d in enumerate(segs):
+            prev = segs[s - 1] if s > 0 else None
+            st = F.falcon_fwd(w.variant_id, d["q"], d["k"], d["v"], d["beta"], d["lam"],
+                              prev["S"] if prev else None, prev["tail_out"] if prev else None,
+                              d["out"], d["S"], d["tail_out"], dims[s], w.chunk, strm.cuda_stream)
+            if st != 0:
+                raise F.FalconError(st)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            launch(sets[i % nsets], stream)
+        stream.synchronize()
+        if F.falcon_device_status(stream.cuda_stream) != 0:
+            raise SystemExit("device-side timeout during warm-up")
+        # ---- clock sampling starts here and runs through a ~1 s soak of the same launches
+        # (the last part of the warm-up) and the whole timed region.
+        clocks = Clocks(local) if rank == 0 else None
+        t_soak = time.perf_counter()
+        i = 0
+        while time.perf_counter() - t_soak < args.soak_s:
+            launch(sets[i % nsets], stream)
+            i += 1
+            if i % 64 == 0:
+                stream.synchronize()
+        stream.synchronize()
+        # ---- timed region: K steps, per-step events on the launching stream
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            launch(sets[i % nsets], stream)
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        clk = clocks.stop() if clocks else None
+        total_ms = t_start.elapsed_time(t_end)
+        per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+        if F.falcon_device_status(stream.cuda_stream) != 0:
+            raise SystemExit("device-side timeout during the timed region")
+
+        # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+        hsegs = [{n: t.pin_memory() for n, t in hs.items()} for hs in host_segs]
+        hout = [torch.empty((B, H, Ts, dv), dtype=w.torch_dtype).pin_memory() for _ in range(w.segments)]
+        e2e_sets = sets[:1]
+        h2d = sum(t.numel() * t.element_size() for hs in hsegs for t in hs.values())
+        d2h = sum(t.numel() * t.element_size() for t in hout)
+
+        def e2e_step():
+            segs = e2e_sets[0]
+            for s in range(w.segments):
+                for n in ("q", "k", "v", "beta", "lam"):
+                    segs[s][n].copy_(hsegs[s][n], non_blocking=True)
+            launch(segs, stream)
+            for s in range(w.segments):
+                hout[s].copy_(segs[s]["out"], non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(3, min(args.steps, 50))
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        stream.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    total_ms = _barrier_max(dist, total_ms)
+    ms_step = total_ms / args.steps
+    tokens_step = w.total_tokens
+    value = world * tokens_step * args.steps / (total_ms / 1e3)
+    e2e_ms = _barrier_max(dist, e2e_ms)
+    if rank != 0:
+        return
+    mean_launch = statistics.mean(per_launch_ms)
+    hbm, tfl, src = _peaks()
+    achieved = step_bytes / (mean_launch / 1e3) / 1e9
+    line = {
+        "metric": "falcon_fwd_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "variant": w.variant, "batch": B, "heads": H, "seq_len": Ts * w.segments,
+                   "segments": w.segments, "d": dk, "chunk": w.chunk, "window": W,
+                   "parallelism": f"dp{world} (independent sequences per GPU, no collective)",
+                   "l2": f"rotating {nsets} input/output sets of {step_bytes / 1e6:.1f} MB (> L2 between reuses)",
+                   "kernel": {1: "cuda-core chunk kernel", 2: "tcgen05/TMA chunk kernel"}.get(kernel_id, "?")},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": _traffic(w.name, kernel_id), "peak_source": src,
+                     "algorithmic_bytes_per_step": step_bytes, "mean_launch_ms": mean_launch},
+        "e2e": {"value": world * tokens_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * w.segments,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--ref-batch", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.0, help="seconds of warm-up launches under clock sampling")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from weight_linear_attention_gb300 import inputs as I
+
+    w = I.WORKLOADS[args.workload or I.HEADLINE]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,129 @@
+/*
+ * falcon.h — C ABI of the GB300 (sm_103a) Falcon fast-weight forward pass.
+ *
+ * The operation ("Fast Weight Attention for Continual Learning", arXiv
+ * 2608.27763; paperlayer.ai summary = [PL], agihunt.info explainer = [AH],
+ * sungsoo.github.io post = [SG]): for every (batch b, head h) sequence, steps
+ * tau = pos+1 .. pos+T update a fast-weight matrix S (dk x dv, fp32) with the
+ * prefix-aligned pair x_tau = k_{tau-1} (x_1 = 0), y_tau = v_tau
+ * ([PL] abstract, §3, Appendix p.34) and read o_tau = S_tau^T q_tau after the
+ * write ([AH] Method). With eta = beta / (||x||^2 + lambda + eps) (0 when the
+ * denominator is 0), alpha = min(eta*lambda, 1 - eps_gamma), gamma = 1 - alpha,
+ * and eta = alpha = 0 at tau = 1 ([PL] §3.1, §C.3, §4.6; [SG]):
+ *   FALCON_1   S = gamma S + eta x (y - S^T x)^T             ([AH] Method)
+ *   FALCON_1A  S = gamma S + eta x y^T                        ([AH] Method)
+ *   FALCON_2   as FALCON_1 with a per-column gain beta[..., c] ([PL] §1, Figure 5)
+ *   FALCON_3   window of the last `window` pairs (pair 1 excluded), residuals at
+ *              the pre-update state, step eta/B_tau, eta normalised by the top
+ *              eigenvalue of the window-averaged key covariance ([PL] §4.4, §C.6)
+ * The kernels evaluate it in the chunk-parallel form ([PL] Figure 2, §E.2, §F.2,
+ * §H.3): per chunk one unit-lower-triangular solve with the value and the
+ * projected-history right-hand sides merged, log-prefix decay reset to 0 at
+ * every chunk start ([PL] §D.1, §G.1), and a carried state between chunks.
+ *
+ * Memory: every pointer argument is DEVICE memory owned by the caller; the
+ * library keeps no pointer after a call returns and allocates nothing per call.
+ * Tensors are dense, row-major, contiguous, outermost dimension first.
+ * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ * stream). Argument checking is synchronous: on any nonzero return nothing was
+ * launched and no output was touched.
+ */
+#ifndef FALCON_H
+#define FALCON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FALCON_1 = 1,   /* scalar NLMS regression write                              */
+    FALCON_1A = 2,  /* scalar inner-product write                                */
+    FALCON_2 = 3,   /* per-column NLMS regression write                          */
+    FALCON_2A = 4,  /* per-column inner-product write: reserved, returns UNSUPPORTED */
+    FALCON_3 = 5,   /* sliding-window mini-batch regression write                */
+    FALCON_3A = 6   /* sliding-window inner-product write: reserved, returns UNSUPPORTED */
+} falcon_variant_t;
+
+typedef enum { FALCON_F32 = 0, FALCON_BF16 = 1 } falcon_dtype_t;
+
+/* Status codes returned by every entry point that returns int. */
+enum {
+    FALCON_OK = 0,
+    FALCON_ERR_INVALID_ARG = 1,   /* null required pointer, bad variant/window/chunk/dims, tail vs pos, overlap */
+    FALCON_ERR_UNSUPPORTED = 2,   /* a head size, dtype, window or chunk this build has no kernel for */
+    FALCON_ERR_MISALIGNED = 3,    /* a pointer not aligned as documented below */
+    FALCON_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    FALCON_ERR_DEVICE_TIMEOUT = 5 /* a kernel gave up a bounded wait (see falcon_device_status) */
+};
+
+/* Problem description. 64 bytes, no implicit padding. */
+typedef struct {
+    int64_t batch;    /* B >= 0                                                       */
+    int64_t heads;    /* H >= 0                                                       */
+    int64_t seqlen;   /* T >= 0 tokens in this call                                   */
+    int64_t dk;       /* key/query width: 16, 32, 64 or 128                           */
+    int64_t dv;       /* value width: 16, 32, 64 or 128                               */
+    int32_t window;   /* Falcon-3 window size 1..8; must be 1 for the other variants  */
+    int32_t dtype;    /* falcon_dtype_t of q, k, v, out, tail, tail_out                */
+    int64_t pos;      /* tokens already consumed by earlier calls; 0 = fresh start    */
+    float eps;        /* >= 0, added to the step-size denominator                     */
+    float eps_gamma;  /* in (0, 1): alpha is clamped to 1 - eps_gamma                 */
+} falcon_dims_t;
+
+/*
+ * falcon_fwd — one forward pass over T tokens of B*H sequences.
+ *   q, k      [B,H,T,dk] dtype        queries and keys (phi = identity; callers apply
+ *                                     QK-RMSNorm upstream, [PL] §5, [AH] Method)
+ *   v         [B,H,T,dv] dtype        values (targets y)
+ *   beta      fp32 [B,H,T], or [B,H,T,dv] for FALCON_2; gains, caller keeps them in (0,2)
+ *   lambda    fp32 [B,H,T], >= 0      ridge coefficients
+ *   S0        fp32 [B,H,dk,dv] or NULL (zero initial state)
+ *   tail      NULL iff pos == 0; else falcon_tail_bytes(dims) bytes in dtype laid out
+ *             per (b,h) as keys[window][dk] = k_{pos-window+1..pos} followed by
+ *             vals[window-1][dv] = v_{pos-window+2..pos} (entries with global index
+ *             <= 0 are zero); this is what tail_out of the previous call holds.
+ *             For window 1 it is the pending key k_pos alone ([PL] §C.7, §4.4).
+ *   out       [B,H,T,dv] dtype        o_t = S_t^T q_t; must not overlap any input
+ *   S_final   fp32 [B,H,dk,dv] or NULL; may be the same pointer as S0
+ *   tail_out  NULL or falcon_tail_bytes(dims) bytes: the tail for position pos+T;
+ *             must not overlap tail
+ *   dims      problem description (host pointer)
+ *   chunk     chunk length C: 16, 32 or 64; FALCON_3 needs chunk*window <= 128.
+ *             The result does not depend on C beyond fp32 rounding.
+ *   stream    cudaStream_t to launch on
+ * Alignment: q, k, v, out, tail, tail_out, S0, S_final 16 bytes; beta, lambda 4 bytes.
+ * Returns FALCON_OK or an error code; see falcon_status_string.
+ */
+int falcon_fwd(int variant, const void* q, const void* k, const void* v, const float* beta,
+               const float* lambda, const float* S0, const void* tail, void* out, float* S_final,
+               void* tail_out, const falcon_dims_t* dims, int chunk, void* stream);
+
+/* Bytes of one tail buffer for `dims` (all B*H sequences); 0 for a NULL or invalid dims. */
+size_t falcon_tail_bytes(const falcon_dims_t* dims);
+
+/* Static English text for a status code; never NULL. */
+const char* falcon_status_string(int status);
+
+/*
+ * Synchronizes `stream`, then reports whether any kernel of this library on the
+ * current device gave up a bounded device-side wait since the last call
+ * (FALCON_ERR_DEVICE_TIMEOUT), and clears that flag. Returns FALCON_ERR_CUDA if
+ * the synchronize fails, else FALCON_OK.
+ */
+int falcon_device_status(void* stream);
+
+/* Which kernel falcon_fwd would launch for these arguments (0 = none/invalid,
+ * 1 = CUDA-core chunk kernel, 2 = tcgen05/TMA chunk kernel). Host only, no launch. */
+int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk);
+
+/* ABI version of this header: 1. */
+int falcon_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FALCON_H */

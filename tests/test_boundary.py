@@ -1,0 +1,138 @@
+"""Host-only checks of the C ABI (no GPU needed, nothing is launched).
+
+Every falcon_fwd call below is invalid by construction, so the library must
+return its error code from the synchronous argument check before any launch.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from weight_linear_attention_gb300 import build as fbuild
+from weight_linear_attention_gb300 import falcon as F
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fbuild.build()
+    return F.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "falcon.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b(falcon_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert set(names) == set(F.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert F.falcon_abi_version() == 1
+
+
+def test_dims_struct_layout():
+    assert ctypes.sizeof(F.FalconDims) == 64
+    assert F.FalconDims.pos.offset == 48 and F.FalconDims.eps.offset == 56
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert F.status_string(s)
+    assert F.status_string(99) == "unknown status"
+
+
+def test_tail_bytes(lib):
+    d = F.make_dims(2, 3, 100, 64, 32, window=4, dtype=F.FALCON_BF16)
+    assert F.falcon_tail_bytes(d) == 2 * 3 * (4 * 64 + 3 * 32) * 2
+    d = F.make_dims(2, 3, 100, 64, 32, window=1, dtype=F.FALCON_F32)
+    assert F.falcon_tail_bytes(d) == 2 * 3 * 64 * 4
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(), 1),
+    (dict(dtype=F.FALCON_F32, dk=16, dv=16, chunk=16), 1),
+    (dict(variant=F.FALCON_3, window=4, chunk=32), 1),
+    (dict(variant=F.FALCON_2A), 0),                 # reserved variant
+    (dict(variant=F.FALCON_3A), 0),
+    (dict(variant=7), 0),
+    (dict(window=2), 0),                            # window only for Falcon-3
+    (dict(variant=F.FALCON_3, window=9, chunk=16), 0),
+    (dict(variant=F.FALCON_3, window=4, chunk=64), 0),  # chunk*window > 128
+    (dict(dk=48), 0),
+    (dict(dv=256), 0),
+    (dict(chunk=128), 0),
+    (dict(chunk=0), 0),
+    (dict(dtype=7), 0),
+    (dict(eps_gamma=0.0), 0),
+    (dict(eps_gamma=1.0), 0),
+    (dict(eps=-1.0), 0),
+    (dict(seqlen=-1), 0),
+])
+def test_kernel_for_validation(lib, case, expect):
+    c = dict(variant=F.FALCON_1, batch=8, heads=12, seqlen=1024, dk=64, dv=64, window=1, dtype=F.FALCON_BF16,
+             chunk=64)
+    c.update(case)
+    d = F.make_dims(c["batch"], c["heads"], c["seqlen"], c["dk"], c["dv"], window=c["window"], dtype=c["dtype"],
+                    eps=c.get("eps", 1e-6), eps_gamma=c.get("eps_gamma", 1e-6))
+    got = F.falcon_kernel_for(c["variant"], d, c["chunk"])
+    assert (got != 0) == bool(expect), (case, got)
+
+
+# Fake device addresses: never dereferenced because every call below is rejected.
+A = 1 << 40
+
+
+def _call(variant=F.FALCON_1, q=A, k=A + (1 << 30), v=A + (2 << 30), beta=A + (3 << 30), lam=A + (4 << 30),
+          S0=None, tail=None, out=A + (5 << 30), S_final=None, tail_out=None, dims=None, chunk=64):
+    if dims is None:
+        dims = F.make_dims(2, 2, 64, 64, 64)
+    return F.falcon_fwd(variant, q, k, v, beta, lam, S0, tail, out, S_final, tail_out, dims, chunk, stream=0)
+
+
+def test_null_required_pointers(lib):
+    for name in ("q", "k", "v", "beta", "lam", "out"):
+        assert _call(**{name: 0}) == F.FALCON_ERR_INVALID_ARG, name
+
+
+def test_misaligned_pointers(lib):
+    assert _call(q=A + 2) == F.FALCON_ERR_MISALIGNED
+    assert _call(out=A + (5 << 30) + 8) == F.FALCON_ERR_MISALIGNED
+    assert _call(S0=A + (6 << 30) + 4) == F.FALCON_ERR_MISALIGNED
+    assert _call(beta=A + (3 << 30) + 2) == F.FALCON_ERR_MISALIGNED
+
+
+def test_tail_and_pos_must_agree(lib):
+    d = F.make_dims(2, 2, 64, 64, 64, pos=10)
+    assert _call(dims=d) == F.FALCON_ERR_INVALID_ARG               # pos > 0 without a tail
+    assert _call(tail=A + (7 << 30)) == F.FALCON_ERR_INVALID_ARG   # tail with pos == 0
+
+
+def test_out_must_not_overlap_inputs(lib):
+    assert _call(out=A + 4096) == F.FALCON_ERR_INVALID_ARG          # inside q
+    assert _call(out=A + (2 << 30) - 4096) == F.FALCON_ERR_INVALID_ARG  # runs into v
+    assert _call(S0=A + (5 << 30), S_final=A + (8 << 30)) == F.FALCON_ERR_INVALID_ARG  # S0 inside out
+
+
+def test_tail_out_must_not_overlap_tail(lib):
+    d = F.make_dims(2, 2, 64, 64, 64, pos=10, eps_gamma=2.0)        # also invalid eps_gamma: never launches
+    assert _call(dims=d, tail=A + (7 << 30), tail_out=A + (7 << 30)) == F.FALCON_ERR_INVALID_ARG
+
+
+def test_unsupported_and_invalid_shapes(lib):
+    assert _call(dims=F.make_dims(2, 2, 64, 48, 64)) == F.FALCON_ERR_UNSUPPORTED
+    assert _call(variant=F.FALCON_2A) == F.FALCON_ERR_UNSUPPORTED
+    assert _call(variant=0) == F.FALCON_ERR_INVALID_ARG
+    assert _call(chunk=-4) == F.FALCON_ERR_INVALID_ARG
+    assert _call(chunk=24) == F.FALCON_ERR_UNSUPPORTED
+    assert _call(dims=F.make_dims(2, 2, 64, 64, 64, window=3)) == F.FALCON_ERR_INVALID_ARG
+
+
+def test_binding_raises_when_library_missing(tmp_path):
+    with pytest.raises(RuntimeError):
+        F.load(str(tmp_path / "nope.so"))

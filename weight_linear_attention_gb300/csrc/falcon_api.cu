@@ -1,0 +1,166 @@
+// C-ABI front end: argument checking and kernel dispatch for falcon_fwd.
+// The operation, layouts and error contract are documented in include/falcon.h.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/falcon.h"
+#include "falcon_internal.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool pow2_head(int64_t d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range_of(const void* p, size_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + bytes};
+}
+
+bool overlaps(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+size_t tail_bytes_of(const falcon_dims_t* d) {
+    const size_t es = d->dtype == FALCON_BF16 ? 2 : 4;
+    const size_t per = (size_t)d->window * (size_t)d->dk + (size_t)(d->window - 1) * (size_t)d->dv;
+    return (size_t)d->batch * (size_t)d->heads * per * es;
+}
+
+// Shape/variant/dtype/chunk checks (no pointers). Fills the size fields of `a`.
+int validate_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail, falcon::Launch* a) {
+    if (!d) return FALCON_ERR_INVALID_ARG;
+    if (variant == FALCON_2A || variant == FALCON_3A) return FALCON_ERR_UNSUPPORTED;
+    if (variant != FALCON_1 && variant != FALCON_1A && variant != FALCON_2 && variant != FALCON_3)
+        return FALCON_ERR_INVALID_ARG;
+    if (d->batch < 0 || d->heads < 0 || d->seqlen < 0 || d->pos < 0) return FALCON_ERR_INVALID_ARG;
+    if (d->dk <= 0 || d->dv <= 0) return FALCON_ERR_INVALID_ARG;
+    if (!pow2_head(d->dk) || !pow2_head(d->dv)) return FALCON_ERR_UNSUPPORTED;
+    if (d->dtype != FALCON_F32 && d->dtype != FALCON_BF16) return FALCON_ERR_UNSUPPORTED;
+    if (d->window < 1) return FALCON_ERR_INVALID_ARG;
+    if (variant != FALCON_3 && d->window != 1) return FALCON_ERR_INVALID_ARG;
+    if (d->window > 8) return FALCON_ERR_UNSUPPORTED;
+    if (!(d->eps >= 0.f) || !(d->eps_gamma > 0.f && d->eps_gamma < 1.f)) return FALCON_ERR_INVALID_ARG;
+    if (chunk != 16 && chunk != 32 && chunk != 64) return chunk <= 0 ? FALCON_ERR_INVALID_ARG : FALCON_ERR_UNSUPPORTED;
+    if (variant == FALCON_3 && chunk * d->window > 128) return FALCON_ERR_UNSUPPORTED;
+    if ((d->pos > 0) != has_tail) return FALCON_ERR_INVALID_ARG;
+    a->variant = variant;
+    a->B = d->batch;
+    a->H = d->heads;
+    a->T = d->seqlen;
+    a->dk = d->dk;
+    a->dv = d->dv;
+    a->pos = d->pos;
+    a->W = d->window;
+    a->bf16 = d->dtype == FALCON_BF16;
+    a->eps = d->eps;
+    a->eps_gamma = d->eps_gamma;
+    a->chunk = chunk;
+    if (falcon::generic_smem_bytes(*a, 16) > 200 * 1024 && !falcon::tc_supported(*a)) return FALCON_ERR_UNSUPPORTED;
+    return FALCON_OK;
+}
+
+// Full argument check; fills `a` on success.
+int validate(int variant, const void* q, const void* k, const void* v, const float* beta, const float* lambda,
+             const float* S0, const void* tail, void* out, float* S_final, void* tail_out, const falcon_dims_t* d,
+             int chunk, falcon::Launch* a) {
+    const int st = validate_shape(variant, d, chunk, tail != nullptr, a);
+    if (st != FALCON_OK) return st;
+    const int64_t BH = d->batch * d->heads;
+    const int64_t tokens = BH * d->seqlen;
+    const size_t es = d->dtype == FALCON_BF16 ? 2 : 4;
+    if (tokens > 0 && (!q || !k || !v || !beta || !lambda || !out)) return FALCON_ERR_INVALID_ARG;
+
+    const void* al16[] = {q, k, v, out, tail, tail_out, S0, S_final};
+    for (const void* p : al16)
+        if (p && !aligned(p, 16)) return FALCON_ERR_MISALIGNED;
+    if ((beta && !aligned(beta, 4)) || (lambda && !aligned(lambda, 4))) return FALCON_ERR_MISALIGNED;
+
+    // out must not overlap any input; tail_out must not overlap tail; S_final may equal S0 exactly.
+    if (tokens > 0) {
+        const Range ro = range_of(out, (size_t)tokens * d->dv * es);
+        const size_t bcols = variant == FALCON_2 ? (size_t)d->dv : 1;
+        const Range ins[] = {
+            range_of(q, (size_t)tokens * d->dk * es), range_of(k, (size_t)tokens * d->dk * es),
+            range_of(v, (size_t)tokens * d->dv * es), range_of(beta, (size_t)tokens * bcols * 4),
+            range_of(lambda, (size_t)tokens * 4),
+            S0 ? range_of(S0, (size_t)BH * d->dk * d->dv * 4) : Range{0, 0},
+            tail ? range_of(tail, tail_bytes_of(d)) : Range{0, 0},
+            S_final ? range_of(S_final, (size_t)BH * d->dk * d->dv * 4) : Range{0, 0},
+            tail_out ? range_of(tail_out, tail_bytes_of(d)) : Range{0, 0},
+        };
+        for (const Range& r : ins)
+            if (overlaps(ro, r)) return FALCON_ERR_INVALID_ARG;
+    }
+    if (tail && tail_out && overlaps(range_of(tail, tail_bytes_of(d)), range_of(tail_out, tail_bytes_of(d))))
+        return FALCON_ERR_INVALID_ARG;
+    if (S0 && S_final && S0 != S_final &&
+        overlaps(range_of(S0, (size_t)BH * d->dk * d->dv * 4), range_of(S_final, (size_t)BH * d->dk * d->dv * 4)))
+        return FALCON_ERR_INVALID_ARG;
+
+    a->q = q;
+    a->k = k;
+    a->v = v;
+    a->beta = beta;
+    a->lam = lambda;
+    a->S0 = S0;
+    a->tail = tail;
+    a->out = out;
+    a->S_final = S_final;
+    a->tail_out = tail_out;
+    return FALCON_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int falcon_abi_version(void) { return 1; }
+
+size_t falcon_tail_bytes(const falcon_dims_t* d) {
+    if (!d || d->batch < 0 || d->heads < 0 || d->dk <= 0 || d->dv <= 0 || d->window < 1) return 0;
+    return tail_bytes_of(d);
+}
+
+const char* falcon_status_string(int s) {
+    switch (s) {
+        case FALCON_OK: return "ok";
+        case FALCON_ERR_INVALID_ARG: return "invalid argument";
+        case FALCON_ERR_UNSUPPORTED: return "unsupported size, dtype, window, chunk or variant";
+        case FALCON_ERR_MISALIGNED: return "pointer not aligned as required";
+        case FALCON_ERR_CUDA: return "CUDA runtime error";
+        case FALCON_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk) {
+    falcon::Launch a = {};
+    if (validate_shape(variant, dims, chunk, dims && dims->pos > 0, &a) != FALCON_OK) return 0;
+    return falcon::tc_supported(a) ? 2 : 1;
+}
+
+int falcon_fwd(int variant, const void* q, const void* k, const void* v, const float* beta, const float* lambda,
+               const float* S0, const void* tail, void* out, float* S_final, void* tail_out,
+               const falcon_dims_t* dims, int chunk, void* stream) {
+    falcon::Launch a = {};
+    const int st = validate(variant, q, k, v, beta, lambda, S0, tail, out, S_final, tail_out, dims, chunk, &a);
+    if (st != FALCON_OK) return st;
+    if (a.B * a.H == 0) return FALCON_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (falcon::tc_supported(a)) return falcon::launch_tc(a, s);
+    return falcon::launch_generic(a, s);
+}
+
+int falcon_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FALCON_ERR_CUDA;
+    int flag = 0;
+    if (falcon::tc_consume_timeout_flag(&flag) != 0) return FALCON_ERR_CUDA;
+    return flag ? FALCON_ERR_DEVICE_TIMEOUT : FALCON_OK;
+}
+
+}  // extern "C"

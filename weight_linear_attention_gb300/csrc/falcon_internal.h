@@ -1,0 +1,43 @@
+// Internal interface between the C-ABI front end (falcon_api.cu) and the kernels.
+// Not installed; the public interface is include/falcon.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace falcon {
+
+enum Variant { kF1 = 1, kF1A = 2, kF2 = 3, kF3 = 5 };
+
+// Arguments after validation by falcon_fwd: sizes are in range, pointers are
+// non-null where required and aligned, tail is present iff pos > 0.
+struct Launch {
+    int variant;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* beta;
+    const float* lam;
+    const float* S0;      // may be null
+    const void* tail;     // null iff pos == 0
+    void* out;
+    float* S_final;       // may be null
+    void* tail_out;       // may be null
+    int64_t B, H, T, dk, dv, pos;
+    int W;
+    int bf16;             // 1: q/k/v/out/tail are bf16, 0: fp32
+    float eps, eps_gamma;
+    int chunk;
+};
+
+// CUDA-core chunk kernel: every variant, both dtypes, all supported sizes.
+int launch_generic(const Launch& a, cudaStream_t stream);
+size_t generic_smem_bytes(const Launch& a, int dvs);
+
+// tcgen05 / TMA chunk kernel (Falcon-1 and 1A, bf16, dk = dv = 64, chunk 64).
+bool tc_supported(const Launch& a);
+int launch_tc(const Launch& a, cudaStream_t stream);
+// Reads and clears the device-side timeout flag of the tcgen05 kernel (synchronous).
+int tc_consume_timeout_flag(int* flag);
+
+}  // namespace falcon

@@ -16,7 +16,8 @@ Recipe (every workload, seed 0 unless a caller passes another):
   q and k: RMSNorm over the feature axis (no gain, eps 1e-6; the pages' blocks
   use QK-RMSNorm upstream of the fast-memory update), then cast to the dtype.
   v: cast to the dtype directly. beta = sigmoid(logit); lambda = sigmoid(logit +
-  shift) or a constant. beta and lambda stay fp32. S0 stays fp32.
+  shift) or a constant. beta and lambda stay fp32. S0 = N(0,1)/sqrt(dk) in fp32,
+  so that the first reads S0^T q have the values' unit scale.
 """
 
 from __future__ import annotations
@@ -104,7 +105,7 @@ def make_inputs(w: Workload, seed: int = 0, seqlen: int | None = None, batch: in
     bshape = (B, H, T, dv) if w.variant == "falcon2" else (B, H, T)
     beta_logit = torch.randn(*bshape, generator=g)
     lam_logit = torch.randn(B, H, T, generator=g)
-    S0 = torch.randn(B, H, dk, dv, generator=g) if w.nonzero_s0 else None
+    S0 = torch.randn(B, H, dk, dv, generator=g) / dk ** 0.5 if w.nonzero_s0 else None
     dt = w.torch_dtype
     out = {
         "q": _rmsnorm(q).to(dt),
