@@ -205,6 +205,40 @@ def cpu_baseline(w, budget_s=12.0):
                       f"{el:.1f} s"}
 
 
+def _e2e(args, w, host_segs, dev_segs, launch, stream):
+    """Same metric through the C ABI with host buffers: per step, pinned host->device copies of the
+    inputs, the forward pass, and a device->host copy of the output, all inside the timed region."""
+    import torch
+
+    B, H, Ts, dv = w.batch, w.heads, w.seqlen, w.dv
+    hsegs = [{n: t.pin_memory() for n, t in hs.items()} for hs in host_segs]
+    hout = [torch.empty((B, H, Ts, dv), dtype=w.torch_dtype).pin_memory() for _ in range(w.segments)]
+    h2d = sum(t.numel() * t.element_size() for hs in hsegs for t in hs.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def step():
+        for s in range(w.segments):
+            for n in ("q", "k", "v", "beta", "lam"):
+                dev_segs[s][n].copy_(hsegs[s][n], non_blocking=True)
+        launch(dev_segs, stream)
+        for s in range(w.segments):
+            hout[s].copy_(dev_segs[s]["out"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n = max(3, min(args.steps, 50))
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        stream.synchronize()
+    return e0.elapsed_time(e1) / n, h2d, d2h
+
+
 def run_ours(args, w):
     import torch
 
@@ -295,35 +329,11 @@ def run_ours(args, w):
         if F.falcon_device_status(stream.cuda_stream) != 0:
             raise SystemExit("device-side timeout during the timed region")
 
-        # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
-        hsegs = [{n: t.pin_memory() for n, t in hs.items()} for hs in host_segs]
-        hout = [torch.empty((B, H, Ts, dv), dtype=w.torch_dtype).pin_memory() for _ in range(w.segments)]
-        e2e_sets = sets[:1]
-        h2d = sum(t.numel() * t.element_size() for hs in hsegs for t in hs.values())
-        d2h = sum(t.numel() * t.element_size() for t in hout)
 
-        def e2e_step():
-            segs = e2e_sets[0]
-            for s in range(w.segments):
-                for n in ("q", "k", "v", "beta", "lam"):
-                    segs[s][n].copy_(hsegs[s][n], non_blocking=True)
-            launch(segs, stream)
-            for s in range(w.segments):
-                hout[s].copy_(segs[s]["out"], non_blocking=True)
-
-        for _ in range(max(3, args.warmup)):
-            e2e_step()
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e2e_steps = max(3, min(args.steps, 50))
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        stream.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-
+    if args.no_e2e:
+        e2e_ms, h2d, d2h = float("nan"), 0, 0
+    else:
+        e2e_ms, h2d, d2h = _e2e(args, w, host_segs, sets[0], launch, stream)
     total_ms = _barrier_max(dist, total_ms)
     ms_step = total_ms / args.steps
     tokens_step = w.total_tokens
@@ -346,7 +356,7 @@ def run_ours(args, w):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": _traffic(w.name, kernel_id), "peak_source": src,
                      "algorithmic_bytes_per_step": step_bytes, "mean_launch_ms": mean_launch},
-        "e2e": {"value": world * tokens_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": None if args.no_e2e else {"value": world * tokens_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * w.segments,
         "clocks": clk,
@@ -366,12 +376,19 @@ def main():
     ap.add_argument("--ref-batch", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.0, help="seconds of warm-up launches under clock sampling")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--seqlen", type=int, default=None, help="override the workload's tokens per call")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     from weight_linear_attention_gb300 import inputs as I
 
     w = I.WORKLOADS[args.workload or I.HEADLINE]
+    if args.seqlen is not None:
+        w = w.with_(seqlen=args.seqlen)
+    if args.batch is not None:
+        w = w.with_(batch=args.batch)
     if args.impl == "reference":
         run_reference(args, w)
     else:

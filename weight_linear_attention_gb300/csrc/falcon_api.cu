@@ -5,7 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
-#include "../../include/falcon.h"
+#include "falcon.h"
 #include "falcon_internal.h"
 
 namespace {
