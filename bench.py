@@ -259,6 +259,8 @@ def run_ours(args, w):
     dims = [F.make_dims(B, H, Ts, dk, dv, window=W, dtype=F.FALCON_F32 if w.dtype == "f32" else F.FALCON_BF16,
                         pos=s * Ts, eps=w.eps, eps_gamma=w.eps_gamma) for s in range(w.segments)]
     kernel_id = F.falcon_kernel_for(w.variant_id, dims[0], w.chunk)
+    if args.single_pass and kernel_id == 3:
+        kernel_id = 2
     step_bytes = _algorithmic_bytes(w, es)
     nsets = max(2, -(-3 * L2_BYTES // step_bytes) + 1)  # rotating sets: > 3x L2 between reuses
     stream = torch.cuda.Stream(device=dev)
@@ -280,12 +282,15 @@ def run_ours(args, w):
             segs.append(d)
         sets.append(segs)
 
+    # one scratch workspace (the split path's M, U and chunk-start states), reused by every step
+    ws = F.workspace_for(w.variant_id, dims[0], w.chunk, dev) if not args.single_pass else None
+
     def launch(segs, strm):
         for s, d in enumerate(segs):
             prev = segs[s - 1] if s > 0 else None
             st = F.falcon_fwd(w.variant_id, d["q"], d["k"], d["v"], d["beta"], d["lam"],
                               prev["S"] if prev else None, prev["tail_out"] if prev else None,
-                              d["out"], d["S"], d["tail_out"], dims[s], w.chunk, strm.cuda_stream)
+                              d["out"], d["S"], d["tail_out"], dims[s], w.chunk, ws, stream=strm.cuda_stream)
             if st != 0:
                 raise F.FalconError(st)
 
@@ -352,13 +357,14 @@ def run_ours(args, w):
                    "segments": w.segments, "d": dk, "chunk": w.chunk, "window": W,
                    "parallelism": f"dp{world} (independent sequences per GPU, no collective)",
                    "l2": f"rotating {nsets} input/output sets of {step_bytes / 1e6:.1f} MB (> L2 between reuses)",
-                   "kernel": {1: "cuda-core chunk kernel", 2: "tcgen05/TMA chunk kernel"}.get(kernel_id, "?")},
+                   "kernel": {1: "cuda-core chunk kernel", 2: "single-pass tcgen05/TMA chunk kernel",
+                              3: "split path: tcgen05 prep, mma.sync chain, tcgen05 output kernels"}.get(kernel_id, "?")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": _traffic(w.name, kernel_id), "peak_source": src,
                      "algorithmic_bytes_per_step": step_bytes, "mean_launch_ms": mean_launch},
         "e2e": None if args.no_e2e else {"value": world * tokens_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * w.segments,
+        "gpu_launches": args.steps * w.segments * (3 if kernel_id == 3 else 1),
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -379,6 +385,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--seqlen", type=int, default=None, help="override the workload's tokens per call")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
+    ap.add_argument("--single-pass", action="store_true", help="no workspace: time the single-pass kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

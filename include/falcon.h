@@ -20,9 +20,14 @@
  * §H.3): per chunk one unit-lower-triangular solve with the value and the
  * projected-history right-hand sides merged, log-prefix decay reset to 0 at
  * every chunk start ([PL] §D.1, §G.1), and a carried state between chunks.
+ * Falcon-1 and 1A at bf16, dk = dv = 64, chunk 64 also have a split path that
+ * uses a caller-provided workspace: every chunk's state-independent part
+ * (the solve and the chunk transition S -> M S + U it implies) is computed for
+ * all chunks at once, then a short scan carries the state, then every chunk's
+ * reads are formed at once.
  *
  * Memory: every pointer argument is DEVICE memory owned by the caller; the
- * library keeps no pointer after a call returns and allocates nothing per call.
+ * library keeps no pointer after a call returns and allocates no device memory.
  * Tensors are dense, row-major, contiguous, outermost dimension first.
  * Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  * stream). Argument checking is synchronous: on any nonzero return nothing was
@@ -93,13 +98,28 @@ typedef struct {
  *   dims      problem description (host pointer)
  *   chunk     chunk length C: 16, 32 or 64; FALCON_3 needs chunk*window <= 128.
  *             The result does not depend on C beyond fp32 rounding.
+ *   workspace NULL, or scratch device memory of at least
+ *             falcon_workspace_bytes(variant, dims, chunk) bytes that overlaps no other
+ *             argument. When that size is nonzero and the workspace is given, the split
+ *             path runs; with NULL the single-pass kernels run (same results up to fp32
+ *             rounding). Contents on entry are ignored and on return unspecified; calls
+ *             that may run at the same time must not share a workspace.
+ *   workspace_bytes  size of `workspace` (ignored when workspace is NULL); a given
+ *             workspace smaller than falcon_workspace_bytes() is FALCON_ERR_INVALID_ARG
  *   stream    cudaStream_t to launch on
- * Alignment: q, k, v, out, tail, tail_out, S0, S_final 16 bytes; beta, lambda 4 bytes.
+ * Alignment: q, k, v, out, tail, tail_out, S0, S_final 16 bytes; workspace 256 bytes;
+ * beta, lambda 4 bytes.
  * Returns FALCON_OK or an error code; see falcon_status_string.
  */
 int falcon_fwd(int variant, const void* q, const void* k, const void* v, const float* beta,
                const float* lambda, const float* S0, const void* tail, void* out, float* S_final,
-               void* tail_out, const falcon_dims_t* dims, int chunk, void* stream);
+               void* tail_out, const falcon_dims_t* dims, int chunk, void* workspace,
+               size_t workspace_bytes, void* stream);
+
+/* Workspace bytes that enable the split path of falcon_fwd for these arguments
+ * (B*H*ceil(T/64) * 64 KiB for Falcon-1/1A, bf16, dk = dv = 64, chunk 64; 0 when
+ * no path uses a workspace or the arguments are invalid). Host only. */
+size_t falcon_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk);
 
 /* Bytes of one tail buffer for `dims` (all B*H sequences); 0 for a NULL or invalid dims. */
 size_t falcon_tail_bytes(const falcon_dims_t* dims);
@@ -115,11 +135,13 @@ const char* falcon_status_string(int status);
  */
 int falcon_device_status(void* stream);
 
-/* Which kernel falcon_fwd would launch for these arguments (0 = none/invalid,
- * 1 = CUDA-core chunk kernel, 2 = tcgen05/TMA chunk kernel). Host only, no launch. */
+/* Which kernels falcon_fwd launches for these arguments when it is given
+ * falcon_workspace_bytes() of workspace (0 = none/invalid, 1 = CUDA-core chunk
+ * kernel, 2 = single-pass tcgen05/TMA chunk kernel, 3 = split path: prep, chain
+ * and output kernels). Without a workspace, 3 becomes 2. Host only, no launch. */
 int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk);
 
-/* ABI version of this header: 1. */
+/* ABI version of this header: 2. */
 int falcon_abi_version(void);
 
 #ifdef __cplusplus

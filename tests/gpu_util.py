@@ -45,13 +45,14 @@ def tol(dtype) -> float:
 
 
 def run_gpu(variant, inp, *, pos=0, window=1, chunk=64, S0=None, tail=None, eps=1e-6, eps_gamma=1e-6,
-            dev="cuda"):
-    """inp: dict of CPU tensors q,k,v,beta,lam. Returns CPU tensors (out, S_final, tail_flat)."""
+            dev="cuda", split=True):
+    """inp: dict of CPU tensors q,k,v,beta,lam. Returns CPU tensors (out, S_final, tail_flat).
+    split=True passes a workspace (the split path where one exists); False runs the single-pass kernels."""
     g = {n: inp[n].to(dev).contiguous() for n in ("q", "k", "v", "beta", "lam")}
     S0d = S0.to(dev).contiguous() if S0 is not None else None
     taild = tail.to(dev).contiguous() if tail is not None else None
     out, S, t = F.forward(variant, g["q"], g["k"], g["v"], g["beta"], g["lam"], S0d, taild, pos=pos,
-                          window=window, chunk=chunk, eps=eps, eps_gamma=eps_gamma)
+                          window=window, chunk=chunk, eps=eps, eps_gamma=eps_gamma, split=split)
     torch.cuda.synchronize()
     assert F.falcon_device_status() == F.FALCON_OK
     return out.cpu(), S.cpu(), t.cpu()

@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(F.EXPORTED), names
     for n in names:
         assert hasattr(lib, n), n
-    assert F.falcon_abi_version() == 1
+    assert F.falcon_abi_version() == 2
 
 
 def test_dims_struct_layout():
@@ -89,10 +89,12 @@ A = 1 << 40
 
 
 def _call(variant=F.FALCON_1, q=A, k=A + (1 << 30), v=A + (2 << 30), beta=A + (3 << 30), lam=A + (4 << 30),
-          S0=None, tail=None, out=A + (5 << 30), S_final=None, tail_out=None, dims=None, chunk=64):
+          S0=None, tail=None, out=A + (5 << 30), S_final=None, tail_out=None, dims=None, chunk=64, ws=None,
+          ws_bytes=0):
     if dims is None:
         dims = F.make_dims(2, 2, 64, 64, 64)
-    return F.falcon_fwd(variant, q, k, v, beta, lam, S0, tail, out, S_final, tail_out, dims, chunk, stream=0)
+    return F.falcon_fwd(variant, q, k, v, beta, lam, S0, tail, out, S_final, tail_out, dims, chunk, ws, ws_bytes,
+                        stream=0)
 
 
 def test_null_required_pointers(lib):
@@ -131,6 +133,44 @@ def test_unsupported_and_invalid_shapes(lib):
     assert _call(chunk=-4) == F.FALCON_ERR_INVALID_ARG
     assert _call(chunk=24) == F.FALCON_ERR_UNSUPPORTED
     assert _call(dims=F.make_dims(2, 2, 64, 64, 64, window=3)) == F.FALCON_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(), 3),                                           # Falcon-1, bf16, 64, chunk 64: split path
+    (dict(variant=F.FALCON_1A), 3),
+    (dict(variant=F.FALCON_1, seqlen=0), 1),          # nothing to split: no workspace, CUDA-core kernel
+    (dict(chunk=32), 1),
+    (dict(dtype=F.FALCON_F32), 1),
+    (dict(variant=F.FALCON_2), 1),
+    (dict(dk=32, dv=32), 1),
+])
+def test_kernel_choice(lib, case, expect):
+    c = dict(variant=F.FALCON_1, seqlen=1024, dk=64, dv=64, dtype=F.FALCON_BF16, chunk=64)
+    c.update(case)
+    d = F.make_dims(8, 12, c["seqlen"], c["dk"], c["dv"], dtype=c["dtype"])
+    assert F.falcon_kernel_for(c["variant"], d, c["chunk"]) == expect
+
+
+def test_workspace_bytes(lib):
+    # B*H*ceil(T/64) chunks of 64 KiB: M (hi, lo), U, the chunk-start state (hi, lo) and T (hi, lo)
+    assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(8, 12, 1024, 64, 64), 64) == 8 * 12 * 16 * 65536
+    assert F.falcon_workspace_bytes(F.FALCON_1A, F.make_dims(2, 3, 65, 64, 64), 64) == 2 * 3 * 2 * 65536
+    assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 0, 64, 64), 64) == 0
+    assert F.falcon_workspace_bytes(F.FALCON_2, F.make_dims(2, 3, 64, 64, 64), 64) == 0
+    assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 64, 64, 64, dtype=F.FALCON_F32), 64) == 0
+    assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 64, 64, 64), 32) == 0
+    assert F.falcon_workspace_bytes(F.FALCON_2A, F.make_dims(2, 3, 64, 64, 64), 64) == 0
+
+
+def test_workspace_checks(lib):
+    need = F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 2, 64, 64, 64), 64)
+    W = A + (9 << 30)
+    assert _call(ws=W, ws_bytes=need - 1) == F.FALCON_ERR_INVALID_ARG      # too small
+    assert _call(ws=W + 128, ws_bytes=need) == F.FALCON_ERR_MISALIGNED    # 256-byte alignment
+    assert _call(ws=A + 4096, ws_bytes=need) == F.FALCON_ERR_INVALID_ARG   # overlaps q
+    assert _call(ws=A + (5 << 30) - 4096, ws_bytes=need) == F.FALCON_ERR_INVALID_ARG  # runs into out
+    # a well-formed workspace with an otherwise invalid call is still rejected before any launch
+    assert _call(ws=W, ws_bytes=need, chunk=24) == F.FALCON_ERR_UNSUPPORTED
 
 
 def test_binding_raises_when_library_missing(tmp_path):

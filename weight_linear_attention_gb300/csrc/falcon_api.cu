@@ -67,7 +67,7 @@ int validate_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail
 // Full argument check; fills `a` on success.
 int validate(int variant, const void* q, const void* k, const void* v, const float* beta, const float* lambda,
              const float* S0, const void* tail, void* out, float* S_final, void* tail_out, const falcon_dims_t* d,
-             int chunk, falcon::Launch* a) {
+             int chunk, void* ws, size_t ws_bytes, falcon::Launch* a) {
     const int st = validate_shape(variant, d, chunk, tail != nullptr, a);
     if (st != FALCON_OK) return st;
     const int64_t BH = d->batch * d->heads;
@@ -79,6 +79,9 @@ int validate(int variant, const void* q, const void* k, const void* v, const flo
     for (const void* p : al16)
         if (p && !aligned(p, 16)) return FALCON_ERR_MISALIGNED;
     if ((beta && !aligned(beta, 4)) || (lambda && !aligned(lambda, 4))) return FALCON_ERR_MISALIGNED;
+    if (ws && !aligned(ws, 256)) return FALCON_ERR_MISALIGNED;
+    const size_t ws_need = falcon::split_supported(*a) ? falcon::split_workspace_bytes(*a) : 0;
+    if (ws && ws_need > 0 && ws_bytes < ws_need) return FALCON_ERR_INVALID_ARG;
 
     // out must not overlap any input; tail_out must not overlap tail; S_final may equal S0 exactly.
     if (tokens > 0) {
@@ -101,6 +104,21 @@ int validate(int variant, const void* q, const void* k, const void* v, const flo
     if (S0 && S_final && S0 != S_final &&
         overlaps(range_of(S0, (size_t)BH * d->dk * d->dv * 4), range_of(S_final, (size_t)BH * d->dk * d->dv * 4)))
         return FALCON_ERR_INVALID_ARG;
+    if (ws && ws_need > 0) {  // the workspace is written by the kernels: it may overlap nothing
+        const size_t bcols = variant == FALCON_2 ? (size_t)d->dv : 1;
+        const Range rw = range_of(ws, ws_need);
+        const Range all[] = {
+            range_of(q, (size_t)tokens * d->dk * es), range_of(k, (size_t)tokens * d->dk * es),
+            range_of(v, (size_t)tokens * d->dv * es), range_of(beta, (size_t)tokens * bcols * 4),
+            range_of(lambda, (size_t)tokens * 4), range_of(out, (size_t)tokens * d->dv * es),
+            S0 ? range_of(S0, (size_t)BH * d->dk * d->dv * 4) : Range{0, 0},
+            S_final ? range_of(S_final, (size_t)BH * d->dk * d->dv * 4) : Range{0, 0},
+            tail ? range_of(tail, tail_bytes_of(d)) : Range{0, 0},
+            tail_out ? range_of(tail_out, tail_bytes_of(d)) : Range{0, 0},
+        };
+        for (const Range& r : all)
+            if (overlaps(rw, r)) return FALCON_ERR_INVALID_ARG;
+    }
 
     a->q = q;
     a->k = k;
@@ -112,6 +130,8 @@ int validate(int variant, const void* q, const void* k, const void* v, const flo
     a->out = out;
     a->S_final = S_final;
     a->tail_out = tail_out;
+    a->ws = ws_need > 0 ? ws : nullptr;
+    a->ws_bytes = ws_need > 0 && ws ? ws_bytes : 0;
     return FALCON_OK;
 }
 
@@ -119,7 +139,7 @@ int validate(int variant, const void* q, const void* k, const void* v, const flo
 
 extern "C" {
 
-int falcon_abi_version(void) { return 1; }
+int falcon_abi_version(void) { return 2; }
 
 size_t falcon_tail_bytes(const falcon_dims_t* d) {
     if (!d || d->batch < 0 || d->heads < 0 || d->dk <= 0 || d->dv <= 0 || d->window < 1) return 0;
@@ -141,26 +161,36 @@ const char* falcon_status_string(int s) {
 int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk) {
     falcon::Launch a = {};
     if (validate_shape(variant, dims, chunk, dims && dims->pos > 0, &a) != FALCON_OK) return 0;
+    if (falcon::split_supported(a) && falcon::split_workspace_bytes(a) > 0) return 3;
     return falcon::tc_supported(a) ? 2 : 1;
+}
+
+size_t falcon_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk) {
+    falcon::Launch a = {};
+    if (validate_shape(variant, dims, chunk, dims && dims->pos > 0, &a) != FALCON_OK) return 0;
+    return falcon::split_supported(a) ? falcon::split_workspace_bytes(a) : 0;
 }
 
 int falcon_fwd(int variant, const void* q, const void* k, const void* v, const float* beta, const float* lambda,
                const float* S0, const void* tail, void* out, float* S_final, void* tail_out,
-               const falcon_dims_t* dims, int chunk, void* stream) {
+               const falcon_dims_t* dims, int chunk, void* workspace, size_t workspace_bytes, void* stream) {
     falcon::Launch a = {};
-    const int st = validate(variant, q, k, v, beta, lambda, S0, tail, out, S_final, tail_out, dims, chunk, &a);
+    const int st = validate(variant, q, k, v, beta, lambda, S0, tail, out, S_final, tail_out, dims, chunk, workspace,
+                            workspace_bytes, &a);
     if (st != FALCON_OK) return st;
     if (a.B * a.H == 0) return FALCON_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (a.ws) return falcon::launch_split(a, s);
     if (falcon::tc_supported(a)) return falcon::launch_tc(a, s);
     return falcon::launch_generic(a, s);
 }
 
 int falcon_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FALCON_ERR_CUDA;
-    int flag = 0;
-    if (falcon::tc_consume_timeout_flag(&flag) != 0) return FALCON_ERR_CUDA;
-    return flag ? FALCON_ERR_DEVICE_TIMEOUT : FALCON_OK;
+    int f1 = 0, f2 = 0;
+    if (falcon::tc_consume_timeout_flag(&f1) != 0 || falcon::split_consume_timeout_flag(&f2) != 0)
+        return FALCON_ERR_CUDA;
+    return f1 || f2 ? FALCON_ERR_DEVICE_TIMEOUT : FALCON_OK;
 }
 
 }  // extern "C"

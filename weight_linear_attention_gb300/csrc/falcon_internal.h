@@ -28,6 +28,8 @@ struct Launch {
     int bf16;             // 1: q/k/v/out/tail are bf16, 0: fp32
     float eps, eps_gamma;
     int chunk;
+    void* ws;             // caller's workspace, or null
+    size_t ws_bytes;
 };
 
 // CUDA-core chunk kernel: every variant, both dtypes, all supported sizes.
@@ -39,5 +41,12 @@ bool tc_supported(const Launch& a);
 int launch_tc(const Launch& a, cudaStream_t stream);
 // Reads and clears the device-side timeout flag of the tcgen05 kernel (synchronous).
 int tc_consume_timeout_flag(int* flag);
+
+// Split path (Falcon-1 and 1A, bf16, dk = dv = 64, chunk 64): prep, chain and output kernels
+// working through a caller workspace of split_workspace_bytes(a) bytes at a.ws.
+bool split_supported(const Launch& a);
+size_t split_workspace_bytes(const Launch& a);
+int launch_split(const Launch& a, cudaStream_t stream);
+int split_consume_timeout_flag(int* flag);
 
 }  // namespace falcon

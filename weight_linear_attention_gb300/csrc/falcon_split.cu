@@ -1,0 +1,982 @@
+// Chunk-parallel split path for Falcon-1 and Falcon-1A (bf16 I/O, dk = dv = 64, chunk 64).
+//
+// Per chunk of C = 64 tokens (rows i, j) with X the shifted keys (row i = k_{tau_i - 1}), Y the
+// values, Q the queries, eta the step sizes, L / Lx the inclusive / exclusive chunk-local log-decay
+// prefixes (reset to 0 at every chunk start), w_j = eta_j e^{L_C - L_j} and
+//   A_ij = eta_j e^{Lx_i - L_j} x_i.x_j  (j < i),   P_ij = eta_j e^{L_i - L_j} q_i.x_j  (j <= i),
+//   T = (I + A)^{-1},
+// unrolling the Falcon-1 recurrence over the chunk ("Fast Weight Attention for Continual Learning",
+// paperlayer summary: §E.1 WY form of the triangular solve, §E.2 one merged residual solve, §F.2
+// read after write, §G.1 chunk-local log prefixes) gives, with S the state at the chunk start,
+//   R  = T (Y - diag(e^{Lx}) X S)                    residual targets of the chunk
+//   O  = diag(e^{L}) Q S + P R                       the chunk's reads o_i = S_i^T q_i
+//   S' = e^{L_C} S + X^T diag(w) R = M S + U,  where
+//   M  = e^{L_C} I - X^T diag(w) T diag(e^{Lx}) X,   U = X^T diag(w) T Y.
+// M and U do not depend on S, so the work splits into three launches:
+//   falcon_prep_kernel   one CTA per chunk, every chunk of every sequence at once: M_n, U_n
+//   falcon_chain_kernel  one CTA per (sequence, 16 state columns): S_{n+1} = M_n S_n + U_n
+//   falcon_out_kernel    one CTA per chunk, every chunk at once: R and O from S_n
+// Falcon-1A writes the target itself (no residual): T = I, M = e^{L_C} I, U = X^T diag(w) Y.
+//
+// Precision: tensor-core products of the exact bf16 inputs run in bf16. Every derived operand
+// (T, Z = X^T diag(w) T, Y - diag(e^{Lx}) X S, R, P, M, S) is split into bf16 hi and lo parts and
+// the products keep hi*hi, hi*lo and lo*hi, so each operand carries ~16 significant bits and every
+// sum is fp32. Only factors e^{a - b} with a <= b are formed: when the chunk's total log decay is
+// at least -30 they are e^{a} * e^{-b} (both finite, no cancellation), otherwise one exp each.
+//
+// Every mbarrier wait is bounded: on timeout the kernel raises a device flag, drains what it
+// issued (bounded), frees its TMEM and exits; falcon_device_status() reports the flag.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "falcon_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace falcon {
+
+__device__ int g_split_timeout_flag = 0;
+
+namespace {
+
+using namespace ptx;
+using bf16 = __nv_bfloat16;
+
+constexpr int kC = 64;
+constexpr int kTile = 8192;           // 64 x 64 bf16
+constexpr int kS = 68;                // fp32 row stride (floats) of A and T in shared memory
+constexpr int kFBytes = 64 * kS * 4;  // 17408
+constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr float kFastL = 30.f;
+constexpr uint32_t kTmemCols = 256;
+
+struct SplitParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_out, tm_m, tm_s, tm_t, tm_u;
+    const float* beta;
+    const float* lam;
+    const float* S0;
+    const bf16* k;
+    const bf16* tail;
+    bf16* tail_out;
+    float* S_final;
+    bf16* ws_m;   // [BH][N][2][64][64]: M_n hi, lo
+    float* ws_u;  // [BH][N][64][64]:    U_n
+    bf16* ws_s;   // [BH][N][2][64][64]: S_n hi, lo (state at the start of chunk n)
+    bf16* ws_t;   // [BH][N][2][64][64]: T_n hi, lo
+    long long T, pos;
+    int N;
+    float eps, eps_gamma;
+    int variant;
+};
+
+__device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity) {
+    if (mbar_wait_bounded(bar, parity, kTimeoutCycles)) return true;
+    atomicExch(&g_split_timeout_flag, 1);
+    return false;
+}
+// CTA-wide wait by thread 0. False (for every thread) on timeout, after thread 0 has given the
+// barrier one more bounded wait so that nothing it tracks is still landing when the CTA exits.
+__device__ __forceinline__ bool cta_wait(uint32_t bar, uint32_t parity, int tid) {
+    int bad = 0;
+    if (tid == 0 && !wait_or_flag(bar, parity)) {
+        bad = 1;
+        mbar_wait_bounded(bar, parity, kTimeoutCycles);
+    }
+    return !__syncthreads_or(bad);
+}
+__device__ __forceinline__ void release_tmem(uint32_t tmem, int warp) {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+__device__ __forceinline__ void hilo8(const float* v, uint4& h, uint4& l) {
+    split2(v[0], v[1], h.x, l.x);
+    split2(v[2], v[3], h.y, l.y);
+    split2(v[4], v[5], h.z, l.z);
+    split2(v[6], v[7], h.w, l.w);
+}
+
+// ---------------------------------------------------------------- per-token scalars
+struct Scal {
+    float eta[64], L[64], Lx[64], eLx[64], eL[64], cA[64], w[64];
+    float misc[8];  // [0] e^{L_C}, [1..2] warp totals of the scan, [3] 1 when the fast exp form holds
+};
+
+// Threads 0-63 own token i of the chunk; every thread of the CTA takes part in the two barriers.
+// tau0 is the global 1-based index of the chunk's first token; token 1 has x = 0 and eta = 0.
+__device__ __forceinline__ void chunk_scalars(Scal* s, const uint8_t* Xs, int tid, float beta_i, float lam_i, int nv,
+                                              long long tau0, float eps, float eps_gamma) {
+    if (tid < 64) {
+        const int i = tid, lane = tid & 31;
+        float nx = 0.f;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+            float x[8];
+            unpack8(*reinterpret_cast<const uint4*>(Xs + sw128(i, 8 * q8)), x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) nx = fmaf(x[e], x[e], nx);
+        }
+        float eta = 0.f, alpha = 0.f;
+        if (i < nv && tau0 + i >= 2) {
+            const float den = nx + lam_i + eps;
+            eta = den == 0.f ? 0.f : beta_i / den;
+            alpha = fminf(eta * lam_i, 1.f - eps_gamma);
+        }
+        const float l = log1pf(-alpha);
+        float incl = l;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        s->eta[i] = eta;
+        s->L[i] = incl;  // warp-local until the carry is added
+        s->Lx[i] = l;    // the token's own log-decay until then
+        if (lane == 31) s->misc[1 + (i >> 5)] = incl;
+    }
+    __syncthreads();
+    if (tid < 64) {
+        const int i = tid;
+        const float LC = s->misc[1] + s->misc[2];
+        const float Li = s->L[i] + (i >= 32 ? s->misc[1] : 0.f);
+        const float Lxi = Li - s->Lx[i];
+        const float eta = s->eta[i];
+        s->L[i] = Li;
+        s->Lx[i] = Lxi;
+        s->eLx[i] = expf(Lxi);
+        s->eL[i] = expf(Li);
+        s->cA[i] = eta * expf(fminf(-Li, kFastL + 1.f));  // read only when L_C >= -kFastL
+        s->w[i] = eta * expf(LC - Li);
+        if (i == 0) {
+            s->misc[0] = expf(LC);
+            s->misc[3] = LC >= -kFastL ? 1.f : 0.f;
+        }
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------- T = (I + A)^{-1}
+// m16n8k16 fragments of fp32 shared-memory matrices (row stride kS), split into bf16 hi / lo.
+__device__ __forceinline__ void afrag16(const float* M, int r0, int c0, int g, int t, uint32_t (&h)[4],
+                                        uint32_t (&l)[4]) {
+    const float2 v0 = *reinterpret_cast<const float2*>(M + (r0 + g) * kS + c0 + 2 * t);
+    const float2 v1 = *reinterpret_cast<const float2*>(M + (r0 + g + 8) * kS + c0 + 2 * t);
+    const float2 v2 = *reinterpret_cast<const float2*>(M + (r0 + g) * kS + c0 + 2 * t + 8);
+    const float2 v3 = *reinterpret_cast<const float2*>(M + (r0 + g + 8) * kS + c0 + 2 * t + 8);
+    split2(v0.x, v0.y, h[0], l[0]);
+    split2(v1.x, v1.y, h[1], l[1]);
+    split2(v2.x, v2.y, h[2], l[2]);
+    split2(v3.x, v3.y, h[3], l[3]);
+}
+__device__ __forceinline__ void bfrag16(const float* M, int k0, int n0, int g, int t, uint32_t& h0, uint32_t& h1,
+                                        uint32_t& l0, uint32_t& l1) {
+    split2(M[(k0 + 2 * t) * kS + n0 + g], M[(k0 + 2 * t + 1) * kS + n0 + g], h0, l0);
+    split2(M[(k0 + 2 * t + 8) * kS + n0 + g], M[(k0 + 2 * t + 9) * kS + n0 + g], h1, l1);
+}
+// The accumulators of two adjacent n-tiles form the A fragment of the next product.
+__device__ __forceinline__ void cfrag_to_a(const float (&c0)[4], const float (&c1)[4], uint32_t (&h)[4],
+                                           uint32_t (&l)[4]) {
+    split2(c0[0], c0[1], h[0], l[0]);
+    split2(c0[2], c0[3], h[1], l[1]);
+    split2(c1[0], c1[1], h[2], l[2]);
+    split2(c1[2], c1[3], h[3], l[3]);
+}
+
+// A: strictly lower 64 x 64 (fp32, stride kS). TF must hold zeros above its 16 x 16 diagonal
+// blocks on entry. 16 x 16 diagonal blocks by column substitution, then two levels of block
+// merges T_ba = -(T_bb A_ba) T_aa as warp-level bf16x3 products. Ends with a CTA barrier.
+__device__ void invert_unit_lower(const float* AF, float* TF, int tid) {
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    if (tid < 64) {
+        const int b = tid >> 4, c = tid & 15;
+        const float* Ab = AF + 16 * b * kS + 16 * b;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int j = 0; j + 1 < r; j += 2) {
+                a0 = fmaf(Ab[r * kS + j], x[j], a0);
+                a1 = fmaf(Ab[r * kS + j + 1], x[j + 1], a1);
+            }
+            if (r & 1) a0 = fmaf(Ab[r * kS + r - 1], x[r - 1], a0);
+            x[r] = r < c ? 0.f : (r == c ? 1.f : -(a0 + a1));
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) TF[(16 * b + r) * kS + 16 * b + c] = x[r];
+    }
+    __syncthreads();
+    if (warp < 2) {  // T_{b+1,b} for b = 0 (warp 0) and b = 2 (warp 1)
+        const int b = 2 * warp, R1 = 16 * (b + 1), C0 = 16 * b;
+        uint32_t ah[4], al[4];
+        afrag16(TF, R1, R1, g, t, ah, al);
+        float d1[2][4] = {};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t bh0, bh1, bl0, bl1;
+            bfrag16(AF, R1, C0 + 8 * nt, g, t, bh0, bh1, bl0, bl1);
+            mma16816_x3(d1[nt], ah, al, bh0, bh1, bl0, bl1);
+        }
+        cfrag_to_a(d1[0], d1[1], ah, al);
+        float d2[2][4] = {};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t bh0, bh1, bl0, bl1;
+            bfrag16(TF, C0, C0 + 8 * nt, g, t, bh0, bh1, bl0, bl1);
+            mma16816_x3(d2[nt], ah, al, bh0, bh1, bl0, bl1);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            *reinterpret_cast<float2*>(TF + (R1 + g) * kS + C0 + 8 * nt + 2 * t) = make_float2(-d2[nt][0], -d2[nt][1]);
+            *reinterpret_cast<float2*>(TF + (R1 + g + 8) * kS + C0 + 8 * nt + 2 * t) =
+                make_float2(-d2[nt][2], -d2[nt][3]);
+        }
+    }
+    __syncthreads();
+    if (warp < 4) {  // T[32:64, 0:32] = -(T[32:64, 32:64] A[32:64, 0:32]) T[0:32, 0:32], one 16x16 tile per warp
+        const int RB = 32 + 16 * (warp >> 1), CB = 16 * (warp & 1);
+        float d1[4][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            uint32_t ah[4], al[4];
+            afrag16(TF, RB, 32 + 16 * ks, g, t, ah, al);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                uint32_t bh0, bh1, bl0, bl1;
+                bfrag16(AF, 32 + 16 * ks, 8 * nt, g, t, bh0, bh1, bl0, bl1);
+                mma16816_x3(d1[nt], ah, al, bh0, bh1, bl0, bl1);
+            }
+        }
+        float d2[2][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            uint32_t ah[4], al[4];
+            cfrag_to_a(d1[2 * ks], d1[2 * ks + 1], ah, al);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                uint32_t bh0, bh1, bl0, bl1;
+                bfrag16(TF, 16 * ks, CB + 8 * nt, g, t, bh0, bh1, bl0, bl1);
+                mma16816_x3(d2[nt], ah, al, bh0, bh1, bl0, bl1);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            *reinterpret_cast<float2*>(TF + (RB + g) * kS + CB + 8 * nt + 2 * t) = make_float2(-d2[nt][0], -d2[nt][1]);
+            *reinterpret_cast<float2*>(TF + (RB + g + 8) * kS + CB + 8 * nt + 2 * t) =
+                make_float2(-d2[nt][2], -d2[nt][3]);
+        }
+    }
+    __syncthreads();
+}
+
+// One row r of A from 16 columns of G starting at c0 (fp32 to shared memory, stride kS).
+__device__ __forceinline__ void a_row16(const Scal* sc, const uint32_t (&u)[16], int r, int c0, bool fast, float* AF) {
+    float a[16];
+    if (fast) {
+        const float ex = sc->eLx[r];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) a[jj] = c0 + jj < r ? ex * sc->cA[c0 + jj] * __uint_as_float(u[jj]) : 0.f;
+    } else {
+        const float lx = sc->Lx[r];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+            a[jj] = c0 + jj < r ? sc->eta[c0 + jj] * __expf(lx - sc->L[c0 + jj]) * __uint_as_float(u[jj]) : 0.f;
+    }
+    float4* dst = reinterpret_cast<float4*>(AF + r * kS + c0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[k] = make_float4(a[4 * k], a[4 * k + 1], a[4 * k + 2], a[4 * k + 3]);
+}
+
+// ---------------------------------------------------------------- prep kernel: M_n, U_n, T_n
+// All products are M = 128 so that every epilogue reads whole 32-lane TMEM quadrants:
+//   [X; X] X^T            -> G twice (lanes 0-63 and 64-127)
+//   [X^T; X^T] diag(w) T  -> Z twice (X read MN-major, its two copies are the two 64-row atoms)
+//   [Z'; Z] [X | Y]       -> Z' X in lanes 0-63 / columns 0-63, Z Y in lanes 64-127 / columns 64-127
+namespace prep {
+constexpr int X = 0, X2 = kTile, Y = 2 * kTile;  // X2: a second copy of X
+constexpr int AF = 3 * kTile;                    // fp32 A, then Z' hi, Z hi, Z' lo, Z lo (4 tiles)
+constexpr int TF = AF + kFBytes;                 // fp32 T
+constexpr int TT = TF + kFBytes;                 // diag(w) T hi / lo (MN-major B tiles)
+constexpr int SCAL = TT + 2 * kTile;
+constexpr int BAR = SCAL + (int)sizeof(Scal);
+constexpr int BYTES = BAR + 32;
+constexpr int ALLOC = BYTES + 1024;
+constexpr uint32_t D1 = 0, DZ = 64, DMU = 128;  // TMEM columns; DMU spans 128
+static_assert(AF % 1024 == 0 && TT % 1024 == 0 && BAR % 8 == 0 && 4 * kTile <= 2 * kFBytes, "layout");
+}  // namespace prep
+
+__global__ void __launch_bounds__(256, 2) falcon_prep_kernel(const __grid_constant__ SplitParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long cid = blockIdx.x;
+    const long long bh = cid / p.N;
+    const int n = (int)(cid - bh * p.N);
+    const long long t0 = (long long)n * kC;
+    const int nv = (int)min((long long)kC, p.T - t0);
+    const bool f1 = p.variant == kF1;
+    Scal* sc = reinterpret_cast<Scal*>(sm + prep::SCAL);
+    float* AF = reinterpret_cast<float*>(sm + prep::AF);
+    float* TF = reinterpret_cast<float*>(sm + prep::TF);
+    const uint32_t bar_tma = base + prep::BAR, bar_mma = base + prep::BAR + 8;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + prep::BAR + 16);
+
+    if (tid == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init_fence();
+        mbar_expect_tx(bar_tma, 3 * kTile);
+        tma_load_3d(base + prep::X, &p.tm_k, 0, (int)t0 - 1, (int)bh, bar_tma);  // row i = k_{t0+i-1}
+        tma_load_3d(base + prep::X2, &p.tm_k, 0, (int)t0 - 1, (int)bh, bar_tma);
+        tma_load_3d(base + prep::Y, &p.tm_v, 0, (int)t0, (int)bh, bar_tma);
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), kTmemCols);
+    float beta_i = 0.f, lam_i = 0.f;
+    if (tid < nv) {
+        beta_i = p.beta[bh * p.T + t0 + tid];
+        lam_i = p.lam[bh * p.T + t0 + tid];
+    }
+    if (f1)
+        for (int i = tid; i < kFBytes / 16; i += 256) reinterpret_cast<float4*>(TF)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int q4 = warp & 3, hw = warp >> 2;
+    const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);  // this warp's TMEM lane quadrant
+    const int trow = 32 * q4 + lane;                           // this thread's TMEM lane
+
+    if (!cta_wait(bar_tma, 0, tid)) return release_tmem(tmem, warp);
+    if (n == 0 && p.pos > 0 && tid < 16) {  // a continuation's first shifted key is k_pos, from the tail
+        const uint4 v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[tid & 7];
+        *reinterpret_cast<uint4*>(sm + (tid < 8 ? prep::X : prep::X2) + sw128(0, 8 * (tid & 7))) = v;
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(128, 64, false, false);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + prep::D1, desc_k(base + prep::X + 32 * ks), desc_k(base + prep::X + 32 * ks), id, ks > 0);
+        mma_commit(bar_mma);
+    }
+    chunk_scalars(sc, sm + prep::X, tid, beta_i, lam_i, nv, p.pos + t0 + 1, p.eps, p.eps_gamma);
+    const bool fast = sc->misc[3] != 0.f;
+    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp);
+    tc_fence_after();
+
+    // ---- A (Falcon-1): lane l holds G row l % 64; four threads per row, 16 columns each
+    if (f1) {
+        const int r = trow & 63;
+        const int c0 = 16 * (((trow >> 6) << 1) | hw);
+        uint32_t u[16];
+        tmem_ld16(tq + prep::D1 + c0, u);
+        tmem_wait_ld();
+        regs_ready(u);
+        if (c0 < r) a_row16(sc, u, r, c0, fast, AF);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (f1) invert_unit_lower(AF, TF, tid);
+
+    // ---- T (hi / lo, row-major) to the workspace for the output kernel, and diag(w) T as the
+    // MN-major B operand of Z (Falcon-1A: T = I)
+    {
+        uint8_t* TTh = sm + prep::TT;
+        uint4* th = reinterpret_cast<uint4*>(p.ws_t + cid * 2 * 4096);
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+            const int task = tid + 256 * k2, i = task >> 3, c8 = 8 * (task & 7);
+            const float wi = sc->w[i];
+            float v[8];
+            if (f1) {
+                const float4 a = *reinterpret_cast<const float4*>(TF + i * kS + c8);
+                const float4 b = *reinterpret_cast<const float4*>(TF + i * kS + c8 + 4);
+                v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = c8 + e == i ? 1.f : 0.f;
+            }
+            uint4 h, l;
+            hilo8(v, h, l);
+            th[task] = h;        // row i, columns c8..c8+7 of T_hi
+            th[512 + task] = l;  // and of T_lo
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] *= wi;
+            st8_hilo(TTh, TTh + kTile, sw128(i, c8), v);
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {  // Z twice: [X^T; X^T] (T''_hi + T''_lo); X MN-major, its copies 8 KB apart
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(128, 64, true, true);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + prep::DZ, desc_mn(base + prep::X + 2048 * ks, kTile),
+                     desc_mn(base + prep::TT + 2048 * ks, kTile), id, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + prep::DZ, desc_mn(base + prep::X + 2048 * ks, kTile),
+                     desc_mn(base + prep::TT + kTile + 2048 * ks, kTile), id, 1);
+        mma_commit(bar_mma);
+    }
+    if (!cta_wait(bar_mma, 1, tid)) return release_tmem(tmem, warp);
+    tc_fence_after();
+
+    // ---- Z -> Z hi / lo and Z' = Z diag(e^{Lx}) hi / lo (K-major A tiles at AF: Z'h, Zh, Z'l, Zl)
+    {
+        const int a = trow & 63;
+        const int c0 = 16 * (((trow >> 6) << 1) | hw);
+        uint32_t u[16];
+        tmem_ld16(tq + prep::DZ + c0, u);
+        tmem_wait_ld();
+        regs_ready(u);
+        uint8_t* zt = sm + prep::AF;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int j0 = c0 + 8 * c;
+            float z[8], zp[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                z[e] = __uint_as_float(u[8 * c + e]);
+                zp[e] = z[e] * sc->eLx[j0 + e];
+            }
+            const uint32_t off = sw128(a, j0);
+            st8_hilo(zt + kTile, zt + 3 * kTile, off, z);
+            st8_hilo(zt, zt + 2 * kTile, off, zp);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // [Z'; Z] [X | Y]: X and Y are the two 64-column atoms of an MN-major B (16 KB apart)
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(128, 128, false, true);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + prep::DMU, desc_k(base + prep::AF + 32 * ks),
+                     desc_mn(base + prep::X + 2048 * ks, 2 * kTile), id, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + prep::DMU, desc_k(base + prep::AF + 2 * kTile + 32 * ks),
+                     desc_mn(base + prep::X + 2048 * ks, 2 * kTile), id, 1);
+        mma_commit(bar_mma);
+    }
+    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp);
+    tc_fence_after();
+
+    // ---- lanes 0-63: M = e^{L_C} I - Z' X (hi / lo bf16); lanes 64-127: U = Z Y (fp32)
+    {
+        float v[32];
+        const bool mrow = trow < 64;
+        const int a = trow & 63;
+        tmem_ld32(tq + prep::DMU + (mrow ? 0 : 64) + 32 * hw, v);
+        if (mrow) {
+            const float eLC = sc->misc[0];
+            uint4* mh = reinterpret_cast<uint4*>(p.ws_m + (cid * 2 * 64 + a) * 64 + 32 * hw);
+            uint4* ml = reinterpret_cast<uint4*>(p.ws_m + ((cid * 2 + 1) * 64 + a) * 64 + 32 * hw);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float m[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int b = 32 * hw + 8 * c + e;
+                    m[e] = (b == a ? eLC : 0.f) - (f1 ? v[8 * c + e] : 0.f);
+                }
+                uint4 h, l;
+                hilo8(m, h, l);
+                mh[c] = h;
+                ml[c] = l;
+            }
+        } else {
+            float4* u = reinterpret_cast<float4*>(p.ws_u + (cid * 64 + a) * 64 + 32 * hw);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) u[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        }
+    }
+    release_tmem(tmem, warp);
+}
+
+// ---------------------------------------------------------------- chain kernel: S_{n+1} = M_n S_n + U_n
+namespace chain {
+constexpr int kCols = 16;                   // state columns per CTA
+constexpr int kXS = 24;                     // bf16 row stride of the state exchange tiles (48 bytes)
+constexpr int kXBuf = 64 * kXS * 2;         // bytes per (buffer, part)
+constexpr int kUBytes = 64 * kCols * 4;     // U_n columns of this CTA, fp32 [64][16]
+constexpr int kStage = 2 * kTile + kUBytes; // M hi, M lo, U
+constexpr int STAGE = 0;                    // 3 stages
+constexpr int XB = 3 * kStage;              // 2 buffers x {hi, lo}
+constexpr int BAR = XB + 4 * kXBuf;
+constexpr int BYTES = BAR + 32;
+constexpr int ALLOC = BYTES + 1024;
+}  // namespace chain
+
+__global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant__ SplitParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int cb = blockIdx.x;
+    const long long bh = blockIdx.y;
+    const int c0 = chain::kCols * cb;
+    const int N = p.N;
+    uint8_t* xb = sm + chain::XB;
+    auto bar = [&](int s) -> uint32_t { return base + chain::BAR + 8 * s; };
+    auto load_m = [&](int m) {  // thread 0: M_m (hi, lo) and this CTA's columns of U_m into stage m % 3
+        const int s = m % 3;
+        const int row = (int)((bh * N + m) * 128);
+        const uint32_t st = base + chain::STAGE + s * chain::kStage;
+        mbar_expect_tx(bar(s), chain::kStage);
+        tma_load_2d(st, &p.tm_m, 0, row, bar(s));
+        tma_load_2d(st + kTile, &p.tm_m, 0, row + 64, bar(s));
+        tma_load_2d(st + 2 * kTile, &p.tm_u, c0, (int)((bh * N + m) * 64), bar(s));
+    };
+    int issued = 0;
+    if (tid == 0) {
+        for (int s = 0; s < 3; ++s) mbar_init(bar(s), 1);
+        mbar_init_fence();
+        for (; issued < 3 && issued < N; ++issued) load_m(issued);
+    }
+
+    // This thread's state fragment: acc[nt][0..1] = S[r0][c0 + 8nt + 2t + {0,1}], acc[nt][2..3] = row r0 + 8.
+    const int r0 = 16 * warp + g;
+    float acc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
+        if (p.S0) {
+            a = *reinterpret_cast<const float2*>(p.S0 + (bh * 64 + r0) * 64 + c0 + 8 * nt + 2 * t);
+            b = *reinterpret_cast<const float2*>(p.S0 + (bh * 64 + r0 + 8) * 64 + c0 + 8 * nt + 2 * t);
+        }
+        acc[nt][0] = a.x, acc[nt][1] = a.y, acc[nt][2] = b.x, acc[nt][3] = b.y;
+    }
+    auto put_state = [&](int b) {  // fragment -> exchange buffer b (hi at part 0, lo at part 1)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            uint32_t h0, l0, h1, l1;
+            split2(acc[nt][0], acc[nt][1], h0, l0);
+            split2(acc[nt][2], acc[nt][3], h1, l1);
+            const int col = 8 * nt + 2 * t;
+            *reinterpret_cast<uint32_t*>(xb + (2 * b) * chain::kXBuf + (r0 * chain::kXS + col) * 2) = h0;
+            *reinterpret_cast<uint32_t*>(xb + (2 * b + 1) * chain::kXBuf + (r0 * chain::kXS + col) * 2) = l0;
+            *reinterpret_cast<uint32_t*>(xb + (2 * b) * chain::kXBuf + ((r0 + 8) * chain::kXS + col) * 2) = h1;
+            *reinterpret_cast<uint32_t*>(xb + (2 * b + 1) * chain::kXBuf + ((r0 + 8) * chain::kXS + col) * 2) = l1;
+        }
+    };
+    auto store_state = [&](int b, int m) {  // exchange buffer b -> S_m in the workspace (16-byte chunks)
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+            const int task = tid + 128 * k2, row = task >> 2, part = (task >> 1) & 1, ch = task & 1;
+            const uint4 v = *reinterpret_cast<const uint4*>(xb + (2 * b + part) * chain::kXBuf + (row * chain::kXS + 8 * ch) * 2);
+            *reinterpret_cast<uint4*>(p.ws_s + (((bh * N + m) * 2 + part) * 64 + row) * 64 + c0 + 8 * ch) = v;
+        }
+    };
+    if (N > 0) put_state(0);
+    __syncthreads();
+    if (N > 0) store_state(0, 0);
+
+    bool ok = true;
+    for (int n = 0; n < N; ++n) {
+        const int s = n % 3;
+        if (__syncthreads_or(tid == 0 && !wait_or_flag(bar(s), (n / 3) & 1))) {
+            ok = false;
+            break;
+        }
+        const uint32_t st = base + chain::STAGE + s * chain::kStage;
+        const uint32_t xr = base + chain::XB + 2 * (n & 1) * chain::kXBuf;
+        const float* un = reinterpret_cast<const float*>(sm + chain::STAGE + s * chain::kStage + 2 * kTile);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {  // the accumulators start from U_n
+            const float2 a = *reinterpret_cast<const float2*>(un + r0 * chain::kCols + 8 * nt + 2 * t);
+            const float2 b = *reinterpret_cast<const float2*>(un + (r0 + 8) * chain::kCols + 8 * nt + 2 * t);
+            acc[nt][0] = a.x, acc[nt][1] = a.y, acc[nt][2] = b.x, acc[nt][3] = b.y;
+        }
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const int ar = 16 * warp + (lane & 15), ac = 16 * ks + 8 * (lane >> 4);
+            const uint32_t aoff = ar * 128 + ((((ac >> 3)) ^ (ar & 7)) << 4);
+            uint32_t ah[4], al[4];
+            ldsm_x4(st + aoff, ah[0], ah[1], ah[2], ah[3]);
+            ldsm_x4(st + kTile + aoff, al[0], al[1], al[2], al[3]);
+            const int mi = lane >> 3, kr = 16 * ks + (lane & 7) + 8 * (mi & 1), nc = 8 * (mi >> 1);
+            const uint32_t boff = (kr * chain::kXS + nc) * 2;
+            uint32_t bh[4], bl[4];
+            ldsm_x4_t(xr + boff, bh[0], bh[1], bh[2], bh[3]);
+            ldsm_x4_t(xr + chain::kXBuf + boff, bl[0], bl[1], bl[2], bl[3]);
+            mma16816_x3(acc[0], ah, al, bh[0], bh[1], bl[0], bl[1]);
+            mma16816_x3(acc[1], ah, al, bh[2], bh[3], bl[2], bl[3]);
+        }
+        if (n + 1 < N) put_state((n + 1) & 1);
+        __syncthreads();
+        if (tid == 0 && issued < N) {  // stage s is free again: fetch M_{n+3}
+            fence_async_smem();
+            load_m(issued);
+            ++issued;
+        }
+        if (n + 1 < N) store_state((n + 1) & 1, n + 1);
+    }
+    if (!ok) {  // drain the loads still in flight (bounded), then leave
+        if (tid == 0)
+            for (int m = 0; m < issued; ++m) mbar_wait_bounded(bar(m % 3), (m / 3) & 1, kTimeoutCycles);
+        return;
+    }
+    if (p.S_final) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            *reinterpret_cast<float2*>(p.S_final + (bh * 64 + r0) * 64 + c0 + 8 * nt + 2 * t) =
+                make_float2(acc[nt][0], acc[nt][1]);
+            *reinterpret_cast<float2*>(p.S_final + (bh * 64 + r0 + 8) * 64 + c0 + 8 * nt + 2 * t) =
+                make_float2(acc[nt][2], acc[nt][3]);
+        }
+    }
+    if (p.tail_out && cb == 0 && tid < 8) {  // window 1: the tail is the last key (the next call's x)
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (p.T > 0) v = reinterpret_cast<const uint4*>(p.k + (bh * p.T + p.T - 1) * 64)[tid];
+        else if (p.pos > 0) v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[tid];
+        reinterpret_cast<uint4*>(p.tail_out + bh * 64)[tid] = v;
+    }
+}
+
+// ---------------------------------------------------------------- output kernel: R and O from S_n
+// Every product is M = 128 with the wanted rows in TMEM lanes 64-127 (or 0-63 and 64-127 both
+// wanted), so each epilogue reads whole 32-lane quadrants. Where only the second 64 rows are
+// wanted, the first 64 rows of the A operand are whatever tile precedes it in shared memory.
+namespace outk {
+constexpr int X = 0, Q = 1, Y = 2, SH = 3, SL = 4, TH = 5, TL = 6, PH = 7, PL = 8, YH = 9, YL = 10, RH = 11,
+              RL = 12;  // 8 KB tiles, in this order: adjacency forms the stacked M = 128 operands
+constexpr int SCAL = 13 * kTile;
+constexpr int BAR = SCAL + (int)sizeof(Scal);
+constexpr int BYTES = BAR + 32;
+constexpr int ALLOC = BYTES + 1024;
+constexpr uint32_t D1 = 0, DXQ = 64, DR = 128, DO = 0;  // TMEM columns; DO reuses D1 once P is built
+static_assert(BAR % 8 == 0, "layout");
+}  // namespace outk
+
+__global__ void __launch_bounds__(256, 2) falcon_out_kernel(const __grid_constant__ SplitParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    auto tile = [&](int i) -> uint8_t* { return sm + i * kTile; };
+    auto taddr = [&](int i) -> uint32_t { return base + (uint32_t)(i * kTile); };
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long cid = blockIdx.x;
+    const long long bh = cid / p.N;
+    const int n = (int)(cid - bh * p.N);
+    const long long t0 = (long long)n * kC;
+    const int nv = (int)min((long long)kC, p.T - t0);
+    const bool f1 = p.variant == kF1;
+    Scal* sc = reinterpret_cast<Scal*>(sm + outk::SCAL);
+    const uint32_t bar_tma = base + outk::BAR, bar_mma = base + outk::BAR + 8;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + outk::BAR + 16);
+
+    if (tid == 0) {
+        mbar_init(bar_tma, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init_fence();
+        mbar_expect_tx(bar_tma, 7 * kTile);
+        tma_load_3d(taddr(outk::X), &p.tm_k, 0, (int)t0 - 1, (int)bh, bar_tma);
+        tma_load_3d(taddr(outk::Q), &p.tm_q, 0, (int)t0, (int)bh, bar_tma);
+        tma_load_3d(taddr(outk::Y), &p.tm_v, 0, (int)t0, (int)bh, bar_tma);
+        tma_load_2d(taddr(outk::SH), &p.tm_s, 0, (int)(cid * 128), bar_tma);
+        tma_load_2d(taddr(outk::SL), &p.tm_s, 0, (int)(cid * 128 + 64), bar_tma);
+        tma_load_2d(taddr(outk::TH), &p.tm_t, 0, (int)(cid * 128), bar_tma);
+        tma_load_2d(taddr(outk::TL), &p.tm_t, 0, (int)(cid * 128 + 64), bar_tma);
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), kTmemCols);
+    float beta_i = 0.f, lam_i = 0.f;
+    if (tid < nv) {
+        beta_i = p.beta[bh * p.T + t0 + tid];
+        lam_i = p.lam[bh * p.T + t0 + tid];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int q4 = warp & 3, hw = warp >> 2;
+    const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);
+    const int trow = 32 * q4 + lane;
+    const bool upper = trow >= 64;  // lanes 64-127: warps 2, 3, 6, 7
+    const int r = trow & 63;
+
+    if (!cta_wait(bar_tma, 0, tid)) return release_tmem(tmem, warp);
+    if (n == 0 && p.pos > 0 && tid < 8) {
+        const uint4 v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[tid];
+        *reinterpret_cast<uint4*>(tile(outk::X) + sw128(0, 8 * tid)) = v;
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        tc_fence_after();
+        constexpr uint32_t idk = idesc_bf16(128, 64, false, false);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // [G; Sc] = [X; Q] X^T
+            mma_bf16(tmem + outk::D1, desc_k(taddr(outk::X) + 32 * ks), desc_k(taddr(outk::X) + 32 * ks), idk, ks > 0);
+        constexpr uint32_t idm = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)  // [X S; Q S] with S = S_hi + S_lo (MN-major, K = feature)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tmem + outk::DXQ, desc_k(taddr(outk::X) + 32 * ks),
+                         desc_mn(taddr(outk::SH + part) + 2048 * ks, kTile), idm, part + ks > 0);
+        mma_commit(bar_mma);
+    }
+    chunk_scalars(sc, tile(outk::X), tid, beta_i, lam_i, nv, p.pos + t0 + 1, p.eps, p.eps_gamma);
+    const bool fast = sc->misc[3] != 0.f;
+    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp);
+    tc_fence_after();
+
+    // ---- lanes 64-127: P rows (K-major A tiles); lanes 0-63: Y' = Y - diag(e^{Lx}) X S rows (MN-major B)
+    {
+        float v[32];
+        tmem_ld32(tq + (upper ? outk::D1 : outk::DXQ) + 32 * hw, v);
+        if (upper) {
+            const int i = r;
+            float pv[32];
+            if (fast) {
+                const float el = sc->eL[i];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = 32 * hw + jj;
+                    pv[jj] = j <= i ? el * sc->cA[j] * v[jj] : 0.f;
+                }
+            } else {
+                const float li = sc->L[i];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = 32 * hw + jj;
+                    pv[jj] = j <= i ? sc->eta[j] * __expf(li - sc->L[j]) * v[jj] : 0.f;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) st8_hilo(tile(outk::PH), tile(outk::PL), sw128(i, 32 * hw + 8 * c), pv + 8 * c);
+        } else {
+            const float ex = f1 ? sc->eLx[r] : 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t off = sw128(r, 32 * hw + 8 * c);
+                float y[8];
+                unpack8(*reinterpret_cast<const uint4*>(tile(outk::Y) + off), y);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = fmaf(-ex, v[8 * c + e], y[e]);
+                st8_hilo(tile(outk::YH), tile(outk::YL), off, y);
+            }
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // R = T Y' in lanes 64-127: A = [SL; TH] carries T_hi, [TH; TL] carries T_lo
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + outk::DR, desc_k(taddr(outk::TH - 1) + 32 * ks), desc_mn(taddr(outk::YH) + 2048 * ks, kTile),
+                     id, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + outk::DR, desc_k(taddr(outk::TH - 1) + 32 * ks), desc_mn(taddr(outk::YL) + 2048 * ks, kTile),
+                     id, 1);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + outk::DR, desc_k(taddr(outk::TL - 1) + 32 * ks), desc_mn(taddr(outk::YH) + 2048 * ks, kTile),
+                     id, 1);
+        mma_commit(bar_mma);
+    }
+    if (!cta_wait(bar_mma, 1, tid)) return release_tmem(tmem, warp);
+    tc_fence_after();
+    if (upper) {  // R rows -> hi / lo (MN-major B, K = token)
+        float v[32];
+        tmem_ld32(tq + outk::DR + 32 * hw, v);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) st8_hilo(tile(outk::RH), tile(outk::RL), sw128(r, 32 * hw + 8 * c), v + 8 * c);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // P R in lanes 64-127: A = [TL; PH] carries P_hi, [PH; PL] carries P_lo
+        tc_fence_after();
+        constexpr uint32_t id = idesc_bf16(128, 64, false, true);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + outk::DO, desc_k(taddr(outk::PH - 1) + 32 * ks), desc_mn(taddr(outk::RH) + 2048 * ks, kTile),
+                     id, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + outk::DO, desc_k(taddr(outk::PH - 1) + 32 * ks), desc_mn(taddr(outk::RL) + 2048 * ks, kTile),
+                     id, 1);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + outk::DO, desc_k(taddr(outk::PL - 1) + 32 * ks), desc_mn(taddr(outk::RH) + 2048 * ks, kTile),
+                     id, 1);
+        mma_commit(bar_mma);
+    }
+    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp);
+    tc_fence_after();
+    if (upper) {  // O = diag(e^L) Q S + P R -> bf16 tile in the X region
+        float qs[32], po[32];
+        tmem_ld32x2(tq + outk::DXQ + 32 * hw, tq + outk::DO + 32 * hw, qs, po);
+        const float el = sc->eL[r];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = fmaf(el, qs[8 * c + e], po[8 * c + e]);
+            *reinterpret_cast<uint4*>(tile(outk::X) + sw128(r, 32 * hw + 8 * c)) = pack8(o);
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {  // TMA store; rows past T are clipped
+        tma_store_3d(&p.tm_out, taddr(outk::X), 0, (int)t0, (int)bh);
+        tma_store_wait_read();
+    }
+    release_tmem(tmem, warp);
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(q);
+    }
+    return fn;
+}
+
+// [BH][T][64] bf16, 64 x 64 boxes, 128-byte swizzle
+bool encode_bhtd(CUtensorMap* tm, const void* ptr, long long T, long long BH) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {64 * 2, (cuuint64_t)T * 64 * 2};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// [rows][64] bf16, 64 x 64 boxes, 128-byte swizzle
+bool encode_rows(CUtensorMap* tm, const void* ptr, long long rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {64 * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t es[2] = {1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// U: [rows][64] fp32, boxes of 16 columns x 64 rows (one chain CTA's columns), no swizzle
+bool encode_u(CUtensorMap* tm, const void* ptr, long long rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {64 * 4};
+    cuuint32_t box[2] = {16, 64};
+    cuuint32_t es[2] = {1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int smem_optin() {
+    static int v = -1;
+    if (v < 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            v = 0;
+    }
+    return v;
+}
+
+long long n_chunks(const Launch& a) { return (a.T + kC - 1) / kC; }
+
+}  // namespace
+
+bool split_supported(const Launch& a) {
+    const long long BH = a.B * a.H;
+    return (a.variant == kF1 || a.variant == kF1A) && a.bf16 && a.dk == 64 && a.dv == 64 && a.chunk == 64 &&
+           a.W == 1 && a.T < (1LL << 31) - 64 && BH < 65536 && BH * n_chunks(a) * 128 < (1LL << 31);
+}
+
+size_t split_workspace_bytes(const Launch& a) {
+    return (size_t)(a.B * a.H) * (size_t)n_chunks(a) * (size_t)(4 * 16384);
+}
+
+int launch_split(const Launch& a, cudaStream_t st) {
+    if (smem_optin() < outk::ALLOC) return 2;
+    const long long BH = a.B * a.H, N = n_chunks(a);
+    SplitParams p;
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    const size_t per = (size_t)BH * (size_t)N * 16384;
+    p.ws_m = reinterpret_cast<bf16*>(ws);
+    p.ws_u = reinterpret_cast<float*>(ws + per);
+    p.ws_s = reinterpret_cast<bf16*>(ws + 2 * per);
+    p.ws_t = reinterpret_cast<bf16*>(ws + 3 * per);
+    if (N > 0) {
+        if (!encode_bhtd(&p.tm_q, a.q, a.T, BH) || !encode_bhtd(&p.tm_k, a.k, a.T, BH) ||
+            !encode_bhtd(&p.tm_v, a.v, a.T, BH) || !encode_bhtd(&p.tm_out, a.out, a.T, BH) ||
+            !encode_rows(&p.tm_m, p.ws_m, BH * N * 128) || !encode_rows(&p.tm_s, p.ws_s, BH * N * 128) ||
+            !encode_rows(&p.tm_t, p.ws_t, BH * N * 128) || !encode_u(&p.tm_u, p.ws_u, BH * N * 64))
+            return 4;
+    }
+    p.beta = a.beta;
+    p.lam = a.lam;
+    p.S0 = a.S0;
+    p.k = static_cast<const bf16*>(a.k);
+    p.tail = static_cast<const bf16*>(a.tail);
+    p.tail_out = static_cast<bf16*>(a.tail_out);
+    p.S_final = a.S_final;
+    p.T = a.T;
+    p.pos = a.pos;
+    p.N = (int)N;
+    p.eps = a.eps;
+    p.eps_gamma = a.eps_gamma;
+    p.variant = a.variant;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(falcon_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, prep::ALLOC) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(falcon_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, chain::ALLOC) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(falcon_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, outk::ALLOC) !=
+                cudaSuccess)
+            return 4;
+        attr_set = true;
+    }
+    if (N > 0) falcon_prep_kernel<<<(unsigned)(BH * N), 256, prep::ALLOC, st>>>(p);
+    falcon_chain_kernel<<<dim3(64 / chain::kCols, (unsigned)BH), 128, chain::ALLOC, st>>>(p);
+    if (N > 0) falcon_out_kernel<<<(unsigned)(BH * N), 256, outk::ALLOC, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+int split_consume_timeout_flag(int* flag) {
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_split_timeout_flag, sizeof(int)) != cudaSuccess) return 1;
+    if (v && cudaMemcpyToSymbol(g_split_timeout_flag, &zero, sizeof(int)) != cudaSuccess) return 1;
+    *flag = v;
+    return 0;
+}
+
+}  // namespace falcon

@@ -48,8 +48,8 @@ assert ctypes.sizeof(FalconDims) == 64
 _lock = threading.Lock()
 _lib = None
 
-EXPORTED = ("falcon_fwd", "falcon_tail_bytes", "falcon_status_string", "falcon_device_status",
-            "falcon_kernel_for", "falcon_abi_version")
+EXPORTED = ("falcon_fwd", "falcon_workspace_bytes", "falcon_tail_bytes", "falcon_status_string",
+            "falcon_device_status", "falcon_kernel_for", "falcon_abi_version")
 
 
 class FalconError(RuntimeError):
@@ -75,7 +75,9 @@ def load(path: str | None = None):
         vp = ctypes.c_void_p
         lib.falcon_fwd.restype = ctypes.c_int
         lib.falcon_fwd.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                   ctypes.POINTER(FalconDims), ctypes.c_int, vp]
+                                   ctypes.POINTER(FalconDims), ctypes.c_int, vp, ctypes.c_size_t, vp]
+        lib.falcon_workspace_bytes.restype = ctypes.c_size_t
+        lib.falcon_workspace_bytes.argtypes = [ctypes.c_int, ctypes.POINTER(FalconDims), ctypes.c_int]
         lib.falcon_tail_bytes.restype = ctypes.c_size_t
         lib.falcon_tail_bytes.argtypes = [ctypes.POINTER(FalconDims)]
         lib.falcon_status_string.restype = ctypes.c_char_p
@@ -103,6 +105,10 @@ def status_string(status: int) -> str:
 
 def falcon_tail_bytes(dims: FalconDims) -> int:
     return int(load().falcon_tail_bytes(ctypes.byref(dims)))
+
+
+def falcon_workspace_bytes(variant: int, dims: FalconDims, chunk: int) -> int:
+    return int(load().falcon_workspace_bytes(int(variant), ctypes.byref(dims), int(chunk)))
 
 
 def falcon_kernel_for(variant: int, dims: FalconDims, chunk: int) -> int:
@@ -136,19 +142,34 @@ def _stream_handle(stream):
 
 
 def falcon_fwd(variant, q, k, v, beta, lam, S0, tail, out, S_final, tail_out, dims: FalconDims, chunk: int,
-               stream=None) -> int:
-    """The C entry point with the same argument order; tensors or raw device pointers. Returns the status."""
+               workspace=None, workspace_bytes=None, stream=None) -> int:
+    """The C entry point with the same argument order; tensors or raw device pointers. Returns the status.
+
+    ``workspace_bytes`` defaults to the size of a tensor workspace (0 for a raw pointer)."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
     return int(load().falcon_fwd(int(variant), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
                                  _ptr(tail), _ptr(out), _ptr(S_final), _ptr(tail_out), ctypes.byref(dims),
-                                 int(chunk), _stream_handle(stream)))
+                                 int(chunk), _ptr(workspace), int(workspace_bytes), _stream_handle(stream)))
+
+
+def workspace_for(variant, dims: FalconDims, chunk: int, device):
+    """A workspace tensor sized for falcon_fwd's split path, or None when no path needs one."""
+    import torch
+
+    n = falcon_workspace_bytes(variant, dims, chunk)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n > 0 else None
 
 
 def forward(variant, q, k, v, beta, lam, S0=None, tail=None, *, pos=0, window=1, chunk=64, eps=1e-6,
-            eps_gamma=1e-6, want_state=True, want_tail=True, stream=None):
+            eps_gamma=1e-6, want_state=True, want_tail=True, split=True, stream=None):
     """Allocate outputs with torch on q's device and call falcon_fwd; raises FalconError on a nonzero status.
 
     Returns (out, S_final or None, tail_out or None). tail/tail_out are flat byte-sized
     buffers in q's dtype, laid out per (b,h) as keys[window][dk] then vals[window-1][dv].
+    ``split=True`` hands falcon_fwd a workspace whenever a path can use one; ``False`` runs the
+    single-pass kernels.
     """
     import torch
 
@@ -164,7 +185,8 @@ def forward(variant, q, k, v, beta, lam, S0=None, tail=None, *, pos=0, window=1,
     if want_tail:
         n = falcon_tail_bytes(dims) // q.element_size()
         tail_out = torch.empty(n, dtype=q.dtype, device=q.device)
-    st = falcon_fwd(variant, q, k, v, beta, lam, S0, tail, out, S_final, tail_out, dims, chunk, stream)
+    ws = workspace_for(variant, dims, chunk, q.device) if split else None
+    st = falcon_fwd(variant, q, k, v, beta, lam, S0, tail, out, S_final, tail_out, dims, chunk, ws, stream=stream)
     if st != FALCON_OK:
         raise FalconError(st)
     return out, S_final, tail_out
