@@ -50,7 +50,6 @@ constexpr int kS = 68;                // fp32 row stride (floats) of A and T in 
 constexpr int kFBytes = 64 * kS * 4;  // 17408
 constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float kFastL = 30.f;
-constexpr uint32_t kTmemCols = 256;
 
 struct SplitParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_out, tm_m, tm_s, tm_t, tm_u;
@@ -65,6 +64,7 @@ struct SplitParams {
     float* ws_u;  // [BH][N][64][64]:    U_n
     bf16* ws_s;   // [BH][N][2][64][64]: S_n hi, lo (state at the start of chunk n)
     bf16* ws_t;   // [BH][N][2][64][64]: T_n hi, lo
+    uint8_t* ws_sc;  // [BH][N] blocks of kScalBytes: the chunk's per-token scalars (a Scal)
     long long T, pos;
     int N;
     float eps, eps_gamma;
@@ -86,10 +86,10 @@ __device__ __forceinline__ bool cta_wait(uint32_t bar, uint32_t parity, int tid)
     }
     return !__syncthreads_or(bad);
 }
-__device__ __forceinline__ void release_tmem(uint32_t tmem, int warp) {
+__device__ __forceinline__ void release_tmem(uint32_t tmem, int warp, uint32_t cols) {
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 0) tmem_dealloc(tmem, cols);
 }
 __device__ __forceinline__ void hilo8(const float* v, uint4& h, uint4& l) {
     split2(v[0], v[1], h.x, l.x);
@@ -103,6 +103,8 @@ struct Scal {
     float eta[64], L[64], Lx[64], eLx[64], eL[64], cA[64], w[64];
     float misc[8];  // [0] e^{L_C}, [1..2] warp totals of the scan, [3] 1 when the fast exp form holds
 };
+constexpr int kScalBytes = 2048;  // workspace stride of one chunk's Scal
+static_assert(sizeof(Scal) % 16 == 0 && sizeof(Scal) <= kScalBytes, "Scal block");
 
 // Threads 0-63 own token i of the chunk; every thread of the CTA takes part in the two barriers.
 // tau0 is the global 1-based index of the chunk's first token; token 1 has x = 0 and eta = 0.
@@ -110,14 +112,15 @@ __device__ __forceinline__ void chunk_scalars(Scal* s, const uint8_t* Xs, int ti
                                               long long tau0, float eps, float eps_gamma) {
     if (tid < 64) {
         const int i = tid, lane = tid & 31;
-        float nx = 0.f;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {
             float x[8];
             unpack8(*reinterpret_cast<const uint4*>(Xs + sw128(i, 8 * q8)), x);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) nx = fmaf(x[e], x[e], nx);
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(x[e], x[e], acc[e]);
         }
+        const float nx = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         float eta = 0.f, alpha = 0.f;
         if (i < nv && tau0 + i >= 2) {
             const float den = nx + lam_i + eps;
@@ -184,15 +187,16 @@ __device__ __forceinline__ void cfrag_to_a(const float (&c0)[4], const float (&c
     split2(c1[2], c1[3], h[3], l[3]);
 }
 
-// A: strictly lower 64 x 64 (fp32, stride kS). TF must hold zeros above its 16 x 16 diagonal
-// blocks on entry. 16 x 16 diagonal blocks by column substitution, then two levels of block
-// merges T_ba = -(T_bb A_ba) T_aa as warp-level bf16x3 products. Ends with a CTA barrier.
-__device__ void invert_unit_lower(const float* AF, float* TF, int tid) {
+// In place: on entry M holds A, strictly lower 64 x 64 (fp32, stride kS), with zeros in the 16 x 16
+// blocks above the diagonal; on exit M holds T = (I + A)^{-1}. 16 x 16 diagonal blocks by column
+// substitution (in registers), then two levels of block merges T_ba = -(T_bb A_ba) T_aa as warp-level
+// bf16x3 products; each merge reads the A block it replaces before writing it. Ends with a CTA barrier.
+__device__ void invert_unit_lower(float* M, int tid) {
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    float x[16];
     if (tid < 64) {
         const int b = tid >> 4, c = tid & 15;
-        const float* Ab = AF + 16 * b * kS + 16 * b;
-        float x[16];
+        const float* Ab = M + 16 * b * kS + 16 * b;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             float a0 = 0.f, a1 = 0.f;
@@ -204,19 +208,23 @@ __device__ void invert_unit_lower(const float* AF, float* TF, int tid) {
             if (r & 1) a0 = fmaf(Ab[r * kS + r - 1], x[r - 1], a0);
             x[r] = r < c ? 0.f : (r == c ? 1.f : -(a0 + a1));
         }
+    }
+    __syncthreads();
+    if (tid < 64) {
+        const int b = tid >> 4, c = tid & 15;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) TF[(16 * b + r) * kS + 16 * b + c] = x[r];
+        for (int r = 0; r < 16; ++r) M[(16 * b + r) * kS + 16 * b + c] = x[r];
     }
     __syncthreads();
     if (warp < 2) {  // T_{b+1,b} for b = 0 (warp 0) and b = 2 (warp 1)
         const int b = 2 * warp, R1 = 16 * (b + 1), C0 = 16 * b;
         uint32_t ah[4], al[4];
-        afrag16(TF, R1, R1, g, t, ah, al);
+        afrag16(M, R1, R1, g, t, ah, al);
         float d1[2][4] = {};
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             uint32_t bh0, bh1, bl0, bl1;
-            bfrag16(AF, R1, C0 + 8 * nt, g, t, bh0, bh1, bl0, bl1);
+            bfrag16(M, R1, C0 + 8 * nt, g, t, bh0, bh1, bl0, bl1);
             mma16816_x3(d1[nt], ah, al, bh0, bh1, bl0, bl1);
         }
         cfrag_to_a(d1[0], d1[1], ah, al);
@@ -224,14 +232,14 @@ __device__ void invert_unit_lower(const float* AF, float* TF, int tid) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             uint32_t bh0, bh1, bl0, bl1;
-            bfrag16(TF, C0, C0 + 8 * nt, g, t, bh0, bh1, bl0, bl1);
+            bfrag16(M, C0, C0 + 8 * nt, g, t, bh0, bh1, bl0, bl1);
             mma16816_x3(d2[nt], ah, al, bh0, bh1, bl0, bl1);
         }
+        __syncwarp();
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            *reinterpret_cast<float2*>(TF + (R1 + g) * kS + C0 + 8 * nt + 2 * t) = make_float2(-d2[nt][0], -d2[nt][1]);
-            *reinterpret_cast<float2*>(TF + (R1 + g + 8) * kS + C0 + 8 * nt + 2 * t) =
-                make_float2(-d2[nt][2], -d2[nt][3]);
+            *reinterpret_cast<float2*>(M + (R1 + g) * kS + C0 + 8 * nt + 2 * t) = make_float2(-d2[nt][0], -d2[nt][1]);
+            *reinterpret_cast<float2*>(M + (R1 + g + 8) * kS + C0 + 8 * nt + 2 * t) = make_float2(-d2[nt][2], -d2[nt][3]);
         }
     }
     __syncthreads();
@@ -241,14 +249,15 @@ __device__ void invert_unit_lower(const float* AF, float* TF, int tid) {
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
             uint32_t ah[4], al[4];
-            afrag16(TF, RB, 32 + 16 * ks, g, t, ah, al);
+            afrag16(M, RB, 32 + 16 * ks, g, t, ah, al);
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 uint32_t bh0, bh1, bl0, bl1;
-                bfrag16(AF, 32 + 16 * ks, 8 * nt, g, t, bh0, bh1, bl0, bl1);
+                bfrag16(M, 32 + 16 * ks, 8 * nt, g, t, bh0, bh1, bl0, bl1);
                 mma16816_x3(d1[nt], ah, al, bh0, bh1, bl0, bl1);
             }
         }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // every warp has read A[32:64, 0:32]
         float d2[2][4] = {};
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
@@ -257,15 +266,14 @@ __device__ void invert_unit_lower(const float* AF, float* TF, int tid) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 uint32_t bh0, bh1, bl0, bl1;
-                bfrag16(TF, 16 * ks, CB + 8 * nt, g, t, bh0, bh1, bl0, bl1);
+                bfrag16(M, 16 * ks, CB + 8 * nt, g, t, bh0, bh1, bl0, bl1);
                 mma16816_x3(d2[nt], ah, al, bh0, bh1, bl0, bl1);
             }
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            *reinterpret_cast<float2*>(TF + (RB + g) * kS + CB + 8 * nt + 2 * t) = make_float2(-d2[nt][0], -d2[nt][1]);
-            *reinterpret_cast<float2*>(TF + (RB + g + 8) * kS + CB + 8 * nt + 2 * t) =
-                make_float2(-d2[nt][2], -d2[nt][3]);
+            *reinterpret_cast<float2*>(M + (RB + g) * kS + CB + 8 * nt + 2 * t) = make_float2(-d2[nt][0], -d2[nt][1]);
+            *reinterpret_cast<float2*>(M + (RB + g + 8) * kS + CB + 8 * nt + 2 * t) = make_float2(-d2[nt][2], -d2[nt][3]);
         }
     }
     __syncthreads();
@@ -290,24 +298,26 @@ __device__ __forceinline__ void a_row16(const Scal* sc, const uint32_t (&u)[16],
 }
 
 // ---------------------------------------------------------------- prep kernel: M_n, U_n, T_n
-// All products are M = 128 so that every epilogue reads whole 32-lane TMEM quadrants:
-//   [X; X] X^T            -> G twice (lanes 0-63 and 64-127)
-//   [X^T; X^T] diag(w) T  -> Z twice (X read MN-major, its two copies are the two 64-row atoms)
-//   [Z'; Z] [X | Y]       -> Z' X in lanes 0-63 / columns 0-63, Z Y in lanes 64-127 / columns 64-127
+// The products are M = 128 with the wanted rows in TMEM lanes 64-127 (or in both halves), so that
+// every epilogue reads whole 32-lane quadrants; the A operand's first 64 rows are then the tile
+// that precedes the wanted one in shared memory (Y before X):
+//   [Y; X] X^T            -> G in lanes 64-127
+//   [Y^T; X^T] diag(w) T  -> Z = X^T diag(w) T in lanes 64-127 (MN-major A: the tiles are its two atoms)
+//   [Z'; Z] [Y | X]       -> Z' X in lanes 0-63 / columns 64-127, Z Y in lanes 64-127 / columns 0-63
+// The accumulators take turns in TMEM columns 0-127 (each is read out before the next MMA).
 namespace prep {
-constexpr int X = 0, X2 = kTile, Y = 2 * kTile;  // X2: a second copy of X
-constexpr int AF = 3 * kTile;                    // fp32 A, then Z' hi, Z hi, Z' lo, Z lo (4 tiles)
-constexpr int TF = AF + kFBytes;                 // fp32 T
-constexpr int TT = TF + kFBytes;                 // diag(w) T hi / lo (MN-major B tiles)
+constexpr int Y = 0, X = kTile;                  // Y first: [Y; X] stacks with X in rows 64-127
+constexpr int AF = 2 * kTile;                    // fp32 A, inverted in place into T; then Z' hi, Z hi
+constexpr int TT = AF + kFBytes;                 // diag(w) T hi / lo (MN-major B tiles); then Z' lo, Z lo
 constexpr int SCAL = TT + 2 * kTile;
 constexpr int BAR = SCAL + (int)sizeof(Scal);
 constexpr int BYTES = BAR + 32;
 constexpr int ALLOC = BYTES + 1024;
-constexpr uint32_t D1 = 0, DZ = 64, DMU = 128;  // TMEM columns; DMU spans 128
-static_assert(AF % 1024 == 0 && TT % 1024 == 0 && BAR % 8 == 0 && 4 * kTile <= 2 * kFBytes, "layout");
+constexpr uint32_t kCols = 128;
+static_assert(AF % 1024 == 0 && TT % 1024 == 0 && BAR % 8 == 0 && 2 * kTile <= kFBytes, "layout");
 }  // namespace prep
 
-__global__ void __launch_bounds__(256, 2) falcon_prep_kernel(const __grid_constant__ SplitParams p) {
+__global__ void __launch_bounds__(256, 4) falcon_prep_kernel(const __grid_constant__ SplitParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -321,7 +331,6 @@ __global__ void __launch_bounds__(256, 2) falcon_prep_kernel(const __grid_consta
     const bool f1 = p.variant == kF1;
     Scal* sc = reinterpret_cast<Scal*>(sm + prep::SCAL);
     float* AF = reinterpret_cast<float*>(sm + prep::AF);
-    float* TF = reinterpret_cast<float*>(sm + prep::TF);
     const uint32_t bar_tma = base + prep::BAR, bar_mma = base + prep::BAR + 8;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + prep::BAR + 16);
 
@@ -329,19 +338,18 @@ __global__ void __launch_bounds__(256, 2) falcon_prep_kernel(const __grid_consta
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
         mbar_init_fence();
-        mbar_expect_tx(bar_tma, 3 * kTile);
+        mbar_expect_tx(bar_tma, 2 * kTile);
         tma_load_3d(base + prep::X, &p.tm_k, 0, (int)t0 - 1, (int)bh, bar_tma);  // row i = k_{t0+i-1}
-        tma_load_3d(base + prep::X2, &p.tm_k, 0, (int)t0 - 1, (int)bh, bar_tma);
         tma_load_3d(base + prep::Y, &p.tm_v, 0, (int)t0, (int)bh, bar_tma);
     }
-    if (warp == 0) tmem_alloc(smem_u32(tslot), kTmemCols);
+    if (warp == 0) tmem_alloc(smem_u32(tslot), prep::kCols);
     float beta_i = 0.f, lam_i = 0.f;
     if (tid < nv) {
         beta_i = p.beta[bh * p.T + t0 + tid];
         lam_i = p.lam[bh * p.T + t0 + tid];
     }
-    if (f1)
-        for (int i = tid; i < kFBytes / 16; i += 256) reinterpret_cast<float4*>(TF)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (f1)  // A's blocks above the diagonal must read as zero in the block merges
+        for (int i = tid; i < kFBytes / 16; i += 256) reinterpret_cast<float4*>(AF)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -350,39 +358,43 @@ __global__ void __launch_bounds__(256, 2) falcon_prep_kernel(const __grid_consta
     const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);  // this warp's TMEM lane quadrant
     const int trow = 32 * q4 + lane;                           // this thread's TMEM lane
 
-    if (!cta_wait(bar_tma, 0, tid)) return release_tmem(tmem, warp);
-    if (n == 0 && p.pos > 0 && tid < 16) {  // a continuation's first shifted key is k_pos, from the tail
-        const uint4 v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[tid & 7];
-        *reinterpret_cast<uint4*>(sm + (tid < 8 ? prep::X : prep::X2) + sw128(0, 8 * (tid & 7))) = v;
+    if (!cta_wait(bar_tma, 0, tid)) return release_tmem(tmem, warp, prep::kCols);
+    if (n == 0 && p.pos > 0 && tid < 8) {  // a continuation's first shifted key is k_pos, from the tail
+        const uint4 v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[tid];
+        *reinterpret_cast<uint4*>(sm + prep::X + sw128(0, 8 * tid)) = v;
     }
     fence_async_smem();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0) {  // [Y; X] X^T: G in lanes 64-127
         tc_fence_after();
         constexpr uint32_t id = idesc_bf16(128, 64, false, false);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + prep::D1, desc_k(base + prep::X + 32 * ks), desc_k(base + prep::X + 32 * ks), id, ks > 0);
+            mma_bf16(tmem, desc_k(base + prep::Y + 32 * ks), desc_k(base + prep::X + 32 * ks), id, ks > 0);
         mma_commit(bar_mma);
     }
     chunk_scalars(sc, sm + prep::X, tid, beta_i, lam_i, nv, p.pos + t0 + 1, p.eps, p.eps_gamma);
     const bool fast = sc->misc[3] != 0.f;
-    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp);
+    if (tid < (int)(sizeof(Scal) / 16))  // the scalars, for the output kernel
+        reinterpret_cast<uint4*>(p.ws_sc + cid * kScalBytes)[tid] = reinterpret_cast<const uint4*>(sc)[tid];
+    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp, prep::kCols);
     tc_fence_after();
 
-    // ---- A (Falcon-1): lane l holds G row l % 64; four threads per row, 16 columns each
-    if (f1) {
-        const int r = trow & 63;
-        const int c0 = 16 * (((trow >> 6) << 1) | hw);
-        uint32_t u[16];
-        tmem_ld16(tq + prep::D1 + c0, u);
+    // ---- A (Falcon-1): lanes 64-127 hold G; two threads per row (warps 2, 3, 6, 7), 32 columns each
+    if (f1 && trow >= 64) {
+        const int r = trow - 64, c0 = 32 * hw;
+        uint32_t u0[16], u1[16];
+        tmem_ld16(tq + c0, u0);
+        tmem_ld16(tq + c0 + 16, u1);
         tmem_wait_ld();
-        regs_ready(u);
-        if (c0 < r) a_row16(sc, u, r, c0, fast, AF);
+        regs_ready(u0);
+        regs_ready(u1);
+        if (c0 < r) a_row16(sc, u0, r, c0, fast, AF);
+        if (c0 + 16 < r) a_row16(sc, u1, r, c0 + 16, fast, AF);
     }
     tc_fence_before();
     __syncthreads();
-    if (f1) invert_unit_lower(AF, TF, tid);
+    if (f1) invert_unit_lower(AF, tid);
 
     // ---- T (hi / lo, row-major) to the workspace for the output kernel, and diag(w) T as the
     // MN-major B operand of Z (Falcon-1A: T = I)
@@ -395,8 +407,8 @@ __global__ void __launch_bounds__(256, 2) falcon_prep_kernel(const __grid_consta
             const float wi = sc->w[i];
             float v[8];
             if (f1) {
-                const float4 a = *reinterpret_cast<const float4*>(TF + i * kS + c8);
-                const float4 b = *reinterpret_cast<const float4*>(TF + i * kS + c8 + 4);
+                const float4 a = *reinterpret_cast<const float4*>(AF + i * kS + c8);
+                const float4 b = *reinterpret_cast<const float4*>(AF + i * kS + c8 + 4);
                 v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
             } else {
 #pragma unroll
@@ -412,63 +424,56 @@ __global__ void __launch_bounds__(256, 2) falcon_prep_kernel(const __grid_consta
         }
     }
     fence_async_smem();
+    tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // Z twice: [X^T; X^T] (T''_hi + T''_lo); X MN-major, its copies 8 KB apart
+    if (tid == 0) {  // [Y^T; X^T] (T''_hi + T''_lo): Z in lanes 64-127; A MN-major with atoms Y and X
         tc_fence_after();
         constexpr uint32_t id = idesc_bf16(128, 64, true, true);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + prep::DZ, desc_mn(base + prep::X + 2048 * ks, kTile),
-                     desc_mn(base + prep::TT + 2048 * ks, kTile), id, ks > 0);
+            mma_bf16(tmem, desc_mn(base + prep::Y + 2048 * ks, kTile), desc_mn(base + prep::TT + 2048 * ks, kTile), id,
+                     ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + prep::DZ, desc_mn(base + prep::X + 2048 * ks, kTile),
+            mma_bf16(tmem, desc_mn(base + prep::Y + 2048 * ks, kTile),
                      desc_mn(base + prep::TT + kTile + 2048 * ks, kTile), id, 1);
         mma_commit(bar_mma);
     }
-    if (!cta_wait(bar_mma, 1, tid)) return release_tmem(tmem, warp);
+    if (!cta_wait(bar_mma, 1, tid)) return release_tmem(tmem, warp, prep::kCols);
     tc_fence_after();
 
-    // ---- Z -> Z hi / lo and Z' = Z diag(e^{Lx}) hi / lo (K-major A tiles at AF: Z'h, Zh, Z'l, Zl)
-    {
-        const int a = trow & 63;
-        const int c0 = 16 * (((trow >> 6) << 1) | hw);
-        uint32_t u[16];
-        tmem_ld16(tq + prep::DZ + c0, u);
-        tmem_wait_ld();
-        regs_ready(u);
-        uint8_t* zt = sm + prep::AF;
+    // ---- Z (lanes 64-127) -> Z hi / lo and Z' = Z diag(e^{Lx}) hi / lo
+    // (K-major A tiles: [Z'h; Zh] at AF, [Z'l; Zl] at TT)
+    if (trow >= 64) {
+        const int a = trow - 64, c0 = 32 * hw;
+        float z[32];
+        tmem_ld32(tq + c0, z);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 4; ++c) {
             const int j0 = c0 + 8 * c;
-            float z[8], zp[8];
+            float zp[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                z[e] = __uint_as_float(u[8 * c + e]);
-                zp[e] = z[e] * sc->eLx[j0 + e];
-            }
+            for (int e = 0; e < 8; ++e) zp[e] = z[8 * c + e] * sc->eLx[j0 + e];
             const uint32_t off = sw128(a, j0);
-            st8_hilo(zt + kTile, zt + 3 * kTile, off, z);
-            st8_hilo(zt, zt + 2 * kTile, off, zp);
+            st8_hilo(sm + prep::AF + kTile, sm + prep::TT + kTile, off, z + 8 * c);
+            st8_hilo(sm + prep::AF, sm + prep::TT, off, zp);
         }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // [Z'; Z] [X | Y]: X and Y are the two 64-column atoms of an MN-major B (16 KB apart)
+    if (tid == 0) {  // [Z'; Z] [Y | X]: Y and X are the two 64-column atoms of an MN-major B
         tc_fence_after();
         constexpr uint32_t id = idesc_bf16(128, 128, false, true);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + prep::DMU, desc_k(base + prep::AF + 32 * ks),
-                     desc_mn(base + prep::X + 2048 * ks, 2 * kTile), id, ks > 0);
+            mma_bf16(tmem, desc_k(base + prep::AF + 32 * ks), desc_mn(base + prep::Y + 2048 * ks, kTile), id, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + prep::DMU, desc_k(base + prep::AF + 2 * kTile + 32 * ks),
-                     desc_mn(base + prep::X + 2048 * ks, 2 * kTile), id, 1);
+            mma_bf16(tmem, desc_k(base + prep::TT + 32 * ks), desc_mn(base + prep::Y + 2048 * ks, kTile), id, 1);
         mma_commit(bar_mma);
     }
-    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp);
+    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp, prep::kCols);
     tc_fence_after();
 
     // ---- lanes 0-63: M = e^{L_C} I - Z' X (hi / lo bf16); lanes 64-127: U = Z Y (fp32)
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(256, 2) falcon_prep_kernel(const __grid_consta
         float v[32];
         const bool mrow = trow < 64;
         const int a = trow & 63;
-        tmem_ld32(tq + prep::DMU + (mrow ? 0 : 64) + 32 * hw, v);
+        tmem_ld32(tq + (mrow ? 64 : 0) + 32 * hw, v);
         if (mrow) {
             const float eLC = sc->misc[0];
             uint4* mh = reinterpret_cast<uint4*>(p.ws_m + (cid * 2 * 64 + a) * 64 + 32 * hw);
@@ -500,21 +505,26 @@ __global__ void __launch_bounds__(256, 2) falcon_prep_kernel(const __grid_consta
             for (int c = 0; c < 8; ++c) u[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         }
     }
-    release_tmem(tmem, warp);
+    release_tmem(tmem, warp, prep::kCols);
 }
 
 // ---------------------------------------------------------------- chain kernel: S_{n+1} = M_n S_n + U_n
+// One CTA per (sequence, 32-column half of S). Per step one thread issues eight tcgen05 MMAs,
+// D = (M_hi + M_lo) [S_hi | S_lo], whose B operand is a single 64 x 64 tile holding this half's
+// state split into hi (columns 0-31) and lo (columns 32-63) bf16 parts; then every thread reads
+// its fragment of D (16x256b TMEM loads), forms S_{n+1} = D[:, 0:32] + D[:, 32:64] + U_n in fp32,
+// and writes the next B tile (double-buffered) and the chunk-start state for the output kernel.
 namespace chain {
-constexpr int kCols = 16;                   // state columns per CTA
-constexpr int kXS = 24;                     // bf16 row stride of the state exchange tiles (48 bytes)
-constexpr int kXBuf = 64 * kXS * 2;         // bytes per (buffer, part)
-constexpr int kUBytes = 64 * kCols * 4;     // U_n columns of this CTA, fp32 [64][16]
+constexpr int kCols = 32;                   // state columns per CTA
+constexpr int kStages = 3;
+constexpr int kUBytes = 64 * kCols * 4;     // U_n columns of this CTA, fp32 [64][kCols]
 constexpr int kStage = 2 * kTile + kUBytes; // M hi, M lo, U
-constexpr int STAGE = 0;                    // 3 stages
-constexpr int XB = 3 * kStage;              // 2 buffers x {hi, lo}
-constexpr int BAR = XB + 4 * kXBuf;
-constexpr int BYTES = BAR + 32;
+constexpr int BT = kStages * kStage;        // two B tiles
+constexpr int BAR = BT + 2 * kTile;         // full[kStages], mma
+constexpr int BYTES = BAR + 8 * (kStages + 1) + 16;
 constexpr int ALLOC = BYTES + 1024;
+constexpr uint32_t kTmemCols = 64;
+static_assert(kStage % 1024 == 0 && BT % 1024 == 0, "stage alignment");
 }  // namespace chain
 
 __global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant__ SplitParams p) {
@@ -522,118 +532,153 @@ __global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, t = lane & 3;
     const int cb = blockIdx.x;
     const long long bh = blockIdx.y;
-    const int c0 = chain::kCols * cb;
+    const int c0 = chain::kCols * cb;  // this CTA's first state column
     const int N = p.N;
-    uint8_t* xb = sm + chain::XB;
-    auto bar = [&](int s) -> uint32_t { return base + chain::BAR + 8 * s; };
-    auto load_m = [&](int m) {  // thread 0: M_m (hi, lo) and this CTA's columns of U_m into stage m % 3
-        const int s = m % 3;
+    auto full = [&](int s) -> uint32_t { return base + chain::BAR + 8 * s; };
+    const uint32_t bar_mma = base + chain::BAR + 8 * chain::kStages;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chain::BAR + 8 * (chain::kStages + 1));
+    auto load = [&](int m) {  // thread 0: M_m (hi, lo) and this CTA's columns of U_m into stage m % kStages
+        const int s = m % chain::kStages;
+        const uint32_t st = base + s * chain::kStage;
         const int row = (int)((bh * N + m) * 128);
-        const uint32_t st = base + chain::STAGE + s * chain::kStage;
-        mbar_expect_tx(bar(s), chain::kStage);
-        tma_load_2d(st, &p.tm_m, 0, row, bar(s));
-        tma_load_2d(st + kTile, &p.tm_m, 0, row + 64, bar(s));
-        tma_load_2d(st + 2 * kTile, &p.tm_u, c0, (int)((bh * N + m) * 64), bar(s));
+        mbar_expect_tx(full(s), chain::kStage);
+        tma_load_2d(st, &p.tm_m, 0, row, full(s));
+        tma_load_2d(st + kTile, &p.tm_m, 0, row + 64, full(s));
+        tma_load_2d(st + 2 * kTile, &p.tm_u, c0, (int)((bh * N + m) * 64), full(s));
     };
     int issued = 0;
     if (tid == 0) {
-        for (int s = 0; s < 3; ++s) mbar_init(bar(s), 1);
+        for (int s = 0; s < chain::kStages; ++s) mbar_init(full(s), 1);
+        mbar_init(bar_mma, 1);
         mbar_init_fence();
-        for (; issued < 3 && issued < N; ++issued) load_m(issued);
     }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), chain::kTmemCols);
+    pdl_wait();  // the prep kernel's M_n, U_n are complete and visible from here on
+    if (tid == 0)
+        for (; issued < chain::kStages && issued < N; ++issued) load(issued);
+    pdl_launch_dependents();  // the output kernel may start its state-independent part
+    if (cb == 0)  // the sequence's later M_n and U_n into L2, once per sequence
+        for (int i = tid + chain::kStages; i < N; i += 128) {
+            const long long m = bh * N + i;
+            prefetch_l2(p.ws_m + m * 2 * 4096, 2 * 4096 * 2);
+            prefetch_l2(p.ws_u + m * 4096, 4096 * 4);
+        }
 
-    // This thread's state fragment: acc[nt][0..1] = S[r0][c0 + 8nt + 2t + {0,1}], acc[nt][2..3] = row r0 + 8.
-    const int r0 = 16 * warp + g;
-    float acc[2][4];
+    // This thread's fragment (the 16x256b TMEM layout of rows 16 w + lane/4 and +8): rows r0, r0 + 8,
+    // columns 8j + 2t, 8j + 2t + 1 (j = 0..3) of the CTA's 32 columns; sv[j][0..1] row r0, [2..3] row r0 + 8.
+    const int r0 = 16 * warp + (lane >> 2);
+    float sv[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int j = 0; j < 4; ++j) {
         float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
         if (p.S0) {
-            a = *reinterpret_cast<const float2*>(p.S0 + (bh * 64 + r0) * 64 + c0 + 8 * nt + 2 * t);
-            b = *reinterpret_cast<const float2*>(p.S0 + (bh * 64 + r0 + 8) * 64 + c0 + 8 * nt + 2 * t);
+            a = *reinterpret_cast<const float2*>(p.S0 + (bh * 64 + r0) * 64 + c0 + 8 * j + 2 * t);
+            b = *reinterpret_cast<const float2*>(p.S0 + (bh * 64 + r0 + 8) * 64 + c0 + 8 * j + 2 * t);
         }
-        acc[nt][0] = a.x, acc[nt][1] = a.y, acc[nt][2] = b.x, acc[nt][3] = b.y;
+        sv[j][0] = a.x, sv[j][1] = a.y, sv[j][2] = b.x, sv[j][3] = b.y;
     }
-    auto put_state = [&](int b) {  // fragment -> exchange buffer b (hi at part 0, lo at part 1)
+    // S (fragment) -> hi / lo into B tile `buf`
+    auto put_state = [&](int buf) {
+        uint8_t* bt = sm + chain::BT + buf * kTile;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            uint32_t h0, l0, h1, l1;
-            split2(acc[nt][0], acc[nt][1], h0, l0);
-            split2(acc[nt][2], acc[nt][3], h1, l1);
-            const int col = 8 * nt + 2 * t;
-            *reinterpret_cast<uint32_t*>(xb + (2 * b) * chain::kXBuf + (r0 * chain::kXS + col) * 2) = h0;
-            *reinterpret_cast<uint32_t*>(xb + (2 * b + 1) * chain::kXBuf + (r0 * chain::kXS + col) * 2) = l0;
-            *reinterpret_cast<uint32_t*>(xb + (2 * b) * chain::kXBuf + ((r0 + 8) * chain::kXS + col) * 2) = h1;
-            *reinterpret_cast<uint32_t*>(xb + (2 * b + 1) * chain::kXBuf + ((r0 + 8) * chain::kXS + col) * 2) = l1;
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int row = r0 + 8 * hf, col = 8 * j + 2 * t;
+                uint32_t h, l;
+                split2(sv[j][2 * hf], sv[j][2 * hf + 1], h, l);
+                *reinterpret_cast<uint32_t*>(bt + sw128(row, col)) = h;
+                *reinterpret_cast<uint32_t*>(bt + sw128(row, col + 32)) = l;
+            }
+    };
+    // B tile `buf` (complete) -> S_m hi / lo in the workspace, 16-byte chunks, by warps 1-3 while
+    // thread 0 issues the next MMAs
+    auto copy_state = [&](int buf, int m) {
+        if (warp == 0) return;
+        const uint8_t* bt = sm + chain::BT + buf * kTile;
+        bf16* dh = p.ws_s + ((bh * N + m) * 2 * 64) * 64 + c0;
+        for (int task = tid - 32; task < 512; task += 96) {  // logical chunk c: hi 0-3, lo 4-7
+            const int row = task >> 3, c = task & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(bt + row * 128 + ((c ^ (row & 7)) << 4));
+            *reinterpret_cast<uint4*>(dh + ((c >> 2) * 64 + row) * 64 + 8 * (c & 3)) = v;
         }
     };
-    auto store_state = [&](int b, int m) {  // exchange buffer b -> S_m in the workspace (16-byte chunks)
-#pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2) {
-            const int task = tid + 128 * k2, row = task >> 2, part = (task >> 1) & 1, ch = task & 1;
-            const uint4 v = *reinterpret_cast<const uint4*>(xb + (2 * b + part) * chain::kXBuf + (row * chain::kXS + 8 * ch) * 2);
-            *reinterpret_cast<uint4*>(p.ws_s + (((bh * N + m) * 2 + part) * 64 + row) * 64 + c0 + 8 * ch) = v;
-        }
-    };
-    if (N > 0) put_state(0);
+    put_state(0);
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
-    if (N > 0) store_state(0, 0);
+    tc_fence_after();
+    if (N > 0) copy_state(0, 0);
+    const uint32_t tmem = *tslot;
+    const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
 
     bool ok = true;
     for (int n = 0; n < N; ++n) {
-        const int s = n % 3;
-        if (__syncthreads_or(tid == 0 && !wait_or_flag(bar(s), (n / 3) & 1))) {
+        const int s = n % chain::kStages, buf = n & 1;
+        const uint32_t st = base + s * chain::kStage;
+        int bad = 0;
+        if (tid == 0) {
+            if (!wait_or_flag(full(s), (n / chain::kStages) & 1)) {
+                bad = 1;
+            } else {
+                tc_fence_after();
+                constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+                const uint32_t bt = base + chain::BT + buf * kTile;
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tmem, desc_k(st + part * kTile + 32 * ks), desc_mn(bt + 2048 * ks, kTile), id,
+                                 part + ks > 0);
+                mma_commit(bar_mma);
+                if (n > 0 && issued < N) {  // the previous step's stage is free: fetch M_{n+2}
+                    fence_async_smem();
+                    load(issued);
+                    ++issued;
+                }
+                if (!wait_or_flag(bar_mma, n & 1)) bad = 1;
+            }
+        }
+        if (__syncthreads_or(bad)) {
             ok = false;
             break;
         }
-        const uint32_t st = base + chain::STAGE + s * chain::kStage;
-        const uint32_t xr = base + chain::XB + 2 * (n & 1) * chain::kXBuf;
-        const float* un = reinterpret_cast<const float*>(sm + chain::STAGE + s * chain::kStage + 2 * kTile);
+        tc_fence_after();
+        uint32_t d[32];
+        tmem_ld_16x256b_x8(tq, d);
+        const float* un = reinterpret_cast<const float*>(sm + s * chain::kStage + 2 * kTile);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {  // the accumulators start from U_n
-            const float2 a = *reinterpret_cast<const float2*>(un + r0 * chain::kCols + 8 * nt + 2 * t);
-            const float2 b = *reinterpret_cast<const float2*>(un + (r0 + 8) * chain::kCols + 8 * nt + 2 * t);
-            acc[nt][0] = a.x, acc[nt][1] = a.y, acc[nt][2] = b.x, acc[nt][3] = b.y;
+        for (int j = 0; j < 4; ++j) {
+            const float2 ua = *reinterpret_cast<const float2*>(un + r0 * chain::kCols + 8 * j + 2 * t);
+            const float2 ub = *reinterpret_cast<const float2*>(un + (r0 + 8) * chain::kCols + 8 * j + 2 * t);
+            sv[j][0] = __uint_as_float(d[4 * j]) + __uint_as_float(d[4 * j + 16]) + ua.x;
+            sv[j][1] = __uint_as_float(d[4 * j + 1]) + __uint_as_float(d[4 * j + 17]) + ua.y;
+            sv[j][2] = __uint_as_float(d[4 * j + 2]) + __uint_as_float(d[4 * j + 18]) + ub.x;
+            sv[j][3] = __uint_as_float(d[4 * j + 3]) + __uint_as_float(d[4 * j + 19]) + ub.y;
         }
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const int ar = 16 * warp + (lane & 15), ac = 16 * ks + 8 * (lane >> 4);
-            const uint32_t aoff = ar * 128 + ((((ac >> 3)) ^ (ar & 7)) << 4);
-            uint32_t ah[4], al[4];
-            ldsm_x4(st + aoff, ah[0], ah[1], ah[2], ah[3]);
-            ldsm_x4(st + kTile + aoff, al[0], al[1], al[2], al[3]);
-            const int mi = lane >> 3, kr = 16 * ks + (lane & 7) + 8 * (mi & 1), nc = 8 * (mi >> 1);
-            const uint32_t boff = (kr * chain::kXS + nc) * 2;
-            uint32_t bh[4], bl[4];
-            ldsm_x4_t(xr + boff, bh[0], bh[1], bh[2], bh[3]);
-            ldsm_x4_t(xr + chain::kXBuf + boff, bl[0], bl[1], bl[2], bl[3]);
-            mma16816_x3(acc[0], ah, al, bh[0], bh[1], bl[0], bl[1]);
-            mma16816_x3(acc[1], ah, al, bh[2], bh[3], bl[2], bl[3]);
-        }
-        if (n + 1 < N) put_state((n + 1) & 1);
-        __syncthreads();
-        if (tid == 0 && issued < N) {  // stage s is free again: fetch M_{n+3}
-            fence_async_smem();
-            load_m(issued);
-            ++issued;
-        }
-        if (n + 1 < N) store_state((n + 1) & 1, n + 1);
+        put_state(buf ^ 1);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();  // next B tile written; stage s consumed by the MMA and the reads of U
+        if (n + 1 < N) copy_state(buf ^ 1, n + 1);
     }
-    if (!ok) {  // drain the loads still in flight (bounded), then leave
+    if (!ok) {  // drain the loads still in flight (bounded), free TMEM, leave
         if (tid == 0)
-            for (int m = 0; m < issued; ++m) mbar_wait_bounded(bar(m % 3), (m / 3) & 1, kTimeoutCycles);
+            for (int m = 0; m < issued; ++m)
+                mbar_wait_bounded(full(m % chain::kStages), (m / chain::kStages) & 1, kTimeoutCycles);
+        release_tmem(tmem, warp, chain::kTmemCols);
         return;
     }
     if (p.S_final) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            *reinterpret_cast<float2*>(p.S_final + (bh * 64 + r0) * 64 + c0 + 8 * nt + 2 * t) =
-                make_float2(acc[nt][0], acc[nt][1]);
-            *reinterpret_cast<float2*>(p.S_final + (bh * 64 + r0 + 8) * 64 + c0 + 8 * nt + 2 * t) =
-                make_float2(acc[nt][2], acc[nt][3]);
+        for (int j = 0; j < 4; ++j) {
+            *reinterpret_cast<float2*>(p.S_final + (bh * 64 + r0) * 64 + c0 + 8 * j + 2 * t) =
+                make_float2(sv[j][0], sv[j][1]);
+            *reinterpret_cast<float2*>(p.S_final + (bh * 64 + r0 + 8) * 64 + c0 + 8 * j + 2 * t) =
+                make_float2(sv[j][2], sv[j][3]);
         }
     }
     if (p.tail_out && cb == 0 && tid < 8) {  // window 1: the tail is the last key (the next call's x)
@@ -642,6 +687,7 @@ __global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant
         else if (p.pos > 0) v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[tid];
         reinterpret_cast<uint4*>(p.tail_out + bh * 64)[tid] = v;
     }
+    release_tmem(tmem, warp, chain::kTmemCols);
 }
 
 // ---------------------------------------------------------------- output kernel: R and O from S_n
@@ -649,17 +695,21 @@ __global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant
 // wanted), so each epilogue reads whole 32-lane quadrants. Where only the second 64 rows are
 // wanted, the first 64 rows of the A operand are whatever tile precedes it in shared memory.
 namespace outk {
-constexpr int X = 0, Q = 1, Y = 2, SH = 3, SL = 4, TH = 5, TL = 6, PH = 7, PL = 8, YH = 9, YL = 10, RH = 11,
-              RL = 12;  // 8 KB tiles, in this order: adjacency forms the stacked M = 128 operands
-constexpr int SCAL = 13 * kTile;
+// 8 KB tiles. Loaded: X, Q, Y, S_hi, S_lo, T_hi, T_lo; built: P_hi, P_lo. Later tenants of dead
+// tiles: Y' hi / lo in X / Q, R hi / lo in Y / S_hi, the output tile in X. The order makes the
+// stacked operands [X; Q], [S_lo; T_hi], [T_hi; T_lo], [T_lo; P_hi] and [P_hi; P_lo] contiguous.
+constexpr int X = 0, Q = 1, Y = 2, SH = 3, SL = 4, TH = 5, TL = 6, PH = 7, PL = 8;
+constexpr int YH = X, YL = Q, RH = Y, RL = SH, OUT = X;
+constexpr int SCAL = 9 * kTile;
 constexpr int BAR = SCAL + (int)sizeof(Scal);
 constexpr int BYTES = BAR + 32;
 constexpr int ALLOC = BYTES + 1024;
-constexpr uint32_t D1 = 0, DXQ = 64, DR = 128, DO = 0;  // TMEM columns; DO reuses D1 once P is built
-static_assert(BAR % 8 == 0, "layout");
+constexpr uint32_t kCols = 128;
+constexpr uint32_t D1 = 0, DXQ = 64, DR = 0, DO = 0;  // D1 -> DR -> DO take turns in columns 0-63
+static_assert(BAR % 8 == 0 && SCAL % 16 == 0, "layout");
 }  // namespace outk
 
-__global__ void __launch_bounds__(256, 2) falcon_out_kernel(const __grid_constant__ SplitParams p) {
+__global__ void __launch_bounds__(256, 3) falcon_out_kernel(const __grid_constant__ SplitParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -671,31 +721,25 @@ __global__ void __launch_bounds__(256, 2) falcon_out_kernel(const __grid_constan
     const long long bh = cid / p.N;
     const int n = (int)(cid - bh * p.N);
     const long long t0 = (long long)n * kC;
-    const int nv = (int)min((long long)kC, p.T - t0);
     const bool f1 = p.variant == kF1;
-    Scal* sc = reinterpret_cast<Scal*>(sm + outk::SCAL);
-    const uint32_t bar_tma = base + outk::BAR, bar_mma = base + outk::BAR + 8;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + outk::BAR + 16);
+    const Scal* sc = reinterpret_cast<const Scal*>(sm + outk::SCAL);
+    const uint32_t bar_tma = base + outk::BAR, bar_mma = base + outk::BAR + 8, bar_s = base + outk::BAR + 16;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + outk::BAR + 24);
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
+        mbar_init(bar_s, 1);
         mbar_init_fence();
-        mbar_expect_tx(bar_tma, 7 * kTile);
+        mbar_expect_tx(bar_tma, 5 * kTile + (uint32_t)sizeof(Scal));
         tma_load_3d(taddr(outk::X), &p.tm_k, 0, (int)t0 - 1, (int)bh, bar_tma);
         tma_load_3d(taddr(outk::Q), &p.tm_q, 0, (int)t0, (int)bh, bar_tma);
         tma_load_3d(taddr(outk::Y), &p.tm_v, 0, (int)t0, (int)bh, bar_tma);
-        tma_load_2d(taddr(outk::SH), &p.tm_s, 0, (int)(cid * 128), bar_tma);
-        tma_load_2d(taddr(outk::SL), &p.tm_s, 0, (int)(cid * 128 + 64), bar_tma);
         tma_load_2d(taddr(outk::TH), &p.tm_t, 0, (int)(cid * 128), bar_tma);
         tma_load_2d(taddr(outk::TL), &p.tm_t, 0, (int)(cid * 128 + 64), bar_tma);
+        bulk_load(base + outk::SCAL, p.ws_sc + cid * kScalBytes, (uint32_t)sizeof(Scal), bar_tma);
     }
-    if (warp == 0) tmem_alloc(smem_u32(tslot), kTmemCols);
-    float beta_i = 0.f, lam_i = 0.f;
-    if (tid < nv) {
-        beta_i = p.beta[bh * p.T + t0 + tid];
-        lam_i = p.lam[bh * p.T + t0 + tid];
-    }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), outk::kCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -706,7 +750,7 @@ __global__ void __launch_bounds__(256, 2) falcon_out_kernel(const __grid_constan
     const bool upper = trow >= 64;  // lanes 64-127: warps 2, 3, 6, 7
     const int r = trow & 63;
 
-    if (!cta_wait(bar_tma, 0, tid)) return release_tmem(tmem, warp);
+    if (!cta_wait(bar_tma, 0, tid)) return release_tmem(tmem, warp, outk::kCols);
     if (n == 0 && p.pos > 0 && tid < 8) {
         const uint4 v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[tid];
         *reinterpret_cast<uint4*>(tile(outk::X) + sw128(0, 8 * tid)) = v;
@@ -719,61 +763,79 @@ __global__ void __launch_bounds__(256, 2) falcon_out_kernel(const __grid_constan
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // [G; Sc] = [X; Q] X^T
             mma_bf16(tmem + outk::D1, desc_k(taddr(outk::X) + 32 * ks), desc_k(taddr(outk::X) + 32 * ks), idk, ks > 0);
+        mma_commit(bar_mma);
+    }
+    const bool fast = sc->misc[3] != 0.f;
+    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp, outk::kCols);
+    tc_fence_after();
+
+    // ---- lanes 64-127: P rows (K-major A tiles)
+    if (upper) {
+        float v[32];
+        tmem_ld32(tq + outk::D1 + 32 * hw, v);
+        const int i = r;
+        float pv[32];
+        if (fast) {
+            const float el = sc->eL[i];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = 32 * hw + jj;
+                pv[jj] = j <= i ? el * sc->cA[j] * v[jj] : 0.f;
+            }
+        } else {
+            const float li = sc->L[i];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = 32 * hw + jj;
+                pv[jj] = j <= i ? sc->eta[j] * __expf(li - sc->L[j]) * v[jj] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) st8_hilo(tile(outk::PH), tile(outk::PL), sw128(i, 32 * hw + 8 * c), pv + 8 * c);
+    }
+
+    // ---- the chunk-start state from the chain kernel: [X S; Q S]
+    pdl_wait();
+    if (tid == 0) {
+        mbar_expect_tx(bar_s, 2 * kTile);
+        tma_load_2d(taddr(outk::SH), &p.tm_s, 0, (int)(cid * 128), bar_s);
+        tma_load_2d(taddr(outk::SL), &p.tm_s, 0, (int)(cid * 128 + 64), bar_s);
+    }
+    if (!cta_wait(bar_s, 0, tid)) return release_tmem(tmem, warp, outk::kCols);
+    if (tid == 0) {
+        tc_fence_after();
         constexpr uint32_t idm = idesc_bf16(128, 64, false, true);
 #pragma unroll
-        for (int part = 0; part < 2; ++part)  // [X S; Q S] with S = S_hi + S_lo (MN-major, K = feature)
+        for (int part = 0; part < 2; ++part)  // S = S_hi + S_lo (MN-major, K = feature)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16(tmem + outk::DXQ, desc_k(taddr(outk::X) + 32 * ks),
                          desc_mn(taddr(outk::SH + part) + 2048 * ks, kTile), idm, part + ks > 0);
         mma_commit(bar_mma);
     }
-    chunk_scalars(sc, tile(outk::X), tid, beta_i, lam_i, nv, p.pos + t0 + 1, p.eps, p.eps_gamma);
-    const bool fast = sc->misc[3] != 0.f;
-    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp);
+    if (!cta_wait(bar_mma, 1, tid)) return release_tmem(tmem, warp, outk::kCols);
     tc_fence_after();
 
-    // ---- lanes 64-127: P rows (K-major A tiles); lanes 0-63: Y' = Y - diag(e^{Lx}) X S rows (MN-major B)
-    {
+    // ---- lanes 0-63: Y' = Y - diag(e^{Lx}) X S rows (MN-major B), into the dead X and Q tiles
+    if (!upper) {
         float v[32];
-        tmem_ld32(tq + (upper ? outk::D1 : outk::DXQ) + 32 * hw, v);
-        if (upper) {
-            const int i = r;
-            float pv[32];
-            if (fast) {
-                const float el = sc->eL[i];
+        tmem_ld32(tq + outk::DXQ + 32 * hw, v);
+        const float ex = f1 ? sc->eLx[r] : 0.f;
+        float y[4][8];
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * hw + jj;
-                    pv[jj] = j <= i ? el * sc->cA[j] * v[jj] : 0.f;
-                }
-            } else {
-                const float li = sc->L[i];
+        for (int c = 0; c < 4; ++c)
+            unpack8(*reinterpret_cast<const uint4*>(tile(outk::Y) + sw128(r, 32 * hw + 8 * c)), y[c]);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * hw + jj;
-                    pv[jj] = j <= i ? sc->eta[j] * __expf(li - sc->L[j]) * v[jj] : 0.f;
-                }
-            }
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) st8_hilo(tile(outk::PH), tile(outk::PL), sw128(i, 32 * hw + 8 * c), pv + 8 * c);
-        } else {
-            const float ex = f1 ? sc->eLx[r] : 0.f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t off = sw128(r, 32 * hw + 8 * c);
-                float y[8];
-                unpack8(*reinterpret_cast<const uint4*>(tile(outk::Y) + off), y);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = fmaf(-ex, v[8 * c + e], y[e]);
-                st8_hilo(tile(outk::YH), tile(outk::YL), off, y);
-            }
+            for (int e = 0; e < 8; ++e) y[c][e] = fmaf(-ex, v[8 * c + e], y[c][e]);
+            st8_hilo(tile(outk::YH), tile(outk::YL), sw128(r, 32 * hw + 8 * c), y[c]);
         }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // R = T Y' in lanes 64-127: A = [SL; TH] carries T_hi, [TH; TL] carries T_lo
+    if (tid == 0) {  // R = T Y' in lanes 64-127: A = [S_lo; T_hi] carries T_hi, [T_hi; T_lo] carries T_lo
         tc_fence_after();
         constexpr uint32_t id = idesc_bf16(128, 64, false, true);
 #pragma unroll
@@ -790,9 +852,9 @@ __global__ void __launch_bounds__(256, 2) falcon_out_kernel(const __grid_constan
                      id, 1);
         mma_commit(bar_mma);
     }
-    if (!cta_wait(bar_mma, 1, tid)) return release_tmem(tmem, warp);
+    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp, outk::kCols);
     tc_fence_after();
-    if (upper) {  // R rows -> hi / lo (MN-major B, K = token)
+    if (upper) {  // R rows -> hi / lo (MN-major B, K = token) in the dead Y and S_hi tiles
         float v[32];
         tmem_ld32(tq + outk::DR + 32 * hw, v);
 #pragma unroll
@@ -801,7 +863,7 @@ __global__ void __launch_bounds__(256, 2) falcon_out_kernel(const __grid_constan
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // P R in lanes 64-127: A = [TL; PH] carries P_hi, [PH; PL] carries P_lo
+    if (tid == 0) {  // P R in lanes 64-127: A = [T_lo; P_hi] carries P_hi, [P_hi; P_lo] carries P_lo
         tc_fence_after();
         constexpr uint32_t id = idesc_bf16(128, 64, false, true);
 #pragma unroll
@@ -818,9 +880,9 @@ __global__ void __launch_bounds__(256, 2) falcon_out_kernel(const __grid_constan
                      id, 1);
         mma_commit(bar_mma);
     }
-    if (!cta_wait(bar_mma, 0, tid)) return release_tmem(tmem, warp);
+    if (!cta_wait(bar_mma, 1, tid)) return release_tmem(tmem, warp, outk::kCols);
     tc_fence_after();
-    if (upper) {  // O = diag(e^L) Q S + P R -> bf16 tile in the X region
+    if (upper) {  // O = diag(e^L) Q S + P R -> bf16 output tile
         float qs[32], po[32];
         tmem_ld32x2(tq + outk::DXQ + 32 * hw, tq + outk::DO + 32 * hw, qs, po);
         const float el = sc->eL[r];
@@ -829,16 +891,16 @@ __global__ void __launch_bounds__(256, 2) falcon_out_kernel(const __grid_constan
             float o[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = fmaf(el, qs[8 * c + e], po[8 * c + e]);
-            *reinterpret_cast<uint4*>(tile(outk::X) + sw128(r, 32 * hw + 8 * c)) = pack8(o);
+            *reinterpret_cast<uint4*>(tile(outk::OUT) + sw128(r, 32 * hw + 8 * c)) = pack8(o);
         }
     }
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {  // TMA store; rows past T are clipped
-        tma_store_3d(&p.tm_out, taddr(outk::X), 0, (int)t0, (int)bh);
+        tma_store_3d(&p.tm_out, taddr(outk::OUT), 0, (int)t0, (int)bh);
         tma_store_wait_read();
     }
-    release_tmem(tmem, warp);
+    release_tmem(tmem, warp, outk::kCols);
 }
 
 // ---------------------------------------------------------------- host side
@@ -886,13 +948,13 @@ bool encode_rows(CUtensorMap* tm, const void* ptr, long long rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// U: [rows][64] fp32, boxes of 16 columns x 64 rows (one chain CTA's columns), no swizzle
+// U: [rows][64] fp32, boxes of chain::kCols columns x 64 rows (one chain CTA's columns), no swizzle
 bool encode_u(CUtensorMap* tm, const void* ptr, long long rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {64, (cuuint64_t)rows};
     cuuint64_t strides[1] = {64 * 4};
-    cuuint32_t box[2] = {16, 64};
+    cuuint32_t box[2] = {chain::kCols, 64};
     cuuint32_t es[2] = {1, 1};
     return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -921,7 +983,7 @@ bool split_supported(const Launch& a) {
 }
 
 size_t split_workspace_bytes(const Launch& a) {
-    return (size_t)(a.B * a.H) * (size_t)n_chunks(a) * (size_t)(4 * 16384);
+    return (size_t)(a.B * a.H) * (size_t)n_chunks(a) * (size_t)(4 * 16384 + kScalBytes);
 }
 
 int launch_split(const Launch& a, cudaStream_t st) {
@@ -934,6 +996,7 @@ int launch_split(const Launch& a, cudaStream_t st) {
     p.ws_u = reinterpret_cast<float*>(ws + per);
     p.ws_s = reinterpret_cast<bf16*>(ws + 2 * per);
     p.ws_t = reinterpret_cast<bf16*>(ws + 3 * per);
+    p.ws_sc = ws + 4 * per;
     if (N > 0) {
         if (!encode_bhtd(&p.tm_q, a.q, a.T, BH) || !encode_bhtd(&p.tm_k, a.k, a.T, BH) ||
             !encode_bhtd(&p.tm_v, a.v, a.T, BH) || !encode_bhtd(&p.tm_out, a.out, a.T, BH) ||
@@ -965,10 +1028,28 @@ int launch_split(const Launch& a, cudaStream_t st) {
             return 4;
         attr_set = true;
     }
+    // prep: an ordinary launch (it overwrites the workspace the previous call's output kernel read);
+    // chain and output: programmatic dependent launches that overlap their predecessor's tail.
     if (N > 0) falcon_prep_kernel<<<(unsigned)(BH * N), 256, prep::ALLOC, st>>>(p);
-    falcon_chain_kernel<<<dim3(64 / chain::kCols, (unsigned)BH), 128, chain::ALLOC, st>>>(p);
-    if (N > 0) falcon_out_kernel<<<(unsigned)(BH * N), 256, outk::ALLOC, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+    if (cudaGetLastError() != cudaSuccess) return 4;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(64 / chain::kCols, (unsigned)BH);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = chain::ALLOC;
+    if (cudaLaunchKernelEx(&cfg, falcon_chain_kernel, p) != cudaSuccess) return 4;
+    if (N > 0) {
+        cfg.gridDim = dim3((unsigned)(BH * N));
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = outk::ALLOC;
+        if (cudaLaunchKernelEx(&cfg, falcon_out_kernel, p) != cudaSuccess) return 4;
+    }
+    return 0;
 }
 
 int split_consume_timeout_flag(int* flag) {
