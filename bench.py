@@ -126,6 +126,11 @@ def _dist_setup():
     return None, rank, world, local
 
 
+def _job_value(world, tokens_per_rank_step, steps, max_total_ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time (weak scaling)."""
+    return world * tokens_per_rank_step * steps / (max_total_ms / 1e3)
+
+
 def _barrier_max(dist, value):
     if dist is None:
         return value
@@ -342,7 +347,7 @@ def run_ours(args, w):
     total_ms = _barrier_max(dist, total_ms)
     ms_step = total_ms / args.steps
     tokens_step = w.total_tokens
-    value = world * tokens_step * args.steps / (total_ms / 1e3)
+    value = _job_value(world, tokens_step, args.steps, total_ms)
     e2e_ms = _barrier_max(dist, e2e_ms)
     if rank != 0:
         return
@@ -358,8 +363,9 @@ def run_ours(args, w):
                    "parallelism": f"dp{world} (independent sequences per GPU, no collective)",
                    "l2": f"rotating {nsets} input/output sets of {step_bytes / 1e6:.1f} MB (> L2 between reuses)",
                    "kernel": {1: "cuda-core chunk kernel", 2: "single-pass tcgen05/TMA chunk kernel",
-                              3: "split path: tcgen05 prep, mma.sync chain, tcgen05 output kernels"}.get(kernel_id, "?")},
+                              3: "split path: tcgen05/TMA prep, chain and output kernels"}.get(kernel_id, "?")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "scope": "one falcon_fwd call (all kernels it launches); per-kernel shares in profiles/",
                      "traffic": _traffic(w.name, kernel_id), "peak_source": src,
                      "algorithmic_bytes_per_step": step_bytes, "mean_launch_ms": mean_launch},
         "e2e": None if args.no_e2e else {"value": world * tokens_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
