@@ -121,6 +121,24 @@ int falcon_fwd(int variant, const void* q, const void* k, const void* v, const f
  * no path uses a workspace or the arguments are invalid). Host only. */
 size_t falcon_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk);
 
+/*
+ * falcon_fwd_static — falcon_fwd with the library's own scratch instead of a caller workspace.
+ * The paper has no counterpart: this is an engineering entry point for callers that must not
+ * allocate (for example while building a CUDA graph). Same arguments and results as falcon_fwd
+ * with a workspace. The scratch is a fixed FALCON_STATIC_WORKSPACE_BYTES device array inside the
+ * library, located once per device on the first call (cudaGetSymbolAddress) and never allocated
+ * or freed. Nothing in it needs zeroing: every byte a kernel reads was written earlier in the same
+ * call. A shape whose split path needs more than FALCON_STATIC_WORKSPACE_BYTES returns
+ * FALCON_ERR_UNSUPPORTED without launching; a shape with no split path runs the single-pass
+ * kernels. Calls that may overlap in time on one device (any streams) race on the scratch and
+ * must be serialized by the caller. Make the first call on each device before capturing a stream
+ * into a graph, so that the one-time set-up is not inside the capture.
+ */
+#define FALCON_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
+int falcon_fwd_static(int variant, const void* q, const void* k, const void* v, const float* beta,
+                      const float* lambda, const float* S0, const void* tail, void* out, float* S_final,
+                      void* tail_out, const falcon_dims_t* dims, int chunk, void* stream);
+
 /* Bytes of one tail buffer for `dims` (all B*H sequences); 0 for a NULL or invalid dims. */
 size_t falcon_tail_bytes(const falcon_dims_t* dims);
 

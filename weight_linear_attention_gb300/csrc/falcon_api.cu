@@ -5,10 +5,27 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "falcon.h"
 #include "falcon_internal.h"
 
+// Scratch of falcon_fwd_static: a file-scope device array (one per device), never allocated.
+static __device__ __align__(256) uint8_t g_static_workspace[FALCON_STATIC_WORKSPACE_BYTES];
+
 namespace {
+
+// Its address on the current device, looked up once per device.
+void* static_workspace_address() {
+    constexpr int kMaxDevices = 64;
+    static void* addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev] && cudaGetSymbolAddress(&addr[dev], g_static_workspace) != cudaSuccess) addr[dev] = nullptr;
+    return addr[dev];
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -183,6 +200,20 @@ int falcon_fwd(int variant, const void* q, const void* k, const void* v, const f
     if (a.ws) return falcon::launch_split(a, s);
     if (falcon::tc_supported(a)) return falcon::launch_tc(a, s);
     return falcon::launch_generic(a, s);
+}
+
+int falcon_fwd_static(int variant, const void* q, const void* k, const void* v, const float* beta,
+                      const float* lambda, const float* S0, const void* tail, void* out, float* S_final,
+                      void* tail_out, const falcon_dims_t* dims, int chunk, void* stream) {
+    falcon::Launch shape = {};
+    const int st = validate_shape(variant, dims, chunk, tail != nullptr, &shape);
+    if (st != FALCON_OK) return st;
+    const size_t need = falcon::split_supported(shape) ? falcon::split_workspace_bytes(shape) : 0;
+    if (need > FALCON_STATIC_WORKSPACE_BYTES) return FALCON_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    if (need > 0 && !(ws = static_workspace_address())) return FALCON_ERR_CUDA;
+    return falcon_fwd(variant, q, k, v, beta, lambda, S0, tail, out, S_final, tail_out, dims, chunk, ws,
+                      ws ? FALCON_STATIC_WORKSPACE_BYTES : 0, stream);
 }
 
 int falcon_device_status(void* stream) {

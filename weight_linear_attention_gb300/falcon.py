@@ -48,8 +48,9 @@ assert ctypes.sizeof(FalconDims) == 64
 _lock = threading.Lock()
 _lib = None
 
-EXPORTED = ("falcon_fwd", "falcon_workspace_bytes", "falcon_tail_bytes", "falcon_status_string",
-            "falcon_device_status", "falcon_kernel_for", "falcon_abi_version")
+EXPORTED = ("falcon_fwd", "falcon_workspace_bytes", "falcon_fwd_static", "falcon_tail_bytes",
+            "falcon_status_string", "falcon_device_status", "falcon_kernel_for", "falcon_abi_version")
+STATIC_WORKSPACE_BYTES = 16 << 20
 
 
 class FalconError(RuntimeError):
@@ -76,6 +77,9 @@ def load(path: str | None = None):
         lib.falcon_fwd.restype = ctypes.c_int
         lib.falcon_fwd.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                    ctypes.POINTER(FalconDims), ctypes.c_int, vp, ctypes.c_size_t, vp]
+        lib.falcon_fwd_static.restype = ctypes.c_int
+        lib.falcon_fwd_static.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          ctypes.POINTER(FalconDims), ctypes.c_int, vp]
         lib.falcon_workspace_bytes.restype = ctypes.c_size_t
         lib.falcon_workspace_bytes.argtypes = [ctypes.c_int, ctypes.POINTER(FalconDims), ctypes.c_int]
         lib.falcon_tail_bytes.restype = ctypes.c_size_t
@@ -152,6 +156,14 @@ def falcon_fwd(variant, q, k, v, beta, lam, S0, tail, out, S_final, tail_out, di
     return int(load().falcon_fwd(int(variant), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
                                  _ptr(tail), _ptr(out), _ptr(S_final), _ptr(tail_out), ctypes.byref(dims),
                                  int(chunk), _ptr(workspace), int(workspace_bytes), _stream_handle(stream)))
+
+
+def falcon_fwd_static(variant, q, k, v, beta, lam, S0, tail, out, S_final, tail_out, dims: FalconDims, chunk: int,
+                      stream=None) -> int:
+    """The no-allocation C entry point (the library's own fixed scratch); returns the status."""
+    return int(load().falcon_fwd_static(int(variant), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
+                                        _ptr(tail), _ptr(out), _ptr(S_final), _ptr(tail_out), ctypes.byref(dims),
+                                        int(chunk), _stream_handle(stream)))
 
 
 def workspace_for(variant, dims: FalconDims, chunk: int, device):
