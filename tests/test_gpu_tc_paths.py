@@ -165,3 +165,20 @@ def test_bad_workspace_call_leaves_outputs():
     assert st == F.FALCON_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(out == 7.0)
+
+
+@pytest.mark.parametrize("variant", [F1, F1A])
+def test_odd_sequence_count_with_state_and_tail(variant):
+    """2 x 19 sequences (not a multiple of any launch width), from a nonzero state, continued
+    from a tail after a cut inside the second chunk."""
+    w = _wl(variant, heads=19, nonzero_s0=True)
+    T = 200
+    inp = I.make_inputs(w, seed=29, seqlen=T, batch=2)
+    cut = 70
+    a, b = slice_inputs(inp, 0, cut), slice_inputs(inp, cut, T)
+    o1, S1, t1 = run_gpu(variant, a, chunk=64, S0=inp["S0"])
+    o2, S2, t2 = run_gpu(variant, b, chunk=64, pos=cut, S0=S1, tail=t1)
+    ro, rS, rt = run_oracle(variant, inp, S0=inp["S0"])
+    _check("groups out", torch.cat([o1, o2], dim=2), ro)
+    _check("groups S", S2, rS)
+    np.testing.assert_array_equal(F.split_tail(t2, 2, 19, 1, 64, 64)[0].double().numpy(), rt[0])
