@@ -102,22 +102,22 @@ __host__ __device__ inline size_t smem_floats(int variant, int dk, int dvs, int 
         if (dst) *dst = base + off;
         off += (n + 3) & ~size_t(3);  // keep 16-byte alignment of every array
     };
-    take(s ? &s->X : nullptr, size_t(NE) * dk);
-    take(s ? &s->Q : nullptr, size_t(C) * dk);
+    take(s ? &s->X : nullptr, size_t(NE) * (dk + 1));  // rows padded: the Gram reads rows across lanes
+    take(s ? &s->Q : nullptr, size_t(C) * (dk + 1));
     take(s ? &s->Y : nullptr, size_t(NE) * dvs);
     take(s ? &s->S : nullptr, size_t(dk) * dvs);
     take(s ? &s->G : nullptr, size_t(NE) * NE);
     take(s ? &s->Sc : nullptr, size_t(C) * NE);
     take(s ? &s->H : nullptr, size_t(NE) * dvs);
     take(s ? &s->QS : nullptr, size_t(C) * dvs);
-    take(s ? &s->R : nullptr, size_t(C) * W * dvs);
+    take(s ? &s->R : nullptr, size_t(C * W + 1) * dvs);  // column-major, odd stride (see RS)
     take(s ? &s->A : nullptr, size_t(C) * C);
     take(s ? &s->P : nullptr, size_t(C) * C);
-    take(s ? &s->eta : nullptr, size_t(C) * per_col);
-    take(s ? &s->L : nullptr, size_t(C) * per_col);
-    take(s ? &s->Lx : nullptr, size_t(C) * per_col);
+    take(s ? &s->eta : nullptr, size_t(C + 1) * per_col);  // Falcon-2: column-major, odd stride (see CS)
+    take(s ? &s->L : nullptr, size_t(C + 1) * per_col);
+    take(s ? &s->Lx : nullptr, size_t(C + 1) * per_col);
     take(s ? &s->kap : nullptr, size_t(C));
-    take(s ? &s->w : nullptr, size_t(C) * per_col);
+    take(s ? &s->w : nullptr, size_t(C + 1) * per_col);
     return off;
 }
 
@@ -126,7 +126,11 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
     extern __shared__ __align__(16) float smem_raw[];
     const int tid = threadIdx.x;
     const int DK = p.dk, DV = p.dv, DVS = p.dvs, C = p.C;
+    const int XS = DK + 1;  // row stride of X and Q in shared memory (odd: rows fall in different banks)
     const int W = (VAR == kF3) ? p.W : 1;
+    // R (and Falcon-2's per-column scalars) are stored column-major with an odd stride, since the
+    // forward substitution runs down one column across the lanes of a warp.
+    const int RS = C * W + 1, CS = C + 1;
     const int NE = C + W - 1;
     const long long T = p.T, pos = p.pos;
     const int slices = DV / DVS;
@@ -175,11 +179,11 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             const long long gpair = pos + t0 + 2 - W + e;
             float x = 0.f;
             if (e < n + W - 1 && gpair >= 2) x = load_key(t0 - W + e, cc);
-            s.X[idx] = x;
+            s.X[e * XS + cc] = x;
         }
         for (int idx = tid; idx < C * DK; idx += kThreads) {
             const int i = idx / DK, cc = idx % DK;
-            s.Q[idx] = i < n ? ldf(q + (t0 + i) * DK + cc) : 0.f;
+            s.Q[i * XS + cc] = i < n ? ldf(q + (t0 + i) * DK + cc) : 0.f;
         }
         for (int idx = tid; idx < NE * DVS; idx += kThreads) {
             const int e = idx / DVS, cc = idx % DVS;
@@ -193,25 +197,25 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         for (int idx = tid; idx < NE * NE; idx += kThreads) {
             const int a = idx / NE, b = idx % NE;
             float acc = 0.f;
-            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.X[a * DK + cc], s.X[b * DK + cc], acc);
+            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.X[a * XS + cc], s.X[b * XS + cc], acc);
             s.G[idx] = acc;
         }
         for (int idx = tid; idx < C * NE; idx += kThreads) {
             const int i = idx / NE, b = idx % NE;
             float acc = 0.f;
-            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.Q[i * DK + cc], s.X[b * DK + cc], acc);
+            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.Q[i * XS + cc], s.X[b * XS + cc], acc);
             s.Sc[idx] = acc;
         }
         for (int idx = tid; idx < NE * DVS; idx += kThreads) {
             const int e = idx / DVS, c = idx % DVS;
             float acc = 0.f;
-            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.X[e * DK + cc], s.S[cc * DVS + c], acc);
+            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.X[e * XS + cc], s.S[cc * DVS + c], acc);
             s.H[idx] = acc;
         }
         for (int idx = tid; idx < C * DVS; idx += kThreads) {
             const int i = idx / DVS, c = idx % DVS;
             float acc = 0.f;
-            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.Q[i * DK + cc], s.S[cc * DVS + c], acc);
+            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.Q[i * XS + cc], s.S[cc * DVS + c], acc);
             s.QS[idx] = acc;
         }
         __syncthreads();
@@ -229,10 +233,10 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                         eta = den == 0.f ? 0.f : beta[(t0 + i) * DV + c0 + c] / den;
                         alpha = fminf(eta * lm, 1.f - p.eps_gamma);
                     }
-                    s.eta[i * DVS + c] = eta;
-                    s.Lx[i * DVS + c] = run;
+                    s.eta[c * CS + i] = eta;
+                    s.Lx[c * CS + i] = run;
                     run += log1pf(-alpha);
-                    s.L[i * DVS + c] = run;
+                    s.L[c * CS + i] = run;
                 }
             }
         } else if (tid < 32) {
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         } else {
             for (int idx = tid; idx < C * DVS; idx += kThreads) {
                 const int j = idx / DVS, c = idx % DVS;
-                s.w[idx] = s.eta[idx] * expf(s.L[(C - 1) * DVS + c] - s.L[idx]);
+                s.w[c * CS + j] = s.eta[c * CS + j] * expf(s.L[c * CS + C - 1] - s.L[c * CS + j]);
             }
         }
         __syncthreads();
@@ -319,17 +323,17 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             for (int i = 0; i < n; ++i) {
                 float acc = 0.f;
                 if (VAR == kF1) {
-                    for (int j = lg; j < i; j += gl) acc = fmaf(s.A[i * C + j], s.R[j * DVS + col], acc);
+                    for (int j = lg; j < i; j += gl) acc = fmaf(s.A[i * C + j], s.R[col * RS + j], acc);
                 } else {
-                    const float lxi = s.Lx[i * DVS + col];
+                    const float lxi = s.Lx[col * CS + i];
                     for (int j = lg; j < i; j += gl)
-                        acc = fmaf(s.eta[j * DVS + col] * expf(lxi - s.L[j * DVS + col]) * s.G[i * NE + j],
-                                   s.R[j * DVS + col], acc);
+                        acc = fmaf(s.eta[col * CS + j] * expf(lxi - s.L[col * CS + j]) * s.G[i * NE + j],
+                                   s.R[col * RS + j], acc);
                 }
                 for (int o = gl >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                const float dcy = (VAR == kF1) ? expf(s.Lx[i]) : expf(s.Lx[i * DVS + col]);
+                const float dcy = (VAR == kF1) ? expf(s.Lx[i]) : expf(s.Lx[col * CS + i]);
                 const float r = (s.Y[i * DVS + col] - dcy * s.H[i * DVS + col]) - acc;
-                if (lg == 0) s.R[i * DVS + col] = r;
+                if (lg == 0) s.R[col * RS + i] = r;
                 __syncwarp();
             }
         } else if (VAR == kF3) {
@@ -341,11 +345,11 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                     float acc = 0.f;
                     for (int m = lg; m < i * W; m += gl) {
                         const int l = m / W, b = m % W;
-                        acc = fmaf(s.A[i * C + l] * s.G[pa * NE + (l - b + W - 1)], s.R[m * DVS + col], acc);
+                        acc = fmaf(s.A[i * C + l] * s.G[pa * NE + (l - b + W - 1)], s.R[col * RS + m], acc);
                     }
                     for (int o = gl >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
                     const float r = valid ? (s.Y[pa * DVS + col] - dcy * s.H[pa * DVS + col]) - acc : 0.f;
-                    if (lg == 0) s.R[(i * W + a) * DVS + col] = r;
+                    if (lg == 0) s.R[col * RS + i * W + a] = r;
                     __syncwarp();
                 }
             }
@@ -357,22 +361,24 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             const int i = idx / DVS, c = idx % DVS;
             float o;
             if (VAR == kF2) {
-                const float li = s.L[i * DVS + c];
+                const float li = s.L[c * CS + i];
                 o = expf(li) * s.QS[idx];
                 for (int j = 0; j <= i; ++j)
-                    o = fmaf(s.eta[j * DVS + c] * expf(li - s.L[j * DVS + c]) * s.Sc[i * NE + j], s.R[j * DVS + c], o);
+                    o = fmaf(s.eta[c * CS + j] * expf(li - s.L[c * CS + j]) * s.Sc[i * NE + j], s.R[c * RS + j], o);
             } else if (VAR == kF3) {
                 o = expf(s.L[i]) * s.QS[idx];
                 for (int l = 0; l <= i; ++l) {
                     const float f = s.P[i * C + l];
                     float acc = 0.f;
-                    for (int b = 0; b < W; ++b) acc = fmaf(s.Sc[i * NE + (l - b + W - 1)], s.R[(l * W + b) * DVS + c], acc);
+                    for (int b = 0; b < W; ++b) acc = fmaf(s.Sc[i * NE + (l - b + W - 1)], s.R[c * RS + l * W + b], acc);
                     o = fmaf(f, acc, o);
                 }
-            } else {
-                const float* Rm = (VAR == kF1A) ? s.Y : s.R;
+            } else if (VAR == kF1A) {
                 o = expf(s.L[i]) * s.QS[idx];
-                for (int j = 0; j <= i; ++j) o = fmaf(s.P[i * C + j], Rm[j * DVS + c], o);
+                for (int j = 0; j <= i; ++j) o = fmaf(s.P[i * C + j], s.Y[j * DVS + c], o);
+            } else {
+                o = expf(s.L[i]) * s.QS[idx];
+                for (int j = 0; j <= i; ++j) o = fmaf(s.P[i * C + j], s.R[c * RS + j], o);
             }
             stf(out + (t0 + i) * DV + c0 + c, o);
         }
@@ -382,16 +388,18 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             if (VAR == kF3) {
                 for (int l = 0; l < n; ++l) {
                     float inner = 0.f;
-                    for (int b = 0; b < W; ++b) inner = fmaf(s.X[(l - b + W - 1) * DK + r], s.R[(l * W + b) * DVS + c], inner);
+                    for (int b = 0; b < W; ++b) inner = fmaf(s.X[(l - b + W - 1) * XS + r], s.R[c * RS + l * W + b], inner);
                     acc = fmaf(s.w[l], inner, acc);
                 }
                 s.S[idx] = fmaf(expf(s.L[C - 1]), s.S[idx], acc);
             } else if (VAR == kF2) {
-                for (int j = 0; j < n; ++j) acc = fmaf(s.X[j * DK + r] * s.w[j * DVS + c], s.R[j * DVS + c], acc);
-                s.S[idx] = fmaf(expf(s.L[(C - 1) * DVS + c]), s.S[idx], acc);
+                for (int j = 0; j < n; ++j) acc = fmaf(s.X[j * XS + r] * s.w[c * CS + j], s.R[c * RS + j], acc);
+                s.S[idx] = fmaf(expf(s.L[c * CS + C - 1]), s.S[idx], acc);
+            } else if (VAR == kF1A) {
+                for (int j = 0; j < n; ++j) acc = fmaf(s.X[j * XS + r] * s.w[j], s.Y[j * DVS + c], acc);
+                s.S[idx] = fmaf(expf(s.L[C - 1]), s.S[idx], acc);
             } else {
-                const float* Rm = (VAR == kF1A) ? s.Y : s.R;
-                for (int j = 0; j < n; ++j) acc = fmaf(s.X[j * DK + r] * s.w[j], Rm[j * DVS + c], acc);
+                for (int j = 0; j < n; ++j) acc = fmaf(s.X[j * XS + r] * s.w[j], s.R[c * RS + j], acc);
                 s.S[idx] = fmaf(expf(s.L[C - 1]), s.S[idx], acc);
             }
         }
