@@ -161,36 +161,32 @@ __device__ __forceinline__ void chunk_scalars(Scal* s, const uint8_t* Xs, int ti
 }
 
 // ---------------------------------------------------------------- T = (I + A)^{-1}
-// m16n8k16 fragments of fp32 shared-memory matrices (row stride kS), split into bf16 hi / lo.
-__device__ __forceinline__ void afrag16(const float* M, int r0, int c0, int g, int t, uint32_t (&h)[4],
-                                        uint32_t (&l)[4]) {
-    const float2 v0 = *reinterpret_cast<const float2*>(M + (r0 + g) * kS + c0 + 2 * t);
-    const float2 v1 = *reinterpret_cast<const float2*>(M + (r0 + g + 8) * kS + c0 + 2 * t);
-    const float2 v2 = *reinterpret_cast<const float2*>(M + (r0 + g) * kS + c0 + 2 * t + 8);
-    const float2 v3 = *reinterpret_cast<const float2*>(M + (r0 + g + 8) * kS + c0 + 2 * t + 8);
-    split2(v0.x, v0.y, h[0], l[0]);
-    split2(v1.x, v1.y, h[1], l[1]);
-    split2(v2.x, v2.y, h[2], l[2]);
-    split2(v3.x, v3.y, h[3], l[3]);
-}
-__device__ __forceinline__ void bfrag16(const float* M, int k0, int n0, int g, int t, uint32_t& h0, uint32_t& h1,
-                                        uint32_t& l0, uint32_t& l1) {
-    split2(M[(k0 + 2 * t) * kS + n0 + g], M[(k0 + 2 * t + 1) * kS + n0 + g], h0, l0);
-    split2(M[(k0 + 2 * t + 8) * kS + n0 + g], M[(k0 + 2 * t + 9) * kS + n0 + g], h1, l1);
-}
-// The accumulators of two adjacent n-tiles form the A fragment of the next product.
-__device__ __forceinline__ void cfrag_to_a(const float (&c0)[4], const float (&c1)[4], uint32_t (&h)[4],
-                                           uint32_t (&l)[4]) {
-    split2(c0[0], c0[1], h[0], l[0]);
-    split2(c0[2], c0[3], h[1], l[1]);
-    split2(c1[0], c1[1], h[2], l[2]);
-    split2(c1[2], c1[3], h[3], l[3]);
-}
-
 // In place: on entry M holds A, strictly lower 64 x 64 (fp32, stride kS), with zeros in the 16 x 16
 // blocks above the diagonal; on exit M holds T = (I + A)^{-1}. 16 x 16 diagonal blocks by column
-// substitution (in registers), then two levels of block merges T_ba = -(T_bb A_ba) T_aa as warp-level
-// bf16x3 products; each merge reads the A block it replaces before writing it. Ends with a CTA barrier.
+// substitution in fp32 (in registers), then two levels of block merges T_ba = -(T_bb A_ba) T_aa as
+// warp-level tf32 products (operands rounded to nearest tf32, fp32 accumulation); each merge reads
+// the A block it replaces before writing it. Ends with a CTA barrier.
+//
+// tf32 m16n8k8 fragments: A a0 = (g, t), a1 = (g + 8, t), a2 = (g, t + 4), a3 = (g + 8, t + 4);
+// B b0 = (t, g), b1 = (t + 4, g); C c0, c1 = (g, 2t), (g, 2t + 1); c2, c3 = rows g + 8. A product
+// whose A operand is a previous accumulator takes it with the k-slots t / t + 4 standing for
+// columns 2t / 2t + 1, so its B rows are read in the same order (2t, 2t + 1).
+__device__ __forceinline__ void mma_tf_a(float (&d)[4], const float* M, int r0, int k0, int k0b, int n0, int g, int t,
+                                         bool permuted_b) {
+    // d += M[r0.., k0..k0+7] (A, 16 x 8) x M[k0b.., n0..n0+7] (B, 8 x 8)
+    const uint32_t a0 = tf32_rn(M[(r0 + g) * kS + k0 + t]), a1 = tf32_rn(M[(r0 + g + 8) * kS + k0 + t]);
+    const uint32_t a2 = tf32_rn(M[(r0 + g) * kS + k0 + t + 4]), a3 = tf32_rn(M[(r0 + g + 8) * kS + k0 + t + 4]);
+    const int kb0 = permuted_b ? 2 * t : t, kb1 = permuted_b ? 2 * t + 1 : t + 4;
+    const uint32_t b0 = tf32_rn(M[(k0b + kb0) * kS + n0 + g]), b1 = tf32_rn(M[(k0b + kb1) * kS + n0 + g]);
+    mma1688_tf32(d, a0, a1, a2, a3, b0, b1);
+}
+__device__ __forceinline__ void mma_tf_c(float (&d)[4], const float (&c)[4], const float* M, int k0b, int n0, int g,
+                                         int t) {
+    // d += C (accumulator fragment of a 16 x 8 tile, as the A operand of a k8 step) x M[k0b.., n0..]
+    const uint32_t b0 = tf32_rn(M[(k0b + 2 * t) * kS + n0 + g]), b1 = tf32_rn(M[(k0b + 2 * t + 1) * kS + n0 + g]);
+    mma1688_tf32(d, tf32_rn(c[0]), tf32_rn(c[2]), tf32_rn(c[1]), tf32_rn(c[3]), b0, b1);
+}
+
 __device__ void invert_unit_lower(float* M, int tid) {
     const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     float x[16];
@@ -199,14 +195,18 @@ __device__ void invert_unit_lower(float* M, int tid) {
         const float* Ab = M + 16 * b * kS + 16 * b;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            float a0 = 0.f, a1 = 0.f;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int j = 0; j + 1 < r; j += 2) {
-                a0 = fmaf(Ab[r * kS + j], x[j], a0);
-                a1 = fmaf(Ab[r * kS + j + 1], x[j + 1], a1);
+            for (int j = 0; j + 3 < r; j += 4) {
+                const float4 av = *reinterpret_cast<const float4*>(Ab + r * kS + j);
+                a0 = fmaf(av.x, x[j], a0);
+                a1 = fmaf(av.y, x[j + 1], a1);
+                a2 = fmaf(av.z, x[j + 2], a2);
+                a3 = fmaf(av.w, x[j + 3], a3);
             }
-            if (r & 1) a0 = fmaf(Ab[r * kS + r - 1], x[r - 1], a0);
-            x[r] = r < c ? 0.f : (r == c ? 1.f : -(a0 + a1));
+#pragma unroll
+            for (int j = r & ~3; j < r; ++j) a0 = fmaf(Ab[r * kS + j], x[j], a0);
+            x[r] = r < c ? 0.f : (r == c ? 1.f : -((a0 + a1) + (a2 + a3)));
         }
     }
     __syncthreads();
@@ -216,25 +216,18 @@ __device__ void invert_unit_lower(float* M, int tid) {
         for (int r = 0; r < 16; ++r) M[(16 * b + r) * kS + 16 * b + c] = x[r];
     }
     __syncthreads();
-    if (warp < 2) {  // T_{b+1,b} for b = 0 (warp 0) and b = 2 (warp 1)
+    if (warp < 2) {  // T_{b+1,b} = -(T_{b+1,b+1} A_{b+1,b}) T_bb for b = 0 (warp 0) and b = 2 (warp 1)
         const int b = 2 * warp, R1 = 16 * (b + 1), C0 = 16 * b;
-        uint32_t ah[4], al[4];
-        afrag16(M, R1, R1, g, t, ah, al);
         float d1[2][4] = {};
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            uint32_t bh0, bh1, bl0, bl1;
-            bfrag16(M, R1, C0 + 8 * nt, g, t, bh0, bh1, bl0, bl1);
-            mma16816_x3(d1[nt], ah, al, bh0, bh1, bl0, bl1);
-        }
-        cfrag_to_a(d1[0], d1[1], ah, al);
+        for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) mma_tf_a(d1[nt], M, R1, R1 + 8 * ks, R1 + 8 * ks, C0 + 8 * nt, g, t, false);
         float d2[2][4] = {};
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            uint32_t bh0, bh1, bl0, bl1;
-            bfrag16(M, C0, C0 + 8 * nt, g, t, bh0, bh1, bl0, bl1);
-            mma16816_x3(d2[nt], ah, al, bh0, bh1, bl0, bl1);
-        }
+        for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) mma_tf_c(d2[nt], d1[ks], M, C0 + 8 * ks, C0 + 8 * nt, g, t);
         __syncwarp();
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -247,29 +240,15 @@ __device__ void invert_unit_lower(float* M, int tid) {
         const int RB = 32 + 16 * (warp >> 1), CB = 16 * (warp & 1);
         float d1[4][4] = {};
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            uint32_t ah[4], al[4];
-            afrag16(M, RB, 32 + 16 * ks, g, t, ah, al);
+        for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                uint32_t bh0, bh1, bl0, bl1;
-                bfrag16(M, 32 + 16 * ks, 8 * nt, g, t, bh0, bh1, bl0, bl1);
-                mma16816_x3(d1[nt], ah, al, bh0, bh1, bl0, bl1);
-            }
-        }
+            for (int nt = 0; nt < 4; ++nt) mma_tf_a(d1[nt], M, RB, 32 + 8 * ks, 32 + 8 * ks, 8 * nt, g, t, false);
         asm volatile("bar.sync 1, 128;" ::: "memory");  // every warp has read A[32:64, 0:32]
         float d2[2][4] = {};
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            uint32_t ah[4], al[4];
-            cfrag_to_a(d1[2 * ks], d1[2 * ks + 1], ah, al);
+        for (int ks = 0; ks < 4; ++ks)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                uint32_t bh0, bh1, bl0, bl1;
-                bfrag16(M, 16 * ks, CB + 8 * nt, g, t, bh0, bh1, bl0, bl1);
-                mma16816_x3(d2[nt], ah, al, bh0, bh1, bl0, bl1);
-            }
-        }
+            for (int nt = 0; nt < 2; ++nt) mma_tf_c(d2[nt], d1[ks], M, 8 * ks, CB + 8 * nt, g, t);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             *reinterpret_cast<float2*>(M + (RB + g) * kS + CB + 8 * nt + 2 * t) = make_float2(-d2[nt][0], -d2[nt][1]);
@@ -509,45 +488,46 @@ __global__ void __launch_bounds__(256, 4) falcon_prep_kernel(const __grid_consta
 }
 
 // ---------------------------------------------------------------- chain kernel: S_{n+1} = M_n S_n + U_n
-// One CTA per (sequence, 32-column half of S). Per step one thread issues eight tcgen05 MMAs,
-// D = (M_hi + M_lo) [S_hi | S_lo], whose B operand is a single 64 x 64 tile holding this half's
-// state split into hi (columns 0-31) and lo (columns 32-63) bf16 parts; then every thread reads
-// its fragment of D (16x256b TMEM loads), forms S_{n+1} = D[:, 0:32] + D[:, 32:64] + U_n in fp32,
-// and writes the next B tile (double-buffered) and the chunk-start state for the output kernel.
+// One CTA (8 warps) per sequence, one per SM. Per step one thread issues eight tcgen05 MMAs,
+// D = (M_hi + M_lo) [S_hi | S_lo] (M = 64, N = 128): the B operand is the state split into bf16
+// hi and lo tiles, the two 64-column atoms of one MN-major operand. Every warp then reads its
+// fragment of D (16x256b TMEM loads: quadrant w % 4, state columns 32 (w / 4) ..), forms
+// S_{n+1} = D[:, c] + D[:, 64 + c] + U_n in fp32 and writes the next (double-buffered) B tiles,
+// which thread 0 also stores to the workspace, as the output kernel's chunk-start state, with TMA.
 namespace chain {
-constexpr int kCols = 32;                   // state columns per CTA
 constexpr int kStages = 3;
-constexpr int kUBytes = 64 * kCols * 4;     // U_n columns of this CTA, fp32 [64][kCols]
+constexpr int kUBytes = 64 * 64 * 4;        // U_n, fp32, as two [64][32] halves (32-column TMA boxes)
+constexpr int kUBytesHalf = kUBytes / 2;
 constexpr int kStage = 2 * kTile + kUBytes; // M hi, M lo, U
-constexpr int BT = kStages * kStage;        // two B tiles
-constexpr int BAR = BT + 2 * kTile;         // full[kStages], mma
+constexpr int BT = kStages * kStage;        // 2 buffers x {S hi, S lo}
+constexpr int BAR = BT + 4 * kTile;         // full[kStages], mma
 constexpr int BYTES = BAR + 8 * (kStages + 1) + 16;
 constexpr int ALLOC = BYTES + 1024;
-constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kTmemCols = 128;
 static_assert(kStage % 1024 == 0 && BT % 1024 == 0, "stage alignment");
 }  // namespace chain
 
-__global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant__ SplitParams p) {
+__global__ void __launch_bounds__(256, 1) falcon_chain_kernel(const __grid_constant__ SplitParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, t = lane & 3;
-    const int cb = blockIdx.x;
-    const long long bh = blockIdx.y;
-    const int c0 = chain::kCols * cb;  // this CTA's first state column
+    const long long bh = blockIdx.x;
     const int N = p.N;
+    const int q4 = warp & 3, c0 = 32 * (warp >> 2);  // TMEM quadrant; first of this warp's 32 state columns
     auto full = [&](int s) -> uint32_t { return base + chain::BAR + 8 * s; };
     const uint32_t bar_mma = base + chain::BAR + 8 * chain::kStages;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chain::BAR + 8 * (chain::kStages + 1));
-    auto load = [&](int m) {  // thread 0: M_m (hi, lo) and this CTA's columns of U_m into stage m % kStages
+    auto load = [&](int m) {  // thread 0: M_m (hi, lo) and U_m into stage m % kStages
         const int s = m % chain::kStages;
         const uint32_t st = base + s * chain::kStage;
         const int row = (int)((bh * N + m) * 128);
         mbar_expect_tx(full(s), chain::kStage);
         tma_load_2d(st, &p.tm_m, 0, row, full(s));
         tma_load_2d(st + kTile, &p.tm_m, 0, row + 64, full(s));
-        tma_load_2d(st + 2 * kTile, &p.tm_u, c0, (int)((bh * N + m) * 64), full(s));
+        tma_load_2d(st + 2 * kTile, &p.tm_u, 0, (int)((bh * N + m) * 64), full(s));
+        tma_load_2d(st + 2 * kTile + chain::kUBytesHalf, &p.tm_u, 32, (int)((bh * N + m) * 64), full(s));
     };
     int issued = 0;
     if (tid == 0) {
@@ -560,16 +540,15 @@ __global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant
     if (tid == 0)
         for (; issued < chain::kStages && issued < N; ++issued) load(issued);
     pdl_launch_dependents();  // the output kernel may start its state-independent part
-    if (cb == 0)  // the sequence's later M_n and U_n into L2, once per sequence
-        for (int i = tid + chain::kStages; i < N; i += 128) {
-            const long long m = bh * N + i;
-            prefetch_l2(p.ws_m + m * 2 * 4096, 2 * 4096 * 2);
-            prefetch_l2(p.ws_u + m * 4096, 4096 * 4);
-        }
+    for (int i = tid + chain::kStages; i < N; i += 256) {  // the sequence's later M_n and U_n into L2
+        const long long m = bh * N + i;
+        prefetch_l2(p.ws_m + m * 2 * 4096, 2 * 4096 * 2);
+        prefetch_l2(p.ws_u + m * 4096, 4096 * 4);
+    }
 
-    // This thread's fragment (the 16x256b TMEM layout of rows 16 w + lane/4 and +8): rows r0, r0 + 8,
-    // columns 8j + 2t, 8j + 2t + 1 (j = 0..3) of the CTA's 32 columns; sv[j][0..1] row r0, [2..3] row r0 + 8.
-    const int r0 = 16 * warp + (lane >> 2);
+    // This thread's fragment (16x256b layout of quadrant q4): rows r0 and r0 + 8, columns
+    // c0 + 8j + 2t (+1), j = 0..3; sv[j][0..1] row r0, sv[j][2..3] row r0 + 8.
+    const int r0 = 16 * q4 + (lane >> 2);
     float sv[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -580,40 +559,33 @@ __global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant
         }
         sv[j][0] = a.x, sv[j][1] = a.y, sv[j][2] = b.x, sv[j][3] = b.y;
     }
-    // S (fragment) -> hi / lo into B tile `buf`
-    auto put_state = [&](int buf) {
-        uint8_t* bt = sm + chain::BT + buf * kTile;
+    auto put_state = [&](int buf) {  // fragment -> hi / lo B tiles of buffer buf
+        uint8_t* bt = sm + chain::BT + 2 * buf * kTile;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                const int row = r0 + 8 * hf, col = 8 * j + 2 * t;
+                const int row = r0 + 8 * hf, col = c0 + 8 * j + 2 * t;
                 uint32_t h, l;
                 split2(sv[j][2 * hf], sv[j][2 * hf + 1], h, l);
                 *reinterpret_cast<uint32_t*>(bt + sw128(row, col)) = h;
-                *reinterpret_cast<uint32_t*>(bt + sw128(row, col + 32)) = l;
+                *reinterpret_cast<uint32_t*>(bt + kTile + sw128(row, col)) = l;
             }
     };
-    // B tile `buf` (complete) -> S_m hi / lo in the workspace, 16-byte chunks, by warps 1-3 while
-    // thread 0 issues the next MMAs
-    auto copy_state = [&](int buf, int m) {
-        if (warp == 0) return;
-        const uint8_t* bt = sm + chain::BT + buf * kTile;
-        bf16* dh = p.ws_s + ((bh * N + m) * 2 * 64) * 64 + c0;
-        for (int task = tid - 32; task < 512; task += 96) {  // logical chunk c: hi 0-3, lo 4-7
-            const int row = task >> 3, c = task & 7;
-            const uint4 v = *reinterpret_cast<const uint4*>(bt + row * 128 + ((c ^ (row & 7)) << 4));
-            *reinterpret_cast<uint4*>(dh + ((c >> 2) * 64 + row) * 64 + 8 * (c & 3)) = v;
-        }
+    auto store_state = [&](int buf, int m) {  // thread 0: B tiles of buffer buf -> S_m in the workspace
+        const uint32_t bt = base + chain::BT + 2 * buf * kTile;
+        tma_store_2d(&p.tm_s, bt, 0, (int)((bh * N + m) * 128));
+        tma_store_2d(&p.tm_s, bt + kTile, 0, (int)((bh * N + m) * 128 + 64));
+        bulk_commit();
     };
     put_state(0);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (N > 0) copy_state(0, 0);
+    if (tid == 0 && N > 0) store_state(0, 0);
     const uint32_t tmem = *tslot;
-    const uint32_t tq = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);
 
     bool ok = true;
     for (int n = 0; n < N; ++n) {
@@ -625,8 +597,8 @@ __global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant
                 bad = 1;
             } else {
                 tc_fence_after();
-                constexpr uint32_t id = idesc_bf16(64, 64, false, true);
-                const uint32_t bt = base + chain::BT + buf * kTile;
+                constexpr uint32_t id = idesc_bf16(64, 128, false, true);
+                const uint32_t bt = base + chain::BT + 2 * buf * kTile;
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
@@ -639,6 +611,7 @@ __global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant
                     load(issued);
                     ++issued;
                 }
+                bulk_wait_read_1();  // the store of buffer buf ^ 1 (two steps ago) has read its tiles
                 if (!wait_or_flag(bar_mma, n & 1)) bad = 1;
             }
         }
@@ -647,24 +620,30 @@ __global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant
             break;
         }
         tc_fence_after();
-        uint32_t d[32];
-        tmem_ld_16x256b_x8(tq, d);
+        uint32_t d0[16], d1[16];
+        tmem_ld_16x256b_x4(tq + c0, d0);        // M S_hi part, columns c0 ..
+        tmem_ld_16x256b_x4(tq + 64 + c0, d1);   // M S_lo part
+        tmem_wait_ld();
+        regs_ready(d0);
+        regs_ready(d1);
         const float* un = reinterpret_cast<const float*>(sm + s * chain::kStage + 2 * kTile);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float2 ua = *reinterpret_cast<const float2*>(un + r0 * chain::kCols + 8 * j + 2 * t);
-            const float2 ub = *reinterpret_cast<const float2*>(un + (r0 + 8) * chain::kCols + 8 * j + 2 * t);
-            sv[j][0] = __uint_as_float(d[4 * j]) + __uint_as_float(d[4 * j + 16]) + ua.x;
-            sv[j][1] = __uint_as_float(d[4 * j + 1]) + __uint_as_float(d[4 * j + 17]) + ua.y;
-            sv[j][2] = __uint_as_float(d[4 * j + 2]) + __uint_as_float(d[4 * j + 18]) + ub.x;
-            sv[j][3] = __uint_as_float(d[4 * j + 3]) + __uint_as_float(d[4 * j + 19]) + ub.y;
+            const int col = c0 + 8 * j + 2 * t, h = col >> 5, cc = col & 31;  // U halves: [64][32] each
+            const float2 ua = *reinterpret_cast<const float2*>(un + h * 2048 + r0 * 32 + cc);
+            const float2 ub = *reinterpret_cast<const float2*>(un + h * 2048 + (r0 + 8) * 32 + cc);
+            sv[j][0] = __uint_as_float(d0[4 * j]) + __uint_as_float(d1[4 * j]) + ua.x;
+            sv[j][1] = __uint_as_float(d0[4 * j + 1]) + __uint_as_float(d1[4 * j + 1]) + ua.y;
+            sv[j][2] = __uint_as_float(d0[4 * j + 2]) + __uint_as_float(d1[4 * j + 2]) + ub.x;
+            sv[j][3] = __uint_as_float(d0[4 * j + 3]) + __uint_as_float(d1[4 * j + 3]) + ub.y;
         }
         put_state(buf ^ 1);
         fence_async_smem();
         tc_fence_before();
-        __syncthreads();  // next B tile written; stage s consumed by the MMA and the reads of U
-        if (n + 1 < N) copy_state(buf ^ 1, n + 1);
+        __syncthreads();  // next B tiles written; stage s consumed by the MMA and the reads of U
+        if (tid == 0 && n + 1 < N) store_state(buf ^ 1, n + 1);
     }
+    if (tid == 0) bulk_wait_all();
     if (!ok) {  // drain the loads still in flight (bounded), free TMEM, leave
         if (tid == 0)
             for (int m = 0; m < issued; ++m)
@@ -681,7 +660,7 @@ __global__ void __launch_bounds__(128) falcon_chain_kernel(const __grid_constant
                 make_float2(sv[j][2], sv[j][3]);
         }
     }
-    if (p.tail_out && cb == 0 && tid < 8) {  // window 1: the tail is the last key (the next call's x)
+    if (p.tail_out && tid < 8) {  // window 1: the tail is the last key (the next call's x)
         uint4 v = make_uint4(0, 0, 0, 0);
         if (p.T > 0) v = reinterpret_cast<const uint4*>(p.k + (bh * p.T + p.T - 1) * 64)[tid];
         else if (p.pos > 0) v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[tid];
@@ -948,13 +927,13 @@ bool encode_rows(CUtensorMap* tm, const void* ptr, long long rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// U: [rows][64] fp32, boxes of chain::kCols columns x 64 rows (one chain CTA's columns), no swizzle
+// U: [rows][64] fp32, boxes of 32 columns x 64 rows, no swizzle
 bool encode_u(CUtensorMap* tm, const void* ptr, long long rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {64, (cuuint64_t)rows};
     cuuint64_t strides[1] = {64 * 4};
-    cuuint32_t box[2] = {chain::kCols, 64};
+    cuuint32_t box[2] = {32, 64};
     cuuint32_t es[2] = {1, 1};
     return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1039,8 +1018,8 @@ int launch_split(const Launch& a, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    cfg.gridDim = dim3(64 / chain::kCols, (unsigned)BH);
-    cfg.blockDim = dim3(128);
+    cfg.gridDim = dim3((unsigned)BH);
+    cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = chain::ALLOC;
     if (cudaLaunchKernelEx(&cfg, falcon_chain_kernel, p) != cudaSuccess) return 4;
     if (N > 0) {
