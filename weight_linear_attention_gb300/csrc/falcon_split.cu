@@ -14,7 +14,7 @@
 //   M  = e^{L_C} I - X^T diag(w) T diag(e^{Lx}) X,   U = X^T diag(w) T Y.
 // M and U do not depend on S, so the work splits into three launches:
 //   falcon_prep_kernel   one CTA per chunk, every chunk of every sequence at once: M_n, U_n
-//   falcon_chain_kernel  one CTA per (sequence, 16 state columns): S_{n+1} = M_n S_n + U_n
+//   falcon_chain_kernel  one CTA per sequence: S_{n+1} = M_n S_n + U_n, two 32-column halves pipelined
 //   falcon_out_kernel    one CTA per chunk, every chunk at once: R and O from S_n
 // Falcon-1A writes the target itself (no residual): T = I, M = e^{L_C} I, U = X^T diag(w) Y.
 //
@@ -488,26 +488,33 @@ __global__ void __launch_bounds__(256, 4) falcon_prep_kernel(const __grid_consta
 }
 
 // ---------------------------------------------------------------- chain kernel: S_{n+1} = M_n S_n + U_n
-// One CTA (8 warps) per sequence, one per SM. Per step one thread issues eight tcgen05 MMAs,
-// D = (M_hi + M_lo) [S_hi | S_lo] (M = 64, N = 128): the B operand is the state split into bf16
-// hi and lo tiles, the two 64-column atoms of one MN-major operand. Every warp then reads its
-// fragment of D (16x256b TMEM loads: quadrant w % 4, state columns 32 (w / 4) ..), forms
-// S_{n+1} = D[:, c] + D[:, 64 + c] + U_n in fp32 and writes the next (double-buffered) B tiles,
-// which thread 0 also stores to the workspace, as the output kernel's chunk-start state, with TMA.
+// One CTA per sequence (one per SM). The state's columns split into two 32-column halves that
+// evolve independently (S_{n+1}[:, c] depends only on S_n[:, c]); each half is its own pipeline:
+//   warp 8 (issuer)    TMA loads of M_n (hi, lo) and U_n through a 3-stage ring; per half and step
+//                      eight tcgen05 MMAs D_h = (M_hi + M_lo) B_h, where the B tile of half h is
+//                      [S_hi | S_lo] of its 32 columns (one 64-column MN-major atom)
+//   warps 4h..4h+3     the epilogue of half h: 16x256b TMEM loads of D_h, S_{n+1} = D_h[:, c] +
+//                      D_h[:, 32 + c] + U_n in fp32, written as the next (double-buffered) B tile
+//   warp 9 (copier)    each finished B tile to the workspace, as the output kernel's S_n
+// so that one half's epilogue runs while the other half's MMAs do. The barriers that hand a B
+// tile over are kept per buffer, so no waiter can fall two phases behind its barrier. All waits
+// are bounded; a timeout raises the device flag and every role leaves its loop.
 namespace chain {
 constexpr int kStages = 3;
-constexpr int kUBytes = 64 * 64 * 4;        // U_n, fp32, as two [64][32] halves (32-column TMA boxes)
+constexpr int kUBytes = 64 * 64 * 4;        // U_n, fp32, as two [64][32] halves (128-byte swizzle)
 constexpr int kUBytesHalf = kUBytes / 2;
 constexpr int kStage = 2 * kTile + kUBytes; // M hi, M lo, U
-constexpr int BT = kStages * kStage;        // 2 buffers x {S hi, S lo}
-constexpr int BAR = BT + 4 * kTile;         // full[kStages], mma
-constexpr int BYTES = BAR + 8 * (kStages + 1) + 16;
+constexpr int BT = kStages * kStage;        // B tiles [half][buffer]
+constexpr int BAR = BT + 4 * kTile;
+constexpr int kBars = kStages + 2 + 4 + 4 + 1;  // full, mma done[h], state ready[h][b], copied[h][b], drain
+constexpr int BYTES = BAR + 8 * kBars + 16;
 constexpr int ALLOC = BYTES + 1024;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 128;
 static_assert(kStage % 1024 == 0 && BT % 1024 == 0, "stage alignment");
 }  // namespace chain
 
-__global__ void __launch_bounds__(256, 1) falcon_chain_kernel(const __grid_constant__ SplitParams p) {
+__global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const __grid_constant__ SplitParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -515,11 +522,23 @@ __global__ void __launch_bounds__(256, 1) falcon_chain_kernel(const __grid_const
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, t = lane & 3;
     const long long bh = blockIdx.x;
     const int N = p.N;
-    const int q4 = warp & 3, c0 = 32 * (warp >> 2);  // TMEM quadrant; first of this warp's 32 state columns
-    auto full = [&](int s) -> uint32_t { return base + chain::BAR + 8 * s; };
-    const uint32_t bar_mma = base + chain::BAR + 8 * chain::kStages;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chain::BAR + 8 * (chain::kStages + 1));
-    auto load = [&](int m) {  // thread 0: M_m (hi, lo) and U_m into stage m % kStages
+    auto bar = [&](int i) -> uint32_t { return base + chain::BAR + 8 * i; };
+    auto full = [&](int s) { return bar(s); };
+    auto mmad = [&](int h) { return bar(chain::kStages + h); };
+    auto ready = [&](int h, int b) { return bar(chain::kStages + 2 + 2 * h + b); };   // phase k: S_{b+2k} in tile (h, b)
+    auto copied = [&](int h, int b) { return bar(chain::kStages + 6 + 2 * h + b); };  // phase k: S_{b+2k} stored
+    const uint32_t drain = bar(chain::kStages + 10);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + chain::BAR + 8 * chain::kBars);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chain::BAR + 8 * chain::kBars + 4);
+    auto btile = [&](int h, int b) { return chain::BT + (2 * h + b) * kTile; };
+    auto wait = [&](uint32_t br, uint32_t parity) -> bool {  // bounded; on timeout every role stops
+        if (*abort_flag) return false;
+        if (mbar_wait_bounded(br, parity, kTimeoutCycles)) return true;
+        *abort_flag = 1;
+        atomicExch(&g_split_timeout_flag, 1);
+        return false;
+    };
+    auto load = [&](int m) {  // M_m (hi, lo) and U_m into stage m % kStages
         const int s = m % chain::kStages;
         const uint32_t st = base + s * chain::kStage;
         const int row = (int)((bh * N + m) * 128);
@@ -529,142 +548,189 @@ __global__ void __launch_bounds__(256, 1) falcon_chain_kernel(const __grid_const
         tma_load_2d(st + 2 * kTile, &p.tm_u, 0, (int)((bh * N + m) * 64), full(s));
         tma_load_2d(st + 2 * kTile + chain::kUBytesHalf, &p.tm_u, 32, (int)((bh * N + m) * 64), full(s));
     };
-    int issued = 0;
     if (tid == 0) {
         for (int s = 0; s < chain::kStages; ++s) mbar_init(full(s), 1);
-        mbar_init(bar_mma, 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(mmad(h), 1);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(ready(h, b), 128);
+                mbar_init(copied(h, b), 32);
+            }
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
         mbar_init_fence();
     }
     if (warp == 0) tmem_alloc(smem_u32(tslot), chain::kTmemCols);
     pdl_wait();  // the prep kernel's M_n, U_n are complete and visible from here on
-    if (tid == 0)
-        for (; issued < chain::kStages && issued < N; ++issued) load(issued);
-    pdl_launch_dependents();  // the output kernel may start its state-independent part
-    for (int i = tid + chain::kStages; i < N; i += 256) {  // the sequence's later M_n and U_n into L2
-        const long long m = bh * N + i;
-        prefetch_l2(p.ws_m + m * 2 * 4096, 2 * 4096 * 2);
-        prefetch_l2(p.ws_u + m * 4096, 4096 * 4);
-    }
-
-    // This thread's fragment (16x256b layout of quadrant q4): rows r0 and r0 + 8, columns
-    // c0 + 8j + 2t (+1), j = 0..3; sv[j][0..1] row r0, sv[j][2..3] row r0 + 8.
-    const int r0 = 16 * q4 + (lane >> 2);
-    float sv[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
-        if (p.S0) {
-            a = *reinterpret_cast<const float2*>(p.S0 + (bh * 64 + r0) * 64 + c0 + 8 * j + 2 * t);
-            b = *reinterpret_cast<const float2*>(p.S0 + (bh * 64 + r0 + 8) * 64 + c0 + 8 * j + 2 * t);
-        }
-        sv[j][0] = a.x, sv[j][1] = a.y, sv[j][2] = b.x, sv[j][3] = b.y;
-    }
-    auto put_state = [&](int buf) {  // fragment -> hi / lo B tiles of buffer buf
-        uint8_t* bt = sm + chain::BT + 2 * buf * kTile;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int row = r0 + 8 * hf, col = c0 + 8 * j + 2 * t;
-                uint32_t h, l;
-                split2(sv[j][2 * hf], sv[j][2 * hf + 1], h, l);
-                *reinterpret_cast<uint32_t*>(bt + sw128(row, col)) = h;
-                *reinterpret_cast<uint32_t*>(bt + kTile + sw128(row, col)) = l;
-            }
-    };
-    auto store_state = [&](int buf, int m) {  // thread 0: B tiles of buffer buf -> S_m in the workspace
-        const uint32_t bt = base + chain::BT + 2 * buf * kTile;
-        tma_store_2d(&p.tm_s, bt, 0, (int)((bh * N + m) * 128));
-        tma_store_2d(&p.tm_s, bt + kTile, 0, (int)((bh * N + m) * 128 + 64));
-        bulk_commit();
-    };
-    put_state(0);
-    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0 && N > 0) store_state(0, 0);
+    pdl_launch_dependents();  // the output kernel may start its state-independent part
     const uint32_t tmem = *tslot;
-    const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);
-
     bool ok = true;
-    for (int n = 0; n < N; ++n) {
-        const int s = n % chain::kStages, buf = n & 1;
-        const uint32_t st = base + s * chain::kStage;
-        int bad = 0;
-        if (tid == 0) {
-            if (!wait_or_flag(full(s), (n / chain::kStages) & 1)) {
-                bad = 1;
-            } else {
-                tc_fence_after();
-                constexpr uint32_t id = idesc_bf16(64, 128, false, true);
-                const uint32_t bt = base + chain::BT + 2 * buf * kTile;
+
+    if (warp < 8) {
+        // ------------------------------------------------------------ epilogue of half h
+        const int h = warp >> 2, q4 = warp & 3;
+        const int r0 = 16 * q4 + (lane >> 2);  // rows r0 and r0 + 8 (TMEM quadrant q4)
+        const int c0 = 32 * h;                 // this half's first state column
+        const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16) + 64 * h;
+        float sv[4][4];  // columns c0 + 8j + 2t (+1), j = 0..3; [0..1] row r0, [2..3] row r0 + 8
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
+        for (int j = 0; j < 4; ++j) {
+            float2 x = make_float2(0.f, 0.f), y = make_float2(0.f, 0.f);
+            if (p.S0) {
+                x = *reinterpret_cast<const float2*>(p.S0 + (bh * 64 + r0) * 64 + c0 + 8 * j + 2 * t);
+                y = *reinterpret_cast<const float2*>(p.S0 + (bh * 64 + r0 + 8) * 64 + c0 + 8 * j + 2 * t);
+            }
+            sv[j][0] = x.x, sv[j][1] = x.y, sv[j][2] = y.x, sv[j][3] = y.y;
+        }
+        auto put_state = [&](int b) {  // fragment -> B tile (h, b): hi in columns 0-31, lo in 32-63
+            uint8_t* bt = sm + btile(h, b);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem, desc_k(st + part * kTile + 32 * ks), desc_mn(bt + 2048 * ks, kTile), id,
-                                 part + ks > 0);
-                mma_commit(bar_mma);
-                if (n > 0 && issued < N) {  // the previous step's stage is free: fetch M_{n+2}
-                    fence_async_smem();
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int row = r0 + 8 * hf, col = 8 * j + 2 * t;
+                    uint32_t hi, lo;
+                    split2(sv[j][2 * hf], sv[j][2 * hf + 1], hi, lo);
+                    *reinterpret_cast<uint32_t*>(bt + sw128(row, col)) = hi;
+                    *reinterpret_cast<uint32_t*>(bt + sw128(row, col + 32)) = lo;
+                }
+            fence_async_smem();
+        };
+        // U half tile: [64][32] fp32 rows of 128 bytes, 16-byte chunks swizzled by row % 8
+        auto u_at = [&](const uint8_t* uh, int row, int col) {
+            return *reinterpret_cast<const float2*>(uh + row * 128 + ((((col >> 2) ^ (row & 7))) << 4) + 4 * (col & 3));
+        };
+        put_state(0);
+        mbar_arrive(ready(h, 0));
+        for (int n = 0; n < N; ++n) {
+            const int s = n % chain::kStages;
+            if (!wait(full(s), (n / chain::kStages) & 1)) {  // U_n in stage s (read before the MMAs end)
+                ok = false;
+                break;
+            }
+            const uint8_t* uh = sm + s * chain::kStage + 2 * kTile + h * chain::kUBytesHalf;
+            float2 ua[4], ub[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                ua[j] = u_at(uh, r0, 8 * j + 2 * t);
+                ub[j] = u_at(uh, r0 + 8, 8 * j + 2 * t);
+            }
+            if (!wait(mmad(h), n & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t d0[16], d1[16];
+            tmem_ld_16x256b_x4(tq, d0);       // M S_hi part
+            tmem_ld_16x256b_x4(tq + 32, d1);  // M S_lo part
+            tmem_wait_ld();
+            regs_ready(d0);
+            regs_ready(d1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                sv[j][0] = __uint_as_float(d0[4 * j]) + __uint_as_float(d1[4 * j]) + ua[j].x;
+                sv[j][1] = __uint_as_float(d0[4 * j + 1]) + __uint_as_float(d1[4 * j + 1]) + ua[j].y;
+                sv[j][2] = __uint_as_float(d0[4 * j + 2]) + __uint_as_float(d1[4 * j + 2]) + ub[j].x;
+                sv[j][3] = __uint_as_float(d0[4 * j + 3]) + __uint_as_float(d1[4 * j + 3]) + ub[j].y;
+            }
+            const int b = (n + 1) & 1;  // the tile that held S_{n-1}: its copy must be done
+            if (n >= 1 && !wait(copied(h, b), ((n - 1) >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            put_state(b);
+            tc_fence_before();
+            mbar_arrive(ready(h, b));  // S_{n+1} written; D_h and U_n read
+        }
+        if (ok && p.S_final) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                *reinterpret_cast<float2*>(p.S_final + (bh * 64 + r0) * 64 + c0 + 8 * j + 2 * t) =
+                    make_float2(sv[j][0], sv[j][1]);
+                *reinterpret_cast<float2*>(p.S_final + (bh * 64 + r0 + 8) * 64 + c0 + 8 * j + 2 * t) =
+                    make_float2(sv[j][2], sv[j][3]);
+            }
+        }
+    } else if (warp == 8) {
+        // ------------------------------------------------------------ issuer
+        if (lane == 0) {
+            int issued = 0, consumed = 0, mma_issued = 0;
+            for (; issued < chain::kStages && issued < N; ++issued) load(issued);
+            for (int n = 0; n < N && ok; ++n) {
+                const int s = n % chain::kStages;
+                if (!wait(full(s), (n / chain::kStages) & 1)) {
+                    ok = false;
+                    break;
+                }
+                ++consumed;
+                const uint32_t st = base + s * chain::kStage;
+                for (int h = 0; h < 2; ++h) {
+                    if (!wait(ready(h, n & 1), (n >> 1) & 1)) {  // S_n in tile (h, n & 1); D_h read out
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    constexpr uint32_t id = idesc_bf16(64, 64, false, true);
+                    const uint32_t bt = base + btile(h, n & 1);
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma_bf16(tmem + 64 * h, desc_k(st + part * kTile + 32 * ks),
+                                     desc_mn(bt + 2048 * ks, kTile), id, part + ks > 0);
+                    mma_commit(mmad(h));
+                    mma_issued = 1;
+                }
+                // both halves have finished step n - 1, so its stage is free: fetch M_{n+2}, U_{n+2}
+                if (ok && n >= 1 && issued < N) {
                     load(issued);
                     ++issued;
                 }
-                bulk_wait_read_1();  // the store of buffer buf ^ 1 (two steps ago) has read its tiles
-                if (!wait_or_flag(bar_mma, n & 1)) bad = 1;
+            }
+            if (!ok) {  // let the MMAs and loads in flight finish (bounded) before TMEM is freed
+                if (mma_issued) {
+                    mma_commit(drain);
+                    mbar_wait_bounded(drain, 0, kTimeoutCycles);
+                }
+                for (int m = consumed; m < issued; ++m)
+                    mbar_wait_bounded(full(m % chain::kStages), (m / chain::kStages) & 1, kTimeoutCycles);
             }
         }
-        if (__syncthreads_or(bad)) {
-            ok = false;
-            break;
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ copier: B tiles -> S_m in the workspace
+        for (int i = lane + chain::kStages; i < N; i += 32) {  // the sequence's later M_n, U_n into L2
+            const long long m = bh * N + i;
+            prefetch_l2(p.ws_m + m * 2 * 4096, 2 * 4096 * 2);
+            prefetch_l2(p.ws_u + m * 4096, 4096 * 4);
         }
-        tc_fence_after();
-        uint32_t d0[16], d1[16];
-        tmem_ld_16x256b_x4(tq + c0, d0);        // M S_hi part, columns c0 ..
-        tmem_ld_16x256b_x4(tq + 64 + c0, d1);   // M S_lo part
-        tmem_wait_ld();
-        regs_ready(d0);
-        regs_ready(d1);
-        const float* un = reinterpret_cast<const float*>(sm + s * chain::kStage + 2 * kTile);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int col = c0 + 8 * j + 2 * t, h = col >> 5, cc = col & 31;  // U halves: [64][32] each
-            const float2 ua = *reinterpret_cast<const float2*>(un + h * 2048 + r0 * 32 + cc);
-            const float2 ub = *reinterpret_cast<const float2*>(un + h * 2048 + (r0 + 8) * 32 + cc);
-            sv[j][0] = __uint_as_float(d0[4 * j]) + __uint_as_float(d1[4 * j]) + ua.x;
-            sv[j][1] = __uint_as_float(d0[4 * j + 1]) + __uint_as_float(d1[4 * j + 1]) + ua.y;
-            sv[j][2] = __uint_as_float(d0[4 * j + 2]) + __uint_as_float(d1[4 * j + 2]) + ub.x;
-            sv[j][3] = __uint_as_float(d0[4 * j + 3]) + __uint_as_float(d1[4 * j + 3]) + ub.y;
+        for (int m = 0; m < N && ok; ++m) {
+            for (int h = 0; h < 2; ++h) {
+                if (!wait(ready(h, m & 1), (m >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* bt = sm + btile(h, m & 1);
+                bf16* dh = p.ws_s + ((bh * N + m) * 2 * 64) * 64 + 32 * h;
+#pragma unroll 4
+                for (int k = 0; k < 16; ++k) {
+                    const int task = lane + 32 * k, row = task >> 3, c = task & 7;  // chunk c: hi 0-3, lo 4-7
+                    const uint4 v = *reinterpret_cast<const uint4*>(bt + row * 128 + ((c ^ (row & 7)) << 4));
+                    *reinterpret_cast<uint4*>(dh + ((c >> 2) * 64 + row) * 64 + 8 * (c & 3)) = v;
+                }
+                mbar_arrive(copied(h, m & 1));
+            }
         }
-        put_state(buf ^ 1);
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();  // next B tiles written; stage s consumed by the MMA and the reads of U
-        if (tid == 0 && n + 1 < N) store_state(buf ^ 1, n + 1);
-    }
-    if (tid == 0) bulk_wait_all();
-    if (!ok) {  // drain the loads still in flight (bounded), free TMEM, leave
-        if (tid == 0)
-            for (int m = 0; m < issued; ++m)
-                mbar_wait_bounded(full(m % chain::kStages), (m / chain::kStages) & 1, kTimeoutCycles);
-        release_tmem(tmem, warp, chain::kTmemCols);
-        return;
-    }
-    if (p.S_final) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            *reinterpret_cast<float2*>(p.S_final + (bh * 64 + r0) * 64 + c0 + 8 * j + 2 * t) =
-                make_float2(sv[j][0], sv[j][1]);
-            *reinterpret_cast<float2*>(p.S_final + (bh * 64 + r0 + 8) * 64 + c0 + 8 * j + 2 * t) =
-                make_float2(sv[j][2], sv[j][3]);
+        if (ok && p.tail_out && lane < 8) {  // window 1: the tail is the last key (the next call's x)
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (p.T > 0) v = reinterpret_cast<const uint4*>(p.k + (bh * p.T + p.T - 1) * 64)[lane];
+            else if (p.pos > 0) v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[lane];
+            reinterpret_cast<uint4*>(p.tail_out + bh * 64)[lane] = v;
         }
-    }
-    if (p.tail_out && tid < 8) {  // window 1: the tail is the last key (the next call's x)
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (p.T > 0) v = reinterpret_cast<const uint4*>(p.k + (bh * p.T + p.T - 1) * 64)[tid];
-        else if (p.pos > 0) v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[tid];
-        reinterpret_cast<uint4*>(p.tail_out + bh * 64)[tid] = v;
     }
     release_tmem(tmem, warp, chain::kTmemCols);
 }
@@ -927,7 +993,7 @@ bool encode_rows(CUtensorMap* tm, const void* ptr, long long rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// U: [rows][64] fp32, boxes of 32 columns x 64 rows, no swizzle
+// U: [rows][64] fp32, boxes of 32 columns x 64 rows, 128-byte swizzle
 bool encode_u(CUtensorMap* tm, const void* ptr, long long rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -936,7 +1002,7 @@ bool encode_u(CUtensorMap* tm, const void* ptr, long long rows) {
     cuuint32_t box[2] = {32, 64};
     cuuint32_t es[2] = {1, 1};
     return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1019,7 +1085,7 @@ int launch_split(const Launch& a, cudaStream_t st) {
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3((unsigned)BH);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(chain::kThreads);
     cfg.dynamicSmemBytes = chain::ALLOC;
     if (cudaLaunchKernelEx(&cfg, falcon_chain_kernel, p) != cudaSuccess) return 4;
     if (N > 0) {
