@@ -65,6 +65,14 @@ struct SplitParams {
     bf16* ws_s;   // [BH][N][2][64][64]: S_n hi, lo (state at the start of chunk n)
     bf16* ws_t;   // [BH][N][2][64][64]: T_n hi, lo
     uint8_t* ws_sc;  // [BH][N] blocks of kScalBytes: the chunk's per-token scalars (a Scal)
+    // Flags between the three kernels, which run overlapped. The prep CTA of a chunk clears both of
+    // the chunk's flags before it lets the chain kernel launch (the kernels after it cannot start
+    // before every prep CTA has), and a producer sets a flag to `epoch` once the data it guards is
+    // complete.
+    unsigned long long* fl_prep;  // [BH][N]: the prep kernel has written the chunk's M, U, T and scalars
+    unsigned long long* fl_s;     // [BH][N]: the chain kernel has written S_n
+    unsigned long long epoch;
+    long long BH;
     long long T, pos;
     int N;
     float eps, eps_gamma;
@@ -76,15 +84,31 @@ __device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity) {
     atomicExch(&g_split_timeout_flag, 1);
     return false;
 }
-// CTA-wide wait by thread 0. False (for every thread) on timeout, after thread 0 has given the
-// barrier one more bounded wait so that nothing it tracks is still landing when the CTA exits.
-__device__ __forceinline__ bool cta_wait(uint32_t bar, uint32_t parity, int tid) {
-    int bad = 0;
+// CTA-wide wait by thread 0. False (for every thread) on timeout or when thread 0 passes
+// `bad` = 1, after thread 0 has given the barrier one more bounded wait so that nothing it tracks
+// is still landing when the CTA exits.
+__device__ __forceinline__ bool cta_wait(uint32_t bar, uint32_t parity, int tid, int bad = 0) {
     if (tid == 0 && !wait_or_flag(bar, parity)) {
         bad = 1;
         mbar_wait_bounded(bar, parity, kTimeoutCycles);
     }
     return !__syncthreads_or(bad);
+}
+// Thread 0 of a consumer CTA: wait (bounded) for a producer's flag; on timeout raise the device flag.
+__device__ __forceinline__ bool wait_producer(const unsigned long long* flag, unsigned long long epoch) {
+    if (wait_flag_bounded(flag, epoch, kTimeoutCycles)) {
+        fence_proxy_async_global();  // the TMA loads that follow see what the flag guards
+        return true;
+    }
+    atomicExch(&g_split_timeout_flag, 1);
+    return false;
+}
+// Every thread of a producer CTA calls this after its last global store of the chunk's data;
+// thread 0 then publishes `flag`. Contains a CTA barrier.
+__device__ __forceinline__ void publish(unsigned long long* flag, unsigned long long epoch, int tid) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) st_release_gpu(flag, epoch);
 }
 __device__ __forceinline__ void release_tmem(uint32_t tmem, int warp, uint32_t cols) {
     tc_fence_before();
@@ -302,9 +326,9 @@ __global__ void __launch_bounds__(256, 4) falcon_prep_kernel(const __grid_consta
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const long long cid = blockIdx.x;
-    const long long bh = cid / p.N;
-    const int n = (int)(cid - bh * p.N);
+    const int n = (int)(blockIdx.x / p.BH);  // chunk-major: every sequence's chunk n before chunk n + 1
+    const long long bh = blockIdx.x - (long long)n * p.BH;
+    const long long cid = bh * p.N + n;      // the chunk's workspace slot
     const long long t0 = (long long)n * kC;
     const int nv = (int)min((long long)kC, p.T - t0);
     const bool f1 = p.variant == kF1;
@@ -322,6 +346,11 @@ __global__ void __launch_bounds__(256, 4) falcon_prep_kernel(const __grid_consta
         tma_load_3d(base + prep::Y, &p.tm_v, 0, (int)t0, (int)bh, bar_tma);
     }
     if (warp == 0) tmem_alloc(smem_u32(tslot), prep::kCols);
+    if (tid == 32) {  // this call's flags of the chunk start cleared, visibly before the trigger below
+        p.fl_prep[cid] = 0;
+        p.fl_s[cid] = 0;
+        __threadfence();
+    }
     float beta_i = 0.f, lam_i = 0.f;
     if (tid < nv) {
         beta_i = p.beta[bh * p.T + t0 + tid];
@@ -332,6 +361,8 @@ __global__ void __launch_bounds__(256, 4) falcon_prep_kernel(const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // The chain kernel may launch once every prep CTA is resident; it waits on the chunk flags.
+    pdl_launch_dependents();
     const uint32_t tmem = *tslot;
     const int q4 = warp & 3, hw = warp >> 2;
     const uint32_t tq = tmem + ((uint32_t)(32 * q4) << 16);  // this warp's TMEM lane quadrant
@@ -484,34 +515,43 @@ __global__ void __launch_bounds__(256, 4) falcon_prep_kernel(const __grid_consta
             for (int c = 0; c < 8; ++c) u[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         }
     }
-    release_tmem(tmem, warp, prep::kCols);
+    tc_fence_before();
+    publish(p.fl_prep + cid, p.epoch, tid);  // M, U, T and the scalars of chunk n are in the workspace
+    if (warp == 0) tmem_dealloc(tmem, prep::kCols);
 }
 
 // ---------------------------------------------------------------- chain kernel: S_{n+1} = M_n S_n + U_n
 // One CTA per sequence (one per SM). The state's columns split into two 32-column halves that
 // evolve independently (S_{n+1}[:, c] depends only on S_n[:, c]); each half is its own pipeline:
-//   warp 8 (issuer)    TMA loads of M_n (hi, lo) and U_n through a 3-stage ring; per half and step
-//                      eight tcgen05 MMAs D_h = (M_hi + M_lo) B_h, where the B tile of half h is
-//                      [S_hi | S_lo] of its 32 columns (one 64-column MN-major atom)
+//   warp 10 (loader)   per chunk, waits for the prep kernel's flag, then TMA-loads M_n (hi, lo) and
+//                      U_n into a 3-stage ring
+//   warp 8 (issuer)    per half and step eight tcgen05 MMAs D_h = (M_hi + M_lo) B_h, where the B
+//                      tile of half h is [S_hi | S_lo] of its 32 columns (one 64-column MN-major atom)
 //   warps 4h..4h+3     the epilogue of half h: 16x256b TMEM loads of D_h, S_{n+1} = D_h[:, c] +
 //                      D_h[:, 32 + c] + U_n in fp32, written as the next (double-buffered) B tile
-//   warp 9 (copier)    each finished B tile to the workspace, as the output kernel's S_n
-// so that one half's epilogue runs while the other half's MMAs do. The barriers that hand a B
-// tile over are kept per buffer, so no waiter can fall two phases behind its barrier. All waits
-// are bounded; a timeout raises the device flag and every role leaves its loop.
+//   warp 9 (copier)    each finished B tile to the workspace as the output kernel's S_n, then the
+//                      chunk's flag
+// so that one half's epilogue runs while the other half's MMAs do, and the scan follows the prep
+// kernel chunk by chunk instead of waiting for all of it. The barriers that hand a B tile over are
+// kept per buffer, so no waiter can fall two phases behind its barrier. All waits are bounded; a
+// timeout raises the device flag and every role leaves its loop.
 namespace chain {
 constexpr int kStages = 3;
 constexpr int kUBytes = 64 * 64 * 4;        // U_n, fp32, as two [64][32] halves (128-byte swizzle)
 constexpr int kUBytesHalf = kUBytes / 2;
 constexpr int kStage = 2 * kTile + kUBytes; // M hi, M lo, U
 constexpr int BT = kStages * kStage;        // B tiles [half][buffer]
-constexpr int BAR = BT + 4 * kTile;
-constexpr int kBars = kStages + 2 + 4 + 4 + 1;  // full, mma done[h], state ready[h][b], copied[h][b], drain
+constexpr int kStaging = 2;                 // staging buffers, each S_m hi and lo as standard 64 x 64 tiles
+constexpr int kLag = 3;                     // S_m's flag is published once S_{m + kLag} has been stored
+constexpr int SG = BT + 4 * kTile;
+constexpr int BAR = SG + kStaging * 2 * kTile;
+// full[s], empty[s], mma done[h], state ready[h][b], copied[h][b], drain
+constexpr int kBars = 2 * kStages + 2 + 4 + 4 + 1;
 constexpr int BYTES = BAR + 8 * kBars + 16;
 constexpr int ALLOC = BYTES + 1024;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr uint32_t kTmemCols = 128;
-static_assert(kStage % 1024 == 0 && BT % 1024 == 0, "stage alignment");
+static_assert(kStage % 1024 == 0 && BT % 1024 == 0 && SG % 1024 == 0, "stage alignment");
 }  // namespace chain
 
 __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const __grid_constant__ SplitParams p) {
@@ -524,32 +564,34 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
     const int N = p.N;
     auto bar = [&](int i) -> uint32_t { return base + chain::BAR + 8 * i; };
     auto full = [&](int s) { return bar(s); };
-    auto mmad = [&](int h) { return bar(chain::kStages + h); };
-    auto ready = [&](int h, int b) { return bar(chain::kStages + 2 + 2 * h + b); };   // phase k: S_{b+2k} in tile (h, b)
-    auto copied = [&](int h, int b) { return bar(chain::kStages + 6 + 2 * h + b); };  // phase k: S_{b+2k} stored
-    const uint32_t drain = bar(chain::kStages + 10);
+    auto empty = [&](int s) { return bar(chain::kStages + s); };
+    auto mmad = [&](int h) { return bar(2 * chain::kStages + h); };
+    auto ready = [&](int h, int b) { return bar(2 * chain::kStages + 2 + 2 * h + b); };   // phase k: S_{b+2k} in tile (h, b)
+    auto copied = [&](int h, int b) { return bar(2 * chain::kStages + 6 + 2 * h + b); };  // phase k: S_{b+2k} stored
+    const uint32_t drain = bar(2 * chain::kStages + 10);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + chain::BAR + 8 * chain::kBars);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chain::BAR + 8 * chain::kBars + 4);
     auto btile = [&](int h, int b) { return chain::BT + (2 * h + b) * kTile; };
-    auto wait = [&](uint32_t br, uint32_t parity) -> bool {  // bounded; on timeout every role stops
-        if (*abort_flag) return false;
-        if (mbar_wait_bounded(br, parity, kTimeoutCycles)) return true;
+    auto fail = [&]() {
         *abort_flag = 1;
         atomicExch(&g_split_timeout_flag, 1);
         return false;
     };
-    auto load = [&](int m) {  // M_m (hi, lo) and U_m into stage m % kStages
-        const int s = m % chain::kStages;
-        const uint32_t st = base + s * chain::kStage;
-        const int row = (int)((bh * N + m) * 128);
-        mbar_expect_tx(full(s), chain::kStage);
-        tma_load_2d(st, &p.tm_m, 0, row, full(s));
-        tma_load_2d(st + kTile, &p.tm_m, 0, row + 64, full(s));
-        tma_load_2d(st + 2 * kTile, &p.tm_u, 0, (int)((bh * N + m) * 64), full(s));
-        tma_load_2d(st + 2 * kTile + chain::kUBytesHalf, &p.tm_u, 32, (int)((bh * N + m) * 64), full(s));
+    auto wait = [&](uint32_t br, uint32_t parity) -> bool {  // bounded; gives up early once any role failed
+        if (mbar_try(br, parity)) return true;
+        const long long c0 = clock64();
+        while (!mbar_try(br, parity)) {
+            if (*abort_flag) return false;
+            __nanosleep(20);
+            if (clock64() - c0 > kTimeoutCycles) return fail();
+        }
+        return true;
     };
     if (tid == 0) {
-        for (int s = 0; s < chain::kStages; ++s) mbar_init(full(s), 1);
+        for (int s = 0; s < chain::kStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 256);
+        }
         for (int h = 0; h < 2; ++h) {
             mbar_init(mmad(h), 1);
             for (int b = 0; b < 2; ++b) {
@@ -562,11 +604,11 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
         mbar_init_fence();
     }
     if (warp == 0) tmem_alloc(smem_u32(tslot), chain::kTmemCols);
-    pdl_wait();  // the prep kernel's M_n, U_n are complete and visible from here on
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    pdl_launch_dependents();  // the output kernel may start its state-independent part
+    // The output kernel may launch once every chain CTA is resident; it waits on the state flags.
+    pdl_launch_dependents();
     const uint32_t tmem = *tslot;
     bool ok = true;
 
@@ -608,7 +650,7 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
         mbar_arrive(ready(h, 0));
         for (int n = 0; n < N; ++n) {
             const int s = n % chain::kStages;
-            if (!wait(full(s), (n / chain::kStages) & 1)) {  // U_n in stage s (read before the MMAs end)
+            if (!wait(full(s), (n / chain::kStages) & 1)) {  // U_n in stage s
                 ok = false;
                 break;
             }
@@ -623,6 +665,7 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
                 ok = false;
                 break;
             }
+            mbar_arrive(empty(s));  // this half's MMAs of step n are done with M_n, and U_n is read
             tc_fence_after();
             uint32_t d0[16], d1[16];
             tmem_ld_16x256b_x4(tq, d0);       // M S_hi part
@@ -644,7 +687,7 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
             }
             put_state(b);
             tc_fence_before();
-            mbar_arrive(ready(h, b));  // S_{n+1} written; D_h and U_n read
+            mbar_arrive(ready(h, b));  // S_{n+1} written; D_h read
         }
         if (ok && p.S_final) {
 #pragma unroll
@@ -658,15 +701,13 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
     } else if (warp == 8) {
         // ------------------------------------------------------------ issuer
         if (lane == 0) {
-            int issued = 0, consumed = 0, mma_issued = 0;
-            for (; issued < chain::kStages && issued < N; ++issued) load(issued);
+            int mma_issued = 0;
             for (int n = 0; n < N && ok; ++n) {
                 const int s = n % chain::kStages;
                 if (!wait(full(s), (n / chain::kStages) & 1)) {
                     ok = false;
                     break;
                 }
-                ++consumed;
                 const uint32_t st = base + s * chain::kStage;
                 for (int h = 0; h < 2; ++h) {
                     if (!wait(ready(h, n & 1), (n >> 1) & 1)) {  // S_n in tile (h, n & 1); D_h read out
@@ -685,53 +726,112 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
                     mma_commit(mmad(h));
                     mma_issued = 1;
                 }
-                // both halves have finished step n - 1, so its stage is free: fetch M_{n+2}, U_{n+2}
-                if (ok && n >= 1 && issued < N) {
-                    load(issued);
-                    ++issued;
-                }
             }
-            if (!ok) {  // let the MMAs and loads in flight finish (bounded) before TMEM is freed
-                if (mma_issued) {
-                    mma_commit(drain);
-                    mbar_wait_bounded(drain, 0, kTimeoutCycles);
-                }
-                for (int m = consumed; m < issued; ++m)
-                    mbar_wait_bounded(full(m % chain::kStages), (m / chain::kStages) & 1, kTimeoutCycles);
+            if (!ok && mma_issued) {  // let the MMAs in flight finish (bounded) before TMEM is freed
+                mma_commit(drain);
+                mbar_wait_bounded(drain, 0, kTimeoutCycles);
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ copier: B tiles -> S_m in the workspace
-        for (int i = lane + chain::kStages; i < N; i += 32) {  // the sequence's later M_n, U_n into L2
-            const long long m = bh * N + i;
-            prefetch_l2(p.ws_m + m * 2 * 4096, 2 * 4096 * 2);
-            prefetch_l2(p.ws_u + m * 4096, 4096 * 4);
-        }
+        // Each half's B tile is regrouped into standard hi and lo tiles in a staging buffer, which lane 0
+        // stores with TMA. A staging buffer is reused once its store has read it; S_m's flag is published
+        // once the store is complete, which lane 0 checks kLag steps later (or at the end), so that the
+        // copier, and through it the scan, never waits for a write to reach memory.
+        auto publish_s = [&](int m) {  // lane 0; every store up to S_m has completed
+            fence_proxy_async_global();
+            st_release_gpu(p.fl_s + bh * N + m, p.epoch);
+        };
         for (int m = 0; m < N && ok; ++m) {
+            const int g = m % chain::kStaging;
+            uint8_t* sg = sm + chain::SG + g * 2 * kTile;
+            if (lane == 0) bulk_wait_read<chain::kStaging - 1>();  // the store that last used buffer g has read it
+            __syncwarp();
             for (int h = 0; h < 2; ++h) {
                 if (!wait(ready(h, m & 1), (m >> 1) & 1)) {
                     ok = false;
                     break;
                 }
                 const uint8_t* bt = sm + btile(h, m & 1);
-                bf16* dh = p.ws_s + ((bh * N + m) * 2 * 64) * 64 + 32 * h;
-#pragma unroll 4
+                // all loads before any store: the two areas share one array, so interleaving them
+                // would serialise every load behind the store before it
+                const int c = lane & 7, cs = 4 * h + (c & 3);  // chunk c: hi 0-3, lo 4-7; its place in the standard tile
+                uint4 v[16];
+#pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const int task = lane + 32 * k, row = task >> 3, c = task & 7;  // chunk c: hi 0-3, lo 4-7
-                    const uint4 v = *reinterpret_cast<const uint4*>(bt + row * 128 + ((c ^ (row & 7)) << 4));
-                    *reinterpret_cast<uint4*>(dh + ((c >> 2) * 64 + row) * 64 + 8 * (c & 3)) = v;
+                    const int row = (lane >> 3) + 4 * k;
+                    v[k] = *reinterpret_cast<const uint4*>(bt + row * 128 + ((c ^ (row & 7)) << 4));
                 }
-                mbar_arrive(copied(h, m & 1));
+                mbar_arrive(copied(h, m & 1));  // tile (h, m & 1) has been read
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int row = (lane >> 3) + 4 * k;
+                    *reinterpret_cast<uint4*>(sg + (c >> 2) * kTile + row * 128 + ((cs ^ (row & 7)) << 4)) = v[k];
+                }
+            }
+            if (!ok) break;
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t sa = base + chain::SG + g * 2 * kTile;
+                tma_store_2d(&p.tm_s, sa, 0, (int)((bh * N + m) * 128));
+                tma_store_2d(&p.tm_s, sa + kTile, 0, (int)((bh * N + m) * 128 + 64));
+                bulk_commit();
+                if (m >= chain::kLag) {
+                    bulk_wait_done<chain::kLag>();  // S_{m - kLag}'s store is complete
+                    publish_s(m - chain::kLag);
+                }
             }
         }
+        if (lane == 0) {
+            bulk_wait_all();
+            if (ok)
+                for (int m = max(N - chain::kLag, 0); m < N; ++m) publish_s(m);
+        }
+        __syncwarp();
         if (ok && p.tail_out && lane < 8) {  // window 1: the tail is the last key (the next call's x)
             uint4 v = make_uint4(0, 0, 0, 0);
             if (p.T > 0) v = reinterpret_cast<const uint4*>(p.k + (bh * p.T + p.T - 1) * 64)[lane];
             else if (p.pos > 0) v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[lane];
             reinterpret_cast<uint4*>(p.tail_out + bh * 64)[lane] = v;
         }
+    } else {
+        // ------------------------------------------------------------ loader
+        if (lane == 0) {
+            int last[chain::kStages] = {-1, -1, -1};
+            for (int m = 0; m < N && ok; ++m) {
+                const int s = m % chain::kStages;
+                if (m >= chain::kStages && !wait(empty(s), ((m / chain::kStages) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (!wait_flag_bounded(p.fl_prep + bh * N + m, p.epoch, kTimeoutCycles)) {
+                    ok = fail();
+                    break;
+                }
+                fence_proxy_async_global();
+                const uint32_t st = base + s * chain::kStage;
+                const int row = (int)((bh * N + m) * 128);
+                mbar_expect_tx(full(s), chain::kStage);
+                tma_load_2d(st, &p.tm_m, 0, row, full(s));
+                tma_load_2d(st + kTile, &p.tm_m, 0, row + 64, full(s));
+                tma_load_2d(st + 2 * kTile, &p.tm_u, 0, (int)((bh * N + m) * 64), full(s));
+                tma_load_2d(st + 2 * kTile + chain::kUBytesHalf, &p.tm_u, 32, (int)((bh * N + m) * 64), full(s));
+                last[s] = m;
+            }
+            if (!ok)  // drain the loads in flight (at most one per stage), bounded
+                for (int s = 0; s < chain::kStages; ++s)
+                    if (last[s] >= 0) mbar_wait_bounded(full(s), (last[s] / chain::kStages) & 1, kTimeoutCycles);
+        }
+        __syncwarp();
     }
+    // Completion of this grid implies completion of the prep grid (the stream's next launch relies on it).
+    pdl_wait();
     release_tmem(tmem, warp, chain::kTmemCols);
 }
 
@@ -762,27 +862,34 @@ __global__ void __launch_bounds__(256, 3) falcon_out_kernel(const __grid_constan
     auto tile = [&](int i) -> uint8_t* { return sm + i * kTile; };
     auto taddr = [&](int i) -> uint32_t { return base + (uint32_t)(i * kTile); };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const long long cid = blockIdx.x;
-    const long long bh = cid / p.N;
-    const int n = (int)(cid - bh * p.N);
+    const int n = (int)(blockIdx.x / p.BH);  // chunk-major, in the order the chain produces S_n
+    const long long bh = blockIdx.x - (long long)n * p.BH;
+    const long long cid = bh * p.N + n;      // the chunk's workspace slot
     const long long t0 = (long long)n * kC;
     const bool f1 = p.variant == kF1;
     const Scal* sc = reinterpret_cast<const Scal*>(sm + outk::SCAL);
     const uint32_t bar_tma = base + outk::BAR, bar_mma = base + outk::BAR + 8, bar_s = base + outk::BAR + 16;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + outk::BAR + 24);
 
+    int bad = 0;  // thread 0: a producer's flag never came
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_s, 1);
         mbar_init_fence();
-        mbar_expect_tx(bar_tma, 5 * kTile + (uint32_t)sizeof(Scal));
+        mbar_expect_tx_only(bar_tma, 3 * kTile);  // the inputs first; the phase still needs the arrive below
         tma_load_3d(taddr(outk::X), &p.tm_k, 0, (int)t0 - 1, (int)bh, bar_tma);
         tma_load_3d(taddr(outk::Q), &p.tm_q, 0, (int)t0, (int)bh, bar_tma);
         tma_load_3d(taddr(outk::Y), &p.tm_v, 0, (int)t0, (int)bh, bar_tma);
-        tma_load_2d(taddr(outk::TH), &p.tm_t, 0, (int)(cid * 128), bar_tma);
-        tma_load_2d(taddr(outk::TL), &p.tm_t, 0, (int)(cid * 128 + 64), bar_tma);
-        bulk_load(base + outk::SCAL, p.ws_sc + cid * kScalBytes, (uint32_t)sizeof(Scal), bar_tma);
+        if (wait_producer(p.fl_prep + cid, p.epoch)) {  // T and the scalars of the chunk come from the prep kernel
+            mbar_expect_tx(bar_tma, 2 * kTile + (uint32_t)sizeof(Scal));
+            tma_load_2d(taddr(outk::TH), &p.tm_t, 0, (int)(cid * 128), bar_tma);
+            tma_load_2d(taddr(outk::TL), &p.tm_t, 0, (int)(cid * 128 + 64), bar_tma);
+            bulk_load(base + outk::SCAL, p.ws_sc + cid * kScalBytes, (uint32_t)sizeof(Scal), bar_tma);
+        } else {
+            bad = 1;
+            mbar_arrive(bar_tma);  // the phase completes once the inputs have landed
+        }
     }
     if (warp == 0) tmem_alloc(smem_u32(tslot), outk::kCols);
     tc_fence_before();
@@ -795,7 +902,7 @@ __global__ void __launch_bounds__(256, 3) falcon_out_kernel(const __grid_constan
     const bool upper = trow >= 64;  // lanes 64-127: warps 2, 3, 6, 7
     const int r = trow & 63;
 
-    if (!cta_wait(bar_tma, 0, tid)) return release_tmem(tmem, warp, outk::kCols);
+    if (!cta_wait(bar_tma, 0, tid, bad)) return release_tmem(tmem, warp, outk::kCols);
     if (n == 0 && p.pos > 0 && tid < 8) {
         const uint4 v = reinterpret_cast<const uint4*>(p.tail + bh * 64)[tid];
         *reinterpret_cast<uint4*>(tile(outk::X) + sw128(0, 8 * tid)) = v;
@@ -840,13 +947,17 @@ __global__ void __launch_bounds__(256, 3) falcon_out_kernel(const __grid_constan
     }
 
     // ---- the chunk-start state from the chain kernel: [X S; Q S]
-    pdl_wait();
     if (tid == 0) {
-        mbar_expect_tx(bar_s, 2 * kTile);
-        tma_load_2d(taddr(outk::SH), &p.tm_s, 0, (int)(cid * 128), bar_s);
-        tma_load_2d(taddr(outk::SL), &p.tm_s, 0, (int)(cid * 128 + 64), bar_s);
+        if (wait_producer(p.fl_s + cid, p.epoch)) {
+            mbar_expect_tx(bar_s, 2 * kTile);
+            tma_load_2d(taddr(outk::SH), &p.tm_s, 0, (int)(cid * 128), bar_s);
+            tma_load_2d(taddr(outk::SL), &p.tm_s, 0, (int)(cid * 128 + 64), bar_s);
+        } else {
+            bad = 1;
+            mbar_arrive(bar_s);
+        }
     }
-    if (!cta_wait(bar_s, 0, tid)) return release_tmem(tmem, warp, outk::kCols);
+    if (!cta_wait(bar_s, 0, tid, bad)) return release_tmem(tmem, warp, outk::kCols);
     if (tid == 0) {
         tc_fence_after();
         constexpr uint32_t idm = idesc_bf16(128, 64, false, true);
@@ -945,6 +1056,8 @@ __global__ void __launch_bounds__(256, 3) falcon_out_kernel(const __grid_constan
         tma_store_3d(&p.tm_out, taddr(outk::OUT), 0, (int)t0, (int)bh);
         tma_store_wait_read();
     }
+    // Completion of this grid implies completion of the chain grid (and through it the prep grid).
+    if (n == p.N - 1) pdl_wait();
     release_tmem(tmem, warp, outk::kCols);
 }
 
@@ -1019,6 +1132,7 @@ int smem_optin() {
 
 long long n_chunks(const Launch& a) { return (a.T + kC - 1) / kC; }
 
+
 }  // namespace
 
 bool split_supported(const Launch& a) {
@@ -1027,8 +1141,9 @@ bool split_supported(const Launch& a) {
            a.W == 1 && a.T < (1LL << 31) - 64 && BH < 65536 && BH * n_chunks(a) * 128 < (1LL << 31);
 }
 
+// Per chunk: M, U, S, T (16 KB each), the scalars (kScalBytes) and two 8-byte flags.
 size_t split_workspace_bytes(const Launch& a) {
-    return (size_t)(a.B * a.H) * (size_t)n_chunks(a) * (size_t)(4 * 16384 + kScalBytes);
+    return (size_t)(a.B * a.H) * (size_t)n_chunks(a) * (size_t)(4 * 16384 + kScalBytes + 16);
 }
 
 int launch_split(const Launch& a, cudaStream_t st) {
@@ -1042,6 +1157,10 @@ int launch_split(const Launch& a, cudaStream_t st) {
     p.ws_s = reinterpret_cast<bf16*>(ws + 2 * per);
     p.ws_t = reinterpret_cast<bf16*>(ws + 3 * per);
     p.ws_sc = ws + 4 * per;
+    p.fl_prep = reinterpret_cast<unsigned long long*>(ws + 4 * per + (size_t)BH * (size_t)N * kScalBytes);
+    p.fl_s = p.fl_prep + BH * N;
+    p.epoch = 1;
+    p.BH = BH;
     if (N > 0) {
         if (!encode_bhtd(&p.tm_q, a.q, a.T, BH) || !encode_bhtd(&p.tm_k, a.k, a.T, BH) ||
             !encode_bhtd(&p.tm_v, a.v, a.T, BH) || !encode_bhtd(&p.tm_out, a.out, a.T, BH) ||
@@ -1073,8 +1192,10 @@ int launch_split(const Launch& a, cudaStream_t st) {
             return 4;
         attr_set = true;
     }
-    // prep: an ordinary launch (it overwrites the workspace the previous call's output kernel read);
-    // chain and output: programmatic dependent launches that overlap their predecessor's tail.
+    // prep: an ordinary launch, after everything that used the workspace before. chain and output:
+    // programmatic dependent launches, which start once every CTA of the kernel before them is
+    // resident and then follow it chunk by chunk through the flags; none of them waits on a kernel
+    // launched after it.
     if (N > 0) falcon_prep_kernel<<<(unsigned)(BH * N), 256, prep::ALLOC, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return 4;
     cudaLaunchAttribute pdl[1];

@@ -88,6 +88,34 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ---- flags between kernels that run at the same time (a producer publishes, a consumer polls)
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// Orders this thread's earlier generic-proxy accesses of global memory before its later
+// async-proxy (TMA) accesses: taken after acquiring a flag, before loading what it guards.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+// Poll `flag` until it holds `value`, for at most `limit` cycles; false on timeout.
+__device__ __forceinline__ bool wait_flag_bounded(const unsigned long long* flag, unsigned long long value,
+                                                  long long limit) {
+    if (ld_acquire_gpu(flag) == value) return true;
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(flag) != value) {
+        __nanosleep(64);
+        if (clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+// Add `bytes` to the current phase's transaction count without arriving.
+__device__ __forceinline__ void mbar_expect_tx_only(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 // ---- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1, uint32_t bar) {
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
@@ -121,6 +149,12 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // wait until at most one committed bulk group still reads shared memory
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// This thread's bulk groups, all but the newest N complete (writes performed).
+template <int N>
+__device__ __forceinline__ void bulk_wait_done() { asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory"); }
+// This thread's bulk groups, all but the newest N have finished reading their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 
 // ---- TMEM loads: 16 consecutive columns of this thread's lane; the wait is separate so that
 // several loads share one wait, and `regs_ready` pins every use of the registers after it.
