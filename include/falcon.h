@@ -117,7 +117,7 @@ int falcon_fwd(int variant, const void* q, const void* k, const void* v, const f
                size_t workspace_bytes, void* stream);
 
 /* Workspace bytes that enable the split path of falcon_fwd for these arguments
- * (B*H*ceil(T/64) * (66 KiB + 16 bytes) for Falcon-1/1A, bf16, dk = dv = 64, chunk 64; 0 when
+ * (B*H*ceil(T/64) * (66 KiB + 8 bytes) for Falcon-1/1A, bf16, dk = dv = 64, chunk 64; 0 when
  * no path uses a workspace or the arguments are invalid). Host only. */
 size_t falcon_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk);
 

@@ -152,10 +152,10 @@ def test_kernel_choice(lib, case, expect):
 
 
 def test_workspace_bytes(lib):
-    # B*H*ceil(T/64) chunks of 66 KiB + 16 bytes: M (hi, lo), U, the chunk-start state (hi, lo), T (hi, lo),
-    # scalars, and two 8-byte flags between the kernels
-    assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(8, 12, 1024, 64, 64), 64) == 8 * 12 * 16 * 67600
-    assert F.falcon_workspace_bytes(F.FALCON_1A, F.make_dims(2, 3, 65, 64, 64), 64) == 2 * 3 * 2 * 67600
+    # B*H*ceil(T/64) chunks of 66 KiB + 8 bytes: M (hi, lo), U, the chunk-start state (hi, lo), T (hi, lo),
+    # scalars, and the 8-byte flag the chain kernel waits on
+    assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(8, 12, 1024, 64, 64), 64) == 8 * 12 * 16 * 67592
+    assert F.falcon_workspace_bytes(F.FALCON_1A, F.make_dims(2, 3, 65, 64, 64), 64) == 2 * 3 * 2 * 67592
     assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 0, 64, 64), 64) == 0
     assert F.falcon_workspace_bytes(F.FALCON_2, F.make_dims(2, 3, 64, 64, 64), 64) == 0
     assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 64, 64, 64, dtype=F.FALCON_F32), 64) == 0

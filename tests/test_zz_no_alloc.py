@@ -18,7 +18,7 @@ def test_static_entry_rejects_oversize_without_launch():
 
     build.build()
     F.load()
-    d = F.make_dims(8, 12, 1024, 64, 64)  # 1536 chunks x (66 KiB + 16 bytes) > 16 MiB
+    d = F.make_dims(8, 12, 1024, 64, 64)  # 1536 chunks x (66 KiB + 8 bytes) > 16 MiB
     assert F.falcon_workspace_bytes(F.FALCON_1, d, 64) > F.STATIC_WORKSPACE_BYTES
     st = F.falcon_fwd_static(F.FALCON_1, A, A + (1 << 30), A + (2 << 30), A + (3 << 30), A + (4 << 30), None, None,
                              A + (5 << 30), None, None, d, 64, stream=0)

@@ -65,12 +65,10 @@ struct SplitParams {
     bf16* ws_s;   // [BH][N][2][64][64]: S_n hi, lo (state at the start of chunk n)
     bf16* ws_t;   // [BH][N][2][64][64]: T_n hi, lo
     uint8_t* ws_sc;  // [BH][N] blocks of kScalBytes: the chunk's per-token scalars (a Scal)
-    // Flags between the three kernels, which run overlapped. The prep CTA of a chunk clears both of
-    // the chunk's flags before it lets the chain kernel launch (the kernels after it cannot start
-    // before every prep CTA has), and a producer sets a flag to `epoch` once the data it guards is
-    // complete.
-    unsigned long long* fl_prep;  // [BH][N]: the prep kernel has written the chunk's M, U, T and scalars
-    unsigned long long* fl_s;     // [BH][N]: the chain kernel has written S_n
+    // The chain kernel follows the prep kernel chunk by chunk through a flag per chunk: the prep CTA
+    // of the chunk clears it before it lets the chain kernel launch (which cannot happen before every
+    // prep CTA has), and sets it to `epoch` once M_n, U_n, T_n and the scalars are in the workspace.
+    unsigned long long* fl_prep;  // [BH][N]
     unsigned long long epoch;
     long long BH;
     long long T, pos;
@@ -346,9 +344,8 @@ __global__ void __launch_bounds__(256, 4) falcon_prep_kernel(const __grid_consta
         tma_load_3d(base + prep::Y, &p.tm_v, 0, (int)t0, (int)bh, bar_tma);
     }
     if (warp == 0) tmem_alloc(smem_u32(tslot), prep::kCols);
-    if (tid == 32) {  // this call's flags of the chunk start cleared, visibly before the trigger below
+    if (tid == 32) {  // this call's flag of the chunk starts cleared, visibly before the trigger below
         p.fl_prep[cid] = 0;
-        p.fl_s[cid] = 0;
         __threadfence();
     }
     float beta_i = 0.f, lam_i = 0.f;
@@ -528,9 +525,8 @@ __global__ void __launch_bounds__(256, 4) falcon_prep_kernel(const __grid_consta
 //   warp 8 (issuer)    per half and step eight tcgen05 MMAs D_h = (M_hi + M_lo) B_h, where the B
 //                      tile of half h is [S_hi | S_lo] of its 32 columns (one 64-column MN-major atom)
 //   warps 4h..4h+3     the epilogue of half h: 16x256b TMEM loads of D_h, S_{n+1} = D_h[:, c] +
-//                      D_h[:, 32 + c] + U_n in fp32, written as the next (double-buffered) B tile
-//   warp 9 (copier)    each finished B tile to the workspace as the output kernel's S_n, then the
-//                      chunk's flag
+//                      D_h[:, 32 + c] + U_n in fp32, written as the next B tile (three per half)
+//   warp 9 (copier)    each finished B tile to the workspace as the output kernel's S_n
 // so that one half's epilogue runs while the other half's MMAs do, and the scan follows the prep
 // kernel chunk by chunk instead of waiting for all of it. The barriers that hand a B tile over are
 // kept per buffer, so no waiter can fall two phases behind its barrier. All waits are bounded; a
@@ -541,12 +537,12 @@ constexpr int kUBytes = 64 * 64 * 4;        // U_n, fp32, as two [64][32] halves
 constexpr int kUBytesHalf = kUBytes / 2;
 constexpr int kStage = 2 * kTile + kUBytes; // M hi, M lo, U
 constexpr int BT = kStages * kStage;        // B tiles [half][buffer]
+constexpr int kBuf = 3;                     // B tiles per half: S_n, S_{n+1} and the one being copied
 constexpr int kStaging = 2;                 // staging buffers, each S_m hi and lo as standard 64 x 64 tiles
-constexpr int kLag = 3;                     // S_m's flag is published once S_{m + kLag} has been stored
-constexpr int SG = BT + 4 * kTile;
+constexpr int SG = BT + 2 * kBuf * kTile;
 constexpr int BAR = SG + kStaging * 2 * kTile;
 // full[s], empty[s], mma done[h], state ready[h][b], copied[h][b], drain
-constexpr int kBars = 2 * kStages + 2 + 4 + 4 + 1;
+constexpr int kBars = 2 * kStages + 2 + 4 * kBuf + 1;
 constexpr int BYTES = BAR + 8 * kBars + 16;
 constexpr int ALLOC = BYTES + 1024;
 constexpr int kThreads = 352;
@@ -566,12 +562,14 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
     auto full = [&](int s) { return bar(s); };
     auto empty = [&](int s) { return bar(chain::kStages + s); };
     auto mmad = [&](int h) { return bar(2 * chain::kStages + h); };
-    auto ready = [&](int h, int b) { return bar(2 * chain::kStages + 2 + 2 * h + b); };   // phase k: S_{b+2k} in tile (h, b)
-    auto copied = [&](int h, int b) { return bar(2 * chain::kStages + 6 + 2 * h + b); };  // phase k: S_{b+2k} stored
-    const uint32_t drain = bar(2 * chain::kStages + 10);
+    constexpr int kB = chain::kBuf;
+    // phase k of ready(h, b) / copied(h, b): S_{b + kB k} is in tile (h, b) / has been read from it
+    auto ready = [&](int h, int b) { return bar(2 * chain::kStages + 2 + kB * h + b); };
+    auto copied = [&](int h, int b) { return bar(2 * chain::kStages + 2 + 2 * kB + kB * h + b); };
+    const uint32_t drain = bar(2 * chain::kStages + 2 + 4 * kB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + chain::BAR + 8 * chain::kBars);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chain::BAR + 8 * chain::kBars + 4);
-    auto btile = [&](int h, int b) { return chain::BT + (2 * h + b) * kTile; };
+    auto btile = [&](int h, int b) { return chain::BT + (kB * h + b) * kTile; };
     auto fail = [&]() {
         *abort_flag = 1;
         atomicExch(&g_split_timeout_flag, 1);
@@ -594,7 +592,7 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(mmad(h), 1);
-            for (int b = 0; b < 2; ++b) {
+            for (int b = 0; b < kB; ++b) {
                 mbar_init(ready(h, b), 128);
                 mbar_init(copied(h, b), 32);
             }
@@ -607,7 +605,8 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // The output kernel may launch once every chain CTA is resident; it waits on the state flags.
+    // The output kernel may launch once every chain CTA is resident: its state-independent part runs
+    // alongside the scan, and it waits for this kernel's completion before it reads S_n.
     pdl_launch_dependents();
     const uint32_t tmem = *tslot;
     bool ok = true;
@@ -680,8 +679,8 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
                 sv[j][2] = __uint_as_float(d0[4 * j + 2]) + __uint_as_float(d1[4 * j + 2]) + ub[j].x;
                 sv[j][3] = __uint_as_float(d0[4 * j + 3]) + __uint_as_float(d1[4 * j + 3]) + ub[j].y;
             }
-            const int b = (n + 1) & 1;  // the tile that held S_{n-1}: its copy must be done
-            if (n >= 1 && !wait(copied(h, b), ((n - 1) >> 1) & 1)) {
+            const int b = (n + 1) % kB;  // the tile that held S_{n+1-kB}: its copy must be done
+            if (n + 1 >= kB && !wait(copied(h, b), ((n + 1 - kB) / kB) & 1)) {
                 ok = false;
                 break;
             }
@@ -710,13 +709,13 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
                 }
                 const uint32_t st = base + s * chain::kStage;
                 for (int h = 0; h < 2; ++h) {
-                    if (!wait(ready(h, n & 1), (n >> 1) & 1)) {  // S_n in tile (h, n & 1); D_h read out
+                    if (!wait(ready(h, n % kB), (n / kB) & 1)) {  // S_n in tile (h, n % kB); D_h read out
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     constexpr uint32_t id = idesc_bf16(64, 64, false, true);
-                    const uint32_t bt = base + btile(h, n & 1);
+                    const uint32_t bt = base + btile(h, n % kB);
 #pragma unroll
                     for (int part = 0; part < 2; ++part)
 #pragma unroll
@@ -736,24 +735,18 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
     } else if (warp == 9) {
         // ------------------------------------------------------------ copier: B tiles -> S_m in the workspace
         // Each half's B tile is regrouped into standard hi and lo tiles in a staging buffer, which lane 0
-        // stores with TMA. A staging buffer is reused once its store has read it; S_m's flag is published
-        // once the store is complete, which lane 0 checks kLag steps later (or at the end), so that the
-        // copier, and through it the scan, never waits for a write to reach memory.
-        auto publish_s = [&](int m) {  // lane 0; every store up to S_m has completed
-            fence_proxy_async_global();
-            st_release_gpu(p.fl_s + bh * N + m, p.epoch);
-        };
+        // stores with TMA; a staging buffer is reused once its store has read it.
         for (int m = 0; m < N && ok; ++m) {
             const int g = m % chain::kStaging;
             uint8_t* sg = sm + chain::SG + g * 2 * kTile;
             if (lane == 0) bulk_wait_read<chain::kStaging - 1>();  // the store that last used buffer g has read it
             __syncwarp();
             for (int h = 0; h < 2; ++h) {
-                if (!wait(ready(h, m & 1), (m >> 1) & 1)) {
+                if (!wait(ready(h, m % kB), (m / kB) & 1)) {
                     ok = false;
                     break;
                 }
-                const uint8_t* bt = sm + btile(h, m & 1);
+                const uint8_t* bt = sm + btile(h, m % kB);
                 // all loads before any store: the two areas share one array, so interleaving them
                 // would serialise every load behind the store before it
                 const int c = lane & 7, cs = 4 * h + (c & 3);  // chunk c: hi 0-3, lo 4-7; its place in the standard tile
@@ -763,7 +756,7 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
                     const int row = (lane >> 3) + 4 * k;
                     v[k] = *reinterpret_cast<const uint4*>(bt + row * 128 + ((c ^ (row & 7)) << 4));
                 }
-                mbar_arrive(copied(h, m & 1));  // tile (h, m & 1) has been read
+                mbar_arrive(copied(h, m % kB));  // tile (h, m % kB) has been read
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     const int row = (lane >> 3) + 4 * k;
@@ -778,17 +771,9 @@ __global__ void __launch_bounds__(chain::kThreads, 1) falcon_chain_kernel(const 
                 tma_store_2d(&p.tm_s, sa, 0, (int)((bh * N + m) * 128));
                 tma_store_2d(&p.tm_s, sa + kTile, 0, (int)((bh * N + m) * 128 + 64));
                 bulk_commit();
-                if (m >= chain::kLag) {
-                    bulk_wait_done<chain::kLag>();  // S_{m - kLag}'s store is complete
-                    publish_s(m - chain::kLag);
-                }
             }
         }
-        if (lane == 0) {
-            bulk_wait_all();
-            if (ok)
-                for (int m = max(N - chain::kLag, 0); m < N; ++m) publish_s(m);
-        }
+        if (lane == 0) bulk_wait_all();
         __syncwarp();
         if (ok && p.tail_out && lane < 8) {  // window 1: the tail is the last key (the next call's x)
             uint4 v = make_uint4(0, 0, 0, 0);
@@ -947,15 +932,11 @@ __global__ void __launch_bounds__(256, 3) falcon_out_kernel(const __grid_constan
     }
 
     // ---- the chunk-start state from the chain kernel: [X S; Q S]
+    pdl_wait();  // the chain kernel has completed: every S_n is in the workspace
     if (tid == 0) {
-        if (wait_producer(p.fl_s + cid, p.epoch)) {
-            mbar_expect_tx(bar_s, 2 * kTile);
-            tma_load_2d(taddr(outk::SH), &p.tm_s, 0, (int)(cid * 128), bar_s);
-            tma_load_2d(taddr(outk::SL), &p.tm_s, 0, (int)(cid * 128 + 64), bar_s);
-        } else {
-            bad = 1;
-            mbar_arrive(bar_s);
-        }
+        mbar_expect_tx(bar_s, 2 * kTile);
+        tma_load_2d(taddr(outk::SH), &p.tm_s, 0, (int)(cid * 128), bar_s);
+        tma_load_2d(taddr(outk::SL), &p.tm_s, 0, (int)(cid * 128 + 64), bar_s);
     }
     if (!cta_wait(bar_s, 0, tid, bad)) return release_tmem(tmem, warp, outk::kCols);
     if (tid == 0) {
@@ -1056,8 +1037,6 @@ __global__ void __launch_bounds__(256, 3) falcon_out_kernel(const __grid_constan
         tma_store_3d(&p.tm_out, taddr(outk::OUT), 0, (int)t0, (int)bh);
         tma_store_wait_read();
     }
-    // Completion of this grid implies completion of the chain grid (and through it the prep grid).
-    if (n == p.N - 1) pdl_wait();
     release_tmem(tmem, warp, outk::kCols);
 }
 
@@ -1141,9 +1120,9 @@ bool split_supported(const Launch& a) {
            a.W == 1 && a.T < (1LL << 31) - 64 && BH < 65536 && BH * n_chunks(a) * 128 < (1LL << 31);
 }
 
-// Per chunk: M, U, S, T (16 KB each), the scalars (kScalBytes) and two 8-byte flags.
+// Per chunk: M, U, S, T (16 KB each), the scalars (kScalBytes) and an 8-byte flag.
 size_t split_workspace_bytes(const Launch& a) {
-    return (size_t)(a.B * a.H) * (size_t)n_chunks(a) * (size_t)(4 * 16384 + kScalBytes + 16);
+    return (size_t)(a.B * a.H) * (size_t)n_chunks(a) * (size_t)(4 * 16384 + kScalBytes + 8);
 }
 
 int launch_split(const Launch& a, cudaStream_t st) {
@@ -1158,7 +1137,6 @@ int launch_split(const Launch& a, cudaStream_t st) {
     p.ws_t = reinterpret_cast<bf16*>(ws + 3 * per);
     p.ws_sc = ws + 4 * per;
     p.fl_prep = reinterpret_cast<unsigned long long*>(ws + 4 * per + (size_t)BH * (size_t)N * kScalBytes);
-    p.fl_s = p.fl_prep + BH * N;
     p.epoch = 1;
     p.BH = BH;
     if (N > 0) {
@@ -1192,10 +1170,11 @@ int launch_split(const Launch& a, cudaStream_t st) {
             return 4;
         attr_set = true;
     }
-    // prep: an ordinary launch, after everything that used the workspace before. chain and output:
-    // programmatic dependent launches, which start once every CTA of the kernel before them is
-    // resident and then follow it chunk by chunk through the flags; none of them waits on a kernel
-    // launched after it.
+    // prep: an ordinary launch, after everything that used the workspace before. chain: a programmatic
+    // dependent launch that starts once every prep CTA is resident and follows the prep kernel chunk
+    // by chunk through the flags. output: a programmatic dependent launch whose state-independent part
+    // overlaps the chain and which waits for the chain's completion before it reads S_n. No kernel
+    // waits on one launched after it.
     if (N > 0) falcon_prep_kernel<<<(unsigned)(BH * N), 256, prep::ALLOC, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return 4;
     cudaLaunchAttribute pdl[1];
