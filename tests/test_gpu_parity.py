@@ -151,6 +151,17 @@ def test_clamp_stress(variant):
     _parity(w, inp, name=f"clamp v{variant}")
 
 
+def test_falcon2_mixed_decay_columns():
+    """Falcon-2 with lambda = 1000 and per-column gains alternating 1.5 (clamped: strong decay) and 1e-3
+    (weak decay): in one chunk some columns take the factored exponentials, the others do not."""
+    w = I.WORKLOADS[HEAD].with_(variant="falcon2", chunk=64, lam_const=1000.0, lam_shift=None)
+    inp = I.make_inputs(w, seed=11, seqlen=200, batch=1)
+    b = torch.full_like(inp["beta"], 1e-3)
+    b[..., 0::2] = 1.5
+    inp["beta"] = b
+    _parity(w, inp, name="falcon2 mixed columns")
+
+
 @pytest.mark.parametrize("variant", [F1, F1A, F2, F3])
 def test_zero_keys_with_zero_denominator(variant):
     """lambda = eps = 0 and some all-zero keys: eta = 0 there (no NaN)."""

@@ -21,10 +21,15 @@
 //   S <- exp(L_C) S + X^T diag(eta_j exp(L_C - L_j)) R
 // Falcon-2 uses per-column eta, L; Falcon-3 solves over (token, window slot)
 // unknowns with a block-strict-lower system (§H, "tensorInv").
-// Only exp(L_a - L_b) with a >= b is formed, so no factor exceeds 1.
+// Factors exp(L_a - L_b) have a >= b, so none exceeds 1; Falcon-2 forms them as exp(L_a) exp(-L_b)
+// where the column's chunk decay keeps both finite, else one by one.
+// With bf16 inputs (whose tiles hold exact bf16 values) G and Sc are warp-level bf16 mma.sync
+// products with fp32 sums; fp32 inputs keep fp32 FMA loops throughout.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "falcon_internal.h"
 
@@ -32,6 +37,7 @@ namespace falcon {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr float kFastL = 30.f;  // Falcon-2: per-column chunk log decay above which e^{a-b} = e^{a} e^{-b}
 constexpr int kMaxW = 8;
 
 struct GParams {
@@ -51,6 +57,20 @@ struct GParams {
 };
 
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
+// Eight consecutive elements from a 16-byte aligned address, as fp32.
+__device__ __forceinline__ void ld8(const float* p, float (&o)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    o[0] = a.x, o[1] = a.y, o[2] = a.z, o[3] = a.w, o[4] = b.x, o[5] = b.y, o[6] = b.z, o[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, float (&o)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float2 f = __bfloat1622float2(h[m]);
+        o[2 * m] = f.x, o[2 * m + 1] = f.y;
+    }
+}
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void stf(float* p, float x) { *p = x; }
 __device__ __forceinline__ void stf(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
@@ -86,6 +106,51 @@ __device__ float lambda_max_small(float (*a)[kMaxW], int n) {
     float mx = a[0][0];
     for (int p = 1; p < n; ++p) mx = fmaxf(mx, a[p][p]);
     return mx;
+}
+
+// d += A (16 x 16, row-major bf16) * B (16 x 8, column-major bf16), fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// Two fp32 values that are exact bf16 numbers, packed (lo = first) without rounding error.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+// G = X X^T (C x C) and Sc = Q X^T (C x C) from fp32 tiles (row stride xs) holding bf16 values, C a
+// multiple of 16, dk a multiple of 16: each warp takes one 16-row block of one product across all
+// its 8-column tiles. Fragments follow the m16n8k16 layout (g = lane / 4, t = lane % 4).
+__device__ void gram_mma(const float* X, const float* Q, float* G, float* Sc, int C, int dk, int xs, int ld, int tid) {
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int mbs = C / 16;
+    for (int job = warp; job < 2 * mbs; job += kThreads / 32) {
+        const float* A = job < mbs ? X : Q;
+        float* D = job < mbs ? G : Sc;
+        const int r0 = 16 * (job % mbs);
+        float acc[8][4] = {};
+        for (int k0 = 0; k0 < dk; k0 += 16) {
+            const float* ar = A + (r0 + g) * xs + k0 + 2 * t;
+            const uint32_t a0 = pack_bf16(ar[0], ar[1]), a1 = pack_bf16(ar[8 * xs], ar[8 * xs + 1]);
+            const uint32_t a2 = pack_bf16(ar[8], ar[9]), a3 = pack_bf16(ar[8 * xs + 8], ar[8 * xs + 9]);
+#pragma unroll
+            for (int nb = 0; nb < 8; ++nb) {
+                if (8 * nb >= C) break;
+                const float* br = X + (8 * nb + g) * xs + k0 + 2 * t;
+                mma_bf16_16816(acc[nb], a0, a1, a2, a3, pack_bf16(br[0], br[1]), pack_bf16(br[8], br[9]));
+            }
+        }
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+            if (8 * nb >= C) break;
+            float* dr = D + (r0 + g) * ld + 8 * nb + 2 * t;
+            dr[0] = acc[nb][0], dr[1] = acc[nb][1];
+            dr[8 * ld] = acc[nb][2], dr[8 * ld + 1] = acc[nb][3];
+        }
+    }
 }
 
 // Shared-memory carve-up (floats). NE = C + W - 1 extended pair rows.
@@ -173,38 +238,78 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
     for (long long t0 = 0; t0 < T; t0 += C) {
         const int n = (int)min((long long)C, T - t0);
         __syncthreads();  // previous chunk finished with every buffer
-        // ---- (1) tiles. Extended row e <-> pair with global index pos + t0 + 2 - W + e.
-        for (int idx = tid; idx < NE * DK; idx += kThreads) {
-            const int e = idx / DK, cc = idx % DK;
-            const long long gpair = pos + t0 + 2 - W + e;
-            float x = 0.f;
-            if (e < n + W - 1 && gpair >= 2) x = load_key(t0 - W + e, cc);
-            s.X[e * XS + cc] = x;
+        // ---- (1) tiles. Extended row e <-> pair with global index pos + t0 + 2 - W + e. Eight elements
+        // per 16-byte load (rows of q, k, v and the tail are 16-byte aligned), every load of a thread
+        // issued before its stores.
+        {
+            const int KV = DK / 8, VV = DVS / 8;
+            const int nx = NE * KV, nq = C * KV, ny = NE * VV;
+            constexpr int kPer = 4;  // vector loads in flight per thread and round
+            for (int base = tid; base < nx + nq + ny; base += kPer * kThreads) {
+                float buf[kPer][8];
+#pragma unroll
+                for (int m = 0; m < kPer; ++m) {
+                    const int idx = base + m * kThreads;
+#pragma unroll
+                    for (int e8 = 0; e8 < 8; ++e8) buf[m][e8] = 0.f;
+                    if (idx < nx) {  // shifted keys, from k, the tail or the x_1 = 0 sentinel
+                        const int e = idx / KV, c8 = 8 * (idx % KV);
+                        const long long gpair = pos + t0 + 2 - W + e, u = t0 - W + e;
+                        if (e < n + W - 1 && gpair >= 2) {
+                            if (u >= 0) ld8(k + u * DK + c8, buf[m]);
+                            else if (tail != nullptr && pos + 1 + u > 0) ld8(tail + (u + W) * DK + c8, buf[m]);
+                        }
+                    } else if (idx < nx + nq) {
+                        const int i = (idx - nx) / KV, c8 = 8 * ((idx - nx) % KV);
+                        if (i < n) ld8(q + (t0 + i) * DK + c8, buf[m]);
+                    } else if (idx < nx + nq + ny) {  // values of the extended rows, this CTA's columns
+                        const int e = (idx - nx - nq) / VV, c8 = 8 * ((idx - nx - nq) % VV);
+                        const long long gpair = pos + t0 + 2 - W + e, u = t0 + 1 - W + e;
+                        if (e < n + W - 1 && gpair >= 2) {
+                            if (u >= 0) ld8(v + u * DV + c0 + c8, buf[m]);
+                            else if (tail != nullptr && pos + 1 + u > 0)
+                                ld8(tail + (long long)W * DK + (u + W - 1) * DV + c0 + c8, buf[m]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < kPer; ++m) {
+                    const int idx = base + m * kThreads;
+                    float* dst = nullptr;
+                    if (idx < nx) dst = s.X + (idx / KV) * XS + 8 * (idx % KV);
+                    else if (idx < nx + nq) dst = s.Q + ((idx - nx) / KV) * XS + 8 * ((idx - nx) % KV);
+                    else if (idx < nx + nq + ny) dst = s.Y + ((idx - nx - nq) / VV) * DVS + 8 * ((idx - nx - nq) % VV);
+                    if (dst)
+#pragma unroll
+                        for (int e8 = 0; e8 < 8; ++e8) dst[e8] = buf[m][e8];
+                }
+            }
         }
-        for (int idx = tid; idx < C * DK; idx += kThreads) {
-            const int i = idx / DK, cc = idx % DK;
-            s.Q[i * XS + cc] = i < n ? ldf(q + (t0 + i) * DK + cc) : 0.f;
-        }
-        for (int idx = tid; idx < NE * DVS; idx += kThreads) {
-            const int e = idx / DVS, cc = idx % DVS;
-            const long long gpair = pos + t0 + 2 - W + e;
-            float y = 0.f;
-            if (e < n + W - 1 && gpair >= 2) y = load_val(t0 + 1 - W + e, c0 + cc);
-            s.Y[idx] = y;
+        if (VAR == kF2) {  // the chunk's gains (per column, into eta) and ridge coefficients (into kap)
+            for (int idx = tid; idx < C * DVS; idx += kThreads) {
+                const int i = idx / DVS, c = idx % DVS;
+                s.eta[c * CS + i] = i < n ? beta[(t0 + i) * DV + c0 + c] : 0.f;
+            }
+            for (int i = tid; i < C; i += kThreads) s.kap[i] = i < n ? lam[t0 + i] : 0.f;
         }
         __syncthreads();
         // ---- (2) Gram, scores, projected history, Q S
-        for (int idx = tid; idx < NE * NE; idx += kThreads) {
-            const int a = idx / NE, b = idx % NE;
-            float acc = 0.f;
-            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.X[a * XS + cc], s.X[b * XS + cc], acc);
-            s.G[idx] = acc;
-        }
-        for (int idx = tid; idx < C * NE; idx += kThreads) {
-            const int i = idx / NE, b = idx % NE;
-            float acc = 0.f;
-            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.Q[i * XS + cc], s.X[b * XS + cc], acc);
-            s.Sc[idx] = acc;
+        constexpr bool kMmaGram = std::is_same<Tin, __nv_bfloat16>::value && VAR != kF3;
+        if (kMmaGram && C <= 64 && C % 16 == 0 && DK % 16 == 0) {
+            gram_mma(s.X, s.Q, s.G, s.Sc, C, DK, XS, NE, tid);
+        } else {
+            for (int idx = tid; idx < NE * NE; idx += kThreads) {
+                const int a = idx / NE, b = idx % NE;
+                float acc = 0.f;
+                for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.X[a * XS + cc], s.X[b * XS + cc], acc);
+                s.G[idx] = acc;
+            }
+            for (int idx = tid; idx < C * NE; idx += kThreads) {
+                const int i = idx / NE, b = idx % NE;
+                float acc = 0.f;
+                for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.Q[i * XS + cc], s.X[b * XS + cc], acc);
+                s.Sc[idx] = acc;
+            }
         }
         for (int idx = tid; idx < NE * DVS; idx += kThreads) {
             const int e = idx / DVS, c = idx % DVS;
@@ -221,22 +326,42 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         __syncthreads();
         // ---- (3) per-token scalars and the chunk-local log-decay prefix
         if (VAR == kF2) {
-            if (tid < DVS) {
-                const int c = tid;
-                float run = 0.f;
-                for (int i = 0; i < C; ++i) {
-                    float eta = 0.f, alpha = 0.f;
-                    const long long tau = pos + t0 + i + 1;
-                    if (i < n && tau >= 2) {
-                        const float lm = lam[t0 + i];
-                        const float den = s.G[i * NE + i] + lm + p.eps;
-                        eta = den == 0.f ? 0.f : beta[(t0 + i) * DV + c0 + c] / den;
-                        alpha = fminf(eta * lm, 1.f - p.eps_gamma);
+            // every (token, column) in parallel, then one warp scan of log(gamma) per column
+            for (int idx = tid; idx < C * DVS; idx += kThreads) {
+                const int i = idx / DVS, c = idx % DVS;
+                float eta = 0.f, alpha = 0.f;
+                const long long tau = pos + t0 + i + 1;
+                if (i < n && tau >= 2) {
+                    const float lm = s.kap[i];
+                    const float den = s.G[i * NE + i] + lm + p.eps;
+                    eta = den == 0.f ? 0.f : s.eta[c * CS + i] / den;
+                    alpha = fminf(eta * lm, 1.f - p.eps_gamma);
+                }
+                s.eta[c * CS + i] = eta;
+                s.L[c * CS + i] = log1pf(-alpha);
+            }
+            __syncthreads();
+            const int wid = tid >> 5, lane = tid & 31, per = (C + 31) / 32;
+            for (int c = wid; c < DVS; c += kThreads / 32) {
+                float ls[2] = {0.f, 0.f}, lsum = 0.f;
+                for (int m = 0; m < per; ++m) {
+                    const int i = lane * per + m;
+                    ls[m] = i < C ? s.L[c * CS + i] : 0.f;
+                    lsum += ls[m];
+                }
+                float incl = lsum;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                float run = incl - lsum;
+                for (int m = 0; m < per; ++m) {
+                    const int i = lane * per + m;
+                    if (i < C) {
+                        s.Lx[c * CS + i] = run;
+                        run += ls[m];
+                        s.L[c * CS + i] = run;
                     }
-                    s.eta[c * CS + i] = eta;
-                    s.Lx[c * CS + i] = run;
-                    run += log1pf(-alpha);
-                    s.L[c * CS + i] = run;
                 }
             }
         } else if (tid < 32) {
@@ -312,29 +437,64 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             }
             for (int j = tid; j < C; j += kThreads) s.w[j] = s.kap[j] * expf(LC - s.L[j]);
         } else {
+            // Falcon-2, per column c: when the chunk's total log decay is at least -kFastL every factor
+            // e^{a - b} (a >= b) is formed as e^{a} e^{-b}, both finite, and w holds eta_j e^{-L_j}
+            // ("fast"); otherwise w holds eta_j e^{L_C - L_j} and the factors are formed one by one.
+            // Slot C of each column records which.
             for (int idx = tid; idx < C * DVS; idx += kThreads) {
                 const int j = idx / DVS, c = idx % DVS;
-                s.w[c * CS + j] = s.eta[c * CS + j] * expf(s.L[c * CS + C - 1] - s.L[c * CS + j]);
+                const float LC = s.L[c * CS + C - 1];
+                const bool fast = LC >= -kFastL;
+                s.w[c * CS + j] = s.eta[c * CS + j] * expf((fast ? 0.f : LC) - s.L[c * CS + j]);
+                if (j == 0) s.w[c * CS + C] = fast ? 1.f : 0.f;
             }
         }
         __syncthreads();
-        // ---- (5) merged-RHS forward substitution, column `col`, `gl` lanes per column
+        // ---- (5) merged-RHS forward substitution. Falcon-1 and -2: a half-warp per column, 16 rows at a
+        // time: each lane owns one row, first sums the earlier blocks' terms, then the block's rows are
+        // finished in order, each new r_j handed to the other lanes by a shuffle.
         if (VAR == kF1 || VAR == kF2) {
-            for (int i = 0; i < n; ++i) {
-                float acc = 0.f;
-                if (VAR == kF1) {
-                    for (int j = lg; j < i; j += gl) acc = fmaf(s.A[i * C + j], s.R[col * RS + j], acc);
-                } else {
-                    const float lxi = s.Lx[col * CS + i];
-                    for (int j = lg; j < i; j += gl)
-                        acc = fmaf(s.eta[col * CS + j] * expf(lxi - s.L[col * CS + j]) * s.G[i * NE + j],
-                                   s.R[col * RS + j], acc);
+            const int lane = tid & 31, li = lane & 15;
+            for (int cg = 0; cg < DVS; cg += 2 * (kThreads / 32)) {
+                const int cl = cg + 2 * (tid >> 5) + (lane >> 4);  // this half-warp's column
+                const bool cvalid = cl < DVS;
+                // Falcon-2 "fast" columns keep R~_j = eta_j e^{-L_j} r_j, with A_ij R_j = e^{Lx_i} G_ij R~_j
+                const bool fast = VAR == kF2 && cvalid && s.w[cl * CS + C] != 0.f;
+                auto coef = [&](int i, int j) -> float {  // the factor of the stored R_j (or R~_j) in row i
+                    if (VAR == kF1) return s.A[i * C + j];
+                    if (fast) return s.G[i * NE + j];
+                    return s.eta[cl * CS + j] * expf(s.Lx[cl * CS + i] - s.L[cl * CS + j]) * s.G[i * NE + j];
+                };
+                for (int b0 = 0; b0 < n; b0 += 16) {
+                    const int i = b0 + li;
+                    const bool row = cvalid && i < n;
+                    float acc = 0.f, dcy = 0.f, yv = 0.f, hv = 0.f, ca = 1.f;
+                    float cf[16];
+                    if (row) {
+                        for (int m = 0; m < b0; ++m) {  // earlier blocks; lanes start apart (no bank clash)
+                            int j = m + li;
+                            if (j >= b0) j -= b0;
+                            acc = fmaf(coef(i, j), s.R[cl * RS + j], acc);
+                        }
+                        dcy = expf(VAR == kF1 ? s.Lx[i] : s.Lx[cl * CS + i]);
+                        yv = s.Y[i * DVS + cl];
+                        hv = s.H[i * DVS + cl];
+                        if (fast) ca = s.w[cl * CS + i];
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) cf[jj] = (row && b0 + jj < i) ? coef(i, b0 + jj) : 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        float rv = 0.f;
+                        if (li == jj && row) {
+                            const float r = fast ? yv - dcy * (hv + acc) : (yv - dcy * hv) - acc;
+                            rv = ca * r;
+                            s.R[cl * RS + i] = rv;
+                        }
+                        rv = __shfl_sync(0xffffffffu, rv, jj, 16);
+                        acc = fmaf(cf[jj], rv, acc);
+                    }
                 }
-                for (int o = gl >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                const float dcy = (VAR == kF1) ? expf(s.Lx[i]) : expf(s.Lx[col * CS + i]);
-                const float r = (s.Y[i * DVS + col] - dcy * s.H[i * DVS + col]) - acc;
-                if (lg == 0) s.R[col * RS + i] = r;
-                __syncwarp();
             }
         } else if (VAR == kF3) {
             for (int i = 0; i < n; ++i) {
@@ -362,9 +522,16 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             float o;
             if (VAR == kF2) {
                 const float li = s.L[c * CS + i];
-                o = expf(li) * s.QS[idx];
-                for (int j = 0; j <= i; ++j)
-                    o = fmaf(s.eta[c * CS + j] * expf(li - s.L[c * CS + j]) * s.Sc[i * NE + j], s.R[c * RS + j], o);
+                if (s.w[c * CS + C] != 0.f) {  // fast: o = e^{L_i} (QS + sum_j Sc_ij R~_j)
+                    o = s.QS[idx];
+                    for (int j = 0; j <= i; ++j) o = fmaf(s.Sc[i * NE + j], s.R[c * RS + j], o);
+                    o *= expf(li);
+                } else {
+                    o = expf(li) * s.QS[idx];
+                    for (int j = 0; j <= i; ++j)
+                        o = fmaf(s.eta[c * CS + j] * expf(li - s.L[c * CS + j]) * s.Sc[i * NE + j], s.R[c * RS + j],
+                                 o);
+                }
             } else if (VAR == kF3) {
                 o = expf(s.L[i]) * s.QS[idx];
                 for (int l = 0; l <= i; ++l) {
@@ -393,8 +560,14 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                 }
                 s.S[idx] = fmaf(expf(s.L[C - 1]), s.S[idx], acc);
             } else if (VAR == kF2) {
-                for (int j = 0; j < n; ++j) acc = fmaf(s.X[j * XS + r] * s.w[c * CS + j], s.R[c * RS + j], acc);
-                s.S[idx] = fmaf(expf(s.L[c * CS + C - 1]), s.S[idx], acc);
+                const float gC = expf(s.L[c * CS + C - 1]);
+                if (s.w[c * CS + C] != 0.f) {  // fast: S' = e^{L_C} (S + sum_j x_j R~_j)
+                    for (int j = 0; j < n; ++j) acc = fmaf(s.X[j * XS + r], s.R[c * RS + j], acc);
+                    s.S[idx] = gC * (s.S[idx] + acc);
+                } else {
+                    for (int j = 0; j < n; ++j) acc = fmaf(s.X[j * XS + r] * s.w[c * CS + j], s.R[c * RS + j], acc);
+                    s.S[idx] = fmaf(gC, s.S[idx], acc);
+                }
             } else if (VAR == kF1A) {
                 for (int j = 0; j < n; ++j) acc = fmaf(s.X[j * XS + r] * s.w[j], s.Y[j * DVS + c], acc);
                 s.S[idx] = fmaf(expf(s.L[C - 1]), s.S[idx], acc);
