@@ -43,6 +43,7 @@ def _algorithmic_bytes(w, es):
     tail = BH * (w.window * w.dk + (w.window - 1) * w.dv) * es
     total = w.segments * (per_seg + tail)
     total += (w.segments - 1) * (BH * w.dk * w.dv * 4 + tail)  # S0 and tail read by later segments
+    total += (BH * w.dk * w.dv * 4 if w.nonzero_s0 else 0) + (tail if w.pos0 > 0 else 0)  # the first call's
     return total
 
 
@@ -159,11 +160,13 @@ def run_reference(args, w):
         sl = slice(s * w.seqlen, (s + 1) * w.seqlen)
         segs.append({n: inp[n][:bs, :, sl] for n in ("q", "k", "v", "beta", "lam")})
 
+    S_first, tail_first = _oracle_start(w, inp, bs)
+
     def step():
-        S, tail = None, None
+        S, tail = S_first, tail_first
         for s, x in enumerate(segs):
             _, S, tail = oracle.falcon_ref_fwd(w.variant_id, x["q"], x["k"], x["v"], x["beta"], x["lam"], S, tail,
-                                               pos=s * w.seqlen, window=w.window, eps=w.eps,
+                                               pos=w.pos0 + s * w.seqlen, window=w.window, eps=w.eps,
                                                eps_gamma=w.eps_gamma, nthreads=cores)
 
     for _ in range(args.warmup):
@@ -196,10 +199,11 @@ def cpu_baseline(w, budget_s=12.0):
     inp = I.make_inputs(w, seed=0)
     bs = 1
     x = {n: inp[n][:bs, :, :w.seqlen] for n in ("q", "k", "v", "beta", "lam")}
+    S0, tail = _oracle_start(w, inp, bs)
     runs, t0 = 0, time.perf_counter()
     while True:
-        oracle.falcon_ref_fwd(w.variant_id, x["q"], x["k"], x["v"], x["beta"], x["lam"], window=w.window,
-                              eps=w.eps, eps_gamma=w.eps_gamma, nthreads=cores)
+        oracle.falcon_ref_fwd(w.variant_id, x["q"], x["k"], x["v"], x["beta"], x["lam"], S0, tail, pos=w.pos0,
+                              window=w.window, eps=w.eps, eps_gamma=w.eps_gamma, nthreads=cores)
         runs += 1
         if time.perf_counter() - t0 > budget_s or runs >= 100000:
             break
@@ -208,6 +212,18 @@ def cpu_baseline(w, budget_s=12.0):
             "kind": "oracle",
             "sample": f"{runs} runs of batch row 0 ({w.heads} heads x {w.seqlen} tokens, first segment), "
                       f"{el:.1f} s"}
+
+
+def _oracle_start(w, inp, bs):
+    """The first call's S0 and tail, as the oracle takes them, for the first `bs` batch rows."""
+    import numpy as np
+
+    S0 = inp["S0"][:bs] if inp.get("S0") is not None else None
+    tail = None
+    if inp.get("tail") is not None:
+        keys = inp["tail"].view(w.batch, w.heads, 1, w.dk)[:bs].double().numpy()
+        tail = (keys, np.zeros((bs, w.heads, 0, w.dv)))
+    return S0, tail
 
 
 def _e2e(args, w, host_segs, dev_segs, launch, stream):
@@ -223,7 +239,7 @@ def _e2e(args, w, host_segs, dev_segs, launch, stream):
 
     def step():
         for s in range(w.segments):
-            for n in ("q", "k", "v", "beta", "lam"):
+            for n in hsegs[s]:
                 dev_segs[s][n].copy_(hsegs[s][n], non_blocking=True)
         launch(dev_segs, stream)
         for s in range(w.segments):
@@ -262,7 +278,7 @@ def run_ours(args, w):
     inp = I.make_inputs(w, seed=0)
     B, H, Ts, dk, dv, W = w.batch, w.heads, w.seqlen, w.dk, w.dv, w.window
     dims = [F.make_dims(B, H, Ts, dk, dv, window=W, dtype=F.FALCON_F32 if w.dtype == "f32" else F.FALCON_BF16,
-                        pos=s * Ts, eps=w.eps, eps_gamma=w.eps_gamma) for s in range(w.segments)]
+                        pos=w.pos0 + s * Ts, eps=w.eps, eps_gamma=w.eps_gamma) for s in range(w.segments)]
     kernel_id = F.falcon_kernel_for(w.variant_id, dims[0], w.chunk)
     if args.single_pass and kernel_id == 3:
         kernel_id = 2
@@ -273,7 +289,10 @@ def run_ours(args, w):
 
     def seg_inputs(s):
         sl = slice(s * Ts, (s + 1) * Ts)
-        return {n: inp[n][:, :, sl].contiguous() for n in ("q", "k", "v", "beta", "lam")}
+        d = {n: inp[n][:, :, sl].contiguous() for n in ("q", "k", "v", "beta", "lam")}
+        if s == 0:  # a workload that starts from a given state and tail
+            d.update({n: inp[n].contiguous() for n in ("S0", "tail") if inp.get(n) is not None})
+        return d
 
     host_segs = [seg_inputs(s) for s in range(w.segments)]
     sets = []
@@ -293,8 +312,9 @@ def run_ours(args, w):
     def launch(segs, strm):
         for s, d in enumerate(segs):
             prev = segs[s - 1] if s > 0 else None
-            st = F.falcon_fwd(w.variant_id, d["q"], d["k"], d["v"], d["beta"], d["lam"],
-                              prev["S"] if prev else None, prev["tail_out"] if prev else None,
+            S0 = prev["S"] if prev else d.get("S0")
+            tail = prev["tail_out"] if prev else d.get("tail")
+            st = F.falcon_fwd(w.variant_id, d["q"], d["k"], d["v"], d["beta"], d["lam"], S0, tail,
                               d["out"], d["S"], d["tail_out"], dims[s], w.chunk, ws, stream=strm.cuda_stream)
             if st != 0:
                 raise F.FalconError(st)
@@ -359,7 +379,9 @@ def run_ours(args, w):
                    "segments": w.segments, "d": dk, "chunk": w.chunk, "window": W,
                    "parallelism": f"dp{world} (independent sequences per GPU, no collective)",
                    "l2": f"rotating {nsets} input/output sets of {step_bytes / 1e6:.1f} MB (> L2 between reuses)",
+                   "pos0": w.pos0,
                    "kernel": {1: "cuda-core chunk kernel", 2: "single-pass tcgen05/TMA chunk kernel",
+                              4: "single-token kernel",
                               3: "split path: tcgen05/TMA prep, chain and output kernels"}.get(kernel_id, "?")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "scope": "one falcon_fwd call (all kernels it launches); per-kernel shares in profiles/",

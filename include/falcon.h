@@ -20,6 +20,9 @@
  * §H.3): per chunk one unit-lower-triangular solve with the value and the
  * projected-history right-hand sides merged, log-prefix decay reset to 0 at
  * every chunk start ([PL] §D.1, §G.1), and a carried state between chunks.
+ * A call with T = 1 (Falcon-1, 1A, 2; dk = dv = 64) runs a single-token kernel instead: the recurrent
+ * form of the same update, one (batch, head) state per CTA, so a decoding step costs one read and
+ * one write of the state ([PL] §3; [AH] Method).
  * Falcon-1 and 1A at bf16, dk = dv = 64, chunk 64 also have a split path that
  * uses a caller-provided workspace: every chunk's state-independent part
  * (the solve and the chunk transition S -> M S + U it implies) is computed for
@@ -117,7 +120,7 @@ int falcon_fwd(int variant, const void* q, const void* k, const void* v, const f
                size_t workspace_bytes, void* stream);
 
 /* Workspace bytes that enable the split path of falcon_fwd for these arguments
- * (B*H*ceil(T/64) * (66 KiB + 8 bytes) for Falcon-1/1A, bf16, dk = dv = 64, chunk 64; 0 when
+ * (B*H*ceil(T/64) * (66 KiB + 8 bytes) for Falcon-1/1A, bf16, dk = dv = 64, chunk 64, T > 1; 0 when
  * no path uses a workspace or the arguments are invalid). Host only. */
 size_t falcon_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk);
 
@@ -156,7 +159,8 @@ int falcon_device_status(void* stream);
 /* Which kernels falcon_fwd launches for these arguments when it is given
  * falcon_workspace_bytes() of workspace (0 = none/invalid, 1 = CUDA-core chunk
  * kernel, 2 = single-pass tcgen05/TMA chunk kernel, 3 = split path: prep, chain
- * and output kernels). Without a workspace, 3 becomes 2. Host only, no launch. */
+ * and output kernels, 4 = single-token kernel for T = 1, workspace or not).
+ * Without a workspace, 3 becomes 2. Host only, no launch. */
 int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk);
 
 /* ABI version of this header: 2. */

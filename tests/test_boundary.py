@@ -143,6 +143,11 @@ def test_unsupported_and_invalid_shapes(lib):
     (dict(dtype=F.FALCON_F32), 1),
     (dict(variant=F.FALCON_2), 1),
     (dict(dk=32, dv=32), 1),
+    (dict(seqlen=1), 4),                                  # one token: the single-token kernel
+    (dict(seqlen=1, variant=F.FALCON_1A, dtype=F.FALCON_F32), 4),
+    (dict(seqlen=1, variant=F.FALCON_2), 4),
+    (dict(seqlen=1, dk=32, dv=32), 1),
+    (dict(seqlen=2), 3),
 ])
 def test_kernel_choice(lib, case, expect):
     c = dict(variant=F.FALCON_1, seqlen=1024, dk=64, dv=64, dtype=F.FALCON_BF16, chunk=64)
@@ -161,6 +166,7 @@ def test_workspace_bytes(lib):
     assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 64, 64, 64, dtype=F.FALCON_F32), 64) == 0
     assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 64, 64, 64), 32) == 0
     assert F.falcon_workspace_bytes(F.FALCON_2A, F.make_dims(2, 3, 64, 64, 64), 64) == 0
+    assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(8, 12, 1, 64, 64), 64) == 0  # single-token kernel
 
 
 def test_workspace_checks(lib):

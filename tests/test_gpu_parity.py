@@ -43,10 +43,20 @@ def _check(name, gpu, ref, dtype, bound=None):
 
 
 def _parity(w: I.Workload, inp, *, chunk=None, S0=None, name=""):
+    """GPU against the oracle on `inp`; a workload that starts after pos0 tokens starts from its drawn
+    state and tail."""
     chunk = chunk or w.chunk
-    out, S, tail = run_gpu(w.variant_id, inp, window=w.window, chunk=chunk, S0=S0, eps=w.eps,
+    pos, tail0, rtail0 = 0, None, None
+    if w.pos0 > 0 and inp.get("tail") is not None:
+        B, H, _, dk = inp["q"].shape
+        pos, tail0 = w.pos0, inp["tail"][: B * H * dk]
+        rtail0 = (tail0.view(B, H, 1, dk).double().numpy(), np.zeros((B, H, 0, inp["v"].shape[-1])))
+        if S0 is None and inp.get("S0") is not None:
+            S0 = inp["S0"][:B]
+    out, S, tail = run_gpu(w.variant_id, inp, window=w.window, chunk=chunk, S0=S0, tail=tail0, pos=pos, eps=w.eps,
                            eps_gamma=w.eps_gamma)
-    r_out, r_S, r_tail = run_oracle(w.variant_id, inp, window=w.window, S0=S0, eps=w.eps, eps_gamma=w.eps_gamma)
+    r_out, r_S, r_tail = run_oracle(w.variant_id, inp, window=w.window, S0=S0, tail=rtail0, pos=pos, eps=w.eps,
+                                    eps_gamma=w.eps_gamma)
     _check(f"{name} out", out, r_out, w.torch_dtype)
     _check(f"{name} S_final", S, r_S, torch.float32 if w.dtype == "f32" else w.torch_dtype)
     B, H, T, dk = inp["q"].shape

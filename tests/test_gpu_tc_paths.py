@@ -49,7 +49,9 @@ def _wl(variant, **kw):
 def _both(variant, inp, split, name, S0=None, pos=0, tail=None, eps_gamma=1e-6):
     dims = F.make_dims(*inp["q"].shape[:3], 64, 64, dtype=F.FALCON_BF16, pos=pos)
     expect = 3 if split else 2
-    if inp["q"].shape[2] > 0:
+    if inp["q"].shape[2] == 1:  # one token: the single-token kernel, with or without a workspace
+        assert F.falcon_kernel_for(variant, dims, 64) == 4
+    elif inp["q"].shape[2] > 0:
         assert (F.falcon_kernel_for(variant, dims, 64) if split else 2) == expect
     out, S, t = run_gpu(variant, inp, chunk=64, S0=S0, pos=pos, tail=tail, eps_gamma=eps_gamma, split=split)
     return out, S, t

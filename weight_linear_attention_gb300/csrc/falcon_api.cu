@@ -49,6 +49,13 @@ size_t tail_bytes_of(const falcon_dims_t* d) {
 }
 
 // Shape/variant/dtype/chunk checks (no pointers). Fills the size fields of `a`.
+// Workspace bytes a call with these (validated) arguments can use: the split path's, unless the
+// single-token kernel runs.
+size_t workspace_need(const falcon::Launch& a) {
+    if (falcon::decode_supported(a) || !falcon::split_supported(a)) return 0;
+    return falcon::split_workspace_bytes(a);
+}
+
 int validate_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail, falcon::Launch* a) {
     if (!d) return FALCON_ERR_INVALID_ARG;
     if (variant == FALCON_2A || variant == FALCON_3A) return FALCON_ERR_UNSUPPORTED;
@@ -97,7 +104,7 @@ int validate(int variant, const void* q, const void* k, const void* v, const flo
         if (p && !aligned(p, 16)) return FALCON_ERR_MISALIGNED;
     if ((beta && !aligned(beta, 4)) || (lambda && !aligned(lambda, 4))) return FALCON_ERR_MISALIGNED;
     if (ws && !aligned(ws, 256)) return FALCON_ERR_MISALIGNED;
-    const size_t ws_need = falcon::split_supported(*a) ? falcon::split_workspace_bytes(*a) : 0;
+    const size_t ws_need = workspace_need(*a);
     if (ws && ws_need > 0 && ws_bytes < ws_need) return FALCON_ERR_INVALID_ARG;
 
     // out must not overlap any input; tail_out must not overlap tail; S_final may equal S0 exactly.
@@ -178,6 +185,7 @@ const char* falcon_status_string(int s) {
 int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk) {
     falcon::Launch a = {};
     if (validate_shape(variant, dims, chunk, dims && dims->pos > 0, &a) != FALCON_OK) return 0;
+    if (falcon::decode_supported(a)) return 4;
     if (falcon::split_supported(a) && falcon::split_workspace_bytes(a) > 0) return 3;
     return falcon::tc_supported(a) ? 2 : 1;
 }
@@ -185,7 +193,7 @@ int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk) {
 size_t falcon_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk) {
     falcon::Launch a = {};
     if (validate_shape(variant, dims, chunk, dims && dims->pos > 0, &a) != FALCON_OK) return 0;
-    return falcon::split_supported(a) ? falcon::split_workspace_bytes(a) : 0;
+    return workspace_need(a);
 }
 
 int falcon_fwd(int variant, const void* q, const void* k, const void* v, const float* beta, const float* lambda,
@@ -197,6 +205,7 @@ int falcon_fwd(int variant, const void* q, const void* k, const void* v, const f
     if (st != FALCON_OK) return st;
     if (a.B * a.H == 0) return FALCON_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (falcon::decode_supported(a)) return falcon::launch_decode(a, s);
     if (a.ws) return falcon::launch_split(a, s);
     if (falcon::tc_supported(a)) return falcon::launch_tc(a, s);
     return falcon::launch_generic(a, s);
@@ -208,7 +217,7 @@ int falcon_fwd_static(int variant, const void* q, const void* k, const void* v, 
     falcon::Launch shape = {};
     const int st = validate_shape(variant, dims, chunk, tail != nullptr, &shape);
     if (st != FALCON_OK) return st;
-    const size_t need = falcon::split_supported(shape) ? falcon::split_workspace_bytes(shape) : 0;
+    const size_t need = workspace_need(shape);
     if (need > FALCON_STATIC_WORKSPACE_BYTES) return FALCON_ERR_UNSUPPORTED;
     void* ws = nullptr;
     if (need > 0 && !(ws = static_workspace_address())) return FALCON_ERR_CUDA;

@@ -49,4 +49,8 @@ size_t split_workspace_bytes(const Launch& a);
 int launch_split(const Launch& a, cudaStream_t stream);
 int split_consume_timeout_flag(int* flag);
 
+// Single-token step (T = 1; Falcon-1, 1A and 2; dk = dv = 64): one CTA per (batch, head) state.
+bool decode_supported(const Launch& a);
+int launch_decode(const Launch& a, cudaStream_t stream);
+
 }  // namespace falcon

@@ -18,6 +18,8 @@ Recipe (every workload, seed 0 unless a caller passes another):
   v: cast to the dtype directly. beta = sigmoid(logit); lambda = sigmoid(logit +
   shift) or a constant. beta and lambda stay fp32. S0 = N(0,1)/sqrt(dk) in fp32,
   so that the first reads S0^T q have the values' unit scale.
+  A workload that starts after pos0 > 0 earlier tokens (window 1) also draws, last, the pending key
+  k_pos0 [B,H,1,dk] (RMS-normed like k), which is its tail.
 """
 
 from __future__ import annotations
@@ -48,6 +50,7 @@ class Workload:
     eps_gamma: float = 1e-6
     segments: int = 1                # the sequence is `segments` calls of `seqlen` tokens
     nonzero_s0: bool = False
+    pos0: int = 0                    # tokens consumed before the first call (needs a tail; window 1)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -79,6 +82,9 @@ WORKLOADS = {
                                    lam_const=0.01),
     "f3w4_b2h12t16384_bf16": Workload("f3w4_b2h12t16384_bf16", "falcon3", 2, 12, 8192, 64, 64, "bf16", 32,
                                       window=4, lam_shift=-2.0, segments=2),
+    # one decoding step of 256 sequences (12 heads of 64) after 1024 tokens: the recurrent form
+    "f1_decode_b256h12_bf16": Workload("f1_decode_b256h12_bf16", "falcon1", 256, 12, 1, 64, 64, "bf16", 64,
+                                       lam_shift=-4.0, nonzero_s0=True, pos0=1024),
 }
 
 HEADLINE = "f1_b8h12t1024_bf16"
@@ -106,6 +112,8 @@ def make_inputs(w: Workload, seed: int = 0, seqlen: int | None = None, batch: in
     beta_logit = torch.randn(*bshape, generator=g)
     lam_logit = torch.randn(B, H, T, generator=g)
     S0 = torch.randn(B, H, dk, dv, generator=g) / dk ** 0.5 if w.nonzero_s0 else None
+    assert w.pos0 == 0 or w.window == 1, "a starting tail is drawn for window 1 only"
+    tail_k = torch.randn(B, H, 1, dk, generator=g) if w.pos0 > 0 else None
     dt = w.torch_dtype
     out = {
         "q": _rmsnorm(q).to(dt),
@@ -115,5 +123,6 @@ def make_inputs(w: Workload, seed: int = 0, seqlen: int | None = None, batch: in
         "lam": (torch.full((B, H, T), float(w.lam_const)) if w.lam_const is not None
                 else torch.sigmoid(lam_logit + float(w.lam_shift))).float().contiguous(),
         "S0": S0,
+        "tail": _rmsnorm(tail_k).to(dt).reshape(-1).contiguous() if tail_k is not None else None,
     }
     return out
