@@ -22,7 +22,9 @@ namespace falcon {
 namespace {
 
 constexpr int kD = 64;
-constexpr int kThreads = 256;  // thread t: columns 4 (t % 16) .. + 3, rows 4 (t / 16) .. + 3
+constexpr int kThreads = 128;  // thread t: columns 4 (t % 16) .. + 3, rows kRows (t / 16) .. + kRows - 1
+constexpr int kRows = kD * 16 / kThreads;
+constexpr int kGroups = kThreads / 16;  // row groups
 
 struct DParams {
     const void* q;
@@ -54,20 +56,20 @@ __device__ __forceinline__ void set(float4& v, int j, float x) {
 template <typename Tin, int VAR>
 __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p) {
     __shared__ float xs[kD], qs[kD], ys[kD], rs[kD], eta_s[kD], gam_s[kD];
-    __shared__ float part[kThreads / 16][kD];
+    __shared__ float part[kGroups][kD];
     __shared__ float nx_s;
     const int tid = threadIdx.x, lane = tid & 31;
     const long long bh = blockIdx.x;
-    const int cq = tid & 15, rg = tid >> 4, c0 = 4 * cq, r0 = 4 * rg;
+    const int cq = tid & 15, rg = tid >> 4, c0 = 4 * cq, r0 = kRows * rg;
     const Tin* q = static_cast<const Tin*>(p.q) + bh * kD;
     const Tin* k = static_cast<const Tin*>(p.k) + bh * kD;
     const Tin* v = static_cast<const Tin*>(p.v) + bh * kD;
     const bool first = p.pos == 0;  // tau = 1: x = 0, eta = alpha = 0
 
-    // ---- the state tile of this thread (rows r0 .. r0 + 3, columns c0 .. c0 + 3)
-    float4 sv[4];
+    // ---- the state tile of this thread (rows r0 .. r0 + kRows - 1, columns c0 .. c0 + 3)
+    float4 sv[kRows];
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
+    for (int m = 0; m < kRows; ++m)
         sv[m] = p.S0 ? *reinterpret_cast<const float4*>(p.S0 + (bh * kD + r0 + m) * kD + c0)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid < kD) {
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p
         for (int j = 0; j < 4; ++j) {
             float a = 0.f;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) a = fmaf(get(sv[m], j), xs[r0 + m], a);
+            for (int m = 0; m < kRows; ++m) a = fmaf(get(sv[m], j), xs[r0 + m], a);
             part[rg][c0 + j] = a;
         }
     }
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p
         float a = 0.f;
         if (VAR != kF1A)
 #pragma unroll
-            for (int g = 0; g < kThreads / 16; ++g) a += part[g][tid];
+            for (int g = 0; g < kGroups; ++g) a += part[g][tid];
         rs[tid] = ys[tid] - a;
     }
     __syncthreads();
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p
         const float g = gam_s[c], er = eta_s[c] * rs[c];
         float a = 0.f;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < kRows; ++m) {
             const float s = fmaf(g, get(sv[m], j), er * xs[r0 + m]);
             set(sv[m], j, s);
             a = fmaf(s, qs[r0 + m], a);
@@ -133,12 +135,12 @@ __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p
     }
     if (p.S_final)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) *reinterpret_cast<float4*>(p.S_final + (bh * kD + r0 + m) * kD + c0) = sv[m];
+        for (int m = 0; m < kRows; ++m) *reinterpret_cast<float4*>(p.S_final + (bh * kD + r0 + m) * kD + c0) = sv[m];
     __syncthreads();
     if (tid < kD) {
         float a = 0.f;
 #pragma unroll
-        for (int g = 0; g < kThreads / 16; ++g) a += part[g][tid];
+        for (int g = 0; g < kGroups; ++g) a += part[g][tid];
         stf(static_cast<Tin*>(p.out) + bh * kD + tid, a);
     }
 }
