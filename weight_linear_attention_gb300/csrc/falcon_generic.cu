@@ -75,37 +75,61 @@ __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat16
 __device__ __forceinline__ void stf(float* p, float x) { *p = x; }
 __device__ __forceinline__ void stf(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-// Largest eigenvalue of a small symmetric matrix (n <= kMaxW), cyclic Jacobi in fp32.
-__device__ float lambda_max_small(float (*a)[kMaxW], int n) {
+// Largest eigenvalue of a small symmetric matrix, cyclic Jacobi in fp32 on an N x N matrix held in
+// registers (every index a compile-time constant), until the off-diagonal mass is 1e-12 of the
+// diagonal's: convergence is quadratic, so a few sweeps; the eigenvalue's error is second order in
+// the off-diagonal part, far below fp32 rounding.
+template <int N>
+__device__ float lambda_max_fixed(float (&a)[N][N]) {
     for (int sweep = 0; sweep < 16; ++sweep) {
         float off = 0.f, dg = 0.f;
-        for (int p = 0; p < n; ++p) {
+#pragma unroll
+        for (int p = 0; p < N; ++p) {
             dg += a[p][p] * a[p][p];
-            for (int r = p + 1; r < n; ++r) off += a[p][r] * a[p][r];
+#pragma unroll
+            for (int r = p + 1; r < N; ++r) off += a[p][r] * a[p][r];
         }
-        if (off <= 1e-14f * dg || off == 0.f) break;
-        for (int p = 0; p < n; ++p)
-            for (int r = p + 1; r < n; ++r) {
-                float apq = a[p][r];
+        if (off <= 1e-12f * dg || off == 0.f) break;
+#pragma unroll
+        for (int p = 0; p < N; ++p)
+#pragma unroll
+            for (int r = p + 1; r < N; ++r) {
+                const float apq = a[p][r];
                 if (apq == 0.f) continue;
-                float th = (a[r][r] - a[p][p]) / (2.f * apq);
-                float t = (th >= 0.f ? 1.f : -1.f) / (fabsf(th) + sqrtf(th * th + 1.f));
-                float c = rsqrtf(t * t + 1.f), s = t * c;
-                for (int m = 0; m < n; ++m) {
-                    float x = a[m][p], y = a[m][r];
-                    a[m][p] = c * x - s * y;
-                    a[m][r] = s * x + c * y;
+                const float th = (a[r][r] - a[p][p]) / (2.f * apq);
+                const float t = (th >= 0.f ? 1.f : -1.f) / (fabsf(th) + sqrtf(th * th + 1.f));
+                const float c = rsqrtf(t * t + 1.f), sn = t * c;
+#pragma unroll
+                for (int m = 0; m < N; ++m) {
+                    const float x = a[m][p], y = a[m][r];
+                    a[m][p] = c * x - sn * y;
+                    a[m][r] = sn * x + c * y;
                 }
-                for (int m = 0; m < n; ++m) {
-                    float x = a[p][m], y = a[r][m];
-                    a[p][m] = c * x - s * y;
-                    a[r][m] = s * x + c * y;
+#pragma unroll
+                for (int m = 0; m < N; ++m) {
+                    const float x = a[p][m], y = a[r][m];
+                    a[p][m] = c * x - sn * y;
+                    a[r][m] = sn * x + c * y;
                 }
             }
     }
     float mx = a[0][0];
-    for (int p = 1; p < n; ++p) mx = fmaxf(mx, a[p][p]);
+#pragma unroll
+    for (int p = 1; p < N; ++p) mx = fmaxf(mx, a[p][p]);
     return mx;
+}
+
+// lambda_max of (1/nb) [G_{slots[x], slots[y]}] (a window's averaged Gram, PSD), zero-padded to N:
+// the padding adds zero eigenvalues only.
+template <int N>
+__device__ float window_lambda_max(const float* G, int ld, const int* slots, int nb) {
+    float a[N][N];
+    const float inv = 1.f / (float)nb;
+#pragma unroll
+    for (int x = 0; x < N; ++x)
+#pragma unroll
+        for (int y = 0; y < N; ++y) a[x][y] = (x < nb && y < nb) ? G[slots[x] * ld + slots[y]] * inv : 0.f;
+    return lambda_max_fixed<N>(a);
 }
 
 // d += A (16 x 16, row-major bf16) * B (16 x 8, column-major bf16), fp32 accumulators.
@@ -232,8 +256,6 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         s.S[idx] = p.S0 ? p.S0[(bh * DK + r) * DV + c0 + c] : 0.f;
     }
 
-    const int gl = kThreads / DVS;  // lanes cooperating on one column in the solve
-    const int col = tid / gl, lg = tid % gl;
 
     for (long long t0 = 0; t0 < T; t0 += C) {
         const int n = (int)min((long long)C, T - t0);
@@ -376,15 +398,22 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                     const long long tau = pos + t0 + i + 1;
                     const float lm = lam[t0 + i];
                     if (VAR == kF3) {
-                        float a[kMaxW][kMaxW];
-                        int slots[kMaxW];
+                        int slots[kMaxW] = {};
                         int nb = 0;
                         for (int sl = 0; sl < W; ++sl)
                             if (tau - sl >= 2) slots[nb++] = i - sl + W - 1;
                         if (nb > 0) {
-                            for (int x = 0; x < nb; ++x)
-                                for (int y = 0; y < nb; ++y) a[x][y] = s.G[slots[x] * NE + slots[y]] / (float)nb;
-                            const float mu = lambda_max_small(a, nb);
+                            float mu;
+                            switch (W) {  // the matrix in registers: one instance per window size
+                                case 1: mu = s.G[slots[0] * NE + slots[0]]; break;
+                                case 2: mu = window_lambda_max<2>(s.G, NE, slots, nb); break;
+                                case 3: mu = window_lambda_max<3>(s.G, NE, slots, nb); break;
+                                case 4: mu = window_lambda_max<4>(s.G, NE, slots, nb); break;
+                                case 5: mu = window_lambda_max<5>(s.G, NE, slots, nb); break;
+                                case 6: mu = window_lambda_max<6>(s.G, NE, slots, nb); break;
+                                case 7: mu = window_lambda_max<7>(s.G, NE, slots, nb); break;
+                                default: mu = window_lambda_max<8>(s.G, NE, slots, nb); break;
+                            }
                             const float den = mu + lm + p.eps;
                             eta = den == 0.f ? 0.f : beta[t0 + i] / den;
                             alpha = fminf(eta * lm, 1.f - p.eps_gamma);
@@ -497,20 +526,49 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                 }
             }
         } else if (VAR == kF3) {
-            for (int i = 0; i < n; ++i) {
-                const float dcy = expf(s.Lx[i]);
-                for (int a = 0; a < W; ++a) {
+            // Unknowns r_{i,a} (token i, window slot a) depend only on earlier tokens, so a token's W
+            // slots are finished together: a half-warp per column takes 16 / W tokens at a time, one
+            // lane per unknown, sums the earlier blocks' terms in parallel, then finishes the block
+            // token by token, each token's W values passed to the other lanes by shuffles.
+            const int lane = tid & 31, li = lane & 15, TPB = 16 / W, NU = TPB * W;
+            for (int cg = 0; cg < DVS; cg += 2 * (kThreads / 32)) {
+                const int cl = cg + 2 * (tid >> 5) + (lane >> 4);
+                const bool cvalid = cl < DVS;
+                for (int b0 = 0; b0 < n; b0 += TPB) {
+                    const int i = b0 + li / W, a = li % W;
+                    const bool row = cvalid && li < NU && i < n;
                     const int pa = i - a + W - 1;
-                    const bool valid = pos + t0 + i + 1 - a >= 2;
-                    float acc = 0.f;
-                    for (int m = lg; m < i * W; m += gl) {
-                        const int l = m / W, b = m % W;
-                        acc = fmaf(s.A[i * C + l] * s.G[pa * NE + (l - b + W - 1)], s.R[col * RS + m], acc);
+                    float acc = 0.f, dcy = 0.f, yv = 0.f, hv = 0.f;
+                    bool valid = false;
+                    if (row) {
+                        // the earlier blocks' tokens l, lanes starting apart (no bank clash)
+                        const int l0 = b0 > 0 ? li % b0 : 0;
+                        for (int ll = 0; ll < b0; ++ll) {
+                            int l = ll + l0;
+                            if (l >= b0) l -= b0;
+                            const float al = s.A[i * C + l];
+                            const float* gr = s.G + pa * NE + l + W - 1;  // G[pa][l - bb + W - 1]
+                            const float* rr = s.R + cl * RS + l * W;
+                            for (int bb = 0; bb < W; ++bb) acc = fmaf(al * gr[-bb], rr[bb], acc);
+                        }
+                        dcy = expf(s.Lx[i]);
+                        yv = s.Y[pa * DVS + cl];
+                        hv = s.H[pa * DVS + cl];
+                        valid = pos + t0 + i + 1 - a >= 2;
                     }
-                    for (int o = gl >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                    const float r = valid ? (s.Y[pa * DVS + col] - dcy * s.H[pa * DVS + col]) - acc : 0.f;
-                    if (lg == 0) s.R[col * RS + i * W + a] = r;
-                    __syncwarp();
+                    for (int st = 0; st < TPB; ++st) {
+                        const int tok = b0 + st;
+                        float rv = 0.f;
+                        if (row && i == tok) {
+                            rv = valid ? (yv - dcy * hv) - acc : 0.f;
+                            s.R[cl * RS + i * W + a] = rv;
+                        }
+                        const float ai = (row && i > tok) ? s.A[i * C + tok] : 0.f;
+                        for (int bb = 0; bb < W; ++bb) {
+                            const float vb = __shfl_sync(0xffffffffu, rv, st * W + bb, 16);
+                            if (row && i > tok) acc = fmaf(ai * s.G[pa * NE + (tok - bb + W - 1)], vb, acc);
+                        }
+                    }
                 }
             }
         }
