@@ -29,7 +29,7 @@ _SRC = os.path.join(_HERE, "falcon_ref.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libfalcon_ref.so")
 
-FALCON_1, FALCON_1A, FALCON_2, FALCON_3 = 1, 2, 3, 5
+FALCON_1, FALCON_1A, FALCON_2, FALCON_2A, FALCON_3, FALCON_3A = 1, 2, 3, 4, 5, 6
 
 _lock = threading.Lock()
 _lib = None
@@ -96,7 +96,7 @@ def falcon_ref_fwd(variant, q, k, v, beta, lam, S0=None, tail=None, *, pos=0, wi
                    eps=1e-6, eps_gamma=1e-6, nthreads=None):
     """Run the fp64 recurrence.
 
-    q, k: [B,H,T,dk]; v: [B,H,T,dv]; beta: [B,H,T] (Falcon-2: [B,H,T,dv]);
+    q, k: [B,H,T,dk]; v: [B,H,T,dv]; beta: [B,H,T] (Falcon-2, 2A: [B,H,T,dv]);
     lam: [B,H,T]; S0: [B,H,dk,dv] or None; tail: (keys [B,H,W,dk] holding
     k_{pos-W+1..pos}, vals [B,H,W-1,dv] holding v_{pos-W+2..pos}) or None iff
     pos == 0. Returns (out [B,H,T,dv], S_final [B,H,dk,dv], (tail_keys, tail_vals))
@@ -113,7 +113,7 @@ def falcon_ref_fwd(variant, q, k, v, beta, lam, S0=None, tail=None, *, pos=0, wi
         assert tv.shape == (B, H, W - 1, dv), tv.shape
     assert k.shape == (B, H, T, dk) and v.shape == (B, H, T, dv)
     assert lam.shape == (B, H, T)
-    if variant == FALCON_2:
+    if variant in (FALCON_2, FALCON_2A):
         assert beta.shape == (B, H, T, dv)
     else:
         assert beta.shape == (B, H, T)

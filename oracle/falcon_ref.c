@@ -34,6 +34,13 @@
  *                         S = gamma S + (eta/B) sum_j x_j r_j^T
  *                                                          [PL §4.4; PL §C.6 "exact top eigenvalue";
  *                                                           AH Method; SG step-size paragraph]
+ *   Falcon-2A             per value column c, the Falcon-1A write with eta_c = beta_c/den and
+ *                         gamma_c from eta_c: S[:,c] = gamma_c S[:,c] + eta_c x y_c
+ *                                                          [PL §4.3 "the A family"; PL "B. Falcon-2A"]
+ *   Falcon-3A             the Falcon-3 window, written with the targets themselves:
+ *                         E = (1/B) sum_{j in I} ||x_j||^2 (the window's mean key energy),
+ *                         eta = beta/(E + lambda + eps), S = gamma S + (eta/B) sum_j x_j y_j^T
+ *                                                          [PL §4.3; PL §4.5; PL §4.6; PL "C. Falcon-3A"]
  *   read                  o_tau = S_tau^T q_tau (read after write)  [AH Method; SG RAW paragraph]
  *   continuation tail     the last W keys and last W-1 values, so that the next
  *                         segment's first pair and window are exact  [PL §C.7; PL §4.4]
@@ -43,7 +50,9 @@
  * S_t, which contradicts PL §4.4, AH and SG); the sentinel pair j = 1 is not a
  * member of the Falcon-3 window (PL §4.5 "skips the boundary update at t = 1");
  * Falcon-2 shares the denominator ||x||^2 + lambda + eps across columns and
- * only beta is per column; the tail also carries the pending key k_T.
+ * only beta is per column (so does Falcon-2A); the tail also carries the pending key k_T; the
+ * pages normalise Falcon-3A's step by the "window energy" without printing it: read here as the
+ * mean of ||x_j||^2 over the window, which keeps W = 1 equal to Falcon-1A and does not grow with W.
  *
  * Arithmetic: plain fp64, token by token, no reassociation tricks. Compile
  * without -ffast-math.
@@ -57,7 +66,9 @@
 #define REF_F1 1
 #define REF_F1A 2
 #define REF_F2 3
+#define REF_F2A 4
 #define REF_F3 5
+#define REF_F3A 6
 
 #define REF_OK 0
 #define REF_EINVAL 1
@@ -154,7 +165,7 @@ static void run_sequence(seq_job *j) {
         const int64_t tau = j->pos + t + 1;
         const double lam = j->lam[t];
         const double *y = j->v + t * dv;
-        if (j->variant == REF_F3) {
+        if (j->variant == REF_F3 || j->variant == REF_F3A) {
             int64_t jlo = tau - W + 1;
             if (jlo < 2) jlo = 2;
             const int64_t B = tau >= 2 ? tau - jlo + 1 : 0;
@@ -169,16 +180,23 @@ static void run_sequence(seq_job *j) {
                         for (int64_t c = 0; c < dk; ++c) g += xs[a][c] * xs[b][c];
                         gram[a * B + b] = g / (double)B;
                     }
-                const double mu = jacobi_lambda_max((int)B, gram);
+                double mu;
+                if (j->variant == REF_F3) {
+                    mu = jacobi_lambda_max((int)B, gram);
+                } else { /* Falcon-3A: the window's mean key energy, the trace of the averaged Gram */
+                    mu = 0.0;
+                    for (int64_t a = 0; a < B; ++a) mu += gram[a * B + a];
+                }
                 const double den = mu + lam + j->eps;
                 const double eta = den == 0.0 ? 0.0 : j->beta[t] / den;
                 double alpha = eta * lam;
                 if (alpha > 1.0 - j->eps_gamma) alpha = 1.0 - j->eps_gamma;
                 const double gamma = 1.0 - alpha;
-                for (int64_t a = 0; a < B; ++a)       /* all residuals at S_{tau-1} */
+                for (int64_t a = 0; a < B; ++a)       /* residuals at S_{tau-1} (Falcon-3A: the targets) */
                     for (int64_t c = 0; c < dv; ++c) {
                         double p = 0.0;
-                        for (int64_t r = 0; r < dk; ++r) p += S[r * dv + c] * xs[a][r];
+                        if (j->variant == REF_F3)
+                            for (int64_t r = 0; r < dk; ++r) p += S[r * dv + c] * xs[a][r];
                         res[a * dv + c] = ys[a][c] - p;
                     }
                 const double w = eta / (double)B;
@@ -194,15 +212,16 @@ static void run_sequence(seq_job *j) {
             double nx = 0.0;
             for (int64_t r = 0; r < dk; ++r) nx += x[r] * x[r];
             const double den = nx + lam + j->eps;
-            if (j->variant == REF_F2) {
+            if (j->variant == REF_F2 || j->variant == REF_F2A) {
                 const double *bt = j->beta + t * dv;
                 for (int64_t c = 0; c < dv; ++c) {
                     const double eta = den == 0.0 ? 0.0 : bt[c] / den;
                     double alpha = eta * lam;
                     if (alpha > 1.0 - j->eps_gamma) alpha = 1.0 - j->eps_gamma;
                     const double gamma = 1.0 - alpha;
-                    double p = 0.0;
-                    for (int64_t r = 0; r < dk; ++r) p += S[r * dv + c] * x[r];
+                    double p = 0.0; /* Falcon-2A writes the target itself */
+                    if (j->variant == REF_F2)
+                        for (int64_t r = 0; r < dk; ++r) p += S[r * dv + c] * x[r];
                     const double rc = y[c] - p;
                     for (int64_t r = 0; r < dk; ++r) S[r * dv + c] = gamma * S[r * dv + c] + eta * x[r] * rc;
                 }
@@ -266,12 +285,13 @@ static void *worker(void *arg) {
 /*
  * Arrays are contiguous fp64 in the layouts below ([B,H,...] outermost).
  *   q, k: [B,H,T,dk]   v: [B,H,T,dv]   beta: [B,H,T] (Falcon-2: [B,H,T,dv])
+ *   (Falcon-2A: [B,H,T,dv] as well)
  *   lam: [B,H,T]       S0: [B,H,dk,dv] or NULL (zero state)
  *   tail_k: [B,H,W,dk] holding k_{pos-W+1..pos}; tail_v: [B,H,W-1,dv] holding
  *   v_{pos-W+2..pos}; both NULL iff pos == 0. Entries at global index <= 0 are zero.
  *   out: [B,H,T,dv]  S_final: [B,H,dk,dv]  tail_k_out / tail_v_out: as tail_k / tail_v
  *   for position pos + T.
- * window must be 1 except for Falcon-3. nthreads <= 0 means one thread.
+ * window must be 1 except for Falcon-3 and 3A. nthreads <= 0 means one thread.
  * Returns 0, or 1 for invalid arguments, 2 when memory runs out.
  */
 int falcon_ref_fwd(int variant, int64_t B, int64_t H, int64_t T, int64_t dk, int64_t dv, int window,
@@ -279,9 +299,9 @@ int falcon_ref_fwd(int variant, int64_t B, int64_t H, int64_t T, int64_t dk, int
                    const double *lam, const double *S0, const double *tail_k, const double *tail_v,
                    double eps, double eps_gamma, double *out, double *S_final, double *tail_k_out,
                    double *tail_v_out, int nthreads) {
-    if (variant != REF_F1 && variant != REF_F1A && variant != REF_F2 && variant != REF_F3) return REF_EINVAL;
+    if (variant < REF_F1 || variant > REF_F3A) return REF_EINVAL;
     if (B < 0 || H < 0 || T < 0 || dk <= 0 || dv <= 0 || window < 1 || pos < 0) return REF_EINVAL;
-    if (variant != REF_F3 && window != 1) return REF_EINVAL;
+    if (variant != REF_F3 && variant != REF_F3A && window != 1) return REF_EINVAL;
     if ((pos > 0) != (tail_k != NULL)) return REF_EINVAL;
     if (pos > 0 && window > 1 && tail_v == NULL) return REF_EINVAL;
     const int64_t n = B * H;
@@ -295,7 +315,7 @@ int falcon_ref_fwd(int variant, int64_t B, int64_t H, int64_t T, int64_t dk, int
         free(work);
         return REF_ENOMEM;
     }
-    const int bt_stride = variant == REF_F2 ? (int)dv : 1;
+    const int bt_stride = (variant == REF_F2 || variant == REF_F2A) ? (int)dv : 1;
     for (int64_t s = 0; s < n; ++s) {
         seq_job *j = &jobs[s];
         j->variant = variant;

@@ -297,3 +297,83 @@ def test_rejects_bad_arguments():
 def test_torch_inputs_are_widened_exactly():
     t = torch.tensor([[[[1.0078125, -3.5]]]], dtype=torch.bfloat16)
     assert oracle._f64(t).tolist() == [[[[1.0078125, -3.5]]]]
+
+
+# ---------------------------------------------------------------- the inner-product variants 2A and 3A
+
+F2A, F3A = 4, 6
+
+
+def test_falcon2a_equal_columns_is_falcon1a():
+    """Falcon-2A with every column's gain equal to one beta is Falcon-1A, bitwise (same operations)."""
+    q, k, v, beta, lam, S0 = _rand(41, 2, 3, 13, 5, 4, F1A, lam_hi=2.0)
+    o1, S1, _ = oracle.falcon_ref_fwd(F1A, q, k, v, beta, lam, S0)
+    b2 = np.repeat(beta[..., None], 4, axis=-1)
+    o2, S2, _ = oracle.falcon_ref_fwd(F2A, q, k, v, b2, lam, S0)
+    assert np.array_equal(o1, o2) and np.array_equal(S1, S2)
+
+
+def test_falcon2a_column_is_falcon1a_on_that_column():
+    """Each value column of Falcon-2A follows Falcon-1A on that column alone with that column's gains."""
+    q, k, v, _, lam, S0 = _rand(42, 1, 2, 11, 5, 3, F1A, lam_hi=3.0)
+    rng = np.random.default_rng(43)
+    b2 = rng.uniform(0.05, 1.9, (1, 2, 11, 3))
+    o2, S2, _ = oracle.falcon_ref_fwd(F2A, q, k, v, b2, lam, S0)
+    for c in range(3):
+        oc, Sc, _ = oracle.falcon_ref_fwd(F1A, q, k, v[..., c:c + 1], b2[..., c], lam, S0[..., c:c + 1])
+        np.testing.assert_allclose(o2[..., c:c + 1], oc, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(S2[..., c:c + 1], Sc, rtol=1e-13, atol=1e-13)
+
+
+def test_falcon3a_window1_is_falcon1a():
+    """A window of one pair reduces Falcon-3A to Falcon-1A (paperlayer §4.5)."""
+    q, k, v, beta, lam, S0 = _rand(44, 2, 2, 17, 6, 5, F1A, beta_hi=1.9, lam_hi=4.0)
+    o1, S1, _ = oracle.falcon_ref_fwd(F1A, q, k, v, beta, lam, S0)
+    o3, S3, _ = oracle.falcon_ref_fwd(F3A, q, k, v, beta, lam, S0, window=1)
+    np.testing.assert_allclose(o3, o1, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(S3, S1, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("W", [2, 3, 5])
+def test_falcon3a_is_the_masked_attention_form(W):
+    """Falcon-3A's parallel form (paperlayer §4.6): O = Diag(delta) Q S0 + (Q X^T (.) M) Y, with
+    delta_t = prod_{s<=t} gamma_s and M_tj = sum over updates u <= t whose window holds pair j of
+    (prod_{u<s<=t} gamma_s) eta_u / B_u. Built here by brute force over (t, u, j)."""
+    T, dk, dv = 14, 4, 3
+    q, k, v, beta, lam, S0 = _rand(45, 1, 1, T, dk, dv, F1A, beta_hi=1.9, lam_hi=3.0)
+    eps, eps_g = 1e-6, 1e-6
+    out, S, _ = oracle.falcon_ref_fwd(F3A, q, k, v, beta, lam, S0, window=W, eps=eps, eps_gamma=eps_g)
+    X = np.vstack([np.zeros((1, dk)), k[0, 0, :-1]])  # x_tau = k_{tau-1}, x_1 = 0 (rows tau-1)
+    Y = v[0, 0]
+    gam, eta_b, win = np.ones(T), np.zeros(T), []
+    for t in range(T):  # update at global step tau = t + 1
+        tau = t + 1
+        members = [j for j in range(max(2, tau - W + 1), tau + 1)] if tau >= 2 else []
+        win.append(members)
+        if not members:
+            continue
+        E = np.mean([X[j - 1] @ X[j - 1] for j in members])
+        eta = beta[0, 0, t] / (E + lam[0, 0, t] + eps)
+        alpha = min(eta * lam[0, 0, t], 1 - eps_g)
+        gam[t] = 1 - alpha
+        eta_b[t] = eta / len(members)
+    ref = np.zeros((T, dv))
+    for t in range(T):
+        delta = np.prod(gam[: t + 1])
+        ref[t] = delta * (S0[0, 0].T @ q[0, 0, t])
+        for j in range(1, T + 1):
+            m = sum(np.prod(gam[u + 1: t + 1]) * eta_b[u] for u in range(t + 1) if j in win[u])
+            ref[t] += m * (q[0, 0, t] @ X[j - 1]) * Y[j - 1]
+    np.testing.assert_allclose(out[0, 0], ref, rtol=1e-11, atol=1e-12)
+
+
+def test_inner_product_variants_sentinel_and_arguments():
+    """x_1 = 0: the first step is a no-op for 2A and 3A too; 2A takes per-column gains, 3A a window."""
+    q, k, v, beta, lam, S0 = _rand(46, 2, 3, 1, 5, 4, F1A)
+    b2 = np.repeat(beta[..., None], 4, axis=-1)
+    _, S, _ = oracle.falcon_ref_fwd(F2A, q, k, v, b2, lam, S0)
+    assert np.array_equal(S, S0)
+    _, S, _ = oracle.falcon_ref_fwd(F3A, q, k, v, beta, lam, S0, window=3)
+    assert np.array_equal(S, S0)
+    with pytest.raises(AssertionError):
+        oracle.falcon_ref_fwd(F2A, q, k, v, beta, lam, S0)  # gains must be per column
