@@ -289,7 +289,7 @@ def test_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.falcon_ref_fwd(F1, q, k, v, beta, lam, S0, window=2)      # window only for Falcon-3
     with pytest.raises(ValueError):
-        oracle.falcon_ref_fwd(4, q, k, v, beta, lam, S0)                  # Falcon-2A is not built
+        oracle.falcon_ref_fwd(7, q, k, v, beta, lam, S0)                  # no such variant
     with pytest.raises(ValueError):
         oracle.falcon_ref_fwd(F1, q, k, v, beta, lam, S0, pos=3)          # pos > 0 needs a tail
 
