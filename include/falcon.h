@@ -13,14 +13,17 @@
  *   FALCON_1   S = gamma S + eta x (y - S^T x)^T             ([AH] Method)
  *   FALCON_1A  S = gamma S + eta x y^T                        ([AH] Method)
  *   FALCON_2   as FALCON_1 with a per-column gain beta[..., c] ([PL] §1, Figure 5)
+ *   FALCON_2A  as FALCON_1A with a per-column gain beta[..., c] ([PL] §4.3, "B. Falcon-2A")
  *   FALCON_3   window of the last `window` pairs (pair 1 excluded), residuals at
  *              the pre-update state, step eta/B_tau, eta normalised by the top
  *              eigenvalue of the window-averaged key covariance ([PL] §4.4, §C.6)
+ *   FALCON_3A  the same window written with the targets themselves, eta normalised by
+ *              the window's mean key energy (1/B) sum ||x_j||^2 ([PL] §4.5, §4.6, "C. Falcon-3A")
  * The kernels evaluate it in the chunk-parallel form ([PL] Figure 2, §E.2, §F.2,
  * §H.3): per chunk one unit-lower-triangular solve with the value and the
  * projected-history right-hand sides merged, log-prefix decay reset to 0 at
  * every chunk start ([PL] §D.1, §G.1), and a carried state between chunks.
- * A call with T = 1 (Falcon-1, 1A, 2; dk = dv = 64) runs a single-token kernel instead: the recurrent
+ * A call with T = 1 (Falcon-1, 1A, 2, 2A; dk = dv = 64) runs a single-token kernel instead: the recurrent
  * form of the same update, one (batch, head) state per CTA, so a decoding step costs one read and
  * one write of the state ([PL] §3; [AH] Method).
  * Falcon-1 and 1A at bf16, dk = dv = 64, chunk 64 also have a split path that
@@ -50,9 +53,9 @@ typedef enum {
     FALCON_1 = 1,   /* scalar NLMS regression write                              */
     FALCON_1A = 2,  /* scalar inner-product write                                */
     FALCON_2 = 3,   /* per-column NLMS regression write                          */
-    FALCON_2A = 4,  /* per-column inner-product write: reserved, returns UNSUPPORTED */
+    FALCON_2A = 4,  /* per-column inner-product write                            */
     FALCON_3 = 5,   /* sliding-window mini-batch regression write                */
-    FALCON_3A = 6   /* sliding-window inner-product write: reserved, returns UNSUPPORTED */
+    FALCON_3A = 6   /* sliding-window inner-product write                        */
 } falcon_variant_t;
 
 typedef enum { FALCON_F32 = 0, FALCON_BF16 = 1 } falcon_dtype_t;
@@ -74,7 +77,7 @@ typedef struct {
     int64_t seqlen;   /* T >= 0 tokens in this call                                   */
     int64_t dk;       /* key/query width: 16, 32, 64 or 128                           */
     int64_t dv;       /* value width: 16, 32, 64 or 128                               */
-    int32_t window;   /* Falcon-3 window size 1..8; must be 1 for the other variants  */
+    int32_t window;   /* Falcon-3 / 3A window size 1..8; must be 1 for the other variants */
     int32_t dtype;    /* falcon_dtype_t of q, k, v, out, tail, tail_out                */
     int64_t pos;      /* tokens already consumed by earlier calls; 0 = fresh start    */
     float eps;        /* >= 0, added to the step-size denominator                     */
@@ -86,7 +89,7 @@ typedef struct {
  *   q, k      [B,H,T,dk] dtype        queries and keys (phi = identity; callers apply
  *                                     QK-RMSNorm upstream, [PL] §5, [AH] Method)
  *   v         [B,H,T,dv] dtype        values (targets y)
- *   beta      fp32 [B,H,T], or [B,H,T,dv] for FALCON_2; gains, caller keeps them in (0,2)
+ *   beta      fp32 [B,H,T], or [B,H,T,dv] for FALCON_2 and 2A; gains, caller keeps them in (0,2)
  *   lambda    fp32 [B,H,T], >= 0      ridge coefficients
  *   S0        fp32 [B,H,dk,dv] or NULL (zero initial state)
  *   tail      NULL iff pos == 0; else falcon_tail_bytes(dims) bytes in dtype laid out
@@ -99,7 +102,7 @@ typedef struct {
  *   tail_out  NULL or falcon_tail_bytes(dims) bytes: the tail for position pos+T;
  *             must not overlap tail
  *   dims      problem description (host pointer)
- *   chunk     chunk length C: 16, 32 or 64; FALCON_3 needs chunk*window <= 128.
+ *   chunk     chunk length C: 16, 32 or 64; FALCON_3 and 3A need chunk*window <= 128.
  *             The result does not depend on C beyond fp32 rounding.
  *   workspace NULL, or scratch device memory of at least
  *             falcon_workspace_bytes(variant, dims, chunk) bytes that overlaps no other

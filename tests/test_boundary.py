@@ -58,8 +58,9 @@ def test_tail_bytes(lib):
     (dict(), 1),
     (dict(dtype=F.FALCON_F32, dk=16, dv=16, chunk=16), 1),
     (dict(variant=F.FALCON_3, window=4, chunk=32), 1),
-    (dict(variant=F.FALCON_2A), 0),                 # reserved variant
-    (dict(variant=F.FALCON_3A), 0),
+    (dict(variant=F.FALCON_2A), 1),                 # inner-product variants: CUDA-core kernel
+    (dict(variant=F.FALCON_3A, window=3, chunk=32), 1),
+    (dict(variant=F.FALCON_3A, window=4, chunk=64), 0),  # chunk*window > 128
     (dict(variant=7), 0),
     (dict(window=2), 0),                            # window only for Falcon-3
     (dict(variant=F.FALCON_3, window=9, chunk=16), 0),
@@ -128,7 +129,7 @@ def test_tail_out_must_not_overlap_tail(lib):
 
 def test_unsupported_and_invalid_shapes(lib):
     assert _call(dims=F.make_dims(2, 2, 64, 48, 64)) == F.FALCON_ERR_UNSUPPORTED
-    assert _call(variant=F.FALCON_2A) == F.FALCON_ERR_UNSUPPORTED
+    assert _call(variant=8) == F.FALCON_ERR_INVALID_ARG
     assert _call(variant=0) == F.FALCON_ERR_INVALID_ARG
     assert _call(chunk=-4) == F.FALCON_ERR_INVALID_ARG
     assert _call(chunk=24) == F.FALCON_ERR_UNSUPPORTED
@@ -148,6 +149,8 @@ def test_unsupported_and_invalid_shapes(lib):
     (dict(seqlen=1, variant=F.FALCON_2), 4),
     (dict(seqlen=1, dk=32, dv=32), 1),
     (dict(seqlen=2), 3),
+    (dict(variant=F.FALCON_2A), 1),                      # inner-product variants: CUDA-core kernel
+    (dict(variant=F.FALCON_2A, seqlen=1), 4),            # ... and the single-token kernel for 2A
 ])
 def test_kernel_choice(lib, case, expect):
     c = dict(variant=F.FALCON_1, seqlen=1024, dk=64, dv=64, dtype=F.FALCON_BF16, chunk=64)

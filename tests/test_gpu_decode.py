@@ -1,4 +1,4 @@
-"""GPU parity of the single-token kernel (T = 1 per call, Falcon-1, 1A, 2 with d = 64) against the
+"""GPU parity of the single-token kernel (T = 1 per call, Falcon-1, 1A, 2, 2A with d = 64) against the
 fp64 oracle: fresh starts, continuations from a tail and a nonzero state, the state updated in place,
 and a run of consecutive steps that must equal one call over the same tokens."""
 
@@ -12,7 +12,7 @@ from weight_linear_attention_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
 
-NAMES = {1: "falcon1", 2: "falcon1a", 3: "falcon2"}
+NAMES = {1: "falcon1", 2: "falcon1a", 3: "falcon2", 4: "falcon2a"}
 
 
 def _inputs(variant, dtype, seqlen, batch=3, seed=21):
@@ -40,7 +40,7 @@ def _step(variant, inp, t, dims_pos, S, tail, dt, inplace=False):
     return out, S_final, tail_out
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_single_step_fresh_and_continued(variant, dtype):
     w, inp = _inputs(variant, dtype, seqlen=40)
@@ -65,7 +65,7 @@ def test_single_step_fresh_and_continued(variant, dtype):
     assert F.falcon_device_status() == F.FALCON_OK
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 def test_consecutive_steps_in_place_match_one_call(variant):
     """24 single-token calls, the state updated in place and the tail carried, equal the oracle over the
     24 tokens (the decode loop of a server)."""

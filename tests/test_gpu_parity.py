@@ -242,3 +242,55 @@ def test_rejects_bad_call_without_touching_outputs():
     assert st == F.FALCON_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(out == 7.0)
+
+
+# ------------------------------------------------------------------ inner-product variants 2A and 3A
+
+F2A, F3A = 4, 6
+_IP = {F2A: "falcon2a", F3A: "falcon3a"}
+
+
+@pytest.mark.parametrize("variant,W", [(F2A, 1), (F3A, 2), (F3A, 4)])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("chunk", [16, 32])
+def test_inner_product_variants(variant, W, dtype, chunk):
+    """Falcon-2A and 3A from a nonzero state, several chunks and a ragged tail."""
+    w = I.WORKLOADS[HEAD].with_(variant=_IP[variant], window=W, chunk=chunk, dtype=dtype, nonzero_s0=True,
+                                heads=4)
+    inp = I.make_inputs(w, seed=31, seqlen=3 * chunk + 11, batch=2)
+    _parity(w, inp, S0=inp["S0"], name=f"v{variant} W{W} {dtype} C{chunk}")
+
+
+@pytest.mark.parametrize("variant,W", [(F2A, 1), (F3A, 3)])
+def test_inner_product_clamp_stress(variant, W):
+    """beta = 1.5, lambda = 1000: alpha = 1 - eps_gamma on every step (strong decay in every chunk)."""
+    w = I.WORKLOADS[HEAD].with_(variant=_IP[variant], window=W, chunk=32, lam_const=1000.0, lam_shift=None)
+    inp = I.make_inputs(w, seed=32, seqlen=100, batch=1)
+    inp["beta"] = torch.full_like(inp["beta"], 1.5)
+    _parity(w, inp, name=f"clamp v{variant}")
+
+
+@pytest.mark.parametrize("variant,W,split", [(F2A, 1, 37), (F3A, 4, 2), (F3A, 3, 50)])
+def test_inner_product_continuation(variant, W, split):
+    """Two calls carrying S_final and the tail equal the oracle over the whole sequence."""
+    w = I.WORKLOADS[HEAD].with_(variant=_IP[variant], window=W, chunk=32)
+    T = 140
+    inp = I.make_inputs(w, seed=33, seqlen=T, batch=1)
+    a, b = slice_inputs(inp, 0, split), slice_inputs(inp, split, T)
+    o1, S1, t1 = run_gpu(variant, a, window=W, chunk=32)
+    o2, S2, t2 = run_gpu(variant, b, window=W, chunk=32, pos=split, S0=S1, tail=t1)
+    ro, rS, rt = run_oracle(variant, inp, window=W)
+    _check("out", torch.cat([o1, o2], dim=2), ro, torch.bfloat16)
+    _check("S", S2, rS, torch.bfloat16)
+    tk, tv = F.split_tail(t2, 1, 12, W, 64, 64)
+    np.testing.assert_array_equal(tk.double().numpy(), rt[0])
+    np.testing.assert_array_equal(tv.double().numpy(), rt[1])
+
+
+@pytest.mark.parametrize("variant", [F2A, F3A])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (128, 64), (16, 128)])
+def test_inner_product_head_sizes(variant, dk, dv):
+    W = 2 if variant == F3A else 1
+    w = I.WORKLOADS[HEAD].with_(variant=_IP[variant], window=W, chunk=32, dk=dk, dv=dv, heads=3)
+    inp = I.make_inputs(w, seed=34, seqlen=90, batch=2)
+    _parity(w, inp, name=f"dk{dk} dv{dv} v{variant}")

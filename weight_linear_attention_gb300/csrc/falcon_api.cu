@@ -58,19 +58,18 @@ size_t workspace_need(const falcon::Launch& a) {
 
 int validate_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail, falcon::Launch* a) {
     if (!d) return FALCON_ERR_INVALID_ARG;
-    if (variant == FALCON_2A || variant == FALCON_3A) return FALCON_ERR_UNSUPPORTED;
-    if (variant != FALCON_1 && variant != FALCON_1A && variant != FALCON_2 && variant != FALCON_3)
-        return FALCON_ERR_INVALID_ARG;
+    if (variant < FALCON_1 || variant > FALCON_3A) return FALCON_ERR_INVALID_ARG;
     if (d->batch < 0 || d->heads < 0 || d->seqlen < 0 || d->pos < 0) return FALCON_ERR_INVALID_ARG;
     if (d->dk <= 0 || d->dv <= 0) return FALCON_ERR_INVALID_ARG;
     if (!pow2_head(d->dk) || !pow2_head(d->dv)) return FALCON_ERR_UNSUPPORTED;
     if (d->dtype != FALCON_F32 && d->dtype != FALCON_BF16) return FALCON_ERR_UNSUPPORTED;
     if (d->window < 1) return FALCON_ERR_INVALID_ARG;
-    if (variant != FALCON_3 && d->window != 1) return FALCON_ERR_INVALID_ARG;
+    const bool win = variant == FALCON_3 || variant == FALCON_3A;
+    if (!win && d->window != 1) return FALCON_ERR_INVALID_ARG;
     if (d->window > 8) return FALCON_ERR_UNSUPPORTED;
     if (!(d->eps >= 0.f) || !(d->eps_gamma > 0.f && d->eps_gamma < 1.f)) return FALCON_ERR_INVALID_ARG;
     if (chunk != 16 && chunk != 32 && chunk != 64) return chunk <= 0 ? FALCON_ERR_INVALID_ARG : FALCON_ERR_UNSUPPORTED;
-    if (variant == FALCON_3 && chunk * d->window > 128) return FALCON_ERR_UNSUPPORTED;
+    if (win && chunk * d->window > 128) return FALCON_ERR_UNSUPPORTED;
     if ((d->pos > 0) != has_tail) return FALCON_ERR_INVALID_ARG;
     a->variant = variant;
     a->B = d->batch;
@@ -110,7 +109,7 @@ int validate(int variant, const void* q, const void* k, const void* v, const flo
     // out must not overlap any input; tail_out must not overlap tail; S_final may equal S0 exactly.
     if (tokens > 0) {
         const Range ro = range_of(out, (size_t)tokens * d->dv * es);
-        const size_t bcols = variant == FALCON_2 ? (size_t)d->dv : 1;
+        const size_t bcols = (variant == FALCON_2 || variant == FALCON_2A) ? (size_t)d->dv : 1;
         const Range ins[] = {
             range_of(q, (size_t)tokens * d->dk * es), range_of(k, (size_t)tokens * d->dk * es),
             range_of(v, (size_t)tokens * d->dv * es), range_of(beta, (size_t)tokens * bcols * 4),
@@ -129,7 +128,7 @@ int validate(int variant, const void* q, const void* k, const void* v, const flo
         overlaps(range_of(S0, (size_t)BH * d->dk * d->dv * 4), range_of(S_final, (size_t)BH * d->dk * d->dv * 4)))
         return FALCON_ERR_INVALID_ARG;
     if (ws && ws_need > 0) {  // the workspace is written by the kernels: it may overlap nothing
-        const size_t bcols = variant == FALCON_2 ? (size_t)d->dv : 1;
+        const size_t bcols = (variant == FALCON_2 || variant == FALCON_2A) ? (size_t)d->dv : 1;
         const Range rw = range_of(ws, ws_need);
         const Range all[] = {
             range_of(q, (size_t)tokens * d->dk * es), range_of(k, (size_t)tokens * d->dk * es),

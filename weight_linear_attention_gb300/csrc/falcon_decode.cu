@@ -1,4 +1,4 @@
-// Single-token step (T = 1) for Falcon-1, 1A and 2 with dk = dv = 64: the recurrent form of the
+// Single-token step (T = 1) for Falcon-1, 1A, 2 and 2A with dk = dv = 64: the recurrent form of the
 // update ("Fast Weight Attention for Continual Learning", paperlayer summary §3, Appendix p.34;
 // agihunt explainer "Method"), one (batch, head) state per CTA. The state is read once and written
 // once, so the step is bound by those 2 x 16 KB per head of HBM traffic.
@@ -8,7 +8,7 @@
 //   eta = beta / (|x|^2 + lambda + eps) (0 when the denominator is 0, and at tau = 1)
 //   alpha = min(eta lambda, 1 - eps_gamma) (0 at tau = 1), gamma = 1 - alpha
 //   Falcon-1:  S' = gamma S + eta x (y - S^T x)^T      Falcon-1A: S' = gamma S + eta x y^T
-//   Falcon-2:  the same per value column c with beta_c (eta_c, gamma_c)
+//   Falcon-2, 2A: Falcon-1, 1A per value column c with beta_c (eta_c, gamma_c)
 //   o = S'^T q (read after write), tail_out = k (the next step's x).
 // fp32 arithmetic throughout; S_final may be the same buffer as S0 (each element is read and
 // written by the same thread).
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p
         float eta = 0.f, alpha = 0.f;
         if (!first) {
             const float lm = p.lam[bh];
-            const float b = VAR == kF2 ? p.beta[bh * kD + tid] : p.beta[bh];
+            const float b = per_column(VAR) ? p.beta[bh * kD + tid] : p.beta[bh];
             const float den = nx_s + lm + p.eps;
             eta = den == 0.f ? 0.f : b / den;
             alpha = fminf(eta * lm, 1.f - p.eps_gamma);
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p
     }
 
     // ---- residual r = y - S^T x (Falcon-1, 2) or r = y (Falcon-1A)
-    if (VAR != kF1A) {
+    if (!inner_product(VAR)) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             float a = 0.f;
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p
     __syncthreads();
     if (tid < kD) {
         float a = 0.f;
-        if (VAR != kF1A)
+        if (!inner_product(VAR))
 #pragma unroll
             for (int g = 0; g < kGroups; ++g) a += part[g][tid];
         rs[tid] = ys[tid] - a;
@@ -152,6 +152,7 @@ cudaError_t launch_typed(const Launch& a, const DParams& p, cudaStream_t st) {
         case kF1: falcon_decode_kernel<Tin, kF1><<<grid, kThreads, 0, st>>>(p); break;
         case kF1A: falcon_decode_kernel<Tin, kF1A><<<grid, kThreads, 0, st>>>(p); break;
         case kF2: falcon_decode_kernel<Tin, kF2><<<grid, kThreads, 0, st>>>(p); break;
+        case kF2A: falcon_decode_kernel<Tin, kF2A><<<grid, kThreads, 0, st>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -160,7 +161,7 @@ cudaError_t launch_typed(const Launch& a, const DParams& p, cudaStream_t st) {
 }  // namespace
 
 bool decode_supported(const Launch& a) {
-    return a.T == 1 && (a.variant == kF1 || a.variant == kF1A || a.variant == kF2) && a.W == 1 && a.dk == kD &&
+    return a.T == 1 && !windowed(a.variant) && a.W == 1 && a.dk == kD &&
            a.dv == kD && a.B * a.H < (1LL << 31);
 }
 

@@ -185,7 +185,7 @@ struct Smem {
 
 __host__ __device__ inline size_t smem_floats(int variant, int dk, int dvs, int C, int W, Smem* s, float* base) {
     const int NE = C + W - 1;
-    const int per_col = (variant == kF2) ? dvs : 1;
+    const int per_col = per_column(variant) ? dvs : 1;
     size_t off = 0;
     auto take = [&](float** dst, size_t n) {
         if (dst) *dst = base + off;
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
     const int tid = threadIdx.x;
     const int DK = p.dk, DV = p.dv, DVS = p.dvs, C = p.C;
     const int XS = DK + 1;  // row stride of X and Q in shared memory (odd: rows fall in different banks)
-    const int W = (VAR == kF3) ? p.W : 1;
+    const int W = windowed(VAR) ? p.W : 1;
     // R (and Falcon-2's per-column scalars) are stored column-major with an odd stride, since the
     // forward substitution runs down one column across the lanes of a warp.
     const int RS = C * W + 1, CS = C + 1;
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
     const Tin* q = static_cast<const Tin*>(p.q) + bh * T * DK;
     const Tin* k = static_cast<const Tin*>(p.k) + bh * T * DK;
     const Tin* v = static_cast<const Tin*>(p.v) + bh * T * DV;
-    const float* beta = p.beta + bh * T * (VAR == kF2 ? DV : 1);
+    const float* beta = p.beta + bh * T * (per_column(VAR) ? DV : 1);
     const float* lam = p.lam + bh * T;
     const long long tail_stride = (long long)W * DK + (long long)(W - 1) * DV;
     const Tin* tail = p.tail ? static_cast<const Tin*>(p.tail) + bh * tail_stride : nullptr;
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                 }
             }
         }
-        if (VAR == kF2) {  // the chunk's gains (per column, into eta) and ridge coefficients (into kap)
+        if (per_column(VAR)) {  // the chunk's gains (per column, into eta) and ridge coefficients (into kap)
             for (int idx = tid; idx < C * DVS; idx += kThreads) {
                 const int i = idx / DVS, c = idx % DVS;
                 s.eta[c * CS + i] = i < n ? beta[(t0 + i) * DV + c0 + c] : 0.f;
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         }
         __syncthreads();
         // ---- (2) Gram, scores, projected history, Q S
-        constexpr bool kMmaGram = std::is_same<Tin, __nv_bfloat16>::value && VAR != kF3;
+        constexpr bool kMmaGram = std::is_same<Tin, __nv_bfloat16>::value && !windowed(VAR);
         if (kMmaGram && C <= 64 && C % 16 == 0 && DK % 16 == 0) {
             gram_mma(s.X, s.Q, s.G, s.Sc, C, DK, XS, NE, tid);
         } else {
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         }
         __syncthreads();
         // ---- (3) per-token scalars and the chunk-local log-decay prefix
-        if (VAR == kF2) {
+        if (per_column(VAR)) {
             // every (token, column) in parallel, then one warp scan of log(gamma) per column
             for (int idx = tid; idx < C * DVS; idx += kThreads) {
                 const int i = idx / DVS, c = idx % DVS;
@@ -397,14 +397,17 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                 if (i < n) {
                     const long long tau = pos + t0 + i + 1;
                     const float lm = lam[t0 + i];
-                    if (VAR == kF3) {
+                    if (windowed(VAR)) {
                         int slots[kMaxW] = {};
                         int nb = 0;
                         for (int sl = 0; sl < W; ++sl)
                             if (tau - sl >= 2) slots[nb++] = i - sl + W - 1;
                         if (nb > 0) {
-                            float mu;
-                            switch (W) {  // the matrix in registers: one instance per window size
+                            float mu = 0.f;
+                            if (VAR == kF3A) {  // the window's mean key energy (trace of the averaged Gram)
+                                for (int x = 0; x < nb; ++x) mu += s.G[slots[x] * NE + slots[x]];
+                                mu /= (float)nb;
+                            } else switch (W) {  // the matrix in registers: one instance per window size
                                 case 1: mu = s.G[slots[0] * NE + slots[0]]; break;
                                 case 2: mu = window_lambda_max<2>(s.G, NE, slots, nb); break;
                                 case 3: mu = window_lambda_max<3>(s.G, NE, slots, nb); break;
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                 }
                 if (i < C) {
                     s.eta[i] = eta;
-                    s.kap[i] = (VAR == kF3) ? kap : eta;
+                    s.kap[i] = windowed(VAR) ? kap : eta;
                 }
                 ls[m] = log1pf(-alpha);
                 lsum += ls[m];
@@ -450,14 +453,14 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         }
         __syncthreads();
         // ---- (4) decay-weighted coefficient matrices (shared by all columns)
-        if (VAR != kF2) {
+        if (!per_column(VAR)) {
             const float LC = s.L[C - 1];
             for (int idx = tid; idx < C * C; idx += kThreads) {
                 const int i = idx / C, j = idx % C;
                 float a = 0.f, pp = 0.f;
                 if (j < i) a = s.kap[j] * expf(s.Lx[i] - s.L[j]);
                 if (j <= i) pp = s.kap[j] * expf(s.L[i] - s.L[j]);
-                if (VAR != kF3) {
+                if (!windowed(VAR)) {
                     a *= s.G[i * NE + j];
                     pp *= s.Sc[i * NE + j];
                 }
@@ -571,6 +574,18 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                     }
                 }
             }
+        } else if (VAR == kF2A) {  // no solve: the targets (Falcon-2A fast columns keep eta_j e^{-L_j} y_j)
+            for (int idx = tid; idx < n * DVS; idx += kThreads) {
+                const int j = idx / DVS, c = idx % DVS;
+                const float y = s.Y[j * DVS + c];
+                s.R[c * RS + j] = s.w[c * CS + C] != 0.f ? s.w[c * CS + j] * y : y;
+            }
+        } else if (VAR == kF3A) {  // no solve: every window slot's target (zero for the sentinel pair)
+            for (int idx = tid; idx < n * W * DVS; idx += kThreads) {
+                const int m = idx / DVS, c = idx % DVS, i = m / W, a = m % W;
+                const bool valid = pos + t0 + i + 1 - a >= 2;
+                s.R[c * RS + m] = valid ? s.Y[(i - a + W - 1) * DVS + c] : 0.f;
+            }
         }
         __syncthreads();
         // ---- (6) outputs (read after write) and (7) carried state
@@ -578,7 +593,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         for (int idx = tid; idx < n * DVS; idx += kThreads) {
             const int i = idx / DVS, c = idx % DVS;
             float o;
-            if (VAR == kF2) {
+            if (per_column(VAR)) {
                 const float li = s.L[c * CS + i];
                 if (s.w[c * CS + C] != 0.f) {  // fast: o = e^{L_i} (QS + sum_j Sc_ij R~_j)
                     o = s.QS[idx];
@@ -590,7 +605,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                         o = fmaf(s.eta[c * CS + j] * expf(li - s.L[c * CS + j]) * s.Sc[i * NE + j], s.R[c * RS + j],
                                  o);
                 }
-            } else if (VAR == kF3) {
+            } else if (windowed(VAR)) {
                 o = expf(s.L[i]) * s.QS[idx];
                 for (int l = 0; l <= i; ++l) {
                     const float f = s.P[i * C + l];
@@ -610,14 +625,14 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         for (int idx = tid; idx < DK * DVS; idx += kThreads) {
             const int r = idx / DVS, c = idx % DVS;
             float acc = 0.f;
-            if (VAR == kF3) {
+            if (windowed(VAR)) {
                 for (int l = 0; l < n; ++l) {
                     float inner = 0.f;
                     for (int b = 0; b < W; ++b) inner = fmaf(s.X[(l - b + W - 1) * XS + r], s.R[c * RS + l * W + b], inner);
                     acc = fmaf(s.w[l], inner, acc);
                 }
                 s.S[idx] = fmaf(expf(s.L[C - 1]), s.S[idx], acc);
-            } else if (VAR == kF2) {
+            } else if (per_column(VAR)) {
                 const float gC = expf(s.L[c * CS + C - 1]);
                 if (s.w[c * CS + C] != 0.f) {  // fast: S' = e^{L_C} (S + sum_j x_j R~_j)
                     for (int j = 0; j < n; ++j) acc = fmaf(s.X[j * XS + r], s.R[c * RS + j], acc);
@@ -662,7 +677,9 @@ cudaError_t launch_typed(const Launch& a, const GParams& gp, dim3 grid, size_t s
         case kF1: fn = falcon_chunk_generic_kernel<Tin, kF1>; break;
         case kF1A: fn = falcon_chunk_generic_kernel<Tin, kF1A>; break;
         case kF2: fn = falcon_chunk_generic_kernel<Tin, kF2>; break;
+        case kF2A: fn = falcon_chunk_generic_kernel<Tin, kF2A>; break;
         case kF3: fn = falcon_chunk_generic_kernel<Tin, kF3>; break;
+        case kF3A: fn = falcon_chunk_generic_kernel<Tin, kF3A>; break;
         default: return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -684,7 +701,7 @@ int choose_dvs(const Launch& a) {
 }  // namespace
 
 size_t generic_smem_bytes(const Launch& a, int dvs) {
-    const int W = a.variant == kF3 ? a.W : 1;
+    const int W = windowed(a.variant) ? a.W : 1;
     return smem_floats(a.variant, (int)a.dk, dvs, a.chunk, W, nullptr, nullptr) * sizeof(float);
 }
 
@@ -708,7 +725,7 @@ int launch_generic(const Launch& a, cudaStream_t st) {
     gp.dv = (int)a.dv;
     gp.dvs = dvs;
     gp.C = a.chunk;
-    gp.W = a.variant == kF3 ? a.W : 1;
+    gp.W = windowed(a.variant) ? a.W : 1;
     gp.eps = a.eps;
     gp.eps_gamma = a.eps_gamma;
     const size_t smem = generic_smem_bytes(a, dvs);

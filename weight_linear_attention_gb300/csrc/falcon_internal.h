@@ -7,7 +7,11 @@
 
 namespace falcon {
 
-enum Variant { kF1 = 1, kF1A = 2, kF2 = 3, kF3 = 5 };
+enum Variant { kF1 = 1, kF1A = 2, kF2 = 3, kF2A = 4, kF3 = 5, kF3A = 6 };
+// per-column gains (2, 2A); a window of W pairs (3, 3A); the target written as is, no solve (1A, 2A, 3A)
+__host__ __device__ constexpr bool per_column(int v) { return v == kF2 || v == kF2A; }
+__host__ __device__ constexpr bool windowed(int v) { return v == kF3 || v == kF3A; }
+__host__ __device__ constexpr bool inner_product(int v) { return v == kF1A || v == kF2A || v == kF3A; }
 
 // Arguments after validation by falcon_fwd: sizes are in range, pointers are
 // non-null where required and aligned, tail is present iff pos > 0.
@@ -49,7 +53,7 @@ size_t split_workspace_bytes(const Launch& a);
 int launch_split(const Launch& a, cudaStream_t stream);
 int split_consume_timeout_flag(int* flag);
 
-// Single-token step (T = 1; Falcon-1, 1A and 2; dk = dv = 64): one CTA per (batch, head) state.
+// Single-token step (T = 1; Falcon-1, 1A, 2 and 2A; dk = dv = 64): one CTA per (batch, head) state.
 bool decode_supported(const Launch& a);
 int launch_decode(const Launch& a, cudaStream_t stream);
 

@@ -25,7 +25,8 @@ FALCON_ERR_MISALIGNED = 3
 FALCON_ERR_CUDA = 4
 FALCON_ERR_DEVICE_TIMEOUT = 5
 
-VARIANTS = {"falcon1": FALCON_1, "falcon1a": FALCON_1A, "falcon2": FALCON_2, "falcon3": FALCON_3}
+VARIANTS = {"falcon1": FALCON_1, "falcon1a": FALCON_1A, "falcon2": FALCON_2, "falcon2a": FALCON_2A,
+            "falcon3": FALCON_3, "falcon3a": FALCON_3A}
 
 
 class FalconDims(ctypes.Structure):

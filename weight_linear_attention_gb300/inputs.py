@@ -11,7 +11,7 @@ Recipe (every workload, seed 0 unless a caller passes another):
   generator = torch.Generator("cpu").manual_seed(seed); draws in this order,
   each N(0, 1) in fp32 of the full tensor shape:
     q [B,H,T,dk], k [B,H,T,dk], v [B,H,T,dv],
-    beta logits [B,H,T] (Falcon-2: [B,H,T,dv]), lambda logits [B,H,T],
+    beta logits [B,H,T] (Falcon-2, 2A: [B,H,T,dv]), lambda logits [B,H,T],
     then S0 [B,H,dk,dv] only when the workload asks for a nonzero initial state.
   q and k: RMSNorm over the feature axis (no gain, eps 1e-6; the pages' blocks
   use QK-RMSNorm upstream of the fast-memory update), then cast to the dtype.
@@ -28,13 +28,13 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-VARIANT_IDS = {"falcon1": 1, "falcon1a": 2, "falcon2": 3, "falcon3": 5}
+VARIANT_IDS = {"falcon1": 1, "falcon1a": 2, "falcon2": 3, "falcon2a": 4, "falcon3": 5, "falcon3a": 6}
 
 
 @dataclass(frozen=True)
 class Workload:
     name: str
-    variant: str          # falcon1 | falcon1a | falcon2 | falcon3
+    variant: str          # falcon1 | falcon1a | falcon2 | falcon2a | falcon3 | falcon3a
     batch: int
     heads: int
     seqlen: int           # tokens per call (per segment for segmented workloads)
@@ -108,7 +108,7 @@ def make_inputs(w: Workload, seed: int = 0, seqlen: int | None = None, batch: in
     q = torch.randn(B, H, T, dk, generator=g)
     k = torch.randn(B, H, T, dk, generator=g)
     v = torch.randn(B, H, T, dv, generator=g)
-    bshape = (B, H, T, dv) if w.variant == "falcon2" else (B, H, T)
+    bshape = (B, H, T, dv) if w.variant in ("falcon2", "falcon2a") else (B, H, T)
     beta_logit = torch.randn(*bshape, generator=g)
     lam_logit = torch.randn(B, H, T, generator=g)
     S0 = torch.randn(B, H, dk, dv, generator=g) / dk ** 0.5 if w.nonzero_s0 else None
