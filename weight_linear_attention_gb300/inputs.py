@@ -82,6 +82,11 @@ WORKLOADS = {
                                    lam_const=0.01),
     "f3w4_b2h12t16384_bf16": Workload("f3w4_b2h12t16384_bf16", "falcon3", 2, 12, 8192, 64, 64, "bf16", 32,
                                       window=4, lam_shift=-2.0, segments=2),
+    # the inner-product variants at the Falcon-2 and Falcon-3 shapes
+    "f2a_b8h12t2048_bf16": Workload("f2a_b8h12t2048_bf16", "falcon2a", 8, 12, 2048, 64, 64, "bf16", 64,
+                                    lam_const=0.01),
+    "f3aw4_b2h12t16384_bf16": Workload("f3aw4_b2h12t16384_bf16", "falcon3a", 2, 12, 8192, 64, 64, "bf16", 32,
+                                       window=4, lam_shift=-2.0, segments=2),
     # one decoding step of 256 sequences (12 heads of 64) after 1024 tokens: the recurrent form
     "f1_decode_b256h12_bf16": Workload("f1_decode_b256h12_bf16", "falcon1", 256, 12, 1, 64, 64, "bf16", 64,
                                        lam_shift=-4.0, nonzero_s0=True, pos0=1024),
