@@ -232,3 +232,142 @@ def chunk_forward(variant, q, k, v, beta, lam, S0=None, *, C, pos=0, tail=None, 
             out[t0:t1] = np.exp(Lc)[:, None] * (Q @ S) + Ps @ R
             S = np.exp(LC) * S + Xw.T @ R
     return out, S
+
+
+# --------------------------------------------------------------------------------------
+# 3. chunk-parallel backward (Falcon-1, 1A)
+# --------------------------------------------------------------------------------------
+
+def chunk_backward(variant, q, k, v, beta, lam, dout, S0=None, dS_final=None, *, C, pos=0, tail=None,
+                   eps=1e-6, eps_gamma=1e-6):
+    """Gradients of sum(out * dout) + sum(S_final * dS_final) for one sequence by the chunk algebra
+    the CUDA backward follows (paperlayer §D.2, §E.3, §G.3: reverse the output materialisation, the
+    inter-chunk recurrence and the local structure). Three phases:
+      1. per chunk, independent of the state: T = (I + A)^-1, the transition S -> M S + U and the
+         state-free part V of the chunk's state adjoint, dS_n = M^T dS_{n+1} + V;
+      2. the two scans: S_{n+1} = M S_n + U forward, dS_n = M^T dS_{n+1} + V backward;
+      3. per chunk, from S_n and dS_{n+1}: every input gradient of the chunk.
+    q, k [T,dk], v [T,dv], beta, lam [T], dout [T,dv]; tail = the pending key k_pos (pos > 0).
+    Returns a dict like the oracle's (dq, dk, dv, dbeta, dlam, dS0, dtail)."""
+    q, k, v, beta, lam, dout, S0, dS_final = (_np(a) for a in (q, k, v, beta, lam, dout, S0, dS_final))
+    tail = None if tail is None else _np(tail).reshape(-1)
+    T, dk = q.shape
+    dv = v.shape[1]
+    xs = np.zeros((T, dk))
+    if T:
+        xs[1:] = k[:-1]
+        if pos > 0:
+            xs[0] = tail
+    taus = pos + np.arange(T) + 1
+    first = taus == 1
+    den = np.sum(xs * xs, axis=1) + lam + eps
+    eta, alpha = _scalars(beta, lam, den, first, eps_gamma)
+    lg = np.log1p(-alpha)
+    chunks = [(t0, min(T, t0 + C)) for t0 in range(0, T, C)]
+    inner = variant == F1A
+
+    def local(t0, t1):
+        X, Q, Y, dO = xs[t0:t1], q[t0:t1], v[t0:t1], dout[t0:t1]
+        n = t1 - t0
+        e = eta[t0:t1]
+        L = np.cumsum(lg[t0:t1])
+        Lx = np.concatenate([[0.0], L[:-1]])
+        LC = L[-1]
+        Ex = np.exp(np.minimum(Lx[:, None] - L[None, :], 0.0)) * np.tril(np.ones((n, n)), -1)
+        Ep = np.exp(np.minimum(L[:, None] - L[None, :], 0.0)) * np.tril(np.ones((n, n)), 0)
+        G, Sc = X @ X.T, Q @ X.T
+        A = e[None, :] * Ex * G
+        P = e[None, :] * Ep * Sc
+        Tm = np.eye(n) if inner else np.linalg.inv(np.eye(n) + A)
+        w = e * np.exp(LC - L)
+        return dict(X=X, Q=Q, Y=Y, dO=dO, e=e, L=L, Lx=Lx, LC=LC, Ex=Ex, Ep=Ep, G=G, Sc=Sc, A=A, P=P,
+                    T=Tm, w=w)
+
+    # phase 1: state-free chunk operators
+    ops = []
+    for t0, t1 in chunks:
+        c = local(t0, t1)
+        D = np.exp(c["Lx"])[:, None] * c["X"]          # diag(e^Lx) X
+        if inner:
+            M = np.exp(c["LC"]) * np.eye(dk)
+            V = c["Q"].T @ (np.exp(c["L"])[:, None] * c["dO"])
+        else:
+            M = np.exp(c["LC"]) * np.eye(dk) - c["X"].T @ (c["w"][:, None] * (c["T"] @ D))
+            V = c["Q"].T @ (np.exp(c["L"])[:, None] * c["dO"]) - D.T @ (c["T"].T @ (c["P"].T @ c["dO"]))
+        U = c["X"].T @ (c["w"][:, None] * (c["T"] @ c["Y"]))
+        ops.append((M, U, V))
+    # phase 2: scans
+    S_in = [np.zeros((dk, dv)) if S0 is None else S0.copy()]
+    for M, U, _ in ops:
+        S_in.append(M @ S_in[-1] + U)
+    dS_out = [None] * len(chunks)
+    g = np.zeros((dk, dv)) if dS_final is None else dS_final.copy()
+    for i in range(len(chunks) - 1, -1, -1):
+        dS_out[i] = g
+        M, _, V = ops[i]
+        g = M.T @ g + V
+    dS0 = g
+    # phase 3: chunk gradients
+    dq, dx, dvv = np.zeros_like(q), np.zeros_like(xs), np.zeros_like(v)
+    deta, dL_all = np.zeros(T), np.zeros(T)
+    for ci, (t0, t1) in enumerate(chunks):
+        c = local(t0, t1)
+        S, dSn = S_in[ci], dS_out[ci]
+        X, Q, Y, dO, e, L, Lx, LC = (c[n] for n in ("X", "Q", "Y", "dO", "e", "L", "Lx", "LC"))
+        n = t1 - t0
+        H = np.exp(Lx)[:, None] * (X @ S)
+        R = Y if inner else c["T"] @ (Y - H)
+        XdS = X @ dSn
+        dR = c["P"].T @ dO + c["w"][:, None] * XdS
+        dOS = dO @ S.T
+        dP = (dO @ R.T) * np.tril(np.ones((n, n)), 0)
+        EP = dP * c["Ep"]                       # dP_ij e^{L_i - L_j}
+        dSc = EP * e[None, :]
+        dQ = np.exp(L)[:, None] * dOS + dSc @ X
+        dX = dSc.T @ Q + c["w"][:, None] * (R @ dSn.T)
+        de = np.sum(EP * c["Sc"], axis=0)
+        dw = np.sum(XdS * R, axis=1)
+        de += dw * np.exp(LC - L)
+        PP = np.sum(dP * c["P"], axis=0)        # sum_i dP_ij P_ij  (by column j)
+        dL = np.exp(L) * np.sum(Q * dOS, axis=1) + np.sum(dP * c["P"], axis=1) - PP
+        dL[-1] += np.sum(dw * c["w"]) + np.exp(LC) * np.sum(dSn * S)
+        dL -= dw * c["w"]
+        dLx = np.zeros(n)
+        if inner:
+            dY = dR
+        else:
+            dZ = c["T"].T @ dR
+            dY = dZ
+            dA = -(dZ @ R.T) * np.tril(np.ones((n, n)), -1)
+            EA = dA * c["Ex"]
+            dG = EA * e[None, :]
+            dX += (dG + dG.T) @ X
+            de += np.sum(EA * c["G"], axis=0)
+            AA = dA * c["A"]
+            dLx += np.sum(AA, axis=1)
+            dL -= np.sum(AA, axis=0)
+            dZS = dZ @ S.T
+            dX -= np.exp(Lx)[:, None] * dZS
+            dLx -= np.exp(Lx) * np.sum(X * dZS, axis=1)
+        dL[:-1] += dLx[1:]
+        dq[t0:t1], dx[t0:t1], dvv[t0:t1] = dQ, dX, dY
+        deta[t0:t1] = de
+        dL_all[t0:t1] = dL
+    # chunk-local prefixes: d log(gamma_u) = sum of dL_i over the chunk's i >= u
+    dlg = np.zeros(T)
+    for t0, t1 in chunks:
+        dlg[t0:t1] = np.cumsum(dL_all[t0:t1][::-1])[::-1]
+    unclamped = (eta * lam < 1.0 - eps_gamma) & ~first
+    dalpha = np.where(unclamped, -dlg / (1.0 - alpha), 0.0)
+    deta = deta + np.where(unclamped, dalpha * lam, 0.0)
+    dlam = np.where(unclamped, dalpha * eta, 0.0)
+    live = (den != 0) & ~first
+    dbeta = np.where(live, deta / np.where(live, den, 1.0), 0.0)
+    dden = np.where(live, -deta * eta / np.where(live, den, 1.0), 0.0)
+    dlam = dlam + dden
+    dx = dx + 2.0 * dden[:, None] * xs
+    dk_ = np.zeros_like(k)
+    if T:
+        dk_[:-1] = dx[1:]
+    return {"dq": dq, "dk": dk_, "dv": dvv, "dbeta": dbeta, "dlam": dlam,
+            "dS0": dS0, "dtail": dx[0] if (T and pos > 0) else None}
