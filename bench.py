@@ -397,6 +397,218 @@ def run_ours(args, w):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------------------------------
+# backward workloads (falcon_bwd)
+
+ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12  # fp32 FMA lanes x 2 flops x max SM clock
+
+
+def _bwd_flops_per_chunk(w):
+    """fp32 flops the three backward kernels issue per 64-token chunk (64 x 64 x 64 products, 2 flops
+    per multiply-add): Falcon-1 prep 10 products and the triangular inverse (~1/3), the two scans 2,
+    gradients 15; Falcon-1A prep 2, scans 2, gradients 9."""
+    one = 2 * 64 ** 3
+    return one * ((10 + 1 / 3 + 2 + 15) if w.variant == "falcon1" else (2 + 2 + 9))
+
+
+def _bwd_bytes(w, es):
+    """Bytes a backward step must move at least once: q, k, v, dout read (dtype), beta, lambda read,
+    the fp32 gradients of q, k, v, beta, lambda written, dS_final read and dS0 written."""
+    BH = w.batch * w.heads
+    tok = BH * w.seqlen
+    return tok * (2 * w.dk + 2 * w.dv) * es + tok * 8 + tok * (2 * w.dk + w.dv) * 4 + tok * 8 \
+        + 2 * BH * w.dk * w.dv * 4 + (BH * w.dk * w.dv * 4 if w.nonzero_s0 else 0)
+
+
+def cpu_baseline_bwd(w, budget_s=12.0):
+    import torch
+
+    from oracle import falcon_bwd as OB
+    from weight_linear_attention_gb300 import inputs as I
+
+    inp = I.make_inputs(w, seed=0, batch=1)
+    inp.update(I.make_adjoints(w, seed=0, batch=1))
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        OB.falcon_ref_bwd(w.variant_id, inp["q"], inp["k"], inp["v"], inp["beta"], inp["lam"], inp["dout"],
+                          inp["S0"], inp["dS_final"], eps=w.eps, eps_gamma=w.eps_gamma)
+        runs += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": runs * w.seqlen / el, "unit": "tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"{runs} runs of batch row 0 ({w.heads} heads x {w.seqlen} tokens), fp64 autograd, {el:.1f} s"}
+
+
+def run_reference_bwd(args, w):
+    _, rank, _, _ = _dist_setup()
+    if rank != 0:
+        return
+    import torch
+
+    from oracle import falcon_bwd as OB
+    from weight_linear_attention_gb300 import inputs as I
+
+    inp = I.make_inputs(w, seed=0, batch=1)
+    inp.update(I.make_adjoints(w, seed=0, batch=1))
+
+    def step():
+        OB.falcon_ref_bwd(w.variant_id, inp["q"], inp["k"], inp["v"], inp["beta"], inp["lam"], inp["dout"],
+                          inp["S0"], inp["dS_final"], eps=w.eps, eps_gamma=w.eps_gamma)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = w.seqlen * args.steps / el
+    line = {
+        "impl": "reference", "metric": "falcon_bwd_tokens_per_s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "seq_len": w.seqlen, "d": w.dk,
+                   "chunk": w.chunk, "variant": w.variant, "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
+                         "sample": f"batch row 0 of {w.batch}, all {w.heads} heads, all {w.seqlen} tokens"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours_bwd(args, w):
+    import torch
+
+    from weight_linear_attention_gb300 import build as fbuild
+    from weight_linear_attention_gb300 import falcon as F
+    from weight_linear_attention_gb300 import inputs as I
+
+    dist, rank, world, local = _dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fbuild.build()
+    F.load()
+    es = 4 if w.dtype == "f32" else 2
+    B, H, T, dk, dv = w.batch, w.heads, w.seqlen, w.dk, w.dv
+    inp = I.make_inputs(w, seed=0)
+    inp.update(I.make_adjoints(w, seed=0))
+    dims = F.make_dims(B, H, T, dk, dv, dtype=F.FALCON_F32 if w.dtype == "f32" else F.FALCON_BF16, eps=w.eps,
+                       eps_gamma=w.eps_gamma)
+    step_bytes = _bwd_bytes(w, es)
+    nsets = max(2, -(-3 * L2_BYTES // step_bytes) + 1)
+    names_in = [n for n in ("q", "k", "v", "beta", "lam", "S0", "dout", "dS_final") if inp.get(n) is not None]
+    host = {n: inp[n].contiguous() for n in names_in}
+    f32 = dict(dtype=torch.float32, device=dev)
+
+    def new_set():
+        d = {n: host[n].to(dev) for n in names_in}
+        d.update(dq=torch.empty((B, H, T, dk), **f32), dk=torch.empty((B, H, T, dk), **f32),
+                 dv=torch.empty((B, H, T, dv), **f32), dbeta=torch.empty((B, H, T), **f32),
+                 dlam=torch.empty((B, H, T), **f32), dS0=torch.empty((B, H, dk, dv), **f32))
+        return d
+
+    sets = [new_set() for _ in range(nsets)]
+    ws = torch.empty(F.falcon_bwd_workspace_bytes(w.variant_id, dims, w.chunk), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch(d, strm):
+        st = F.falcon_bwd(w.variant_id, d["q"], d["k"], d["v"], d["beta"], d["lam"], d.get("S0"), None, d["dout"],
+                          d["dS_final"], d["dq"], d["dk"], d["dv"], d["dbeta"], d["dlam"], d["dS0"], None, dims,
+                          w.chunk, ws, stream=strm.cuda_stream)
+        if st != 0:
+            raise F.FalconError(st, "falcon_bwd")
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            launch(sets[i % nsets], stream)
+        stream.synchronize()
+        clocks = Clocks(local) if rank == 0 else None
+        t_soak, i = time.perf_counter(), 0
+        while time.perf_counter() - t_soak < args.soak_s:
+            launch(sets[i % nsets], stream)
+            i += 1
+            if i % 16 == 0:
+                stream.synchronize()
+        stream.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            launch(sets[i % nsets], stream)
+        e1.record(stream)
+        stream.synchronize()
+        if dist is not None:
+            dist.barrier()
+        clk = clocks.stop() if clocks else None
+        total_ms = e0.elapsed_time(e1)
+        if F.falcon_device_status(stream.cuda_stream) != 0:
+            raise SystemExit("device-side timeout during the timed region")
+        # end to end: pinned host inputs in, every gradient out, per step
+        e2e = None
+        if not args.no_e2e:
+            hin = {n: host[n].pin_memory() for n in names_in}
+            outs = ("dq", "dk", "dv", "dbeta", "dlam", "dS0")
+            hout = {n: torch.empty(sets[0][n].shape, dtype=torch.float32).pin_memory() for n in outs}
+            d = sets[0]
+
+            def e2e_step():
+                for n in names_in:
+                    d[n].copy_(hin[n], non_blocking=True)
+                launch(d, stream)
+                for n in outs:
+                    hout[n].copy_(d[n], non_blocking=True)
+
+            for _ in range(3):
+                e2e_step()
+            stream.synchronize()
+            n_e = max(3, min(args.steps, 20))
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(n_e):
+                e2e_step()
+            a1.record(stream)
+            stream.synchronize()
+            e2e_ms = _barrier_max(dist, a0.elapsed_time(a1) / n_e)
+            e2e = {"value": world * B * T / (e2e_ms / 1e3), "unit": "tokens/s",
+                   "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
+                   "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout.values())}
+    total_ms = _barrier_max(dist, total_ms)
+    ms_step = total_ms / args.steps
+    value = _job_value(world, B * T, args.steps, total_ms)
+    if rank != 0:
+        return
+    hbm, _, src = _peaks()
+    chunks = B * H * (-(-T // w.chunk))
+    flops = _bwd_flops_per_chunk(w) * chunks
+    achieved = flops / (ms_step / 1e3) / 1e12
+    line = {
+        "metric": "falcon_bwd_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if w.dtype == "f32" else "bf16-in/f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "variant": w.variant, "batch": B, "heads": H, "seq_len": T, "d": dk,
+                   "chunk": w.chunk, "parallelism": f"dp{world} (independent sequences per GPU, no collective)",
+                   "l2": f"rotating {nsets} input/gradient sets of {step_bytes / 1e6:.1f} MB (> L2 between reuses)",
+                   "kernel": "backward: CUDA-core prep, chain and gradient kernels"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
+                     "frac": achieved / ALU_PEAK_TFLOPS, "traffic": None,
+                     "scope": "one falcon_bwd call (all three kernels); fp32 FMA flops of the chunk algebra",
+                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz",
+                     "flops_per_step": flops, "hbm_algorithmic_bytes_per_step": step_bytes,
+                     "hbm_frac": step_bytes / (ms_step / 1e3) / 1e9 / hbm, "hbm_peak_source": src},
+        "e2e": e2e,
+        "gpu_launches": args.steps * 3,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_bwd(w)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -421,7 +633,9 @@ def main():
         w = w.with_(seqlen=args.seqlen)
     if args.batch is not None:
         w = w.with_(batch=args.batch)
-    if args.impl == "reference":
+    if w.backward:
+        (run_reference_bwd if args.impl == "reference" else run_ours_bwd)(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_ours(args, w)

@@ -166,7 +166,44 @@ int falcon_device_status(void* stream);
  * Without a workspace, 3 becomes 2. Host only, no launch. */
 int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk);
 
-/* ABI version of this header: 2. */
+/*
+ * falcon_bwd — gradients of one falcon_fwd call (Falcon-1 and 1A; dk = dv = 64; chunk 64).
+ * Given the adjoints dout of `out` and dS_final of `S_final`, returns the gradients of
+ * L = sum(out * dout) + sum(S_final * dS_final) with respect to every input of the call
+ * ([PL] §D.2, §E.3, §G.3: the chunk-parallel backward through the triangular solve, the Gram
+ * matrix, the chunk-local decay prefixes, the clamp and the step-size normalisation).
+ * Conventions of the gradient where the forward pass is not smooth ([PL] §D.2, §E.3, §G.3):
+ * where the clamp binds (eta*lambda >= 1 - eps_gamma) alpha is a constant and passes no gradient;
+ * where eta is 0 by definition (a zero denominator; the first step of a fresh sequence) beta,
+ * lambda and x receive nothing through it.
+ *   q, k, v, beta, lambda, S0, tail, dims, chunk   exactly as passed to falcon_fwd (window 1,
+ *             so `tail` is the pending key k_pos alone; beta [B,H,T])
+ *   dout      [B,H,T,dv] dtype        adjoint of out
+ *   dS_final  fp32 [B,H,dk,dv] or NULL (zero adjoint of S_final)
+ *   dq, dk    fp32 [B,H,T,dk]         dk[..., T-1, :] is 0: the last key reaches only tail_out,
+ *                                     whose gradient (the next call's dtail) the caller adds there
+ *   dv        fp32 [B,H,T,dv]
+ *   dbeta, dlambda  fp32 [B,H,T]      0 at the first step of a fresh sequence
+ *   dS0       fp32 [B,H,dk,dv] or NULL: gradient of S0 (of the zero state when S0 is NULL)
+ *   dtail     fp32 [B,H,dk] or NULL: gradient of the tail key; must be NULL when pos == 0
+ *   workspace at least falcon_bwd_workspace_bytes() bytes of device scratch (required when it is
+ *             nonzero); contents ignored on entry, unspecified on return
+ * Every output and the workspace must overlap no other argument. Alignment: q, k, v, tail, dout,
+ * S0, dS_final, dq, dk, dv, dS0, dtail 16 bytes; beta, lambda, dbeta, dlambda 4; workspace 256.
+ * Shapes other than the above return FALCON_ERR_UNSUPPORTED. Asynchronous on `stream`.
+ */
+int falcon_bwd(int variant, const void* q, const void* k, const void* v, const float* beta,
+               const float* lambda, const float* S0, const void* tail, const void* dout,
+               const float* dS_final, float* dq, float* dk, float* dv, float* dbeta, float* dlambda,
+               float* dS0, float* dtail, const falcon_dims_t* dims, int chunk, void* workspace,
+               size_t workspace_bytes, void* stream);
+
+/* Workspace bytes falcon_bwd needs: B*H*ceil(T/64) * 96 KiB (per chunk: the transition, its
+ * offset, the state-free adjoint term, the inverse of the chunk's triangular system, the chunk-start
+ * state and the chunk-end adjoint, each 64 x 64 fp32); 0 for invalid or unsupported arguments. */
+size_t falcon_bwd_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk);
+
+/* ABI version of this header: 3. */
 int falcon_abi_version(void);
 
 #ifdef __cplusplus

@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(F.EXPORTED), names
     for n in names:
         assert hasattr(lib, n), n
-    assert F.falcon_abi_version() == 2
+    assert F.falcon_abi_version() == 3
 
 
 def test_dims_struct_layout():

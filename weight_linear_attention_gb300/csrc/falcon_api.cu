@@ -158,11 +158,18 @@ int validate(int variant, const void* q, const void* k, const void* v, const flo
     return FALCON_OK;
 }
 
+// Shape checks of falcon_bwd on top of validate_shape.
+int validate_bwd_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail, falcon::Launch* a) {
+    const int st = validate_shape(variant, d, chunk, has_tail, a);
+    if (st != FALCON_OK) return st;
+    return falcon::bwd_supported(*a) ? FALCON_OK : FALCON_ERR_UNSUPPORTED;
+}
+
 }  // namespace
 
 extern "C" {
 
-int falcon_abi_version(void) { return 2; }
+int falcon_abi_version(void) { return 3; }
 
 size_t falcon_tail_bytes(const falcon_dims_t* d) {
     if (!d || d->batch < 0 || d->heads < 0 || d->dk <= 0 || d->dv <= 0 || d->window < 1) return 0;
@@ -222,6 +229,71 @@ int falcon_fwd_static(int variant, const void* q, const void* k, const void* v, 
     if (need > 0 && !(ws = static_workspace_address())) return FALCON_ERR_CUDA;
     return falcon_fwd(variant, q, k, v, beta, lambda, S0, tail, out, S_final, tail_out, dims, chunk, ws,
                       ws ? FALCON_STATIC_WORKSPACE_BYTES : 0, stream);
+}
+
+size_t falcon_bwd_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk) {
+    falcon::Launch a = {};
+    if (validate_bwd_shape(variant, dims, chunk, dims && dims->pos > 0, &a) != FALCON_OK) return 0;
+    return falcon::bwd_workspace_bytes(a);
+}
+
+int falcon_bwd(int variant, const void* q, const void* k, const void* v, const float* beta, const float* lambda,
+               const float* S0, const void* tail, const void* dout, const float* dS_final, float* dq, float* dk,
+               float* dv, float* dbeta, float* dlambda, float* dS0, float* dtail, const falcon_dims_t* dims,
+               int chunk, void* workspace, size_t workspace_bytes, void* stream) {
+    falcon::Launch a = {};
+    int st = validate_bwd_shape(variant, dims, chunk, tail != nullptr, &a);
+    if (st != FALCON_OK) return st;
+    const int64_t BH = a.B * a.H;
+    const int64_t tokens = BH * a.T;
+    const size_t es = a.bf16 ? 2 : 4;
+    if (dtail && a.pos == 0) return FALCON_ERR_INVALID_ARG;
+    if (tokens > 0 && (!q || !k || !v || !beta || !lambda || !dout || !dq || !dk || !dv || !dbeta || !dlambda))
+        return FALCON_ERR_INVALID_ARG;
+    const size_t need = falcon::bwd_workspace_bytes(a);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return FALCON_ERR_INVALID_ARG;
+    const void* al16[] = {q, k, v, tail, dout, S0, dS_final, dq, dk, dv, dS0, dtail};
+    for (const void* p : al16)
+        if (p && !aligned(p, 16)) return FALCON_ERR_MISALIGNED;
+    const void* al4[] = {beta, lambda, dbeta, dlambda};
+    for (const void* p : al4)
+        if (p && !aligned(p, 4)) return FALCON_ERR_MISALIGNED;
+    if (workspace && !aligned(workspace, 256)) return FALCON_ERR_MISALIGNED;
+    // every written buffer (the gradients and the workspace) overlaps no other argument
+    const size_t sbytes = (size_t)BH * a.dk * a.dv * 4;
+    const Range ins[] = {
+        range_of(q, (size_t)tokens * a.dk * es), range_of(k, (size_t)tokens * a.dk * es),
+        range_of(v, (size_t)tokens * a.dv * es), range_of(beta, (size_t)tokens * 4),
+        range_of(lambda, (size_t)tokens * 4), range_of(dout, (size_t)tokens * a.dv * es),
+        S0 ? range_of(S0, sbytes) : Range{0, 0}, dS_final ? range_of(dS_final, sbytes) : Range{0, 0},
+        tail ? range_of(tail, tail_bytes_of(dims)) : Range{0, 0},
+    };
+    const Range outs[] = {
+        range_of(dq, (size_t)tokens * a.dk * 4), range_of(dk, (size_t)tokens * a.dk * 4),
+        range_of(dv, (size_t)tokens * a.dv * 4), range_of(dbeta, (size_t)tokens * 4),
+        range_of(dlambda, (size_t)tokens * 4), dS0 ? range_of(dS0, sbytes) : Range{0, 0},
+        dtail ? range_of(dtail, (size_t)BH * a.dk * 4) : Range{0, 0},
+        need > 0 ? range_of(workspace, need) : Range{0, 0},
+    };
+    const int no = (int)(sizeof(outs) / sizeof(outs[0]));
+    for (int i = 0; i < no; ++i) {
+        for (const Range& r : ins)
+            if (overlaps(outs[i], r)) return FALCON_ERR_INVALID_ARG;
+        for (int j = i + 1; j < no; ++j)
+            if (overlaps(outs[i], outs[j])) return FALCON_ERR_INVALID_ARG;
+    }
+    if (BH == 0) return FALCON_OK;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.beta = beta;
+    a.lam = lambda;
+    a.S0 = S0;
+    a.tail = tail;
+    a.ws = workspace;
+    a.ws_bytes = workspace_bytes;
+    falcon::BwdArgs g = {dout, dS_final, dq, dk, dv, dbeta, dlambda, dS0, dtail};
+    return falcon::launch_bwd(a, g, static_cast<cudaStream_t>(stream));
 }
 
 int falcon_device_status(void* stream) {

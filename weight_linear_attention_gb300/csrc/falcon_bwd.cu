@@ -1,0 +1,769 @@
+// Chunk-parallel backward pass of Falcon-1 and 1A (dk = dv = 64, chunk 64, fp32 or bf16 inputs,
+// fp32 arithmetic and gradients). "Fast Weight Attention for Continual Learning", paperlayer summary
+// §D.2, §E.3, §G.3: reverse the output materialisation, the inter-chunk recurrence and the local
+// structure, backpropagate through the triangular solve, the Gram matrix, the chunk-local decay
+// prefixes, the clamp and the step-size normalisation.
+//
+// Per chunk of C tokens (rows i, j; X the shifted keys, Q, Y = V, dO the output adjoint; eta_j,
+// L_i = sum_{u<=i} log(1 - alpha_u) reset at the chunk start, Lx_i = L_{i-1}; S the chunk-start state,
+// dS' the adjoint of the chunk-end state):
+//   forward   A_ij = eta_j e^{Lx_i - L_j} x_i.x_j (j < i), P_ij = eta_j e^{L_i - L_j} q_i.x_j (j <= i),
+//             T = (I + A)^-1, R = T (Y - diag(e^Lx) X S), O = diag(e^L) Q S + P R,
+//             S' = e^{L_C} S + X^T diag(w) R with w_j = eta_j e^{L_C - L_j}      (Falcon-1A: R = Y)
+//   backward  dR = P^T dO + diag(w) X dS',  dZ = T^T dR,  dV = dZ,
+//             dP = dO R^T (j <= i),  dA = -dZ R^T (j < i),
+//             dQ = diag(e^L) dO S^T + dSc X,  dX = dSc^T Q + (dG + dG^T) X - diag(e^Lx) dZ S^T
+//                  + diag(w) R dS'^T + 2 dden x,  with dSc_ij = dP_ij eta_j e^{L_i - L_j} and
+//                  dG_ij = dA_ij eta_j e^{Lx_i - L_j},
+//             d eta, d L from every factor, d log(gamma_u) = sum_{i >= u} dL_i inside the chunk,
+//             d alpha = -d log(gamma) / gamma where the clamp is inactive (0 where it binds),
+//             eta = beta / den: d beta = d eta / den, d den = -d eta eta / den (none where eta is 0
+//             by definition: a zero denominator or the first step of a fresh sequence).
+// The chunk-start state adjoint is dS = M^T dS' + V with M = e^{L_C} I - X^T diag(w) T diag(e^Lx) X
+// and V = Q^T diag(e^L) dO - X^T diag(e^Lx) T^T P^T dO, so three launches do the whole pass:
+//   falcon_bwd_prep   every chunk at once: T, the forward transition (M, U = X^T diag(w) T Y) and V;
+//   falcon_bwd_chain  per sequence (four CTAs of 16 value columns each): S_{n+1} = M_n S_n + U_n
+//                     forward, then dS_n = M_n^T dS_{n+1} + V_n backward, storing S_n and dS_{n+1};
+//   falcon_bwd_grad   every chunk at once: all input gradients from S_n and dS_{n+1}.
+// Every 64 x 64 x 64 product runs on the CUDA cores in fp32 from shared memory.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "falcon_internal.h"
+
+namespace falcon {
+namespace {
+
+constexpr int kD = 64;        // dk = dv
+constexpr int kC = 64;        // chunk length
+constexpr int kLd = 65;       // shared-memory row stride (floats): conflict-free rows and columns
+constexpr int kMat = kC * kLd;
+constexpr int kThreads = 256;
+constexpr int kCols = 16;     // value columns per chain CTA
+constexpr int kWsMat = kD * kD;             // floats per workspace matrix
+constexpr int kWsChunk = 6 * kWsMat;        // M, U, V, T, S_n, dS_{n+1}
+enum { kWsM = 0, kWsU = 1, kWsV = 2, kWsT = 3, kWsS = 4, kWsDS = 5 };
+
+struct BParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* dout;
+    const void* tail;  // pending key k_pos [BH][dk] (pos > 0) or null
+    const float* beta;
+    const float* lam;
+    const float* S0;
+    const float* dS_final;
+    float* dq;
+    float* dk;
+    float* dv;
+    float* dbeta;
+    float* dlam;
+    float* dS0;
+    float* dtail;
+    float* ws;
+    long long T, pos, N, BH;  // tokens, position, chunks per sequence, sequences
+    float eps, eps_gamma;
+};
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+// Scalars of one chunk, recomputed identically by the prep and gradient kernels.
+struct Scal {
+    float eta[kC], lam[kC], den[kC], gam[kC], L[kC], Lx[kC], eL[kC], eLx[kC], w[kC];
+    int unc[kC], live[kC];  // clamp inactive (alpha differentiable); eta = beta / den differentiable
+    float eLC;
+};
+
+// Rows t0 .. t0 + n - 1 of a [BH, T, 64] tensor into a shared 64 x 64 tile (zero rows past n).
+// shift = 1 loads the shifted keys x_t = k_{t-1} (row -1 is the tail key, or zero).
+template <typename Tin>
+__device__ void load_rows(float* dst, const Tin* src, long long bh, long long T, long long t0, int n, int shift,
+                          const Tin* tail) {
+    for (int e = threadIdx.x; e < kC * kD; e += kThreads) {
+        const int r = e >> 6, c = e & 63;
+        const long long t = t0 + r - shift;
+        float x = 0.f;
+        if (r < n) {
+            if (t >= 0) x = ldf(src + (bh * T + t) * kD + c);
+            else if (tail) x = ldf(tail + bh * kD + c);
+        }
+        dst[r * kLd + c] = x;
+    }
+}
+
+__device__ void load_ws(float* dst, const float* src) {
+    for (int e = threadIdx.x; e < kD * kD; e += kThreads) dst[(e >> 6) * kLd + (e & 63)] = src[e];
+}
+
+// Per-row scalars of the chunk from X (shifted keys), beta and lambda; then the chunk-local log prefixes.
+__device__ void chunk_scalars(Scal& s, const float* X, const BParams& p, long long bh, long long t0, int n) {
+    const int i = threadIdx.x;
+    if (i < kC) {
+        float nx = 0.f;
+#pragma unroll 8
+        for (int c = 0; c < kD; ++c) nx = fmaf(X[i * kLd + c], X[i * kLd + c], nx);
+        float eta = 0.f, alpha = 0.f, lm = 0.f, den = 0.f;
+        int unc = 0, live = 0;
+        if (i < n) {
+            const long long t = t0 + i;
+            lm = p.lam[bh * p.T + t];
+            den = nx + lm + p.eps;
+            const bool first = p.pos + t == 0;
+            if (!first) {
+                eta = den == 0.f ? 0.f : p.beta[bh * p.T + t] / den;
+                const float raw = eta * lm, cap = 1.f - p.eps_gamma;
+                unc = raw < cap;
+                alpha = unc ? raw : cap;
+                live = den != 0.f;
+            }
+        }
+        s.eta[i] = eta;
+        s.lam[i] = lm;
+        s.den[i] = den;
+        s.gam[i] = 1.f - alpha;
+        s.unc[i] = unc;
+        s.live[i] = live;
+        s.L[i] = log1pf(-alpha);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {  // inclusive prefix over 64 rows: lane l holds rows 2l, 2l + 1
+        const int l = threadIdx.x;
+        const float a = s.L[2 * l], b = s.L[2 * l + 1];
+        float v = a + b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v, o);
+            if (l >= o) v += u;
+        }
+        const float ex = v - a - b;  // exclusive prefix of row 2l
+        s.L[2 * l] = ex + a;
+        s.L[2 * l + 1] = v;
+        __syncwarp();
+        const float LC = __shfl_sync(0xffffffffu, v, 31);
+        if (l == 0) s.eLC = expf(LC);
+        s.Lx[2 * l] = ex;
+        s.Lx[2 * l + 1] = ex + a;
+        s.eL[2 * l] = expf(ex + a);
+        s.eL[2 * l + 1] = expf(v);
+        s.eLx[2 * l] = expf(ex);
+        s.eLx[2 * l + 1] = expf(ex + a);
+        s.w[2 * l] = s.eta[2 * l] * expf(LC - (ex + a));
+        s.w[2 * l + 1] = s.eta[2 * l + 1] * expf(LC - v);
+    }
+    __syncthreads();
+}
+
+// acc[m][n] += sum_k A(i_m, k) B(k, j_n) over k < 64, with i_m = ty + 16 m, j_n = tx + 16 n.
+// TA: A is stored transposed (A(i, k) at a[k][i]); TB: B is stored transposed (B(k, j) at b[j][k]).
+template <bool TA, bool TB>
+__device__ __forceinline__ void mm(float (&acc)[4][4], const float* a, const float* b) {
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 4
+    for (int k = 0; k < kD; ++k) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) av[m] = TA ? a[k * kLd + ty + 16 * m] : a[(ty + 16 * m) * kLd + k];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) bv[n] = TB ? b[(tx + 16 * n) * kLd + k] : b[k * kLd + tx + 16 * n];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int n = 0; n < 4; ++n) acc[m][n] = fmaf(av[m], bv[n], acc[m][n]);
+    }
+}
+
+__device__ __forceinline__ void zero(float (&acc)[4][4]) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) acc[m][n] = 0.f;
+}
+
+#define FOR_TILE(...)                                               \
+    _Pragma("unroll") for (int m = 0; m < 4; ++m) {                 \
+        const int i = (threadIdx.x >> 4) + 16 * m;                  \
+        _Pragma("unroll") for (int n = 0; n < 4; ++n) {             \
+            const int j = (threadIdx.x & 15) + 16 * n;              \
+            __VA_ARGS__                                             \
+        }                                                           \
+    }
+
+// Sum of v over the 16 threads that share a tile row (one half-warp).
+__device__ __forceinline__ float row_sum16(float v) {
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// T = (I + A)^-1 for a strictly lower A, by forward substitution one row at a time
+// (thread c = tid & 63 owns column c; the four warps-quarters split the sum over j).
+__device__ void unit_lower_inverse(float* Tm, const float* A, float* part) {
+    const int c = threadIdx.x & 63, r = threadIdx.x >> 6;
+    for (int e = threadIdx.x; e < kC * kLd; e += kThreads) Tm[e] = 0.f;
+    __syncthreads();
+    if (threadIdx.x < kC) Tm[threadIdx.x * kLd + threadIdx.x] = 1.f;
+    __syncthreads();
+    for (int i = 1; i < kC; ++i) {
+        float a = 0.f;
+        for (int j = r; j < i; j += 4) a = fmaf(A[i * kLd + j], Tm[j * kLd + c], a);
+        part[r * kC + c] = a;
+        __syncthreads();
+        if (threadIdx.x < kC && c < i) Tm[i * kLd + c] = -(part[c] + part[kC + c] + part[2 * kC + c] + part[3 * kC + c]);
+        __syncthreads();
+    }
+}
+
+// --------------------------------------------------------------------------------------------------
+// falcon_bwd_prep: one CTA per chunk.
+template <typename Tin, bool IP>
+__global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
+    extern __shared__ __align__(16) float sm[];
+    float* X = sm;
+    float* Q = X + kMat;
+    float* Y = Q + kMat;
+    float* dO = Y + kMat;
+    float* A = dO + kMat;
+    float* Tm = A + kMat;
+    float* P = Tm + kMat;
+    float* DX = P + kMat;
+    float* B1 = DX + kMat;
+    float* B2 = B1 + kMat;
+    Scal& s = *reinterpret_cast<Scal*>(B2 + kMat);
+    float* part = reinterpret_cast<float*>(&s + 1);
+
+    const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N;
+    const long long t0 = nck * kC;
+    const int n = (int)min((long long)kC, p.T - t0);
+    const Tin* tail = static_cast<const Tin*>(p.tail);
+    load_rows(X, static_cast<const Tin*>(p.k), bh, p.T, t0, n, 1, tail);
+    load_rows(Q, static_cast<const Tin*>(p.q), bh, p.T, t0, n, 0, (const Tin*)nullptr);
+    load_rows(Y, static_cast<const Tin*>(p.v), bh, p.T, t0, n, 0, (const Tin*)nullptr);
+    load_rows(dO, static_cast<const Tin*>(p.dout), bh, p.T, t0, n, 0, (const Tin*)nullptr);
+    __syncthreads();
+    chunk_scalars(s, X, p, bh, t0, n);
+    float* ws = p.ws + cid * kWsChunk;
+    float acc[4][4], acc2[4][4];
+
+    // Falcon-1: P, A and diag(e^Lx) X
+    if (!IP) {
+        zero(acc);
+        mm<false, true>(acc, Q, X);
+        FOR_TILE(P[i * kLd + j] = j <= i ? s.eta[j] * expf(s.L[i] - s.L[j]) * acc[m][n] : 0.f;)
+        zero(acc);
+        mm<false, true>(acc, X, X);
+        FOR_TILE(A[i * kLd + j] = j < i ? s.eta[j] * expf(s.Lx[i] - s.L[j]) * acc[m][n] : 0.f;
+                 DX[i * kLd + j] = s.eLx[i] * X[i * kLd + j];)
+    }
+    __syncthreads();
+    if (IP) {
+        // M = e^{L_C} I, U = X^T diag(w) Y, V = Q^T diag(e^L) dO
+        for (int e = threadIdx.x; e < kC * kD; e += kThreads) {
+            const int r = e >> 6, c = e & 63;
+            B2[r * kLd + c] = s.w[r] * Y[r * kLd + c];
+            dO[r * kLd + c] *= s.eL[r];
+        }
+        __syncthreads();
+        zero(acc);
+        mm<true, false>(acc, X, B2);
+        zero(acc2);
+        mm<true, false>(acc2, Q, dO);
+        FOR_TILE(ws[kWsM * kWsMat + i * kD + j] = i == j ? s.eLC : 0.f;
+                 ws[kWsU * kWsMat + i * kD + j] = acc[m][n];
+                 ws[kWsV * kWsMat + i * kD + j] = acc2[m][n];)
+        return;
+    }
+    unit_lower_inverse(Tm, A, part);
+    // B1 = diag(w) T diag(e^Lx) X, B2 = diag(w) T Y, A <- P^T dO
+    zero(acc);
+    mm<false, false>(acc, Tm, DX);
+    zero(acc2);
+    mm<false, false>(acc2, Tm, Y);
+    FOR_TILE(B1[i * kLd + j] = s.w[i] * acc[m][n]; B2[i * kLd + j] = s.w[i] * acc2[m][n];)
+    zero(acc);
+    mm<true, false>(acc, P, dO);
+    FOR_TILE(A[i * kLd + j] = acc[m][n];)
+    __syncthreads();
+    // M = e^{L_C} I - X^T B1, U = X^T B2; P <- T^T (P^T dO); dO <- diag(e^L) dO
+    zero(acc);
+    mm<true, false>(acc, X, B1);
+    zero(acc2);
+    mm<true, false>(acc2, X, B2);
+    FOR_TILE(ws[kWsM * kWsMat + i * kD + j] = (i == j ? s.eLC : 0.f) - acc[m][n];
+             ws[kWsU * kWsMat + i * kD + j] = acc2[m][n];
+             ws[kWsT * kWsMat + i * kD + j] = Tm[i * kLd + j];)
+    zero(acc);
+    mm<true, false>(acc, Tm, A);
+    __syncthreads();  // every read of P and dO above is done
+    FOR_TILE(P[i * kLd + j] = acc[m][n]; dO[i * kLd + j] *= s.eL[i];)
+    __syncthreads();
+    // V = Q^T diag(e^L) dO - (diag(e^Lx) X)^T T^T P^T dO
+    zero(acc);
+    mm<true, false>(acc, Q, dO);
+    zero(acc2);
+    mm<true, false>(acc2, DX, P);
+    FOR_TILE(ws[kWsV * kWsMat + i * kD + j] = acc[m][n] - acc2[m][n];)
+}
+
+// --------------------------------------------------------------------------------------------------
+// falcon_bwd_chain: one CTA per (sequence, group of 16 value columns). Thread (r, c): rows r + 16 m.
+__global__ void __launch_bounds__(kThreads) falcon_bwd_chain(const BParams p) {
+    __shared__ __align__(16) float Ms[2][kD * kLd];
+    __shared__ float Sv[2][kD][kCols + 1];
+    const long long bh = blockIdx.x / (kD / kCols);
+    const int cg = (int)(blockIdx.x % (kD / kCols)) * kCols;
+    const int c = threadIdx.x & 15, r = threadIdx.x >> 4;
+    const long long N = p.N;
+    float* wsq = p.ws + bh * N * kWsChunk;
+
+    auto load_M = [&](long long nck, float (&reg)[16]) {
+        const float4* src = reinterpret_cast<const float4*>(wsq + nck * kWsChunk + kWsM * kWsMat);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float4 v = src[threadIdx.x + u * kThreads];
+            reg[4 * u] = v.x;
+            reg[4 * u + 1] = v.y;
+            reg[4 * u + 2] = v.z;
+            reg[4 * u + 3] = v.w;
+        }
+    };
+    auto store_M = [&](float* dst, const float (&reg)[16]) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = 4 * (threadIdx.x + u * kThreads), row = e >> 6, col = e & 63;
+#pragma unroll
+            for (int z = 0; z < 4; ++z) dst[row * kLd + col + z] = reg[4 * u + z];
+        }
+    };
+
+    float reg[16];
+    // forward: S_{n+1} = M_n S_n + U_n, storing S_n
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int i = r + 16 * m;
+        Sv[0][i][c] = p.S0 ? p.S0[(bh * kD + i) * kD + cg + c] : 0.f;
+    }
+    if (N > 0) {
+        load_M(0, reg);
+        store_M(Ms[0], reg);
+    }
+    __syncthreads();
+    for (long long nck = 0; nck < N; ++nck) {
+        const int b = (int)(nck & 1);
+        float* wc = wsq + nck * kWsChunk;
+        if (nck + 1 < N) load_M(nck + 1, reg);
+        float acc[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int i = r + 16 * m;
+            wc[kWsS * kWsMat + i * kD + cg + c] = Sv[b][i][c];
+            acc[m] = wc[kWsU * kWsMat + i * kD + cg + c];
+        }
+#pragma unroll 8
+        for (int kk = 0; kk < kD; ++kk) {
+            const float sv = Sv[b][kk][c];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) acc[m] = fmaf(Ms[b][(r + 16 * m) * kLd + kk], sv, acc[m]);
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) Sv[b ^ 1][r + 16 * m][c] = acc[m];
+        if (nck + 1 < N) store_M(Ms[b ^ 1], reg);
+        __syncthreads();
+    }
+    // backward: dS_n = M_n^T dS_{n+1} + V_n, storing dS_{n+1}
+    int b = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int i = r + 16 * m;
+        Sv[0][i][c] = p.dS_final ? p.dS_final[(bh * kD + i) * kD + cg + c] : 0.f;
+    }
+    if (N > 0) {
+        load_M(N - 1, reg);
+        store_M(Ms[0], reg);
+    }
+    __syncthreads();
+    for (long long nck = N - 1; nck >= 0; --nck, b ^= 1) {
+        float* wc = wsq + nck * kWsChunk;
+        if (nck > 0) load_M(nck - 1, reg);
+        float acc[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int i = r + 16 * m;
+            wc[kWsDS * kWsMat + i * kD + cg + c] = Sv[b][i][c];
+            acc[m] = wc[kWsV * kWsMat + i * kD + cg + c];
+        }
+#pragma unroll 8
+        for (int kk = 0; kk < kD; ++kk) {
+            const float sv = Sv[b][kk][c];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) acc[m] = fmaf(Ms[b][kk * kLd + r + 16 * m], sv, acc[m]);
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) Sv[b ^ 1][r + 16 * m][c] = acc[m];
+        if (nck > 0) store_M(Ms[b ^ 1], reg);
+        __syncthreads();
+    }
+    if (p.dS0)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int i = r + 16 * m;
+            p.dS0[(bh * kD + i) * kD + cg + c] = Sv[b][i][c];
+        }
+}
+
+// --------------------------------------------------------------------------------------------------
+// falcon_bwd_grad: one CTA per chunk.
+template <typename Tin, bool IP>
+__global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
+    extern __shared__ __align__(16) float sm[];
+    float* X = sm;
+    float* Q = X + kMat;
+    float* Y = Q + kMat;   // Y; Falcon-1: Z, then P, then the dX accumulator
+    float* dO = Y + kMat;
+    float* S = dO + kMat;
+    float* dS = S + kMat;
+    float* Tm = dS + kMat;  // T (Falcon-1), then dP -> dSc
+    float* b0 = Tm + kMat;  // Falcon-1: R; Falcon-1A: P
+    float* b1 = b0 + kMat;  // X dS', then dR; Falcon-1: dA -> dG + dG^T
+    float* b2 = b1 + kMat;  // Sc
+    float* b3 = b2 + kMat;  // G (Falcon-1); Falcon-1A: the dX accumulator
+    float* b4 = IP ? b3 : b3 + kMat;  // dZ (Falcon-1)
+    Scal& s = *reinterpret_cast<Scal*>(b4 + kMat);
+    float* deta = reinterpret_cast<float*>(&s + 1);
+    float* dL = deta + kC;
+    float* dLx = dL + kC;
+    float* dw = dLx + kC;
+    float* c2 = dw + kC;
+    float* red = c2 + kC;  // [8] block reduction
+
+    float* R = IP ? Y : b0;
+    float* P = IP ? b0 : Y;
+    float* DXa = IP ? b3 : Y;
+
+    const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N;
+    const long long t0 = nck * kC;
+    const int n = (int)min((long long)kC, p.T - t0);
+    const Tin* tail = static_cast<const Tin*>(p.tail);
+    const float* ws = p.ws + cid * kWsChunk;
+    load_rows(X, static_cast<const Tin*>(p.k), bh, p.T, t0, n, 1, tail);
+    load_rows(Q, static_cast<const Tin*>(p.q), bh, p.T, t0, n, 0, (const Tin*)nullptr);
+    load_rows(Y, static_cast<const Tin*>(p.v), bh, p.T, t0, n, 0, (const Tin*)nullptr);
+    load_rows(dO, static_cast<const Tin*>(p.dout), bh, p.T, t0, n, 0, (const Tin*)nullptr);
+    load_ws(S, ws + kWsS * kWsMat);
+    load_ws(dS, ws + kWsDS * kWsMat);
+    if (!IP) load_ws(Tm, ws + kWsT * kWsMat);
+    if (threadIdx.x < kC) {
+        deta[threadIdx.x] = 0.f;
+        dL[threadIdx.x] = 0.f;
+        dLx[threadIdx.x] = 0.f;
+    }
+    if (threadIdx.x < 8) red[threadIdx.x] = 0.f;
+    __syncthreads();
+    chunk_scalars(s, X, p, bh, t0, n);
+    const int lane = threadIdx.x & 31, tx = threadIdx.x & 15;
+    float acc[4][4], acc2[4][4];
+
+    // <dS', S>
+    {
+        float a = 0.f;
+        for (int e = threadIdx.x; e < kD * kD; e += kThreads) {
+            const int rr = e >> 6, cc = e & 63;
+            a = fmaf(dS[rr * kLd + cc], S[rr * kLd + cc], a);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) red[threadIdx.x >> 5] = a;
+    }
+    // Z = Y - diag(e^Lx) X S (Falcon-1); X dS'
+    if (!IP) {
+        zero(acc);
+        mm<false, false>(acc, X, S);
+        FOR_TILE(Y[i * kLd + j] -= s.eLx[i] * acc[m][n];)
+    }
+    zero(acc);
+    mm<false, false>(acc, X, dS);
+    FOR_TILE(b1[i * kLd + j] = acc[m][n];)
+    __syncthreads();
+    // R = T Z (Falcon-1); Sc = Q X^T; G = X X^T (Falcon-1)
+    if (!IP) {
+        zero(acc);
+        mm<false, false>(acc, Tm, Y);
+        FOR_TILE(b0[i * kLd + j] = acc[m][n];)
+        zero(acc);
+        mm<false, true>(acc, X, X);
+        FOR_TILE(b3[i * kLd + j] = acc[m][n];)
+    }
+    zero(acc);
+    mm<false, true>(acc, Q, X);
+    FOR_TILE(b2[i * kLd + j] = acc[m][n];)
+    __syncthreads();
+    // dw_j = x_j^T dS' r_j; P
+    if (threadIdx.x < kC) {
+        const int j = threadIdx.x;
+        float a = 0.f;
+#pragma unroll 8
+        for (int cc = 0; cc < kD; ++cc) a = fmaf(b1[j * kLd + cc], R[j * kLd + cc], a);
+        dw[j] = a;
+    }
+    FOR_TILE(P[i * kLd + j] = j <= i ? s.eta[j] * expf(s.L[i] - s.L[j]) * b2[i * kLd + j] : 0.f;)
+    __syncthreads();
+    // dR = P^T dO + diag(w) X dS'  (Falcon-1A: dV = dR)
+    zero(acc);
+    mm<true, false>(acc, P, dO);
+    FOR_TILE(b1[i * kLd + j] = acc[m][n] + s.w[i] * b1[i * kLd + j];)
+    __syncthreads();
+    float* dvo = p.dv + (bh * p.T + t0) * kD;
+    if (!IP) {  // dZ = T^T dR = dV
+        zero(acc);
+        mm<true, false>(acc, Tm, b1);
+        FOR_TILE(b4[i * kLd + j] = acc[m][n]; if (i < n) dvo[i * kD + j] = acc[m][n];)
+    } else {
+        FOR_TILE(if (i < n) dvo[i * kD + j] = b1[i * kLd + j];)
+    }
+    __syncthreads();
+    // dP = dO R^T (j <= i) -> d eta, dL; dSc = dP eta_j e^{L_i - L_j}, into Tm
+    zero(acc);
+    mm<false, true>(acc, dO, R);
+    if (!IP) {
+        zero(acc2);
+        mm<false, true>(acc2, b4, R);  // dZ R^T = -dA
+    }
+    __syncthreads();  // Tm (T) and b1 (dR) are read no more
+    {
+        float rowL[4] = {0.f, 0.f, 0.f, 0.f}, colE[4] = {0.f, 0.f, 0.f, 0.f}, colL[4] = {0.f, 0.f, 0.f, 0.f};
+        FOR_TILE({
+            float v = 0.f;
+            if (j <= i) {
+                const float f = expf(s.L[i] - s.L[j]), d = acc[m][n];
+                const float pp = P[i * kLd + j];
+                colE[n] = fmaf(d * f, b2[i * kLd + j], colE[n]);
+                rowL[m] = fmaf(d, pp, rowL[m]);
+                colL[n] = fmaf(d, pp, colL[n]);
+                v = d * s.eta[j] * f;
+            }
+            Tm[i * kLd + j] = v;
+        })
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float v = row_sum16(rowL[m]);
+            if (tx == 0) atomicAdd(&dL[(threadIdx.x >> 4) + 16 * m], v);
+        }
+#pragma unroll
+        for (int n2 = 0; n2 < 4; ++n2) {
+            atomicAdd(&deta[tx + 16 * n2], colE[n2]);
+            atomicAdd(&dL[tx + 16 * n2], -colL[n2]);
+        }
+    }
+    if (!IP) {  // dA = -dZ R^T (j < i) -> d eta, dLx, dL; dG = dA eta_j e^{Lx_i - L_j}, into b1
+        float rowX[4] = {0.f, 0.f, 0.f, 0.f}, colE[4] = {0.f, 0.f, 0.f, 0.f}, colL[4] = {0.f, 0.f, 0.f, 0.f};
+        FOR_TILE({
+            float v = 0.f;
+            if (j < i) {
+                const float f = expf(s.Lx[i] - s.L[j]), d = -acc2[m][n];
+                const float g = b3[i * kLd + j];
+                const float aa = s.eta[j] * f * g * d;
+                colE[n] = fmaf(d * f, g, colE[n]);
+                rowX[m] += aa;
+                colL[n] += aa;
+                v = d * s.eta[j] * f;
+            }
+            b1[i * kLd + j] = v;
+        })
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float v = row_sum16(rowX[m]);
+            if (tx == 0) atomicAdd(&dLx[(threadIdx.x >> 4) + 16 * m], v);
+        }
+#pragma unroll
+        for (int n2 = 0; n2 < 4; ++n2) {
+            atomicAdd(&deta[tx + 16 * n2], colE[n2]);
+            atomicAdd(&dL[tx + 16 * n2], -colL[n2]);
+        }
+    }
+    __syncthreads();
+    if (!IP) {  // dG + dG^T: mirror the strict lower triangle into the upper one
+        for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
+            const int i = e >> 6, j = e & 63;
+            if (j > i) b1[i * kLd + j] = b1[j * kLd + i];
+        }
+    }
+    // dX accumulator: diag(w) R dS'^T  (for Falcon-1 it overwrites P, last read before the barrier above)
+    zero(acc);
+    mm<false, true>(acc, R, dS);
+    __syncthreads();
+    FOR_TILE(DXa[i * kLd + j] = s.w[i] * acc[m][n];)
+    __syncthreads();
+    // dX += dSc^T Q (+ (dG + dG^T) X - diag(e^Lx) dZ S^T, with dLx_i -= e^Lx_i x_i . (dZ S^T)_i)
+    zero(acc);
+    mm<true, false>(acc, Tm, Q);
+    if (!IP) {
+        mm<false, false>(acc, b1, X);
+        zero(acc2);
+        mm<false, true>(acc2, b4, S);
+        float rowX[4] = {0.f, 0.f, 0.f, 0.f};
+        FOR_TILE(DXa[i * kLd + j] += acc[m][n] - s.eLx[i] * acc2[m][n];
+                 rowX[m] = fmaf(X[i * kLd + j], acc2[m][n], rowX[m]);)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float v = row_sum16(rowX[m]);
+            const int i = (threadIdx.x >> 4) + 16 * m;
+            if (tx == 0) atomicAdd(&dLx[i], -s.eLx[i] * v);
+        }
+    } else {
+        FOR_TILE(DXa[i * kLd + j] += acc[m][n];)
+    }
+    // dQ = diag(e^L) dO S^T + dSc X, with dL_i += e^L_i q_i . (dO S^T)_i
+    zero(acc);
+    mm<false, true>(acc, dO, S);
+    zero(acc2);
+    mm<false, false>(acc2, Tm, X);
+    {
+        float rowL[4] = {0.f, 0.f, 0.f, 0.f};
+        float* dqo = p.dq + (bh * p.T + t0) * kD;
+        FOR_TILE(rowL[m] = fmaf(Q[i * kLd + j], acc[m][n], rowL[m]);
+                 if (i < n) dqo[i * kD + j] = s.eL[i] * acc[m][n] + acc2[m][n];)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float v = row_sum16(rowL[m]);
+            const int i = (threadIdx.x >> 4) + 16 * m;
+            if (tx == 0) atomicAdd(&dL[i], s.eL[i] * v);
+        }
+    }
+    __syncthreads();
+    // scalars: d eta and dL from w and the chunk-end decay; d log gamma; the clamp; eta = beta / den
+    if (threadIdx.x < 32) {
+        const int l = threadIdx.x;
+        float dwsum = 0.f;
+        float dl[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = 2 * l + h;
+            const float ww = dw[j] * s.w[j];
+            dwsum += ww;
+            deta[j] = fmaf(dw[j], expf(s.L[kC - 1] - s.L[j]), deta[j]);
+            dl[h] = dL[j] - ww + (j + 1 < kC ? dLx[j + 1] : 0.f);
+        }
+        dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 16);
+        dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 8);
+        dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 4);
+        dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 2);
+        dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 1);
+        float dss = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) dss += red[u];
+        if (l == 31) dl[1] += dwsum + s.eLC * dss;
+        // suffix sums: d log gamma_u = sum_{i >= u} dL_i
+        float v = dl[0] + dl[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_down_sync(0xffffffffu, v, o);
+            if (l + o < 32) v += u;
+        }
+        const float suf[2] = {v, v - dl[0]};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int u = 2 * l + h;
+            float db = 0.f, dlm = 0.f, cc = 0.f;
+            if (u < n) {
+                float de = deta[u];
+                if (s.unc[u]) {
+                    const float da = -suf[h] / s.gam[u];
+                    de = fmaf(da, s.lam[u], de);
+                    dlm = da * s.eta[u];
+                }
+                if (s.live[u]) {
+                    db = de / s.den[u];
+                    const float dden = -de * s.eta[u] / s.den[u];
+                    dlm += dden;
+                    cc = 2.f * dden;
+                }
+                p.dbeta[bh * p.T + t0 + u] = db;
+                p.dlam[bh * p.T + t0 + u] = dlm;
+            }
+            c2[u] = cc;
+        }
+    }
+    __syncthreads();
+    // dX = accumulator + 2 dden x; row i is dk of token t0 + i - 1 (row 0 of the call: the tail key)
+    for (int e = threadIdx.x; e < kC * kD; e += kThreads) {
+        const int i = e >> 6, j = e & 63;
+        if (i >= n) continue;
+        const float g = fmaf(c2[i], X[i * kLd + j], DXa[i * kLd + j]);
+        const long long t = t0 + i - 1;
+        if (t >= 0) p.dk[(bh * p.T + t) * kD + j] = g;
+        else if (p.dtail) p.dtail[bh * kD + j] = g;
+    }
+    if (t0 + n == p.T)  // the last key feeds only the next call's tail
+        for (int j = threadIdx.x; j < kD; j += kThreads) p.dk[(bh * p.T + p.T - 1) * kD + j] = 0.f;
+}
+
+constexpr size_t kScalBytes = sizeof(Scal);
+constexpr size_t kPrepSmem = 10 * kMat * sizeof(float) + kScalBytes + 4 * kC * sizeof(float);
+constexpr size_t gradSmem(bool ip) { return (ip ? 11 : 12) * kMat * sizeof(float) + kScalBytes + (5 * kC + 8) * sizeof(float); }
+
+template <typename Tin, bool IP>
+int launch_typed(const BParams& p, cudaStream_t st) {
+    const unsigned chunks = (unsigned)(p.BH * p.N);
+    cudaFuncSetAttribute(falcon_bwd_prep<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
+    cudaFuncSetAttribute(falcon_bwd_grad<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gradSmem(IP));
+    falcon_bwd_prep<Tin, IP><<<chunks, kThreads, kPrepSmem, st>>>(p);
+    falcon_bwd_chain<<<(unsigned)(p.BH * (kD / kCols)), kThreads, 0, st>>>(p);
+    falcon_bwd_grad<Tin, IP><<<chunks, kThreads, gradSmem(IP), st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+}  // namespace
+
+bool bwd_supported(const Launch& a) {
+    return (a.variant == kF1 || a.variant == kF1A) && a.dk == kD && a.dv == kD && a.chunk == kC && a.W == 1;
+}
+
+size_t bwd_workspace_bytes(const Launch& a) {
+    const long long N = (a.T + kC - 1) / kC;
+    return (size_t)(a.B * a.H) * (size_t)N * kWsChunk * sizeof(float);
+}
+
+int launch_bwd(const Launch& a, const BwdArgs& g, cudaStream_t st) {
+    BParams p;
+    p.q = a.q;
+    p.k = a.k;
+    p.v = a.v;
+    p.dout = g.dout;
+    p.tail = a.tail;
+    p.beta = a.beta;
+    p.lam = a.lam;
+    p.S0 = a.S0;
+    p.dS_final = g.dS_final;
+    p.dq = g.dq;
+    p.dk = g.dk;
+    p.dv = g.dv;
+    p.dbeta = g.dbeta;
+    p.dlam = g.dlam;
+    p.dS0 = g.dS0;
+    p.dtail = g.dtail;
+    p.ws = static_cast<float*>(a.ws);
+    p.T = a.T;
+    p.pos = a.pos;
+    p.N = (a.T + kC - 1) / kC;
+    p.BH = a.B * a.H;
+    p.eps = a.eps;
+    p.eps_gamma = a.eps_gamma;
+    if (p.BH == 0) return 0;
+    if (p.N == 0) {  // no tokens: dS0 = dS_final, nothing else
+        if (p.dS0) {
+            const size_t bytes = (size_t)p.BH * kD * kD * sizeof(float);
+            const cudaError_t e = p.dS_final ? cudaMemcpyAsync(p.dS0, p.dS_final, bytes, cudaMemcpyDeviceToDevice, st)
+                                             : cudaMemsetAsync(p.dS0, 0, bytes, st);
+            if (e != cudaSuccess) return 4;
+        }
+        if (p.dtail) return cudaMemsetAsync(p.dtail, 0, (size_t)p.BH * kD * sizeof(float), st) == cudaSuccess ? 0 : 4;
+        return 0;
+    }
+    const bool ip = a.variant == kF1A;
+    if (a.bf16) return ip ? launch_typed<__nv_bfloat16, true>(p, st) : launch_typed<__nv_bfloat16, false>(p, st);
+    return ip ? launch_typed<float, true>(p, st) : launch_typed<float, false>(p, st);
+}
+
+}  // namespace falcon

@@ -57,4 +57,21 @@ int split_consume_timeout_flag(int* flag);
 bool decode_supported(const Launch& a);
 int launch_decode(const Launch& a, cudaStream_t stream);
 
+// Backward pass (Falcon-1 and 1A, dk = dv = 64, chunk 64): prep, chain and gradient kernels working
+// through a caller workspace of bwd_workspace_bytes(a) bytes at a.ws. `a` carries the forward inputs.
+struct BwdArgs {
+    const void* dout;        // [B,H,T,dv] in the input dtype
+    const float* dS_final;   // [B,H,dk,dv] or null (zero)
+    float* dq;               // [B,H,T,dk]
+    float* dk;               // [B,H,T,dk]
+    float* dv;               // [B,H,T,dv]
+    float* dbeta;            // [B,H,T]
+    float* dlam;             // [B,H,T]
+    float* dS0;              // [B,H,dk,dv] or null
+    float* dtail;            // [B,H,dk] or null (pos > 0 only)
+};
+bool bwd_supported(const Launch& a);
+size_t bwd_workspace_bytes(const Launch& a);
+int launch_bwd(const Launch& a, const BwdArgs& g, cudaStream_t stream);
+
 }  // namespace falcon

@@ -50,7 +50,8 @@ _lock = threading.Lock()
 _lib = None
 
 EXPORTED = ("falcon_fwd", "falcon_workspace_bytes", "falcon_fwd_static", "falcon_tail_bytes",
-            "falcon_status_string", "falcon_device_status", "falcon_kernel_for", "falcon_abi_version")
+            "falcon_status_string", "falcon_device_status", "falcon_kernel_for", "falcon_abi_version",
+            "falcon_bwd", "falcon_bwd_workspace_bytes")
 STATIC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -93,6 +94,11 @@ def load(path: str | None = None):
         lib.falcon_kernel_for.argtypes = [ctypes.c_int, ctypes.POINTER(FalconDims), ctypes.c_int]
         lib.falcon_abi_version.restype = ctypes.c_int
         lib.falcon_abi_version.argtypes = []
+        lib.falcon_bwd.restype = ctypes.c_int
+        lib.falcon_bwd.argtypes = [ctypes.c_int] + [vp] * 16 + [ctypes.POINTER(FalconDims), ctypes.c_int, vp,
+                                                                ctypes.c_size_t, vp]
+        lib.falcon_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.falcon_bwd_workspace_bytes.argtypes = [ctypes.c_int, ctypes.POINTER(FalconDims), ctypes.c_int]
         if path is None:
             _lib = lib
         return lib
@@ -165,6 +171,50 @@ def falcon_fwd_static(variant, q, k, v, beta, lam, S0, tail, out, S_final, tail_
     return int(load().falcon_fwd_static(int(variant), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
                                         _ptr(tail), _ptr(out), _ptr(S_final), _ptr(tail_out), ctypes.byref(dims),
                                         int(chunk), _stream_handle(stream)))
+
+
+def falcon_bwd(variant, q, k, v, beta, lam, S0, tail, dout, dS_final, dq, dk, dv, dbeta, dlam, dS0, dtail,
+               dims: FalconDims, chunk: int, workspace=None, workspace_bytes=None, stream=None) -> int:
+    """The C entry point falcon_bwd with the same argument order; tensors or raw device pointers."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else \
+            workspace.numel() * workspace.element_size()
+    return int(load().falcon_bwd(int(variant), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(lam), _ptr(S0),
+                                 _ptr(tail), _ptr(dout), _ptr(dS_final), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta),
+                                 _ptr(dlam), _ptr(dS0), _ptr(dtail), ctypes.byref(dims), int(chunk),
+                                 _ptr(workspace), int(workspace_bytes), _stream_handle(stream)))
+
+
+def falcon_bwd_workspace_bytes(variant: int, dims: FalconDims, chunk: int) -> int:
+    return int(load().falcon_bwd_workspace_bytes(int(variant), ctypes.byref(dims), int(chunk)))
+
+
+def backward(variant, q, k, v, beta, lam, dout, S0=None, dS_final=None, tail=None, *, pos=0, chunk=64, eps=1e-6,
+             eps_gamma=1e-6, want_dS0=True, stream=None):
+    """Allocate fp32 gradients and a workspace with torch on q's device and call falcon_bwd; raises
+    FalconError on a nonzero status. Returns a dict dq, dk, dv, dbeta, dlam, dS0 (None unless
+    want_dS0), dtail (None unless pos > 0)."""
+    import torch
+
+    if isinstance(variant, str):
+        variant = VARIANTS[variant]
+    B, H, T, dk_ = q.shape
+    dv_ = v.shape[-1]
+    dt = FALCON_BF16 if q.dtype == torch.bfloat16 else FALCON_F32
+    dims = make_dims(B, H, T, dk_, dv_, dtype=dt, pos=pos, eps=eps, eps_gamma=eps_gamma)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    g = {"dq": torch.empty((B, H, T, dk_), **f32), "dk": torch.empty((B, H, T, dk_), **f32),
+         "dv": torch.empty((B, H, T, dv_), **f32), "dbeta": torch.empty((B, H, T), **f32),
+         "dlam": torch.empty((B, H, T), **f32),
+         "dS0": torch.empty((B, H, dk_, dv_), **f32) if want_dS0 else None,
+         "dtail": torch.empty((B, H, dk_), **f32) if pos > 0 else None}
+    n = falcon_bwd_workspace_bytes(variant, dims, chunk)
+    ws = torch.empty(n, dtype=torch.uint8, device=q.device) if n > 0 else None
+    st = falcon_bwd(variant, q, k, v, beta, lam, S0, tail, dout, dS_final, g["dq"], g["dk"], g["dv"], g["dbeta"],
+                    g["dlam"], g["dS0"], g["dtail"], dims, chunk, ws, stream=stream)
+    if st != FALCON_OK:
+        raise FalconError(st, "falcon_bwd")
+    return g
 
 
 def workspace_for(variant, dims: FalconDims, chunk: int, device):

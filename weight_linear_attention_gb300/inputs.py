@@ -51,6 +51,7 @@ class Workload:
     segments: int = 1                # the sequence is `segments` calls of `seqlen` tokens
     nonzero_s0: bool = False
     pos0: int = 0                    # tokens consumed before the first call (needs a tail; window 1)
+    backward: bool = False           # a backward pass (falcon_bwd) rather than a forward one
     extra: dict = field(default_factory=dict)
 
     @property
@@ -87,12 +88,28 @@ WORKLOADS = {
                                     lam_const=0.01),
     "f3aw4_b2h12t16384_bf16": Workload("f3aw4_b2h12t16384_bf16", "falcon3a", 2, 12, 8192, 64, 64, "bf16", 32,
                                        window=4, lam_shift=-2.0, segments=2),
+    # the backward pass of Falcon-1 and 1A at the 130M shape (output and final-state adjoints drawn too)
+    "f1_bwd_b8h12t1024_bf16": Workload("f1_bwd_b8h12t1024_bf16", "falcon1", 8, 12, 1024, 64, 64, "bf16", 64,
+                                       lam_shift=-4.0, backward=True),
+    "f1a_bwd_b8h12t1024_bf16": Workload("f1a_bwd_b8h12t1024_bf16", "falcon1a", 8, 12, 1024, 64, 64, "bf16", 64,
+                                        lam_shift=-3.0, backward=True),
     # one decoding step of 256 sequences (12 heads of 64) after 1024 tokens: the recurrent form
     "f1_decode_b256h12_bf16": Workload("f1_decode_b256h12_bf16", "falcon1", 256, 12, 1, 64, 64, "bf16", 64,
                                        lam_shift=-4.0, nonzero_s0=True, pos0=1024),
 }
 
 HEADLINE = "f1_b8h12t1024_bf16"
+
+
+def make_adjoints(w: Workload, seed: int = 0, seqlen: int | None = None, batch: int | None = None) -> dict:
+    """Adjoints for a backward pass: dout [B,H,T,dv] in the workload dtype (unit normal) and
+    dS_final [B,H,dk,dv] fp32 (normal, scaled by 1/sqrt(dk) like S0). Drawn from their own seed stream."""
+    B = w.batch if batch is None else batch
+    T = (w.seqlen * w.segments) if seqlen is None else seqlen
+    g = torch.Generator("cpu").manual_seed(1_000_003 + seed)
+    dout = torch.randn(B, w.heads, T, w.dv, generator=g).to(w.torch_dtype)
+    dS = (torch.randn(B, w.heads, w.dk, w.dv, generator=g) / w.dk ** 0.5).float()
+    return {"dout": dout, "dS_final": dS}
 
 
 def _rmsnorm(x: torch.Tensor, eps: float = 1e-6) -> torch.Tensor:
