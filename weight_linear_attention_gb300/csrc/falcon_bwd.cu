@@ -236,14 +236,14 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
 
     const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N;
     const long long t0 = nck * kC;
-    const int n = (int)min((long long)kC, p.T - t0);
+    const int nr = (int)min((long long)kC, p.T - t0);  // rows of this chunk
     const Tin* tail = static_cast<const Tin*>(p.tail);
-    load_rows(X, static_cast<const Tin*>(p.k), bh, p.T, t0, n, 1, tail);
-    load_rows(Q, static_cast<const Tin*>(p.q), bh, p.T, t0, n, 0, (const Tin*)nullptr);
-    load_rows(Y, static_cast<const Tin*>(p.v), bh, p.T, t0, n, 0, (const Tin*)nullptr);
-    load_rows(dO, static_cast<const Tin*>(p.dout), bh, p.T, t0, n, 0, (const Tin*)nullptr);
+    load_rows(X, static_cast<const Tin*>(p.k), bh, p.T, t0, nr, 1, tail);
+    load_rows(Q, static_cast<const Tin*>(p.q), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
+    load_rows(Y, static_cast<const Tin*>(p.v), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
+    load_rows(dO, static_cast<const Tin*>(p.dout), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
     __syncthreads();
-    chunk_scalars(s, X, p, bh, t0, n);
+    chunk_scalars(s, X, p, bh, t0, nr);
     float* ws = p.ws + cid * kWsChunk;
     float acc[4][4], acc2[4][4];
 
@@ -444,13 +444,13 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
 
     const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N;
     const long long t0 = nck * kC;
-    const int n = (int)min((long long)kC, p.T - t0);
+    const int nr = (int)min((long long)kC, p.T - t0);  // rows of this chunk
     const Tin* tail = static_cast<const Tin*>(p.tail);
     const float* ws = p.ws + cid * kWsChunk;
-    load_rows(X, static_cast<const Tin*>(p.k), bh, p.T, t0, n, 1, tail);
-    load_rows(Q, static_cast<const Tin*>(p.q), bh, p.T, t0, n, 0, (const Tin*)nullptr);
-    load_rows(Y, static_cast<const Tin*>(p.v), bh, p.T, t0, n, 0, (const Tin*)nullptr);
-    load_rows(dO, static_cast<const Tin*>(p.dout), bh, p.T, t0, n, 0, (const Tin*)nullptr);
+    load_rows(X, static_cast<const Tin*>(p.k), bh, p.T, t0, nr, 1, tail);
+    load_rows(Q, static_cast<const Tin*>(p.q), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
+    load_rows(Y, static_cast<const Tin*>(p.v), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
+    load_rows(dO, static_cast<const Tin*>(p.dout), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
     load_ws(S, ws + kWsS * kWsMat);
     load_ws(dS, ws + kWsDS * kWsMat);
     if (!IP) load_ws(Tm, ws + kWsT * kWsMat);
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     }
     if (threadIdx.x < 8) red[threadIdx.x] = 0.f;
     __syncthreads();
-    chunk_scalars(s, X, p, bh, t0, n);
+    chunk_scalars(s, X, p, bh, t0, nr);
     const int lane = threadIdx.x & 31, tx = threadIdx.x & 15;
     float acc[4][4], acc2[4][4];
 
@@ -518,9 +518,9 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     if (!IP) {  // dZ = T^T dR = dV
         zero(acc);
         mm<true, false>(acc, Tm, b1);
-        FOR_TILE(b4[i * kLd + j] = acc[m][n]; if (i < n) dvo[i * kD + j] = acc[m][n];)
+        FOR_TILE(b4[i * kLd + j] = acc[m][n]; if (i < nr) dvo[i * kD + j] = acc[m][n];)
     } else {
-        FOR_TILE(if (i < n) dvo[i * kD + j] = b1[i * kLd + j];)
+        FOR_TILE(if (i < nr) dvo[i * kD + j] = b1[i * kLd + j];)
     }
     __syncthreads();
     // dP = dO R^T (j <= i) -> d eta, dL; dSc = dP eta_j e^{L_i - L_j}, into Tm
@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
         float rowL[4] = {0.f, 0.f, 0.f, 0.f};
         float* dqo = p.dq + (bh * p.T + t0) * kD;
         FOR_TILE(rowL[m] = fmaf(Q[i * kLd + j], acc[m][n], rowL[m]);
-                 if (i < n) dqo[i * kD + j] = s.eL[i] * acc[m][n] + acc2[m][n];)
+                 if (i < nr) dqo[i * kD + j] = s.eL[i] * acc[m][n] + acc2[m][n];)
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const float v = row_sum16(rowL[m]);
@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
         for (int h = 0; h < 2; ++h) {
             const int u = 2 * l + h;
             float db = 0.f, dlm = 0.f, cc = 0.f;
-            if (u < n) {
+            if (u < nr) {
                 float de = deta[u];
                 if (s.unc[u]) {
                     const float da = -suf[h] / s.gam[u];
@@ -689,13 +689,13 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     // dX = accumulator + 2 dden x; row i is dk of token t0 + i - 1 (row 0 of the call: the tail key)
     for (int e = threadIdx.x; e < kC * kD; e += kThreads) {
         const int i = e >> 6, j = e & 63;
-        if (i >= n) continue;
+        if (i >= nr) continue;
         const float g = fmaf(c2[i], X[i * kLd + j], DXa[i * kLd + j]);
         const long long t = t0 + i - 1;
         if (t >= 0) p.dk[(bh * p.T + t) * kD + j] = g;
         else if (p.dtail) p.dtail[bh * kD + j] = g;
     }
-    if (t0 + n == p.T)  // the last key feeds only the next call's tail
+    if (t0 + nr == p.T)  // the last key feeds only the next call's tail
         for (int j = threadIdx.x; j < kD; j += kThreads) p.dk[(bh * p.T + p.T - 1) * kD + j] = 0.f;
 }
 
