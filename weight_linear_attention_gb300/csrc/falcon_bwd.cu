@@ -67,9 +67,6 @@ struct BParams {
     float eps, eps_gamma;
 };
 
-__device__ __forceinline__ float ldf(const float* p) { return *p; }
-__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-
 // Scalars of one chunk, recomputed identically by the prep and gradient kernels.
 struct Scal {
     float eta[kC], lam[kC], den[kC], gam[kC], L[kC], Lx[kC], eL[kC], eLx[kC], w[kC];
@@ -77,25 +74,69 @@ struct Scal {
     float eLC;
 };
 
-// Rows t0 .. t0 + n - 1 of a [BH, T, 64] tensor into a shared 64 x 64 tile (zero rows past n).
-// shift = 1 loads the shifted keys x_t = k_{t-1} (row -1 is the tail key, or zero).
-template <typename Tin>
-__device__ void load_rows(float* dst, const Tin* src, long long bh, long long T, long long t0, int n, int shift,
-                          const Tin* tail) {
-    for (int e = threadIdx.x; e < kC * kD; e += kThreads) {
-        const int r = e >> 6, c = e & 63;
-        const long long t = t0 + r - shift;
-        float x = 0.f;
-        if (r < n) {
-            if (t >= 0) x = ldf(src + (bh * T + t) * kD + c);
-            else if (tail) x = ldf(tail + bh * kD + c);
-        }
-        dst[r * kLd + c] = x;
+// Tile loads: every thread issues all of its 16-byte loads of the chunk's tiles before it stores
+// any of them to shared memory, so their latencies overlap.
+__device__ __forceinline__ void put(float* d, const uint4& v, const float*) {
+    d[0] = __uint_as_float(v.x);
+    d[1] = __uint_as_float(v.y);
+    d[2] = __uint_as_float(v.z);
+    d[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ void put(float* d, const uint4& v, const __nv_bfloat16*) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        d[2 * h] = __uint_as_float(w[h] << 16);
+        d[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
     }
 }
 
-__device__ void load_ws(float* dst, const float* src) {
-    for (int e = threadIdx.x; e < kD * kD; e += kThreads) dst[(e >> 6) * kLd + (e & 63)] = src[e];
+// Rows t0 .. t0 + nr - 1 of the [BH, T, 64] tensors k (shifted: x_t = k_{t-1}, row -1 the tail key or
+// zero), q, v and dout into four shared 64 x 64 tiles (zero rows past nr).
+template <typename Tin>
+__device__ void load_inputs(float* X, float* Q, float* Y, float* dO, const BParams& p, long long bh, long long t0,
+                            int nr) {
+    constexpr int vw = 16 / sizeof(Tin), nv = kC * kD / vw / kThreads;
+    const Tin* src[4] = {static_cast<const Tin*>(p.k), static_cast<const Tin*>(p.q), static_cast<const Tin*>(p.v),
+                         static_cast<const Tin*>(p.dout)};
+    float* dst[4] = {X, Q, Y, dO};
+    const Tin* tail = static_cast<const Tin*>(p.tail);
+    uint4 v[4][nv];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int u = 0; u < nv; ++u) {
+            const int e = (threadIdx.x + u * kThreads) * vw, r = e >> 6, c = e & 63;
+            const long long t = t0 + r - (a == 0 ? 1 : 0);
+            const Tin* ptr = nullptr;
+            if (r < nr) ptr = t >= 0 ? src[a] + (bh * p.T + t) * kD + c : (tail ? tail + bh * kD + c : nullptr);
+            v[a][u] = ptr ? *reinterpret_cast<const uint4*>(ptr) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int u = 0; u < nv; ++u) {
+            const int e = (threadIdx.x + u * kThreads) * vw;
+            put(dst[a] + (e >> 6) * kLd + (e & 63), v[a][u], (const Tin*)nullptr);
+        }
+}
+
+// NT dense fp32 64 x 64 workspace matrices into shared tiles.
+template <int NT>
+__device__ void load_ws(float* const (&dst)[NT], const float* const (&src)[NT]) {
+    constexpr int nv = kD * kD / 4 / kThreads;
+    uint4 v[NT][nv];
+#pragma unroll
+    for (int a = 0; a < NT; ++a)
+#pragma unroll
+        for (int u = 0; u < nv; ++u) v[a][u] = reinterpret_cast<const uint4*>(src[a])[threadIdx.x + u * kThreads];
+#pragma unroll
+    for (int a = 0; a < NT; ++a)
+#pragma unroll
+        for (int u = 0; u < nv; ++u) {
+            const int e = (threadIdx.x + u * kThreads) * 4;
+            put(dst[a] + (e >> 6) * kLd + (e & 63), v[a][u], (const float*)nullptr);
+        }
 }
 
 // Per-row scalars of the chunk from X (shifted keys), beta and lambda; then the chunk-local log prefixes.
@@ -237,11 +278,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
     const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N;
     const long long t0 = nck * kC;
     const int nr = (int)min((long long)kC, p.T - t0);  // rows of this chunk
-    const Tin* tail = static_cast<const Tin*>(p.tail);
-    load_rows(X, static_cast<const Tin*>(p.k), bh, p.T, t0, nr, 1, tail);
-    load_rows(Q, static_cast<const Tin*>(p.q), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
-    load_rows(Y, static_cast<const Tin*>(p.v), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
-    load_rows(dO, static_cast<const Tin*>(p.dout), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
+    load_inputs<Tin>(X, Q, Y, dO, p, bh, t0, nr);
     __syncthreads();
     chunk_scalars(s, X, p, bh, t0, nr);
     float* ws = p.ws + cid * kWsChunk;
@@ -308,109 +345,119 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
 }
 
 // --------------------------------------------------------------------------------------------------
-// falcon_bwd_chain: one CTA per (sequence, group of 16 value columns). Thread (r, c): rows r + 16 m.
+// falcon_bwd_chain: one CTA per (sequence, group of 16 value columns). Thread (r4, c) owns rows
+// 4 r4 .. 4 r4 + 3 of column c. The state slice is kept transposed (column-major) so a thread reads four
+// consecutive k of its column at once; M_n is stored so that four consecutive output rows of one k are
+// adjacent (transposed for S_{n+1} = M_n S_n, as is for dS_n = M_n^T dS_{n+1}). The next step's M and
+// U (or V) are loaded into registers while the current step computes.
+constexpr int kLdc = 68;  // 16-byte aligned rows
 __global__ void __launch_bounds__(kThreads) falcon_bwd_chain(const BParams p) {
-    __shared__ __align__(16) float Ms[2][kD * kLd];
-    __shared__ float Sv[2][kD][kCols + 1];
+    __shared__ __align__(16) float Ms[2][kD * kLdc];
+    __shared__ __align__(16) float Sv[2][kCols][kLdc];  // Sv[b][c][k] = S[k][column c]
     const long long bh = blockIdx.x / (kD / kCols);
     const int cg = (int)(blockIdx.x % (kD / kCols)) * kCols;
-    const int c = threadIdx.x & 15, r = threadIdx.x >> 4;
+    const int c = threadIdx.x & 15, r0 = 4 * (threadIdx.x >> 4);
     const long long N = p.N;
     float* wsq = p.ws + bh * N * kWsChunk;
 
-    auto load_M = [&](long long nck, float (&reg)[16]) {
+    auto load_M = [&](long long nck, float4 (&reg)[4]) {
         const float4* src = reinterpret_cast<const float4*>(wsq + nck * kWsChunk + kWsM * kWsMat);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float4 v = src[threadIdx.x + u * kThreads];
-            reg[4 * u] = v.x;
-            reg[4 * u + 1] = v.y;
-            reg[4 * u + 2] = v.z;
-            reg[4 * u + 3] = v.w;
-        }
+        for (int u = 0; u < 4; ++u) reg[u] = src[threadIdx.x + u * kThreads];
     };
-    auto store_M = [&](float* dst, const float (&reg)[16]) {
+    auto store_M = [&](float* dst, const float4 (&reg)[4], bool transpose) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int e = 4 * (threadIdx.x + u * kThreads), row = e >> 6, col = e & 63;
-#pragma unroll
-            for (int z = 0; z < 4; ++z) dst[row * kLd + col + z] = reg[4 * u + z];
+            if (transpose) {
+                dst[col * kLdc + row] = reg[u].x;
+                dst[(col + 1) * kLdc + row] = reg[u].y;
+                dst[(col + 2) * kLdc + row] = reg[u].z;
+                dst[(col + 3) * kLdc + row] = reg[u].w;
+            } else {
+                *reinterpret_cast<float4*>(dst + row * kLdc + col) = reg[u];
+            }
         }
     };
+    auto load_off = [&](long long nck, int which, float (&o)[4]) {
+        const float* src = wsq + nck * kWsChunk + which * kWsMat + cg + c;
+#pragma unroll
+        for (int z = 0; z < 4; ++z) o[z] = src[(r0 + z) * kD];
+    };
+    // one step: out[c][r0 + z] = off[z] + sum_k Ms[k][r0 + z] * Sv[c][k]
+    auto step = [&](const float* Mk, const float* Sc, float* So, const float (&off)[4]) {
+        float acc[4] = {off[0], off[1], off[2], off[3]};
+#pragma unroll 4
+        for (int k = 0; k < kD; k += 4) {
+            const float4 sv = *reinterpret_cast<const float4*>(Sc + k);
+            const float s4[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 mv = *reinterpret_cast<const float4*>(Mk + (k + kk) * kLdc + r0);
+                acc[0] = fmaf(mv.x, s4[kk], acc[0]);
+                acc[1] = fmaf(mv.y, s4[kk], acc[1]);
+                acc[2] = fmaf(mv.z, s4[kk], acc[2]);
+                acc[3] = fmaf(mv.w, s4[kk], acc[3]);
+            }
+        }
+        *reinterpret_cast<float4*>(So + r0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    };
 
-    float reg[16];
+    float4 regM[4];
+    float off[4], offn[4];
     // forward: S_{n+1} = M_n S_n + U_n, storing S_n
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int i = r + 16 * m;
-        Sv[0][i][c] = p.S0 ? p.S0[(bh * kD + i) * kD + cg + c] : 0.f;
-    }
-    if (N > 0) {
-        load_M(0, reg);
-        store_M(Ms[0], reg);
-    }
+    for (int z = 0; z < 4; ++z) Sv[0][c][r0 + z] = p.S0 ? p.S0[(bh * kD + r0 + z) * kD + cg + c] : 0.f;
+    load_M(0, regM);
+    load_off(0, kWsU, off);
+    store_M(Ms[0], regM, true);
     __syncthreads();
     for (long long nck = 0; nck < N; ++nck) {
         const int b = (int)(nck & 1);
-        float* wc = wsq + nck * kWsChunk;
-        if (nck + 1 < N) load_M(nck + 1, reg);
-        float acc[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int i = r + 16 * m;
-            wc[kWsS * kWsMat + i * kD + cg + c] = Sv[b][i][c];
-            acc[m] = wc[kWsU * kWsMat + i * kD + cg + c];
+        const bool more = nck + 1 < N;
+        if (more) {
+            load_M(nck + 1, regM);
+            load_off(nck + 1, kWsU, offn);
         }
-#pragma unroll 8
-        for (int kk = 0; kk < kD; ++kk) {
-            const float sv = Sv[b][kk][c];
+        float* wc = wsq + nck * kWsChunk + kWsS * kWsMat + cg + c;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) acc[m] = fmaf(Ms[b][(r + 16 * m) * kLd + kk], sv, acc[m]);
+        for (int z = 0; z < 4; ++z) wc[(r0 + z) * kD] = Sv[b][c][r0 + z];
+        step(Ms[b], Sv[b][c], Sv[b ^ 1][c], off);
+        if (more) {
+            store_M(Ms[b ^ 1], regM, true);
+#pragma unroll
+            for (int z = 0; z < 4; ++z) off[z] = offn[z];
         }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) Sv[b ^ 1][r + 16 * m][c] = acc[m];
-        if (nck + 1 < N) store_M(Ms[b ^ 1], reg);
         __syncthreads();
     }
     // backward: dS_n = M_n^T dS_{n+1} + V_n, storing dS_{n+1}
-    int b = 0;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int i = r + 16 * m;
-        Sv[0][i][c] = p.dS_final ? p.dS_final[(bh * kD + i) * kD + cg + c] : 0.f;
-    }
-    if (N > 0) {
-        load_M(N - 1, reg);
-        store_M(Ms[0], reg);
-    }
+    for (int z = 0; z < 4; ++z) Sv[0][c][r0 + z] = p.dS_final ? p.dS_final[(bh * kD + r0 + z) * kD + cg + c] : 0.f;
+    load_M(N - 1, regM);
+    load_off(N - 1, kWsV, off);
+    store_M(Ms[0], regM, false);
     __syncthreads();
+    int b = 0;
     for (long long nck = N - 1; nck >= 0; --nck, b ^= 1) {
-        float* wc = wsq + nck * kWsChunk;
-        if (nck > 0) load_M(nck - 1, reg);
-        float acc[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int i = r + 16 * m;
-            wc[kWsDS * kWsMat + i * kD + cg + c] = Sv[b][i][c];
-            acc[m] = wc[kWsV * kWsMat + i * kD + cg + c];
+        const bool more = nck > 0;
+        if (more) {
+            load_M(nck - 1, regM);
+            load_off(nck - 1, kWsV, offn);
         }
-#pragma unroll 8
-        for (int kk = 0; kk < kD; ++kk) {
-            const float sv = Sv[b][kk][c];
+        float* wc = wsq + nck * kWsChunk + kWsDS * kWsMat + cg + c;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) acc[m] = fmaf(Ms[b][kk * kLd + r + 16 * m], sv, acc[m]);
+        for (int z = 0; z < 4; ++z) wc[(r0 + z) * kD] = Sv[b][c][r0 + z];
+        step(Ms[b], Sv[b][c], Sv[b ^ 1][c], off);
+        if (more) {
+            store_M(Ms[b ^ 1], regM, false);
+#pragma unroll
+            for (int z = 0; z < 4; ++z) off[z] = offn[z];
         }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) Sv[b ^ 1][r + 16 * m][c] = acc[m];
-        if (nck > 0) store_M(Ms[b ^ 1], reg);
         __syncthreads();
     }
     if (p.dS0)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int i = r + 16 * m;
-            p.dS0[(bh * kD + i) * kD + cg + c] = Sv[b][i][c];
-        }
+        for (int z = 0; z < 4; ++z) p.dS0[(bh * kD + r0 + z) * kD + cg + c] = Sv[b][c][r0 + z];
 }
 
 // --------------------------------------------------------------------------------------------------
@@ -445,15 +492,17 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N;
     const long long t0 = nck * kC;
     const int nr = (int)min((long long)kC, p.T - t0);  // rows of this chunk
-    const Tin* tail = static_cast<const Tin*>(p.tail);
     const float* ws = p.ws + cid * kWsChunk;
-    load_rows(X, static_cast<const Tin*>(p.k), bh, p.T, t0, nr, 1, tail);
-    load_rows(Q, static_cast<const Tin*>(p.q), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
-    load_rows(Y, static_cast<const Tin*>(p.v), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
-    load_rows(dO, static_cast<const Tin*>(p.dout), bh, p.T, t0, nr, 0, (const Tin*)nullptr);
-    load_ws(S, ws + kWsS * kWsMat);
-    load_ws(dS, ws + kWsDS * kWsMat);
-    if (!IP) load_ws(Tm, ws + kWsT * kWsMat);
+    load_inputs<Tin>(X, Q, Y, dO, p, bh, t0, nr);
+    if (IP) {
+        float* const d2[2] = {S, dS};
+        const float* const s2[2] = {ws + kWsS * kWsMat, ws + kWsDS * kWsMat};
+        load_ws<2>(d2, s2);
+    } else {
+        float* const d3[3] = {S, dS, Tm};
+        const float* const s3[3] = {ws + kWsS * kWsMat, ws + kWsDS * kWsMat, ws + kWsT * kWsMat};
+        load_ws<3>(d3, s3);
+    }
     if (threadIdx.x < kC) {
         deta[threadIdx.x] = 0.f;
         dL[threadIdx.x] = 0.f;
