@@ -31,13 +31,14 @@
 #include <cuda_runtime.h>
 
 #include "falcon_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace falcon {
 namespace {
 
 constexpr int kD = 64;        // dk = dv
 constexpr int kC = 64;        // chunk length
-constexpr int kLd = 65;       // shared-memory row stride (floats): conflict-free rows and columns
+constexpr int kLd = 68;       // shared-memory row stride (floats): 16-byte rows, tensor-core fragments
 constexpr int kMat = kC * kLd;
 constexpr int kThreads = 256;
 constexpr int kCols = 16;     // value columns per chain CTA
@@ -197,22 +198,66 @@ __device__ void chunk_scalars(Scal& s, const float* X, const BParams& p, long lo
     __syncthreads();
 }
 
-// acc[m][n] += sum_k A(i_m, k) B(k, j_n) over k < 64, with i_m = ty + 16 m, j_n = tx + 16 n.
-// TA: A is stored transposed (A(i, k) at a[k][i]); TB: B is stored transposed (B(k, j) at b[j][k]).
-template <bool TA, bool TB>
+// 64 x 64 x 64 products on the tensor cores: mma.sync m16n8k8 with tf32 operands and fp32
+// accumulation, each fp32 operand split into a tf32 head and a tf32 remainder and the product taken
+// as head*head + head*rem + rem*head (the remainder products carry the bits tf32 drops, so the
+// result has fp32 accuracy). An operand flagged exact (a bf16 input, which tf32 holds without loss)
+// has no remainder and skips its pass.
+// Warp w owns output rows 32 (w >> 2) .. + 31 (two m16 tiles) and columns 16 (w & 3) .. + 15 (two n8
+// tiles). acc[m][n]: m = 2 * (m16 tile) + (n8 tile), n = the fragment element (2 * row half + column).
+__device__ __forceinline__ int tile_row(int m, int n) {
+    const int lane = threadIdx.x & 31;
+    return 32 * (threadIdx.x >> 7) + 16 * (m >> 1) + (lane >> 2) + 8 * (n >> 1);
+}
+__device__ __forceinline__ int tile_col(int m, int n) {
+    const int lane = threadIdx.x & 31;
+    return 16 * ((threadIdx.x >> 5) & 3) + 8 * (m & 1) + 2 * (lane & 3) + (n & 1);
+}
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = ptx::tf32_rn(x);
+    lo = ptx::tf32_rn(x - __uint_as_float(hi));
+}
+
+// acc += A B with A(i, k) = a[i][k] (TA: a[k][i]) and B(k, j) = b[k][j] (TB: b[j][k]).
+template <bool TA, bool TB, bool AX = false, bool BX = false>
 __device__ __forceinline__ void mm(float (&acc)[4][4], const float* a, const float* b) {
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-#pragma unroll 4
-    for (int k = 0; k < kD; ++k) {
-        float av[4], bv[4];
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int rb = 32 * (threadIdx.x >> 7), cb = 16 * ((threadIdx.x >> 5) & 3);
+    auto A = [&](int i, int k) { return TA ? a[k * kLd + i] : a[i * kLd + k]; };
+    auto B = [&](int k, int j) { return TB ? b[j * kLd + k] : b[k * kLd + j]; };
+#pragma unroll 2
+    for (int k0 = 0; k0 < kD; k0 += 8) {
+        uint32_t ah[2][4], al[2][4], bh[2][2], bl[2][2];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) av[m] = TA ? a[k * kLd + ty + 16 * m] : a[(ty + 16 * m) * kLd + k];
+        for (int mt = 0; mt < 2; ++mt) {
+            const int r = rb + 16 * mt + g;
+            const float x[4] = {A(r, k0 + t), A(r + 8, k0 + t), A(r, k0 + t + 4), A(r + 8, k0 + t + 4)};
 #pragma unroll
-        for (int n = 0; n < 4; ++n) bv[n] = TB ? b[(tx + 16 * n) * kLd + k] : b[k * kLd + tx + 16 * n];
+            for (int e = 0; e < 4; ++e) {
+                if (AX) ah[mt][e] = __float_as_uint(x[e]), al[mt][e] = 0u;
+                else split_tf32(x[e], ah[mt][e], al[mt][e]);
+            }
+        }
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int nt = 0; nt < 2; ++nt) {
+            const int c = cb + 8 * nt + g;
+            const float y[2] = {B(k0 + t, c), B(k0 + t + 4, c)};
 #pragma unroll
-            for (int n = 0; n < 4; ++n) acc[m][n] = fmaf(av[m], bv[n], acc[m][n]);
+            for (int e = 0; e < 2; ++e) {
+                if (BX) bh[nt][e] = __float_as_uint(y[e]), bl[nt][e] = 0u;
+                else split_tf32(y[e], bh[nt][e], bl[nt][e]);
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                float (&d)[4] = acc[2 * mt + nt];
+                if (!AX) ptx::mma1688_tf32(d, al[mt][0], al[mt][1], al[mt][2], al[mt][3], bh[nt][0], bh[nt][1]);
+                if (!BX) ptx::mma1688_tf32(d, ah[mt][0], ah[mt][1], ah[mt][2], ah[mt][3], bl[nt][0], bl[nt][1]);
+                ptx::mma1688_tf32(d, ah[mt][0], ah[mt][1], ah[mt][2], ah[mt][3], bh[nt][0], bh[nt][1]);
+            }
     }
 }
 
@@ -223,20 +268,43 @@ __device__ __forceinline__ void zero(float (&acc)[4][4]) {
         for (int n = 0; n < 4; ++n) acc[m][n] = 0.f;
 }
 
-#define FOR_TILE(...)                                               \
-    _Pragma("unroll") for (int m = 0; m < 4; ++m) {                 \
-        const int i = (threadIdx.x >> 4) + 16 * m;                  \
-        _Pragma("unroll") for (int n = 0; n < 4; ++n) {             \
-            const int j = (threadIdx.x & 15) + 16 * n;              \
-            __VA_ARGS__                                             \
-        }                                                           \
+// Runs the body for each accumulator element acc[m][n] of this thread, at output (i, j); ri and ci
+// index the thread's four rows and four columns (for row_add / col_add).
+#define FOR_TILE(...)                                                         \
+    _Pragma("unroll") for (int m = 0; m < 4; ++m) {                           \
+        _Pragma("unroll") for (int n = 0; n < 4; ++n) {                       \
+            const int i = tile_row(m, n), j = tile_col(m, n);                 \
+            const int ri = 2 * (m >> 1) + (n >> 1), ci = 2 * (m & 1) + (n & 1); \
+            (void)ri;                                                         \
+            (void)ci;                                                         \
+            __VA_ARGS__                                                       \
+        }                                                                     \
     }
 
-// Sum of v over the 16 threads that share a tile row (one half-warp).
-__device__ __forceinline__ float row_sum16(float v) {
+// arr[i] += sign * scale[i] * (sum over the whole row of this CTA's partial sums v[ri]).
+__device__ __forceinline__ void row_add(float* arr, const float (&v)[4], const float* scale = nullptr,
+                                        float sign = 1.f) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+    for (int ri = 0; ri < 4; ++ri) {
+        float x = v[ri];
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        const int i = tile_row(2 * (ri >> 1), 2 * (ri & 1));
+        if ((lane & 3) == 0) atomicAdd(&arr[i], sign * (scale ? scale[i] : 1.f) * x);
+    }
+}
+// arr[j] += sign * (sum over the whole column of the partial sums v[ci]).
+__device__ __forceinline__ void col_add(float* arr, const float (&v)[4], float sign = 1.f) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int ci = 0; ci < 4; ++ci) {
+        float x = v[ci];
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        x += __shfl_xor_sync(0xffffffffu, x, 8);
+        x += __shfl_xor_sync(0xffffffffu, x, 16);
+        if ((lane >> 2) == 0) atomicAdd(&arr[tile_col(ci >> 1, ci & 1)], sign * x);
+    }
 }
 
 // T = (I + A)^-1 for a strictly lower A, by forward substitution one row at a time
@@ -274,6 +342,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
     float* B2 = B1 + kMat;
     Scal& s = *reinterpret_cast<Scal*>(B2 + kMat);
     float* part = reinterpret_cast<float*>(&s + 1);
+    constexpr bool EX = sizeof(Tin) == 2;  // bf16 inputs are exact tf32 operands
 
     const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N;
     const long long t0 = nck * kC;
@@ -287,10 +356,10 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
     // Falcon-1: P, A and diag(e^Lx) X
     if (!IP) {
         zero(acc);
-        mm<false, true>(acc, Q, X);
+        mm<false, true, EX, EX>(acc, Q, X);
         FOR_TILE(P[i * kLd + j] = j <= i ? s.eta[j] * expf(s.L[i] - s.L[j]) * acc[m][n] : 0.f;)
         zero(acc);
-        mm<false, true>(acc, X, X);
+        mm<false, true, EX, EX>(acc, X, X);
         FOR_TILE(A[i * kLd + j] = j < i ? s.eta[j] * expf(s.Lx[i] - s.L[j]) * acc[m][n] : 0.f;
                  DX[i * kLd + j] = s.eLx[i] * X[i * kLd + j];)
     }
@@ -304,9 +373,9 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
         }
         __syncthreads();
         zero(acc);
-        mm<true, false>(acc, X, B2);
+        mm<true, false, EX, false>(acc, X, B2);
         zero(acc2);
-        mm<true, false>(acc2, Q, dO);
+        mm<true, false, EX, false>(acc2, Q, dO);
         FOR_TILE(ws[kWsM * kWsMat + i * kD + j] = i == j ? s.eLC : 0.f;
                  ws[kWsU * kWsMat + i * kD + j] = acc[m][n];
                  ws[kWsV * kWsMat + i * kD + j] = acc2[m][n];)
@@ -317,17 +386,17 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
     zero(acc);
     mm<false, false>(acc, Tm, DX);
     zero(acc2);
-    mm<false, false>(acc2, Tm, Y);
+    mm<false, false, false, EX>(acc2, Tm, Y);
     FOR_TILE(B1[i * kLd + j] = s.w[i] * acc[m][n]; B2[i * kLd + j] = s.w[i] * acc2[m][n];)
     zero(acc);
-    mm<true, false>(acc, P, dO);
+    mm<true, false, false, EX>(acc, P, dO);
     FOR_TILE(A[i * kLd + j] = acc[m][n];)
     __syncthreads();
     // M = e^{L_C} I - X^T B1, U = X^T B2; P <- T^T (P^T dO); dO <- diag(e^L) dO
     zero(acc);
-    mm<true, false>(acc, X, B1);
+    mm<true, false, EX, false>(acc, X, B1);
     zero(acc2);
-    mm<true, false>(acc2, X, B2);
+    mm<true, false, EX, false>(acc2, X, B2);
     FOR_TILE(ws[kWsM * kWsMat + i * kD + j] = (i == j ? s.eLC : 0.f) - acc[m][n];
              ws[kWsU * kWsMat + i * kD + j] = acc2[m][n];
              ws[kWsT * kWsMat + i * kD + j] = Tm[i * kLd + j];)
@@ -338,7 +407,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
     __syncthreads();
     // V = Q^T diag(e^L) dO - (diag(e^Lx) X)^T T^T P^T dO
     zero(acc);
-    mm<true, false>(acc, Q, dO);
+    mm<true, false, EX, false>(acc, Q, dO);
     zero(acc2);
     mm<true, false>(acc2, DX, P);
     FOR_TILE(ws[kWsV * kWsMat + i * kD + j] = acc[m][n] - acc2[m][n];)
@@ -485,6 +554,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     float* c2 = dw + kC;
     float* red = c2 + kC;  // [8] block reduction
 
+    constexpr bool EX = sizeof(Tin) == 2;  // bf16 inputs are exact tf32 operands
     float* R = IP ? Y : b0;
     float* P = IP ? b0 : Y;
     float* DXa = IP ? b3 : Y;
@@ -511,7 +581,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     if (threadIdx.x < 8) red[threadIdx.x] = 0.f;
     __syncthreads();
     chunk_scalars(s, X, p, bh, t0, nr);
-    const int lane = threadIdx.x & 31, tx = threadIdx.x & 15;
+    const int lane = threadIdx.x & 31;
     float acc[4][4], acc2[4][4];
 
     // <dS', S>
@@ -528,11 +598,11 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     // Z = Y - diag(e^Lx) X S (Falcon-1); X dS'
     if (!IP) {
         zero(acc);
-        mm<false, false>(acc, X, S);
+        mm<false, false, EX, false>(acc, X, S);
         FOR_TILE(Y[i * kLd + j] -= s.eLx[i] * acc[m][n];)
     }
     zero(acc);
-    mm<false, false>(acc, X, dS);
+    mm<false, false, EX, false>(acc, X, dS);
     FOR_TILE(b1[i * kLd + j] = acc[m][n];)
     __syncthreads();
     // R = T Z (Falcon-1); Sc = Q X^T; G = X X^T (Falcon-1)
@@ -541,11 +611,11 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
         mm<false, false>(acc, Tm, Y);
         FOR_TILE(b0[i * kLd + j] = acc[m][n];)
         zero(acc);
-        mm<false, true>(acc, X, X);
+        mm<false, true, EX, EX>(acc, X, X);
         FOR_TILE(b3[i * kLd + j] = acc[m][n];)
     }
     zero(acc);
-    mm<false, true>(acc, Q, X);
+    mm<false, true, EX, EX>(acc, Q, X);
     FOR_TILE(b2[i * kLd + j] = acc[m][n];)
     __syncthreads();
     // dw_j = x_j^T dS' r_j; P
@@ -560,7 +630,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     __syncthreads();
     // dR = P^T dO + diag(w) X dS'  (Falcon-1A: dV = dR)
     zero(acc);
-    mm<true, false>(acc, P, dO);
+    mm<true, false, false, EX>(acc, P, dO);
     FOR_TILE(b1[i * kLd + j] = acc[m][n] + s.w[i] * b1[i * kLd + j];)
     __syncthreads();
     float* dvo = p.dv + (bh * p.T + t0) * kD;
@@ -574,7 +644,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     __syncthreads();
     // dP = dO R^T (j <= i) -> d eta, dL; dSc = dP eta_j e^{L_i - L_j}, into Tm
     zero(acc);
-    mm<false, true>(acc, dO, R);
+    mm<false, true, EX, IP && EX>(acc, dO, R);
     if (!IP) {
         zero(acc2);
         mm<false, true>(acc2, b4, R);  // dZ R^T = -dA
@@ -587,23 +657,16 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
             if (j <= i) {
                 const float f = expf(s.L[i] - s.L[j]), d = acc[m][n];
                 const float pp = P[i * kLd + j];
-                colE[n] = fmaf(d * f, b2[i * kLd + j], colE[n]);
-                rowL[m] = fmaf(d, pp, rowL[m]);
-                colL[n] = fmaf(d, pp, colL[n]);
+                colE[ci] = fmaf(d * f, b2[i * kLd + j], colE[ci]);
+                rowL[ri] = fmaf(d, pp, rowL[ri]);
+                colL[ci] = fmaf(d, pp, colL[ci]);
                 v = d * s.eta[j] * f;
             }
             Tm[i * kLd + j] = v;
         })
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float v = row_sum16(rowL[m]);
-            if (tx == 0) atomicAdd(&dL[(threadIdx.x >> 4) + 16 * m], v);
-        }
-#pragma unroll
-        for (int n2 = 0; n2 < 4; ++n2) {
-            atomicAdd(&deta[tx + 16 * n2], colE[n2]);
-            atomicAdd(&dL[tx + 16 * n2], -colL[n2]);
-        }
+        row_add(dL, rowL);
+        col_add(deta, colE);
+        col_add(dL, colL, -1.f);
     }
     if (!IP) {  // dA = -dZ R^T (j < i) -> d eta, dLx, dL; dG = dA eta_j e^{Lx_i - L_j}, into b1
         float rowX[4] = {0.f, 0.f, 0.f, 0.f}, colE[4] = {0.f, 0.f, 0.f, 0.f}, colL[4] = {0.f, 0.f, 0.f, 0.f};
@@ -611,25 +674,18 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
             float v = 0.f;
             if (j < i) {
                 const float f = expf(s.Lx[i] - s.L[j]), d = -acc2[m][n];
-                const float g = b3[i * kLd + j];
-                const float aa = s.eta[j] * f * g * d;
-                colE[n] = fmaf(d * f, g, colE[n]);
-                rowX[m] += aa;
-                colL[n] += aa;
+                const float gv = b3[i * kLd + j];
+                const float aa = s.eta[j] * f * gv * d;
+                colE[ci] = fmaf(d * f, gv, colE[ci]);
+                rowX[ri] += aa;
+                colL[ci] += aa;
                 v = d * s.eta[j] * f;
             }
             b1[i * kLd + j] = v;
         })
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float v = row_sum16(rowX[m]);
-            if (tx == 0) atomicAdd(&dLx[(threadIdx.x >> 4) + 16 * m], v);
-        }
-#pragma unroll
-        for (int n2 = 0; n2 < 4; ++n2) {
-            atomicAdd(&deta[tx + 16 * n2], colE[n2]);
-            atomicAdd(&dL[tx + 16 * n2], -colL[n2]);
-        }
+        row_add(dLx, rowX);
+        col_add(deta, colE);
+        col_add(dL, colL, -1.f);
     }
     __syncthreads();
     if (!IP) {  // dG + dG^T: mirror the strict lower triangle into the upper one
@@ -640,45 +696,35 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     }
     // dX accumulator: diag(w) R dS'^T  (for Falcon-1 it overwrites P, last read before the barrier above)
     zero(acc);
-    mm<false, true>(acc, R, dS);
+    mm<false, true, IP && EX, false>(acc, R, dS);
     __syncthreads();
     FOR_TILE(DXa[i * kLd + j] = s.w[i] * acc[m][n];)
     __syncthreads();
     // dX += dSc^T Q (+ (dG + dG^T) X - diag(e^Lx) dZ S^T, with dLx_i -= e^Lx_i x_i . (dZ S^T)_i)
     zero(acc);
-    mm<true, false>(acc, Tm, Q);
+    mm<true, false, false, EX>(acc, Tm, Q);
     if (!IP) {
-        mm<false, false>(acc, b1, X);
+        mm<false, false, false, EX>(acc, b1, X);
         zero(acc2);
         mm<false, true>(acc2, b4, S);
         float rowX[4] = {0.f, 0.f, 0.f, 0.f};
         FOR_TILE(DXa[i * kLd + j] += acc[m][n] - s.eLx[i] * acc2[m][n];
-                 rowX[m] = fmaf(X[i * kLd + j], acc2[m][n], rowX[m]);)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float v = row_sum16(rowX[m]);
-            const int i = (threadIdx.x >> 4) + 16 * m;
-            if (tx == 0) atomicAdd(&dLx[i], -s.eLx[i] * v);
-        }
+                 rowX[ri] = fmaf(X[i * kLd + j], acc2[m][n], rowX[ri]);)
+        row_add(dLx, rowX, s.eLx, -1.f);
     } else {
         FOR_TILE(DXa[i * kLd + j] += acc[m][n];)
     }
     // dQ = diag(e^L) dO S^T + dSc X, with dL_i += e^L_i q_i . (dO S^T)_i
     zero(acc);
-    mm<false, true>(acc, dO, S);
+    mm<false, true, EX, false>(acc, dO, S);
     zero(acc2);
-    mm<false, false>(acc2, Tm, X);
+    mm<false, false, false, EX>(acc2, Tm, X);
     {
         float rowL[4] = {0.f, 0.f, 0.f, 0.f};
         float* dqo = p.dq + (bh * p.T + t0) * kD;
-        FOR_TILE(rowL[m] = fmaf(Q[i * kLd + j], acc[m][n], rowL[m]);
+        FOR_TILE(rowL[ri] = fmaf(Q[i * kLd + j], acc[m][n], rowL[ri]);
                  if (i < nr) dqo[i * kD + j] = s.eL[i] * acc[m][n] + acc2[m][n];)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float v = row_sum16(rowL[m]);
-            const int i = (threadIdx.x >> 4) + 16 * m;
-            if (tx == 0) atomicAdd(&dL[i], s.eL[i] * v);
-        }
+        row_add(dL, rowL, s.eL);
     }
     __syncthreads();
     // scalars: d eta and dL from w and the chunk-end decay; d log gamma; the clamp; eta = beta / den
