@@ -226,6 +226,7 @@ __device__ __forceinline__ void mm(float (&acc)[4][4], const float* a, const flo
     const int rb = 32 * (threadIdx.x >> 7), cb = 16 * ((threadIdx.x >> 5) & 3);
     auto A = [&](int i, int k) { return TA ? a[k * kLd + i] : a[i * kLd + k]; };
     auto B = [&](int k, int j) { return TB ? b[j * kLd + k] : b[k * kLd + j]; };
+    float cr[4][4] = {};
 #pragma unroll 2
     for (int k0 = 0; k0 < kD; k0 += 8) {
         uint32_t ah[2][4], al[2][4], bh[2][2], bl[2][2];
@@ -249,16 +250,28 @@ __device__ __forceinline__ void mm(float (&acc)[4][4], const float* a, const flo
                 else split_tf32(y[e], bh[nt][e], bl[nt][e]);
             }
         }
+        // the three passes in turn over the four tiles, remainder terms into their own accumulators,
+        // so that consecutive MMAs are independent
+        if (!AX)
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+            for (int q = 0; q < 4; ++q)
+                ptx::mma1688_tf32(cr[q], al[q >> 1][0], al[q >> 1][1], al[q >> 1][2], al[q >> 1][3], bh[q & 1][0],
+                                  bh[q & 1][1]);
+        if (!BX)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                float (&d)[4] = acc[2 * mt + nt];
-                if (!AX) ptx::mma1688_tf32(d, al[mt][0], al[mt][1], al[mt][2], al[mt][3], bh[nt][0], bh[nt][1]);
-                if (!BX) ptx::mma1688_tf32(d, ah[mt][0], ah[mt][1], ah[mt][2], ah[mt][3], bl[nt][0], bl[nt][1]);
-                ptx::mma1688_tf32(d, ah[mt][0], ah[mt][1], ah[mt][2], ah[mt][3], bh[nt][0], bh[nt][1]);
-            }
+            for (int q = 0; q < 4; ++q)
+                ptx::mma1688_tf32(cr[q], ah[q >> 1][0], ah[q >> 1][1], ah[q >> 1][2], ah[q >> 1][3], bl[q & 1][0],
+                                  bl[q & 1][1]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            ptx::mma1688_tf32(acc[q], ah[q >> 1][0], ah[q >> 1][1], ah[q >> 1][2], ah[q >> 1][3], bh[q & 1][0],
+                              bh[q & 1][1]);
     }
+    if (!AX || !BX)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[q][e] += cr[q][e];
 }
 
 __device__ __forceinline__ void zero(float (&acc)[4][4]) {
@@ -307,20 +320,43 @@ __device__ __forceinline__ void col_add(float* arr, const float (&v)[4], float s
     }
 }
 
-// T = (I + A)^-1 for a strictly lower A, by forward substitution one row at a time
-// (thread c = tid & 63 owns column c; the four warps-quarters split the sum over j).
-__device__ void unit_lower_inverse(float* Tm, const float* A, float* part) {
-    const int c = threadIdx.x & 63, r = threadIdx.x >> 6;
+// T = (I + A)^-1 for a strictly lower 64 x 64 A: the four 16 x 16 diagonal blocks by forward
+// substitution (one warp each, a lane per column), then two levels of block combination,
+// [L11 0; L21 L22]^-1 = [T11 0; -T22 L21 T11, T22], with 16- and then 32-row blocks.
+// W: scratch of 32 rows.
+__device__ void unit_lower_inverse(float* Tm, const float* A, float* W) {
     for (int e = threadIdx.x; e < kC * kLd; e += kThreads) Tm[e] = 0.f;
     __syncthreads();
-    if (threadIdx.x < kC) Tm[threadIdx.x * kLd + threadIdx.x] = 1.f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < 4 && lane < 16) {
+        const int b0 = 16 * warp, c = b0 + lane;
+        Tm[c * kLd + c] = 1.f;
+        __syncwarp(0xffffu);
+        for (int i = b0 + 1; i < b0 + 16; ++i) {
+            if (c < i) {
+                float a = 0.f;
+                for (int j = c; j < i; ++j) a = fmaf(A[i * kLd + j], Tm[j * kLd + c], a);
+                Tm[i * kLd + c] = -a;
+            }
+            __syncwarp(0xffffu);
+        }
+    }
     __syncthreads();
-    for (int i = 1; i < kC; ++i) {
-        float a = 0.f;
-        for (int j = r; j < i; j += 4) a = fmaf(A[i * kLd + j], Tm[j * kLd + c], a);
-        part[r * kC + c] = a;
+    for (int h = 16; h < kC; h *= 2) {
+        const int nb = kC / (2 * h);
+        for (int e = threadIdx.x; e < nb * h * h; e += kThreads) {  // W = L21 T11 (T11 lower: k >= cc)
+            const int blk = e / (h * h), rr = (e / h) % h, cc = e % h, r0 = 2 * h * blk;
+            float a = 0.f;
+            for (int k = cc; k < h; ++k) a = fmaf(A[(r0 + h + rr) * kLd + r0 + k], Tm[(r0 + k) * kLd + r0 + cc], a);
+            W[(blk * h + rr) * kLd + cc] = a;
+        }
         __syncthreads();
-        if (threadIdx.x < kC && c < i) Tm[i * kLd + c] = -(part[c] + part[kC + c] + part[2 * kC + c] + part[3 * kC + c]);
+        for (int e = threadIdx.x; e < nb * h * h; e += kThreads) {  // T21 = -T22 W (T22 lower: k <= rr)
+            const int blk = e / (h * h), rr = (e / h) % h, cc = e % h, r0 = 2 * h * blk;
+            float a = 0.f;
+            for (int k = 0; k <= rr; ++k) a = fmaf(Tm[(r0 + h + rr) * kLd + r0 + h + k], W[(blk * h + k) * kLd + cc], a);
+            Tm[(r0 + h + rr) * kLd + r0 + cc] = -a;
+        }
         __syncthreads();
     }
 }
@@ -341,7 +377,6 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
     float* B1 = DX + kMat;
     float* B2 = B1 + kMat;
     Scal& s = *reinterpret_cast<Scal*>(B2 + kMat);
-    float* part = reinterpret_cast<float*>(&s + 1);
     constexpr bool EX = sizeof(Tin) == 2;  // bf16 inputs are exact tf32 operands
 
     const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N;
@@ -381,7 +416,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
                  ws[kWsV * kWsMat + i * kD + j] = acc2[m][n];)
         return;
     }
-    unit_lower_inverse(Tm, A, part);
+    unit_lower_inverse(Tm, A, B1);
     // B1 = diag(w) T diag(e^Lx) X, B2 = diag(w) T Y, A <- P^T dO
     zero(acc);
     mm<false, false>(acc, Tm, DX);
@@ -795,7 +830,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
 }
 
 constexpr size_t kScalBytes = sizeof(Scal);
-constexpr size_t kPrepSmem = 10 * kMat * sizeof(float) + kScalBytes + 4 * kC * sizeof(float);
+constexpr size_t kPrepSmem = 10 * kMat * sizeof(float) + kScalBytes;
 constexpr size_t gradSmem(bool ip) { return (ip ? 11 : 12) * kMat * sizeof(float) + kScalBytes + (5 * kC + 8) * sizeof(float); }
 
 template <typename Tin, bool IP>
