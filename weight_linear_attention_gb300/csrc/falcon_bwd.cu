@@ -40,7 +40,8 @@ constexpr int kD = 64;        // dk = dv
 constexpr int kC = 64;        // chunk length
 constexpr int kLd = 68;       // shared-memory row stride (floats): 16-byte rows, tensor-core fragments
 constexpr int kMat = kC * kLd;
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;       // prep and gradient kernels: 16 warps
+constexpr int kChainThreads = 256;  // state scans: 16 x 16 threads
 constexpr int kCols = 16;     // value columns per chain CTA
 constexpr int kWsMat = kD * kD;             // floats per workspace matrix
 constexpr int kWsChunk = 6 * kWsMat;        // M, U, V, T, S_n, dS_{n+1}
@@ -203,15 +204,16 @@ __device__ void chunk_scalars(Scal& s, const float* X, const BParams& p, long lo
 // as head*head + head*rem + rem*head (the remainder products carry the bits tf32 drops, so the
 // result has fp32 accuracy). An operand flagged exact (a bf16 input, which tf32 holds without loss)
 // has no remainder and skips its pass.
-// Warp w owns output rows 32 (w >> 2) .. + 31 (two m16 tiles) and columns 16 (w & 3) .. + 15 (two n8
-// tiles). acc[m][n]: m = 2 * (m16 tile) + (n8 tile), n = the fragment element (2 * row half + column).
+// Warp w (of 16) owns output rows 16 (w >> 2) .. + 15 (one m16 tile) and columns 16 (w & 3) .. + 15
+// (two n8 tiles). acc[m][n]: m = the n8 tile, n = the fragment element (2 * row half + column).
 __device__ __forceinline__ int tile_row(int m, int n) {
     const int lane = threadIdx.x & 31;
-    return 32 * (threadIdx.x >> 7) + 16 * (m >> 1) + (lane >> 2) + 8 * (n >> 1);
+    (void)m;
+    return 16 * (threadIdx.x >> 7) + (lane >> 2) + 8 * (n >> 1);
 }
 __device__ __forceinline__ int tile_col(int m, int n) {
     const int lane = threadIdx.x & 31;
-    return 16 * ((threadIdx.x >> 5) & 3) + 8 * (m & 1) + 2 * (lane & 3) + (n & 1);
+    return 16 * ((threadIdx.x >> 5) & 3) + 8 * m + 2 * (lane & 3) + (n & 1);
 }
 
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
@@ -221,23 +223,21 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
 
 // acc += A B with A(i, k) = a[i][k] (TA: a[k][i]) and B(k, j) = b[k][j] (TB: b[j][k]).
 template <bool TA, bool TB, bool AX = false, bool BX = false>
-__device__ __forceinline__ void mm(float (&acc)[4][4], const float* a, const float* b) {
+__device__ __forceinline__ void mm(float (&acc)[2][4], const float* a, const float* b) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int rb = 32 * (threadIdx.x >> 7), cb = 16 * ((threadIdx.x >> 5) & 3);
+    const int r = 16 * (threadIdx.x >> 7) + g, cb = 16 * ((threadIdx.x >> 5) & 3);
     auto A = [&](int i, int k) { return TA ? a[k * kLd + i] : a[i * kLd + k]; };
     auto B = [&](int k, int j) { return TB ? b[j * kLd + k] : b[k * kLd + j]; };
-    float cr[4][4] = {};
+    float cr[2][4] = {};
 #pragma unroll 2
     for (int k0 = 0; k0 < kD; k0 += 8) {
-        uint32_t ah[2][4], al[2][4], bh[2][2], bl[2][2];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            const int r = rb + 16 * mt + g;
+        uint32_t ah[4], al[4], bh[2][2], bl[2][2];
+        {
             const float x[4] = {A(r, k0 + t), A(r + 8, k0 + t), A(r, k0 + t + 4), A(r + 8, k0 + t + 4)};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if (AX) ah[mt][e] = __float_as_uint(x[e]), al[mt][e] = 0u;
-                else split_tf32(x[e], ah[mt][e], al[mt][e]);
+                if (AX) ah[e] = __float_as_uint(x[e]), al[e] = 0u;
+                else split_tf32(x[e], ah[e], al[e]);
             }
         }
 #pragma unroll
@@ -250,44 +250,37 @@ __device__ __forceinline__ void mm(float (&acc)[4][4], const float* a, const flo
                 else split_tf32(y[e], bh[nt][e], bl[nt][e]);
             }
         }
-        // the three passes in turn over the four tiles, remainder terms into their own accumulators,
-        // so that consecutive MMAs are independent
+        // the three passes in turn over the two tiles, remainder terms into their own accumulators
         if (!AX)
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                ptx::mma1688_tf32(cr[q], al[q >> 1][0], al[q >> 1][1], al[q >> 1][2], al[q >> 1][3], bh[q & 1][0],
-                                  bh[q & 1][1]);
+            for (int q = 0; q < 2; ++q) ptx::mma1688_tf32(cr[q], al[0], al[1], al[2], al[3], bh[q][0], bh[q][1]);
         if (!BX)
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                ptx::mma1688_tf32(cr[q], ah[q >> 1][0], ah[q >> 1][1], ah[q >> 1][2], ah[q >> 1][3], bl[q & 1][0],
-                                  bl[q & 1][1]);
+            for (int q = 0; q < 2; ++q) ptx::mma1688_tf32(cr[q], ah[0], ah[1], ah[2], ah[3], bl[q][0], bl[q][1]);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            ptx::mma1688_tf32(acc[q], ah[q >> 1][0], ah[q >> 1][1], ah[q >> 1][2], ah[q >> 1][3], bh[q & 1][0],
-                              bh[q & 1][1]);
+        for (int q = 0; q < 2; ++q) ptx::mma1688_tf32(acc[q], ah[0], ah[1], ah[2], ah[3], bh[q][0], bh[q][1]);
     }
     if (!AX || !BX)
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[q][e] += cr[q][e];
 }
 
-__device__ __forceinline__ void zero(float (&acc)[4][4]) {
+__device__ __forceinline__ void zero(float (&acc)[2][4]) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
+    for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int n = 0; n < 4; ++n) acc[m][n] = 0.f;
 }
 
 // Runs the body for each accumulator element acc[m][n] of this thread, at output (i, j); ri and ci
-// index the thread's four rows and four columns (for row_add / col_add).
+// index the thread's two rows and four columns (for row_add / col_add).
 #define FOR_TILE(...)                                                         \
-    _Pragma("unroll") for (int m = 0; m < 4; ++m) {                           \
+    _Pragma("unroll") for (int m = 0; m < 2; ++m) {                           \
         _Pragma("unroll") for (int n = 0; n < 4; ++n) {                       \
             const int i = tile_row(m, n), j = tile_col(m, n);                 \
-            const int ri = 2 * (m >> 1) + (n >> 1), ci = 2 * (m & 1) + (n & 1); \
+            const int ri = n >> 1, ci = 2 * m + (n & 1);                      \
             (void)ri;                                                         \
             (void)ci;                                                         \
             __VA_ARGS__                                                       \
@@ -295,15 +288,15 @@ __device__ __forceinline__ void zero(float (&acc)[4][4]) {
     }
 
 // arr[i] += sign * scale[i] * (sum over the whole row of this CTA's partial sums v[ri]).
-__device__ __forceinline__ void row_add(float* arr, const float (&v)[4], const float* scale = nullptr,
+__device__ __forceinline__ void row_add(float* arr, const float (&v)[2], const float* scale = nullptr,
                                         float sign = 1.f) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int ri = 0; ri < 4; ++ri) {
+    for (int ri = 0; ri < 2; ++ri) {
         float x = v[ri];
         x += __shfl_xor_sync(0xffffffffu, x, 1);
         x += __shfl_xor_sync(0xffffffffu, x, 2);
-        const int i = tile_row(2 * (ri >> 1), 2 * (ri & 1));
+        const int i = tile_row(0, 2 * ri);
         if ((lane & 3) == 0) atomicAdd(&arr[i], sign * (scale ? scale[i] : 1.f) * x);
     }
 }
@@ -364,7 +357,7 @@ __device__ void unit_lower_inverse(float* Tm, const float* A, float* W) {
 // --------------------------------------------------------------------------------------------------
 // falcon_bwd_prep: one CTA per chunk.
 template <typename Tin, bool IP>
-__global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
+__global__ void __launch_bounds__(kThreads, 1) falcon_bwd_prep(const BParams p) {
     extern __shared__ __align__(16) float sm[];
     float* X = sm;
     float* Q = X + kMat;
@@ -386,7 +379,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
     __syncthreads();
     chunk_scalars(s, X, p, bh, t0, nr);
     float* ws = p.ws + cid * kWsChunk;
-    float acc[4][4], acc2[4][4];
+    float acc[2][4], acc2[2][4];
 
     // Falcon-1: P, A and diag(e^Lx) X
     if (!IP) {
@@ -453,9 +446,9 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_prep(const BParams p) {
 // 4 r4 .. 4 r4 + 3 of column c. The state slice is kept transposed (column-major) so a thread reads four
 // consecutive k of its column at once; M_n is stored so that four consecutive output rows of one k are
 // adjacent (transposed for S_{n+1} = M_n S_n, as is for dS_n = M_n^T dS_{n+1}). The next step's M and
-// U (or V) are loaded into registers while the current step computes.
+// U (or V) of the next two steps are loaded into registers while the current step computes.
 constexpr int kLdc = 68;  // 16-byte aligned rows
-__global__ void __launch_bounds__(kThreads) falcon_bwd_chain(const BParams p) {
+__global__ void __launch_bounds__(kChainThreads) falcon_bwd_chain(const BParams p) {
     __shared__ __align__(16) float Ms[2][kD * kLdc];
     __shared__ __align__(16) float Sv[2][kCols][kLdc];  // Sv[b][c][k] = S[k][column c]
     const long long bh = blockIdx.x / (kD / kCols);
@@ -467,12 +460,12 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_chain(const BParams p) {
     auto load_M = [&](long long nck, float4 (&reg)[4]) {
         const float4* src = reinterpret_cast<const float4*>(wsq + nck * kWsChunk + kWsM * kWsMat);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) reg[u] = src[threadIdx.x + u * kThreads];
+        for (int u = 0; u < 4; ++u) reg[u] = src[threadIdx.x + u * kChainThreads];
     };
     auto store_M = [&](float* dst, const float4 (&reg)[4], bool transpose) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int e = 4 * (threadIdx.x + u * kThreads), row = e >> 6, col = e & 63;
+            const int e = 4 * (threadIdx.x + u * kChainThreads), row = e >> 6, col = e & 63;
             if (transpose) {
                 dst[col * kLdc + row] = reg[u].x;
                 dst[(col + 1) * kLdc + row] = reg[u].y;
@@ -507,55 +500,67 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_chain(const BParams p) {
         *reinterpret_cast<float4*>(So + r0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     };
 
-    float4 regM[4];
-    float off[4], offn[4];
+    // M and U (V) of the next two steps are in flight in registers: the loads for step n + 2 are
+    // issued at step n and stored to shared memory at the end of step n + 1.
+    float4 regM1[4], regM2[4];
+    float off[4], off1[4], off2[4];
     // forward: S_{n+1} = M_n S_n + U_n, storing S_n
 #pragma unroll
     for (int z = 0; z < 4; ++z) Sv[0][c][r0 + z] = p.S0 ? p.S0[(bh * kD + r0 + z) * kD + cg + c] : 0.f;
-    load_M(0, regM);
+    load_M(0, regM1);
     load_off(0, kWsU, off);
-    store_M(Ms[0], regM, true);
+    store_M(Ms[0], regM1, true);
+    if (N > 1) {
+        load_M(1, regM1);
+        load_off(1, kWsU, off1);
+    }
     __syncthreads();
     for (long long nck = 0; nck < N; ++nck) {
         const int b = (int)(nck & 1);
-        const bool more = nck + 1 < N;
-        if (more) {
-            load_M(nck + 1, regM);
-            load_off(nck + 1, kWsU, offn);
+        if (nck + 2 < N) {
+            load_M(nck + 2, regM2);
+            load_off(nck + 2, kWsU, off2);
         }
         float* wc = wsq + nck * kWsChunk + kWsS * kWsMat + cg + c;
 #pragma unroll
         for (int z = 0; z < 4; ++z) wc[(r0 + z) * kD] = Sv[b][c][r0 + z];
         step(Ms[b], Sv[b][c], Sv[b ^ 1][c], off);
-        if (more) {
-            store_M(Ms[b ^ 1], regM, true);
+        if (nck + 1 < N) store_M(Ms[b ^ 1], regM1, true);
 #pragma unroll
-            for (int z = 0; z < 4; ++z) off[z] = offn[z];
+        for (int u = 0; u < 4; ++u) {
+            off[u] = off1[u];
+            off1[u] = off2[u];
+            regM1[u] = regM2[u];
         }
         __syncthreads();
     }
     // backward: dS_n = M_n^T dS_{n+1} + V_n, storing dS_{n+1}
 #pragma unroll
     for (int z = 0; z < 4; ++z) Sv[0][c][r0 + z] = p.dS_final ? p.dS_final[(bh * kD + r0 + z) * kD + cg + c] : 0.f;
-    load_M(N - 1, regM);
+    load_M(N - 1, regM1);
     load_off(N - 1, kWsV, off);
-    store_M(Ms[0], regM, false);
+    store_M(Ms[0], regM1, false);
+    if (N > 1) {
+        load_M(N - 2, regM1);
+        load_off(N - 2, kWsV, off1);
+    }
     __syncthreads();
     int b = 0;
     for (long long nck = N - 1; nck >= 0; --nck, b ^= 1) {
-        const bool more = nck > 0;
-        if (more) {
-            load_M(nck - 1, regM);
-            load_off(nck - 1, kWsV, offn);
+        if (nck >= 2) {
+            load_M(nck - 2, regM2);
+            load_off(nck - 2, kWsV, off2);
         }
         float* wc = wsq + nck * kWsChunk + kWsDS * kWsMat + cg + c;
 #pragma unroll
         for (int z = 0; z < 4; ++z) wc[(r0 + z) * kD] = Sv[b][c][r0 + z];
         step(Ms[b], Sv[b][c], Sv[b ^ 1][c], off);
-        if (more) {
-            store_M(Ms[b ^ 1], regM, false);
+        if (nck > 0) store_M(Ms[b ^ 1], regM1, false);
 #pragma unroll
-            for (int z = 0; z < 4; ++z) off[z] = offn[z];
+        for (int u = 0; u < 4; ++u) {
+            off[u] = off1[u];
+            off1[u] = off2[u];
+            regM1[u] = regM2[u];
         }
         __syncthreads();
     }
@@ -567,7 +572,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_chain(const BParams p) {
 // --------------------------------------------------------------------------------------------------
 // falcon_bwd_grad: one CTA per chunk.
 template <typename Tin, bool IP>
-__global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
+__global__ void __launch_bounds__(kThreads, 1) falcon_bwd_grad(const BParams p) {
     extern __shared__ __align__(16) float sm[];
     float* X = sm;
     float* Q = X + kMat;
@@ -587,7 +592,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     float* dLx = dL + kC;
     float* dw = dLx + kC;
     float* c2 = dw + kC;
-    float* red = c2 + kC;  // [8] block reduction
+    float* red = c2 + kC;  // [warps] block reduction
 
     constexpr bool EX = sizeof(Tin) == 2;  // bf16 inputs are exact tf32 operands
     float* R = IP ? Y : b0;
@@ -613,11 +618,11 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
         dL[threadIdx.x] = 0.f;
         dLx[threadIdx.x] = 0.f;
     }
-    if (threadIdx.x < 8) red[threadIdx.x] = 0.f;
+    if (threadIdx.x < kThreads / 32) red[threadIdx.x] = 0.f;
     __syncthreads();
     chunk_scalars(s, X, p, bh, t0, nr);
     const int lane = threadIdx.x & 31;
-    float acc[4][4], acc2[4][4];
+    float acc[2][4], acc2[2][4];
 
     // <dS', S>
     {
@@ -686,7 +691,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     }
     __syncthreads();  // Tm (T) and b1 (dR) are read no more
     {
-        float rowL[4] = {0.f, 0.f, 0.f, 0.f}, colE[4] = {0.f, 0.f, 0.f, 0.f}, colL[4] = {0.f, 0.f, 0.f, 0.f};
+        float rowL[2] = {0.f, 0.f}, colE[4] = {0.f, 0.f, 0.f, 0.f}, colL[4] = {0.f, 0.f, 0.f, 0.f};
         FOR_TILE({
             float v = 0.f;
             if (j <= i) {
@@ -704,7 +709,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
         col_add(dL, colL, -1.f);
     }
     if (!IP) {  // dA = -dZ R^T (j < i) -> d eta, dLx, dL; dG = dA eta_j e^{Lx_i - L_j}, into b1
-        float rowX[4] = {0.f, 0.f, 0.f, 0.f}, colE[4] = {0.f, 0.f, 0.f, 0.f}, colL[4] = {0.f, 0.f, 0.f, 0.f};
+        float rowX[2] = {0.f, 0.f}, colE[4] = {0.f, 0.f, 0.f, 0.f}, colL[4] = {0.f, 0.f, 0.f, 0.f};
         FOR_TILE({
             float v = 0.f;
             if (j < i) {
@@ -742,7 +747,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
         mm<false, false, false, EX>(acc, b1, X);
         zero(acc2);
         mm<false, true>(acc2, b4, S);
-        float rowX[4] = {0.f, 0.f, 0.f, 0.f};
+        float rowX[2] = {0.f, 0.f};
         FOR_TILE(DXa[i * kLd + j] += acc[m][n] - s.eLx[i] * acc2[m][n];
                  rowX[ri] = fmaf(X[i * kLd + j], acc2[m][n], rowX[ri]);)
         row_add(dLx, rowX, s.eLx, -1.f);
@@ -755,7 +760,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
     zero(acc2);
     mm<false, false, false, EX>(acc2, Tm, X);
     {
-        float rowL[4] = {0.f, 0.f, 0.f, 0.f};
+        float rowL[2] = {0.f, 0.f};
         float* dqo = p.dq + (bh * p.T + t0) * kD;
         FOR_TILE(rowL[ri] = fmaf(Q[i * kLd + j], acc[m][n], rowL[ri]);
                  if (i < nr) dqo[i * kD + j] = s.eL[i] * acc[m][n] + acc2[m][n];)
@@ -782,7 +787,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
         dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 1);
         float dss = 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) dss += red[u];
+        for (int u = 0; u < kThreads / 32; ++u) dss += red[u];
         if (l == 31) dl[1] += dwsum + s.eLC * dss;
         // suffix sums: d log gamma_u = sum_{i >= u} dL_i
         float v = dl[0] + dl[1];
@@ -831,7 +836,7 @@ __global__ void __launch_bounds__(kThreads) falcon_bwd_grad(const BParams p) {
 
 constexpr size_t kScalBytes = sizeof(Scal);
 constexpr size_t kPrepSmem = 10 * kMat * sizeof(float) + kScalBytes;
-constexpr size_t gradSmem(bool ip) { return (ip ? 11 : 12) * kMat * sizeof(float) + kScalBytes + (5 * kC + 8) * sizeof(float); }
+constexpr size_t gradSmem(bool ip) { return (ip ? 11 : 12) * kMat * sizeof(float) + kScalBytes + (5 * kC + kThreads / 32) * sizeof(float); }
 
 template <typename Tin, bool IP>
 int launch_typed(const BParams& p, cudaStream_t st) {
@@ -839,7 +844,7 @@ int launch_typed(const BParams& p, cudaStream_t st) {
     cudaFuncSetAttribute(falcon_bwd_prep<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     cudaFuncSetAttribute(falcon_bwd_grad<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gradSmem(IP));
     falcon_bwd_prep<Tin, IP><<<chunks, kThreads, kPrepSmem, st>>>(p);
-    falcon_bwd_chain<<<(unsigned)(p.BH * (kD / kCols)), kThreads, 0, st>>>(p);
+    falcon_bwd_chain<<<(unsigned)(p.BH * (kD / kCols)), kChainThreads, 0, st>>>(p);
     falcon_bwd_grad<Tin, IP><<<chunks, kThreads, gradSmem(IP), st>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
