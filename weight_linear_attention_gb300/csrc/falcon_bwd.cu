@@ -443,125 +443,106 @@ __global__ void __launch_bounds__(kThreads, 1) falcon_bwd_prep(const BParams p) 
 
 // --------------------------------------------------------------------------------------------------
 // falcon_bwd_chain: one CTA per (sequence, group of 16 value columns). Thread (r4, c) owns rows
-// 4 r4 .. 4 r4 + 3 of column c. The state slice is kept transposed (column-major) so a thread reads four
-// consecutive k of its column at once; M_n is stored so that four consecutive output rows of one k are
-// adjacent (transposed for S_{n+1} = M_n S_n, as is for dS_n = M_n^T dS_{n+1}). The next step's M and
-// U (or V) of the next two steps are loaded into registers while the current step computes.
-constexpr int kLdc = 68;  // 16-byte aligned rows
+// 4 r4 .. 4 r4 + 3 of column c. The state slice is kept transposed (column-major) so that a thread reads
+// four consecutive k of its column at once. M_n (row-major) and the column slice of U_n (forward) or
+// V_n (backward) arrive through a three-stage ring of 16-byte asynchronous copies issued two steps
+// ahead of their use.
+constexpr int kLdc = 68;      // 16-byte aligned rows
+constexpr int kStages = 3;
+constexpr size_t kChainSmem = (size_t)kStages * (kD * kLdc + kD * kCols) * sizeof(float) + 2 * kCols * kLdc * sizeof(float);
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kChainThreads) falcon_bwd_chain(const BParams p) {
-    __shared__ __align__(16) float Ms[2][kD * kLdc];
-    __shared__ __align__(16) float Sv[2][kCols][kLdc];  // Sv[b][c][k] = S[k][column c]
+    extern __shared__ __align__(16) float smc[];
+    float* Ms = smc;                              // [kStages][kD * kLdc]
+    float* Os = Ms + kStages * kD * kLdc;         // [kStages][kD][kCols]  offsets (U or V columns)
+    float (*Sv)[kCols][kLdc] = reinterpret_cast<float (*)[kCols][kLdc]>(Os + kStages * kD * kCols);  // [2]
     const long long bh = blockIdx.x / (kD / kCols);
     const int cg = (int)(blockIdx.x % (kD / kCols)) * kCols;
     const int c = threadIdx.x & 15, r0 = 4 * (threadIdx.x >> 4);
     const long long N = p.N;
-    float* wsq = p.ws + bh * N * kWsChunk;
+    const float* wsq = p.ws + bh * N * kWsChunk;
 
-    auto load_M = [&](long long nck, float4 (&reg)[4]) {
-        const float4* src = reinterpret_cast<const float4*>(wsq + nck * kWsChunk + kWsM * kWsMat);
+    // stage <- (M_n, offset slice `which` of chunk n); an empty group when n is out of range
+    auto issue = [&](long long nck, int which) {
+        if (nck >= 0 && nck < N) {
+            const int st = (int)(((nck % kStages) + kStages) % kStages);
+            const float* m = wsq + nck * kWsChunk + kWsM * kWsMat;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) reg[u] = src[threadIdx.x + u * kChainThreads];
-    };
-    auto store_M = [&](float* dst, const float4 (&reg)[4], bool transpose) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int e = 4 * (threadIdx.x + u * kChainThreads), row = e >> 6, col = e & 63;
-            if (transpose) {
-                dst[col * kLdc + row] = reg[u].x;
-                dst[(col + 1) * kLdc + row] = reg[u].y;
-                dst[(col + 2) * kLdc + row] = reg[u].z;
-                dst[(col + 3) * kLdc + row] = reg[u].w;
-            } else {
-                *reinterpret_cast<float4*>(dst + row * kLdc + col) = reg[u];
+            for (int u = 0; u < 4; ++u) {
+                const int e = 4 * (threadIdx.x + u * kChainThreads), row = e >> 6, col = e & 63;
+                cp_async16(Ms + st * kD * kLdc + row * kLdc + col, m + e);
             }
+            const int row = threadIdx.x >> 2, q = 4 * (threadIdx.x & 3);
+            cp_async16(Os + (st * kD + row) * kCols + q, wsq + nck * kWsChunk + which * kWsMat + row * kD + cg + q);
         }
+        cp_async_commit();
     };
-    auto load_off = [&](long long nck, int which, float (&o)[4]) {
-        const float* src = wsq + nck * kWsChunk + which * kWsMat + cg + c;
-#pragma unroll
-        for (int z = 0; z < 4; ++z) o[z] = src[(r0 + z) * kD];
-    };
-    // one step: out[c][r0 + z] = off[z] + sum_k Ms[k][r0 + z] * Sv[c][k]
-    auto step = [&](const float* Mk, const float* Sc, float* So, const float (&off)[4]) {
-        float acc[4] = {off[0], off[1], off[2], off[3]};
+    // out[r0 + z] = off + sum_k M(r0 + z, k) S(k)   (forward: M(i, k) = Mk[i][k]; backward: M^T, Mk[k][i])
+    auto step = [&](const float* Mk, const float* off, const float* Sc, float* So, bool transpose) {
+        float acc[4] = {off[(r0 + 0) * kCols], off[(r0 + 1) * kCols], off[(r0 + 2) * kCols], off[(r0 + 3) * kCols]};
 #pragma unroll 4
         for (int k = 0; k < kD; k += 4) {
             const float4 sv = *reinterpret_cast<const float4*>(Sc + k);
             const float s4[4] = {sv.x, sv.y, sv.z, sv.w};
+            if (transpose) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const float4 mv = *reinterpret_cast<const float4*>(Mk + (k + kk) * kLdc + r0);
-                acc[0] = fmaf(mv.x, s4[kk], acc[0]);
-                acc[1] = fmaf(mv.y, s4[kk], acc[1]);
-                acc[2] = fmaf(mv.z, s4[kk], acc[2]);
-                acc[3] = fmaf(mv.w, s4[kk], acc[3]);
+                for (int kk = 0; kk < 4; ++kk) {
+                    const float4 mv = *reinterpret_cast<const float4*>(Mk + (k + kk) * kLdc + r0);
+                    acc[0] = fmaf(mv.x, s4[kk], acc[0]);
+                    acc[1] = fmaf(mv.y, s4[kk], acc[1]);
+                    acc[2] = fmaf(mv.z, s4[kk], acc[2]);
+                    acc[3] = fmaf(mv.w, s4[kk], acc[3]);
+                }
+            } else {
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const float4 mv = *reinterpret_cast<const float4*>(Mk + (r0 + z) * kLdc + k);
+                    acc[z] = fmaf(mv.x, s4[0], fmaf(mv.y, s4[1], fmaf(mv.z, s4[2], fmaf(mv.w, s4[3], acc[z]))));
+                }
             }
         }
         *reinterpret_cast<float4*>(So + r0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     };
 
-    // M and U (V) of the next two steps are in flight in registers: the loads for step n + 2 are
-    // issued at step n and stored to shared memory at the end of step n + 1.
-    float4 regM1[4], regM2[4];
-    float off[4], off1[4], off2[4];
     // forward: S_{n+1} = M_n S_n + U_n, storing S_n
 #pragma unroll
     for (int z = 0; z < 4; ++z) Sv[0][c][r0 + z] = p.S0 ? p.S0[(bh * kD + r0 + z) * kD + cg + c] : 0.f;
-    load_M(0, regM1);
-    load_off(0, kWsU, off);
-    store_M(Ms[0], regM1, true);
-    if (N > 1) {
-        load_M(1, regM1);
-        load_off(1, kWsU, off1);
-    }
-    __syncthreads();
+    issue(0, kWsU);
+    issue(1, kWsU);
     for (long long nck = 0; nck < N; ++nck) {
-        const int b = (int)(nck & 1);
-        if (nck + 2 < N) {
-            load_M(nck + 2, regM2);
-            load_off(nck + 2, kWsU, off2);
-        }
-        float* wc = wsq + nck * kWsChunk + kWsS * kWsMat + cg + c;
+        const int b = (int)(nck & 1), st = (int)(nck % kStages);
+        issue(nck + 2, kWsU);
+        cp_async_wait2();
+        __syncthreads();
+        float* wc = p.ws + (bh * N + nck) * kWsChunk + kWsS * kWsMat + cg + c;
 #pragma unroll
         for (int z = 0; z < 4; ++z) wc[(r0 + z) * kD] = Sv[b][c][r0 + z];
-        step(Ms[b], Sv[b][c], Sv[b ^ 1][c], off);
-        if (nck + 1 < N) store_M(Ms[b ^ 1], regM1, true);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            off[u] = off1[u];
-            off1[u] = off2[u];
-            regM1[u] = regM2[u];
-        }
+        step(Ms + st * kD * kLdc, Os + st * kD * kCols + c, Sv[b][c], Sv[b ^ 1][c], false);
         __syncthreads();
     }
     // backward: dS_n = M_n^T dS_{n+1} + V_n, storing dS_{n+1}
 #pragma unroll
     for (int z = 0; z < 4; ++z) Sv[0][c][r0 + z] = p.dS_final ? p.dS_final[(bh * kD + r0 + z) * kD + cg + c] : 0.f;
-    load_M(N - 1, regM1);
-    load_off(N - 1, kWsV, off);
-    store_M(Ms[0], regM1, false);
-    if (N > 1) {
-        load_M(N - 2, regM1);
-        load_off(N - 2, kWsV, off1);
-    }
-    __syncthreads();
+    issue(N - 1, kWsV);
+    issue(N - 2, kWsV);
     int b = 0;
     for (long long nck = N - 1; nck >= 0; --nck, b ^= 1) {
-        if (nck >= 2) {
-            load_M(nck - 2, regM2);
-            load_off(nck - 2, kWsV, off2);
-        }
-        float* wc = wsq + nck * kWsChunk + kWsDS * kWsMat + cg + c;
+        const int st = (int)(nck % kStages);
+        issue(nck - 2, kWsV);
+        cp_async_wait2();
+        __syncthreads();
+        float* wc = p.ws + (bh * N + nck) * kWsChunk + kWsDS * kWsMat + cg + c;
 #pragma unroll
         for (int z = 0; z < 4; ++z) wc[(r0 + z) * kD] = Sv[b][c][r0 + z];
-        step(Ms[b], Sv[b][c], Sv[b ^ 1][c], off);
-        if (nck > 0) store_M(Ms[b ^ 1], regM1, false);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            off[u] = off1[u];
-            off1[u] = off2[u];
-            regM1[u] = regM2[u];
-        }
+        step(Ms + st * kD * kLdc, Os + st * kD * kCols + c, Sv[b][c], Sv[b ^ 1][c], true);
         __syncthreads();
     }
     if (p.dS0)
@@ -844,7 +825,8 @@ int launch_typed(const BParams& p, cudaStream_t st) {
     cudaFuncSetAttribute(falcon_bwd_prep<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     cudaFuncSetAttribute(falcon_bwd_grad<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gradSmem(IP));
     falcon_bwd_prep<Tin, IP><<<chunks, kThreads, kPrepSmem, st>>>(p);
-    falcon_bwd_chain<<<(unsigned)(p.BH * (kD / kCols)), kChainThreads, 0, st>>>(p);
+    cudaFuncSetAttribute(falcon_bwd_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
+    falcon_bwd_chain<<<(unsigned)(p.BH * (kD / kCols)), kChainThreads, kChainSmem, st>>>(p);
     falcon_bwd_grad<Tin, IP><<<chunks, kThreads, gradSmem(IP), st>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
