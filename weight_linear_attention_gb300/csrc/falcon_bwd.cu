@@ -216,9 +216,11 @@ __device__ __forceinline__ int tile_col(int m, int n) {
     return 16 * ((threadIdx.x >> 5) & 3) + 8 * m + 2 * (lane & 3) + (n & 1);
 }
 
+// x = head + remainder; the remainder goes to the tensor core as its fp32 bits (the unit reads the top
+// 19 bits of a tf32 operand, i.e. truncates the remainder, which costs at most 2^-10 of it).
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
     hi = ptx::tf32_rn(x);
-    lo = ptx::tf32_rn(x - __uint_as_float(hi));
+    lo = __float_as_uint(x - __uint_as_float(hi));
 }
 
 // acc += A B with A(i, k) = a[i][k] (TA: a[k][i]) and B(k, j) = b[k][j] (TB: b[j][k]).
@@ -229,7 +231,7 @@ __device__ __forceinline__ void mm(float (&acc)[2][4], const float* a, const flo
     auto A = [&](int i, int k) { return TA ? a[k * kLd + i] : a[i * kLd + k]; };
     auto B = [&](int k, int j) { return TB ? b[j * kLd + k] : b[k * kLd + j]; };
     float cr[2][4] = {};
-#pragma unroll 2
+#pragma unroll
     for (int k0 = 0; k0 < kD; k0 += 8) {
         uint32_t ah[4], al[4], bh[2][2], bl[2][2];
         {
