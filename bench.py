@@ -400,12 +400,13 @@ def run_ours(args, w):
 # --------------------------------------------------------------------------------------------------
 # backward workloads (falcon_bwd)
 
-ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12  # fp32 FMA lanes x 2 flops x max SM clock
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rates
 
 
 def _bwd_flops_per_chunk(w):
-    """fp32 flops the three backward kernels issue per 64-token chunk (64 x 64 x 64 products, 2 flops
-    per multiply-add): Falcon-1 prep 10 products and the triangular inverse (~1/3), the two scans 2,
+    """Flops of the chunk algebra the three backward kernels evaluate per 64-token chunk, each
+    64 x 64 x 64 product counted once (2 flops per multiply-add) whatever the number of tf32 passes
+    it takes: Falcon-1 prep 10 products and the triangular inverse (~1/3), the two scans 2,
     gradients 15; Falcon-1A prep 2, scans 2, gradients 9."""
     one = 2 * 64 ** 3
     return one * ((10 + 1 / 3 + 2 + 15) if w.variant == "falcon1" else (2 + 2 + 9))
@@ -581,7 +582,8 @@ def run_ours_bwd(args, w):
     value = _job_value(world, B * T, args.steps, total_ms)
     if rank != 0:
         return
-    hbm, _, src = _peaks()
+    hbm, bf16_peak, src = _peaks()
+    tf32_peak = bf16_peak * TF32_PER_BF16
     chunks = B * H * (-(-T // w.chunk))
     flops = _bwd_flops_per_chunk(w) * chunks
     achieved = flops / (ms_step / 1e3) / 1e12
@@ -594,10 +596,11 @@ def run_ours_bwd(args, w):
                    "chunk": w.chunk, "parallelism": f"dp{world} (independent sequences per GPU, no collective)",
                    "l2": f"rotating {nsets} input/gradient sets of {step_bytes / 1e6:.1f} MB (> L2 between reuses)",
                    "kernel": "backward: CUDA-core prep, chain and gradient kernels"},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
-                     "frac": achieved / ALU_PEAK_TFLOPS, "traffic": None,
-                     "scope": "one falcon_bwd call (all three kernels); fp32 FMA flops of the chunk algebra",
-                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz",
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tf32_peak, "traffic": None,
+                     "scope": "one falcon_bwd call (all three kernels); flops of the chunk algebra, each product "
+                              "counted once (tf32 tensor cores, 1-3 passes per product for fp32 accuracy)",
+                     "peak_source": f"{src} bf16 x nominal tf32/bf16 ratio 1.1/2.25",
                      "flops_per_step": flops, "hbm_algorithmic_bytes_per_step": step_bytes,
                      "hbm_frac": step_bytes / (ms_step / 1e3) / 1e9 / hbm, "hbm_peak_source": src},
         "e2e": e2e,
