@@ -186,3 +186,50 @@ def test_workspace_checks(lib):
 def test_binding_raises_when_library_missing(tmp_path):
     with pytest.raises(RuntimeError):
         F.load(str(tmp_path / "nope.so"))
+
+
+# ---------------------------------------------------------------- falcon_bwd (host-side checks only)
+
+def _bwd(variant=F.FALCON_1, dims=None, chunk=64, ws=A + (20 << 30), ws_bytes=None, **kw):
+    if dims is None:
+        dims = F.make_dims(2, 2, 64, 64, 64)
+    if ws_bytes is None:
+        ws_bytes = F.falcon_bwd_workspace_bytes(F.FALCON_1, dims, 64)
+    p = dict(q=A, k=A + (1 << 30), v=A + (2 << 30), beta=A + (3 << 30), lam=A + (4 << 30), S0=None, tail=None,
+             dout=A + (5 << 30), dS_final=None, dq=A + (10 << 30), dk=A + (11 << 30), dv=A + (12 << 30),
+             dbeta=A + (13 << 30), dlam=A + (14 << 30), dS0=None, dtail=None)
+    p.update(kw)
+    return F.falcon_bwd(variant, p["q"], p["k"], p["v"], p["beta"], p["lam"], p["S0"], p["tail"], p["dout"],
+                        p["dS_final"], p["dq"], p["dk"], p["dv"], p["dbeta"], p["dlam"], p["dS0"], p["dtail"], dims,
+                        chunk, ws, ws_bytes, stream=0)
+
+
+def test_bwd_workspace_bytes(lib):
+    # B*H*ceil(T/64) chunks of six fp32 64 x 64 matrices (M, U, V, T, S_n, dS_{n+1})
+    assert F.falcon_bwd_workspace_bytes(F.FALCON_1, F.make_dims(8, 12, 1024, 64, 64), 64) == 8 * 12 * 16 * 98304
+    assert F.falcon_bwd_workspace_bytes(F.FALCON_1A, F.make_dims(2, 3, 65, 64, 64, dtype=F.FALCON_F32), 64) \
+        == 2 * 3 * 2 * 98304
+    assert F.falcon_bwd_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 0, 64, 64), 64) == 0
+    for v in (F.FALCON_2, F.FALCON_2A, F.FALCON_3, F.FALCON_3A):  # no backward kernel for these yet
+        assert F.falcon_bwd_workspace_bytes(v, F.make_dims(2, 3, 64, 64, 64, window=2 if v >= 5 else 1), 64) == 0
+    assert F.falcon_bwd_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 64, 32, 32), 64) == 0
+    assert F.falcon_bwd_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 64, 64, 64), 32) == 0
+
+
+def test_bwd_argument_checks(lib):
+    assert _bwd(variant=F.FALCON_2) == F.FALCON_ERR_UNSUPPORTED
+    assert _bwd(chunk=32) == F.FALCON_ERR_UNSUPPORTED
+    assert _bwd(dims=F.make_dims(2, 2, 64, 32, 32)) == F.FALCON_ERR_UNSUPPORTED
+    for name in ("q", "dout", "dq", "dk", "dv", "dbeta", "dlam"):
+        assert _bwd(**{name: 0}) == F.FALCON_ERR_INVALID_ARG, name
+    assert _bwd(ws=None, ws_bytes=0) == F.FALCON_ERR_INVALID_ARG              # the workspace is required
+    assert _bwd(ws_bytes=1000) == F.FALCON_ERR_INVALID_ARG                    # too small
+    assert _bwd(ws=A + (20 << 30) + 128) == F.FALCON_ERR_MISALIGNED
+    assert _bwd(dq=A + (10 << 30) + 4) == F.FALCON_ERR_MISALIGNED
+    assert _bwd(dbeta=A + (13 << 30) + 2) == F.FALCON_ERR_MISALIGNED
+    assert _bwd(dq=A + 1024) == F.FALCON_ERR_INVALID_ARG                      # a gradient over an input
+    assert _bwd(dk=A + (10 << 30) + 4096) == F.FALCON_ERR_INVALID_ARG         # two gradients overlap
+    assert _bwd(ws=A + (14 << 30)) == F.FALCON_ERR_INVALID_ARG                # workspace over a gradient
+    assert _bwd(dtail=A + (15 << 30)) == F.FALCON_ERR_INVALID_ARG             # dtail with pos == 0
+    d = F.make_dims(2, 2, 64, 64, 64, pos=5)
+    assert _bwd(dims=d) == F.FALCON_ERR_INVALID_ARG                            # pos > 0 without a tail
