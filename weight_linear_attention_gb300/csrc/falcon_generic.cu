@@ -689,11 +689,11 @@ cudaError_t launch_typed(const Launch& a, const GParams& gp, dim3 grid, size_t s
 }
 
 int choose_dvs(const Launch& a) {
-    // Enough CTAs to cover the GPU twice over, slices no narrower than 16 columns,
-    // and a shared-memory footprint that fits one CTA.
+    // Enough CTAs to cover the GPU twice over, slices no narrower than 8 columns (one 16-byte
+    // load of bf16 values per row), and a shared-memory footprint that fits one CTA.
     int dvs = (int)a.dv;
     const int64_t seqs = a.B * a.H;
-    while (dvs > 16 && seqs * (a.dv / dvs) < 2 * 152) dvs /= 2;
+    while (dvs > 8 && seqs * (a.dv / dvs) < 2 * 152) dvs /= 2;
     while (dvs > 16 && generic_smem_bytes(a, dvs) > 200 * 1024) dvs /= 2;
     return dvs;
 }
