@@ -1,0 +1,111 @@
+"""GPU parity of the scan path (Falcon-1, 1A, 3, 3A with dk = dv = 64 and few sequences): every
+chunk's affine state map, the associative scan over those maps (groups of 16 chunks), then every
+chunk's outputs, against the fp64 oracle at the same bounds as the other paths (fp32 inputs:
+max|err| / max|ref| <= 1e-4; bf16: max|err| / RMS(ref) <= 2e-2). Cases span one group and several,
+ragged chunks, a nonzero initial state, continuation from a tail, the decay clamp, and the aliased
+S_final = S0 call.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from tests.gpu_util import rel_err, run_gpu, run_oracle, slice_inputs, tol
+from weight_linear_attention_gb300 import falcon as F
+from weight_linear_attention_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+F1, F1A, F3, F3A = 1, 2, 5, 6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from weight_linear_attention_gb300 import build
+
+    build.build()
+    F.load()
+
+
+def _wl(variant, dtype, **kw):
+    base = {F1: "f1_b8h12t1024_bf16", F1A: "f1a_b8h12t1024_bf16", F3: "f3w4_b2h12t16384_bf16",
+            F3A: "f3aw4_b2h12t16384_bf16"}[variant]
+    return I.WORKLOADS[base].with_(dtype=dtype, segments=1, **kw)
+
+
+def _check(name, gpu, ref, dtype):
+    quant = gpu.dtype == torch.bfloat16
+    e = rel_err(gpu.float().numpy(), ref, dtype, quantized_bf16=quant)
+    print(f"PARITY {name}: err {e:.3e} bound {tol(dtype):.1e}")
+    assert np.isfinite(e) and e <= tol(dtype), f"{name}: {e:.3e}"
+
+
+def _run(w, inp, chunk, S0=None, pos=0, tail=None, rtail=None, name=""):
+    dims = F.make_dims(*inp["q"].shape[:3], 64, 64, window=w.window,
+                       dtype=F.FALCON_F32 if w.dtype == "f32" else F.FALCON_BF16, pos=pos)
+    assert F.falcon_kernel_for(w.variant_id, dims, chunk) == 5
+    out, S, t = run_gpu(w.variant_id, inp, window=w.window, chunk=chunk, S0=S0, pos=pos, tail=tail)
+    ro, rS, rt = run_oracle(w.variant_id, inp, window=w.window, S0=S0, pos=pos, tail=rtail)
+    _check(f"{name} out", out, ro, w.torch_dtype)
+    _check(f"{name} S", S, rS, torch.float32 if w.dtype == "f32" else w.torch_dtype)
+    B, H = inp["q"].shape[:2]
+    tk, tv = F.split_tail(t, B, H, w.window, 64, 64)
+    np.testing.assert_array_equal(tk.double().numpy(), rt[0])
+    np.testing.assert_array_equal(tv.double().numpy(), rt[1])
+    return out, S, t, (ro, rS, rt)
+
+
+@pytest.mark.parametrize("variant,dtype,chunk,T", [
+    (F1, "f32", 64, 300),      # one group, ragged last chunk
+    (F1, "f32", 16, 1000),     # 63 chunks: four groups, the last partial
+    (F1A, "f32", 32, 1030),
+    (F1, "bf16", 32, 700),     # bf16 at chunk 32 (no split path there)
+    (F3, "bf16", 32, 1500),
+    (F3A, "bf16", 32, 1500),
+    (F3, "f32", 16, 600),
+])
+def test_scan_path(variant, dtype, chunk, T):
+    w = _wl(variant, dtype, nonzero_s0=True)
+    inp = I.make_inputs(w, seed=60 + T, seqlen=T, batch=2)
+    _run(w, inp, chunk, S0=inp["S0"], name=f"v{variant} {dtype} C={chunk} T={T}")
+
+
+@pytest.mark.parametrize("variant", [F1, F3])
+def test_scan_continuation(variant):
+    """Two calls: the second starts at pos > 0 from the first's S_final and tail."""
+    w = _wl(variant, "bf16")
+    T, cut = 1200, 517
+    inp = I.make_inputs(w, seed=70, seqlen=T, batch=2)
+    a, b = slice_inputs(inp, 0, cut), slice_inputs(inp, cut, T)
+    o1, S1, t1, (_, _, rt1) = _run(w, a, 32, name=f"v{variant} first")
+    W = w.window
+    o2, S2, t2 = run_gpu(w.variant_id, b, window=W, chunk=32, S0=S1, pos=cut, tail=t1)
+    ro, rS, _ = run_oracle(w.variant_id, inp, window=W)
+    _check(f"v{variant} cont out", torch.cat([o1, o2], dim=2), ro, w.torch_dtype)
+    _check(f"v{variant} cont S", S2, rS, w.torch_dtype)
+
+
+def test_scan_clamp():
+    w = _wl(F1, "f32", lam_const=1000.0, lam_shift=None)
+    inp = I.make_inputs(w, seed=71, seqlen=500, batch=1)
+    inp["beta"] = torch.full_like(inp["beta"], 1.5)
+    _run(w, inp, 32, name="clamp")
+
+
+def test_scan_state_alias():
+    w = _wl(F3, "bf16", nonzero_s0=True)
+    inp = I.make_inputs(w, seed=72, seqlen=900, batch=1)
+    dev = {n: inp[n].cuda() for n in ("q", "k", "v", "beta", "lam")}
+    S = inp["S0"].cuda().contiguous()
+    out = torch.empty_like(dev["v"])
+    d = F.make_dims(1, w.heads, 900, 64, 64, window=4, dtype=F.FALCON_BF16)
+    ws = F.workspace_for(F3, d, 32, "cuda")
+    assert ws is not None and F.falcon_kernel_for(F3, d, 32) == 5
+    st = F.falcon_fwd(F3, dev["q"], dev["k"], dev["v"], dev["beta"], dev["lam"], S, None, out, S, None, d, 32, ws)
+    assert st == 0
+    torch.cuda.synchronize()
+    ro, rS, _ = run_oracle(F3, inp, window=4, S0=inp["S0"])
+    _check("alias out", out.cpu(), ro, torch.bfloat16)
+    _check("alias S", S.cpu(), rS, torch.bfloat16)

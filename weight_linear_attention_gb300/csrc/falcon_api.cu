@@ -52,8 +52,10 @@ size_t tail_bytes_of(const falcon_dims_t* d) {
 // Workspace bytes a call with these (validated) arguments can use: the split path's, unless the
 // single-token kernel runs.
 size_t workspace_need(const falcon::Launch& a) {
-    if (falcon::decode_supported(a) || !falcon::split_supported(a)) return 0;
-    return falcon::split_workspace_bytes(a);
+    if (falcon::decode_supported(a)) return 0;
+    if (falcon::split_supported(a)) return falcon::split_workspace_bytes(a);
+    if (falcon::scan_supported(a)) return falcon::scan_workspace_bytes(a);
+    return 0;
 }
 
 int validate_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail, falcon::Launch* a) {
@@ -193,6 +195,7 @@ int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk) {
     if (validate_shape(variant, dims, chunk, dims && dims->pos > 0, &a) != FALCON_OK) return 0;
     if (falcon::decode_supported(a)) return 4;
     if (falcon::split_supported(a) && falcon::split_workspace_bytes(a) > 0) return 3;
+    if (falcon::scan_supported(a)) return 5;
     return falcon::tc_supported(a) ? 2 : 1;
 }
 
@@ -212,7 +215,7 @@ int falcon_fwd(int variant, const void* q, const void* k, const void* v, const f
     if (a.B * a.H == 0) return FALCON_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (falcon::decode_supported(a)) return falcon::launch_decode(a, s);
-    if (a.ws) return falcon::launch_split(a, s);
+    if (a.ws) return falcon::split_supported(a) ? falcon::launch_split(a, s) : falcon::launch_scan(a, s);
     if (falcon::tc_supported(a)) return falcon::launch_tc(a, s);
     return falcon::launch_generic(a, s);
 }
@@ -223,8 +226,11 @@ int falcon_fwd_static(int variant, const void* q, const void* k, const void* v, 
     falcon::Launch shape = {};
     const int st = validate_shape(variant, dims, chunk, tail != nullptr, &shape);
     if (st != FALCON_OK) return st;
-    const size_t need = workspace_need(shape);
-    if (need > FALCON_STATIC_WORKSPACE_BYTES) return FALCON_ERR_UNSUPPORTED;
+    size_t need = workspace_need(shape);
+    if (need > FALCON_STATIC_WORKSPACE_BYTES) {
+        if (falcon::split_supported(shape)) return FALCON_ERR_UNSUPPORTED;
+        need = 0;  // the scan path does not fit: the single-pass kernels run
+    }
     void* ws = nullptr;
     if (need > 0 && !(ws = static_workspace_address())) return FALCON_ERR_CUDA;
     return falcon_fwd(variant, q, k, v, beta, lambda, S0, tail, out, S_final, tail_out, dims, chunk, ws,

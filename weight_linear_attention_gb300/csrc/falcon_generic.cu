@@ -54,6 +54,15 @@ struct GParams {
     long long T, pos;
     int dk, dv, dvs, C, W;
     float eps, eps_gamma;
+    // 0: one CTA walks all chunks of its (sequence, column slice);
+    // 1 (map): one CTA per (sequence, slice, chunk) computes the chunk's affine state map S -> M S + U:
+    //   slices of the 2 dk virtual columns, the first dk those of M (state e_c, no target), the rest
+    //   those of U (zero state, the targets); the result goes to the chunk's workspace block;
+    // 2 (read): one CTA per (sequence, slice, chunk) forms the chunk's outputs from its start state
+    //   S_n in the chunk's workspace block.
+    int mode;
+    float* ws;   // per chunk (sequence-major) [M (dk x dk) | U (dk x dv) | S_n (dk x dv)], fp32
+    long long N; // chunks per sequence (modes 1, 2)
 };
 
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
@@ -222,10 +231,17 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
     const int RS = C * W + 1, CS = C + 1;
     const int NE = C + W - 1;
     const long long T = p.T, pos = p.pos;
-    const int slices = DV / DVS;
-    const long long bh = blockIdx.x / slices;
-    const int slice = blockIdx.x % slices;
-    const int c0 = slice * DVS;
+    const int mode = p.mode;
+    const int slices = (mode == 1 ? DK + DV : DV) / DVS;
+    const long long nck = mode == 0 ? 0 : (long long)(blockIdx.x % p.N);
+    const long long rest = mode == 0 ? (long long)blockIdx.x : (long long)(blockIdx.x / p.N);
+    const long long bh = rest / slices;
+    const int slice = (int)(rest % slices);
+    const int c0 = slice * DVS;          // first (virtual) column of this CTA
+    const bool mpart = mode == 1 && c0 < DK;  // map mode, columns of M: unit state, no targets
+    const int vc0 = mode == 1 ? (mpart ? 0 : c0 - DK) : c0;  // first value column of the targets
+    const long long blk = (long long)DK * DK + 2LL * DK * DV;
+    float* wsb = mode != 0 ? p.ws + (bh * p.N + nck) * blk : nullptr;  // this chunk's workspace block
 
     Smem s;
     smem_floats(VAR, DK, DVS, C, W, &s, smem_raw);
@@ -253,11 +269,15 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
     // Initial state slice.
     for (int idx = tid; idx < DK * DVS; idx += kThreads) {
         const int r = idx / DVS, c = idx % DVS;
-        s.S[idx] = p.S0 ? p.S0[(bh * DK + r) * DV + c0 + c] : 0.f;
+        float x;
+        if (mode == 1) x = mpart && r == c0 + c ? 1.f : 0.f;
+        else if (mode == 2) x = wsb[(long long)DK * DK + (long long)DK * DV + r * DV + c0 + c];
+        else x = p.S0 ? p.S0[(bh * DK + r) * DV + c0 + c] : 0.f;
+        s.S[idx] = x;
     }
 
-
-    for (long long t0 = 0; t0 < T; t0 += C) {
+    const long long t_begin = nck * C, t_end = mode == 0 ? T : min(T, t_begin + C);
+    for (long long t0 = t_begin; t0 < t_end; t0 += C) {
         const int n = (int)min((long long)C, T - t0);
         __syncthreads();  // previous chunk finished with every buffer
         // ---- (1) tiles. Extended row e <-> pair with global index pos + t0 + 2 - W + e. Eight elements
@@ -287,10 +307,10 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                     } else if (idx < nx + nq + ny) {  // values of the extended rows, this CTA's columns
                         const int e = (idx - nx - nq) / VV, c8 = 8 * ((idx - nx - nq) % VV);
                         const long long gpair = pos + t0 + 2 - W + e, u = t0 + 1 - W + e;
-                        if (e < n + W - 1 && gpair >= 2) {
-                            if (u >= 0) ld8(v + u * DV + c0 + c8, buf[m]);
+                        if (e < n + W - 1 && gpair >= 2 && !mpart) {
+                            if (u >= 0) ld8(v + u * DV + vc0 + c8, buf[m]);
                             else if (tail != nullptr && pos + 1 + u > 0)
-                                ld8(tail + (long long)W * DK + (u + W - 1) * DV + c0 + c8, buf[m]);
+                                ld8(tail + (long long)W * DK + (u + W - 1) * DV + vc0 + c8, buf[m]);
                         }
                     }
                 }
@@ -590,7 +610,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         __syncthreads();
         // ---- (6) outputs (read after write) and (7) carried state
         Tin* out = static_cast<Tin*>(p.out) + bh * T * DV;
-        for (int idx = tid; idx < n * DVS; idx += kThreads) {
+        for (int idx = tid; idx < (mode == 1 ? 0 : n * DVS); idx += kThreads) {
             const int i = idx / DVS, c = idx % DVS;
             float o;
             if (per_column(VAR)) {
@@ -622,7 +642,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             }
             stf(out + (t0 + i) * DV + c0 + c, o);
         }
-        for (int idx = tid; idx < DK * DVS; idx += kThreads) {
+        for (int idx = tid; idx < (mode == 2 ? 0 : DK * DVS); idx += kThreads) {
             const int r = idx / DVS, c = idx % DVS;
             float acc = 0.f;
             if (windowed(VAR)) {
@@ -651,12 +671,21 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         }
     }
     __syncthreads();
-    if (p.S_final)
+    if (mode == 1) {  // the chunk's map: M columns or U columns
+        float* dst = mpart ? wsb + c0 : wsb + (long long)DK * DK + vc0;
+        const int ld = mpart ? DK : DV;
+        for (int idx = tid; idx < DK * DVS; idx += kThreads) {
+            const int r = idx / DVS, c = idx % DVS;
+            dst[r * ld + c] = s.S[idx];
+        }
+        return;
+    }
+    if (p.S_final && mode == 0)
         for (int idx = tid; idx < DK * DVS; idx += kThreads) {
             const int r = idx / DVS, c = idx % DVS;
             p.S_final[(bh * DK + r) * DV + c0 + c] = s.S[idx];
         }
-    if (p.tail_out) {
+    if (p.tail_out && (mode == 0 || nck == p.N - 1)) {
         Tin* to = static_cast<Tin*>(p.tail_out) + bh * tail_stride;
         if (slice == 0)
             for (int idx = tid; idx < W * DK; idx += kThreads) {
@@ -705,9 +734,12 @@ size_t generic_smem_bytes(const Launch& a, int dvs) {
     return smem_floats(a.variant, (int)a.dk, dvs, a.chunk, W, nullptr, nullptr) * sizeof(float);
 }
 
-int launch_generic(const Launch& a, cudaStream_t st) {
+int launch_generic(const Launch& a, cudaStream_t st) { return launch_generic_mode(a, 0, nullptr, 0, st); }
+
+int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, cudaStream_t st) {
     if (a.B * a.H == 0) return 0;
-    const int dvs = choose_dvs(a);
+    // map mode: 2 dk virtual columns in slices of 32 (four CTAs per chunk); read mode: slices of 16
+    const int dvs = mode == 0 ? choose_dvs(a) : (mode == 1 ? 32 : 16);
     GParams gp;
     gp.q = a.q;
     gp.k = a.k;
@@ -728,8 +760,12 @@ int launch_generic(const Launch& a, cudaStream_t st) {
     gp.W = windowed(a.variant) ? a.W : 1;
     gp.eps = a.eps;
     gp.eps_gamma = a.eps_gamma;
+    gp.mode = mode;
+    gp.ws = ws;
+    gp.N = N;
     const size_t smem = generic_smem_bytes(a, dvs);
-    dim3 grid((unsigned)((a.dv / dvs) * a.B * a.H));
+    const long long slices = (mode == 1 ? a.dk + a.dv : a.dv) / dvs;
+    dim3 grid((unsigned)(slices * a.B * a.H * (mode == 0 ? 1 : N)));
     cudaError_t e = a.bf16 ? launch_typed<__nv_bfloat16>(a, gp, grid, smem, st)
                            : launch_typed<float>(a, gp, grid, smem, st);
     return e == cudaSuccess ? 0 : 4;

@@ -38,6 +38,9 @@ struct Launch {
 
 // CUDA-core chunk kernel: every variant, both dtypes, all supported sizes.
 int launch_generic(const Launch& a, cudaStream_t stream);
+// The same kernel one chunk per CTA: mode 1 writes every chunk's affine state map into `ws`, mode 2
+// forms every chunk's outputs from the chunk-start states in `ws` (the scan path's layout).
+int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, cudaStream_t stream);
 size_t generic_smem_bytes(const Launch& a, int dvs);
 
 // tcgen05 / TMA chunk kernel (Falcon-1 and 1A, bf16, dk = dv = 64, chunk 64).
@@ -56,6 +59,12 @@ int split_consume_timeout_flag(int* flag);
 // Single-token step (T = 1; Falcon-1, 1A, 2 and 2A; dk = dv = 64): one CTA per (batch, head) state.
 bool decode_supported(const Launch& a);
 int launch_decode(const Launch& a, cudaStream_t stream);
+
+// Scan path (Falcon-1, 1A, 3, 3A with dk = dv = 64, few sequences, no split path): chunk maps,
+// an associative scan over them, then the chunks' outputs, through a caller workspace.
+bool scan_supported(const Launch& a);
+size_t scan_workspace_bytes(const Launch& a);
+int launch_scan(const Launch& a, cudaStream_t stream);
 
 // Backward pass (Falcon-1 and 1A, dk = dv = 64, chunk 64): prep, chain and gradient kernels working
 // through a caller workspace of bwd_workspace_bytes(a) bytes at a.ws. `a` carries the forward inputs.
