@@ -738,8 +738,9 @@ int launch_generic(const Launch& a, cudaStream_t st) { return launch_generic_mod
 
 int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, cudaStream_t st) {
     if (a.B * a.H == 0) return 0;
-    // map mode: 2 dk virtual columns in slices of 32 (four CTAs per chunk); read mode: slices of 16
-    const int dvs = mode == 0 ? choose_dvs(a) : (mode == 1 ? 32 : 16);
+    // map and read modes: whole 64-column slices (the chunks supply the parallelism, so the key-only
+    // work of a chunk is done by two CTAs (map) or one (read) instead of once per narrow slice)
+    const int dvs = mode == 0 ? choose_dvs(a) : (int)a.dv;
     GParams gp;
     gp.q = a.q;
     gp.k = a.k;
