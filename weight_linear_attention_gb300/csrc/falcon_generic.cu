@@ -642,15 +642,25 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             }
             stf(out + (t0 + i) * DV + c0 + c, o);
         }
+        if (windowed(VAR) && mode != 2) {
+            // the write sum_l w_l sum_b x_{l-b} r_{l,b}^T gathered by extended row e = l - b + W - 1 first
+            // (into H, whose last use was the solve): S' = e^{L_C} S + X_ext^T Rf
+            for (int idx = tid; idx < (n + W - 1) * DVS; idx += kThreads) {
+                const int e = idx / DVS, c = idx % DVS;
+                float acc = 0.f;
+                for (int b = 0; b < W; ++b) {
+                    const int l = e + b - (W - 1);
+                    if (l >= 0 && l < n) acc = fmaf(s.w[l], s.R[c * RS + l * W + b], acc);
+                }
+                s.H[idx] = acc;
+            }
+            __syncthreads();
+        }
         for (int idx = tid; idx < (mode == 2 ? 0 : DK * DVS); idx += kThreads) {
             const int r = idx / DVS, c = idx % DVS;
             float acc = 0.f;
             if (windowed(VAR)) {
-                for (int l = 0; l < n; ++l) {
-                    float inner = 0.f;
-                    for (int b = 0; b < W; ++b) inner = fmaf(s.X[(l - b + W - 1) * XS + r], s.R[c * RS + l * W + b], inner);
-                    acc = fmaf(s.w[l], inner, acc);
-                }
+                for (int e = 0; e < n + W - 1; ++e) acc = fmaf(s.X[e * XS + r], s.H[e * DVS + c], acc);
                 s.S[idx] = fmaf(expf(s.L[C - 1]), s.S[idx], acc);
             } else if (per_column(VAR)) {
                 const float gC = expf(s.L[c * CS + C - 1]);
