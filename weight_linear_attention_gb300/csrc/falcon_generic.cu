@@ -186,6 +186,50 @@ __device__ void gram_mma(const float* X, const float* Q, float* G, float* Sc, in
     }
 }
 
+// out[r][c] = sum_{k < K} A(r, k) B(k, c) for r < nr, c < nc on the CUDA cores, A(r, k) = a[r * lda + k],
+// B(k, c) = b[k * ldb + c] (BT: b[c * ldb + k]). Each thread takes two rows (r, r + ceil(nr / 2)) by four
+// columns, so a k step costs six shared loads (two for a 16-byte-aligned row of B) for eight
+// multiply-adds. Columns past nc read a valid neighbour and are not stored.
+template <bool BT>
+__device__ void mm_tiled(float* out, int ldo, const float* a, int lda, const float* b, int ldb, int nr, int nc, int K,
+                         int tid) {
+    const int half = (nr + 1) / 2, ncg = (nc + 3) / 4;
+    const bool vec = !BT && (ldb % 4 == 0) && (nc % 4 == 0);
+    for (int tile = tid; tile < half * ncg; tile += kThreads) {
+        const int r0 = tile / ncg, cb = 4 * (tile % ncg), r1 = r0 + half;
+        const bool v1 = r1 < nr;
+        const float* a0 = a + r0 * lda;
+        const float* a1 = a + (v1 ? r1 : r0) * lda;
+        int cj[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) cj[jj] = min(cb + jj, nc - 1);
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int k = 0; k < K; ++k) {
+            const float x0 = a0[k], x1 = a1[k];
+            float y[4];
+            if (vec) {
+                const float4 v = *reinterpret_cast<const float4*>(b + k * ldb + cb);
+                y[0] = v.x, y[1] = v.y, y[2] = v.z, y[3] = v.w;
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) y[jj] = BT ? b[cj[jj] * ldb + k] : b[k * ldb + cj[jj]];
+            }
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                acc0[jj] = fmaf(x0, y[jj], acc0[jj]);
+                acc1[jj] = fmaf(x1, y[jj], acc1[jj]);
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+            if (cb + jj < nc) {
+                out[r0 * ldo + cb + jj] = acc0[jj];
+                if (v1) out[r1 * ldo + cb + jj] = acc1[jj];
+            }
+    }
+}
+
 // Shared-memory carve-up (floats). NE = C + W - 1 extended pair rows.
 struct Smem {
     float *X, *Q, *Y, *S, *G, *Sc, *H, *QS, *R, *A, *P;
@@ -340,31 +384,11 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         if (kMmaGram && C <= 64 && C % 16 == 0 && DK % 16 == 0) {
             gram_mma(s.X, s.Q, s.G, s.Sc, C, DK, XS, NE, tid);
         } else {
-            for (int idx = tid; idx < NE * NE; idx += kThreads) {
-                const int a = idx / NE, b = idx % NE;
-                float acc = 0.f;
-                for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.X[a * XS + cc], s.X[b * XS + cc], acc);
-                s.G[idx] = acc;
-            }
-            for (int idx = tid; idx < C * NE; idx += kThreads) {
-                const int i = idx / NE, b = idx % NE;
-                float acc = 0.f;
-                for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.Q[i * XS + cc], s.X[b * XS + cc], acc);
-                s.Sc[idx] = acc;
-            }
+            mm_tiled<true>(s.G, NE, s.X, XS, s.X, XS, NE, NE, DK, tid);
+            mm_tiled<true>(s.Sc, NE, s.Q, XS, s.X, XS, C, NE, DK, tid);
         }
-        for (int idx = tid; idx < NE * DVS; idx += kThreads) {
-            const int e = idx / DVS, c = idx % DVS;
-            float acc = 0.f;
-            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.X[e * XS + cc], s.S[cc * DVS + c], acc);
-            s.H[idx] = acc;
-        }
-        for (int idx = tid; idx < C * DVS; idx += kThreads) {
-            const int i = idx / DVS, c = idx % DVS;
-            float acc = 0.f;
-            for (int cc = 0; cc < DK; ++cc) acc = fmaf(s.Q[i * XS + cc], s.S[cc * DVS + c], acc);
-            s.QS[idx] = acc;
-        }
+        mm_tiled<false>(s.H, DVS, s.X, XS, s.S, DVS, NE, DVS, DK, tid);
+        mm_tiled<false>(s.QS, DVS, s.Q, XS, s.S, DVS, C, DVS, DK, tid);
         __syncthreads();
         // ---- (3) per-token scalars and the chunk-local log-decay prefix
         if (per_column(VAR)) {
@@ -610,10 +634,10 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         __syncthreads();
         // ---- (6) outputs (read after write) and (7) carried state
         Tin* out = static_cast<Tin*>(p.out) + bh * T * DV;
-        for (int idx = tid; idx < (mode == 1 ? 0 : n * DVS); idx += kThreads) {
-            const int i = idx / DVS, c = idx % DVS;
-            float o;
-            if (per_column(VAR)) {
+        if (per_column(VAR)) {
+            for (int idx = tid; idx < (mode == 1 ? 0 : n * DVS); idx += kThreads) {
+                const int i = idx / DVS, c = idx % DVS;
+                float o;
                 const float li = s.L[c * CS + i];
                 if (s.w[c * CS + C] != 0.f) {  // fast: o = e^{L_i} (QS + sum_j Sc_ij R~_j)
                     o = s.QS[idx];
@@ -625,22 +649,45 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                         o = fmaf(s.eta[c * CS + j] * expf(li - s.L[c * CS + j]) * s.Sc[i * NE + j], s.R[c * RS + j],
                                  o);
                 }
-            } else if (windowed(VAR)) {
-                o = expf(s.L[i]) * s.QS[idx];
-                for (int l = 0; l <= i; ++l) {
-                    const float f = s.P[i * C + l];
-                    float acc = 0.f;
-                    for (int b = 0; b < W; ++b) acc = fmaf(s.Sc[i * NE + (l - b + W - 1)], s.R[c * RS + l * W + b], acc);
-                    o = fmaf(f, acc, o);
-                }
-            } else if (VAR == kF1A) {
-                o = expf(s.L[i]) * s.QS[idx];
-                for (int j = 0; j <= i; ++j) o = fmaf(s.P[i * C + j], s.Y[j * DVS + c], o);
-            } else {
-                o = expf(s.L[i]) * s.QS[idx];
-                for (int j = 0; j <= i; ++j) o = fmaf(s.P[i * C + j], s.R[c * RS + j], o);
+                stf(out + (t0 + i) * DV + c0 + c, o);
             }
-            stf(out + (t0 + i) * DV + c0 + c, o);
+        } else if (mode != 1) {
+            // o_i = e^{L_i} QS_i + sum_{l <= i} P_il v_l with v_l = sum_b Sc_{i, l-b+W-1} r_{l,b} (windowed), r_l
+            // (Falcon-1) or y_l (Falcon-1A); P is zero above the diagonal. Each thread: rows i and
+            // i + C/2 by four columns.
+            const int half = C / 2, ncg = DVS / 4;
+            for (int tile = tid; tile < half * ncg; tile += kThreads) {
+                const int i0 = tile / ncg, cb = 4 * (tile % ncg), i1 = i0 + half;
+                float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int l = 0; l <= i1; ++l) {
+                    const float f0 = s.P[i0 * C + l], f1 = s.P[i1 * C + l];
+                    if (windowed(VAR)) {
+                        for (int b = 0; b < W; ++b) {
+                            const int e = l - b + W - 1;
+                            const float t0v = f0 * s.Sc[i0 * NE + e], t1v = f1 * s.Sc[i1 * NE + e];
+#pragma unroll
+                            for (int jj = 0; jj < 4; ++jj) {
+                                const float r = s.R[(cb + jj) * RS + l * W + b];
+                                acc0[jj] = fmaf(t0v, r, acc0[jj]);
+                                acc1[jj] = fmaf(t1v, r, acc1[jj]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const float r = VAR == kF1A ? s.Y[l * DVS + cb + jj] : s.R[(cb + jj) * RS + l];
+                            acc0[jj] = fmaf(f0, r, acc0[jj]);
+                            acc1[jj] = fmaf(f1, r, acc1[jj]);
+                        }
+                    }
+                }
+                const float e0 = expf(s.L[i0]), e1 = expf(s.L[i1]);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    if (i0 < n) stf(out + (t0 + i0) * DV + c0 + cb + jj, fmaf(e0, s.QS[i0 * DVS + cb + jj], acc0[jj]));
+                    if (i1 < n) stf(out + (t0 + i1) * DV + c0 + cb + jj, fmaf(e1, s.QS[i1 * DVS + cb + jj], acc1[jj]));
+                }
+            }
         }
         if (windowed(VAR) && mode != 2) {
             // the write sum_l w_l sum_b x_{l-b} r_{l,b}^T gathered by extended row e = l - b + W - 1 first
