@@ -61,6 +61,7 @@ struct GParams {
     // 2 (read): one CTA per (sequence, slice, chunk) forms the chunk's outputs from its start state
     //   S_n in the chunk's workspace block.
     int mode;
+    const float* mu;  // Falcon-3, modes 1 and 2: every token's window normaliser, precomputed ([B*H][T])
     float* ws;   // per chunk (sequence-major) [M (dk x dk) | U (dk x dv) | S_n (dk x dv)], fp32
     long long N; // chunks per sequence (modes 1, 2)
 };
@@ -451,6 +452,8 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                             if (VAR == kF3A) {  // the window's mean key energy (trace of the averaged Gram)
                                 for (int x = 0; x < nb; ++x) mu += s.G[slots[x] * NE + slots[x]];
                                 mu /= (float)nb;
+                            } else if (p.mu) {
+                                mu = p.mu[bh * T + t0 + i];
                             } else switch (W) {  // the matrix in registers: one instance per window size
                                 case 1: mu = s.G[slots[0] * NE + slots[0]]; break;
                                 case 2: mu = window_lambda_max<2>(s.G, NE, slots, nb); break;
@@ -756,6 +759,58 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
     }
 }
 
+// Falcon-3: every token's window normaliser mu = lambda_max((1/B) sum_j x_j x_j^T) over the window's
+// realised pairs, one thread per token (the same Gram entries, summed in the same order, and the same
+// Jacobi as the chunk kernel's own), so that chunk kernels running one chunk per CTA read it instead
+// of each recomputing it.
+template <typename Tin, int W>
+__global__ void __launch_bounds__(128) falcon_window_mu_kernel(const Tin* k, const Tin* tail, float* mu, long long BH,
+                                                             long long T, long long pos, int DK,
+                                                             long long tail_stride) {
+    const long long idx = blockIdx.x * 128LL + threadIdx.x;
+    if (idx >= BH * T) return;
+    const long long bh = idx / T, t = idx % T, tau = pos + t + 1;
+    // the window's realised pairs are a = 0 .. nb - 1 (pair tau - a, key k_{tau - a - 1})
+    const int nb = (int)min((long long)W, max(0LL, tau - 1));
+    const Tin* rows[W];
+#pragma unroll
+    for (int a = 0; a < W; ++a) {
+        const long long u = t - a - 1;  // local index of the key
+        rows[a] = a >= nb ? nullptr : (u >= 0 ? k + (bh * T + u) * DK : tail + bh * tail_stride + (u + W) * DK);
+    }
+    float g[W][W];
+#pragma unroll
+    for (int x = 0; x < W; ++x)
+#pragma unroll
+        for (int y = 0; y < W; ++y) g[x][y] = 0.f;
+    for (int c8 = 0; c8 < DK; c8 += 8) {
+        float v[W][8];
+#pragma unroll
+        for (int x = 0; x < W; ++x) {
+            if (x < nb) ld8(rows[x] + c8, v[x]);
+            else
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[x][e] = 0.f;
+        }
+#pragma unroll
+        for (int x = 0; x < W; ++x)
+#pragma unroll
+            for (int y = 0; y <= x; ++y)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) g[x][y] = fmaf(v[x][e], v[y][e], g[x][y]);
+    }
+    float m = 0.f;
+    if (nb > 0) {
+        const float inv = 1.f / (float)nb;
+#pragma unroll
+        for (int x = 0; x < W; ++x)
+#pragma unroll
+            for (int y = 0; y < W; ++y) g[x][y] = (x >= y ? g[x][y] : g[y][x]) * inv;
+        m = W == 1 ? g[0][0] * (float)nb : lambda_max_fixed<W>(g);
+    }
+    mu[idx] = m;
+}
+
 template <typename Tin>
 cudaError_t launch_typed(const Launch& a, const GParams& gp, dim3 grid, size_t smem, cudaStream_t st) {
     void (*fn)(GParams) = nullptr;
@@ -791,9 +846,38 @@ size_t generic_smem_bytes(const Launch& a, int dvs) {
     return smem_floats(a.variant, (int)a.dk, dvs, a.chunk, W, nullptr, nullptr) * sizeof(float);
 }
 
-int launch_generic(const Launch& a, cudaStream_t st) { return launch_generic_mode(a, 0, nullptr, 0, st); }
+int launch_generic(const Launch& a, cudaStream_t st) { return launch_generic_mode(a, 0, nullptr, 0, nullptr, st); }
 
-int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, cudaStream_t st) {
+int launch_window_mu(const Launch& a, float* mu, cudaStream_t st) {
+    const long long n = a.B * a.H * a.T;
+    if (n == 0) return 0;
+    const long long ts = (long long)a.W * a.dk + (long long)(a.W - 1) * a.dv;
+    const unsigned grid = (unsigned)((n + 127) / 128);
+    auto go = [&](auto tin, auto wc) {
+        using Tin = decltype(tin);
+        constexpr int W = decltype(wc)::value;
+        falcon_window_mu_kernel<Tin, W><<<grid, 128, 0, st>>>(static_cast<const Tin*>(a.k),
+                                                              static_cast<const Tin*>(a.tail), mu, a.B * a.H, a.T,
+                                                              a.pos, (int)a.dk, ts);
+    };
+    auto by_w = [&](auto tin) {
+        switch (a.W) {
+            case 1: go(tin, std::integral_constant<int, 1>{}); break;
+            case 2: go(tin, std::integral_constant<int, 2>{}); break;
+            case 3: go(tin, std::integral_constant<int, 3>{}); break;
+            case 4: go(tin, std::integral_constant<int, 4>{}); break;
+            case 5: go(tin, std::integral_constant<int, 5>{}); break;
+            case 6: go(tin, std::integral_constant<int, 6>{}); break;
+            case 7: go(tin, std::integral_constant<int, 7>{}); break;
+            default: go(tin, std::integral_constant<int, 8>{}); break;
+        }
+    };
+    if (a.bf16) by_w(__nv_bfloat16{});
+    else by_w(float{});
+    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const float* mu, cudaStream_t st) {
     if (a.B * a.H == 0) return 0;
     // map and read modes: whole 64-column slices (the chunks supply the parallelism, so the key-only
     // work of a chunk is done by two CTAs (map) or one (read) instead of once per narrow slice)
@@ -819,6 +903,7 @@ int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, cudaS
     gp.eps = a.eps;
     gp.eps_gamma = a.eps_gamma;
     gp.mode = mode;
+    gp.mu = mu;
     gp.ws = ws;
     gp.N = N;
     const size_t smem = generic_smem_bytes(a, dvs);

@@ -13,7 +13,9 @@
 //                 storing each chunk's start state S_n (and S_final from the last group);
 //      a sequence of N chunks takes 2 G + N / G dependent steps instead of N;
 //   3. read  (CUDA-core chunk kernel, read mode): every chunk's outputs at once from its S_n.
-// Workspace: per chunk (sequence-major) and then per group, blocks [M | U | S] of 64 x 64 fp32.
+// Workspace: per chunk (sequence-major) and then per group, blocks [M | U | S] of 64 x 64 fp32; for
+// Falcon-3 then every token's window normaliser (computed once by a one-thread-per-token kernel and read
+// by the map and read passes).
 
 #include <cuda_runtime.h>
 
@@ -166,13 +168,19 @@ bool scan_supported(const Launch& a) {
 
 size_t scan_workspace_bytes(const Launch& a) {
     const long long N = (a.T + a.chunk - 1) / a.chunk, NG = (N + kGroup - 1) / kGroup;
-    return (size_t)(a.B * a.H) * (size_t)(N + NG) * (size_t)kBlk * sizeof(float);
+    const size_t mu = a.variant == kF3 ? (size_t)(a.B * a.H * a.T) * sizeof(float) : 0;  // Falcon-3 normalisers
+    return (size_t)(a.B * a.H) * (size_t)(N + NG) * (size_t)kBlk * sizeof(float) + mu;
 }
 
 int launch_scan(const Launch& a, cudaStream_t st) {
     const long long BH = a.B * a.H, N = (a.T + a.chunk - 1) / a.chunk, NG = (N + kGroup - 1) / kGroup;
     float* ws = static_cast<float*>(a.ws);
-    int e = launch_generic_mode(a, 1, ws, N, st);
+    float* mu = nullptr;
+    if (a.variant == kF3) {
+        mu = ws + BH * (N + NG) * kBlk;
+        if (launch_window_mu(a, mu, st)) return 4;
+    }
+    int e = launch_generic_mode(a, 1, ws, N, mu, st);
     if (e) return e;
     static_assert(kSmem <= 227 * 1024, "scan kernel shared memory");
     if (cudaFuncSetAttribute(falcon_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) !=
@@ -188,7 +196,7 @@ int launch_scan(const Launch& a, cudaStream_t st) {
     p.mode = 2;
     falcon_scan_kernel<<<(unsigned)(BH * NG * 4), kThreads, kSmem, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return 4;
-    return launch_generic_mode(a, 2, ws, N, st);
+    return launch_generic_mode(a, 2, ws, N, mu, st);
 }
 
 }  // namespace falcon
