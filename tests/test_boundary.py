@@ -237,12 +237,12 @@ def test_bwd_argument_checks(lib):
 
 def test_scan_path_choice(lib):
     # Falcon-3 (W = 4) at 2 x 12 heads, 8192 tokens, chunk 32: few sequences, many chunks -> scan path,
-    # workspace B*H*(N + ceil(N/16)) blocks of three 64 x 64 fp32 matrices, plus (Falcon-3) one fp32
+    # workspace B*H*(N + ceil(N/16)) blocks of five 64 x 64 fp32 matrices, plus (Falcon-3) one fp32
     # window normaliser per token
     d = F.make_dims(2, 12, 8192, 64, 64, window=4)
     assert F.falcon_kernel_for(F.FALCON_3, d, 32) == 5
-    assert F.falcon_workspace_bytes(F.FALCON_3, d, 32) == 24 * (256 + 16) * 3 * 64 * 64 * 4 + 24 * 8192 * 4
-    assert F.falcon_workspace_bytes(F.FALCON_3A, d, 32) == 24 * (256 + 16) * 3 * 64 * 64 * 4
+    assert F.falcon_workspace_bytes(F.FALCON_3, d, 32) == 24 * (256 + 16) * 5 * 64 * 64 * 4 + 24 * 8192 * 4
+    assert F.falcon_workspace_bytes(F.FALCON_3A, d, 32) == 24 * (256 + 16) * 5 * 64 * 64 * 4
     assert F.falcon_kernel_for(F.FALCON_3A, d, 32) == 5
     assert F.falcon_kernel_for(F.FALCON_2, F.make_dims(2, 12, 8192, 64, 64), 64) == 1  # per-column maps: no
     assert F.falcon_kernel_for(F.FALCON_3, F.make_dims(8, 12, 8192, 64, 64, window=4), 32) == 1  # many sequences

@@ -55,15 +55,14 @@ struct GParams {
     int dk, dv, dvs, C, W;
     float eps, eps_gamma;
     // 0: one CTA walks all chunks of its (sequence, column slice);
-    // 1 (map): one CTA per (sequence, slice, chunk) computes the chunk's affine state map S -> M S + U:
-    //   slices of the 2 dk virtual columns, the first dk those of M (state e_c, no target), the rest
-    //   those of U (zero state, the targets); the result goes to the chunk's workspace block;
-    // 2 (read): one CTA per (sequence, slice, chunk) forms the chunk's outputs from its start state
-    //   S_n in the chunk's workspace block.
+    // 1 (map, dk = dv = 64): one CTA per (sequence, slice, chunk) computes the chunk's affine maps
+    //   S -> M S + U (its end state) and S -> Ao S + Bo (its outputs) over the 2 dk virtual columns:
+    //   the first dk those of M and Ao (state e_c, no target), the rest those of U and Bo (zero state,
+    //   the targets); the results go to the chunk's workspace block.
     int mode;
-    const float* mu;  // Falcon-3, modes 1 and 2: every token's window normaliser, precomputed ([B*H][T])
-    float* ws;   // per chunk (sequence-major) [M (dk x dk) | U (dk x dv) | S_n (dk x dv)], fp32
-    long long N; // chunks per sequence (modes 1, 2)
+    const float* mu;  // Falcon-3, mode 1: every token's window normaliser, precomputed ([B*H][T])
+    float* ws;   // per chunk (sequence-major) [M | U | S | Ao | Bo], each 64 x 64 fp32 (Ao, Bo: C rows used)
+    long long N; // chunks per sequence (mode 1)
 };
 
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
@@ -276,7 +275,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
     const int RS = C * W + 1, CS = C + 1;
     const int NE = C + W - 1;
     const long long T = p.T, pos = p.pos;
-    const int mode = p.mode;
+    const int mode = p.mode;  // 0 or 1
     const int slices = (mode == 1 ? DK + DV : DV) / DVS;
     const long long nck = mode == 0 ? 0 : (long long)(blockIdx.x % p.N);
     const long long rest = mode == 0 ? (long long)blockIdx.x : (long long)(blockIdx.x / p.N);
@@ -285,7 +284,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
     const int c0 = slice * DVS;          // first (virtual) column of this CTA
     const bool mpart = mode == 1 && c0 < DK;  // map mode, columns of M: unit state, no targets
     const int vc0 = mode == 1 ? (mpart ? 0 : c0 - DK) : c0;  // first value column of the targets
-    const long long blk = (long long)DK * DK + 2LL * DK * DV;
+    const long long blk = 5LL * DK * DK;
     float* wsb = mode != 0 ? p.ws + (bh * p.N + nck) * blk : nullptr;  // this chunk's workspace block
 
     Smem s;
@@ -316,7 +315,6 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         const int r = idx / DVS, c = idx % DVS;
         float x;
         if (mode == 1) x = mpart && r == c0 + c ? 1.f : 0.f;
-        else if (mode == 2) x = wsb[(long long)DK * DK + (long long)DK * DV + r * DV + c0 + c];
         else x = p.S0 ? p.S0[(bh * DK + r) * DV + c0 + c] : 0.f;
         s.S[idx] = x;
     }
@@ -654,15 +652,16 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                 }
                 stf(out + (t0 + i) * DV + c0 + c, o);
             }
-        } else if (mode != 1) {
+        } else {
             // o_i = e^{L_i} QS_i + sum_{l <= i} P_il v_l with v_l = sum_b Sc_{i, l-b+W-1} r_{l,b} (windowed), r_l
-            // (Falcon-1) or y_l (Falcon-1A); P is zero above the diagonal. Each thread: rows i and
-            // i + C/2 by four columns.
+            // (Falcon-1) or y_l (Falcon-1A); P is zero above the diagonal, and l < n. Each thread: rows i
+            // and i + C/2 by four columns.
             const int half = C / 2, ncg = DVS / 4;
             for (int tile = tid; tile < half * ncg; tile += kThreads) {
                 const int i0 = tile / ncg, cb = 4 * (tile % ncg), i1 = i0 + half;
                 float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int l = 0; l <= i1; ++l) {
+                const int lmax = min(i1, n - 1);  // rows of R past n were never written
+                for (int l = 0; l <= lmax; ++l) {
                     const float f0 = s.P[i0 * C + l], f1 = s.P[i1 * C + l];
                     if (windowed(VAR)) {
                         for (int b = 0; b < W; ++b) {
@@ -687,12 +686,20 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                 const float e0 = expf(s.L[i0]), e1 = expf(s.L[i1]);
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
-                    if (i0 < n) stf(out + (t0 + i0) * DV + c0 + cb + jj, fmaf(e0, s.QS[i0 * DVS + cb + jj], acc0[jj]));
-                    if (i1 < n) stf(out + (t0 + i1) * DV + c0 + cb + jj, fmaf(e1, s.QS[i1 * DVS + cb + jj], acc1[jj]));
+                    const float o0 = fmaf(e0, s.QS[i0 * DVS + cb + jj], acc0[jj]);
+                    const float o1 = fmaf(e1, s.QS[i1 * DVS + cb + jj], acc1[jj]);
+                    if (mode == 1) {  // the output map: Ao (unit state columns) or Bo (targets)
+                        float* ob = wsb + (mpart ? 3LL * DK * DK + c0 : 4LL * DK * DK + vc0) + cb + jj;
+                        ob[i0 * DK] = o0;
+                        ob[i1 * DK] = o1;
+                    } else {
+                        if (i0 < n) stf(out + (t0 + i0) * DV + c0 + cb + jj, o0);
+                        if (i1 < n) stf(out + (t0 + i1) * DV + c0 + cb + jj, o1);
+                    }
                 }
             }
         }
-        if (windowed(VAR) && mode != 2) {
+        if (windowed(VAR)) {
             // the write sum_l w_l sum_b x_{l-b} r_{l,b}^T gathered by extended row e = l - b + W - 1 first
             // (into H, whose last use was the solve): S' = e^{L_C} S + X_ext^T Rf
             for (int idx = tid; idx < (n + W - 1) * DVS; idx += kThreads) {
@@ -706,7 +713,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             }
             __syncthreads();
         }
-        for (int idx = tid; idx < (mode == 2 ? 0 : DK * DVS); idx += kThreads) {
+        for (int idx = tid; idx < DK * DVS; idx += kThreads) {
             const int r = idx / DVS, c = idx % DVS;
             float acc = 0.f;
             if (windowed(VAR)) {
@@ -731,31 +738,31 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         }
     }
     __syncthreads();
-    if (mode == 1) {  // the chunk's map: M columns or U columns
+    if (mode == 1) {  // the chunk's state map: M columns or U columns
         float* dst = mpart ? wsb + c0 : wsb + (long long)DK * DK + vc0;
         const int ld = mpart ? DK : DV;
         for (int idx = tid; idx < DK * DVS; idx += kThreads) {
             const int r = idx / DVS, c = idx % DVS;
             dst[r * ld + c] = s.S[idx];
         }
-        return;
-    }
-    if (p.S_final && mode == 0)
+    } else if (p.S_final) {
         for (int idx = tid; idx < DK * DVS; idx += kThreads) {
             const int r = idx / DVS, c = idx % DVS;
             p.S_final[(bh * DK + r) * DV + c0 + c] = s.S[idx];
         }
-    if (p.tail_out && (mode == 0 || nck == p.N - 1)) {
+    }
+    if (p.tail_out && (mode == 0 || nck == p.N - 1)) {  // map mode: the last chunk's CTAs
         Tin* to = static_cast<Tin*>(p.tail_out) + bh * tail_stride;
         if (slice == 0)
             for (int idx = tid; idx < W * DK; idx += kThreads) {
                 const int sl = idx / DK, cc = idx % DK;
                 stf(to + idx, load_key(T - W + sl, cc));
             }
-        for (int idx = tid; idx < (W - 1) * DVS; idx += kThreads) {
-            const int sl = idx / DVS, cc = idx % DVS;
-            stf(to + (long long)W * DK + sl * DV + c0 + cc, load_val(T - W + 1 + sl, c0 + cc));
-        }
+        if (!mpart)
+            for (int idx = tid; idx < (W - 1) * DVS; idx += kThreads) {
+                const int sl = idx / DVS, cc = idx % DVS;
+                stf(to + (long long)W * DK + sl * DV + vc0 + cc, load_val(T - W + 1 + sl, vc0 + cc));
+            }
     }
 }
 
@@ -879,8 +886,8 @@ int launch_window_mu(const Launch& a, float* mu, cudaStream_t st) {
 
 int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const float* mu, cudaStream_t st) {
     if (a.B * a.H == 0) return 0;
-    // map and read modes: whole 64-column slices (the chunks supply the parallelism, so the key-only
-    // work of a chunk is done by two CTAs (map) or one (read) instead of once per narrow slice)
+    // map mode: whole 64-column slices (the chunks supply the parallelism, so the key-only work of a
+    // chunk is done by two CTAs instead of once per narrow slice)
     const int dvs = mode == 0 ? choose_dvs(a) : (int)a.dv;
     GParams gp;
     gp.q = a.q;

@@ -38,8 +38,8 @@ struct Launch {
 
 // CUDA-core chunk kernel: every variant, both dtypes, all supported sizes.
 int launch_generic(const Launch& a, cudaStream_t stream);
-// The same kernel one chunk per CTA: mode 1 writes every chunk's affine state map into `ws`, mode 2
-// forms every chunk's outputs from the chunk-start states in `ws` (the scan path's layout).
+// The same kernel one chunk per CTA (mode 1): every chunk's affine state and output maps into `ws`
+// (the scan path's layout); mode 0 is launch_generic.
 int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const float* mu, cudaStream_t stream);
 // Falcon-3: every token's window normaliser into mu[B*H][T] (read by modes 1 and 2 instead of recomputed).
 int launch_window_mu(const Launch& a, float* mu, cudaStream_t stream);

@@ -3,20 +3,21 @@
 // paperlayer summary §H.1: chunk maps compose associatively, so the sequential phase can be a scan;
 // §H.2; §E.2 for the three-phase structure).
 //
-// For Falcon-1, 1A, 3 and 3A every chunk acts on the carried state as S -> M_n S + U_n with M_n, U_n
-// fixed by the chunk's inputs alone (the transition is shared by all value columns). With dk = dv = 64:
-//   1. map   (CUDA-core chunk kernel, map mode): every chunk's M_n and U_n at once;
+// For Falcon-1, 1A, 3 and 3A every chunk acts on the carried state as S -> M_n S + U_n, and its
+// outputs are O_n = Ao_n S_n + Bo_n, with M_n, U_n, Ao_n, Bo_n fixed by the chunk's inputs alone (the
+// transition is shared by all value columns). With dk = dv = 64:
+//   1. map   (CUDA-core chunk kernel, map mode): every chunk's four maps at once;
 //   2. scan  (this file), groups of G = 16 chunks:
 //        compose  every group's map (M_g, U_g) = (M_last ... M_first, ...) at once,
 //        groups   per sequence, S_{g+1} = M_g S_g + U_g over the groups,
-//        apply    every group at once, S_{n+1} = M_n S_n + U_n from the group's start state,
-//                 storing each chunk's start state S_n (and S_final from the last group);
-//      a sequence of N chunks takes 2 G + N / G dependent steps instead of N;
-//   3. read  (CUDA-core chunk kernel, read mode): every chunk's outputs at once from its S_n.
-// Workspace: per chunk (sequence-major) and then per group, blocks [M | U | S] of 64 x 64 fp32; for
-// Falcon-3 then every token's window normaliser (computed once by a one-thread-per-token kernel and read
-// by the map and read passes).
+//        apply    every group at once, from the group's start state: O_n = Ao_n S_n + Bo_n, then
+//                 S_{n+1} = M_n S_n + U_n (and S_final from the last group);
+//      a sequence of N chunks takes 2 G + N / G dependent steps instead of N.
+// Workspace: per chunk (sequence-major) and then per group, blocks [M | U | S | Ao | Bo] of 64 x 64 fp32
+// (Ao, Bo: C rows used; S: a group's start state); for Falcon-3 then every token's window normaliser
+// (computed once by a one-thread-per-token kernel and read by the map pass).
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "falcon_internal.h"
@@ -31,14 +32,19 @@ constexpr int kStages = 3;
 constexpr int kThreads = 256;
 constexpr int kGroup = 16;    // chunks per group
 constexpr long long kMat = kD * kD;
-constexpr long long kBlk = 3 * kMat;  // [M | U | S]
-constexpr size_t kSmem = (size_t)kStages * (kD * kLdc + kD * kCols) * sizeof(float) + 2 * kCols * kLdc * sizeof(float);
+constexpr long long kBlk = 5 * kMat;  // [M | U | S | Ao | Bo]
+// shared floats of one ring stage: M, the offset columns, and (apply) the output maps' rows
+__host__ __device__ constexpr int stage_floats(int C) { return kD * kLdc + kD * kCols + C * (kLdc + kCols); }
+constexpr size_t smem_bytes(int C) { return ((size_t)kStages * stage_floats(C) + 2 * kCols * kLdc) * sizeof(float); }
 
 struct ScanParams {
     float* ws;
     const float* S0;
     float* S_final;
-    long long BH, N, NG;
+    void* out;      // apply: [B*H][T][64] in the input dtype
+    long long BH, N, NG, T;
+    int C;          // chunk length (apply: rows of Ao, Bo)
+    int bf16;
     int mode;  // 0 compose, 1 groups, 2 apply
 };
 
@@ -55,9 +61,14 @@ __device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_g
 // columns arrive through a three-stage ring of 16-byte asynchronous copies issued two steps ahead.
 __global__ void __launch_bounds__(kThreads) falcon_scan_kernel(const ScanParams p) {
     extern __shared__ __align__(16) float sm[];
-    float* Ms = sm;                              // [kStages][kD * kLdc]
-    float* Os = Ms + kStages * kD * kLdc;        // [kStages][kD][kCols]
-    float (*Sv)[kCols][kLdc] = reinterpret_cast<float (*)[kCols][kLdc]>(Os + kStages * kD * kCols);  // [2]
+    const int Cr = p.mode == 2 ? p.C : 0;       // output rows fetched per step
+    const int SF = stage_floats(Cr);
+    // stage st: M [kD][kLdc] | offsets [kD][kCols] | Ao [Cr][kLdc] | Bo [Cr][kCols]
+    auto Mst = [&](int st) { return sm + st * SF; };
+    auto Ost = [&](int st) { return sm + st * SF + kD * kLdc; };
+    auto Ast = [&](int st) { return sm + st * SF + kD * kLdc + kD * kCols; };
+    auto Bst = [&](int st) { return sm + st * SF + kD * kLdc + kD * kCols + Cr * kLdc; };
+    float (*Sv)[kCols][kLdc] = reinterpret_cast<float (*)[kCols][kLdc]>(sm + kStages * SF);  // [2]
     const int c = threadIdx.x & 15, r0 = 4 * (threadIdx.x >> 4);
     const long long bid = blockIdx.x;
     long long bh, gi = 0;
@@ -95,11 +106,19 @@ __global__ void __launch_bounds__(kThreads) falcon_scan_kernel(const ScanParams 
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int e = 4 * (threadIdx.x + u * kThreads), row = e >> 6, col = e & 63;
-                cp_async16(Ms + st * kD * kLdc + row * kLdc + col, b + e);
+                cp_async16(Mst(st) + row * kLdc + col, b + e);
             }
             if (has_off) {
                 const int row = threadIdx.x >> 2, q = 4 * (threadIdx.x & 3);
-                cp_async16(Os + (st * kD + row) * kCols + q, b + kMat + row * kD + cg + q);
+                cp_async16(Ost(st) + row * kCols + q, b + kMat + row * kD + cg + q);
+            }
+            for (int e = threadIdx.x; e < Cr * 16; e += kThreads) {  // Ao rows, 16-byte pieces
+                const int row = e >> 4, col = 4 * (e & 15);
+                cp_async16(Ast(st) + row * kLdc + col, b + 3 * kMat + row * kD + col);
+            }
+            for (int e = threadIdx.x; e < Cr * 4; e += kThreads) {   // Bo rows, this CTA's columns
+                const int row = e >> 2, q = 4 * (e & 3);
+                cp_async16(Bst(st) + row * kCols + q, b + 4 * kMat + row * kD + cg + q);
             }
         }
         cp_async_commit();
@@ -125,14 +144,31 @@ __global__ void __launch_bounds__(kThreads) falcon_scan_kernel(const ScanParams 
         issue(j + 2);
         cp_async_wait2();
         __syncthreads();
-        if (p.mode != 0) {  // the state entering this step: a chunk's (apply) or a group's (groups) start state
+        const float* Sc = Sv[b][c];
+        if (p.mode == 1) {  // the state entering this group
             float* so = blk(j) + 2 * kMat + cg + c;
 #pragma unroll
             for (int z = 0; z < 4; ++z) so[(r0 + z) * kD] = Sv[b][c][r0 + z];
+        } else if (p.mode == 2) {  // the chunk's outputs from the state entering it: O = Ao S + Bo
+            const long long t0 = (first + j) * p.C;
+            const int rows = (int)min((long long)p.C, p.T - t0);
+            const float* Ak = Ast(st);
+            const float* Bk = Bst(st);
+            for (int i = threadIdx.x >> 4; i < rows; i += kThreads / 16) {
+                float o = Bk[i * kCols + c];
+#pragma unroll 4
+                for (int k = 0; k < kD; k += 4) {
+                    const float4 sv = *reinterpret_cast<const float4*>(Sc + k);
+                    const float4 av = *reinterpret_cast<const float4*>(Ak + i * kLdc + k);
+                    o = fmaf(av.x, sv.x, fmaf(av.y, sv.y, fmaf(av.z, sv.z, fmaf(av.w, sv.w, o))));
+                }
+                const long long at = (bh * p.T + t0 + i) * kD + cg + c;
+                if (p.bf16) static_cast<__nv_bfloat16*>(p.out)[at] = __float2bfloat16_rn(o);
+                else static_cast<float*>(p.out)[at] = o;
+            }
         }
-        const float* Mk = Ms + st * kD * kLdc;
-        const float* off = Os + st * kD * kCols + c;
-        const float* Sc = Sv[b][c];
+        const float* Mk = Mst(st);
+        const float* off = Ost(st) + c;
         float acc[4];
 #pragma unroll
         for (int z = 0; z < 4; ++z) acc[z] = has_off ? off[(r0 + z) * kCols] : 0.f;
@@ -182,21 +218,20 @@ int launch_scan(const Launch& a, cudaStream_t st) {
     }
     int e = launch_generic_mode(a, 1, ws, N, mu, st);
     if (e) return e;
-    static_assert(kSmem <= 227 * 1024, "scan kernel shared memory");
-    if (cudaFuncSetAttribute(falcon_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) !=
+    static_assert(smem_bytes(64) <= 227 * 1024, "scan kernel shared memory");
+    if (cudaFuncSetAttribute(falcon_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(a.chunk)) !=
         cudaSuccess)
         return 4;
-    ScanParams p{ws, a.S0, a.S_final, BH, N, NG, 0};
+    ScanParams p{ws, a.S0, a.S_final, a.out, BH, N, NG, a.T, a.chunk, a.bf16, 0};
     if (NG > 1) {
         p.mode = 0;
-        falcon_scan_kernel<<<(unsigned)(BH * NG * 8), kThreads, kSmem, st>>>(p);
+        falcon_scan_kernel<<<(unsigned)(BH * NG * 8), kThreads, smem_bytes(0), st>>>(p);
         p.mode = 1;
-        falcon_scan_kernel<<<(unsigned)(BH * 4), kThreads, kSmem, st>>>(p);
+        falcon_scan_kernel<<<(unsigned)(BH * 4), kThreads, smem_bytes(0), st>>>(p);
     }
     p.mode = 2;
-    falcon_scan_kernel<<<(unsigned)(BH * NG * 4), kThreads, kSmem, st>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return 4;
-    return launch_generic_mode(a, 2, ws, N, mu, st);
+    falcon_scan_kernel<<<(unsigned)(BH * NG * 4), kThreads, smem_bytes(a.chunk), st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
 }  // namespace falcon
