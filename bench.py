@@ -47,6 +47,16 @@ def _algorithmic_bytes(w, es):
     return total
 
 
+def _launches_per_call(w, kernel_id):
+    """Kernels one falcon_fwd call launches on the path `kernel_id` takes."""
+    if kernel_id == 3:
+        return 3
+    if kernel_id == 5:  # [window normalisers,] chunk maps, [compose, groups,] apply
+        n = -(-w.seqlen // w.chunk)
+        return (1 if w.variant == "falcon3" else 0) + 1 + (2 if n > 16 else 0) + 1
+    return 1
+
+
 def _kernel_digest():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "weight_linear_attention_gb300", "csrc")
@@ -382,14 +392,16 @@ def run_ours(args, w):
                    "pos0": w.pos0,
                    "kernel": {1: "cuda-core chunk kernel", 2: "single-pass tcgen05/TMA chunk kernel",
                               4: "single-token kernel",
-                              3: "split path: tcgen05/TMA prep, chain and output kernels"}.get(kernel_id, "?")},
+                              3: "split path: tcgen05/TMA prep, chain and output kernels",
+                              5: "scan path: chunk maps on the cuda-core kernel, associative scan over them "
+                                 "with the outputs fused"}.get(kernel_id, "?")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "scope": "one falcon_fwd call (all kernels it launches); per-kernel shares in profiles/",
                      "traffic": _traffic(w.name, kernel_id), "peak_source": src,
                      "algorithmic_bytes_per_step": step_bytes, "ms_per_call": mean_launch},
         "e2e": None if args.no_e2e else {"value": world * tokens_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * w.segments * (3 if kernel_id == 3 else 1),
+        "gpu_launches": args.steps * w.segments * _launches_per_call(w, kernel_id),
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -31,6 +31,10 @@
  * (the solve and the chunk transition S -> M S + U it implies) is computed for
  * all chunks at once, then a short scan carries the state, then every chunk's
  * reads are formed at once.
+ * Falcon-1, 1A, 3 and 3A with dk = dv = 64 over few (batch, head) sequences and no split path have
+ * a scan path that also uses the workspace: every chunk's affine maps of the state and of the
+ * outputs, then an associative scan over the chunk maps in groups of 16 chunks ([PL] §H.1, §H.2),
+ * whose last step also forms every chunk's outputs.
  *
  * Memory: every pointer argument is DEVICE memory owned by the caller; the
  * library keeps no pointer after a call returns and allocates no device memory.
@@ -123,8 +127,10 @@ int falcon_fwd(int variant, const void* q, const void* k, const void* v, const f
                size_t workspace_bytes, void* stream);
 
 /* Workspace bytes that enable the split path of falcon_fwd for these arguments
- * (B*H*ceil(T/64) * (66 KiB + 8 bytes) for Falcon-1/1A, bf16, dk = dv = 64, chunk 64, T > 1; 0 when
- * no path uses a workspace or the arguments are invalid). Host only. */
+ * (B*H*ceil(T/64) * (66 KiB + 8 bytes) for Falcon-1/1A, bf16, dk = dv = 64, chunk 64, T > 1), or
+ * the scan path (B*H*(N + ceil(N/16)) * 80 KiB with N = ceil(T/chunk), plus 4*B*H*T bytes for
+ * Falcon-3; Falcon-1, 1A, 3, 3A with dk = dv = 64, B*H < 76, N >= 4, no split path); 0 when no path
+ * uses a workspace or the arguments are invalid. Host only. */
 size_t falcon_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk);
 
 /*
@@ -162,8 +168,9 @@ int falcon_device_status(void* stream);
 /* Which kernels falcon_fwd launches for these arguments when it is given
  * falcon_workspace_bytes() of workspace (0 = none/invalid, 1 = CUDA-core chunk
  * kernel, 2 = single-pass tcgen05/TMA chunk kernel, 3 = split path: prep, chain
- * and output kernels, 4 = single-token kernel for T = 1, workspace or not).
- * Without a workspace, 3 becomes 2. Host only, no launch. */
+ * and output kernels, 4 = single-token kernel for T = 1, workspace or not, 5 = scan path:
+ * chunk maps on the CUDA-core kernel, then the scan over them).
+ * Without a workspace, 3 becomes 2 and 5 becomes 1. Host only, no launch. */
 int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk);
 
 /*
