@@ -573,6 +573,79 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                     }
                 }
             }
+        } else if (VAR == kF3 && DVS == 64) {
+            // All 64 columns at once, by blocks of TB = 16 / W tokens (NB = TB W unknowns): per block kb,
+            //   r_kb = (I + A_kb,kb)^-1 (rhs_kb - sum_{j < kb} A_kb,j r_j),
+            // the 16 x 16 diagonal-block inverses formed once (shared by every column), the earlier
+            // blocks' terms as a product over all columns. Invalid unknowns (the sentinel pair's slots,
+            // tokens past n) have zero rows and zero right-hand sides, so r = 0 there.
+            const int TB = 16 / W, NB = TB * W, nblk = (C + TB - 1) / TB;
+            auto valid_u = [&](int i, int a) { return i < n && pos + t0 + i + 1 - a >= 2; };
+            // (1) right-hand sides into R
+            for (int idx = tid; idx < C * W * DVS; idx += kThreads) {
+                const int m = idx / DVS, c = idx % DVS, i = m / W, a = m % W, pa = i - a + W - 1;
+                s.R[c * RS + m] = valid_u(i, a) ? s.Y[pa * DVS + c] - expf(s.Lx[i]) * s.H[pa * DVS + c] : 0.f;
+            }
+            __syncthreads();
+            // (2) diagonal-block inverses, one warp per block, a lane per column (Y is free now)
+            float* Dinv = s.Y;  // [nblk][16][16]
+            {
+                const int kb = tid >> 5, col = tid & 31;
+                if (kb < nblk) {
+                    float* D = Dinv + kb * 256;
+                    for (int rr = 0; rr < NB; ++rr) {
+                        const int i = kb * TB + rr / W, a = rr % W, pa = i - a + W - 1;
+                        const bool vr = valid_u(i, a);
+                        float x = (rr == col) ? 1.f : 0.f;
+                        if (vr && col < NB)
+                            for (int r2 = 0; r2 < rr; ++r2) {
+                                const int l = kb * TB + r2 / W, b = r2 % W;
+                                if (l < i) x = fmaf(-s.A[i * C + l] * s.G[pa * NE + (l - b + W - 1)], D[r2 * 16 + col], x);
+                            }
+                        if (col < 16) D[rr * 16 + col] = x;
+                        __syncwarp();
+                    }
+                }
+            }
+            __syncthreads();
+            // (3) block by block
+            float* Tmp = s.H;  // [16][DVS]: right-hand side minus the earlier blocks' terms
+            const int rr = tid >> 4, cb = 4 * (tid & 15);
+            for (int kb = 0; kb < nblk; ++kb) {
+                if (rr < NB) {
+                    const int m = kb * NB + rr, i = kb * TB + rr / W, a = rr % W, pa = i - a + W - 1;
+                    float t4[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (valid_u(i, a)) {
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        for (int l = 0; l < kb * TB; ++l) {
+                            const float al = s.A[i * C + l];
+                            const float* gr = s.G + pa * NE + l + W - 1;  // G[pa][l - b + W - 1] = gr[-b]
+                            for (int b = 0; b < W; ++b) {
+                                const float cf = al * gr[-b];
+#pragma unroll
+                                for (int jj = 0; jj < 4; ++jj) acc[jj] = fmaf(cf, s.R[(cb + jj) * RS + l * W + b], acc[jj]);
+                            }
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) t4[jj] = s.R[(cb + jj) * RS + m] - acc[jj];
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) Tmp[rr * DVS + cb + jj] = t4[jj];
+                }
+                __syncthreads();
+                if (rr < NB) {
+                    const float* D = Dinv + kb * 256 + rr * 16;
+                    float o[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int r2 = 0; r2 < NB; ++r2) {
+                        const float d = D[r2];
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) o[jj] = fmaf(d, Tmp[r2 * DVS + cb + jj], o[jj]);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) s.R[(cb + jj) * RS + kb * NB + rr] = o[jj];
+                }
+                __syncthreads();
+            }
         } else if (VAR == kF3) {
             // Unknowns r_{i,a} (token i, window slot a) depend only on earlier tokens, so a token's W
             // slots are finished together: a half-warp per column takes 16 / W tokens at a time, one
