@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                     for (int jj = 0; jj < 4; ++jj) Tmp[rr * DVS + cb + jj] = t4[jj];
                 }
                 __syncthreads();
-                if (rr < NB) {
+                if (rr < NB && kb * TB + rr / W < C) {  // the last block may reach past the chunk's C tokens
                     const float* D = Dinv + kb * 256 + rr * 16;
                     float o[4] = {0.f, 0.f, 0.f, 0.f};
                     for (int r2 = 0; r2 < NB; ++r2) {
