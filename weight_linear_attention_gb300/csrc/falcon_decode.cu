@@ -1,8 +1,7 @@
 // Single-token step (T = 1) for Falcon-1, 1A, 2 and 2A with dk = dv = 64: the recurrent form of the
 // update ("Fast Weight Attention for Continual Learning", paperlayer summary §3, Appendix p.34;
-// agihunt explainer "Method"), one (batch, head) state per CTA, each of its four warps on 16 value
-// columns. The state is read once and written once, so the step is bound by those 2 x 16 KB per head
-// of HBM traffic.
+// agihunt explainer "Method"), one (batch, head) state per CTA. The state is read once and written
+// once, so the step is bound by those 2 x 16 KB per head of HBM traffic.
 //
 // For the token at global position tau = pos + 1, with x = k_pos (the pending key of the tail; the
 // x_1 = 0 sentinel when pos = 0), y = v, q:
@@ -23,8 +22,9 @@ namespace falcon {
 namespace {
 
 constexpr int kD = 64;
-constexpr int kThreads = 128;  // four warps; warp w owns value columns 16 w .. 16 w + 15 of one head
-constexpr int kHalf = 32;      // rows per lane: lane l holds column 16 w + (l & 15), rows 32 (l >> 4) .. + 31
+constexpr int kThreads = 128;  // thread t: columns 4 (t % 16) .. + 3, rows kRows (t / 16) .. + kRows - 1
+constexpr int kRows = kD * 16 / kThreads;
+constexpr int kGroups = kThreads / 16;  // row groups
 
 struct DParams {
     const void* q;
@@ -45,79 +45,104 @@ __device__ __forceinline__ float ldf(const float* p) { return *p; }
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void stf(float* p, float x) { *p = x; }
 __device__ __forceinline__ void stf(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+__device__ __forceinline__ float get(const float4& v, int j) { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; }
+__device__ __forceinline__ void set(float4& v, int j, float x) {
+    if (j == 0) v.x = x;
+    else if (j == 1) v.y = x;
+    else if (j == 2) v.z = x;
+    else v.w = x;
+}
 
-// Each warp works alone on its 16 columns (the columns of the update are independent once |x|^2 is
-// known), so the step needs no CTA barrier: a lane's 32 state values are loaded at once, its partial
-// sums over its 32 rows meet the other half's by one shuffle.
 template <typename Tin, int VAR>
 __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p) {
-    __shared__ float xs[kThreads / 32][kD], qs[kThreads / 32][kD];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __shared__ float xs[kD], qs[kD], ys[kD], rs[kD], eta_s[kD], gam_s[kD];
+    __shared__ float part[kGroups][kD];
+    __shared__ float nx_s;
+    const int tid = threadIdx.x, lane = tid & 31;
     const long long bh = blockIdx.x;
-    const int c = 16 * warp + (lane & 15), r0 = kHalf * (lane >> 4);
+    const int cq = tid & 15, rg = tid >> 4, c0 = 4 * cq, r0 = kRows * rg;
+    const Tin* q = static_cast<const Tin*>(p.q) + bh * kD;
+    const Tin* k = static_cast<const Tin*>(p.k) + bh * kD;
+    const Tin* v = static_cast<const Tin*>(p.v) + bh * kD;
     const bool first = p.pos == 0;  // tau = 1: x = 0, eta = alpha = 0
 
-    // the lane's state values, all loads issued at once
-    float sv[kHalf];
-    const float* s0 = p.S0 ? p.S0 + (bh * kD + r0) * kD + c : nullptr;
+    // ---- the state tile of this thread (rows r0 .. r0 + kRows - 1, columns c0 .. c0 + 3)
+    float4 sv[kRows];
 #pragma unroll
-    for (int j = 0; j < kHalf; ++j) sv[j] = s0 ? s0[j * kD] : 0.f;
-    // x (the pending key), q, this column's target
-    const Tin* q = static_cast<const Tin*>(p.q) + bh * kD;
-    float x0 = 0.f, x1 = 0.f;
-    if (!first) {
-        const Tin* tl = static_cast<const Tin*>(p.tail) + bh * kD;
-        x0 = ldf(tl + 2 * lane);
-        x1 = ldf(tl + 2 * lane + 1);
+    for (int m = 0; m < kRows; ++m)
+        sv[m] = p.S0 ? *reinterpret_cast<const float4*>(p.S0 + (bh * kD + r0 + m) * kD + c0)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid < kD) {
+        xs[tid] = first ? 0.f : ldf(static_cast<const Tin*>(p.tail) + bh * kD + tid);
+        qs[tid] = ldf(q + tid);
+        ys[tid] = ldf(v + tid);
+        if (p.tail_out) stf(static_cast<Tin*>(p.tail_out) + bh * kD + tid, ldf(k + tid));
     }
-    xs[warp][2 * lane] = x0;
-    xs[warp][2 * lane + 1] = x1;
-    qs[warp][2 * lane] = ldf(q + 2 * lane);
-    qs[warp][2 * lane + 1] = ldf(q + 2 * lane + 1);
-    const float y = ldf(static_cast<const Tin*>(p.v) + bh * kD + c);
-    if (p.tail_out && warp == 0) {
-        const Tin* kk = static_cast<const Tin*>(p.k) + bh * kD;
-        stf(static_cast<Tin*>(p.tail_out) + bh * kD + 2 * lane, ldf(kk + 2 * lane));
-        stf(static_cast<Tin*>(p.tail_out) + bh * kD + 2 * lane + 1, ldf(kk + 2 * lane + 1));
-    }
-    float nx = x0 * x0 + x1 * x1;
+    __syncthreads();
+    if (tid < 32) {  // |x|^2
+        float a = xs[lane] * xs[lane] + xs[lane + 32] * xs[lane + 32];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) nx += __shfl_xor_sync(0xffffffffu, nx, o);
-    __syncwarp();
-    float eta = 0.f, alpha = 0.f;
-    if (!first) {
-        const float lm = p.lam[bh];
-        const float b = per_column(VAR) ? p.beta[bh * kD + c] : p.beta[bh];
-        const float den = nx + lm + p.eps;
-        eta = den == 0.f ? 0.f : b / den;
-        alpha = fminf(eta * lm, 1.f - p.eps_gamma);
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) nx_s = a;
     }
-    const float* xw = xs[warp] + r0;
-    const float* qw = qs[warp] + r0;
-    // r = y - S^T x (Falcon-1, 2) or y (Falcon-1A, 2A)
-    float r = y;
+    __syncthreads();
+    if (tid < kD) {  // eta, gamma per value column (one value for Falcon-1 and 1A)
+        float eta = 0.f, alpha = 0.f;
+        if (!first) {
+            const float lm = p.lam[bh];
+            const float b = per_column(VAR) ? p.beta[bh * kD + tid] : p.beta[bh];
+            const float den = nx_s + lm + p.eps;
+            eta = den == 0.f ? 0.f : b / den;
+            alpha = fminf(eta * lm, 1.f - p.eps_gamma);
+        }
+        eta_s[tid] = eta;
+        gam_s[tid] = 1.f - alpha;
+    }
+
+    // ---- residual r = y - S^T x (Falcon-1, 2) or r = y (Falcon-1A)
     if (!inner_product(VAR)) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float a = 0.f;
+#pragma unroll
+            for (int m = 0; m < kRows; ++m) a = fmaf(get(sv[m], j), xs[r0 + m], a);
+            part[rg][c0 + j] = a;
+        }
+    }
+    __syncthreads();
+    if (tid < kD) {
+        float a = 0.f;
+        if (!inner_product(VAR))
+#pragma unroll
+            for (int g = 0; g < kGroups; ++g) a += part[g][tid];
+        rs[tid] = ys[tid] - a;
+    }
+    __syncthreads();
+
+    // ---- S' = gamma S + eta x r^T, and this thread's part of o = S'^T q
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int c = c0 + j;
+        const float g = gam_s[c], er = eta_s[c] * rs[c];
         float a = 0.f;
 #pragma unroll
-        for (int j = 0; j < kHalf; ++j) a = fmaf(sv[j], xw[j], a);
-        a += __shfl_xor_sync(0xffffffffu, a, 16);
-        r = y - a;
+        for (int m = 0; m < kRows; ++m) {
+            const float s = fmaf(g, get(sv[m], j), er * xs[r0 + m]);
+            set(sv[m], j, s);
+            a = fmaf(s, qs[r0 + m], a);
+        }
+        part[rg][c] = a;
     }
-    // S' = gamma S + eta x r^T, and o = S'^T q
-    const float g = 1.f - alpha, er = eta * r;
-    float o = 0.f;
+    if (p.S_final)
 #pragma unroll
-    for (int j = 0; j < kHalf; ++j) {
-        sv[j] = fmaf(g, sv[j], er * xw[j]);
-        o = fmaf(sv[j], qw[j], o);
-    }
-    o += __shfl_xor_sync(0xffffffffu, o, 16);
-    if (p.S_final) {
-        float* sf = p.S_final + (bh * kD + r0) * kD + c;
+        for (int m = 0; m < kRows; ++m) *reinterpret_cast<float4*>(p.S_final + (bh * kD + r0 + m) * kD + c0) = sv[m];
+    __syncthreads();
+    if (tid < kD) {
+        float a = 0.f;
 #pragma unroll
-        for (int j = 0; j < kHalf; ++j) sf[j * kD] = sv[j];
+        for (int g = 0; g < kGroups; ++g) a += part[g][tid];
+        stf(static_cast<Tin*>(p.out) + bh * kD + tid, a);
     }
-    if (lane < 16) stf(static_cast<Tin*>(p.out) + bh * kD + c, o);
 }
 
 template <typename Tin>
