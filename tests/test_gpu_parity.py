@@ -84,17 +84,20 @@ def test_workload_full_size(wname):
     _parity(w, inp, name=wname)
 
 
-def test_falcon3_two_segments_full_size():
-    """Falcon-3, window 4, 2 x 12 x 16384 run as two 8192-token segments carrying S and the tail."""
-    w = I.WORKLOADS["f3w4_b2h12t16384_bf16"]
+@pytest.mark.parametrize("wname", ["f3w4_b2h12t16384_bf16", "f3aw4_b2h12t16384_bf16"])
+def test_falcon3_two_segments_full_size(wname):
+    """Falcon-3 / 3A, window 4, 2 x 12 x 16384 run as two 8192-token segments carrying S and the tail
+    (the launch configuration the benchmark times)."""
+    w = I.WORKLOADS[wname]
+    V = w.variant_id
     inp = I.make_inputs(w, seed=0)
     Ts = w.seqlen
     a, b = slice_inputs(inp, 0, Ts), slice_inputs(inp, Ts, 2 * Ts)
-    o1, S1, t1 = run_gpu(F3, a, window=4, chunk=w.chunk)
+    o1, S1, t1 = run_gpu(V, a, window=4, chunk=w.chunk)
     S1d = S1.clone()
-    o2, S2, t2 = run_gpu(F3, b, window=4, chunk=w.chunk, pos=Ts, S0=S1d, tail=t1)
-    ro1, rS1, rt1 = run_oracle(F3, a, window=4)
-    ro2, rS2, rt2 = run_oracle(F3, b, window=4, pos=Ts, S0=rS1, tail=rt1)
+    o2, S2, t2 = run_gpu(V, b, window=4, chunk=w.chunk, pos=Ts, S0=S1d, tail=t1)
+    ro1, rS1, rt1 = run_oracle(V, a, window=4)
+    ro2, rS2, rt2 = run_oracle(V, b, window=4, pos=Ts, S0=rS1, tail=rt1)
     _check("seg1 out", o1, ro1, torch.bfloat16)
     _check("seg1 S", S1, rS1, torch.bfloat16)
     _check("seg2 out", o2, ro2, torch.bfloat16)
@@ -104,7 +107,7 @@ def test_falcon3_two_segments_full_size():
     np.testing.assert_array_equal(tk.double().numpy(), rt2[0])
     np.testing.assert_array_equal(tv.double().numpy(), rt2[1])
     # and the oracle's own split equals its unsplit run (exact continuation)
-    ro_full, rS_full, _ = run_oracle(F3, inp, window=4)
+    ro_full, rS_full, _ = run_oracle(V, inp, window=4)
     np.testing.assert_allclose(np.concatenate([ro1, ro2], axis=2), ro_full, rtol=0, atol=1e-9)
     np.testing.assert_allclose(rS2, rS_full, rtol=0, atol=1e-9)
 
