@@ -1,9 +1,10 @@
-"""Falcon forward throughput on GB300: tokens/s through the C ABI, roofline, oracle baseline.
+"""Falcon throughput on GB300: tokens/s through the C ABI, roofline, oracle baseline.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 One step = one full forward pass of the workload (all its segments) over one
-batch of synthetic input already resident in HBM. Rank 0 prints one JSON line.
+batch of synthetic input already resident in HBM; for the backward workloads
+(`*_bwd_*`) one falcon_bwd call (every gradient). Rank 0 prints one JSON line.
 Under torchrun each rank runs the whole workload on its own GPU (sequences are
 independent, so there is no data-path collective: weak scaling); the value is
 all ranks' tokens over the slowest rank's time.

@@ -25,7 +25,9 @@
 //   falcon_bwd_chain  per sequence (four CTAs of 16 value columns each): S_{n+1} = M_n S_n + U_n
 //                     forward, then dS_n = M_n^T dS_{n+1} + V_n backward, storing S_n and dS_{n+1};
 //   falcon_bwd_grad   every chunk at once: all input gradients from S_n and dS_{n+1}.
-// Every 64 x 64 x 64 product runs on the CUDA cores in fp32 from shared memory.
+// The 64 x 64 x 64 products of prep and grad run on the tensor cores as warp-level tf32 MMAs with
+// every fp32 operand split into a tf32 head and remainder (fp32-accurate); the scans, the scalars
+// and the triangular inverse run on the CUDA cores in fp32.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>

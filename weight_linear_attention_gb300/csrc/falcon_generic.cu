@@ -1,6 +1,7 @@
 // CUDA-core chunk-parallel Falcon forward kernel (all variants, fp32 or bf16 I/O).
 //
-// One CTA owns one (batch, head) sequence and a slice of `dvs` value columns.
+// One CTA owns one (batch, head) sequence and a slice of `dvs` value columns (mode 0), or one chunk
+// of one sequence (map mode, used by the scan path: the chunk's affine state and output maps).
 // Falcon-1/1A/2/3 value columns evolve independently once the chunk operators
 // are known (paperlayer summary §G.1: the shared transition acts on every
 // column; Falcon-2 and Falcon-3 only change the per-token scalars or add window
