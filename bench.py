@@ -58,23 +58,25 @@ def _launches_per_call(w, kernel_id):
     return 1
 
 
-def _kernel_digest():
+def _kernel_digest(files=None):
+    """Digest of the kernel sources (all of csrc/, or the listed files of it)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "weight_linear_attention_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(files or os.listdir(d)):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def _traffic(workload, kernel_id):
-    """DRAM bytes per launch from a committed ncu summary, only if taken on the current kernel sources."""
+    """DRAM bytes per launch from a committed ncu summary, only if taken on the current sources of the
+    kernels that path launches (the entry lists them)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     e = d.get(f"{workload}:{kernel_id}")
-    if not e or e.get("kernel_digest") != _kernel_digest():
+    if not e or e.get("kernel_digest") != _kernel_digest(e.get("sources")):
         return None
     return e.get("dram_bytes_per_step")
 
