@@ -611,8 +611,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             __syncthreads();
             // (3) block by block
             float* Tmp = s.H;  // [16][DVS]: right-hand side minus the earlier blocks' terms
-            // thread: row rr of the block, columns c0 + 16 jj (column-major R: lanes on distinct banks)
-            const int rr = tid >> 4, c0s = tid & 15;
+            const int rr = tid >> 4, cb = 4 * (tid & 15);
             for (int kb = 0; kb < nblk; ++kb) {
                 if (rr < NB) {
                     const int m = kb * NB + rr, i = kb * TB + rr / W, a = rr % W, pa = i - a + W - 1;
@@ -625,15 +624,14 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                             for (int b = 0; b < W; ++b) {
                                 const float cf = al * gr[-b];
 #pragma unroll
-                                for (int jj = 0; jj < 4; ++jj)
-                                    acc[jj] = fmaf(cf, s.R[(c0s + 16 * jj) * RS + l * W + b], acc[jj]);
+                                for (int jj = 0; jj < 4; ++jj) acc[jj] = fmaf(cf, s.R[(cb + jj) * RS + l * W + b], acc[jj]);
                             }
                         }
 #pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) t4[jj] = s.R[(c0s + 16 * jj) * RS + m] - acc[jj];
+                        for (int jj = 0; jj < 4; ++jj) t4[jj] = s.R[(cb + jj) * RS + m] - acc[jj];
                     }
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) Tmp[rr * DVS + c0s + 16 * jj] = t4[jj];
+                    for (int jj = 0; jj < 4; ++jj) Tmp[rr * DVS + cb + jj] = t4[jj];
                 }
                 __syncthreads();
                 if (rr < NB && kb * TB + rr / W < C) {  // the last block may reach past the chunk's C tokens
@@ -642,10 +640,10 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                     for (int r2 = 0; r2 < NB; ++r2) {
                         const float d = D[r2];
 #pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) o[jj] = fmaf(d, Tmp[r2 * DVS + c0s + 16 * jj], o[jj]);
+                        for (int jj = 0; jj < 4; ++jj) o[jj] = fmaf(d, Tmp[r2 * DVS + cb + jj], o[jj]);
                     }
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) s.R[(c0s + 16 * jj) * RS + kb * NB + rr] = o[jj];
+                    for (int jj = 0; jj < 4; ++jj) s.R[(cb + jj) * RS + kb * NB + rr] = o[jj];
                 }
                 __syncthreads();
             }
@@ -731,11 +729,10 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         } else {
             // o_i = e^{L_i} QS_i + sum_{l <= i} P_il v_l with v_l = sum_b Sc_{i, l-b+W-1} r_{l,b} (windowed), r_l
             // (Falcon-1) or y_l (Falcon-1A); P is zero above the diagonal, and l < n. Each thread: rows i
-            // and i + C/2 by four columns, DVS / 4 apart.
+            // and i + C/2 by four columns.
             const int half = C / 2, ncg = DVS / 4;
             for (int tile = tid; tile < half * ncg; tile += kThreads) {
-                // columns cs + ncg jj: lanes of a warp read R (column-major, odd stride) on distinct banks
-                const int i0 = tile / ncg, cs = tile % ncg, i1 = i0 + half;
+                const int i0 = tile / ncg, cb = 4 * (tile % ncg), i1 = i0 + half;
                 float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
                 const int lmax = min(i1, n - 1);  // rows of R past n were never written
                 for (int l = 0; l <= lmax; ++l) {
@@ -746,7 +743,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                             const float t0v = f0 * s.Sc[i0 * NE + e], t1v = f1 * s.Sc[i1 * NE + e];
 #pragma unroll
                             for (int jj = 0; jj < 4; ++jj) {
-                                const float r = s.R[(cs + ncg * jj) * RS + l * W + b];
+                                const float r = s.R[(cb + jj) * RS + l * W + b];
                                 acc0[jj] = fmaf(t0v, r, acc0[jj]);
                                 acc1[jj] = fmaf(t1v, r, acc1[jj]);
                             }
@@ -754,8 +751,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                     } else {
 #pragma unroll
                         for (int jj = 0; jj < 4; ++jj) {
-                            const int c = cs + ncg * jj;
-                            const float r = VAR == kF1A ? s.Y[l * DVS + c] : s.R[c * RS + l];
+                            const float r = VAR == kF1A ? s.Y[l * DVS + cb + jj] : s.R[(cb + jj) * RS + l];
                             acc0[jj] = fmaf(f0, r, acc0[jj]);
                             acc1[jj] = fmaf(f1, r, acc1[jj]);
                         }
@@ -764,16 +760,15 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
                 const float e0 = expf(s.L[i0]), e1 = expf(s.L[i1]);
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
-                    const int c = cs + ncg * jj;
-                    const float o0 = fmaf(e0, s.QS[i0 * DVS + c], acc0[jj]);
-                    const float o1 = fmaf(e1, s.QS[i1 * DVS + c], acc1[jj]);
+                    const float o0 = fmaf(e0, s.QS[i0 * DVS + cb + jj], acc0[jj]);
+                    const float o1 = fmaf(e1, s.QS[i1 * DVS + cb + jj], acc1[jj]);
                     if (mode == 1) {  // the output map: Ao (unit state columns) or Bo (targets)
-                        float* ob = wsb + (mpart ? 3LL * DK * DK + c0 : 4LL * DK * DK + vc0) + c;
+                        float* ob = wsb + (mpart ? 3LL * DK * DK + c0 : 4LL * DK * DK + vc0) + cb + jj;
                         ob[i0 * DK] = o0;
                         ob[i1 * DK] = o1;
                     } else {
-                        if (i0 < n) stf(out + (t0 + i0) * DV + c0 + c, o0);
-                        if (i1 < n) stf(out + (t0 + i1) * DV + c0 + c, o1);
+                        if (i0 < n) stf(out + (t0 + i0) * DV + c0 + cb + jj, o0);
+                        if (i1 < n) stf(out + (t0 + i1) * DV + c0 + cb + jj, o1);
                     }
                 }
             }
