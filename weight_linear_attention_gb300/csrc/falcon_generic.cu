@@ -265,7 +265,7 @@ __host__ __device__ inline size_t smem_floats(int variant, int dk, int dvs, int 
 }
 
 template <typename Tin, int VAR>
-__global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams p) {
+__global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GParams p) {
     extern __shared__ __align__(16) float smem_raw[];
     const int tid = threadIdx.x;
     const int DK = p.dk, DV = p.dv, DVS = p.dvs, C = p.C;
@@ -283,6 +283,8 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
     const long long bh = rest / slices;
     const int slice = (int)(rest % slices);
     const int c0 = slice * DVS;          // first (virtual) column of this CTA
+    // DVS, DK and C are powers of two: index splits by shift and mask
+    const int dvs_sh = 31 - __clz(DVS), c_sh = 31 - __clz(C);
     const bool mpart = mode == 1 && c0 < DK;  // map mode, columns of M: unit state, no targets
     const int vc0 = mode == 1 ? (mpart ? 0 : c0 - DK) : c0;  // first value column of the targets
     const long long blk = 5LL * DK * DK;
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
 
     // Initial state slice.
     for (int idx = tid; idx < DK * DVS; idx += kThreads) {
-        const int r = idx / DVS, c = idx % DVS;
+        const int r = (idx >> dvs_sh), c = (idx & (DVS - 1));
         float x;
         if (mode == 1) x = mpart && r == c0 + c ? 1.f : 0.f;
         else x = p.S0 ? p.S0[(bh * DK + r) * DV + c0 + c] : 0.f;
@@ -373,7 +375,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         }
         if (per_column(VAR)) {  // the chunk's gains (per column, into eta) and ridge coefficients (into kap)
             for (int idx = tid; idx < C * DVS; idx += kThreads) {
-                const int i = idx / DVS, c = idx % DVS;
+                const int i = (idx >> dvs_sh), c = (idx & (DVS - 1));
                 s.eta[c * CS + i] = i < n ? beta[(t0 + i) * DV + c0 + c] : 0.f;
             }
             for (int i = tid; i < C; i += kThreads) s.kap[i] = i < n ? lam[t0 + i] : 0.f;
@@ -394,7 +396,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         if (per_column(VAR)) {
             // every (token, column) in parallel, then one warp scan of log(gamma) per column
             for (int idx = tid; idx < C * DVS; idx += kThreads) {
-                const int i = idx / DVS, c = idx % DVS;
+                const int i = (idx >> dvs_sh), c = (idx & (DVS - 1));
                 float eta = 0.f, alpha = 0.f;
                 const long long tau = pos + t0 + i + 1;
                 if (i < n && tau >= 2) {
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         if (!per_column(VAR)) {
             const float LC = s.L[C - 1];
             for (int idx = tid; idx < C * C; idx += kThreads) {
-                const int i = idx / C, j = idx % C;
+                const int i = idx >> c_sh, j = idx & (C - 1);
                 float a = 0.f, pp = 0.f;
                 if (j < i) a = s.kap[j] * expf(s.Lx[i] - s.L[j]);
                 if (j <= i) pp = s.kap[j] * expf(s.L[i] - s.L[j]);
@@ -520,7 +522,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             // ("fast"); otherwise w holds eta_j e^{L_C - L_j} and the factors are formed one by one.
             // Slot C of each column records which.
             for (int idx = tid; idx < C * DVS; idx += kThreads) {
-                const int j = idx / DVS, c = idx % DVS;
+                const int j = (idx >> dvs_sh), c = (idx & (DVS - 1));
                 const float LC = s.L[c * CS + C - 1];
                 const bool fast = LC >= -kFastL;
                 s.w[c * CS + j] = s.eta[c * CS + j] * expf((fast ? 0.f : LC) - s.L[c * CS + j]);
@@ -584,7 +586,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             auto valid_u = [&](int i, int a) { return i < n && pos + t0 + i + 1 - a >= 2; };
             // (1) right-hand sides into R
             for (int idx = tid; idx < C * W * DVS; idx += kThreads) {
-                const int m = idx / DVS, c = idx % DVS, i = m / W, a = m % W, pa = i - a + W - 1;
+                const int m = (idx >> dvs_sh), c = (idx & (DVS - 1)), i = m / W, a = m % W, pa = i - a + W - 1;
                 s.R[c * RS + m] = valid_u(i, a) ? s.Y[pa * DVS + c] - expf(s.Lx[i]) * s.H[pa * DVS + c] : 0.f;
             }
             __syncthreads();
@@ -695,13 +697,13 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             }
         } else if (VAR == kF2A) {  // no solve: the targets (Falcon-2A fast columns keep eta_j e^{-L_j} y_j)
             for (int idx = tid; idx < n * DVS; idx += kThreads) {
-                const int j = idx / DVS, c = idx % DVS;
+                const int j = (idx >> dvs_sh), c = (idx & (DVS - 1));
                 const float y = s.Y[j * DVS + c];
                 s.R[c * RS + j] = s.w[c * CS + C] != 0.f ? s.w[c * CS + j] * y : y;
             }
         } else if (VAR == kF3A) {  // no solve: every window slot's target (zero for the sentinel pair)
             for (int idx = tid; idx < n * W * DVS; idx += kThreads) {
-                const int m = idx / DVS, c = idx % DVS, i = m / W, a = m % W;
+                const int m = (idx >> dvs_sh), c = (idx & (DVS - 1)), i = m / W, a = m % W;
                 const bool valid = pos + t0 + i + 1 - a >= 2;
                 s.R[c * RS + m] = valid ? s.Y[(i - a + W - 1) * DVS + c] : 0.f;
             }
@@ -711,7 +713,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         Tin* out = static_cast<Tin*>(p.out) + bh * T * DV;
         if (per_column(VAR)) {
             for (int idx = tid; idx < (mode == 1 ? 0 : n * DVS); idx += kThreads) {
-                const int i = idx / DVS, c = idx % DVS;
+                const int i = (idx >> dvs_sh), c = (idx & (DVS - 1));
                 float o;
                 const float li = s.L[c * CS + i];
                 if (s.w[c * CS + C] != 0.f) {  // fast: o = e^{L_i} (QS + sum_j Sc_ij R~_j)
@@ -777,7 +779,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             // the write sum_l w_l sum_b x_{l-b} r_{l,b}^T gathered by extended row e = l - b + W - 1 first
             // (into H, whose last use was the solve): S' = e^{L_C} S + X_ext^T Rf
             for (int idx = tid; idx < (n + W - 1) * DVS; idx += kThreads) {
-                const int e = idx / DVS, c = idx % DVS;
+                const int e = (idx >> dvs_sh), c = (idx & (DVS - 1));
                 float acc = 0.f;
                 for (int b = 0; b < W; ++b) {
                     const int l = e + b - (W - 1);
@@ -788,7 +790,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             __syncthreads();
         }
         for (int idx = tid; idx < DK * DVS; idx += kThreads) {
-            const int r = idx / DVS, c = idx % DVS;
+            const int r = (idx >> dvs_sh), c = (idx & (DVS - 1));
             float acc = 0.f;
             if (windowed(VAR)) {
                 for (int e = 0; e < n + W - 1; ++e) acc = fmaf(s.X[e * XS + r], s.H[e * DVS + c], acc);
@@ -816,12 +818,12 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
         float* dst = mpart ? wsb + c0 : wsb + (long long)DK * DK + vc0;
         const int ld = mpart ? DK : DV;
         for (int idx = tid; idx < DK * DVS; idx += kThreads) {
-            const int r = idx / DVS, c = idx % DVS;
+            const int r = (idx >> dvs_sh), c = (idx & (DVS - 1));
             dst[r * ld + c] = s.S[idx];
         }
     } else if (p.S_final) {
         for (int idx = tid; idx < DK * DVS; idx += kThreads) {
-            const int r = idx / DVS, c = idx % DVS;
+            const int r = (idx >> dvs_sh), c = (idx & (DVS - 1));
             p.S_final[(bh * DK + r) * DV + c0 + c] = s.S[idx];
         }
     }
@@ -834,7 +836,7 @@ __global__ void __launch_bounds__(kThreads) falcon_chunk_generic_kernel(GParams 
             }
         if (!mpart)
             for (int idx = tid; idx < (W - 1) * DVS; idx += kThreads) {
-                const int sl = idx / DVS, cc = idx % DVS;
+                const int sl = (idx >> dvs_sh), cc = (idx & (DVS - 1));
                 stf(to + (long long)W * DK + sl * DV + vc0 + cc, load_val(T - W + 1 + sl, vc0 + cc));
             }
     }
