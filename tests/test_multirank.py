@@ -85,3 +85,21 @@ def test_reference_arm_runs_on_rank_zero_only():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
     assert not [l for l in outs[1].splitlines() if l.startswith("{")]  # rank 1: no work, no line
+
+
+def test_backward_reference_arm_runs_on_rank_zero_only():
+    code = textwrap.dedent("""
+        import types
+        import bench
+        from weight_linear_attention_gb300 import inputs as I
+        w = I.WORKLOADS["f1_bwd_b8h12t1024_bf16"].with_(seqlen=64)
+        args = types.SimpleNamespace(steps=1, warmup=1, gpus=2)
+        bench.run_reference_bwd(args, w)
+    """)
+    outs = _run_ranks(code)
+    lines0 = [l for l in outs[0].splitlines() if l.startswith("{")]
+    assert len(lines0) == 1
+    d = json.loads(lines0[0])
+    assert d["impl"] == "reference" and d["metric"] == "falcon_bwd_tokens_per_s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert not [l for l in outs[1].splitlines() if l.startswith("{")]
