@@ -141,8 +141,8 @@ size_t falcon_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk)
  * library, located once per device on the first call (cudaGetSymbolAddress) and never allocated
  * or freed. Nothing in it needs zeroing: every byte a kernel reads was written earlier in the same
  * call. A shape whose split path needs more than FALCON_STATIC_WORKSPACE_BYTES returns
- * FALCON_ERR_UNSUPPORTED without launching; a shape with no split path runs the single-pass
- * kernels. Calls that may overlap in time on one device (any streams) race on the scratch and
+ * FALCON_ERR_UNSUPPORTED without launching; a shape whose scan path needs more runs the single-pass
+ * kernels instead, as does a shape with neither path. Calls that may overlap in time on one device (any streams) race on the scratch and
  * must be serialized by the caller. Make the first call on each device before capturing a stream
  * into a graph, so that the one-time set-up is not inside the capture.
  */

@@ -109,3 +109,22 @@ def test_scan_state_alias():
     ro, rS, _ = run_oracle(F3, inp, window=4, S0=inp["S0"])
     _check("alias out", out.cpu(), ro, torch.bfloat16)
     _check("alias S", S.cpu(), rS, torch.bfloat16)
+
+
+def test_scan_path_on_static_scratch():
+    """falcon_fwd_static: a small Falcon-3 call whose scan path fits the library's own scratch."""
+    w = _wl(F3, "bf16", nonzero_s0=True, heads=2)
+    inp = I.make_inputs(w, seed=73, seqlen=500, batch=1)
+    dev = {n: inp[n].cuda() for n in ("q", "k", "v", "beta", "lam")}
+    S0 = inp["S0"].cuda().contiguous()
+    out = torch.empty_like(dev["v"])
+    S = torch.empty_like(S0)
+    d = F.make_dims(1, 2, 500, 64, 64, window=4, dtype=F.FALCON_BF16)
+    assert F.falcon_kernel_for(F3, d, 32) == 5
+    assert 0 < F.falcon_workspace_bytes(F3, d, 32) <= F.STATIC_WORKSPACE_BYTES
+    st = F.falcon_fwd_static(F3, dev["q"], dev["k"], dev["v"], dev["beta"], dev["lam"], S0, None, out, S, None, d, 32)
+    assert st == 0
+    torch.cuda.synchronize()
+    ro, rS, _ = run_oracle(F3, inp, window=4, S0=inp["S0"])
+    _check("static out", out.cpu(), ro, torch.bfloat16)
+    _check("static S", S.cpu(), rS, torch.bfloat16)
