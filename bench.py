@@ -239,38 +239,76 @@ def _oracle_start(w, inp, bs):
     return S0, tail
 
 
-def _e2e(args, w, host_segs, dev_segs, launch, stream):
-    """Same metric through the C ABI with host buffers: per step, pinned host->device copies of the
-    inputs, the forward pass, and a device->host copy of the output, all inside the timed region."""
+def _pipelined_ms(n_steps, warm, h2d, compute, d2h):
+    """Milliseconds per step of a host-to-host pipeline: step i uses device buffer set b = i % 2; its
+    host->device copies run on a copy-in stream, its compute on a compute stream, its device->host
+    copies on a copy-out stream, so that step i's compute overlaps the copies of steps i + 1 and i - 1.
+    Events order every reuse of a set (the copy-in of step i waits for step i - 2's compute; the
+    compute of step i for step i - 2's copy-out). Timed from before the first copy-in to after the
+    last copy-out, with CUDA events."""
+    import torch
+
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_c = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+
+    def one(i):
+        b = i % 2
+        if used[b]:
+            s_in.wait_event(ev_c[b])
+        with torch.cuda.stream(s_in):
+            h2d(b)
+        ev_in[b].record(s_in)
+        s_c.wait_event(ev_in[b])
+        if used[b]:
+            s_c.wait_event(ev_out[b])
+        compute(b, s_c)
+        ev_c[b].record(s_c)
+        s_out.wait_event(ev_c[b])
+        with torch.cuda.stream(s_out):
+            d2h(b)
+        ev_out[b].record(s_out)
+        used[b] = True
+
+    for i in range(warm):
+        one(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(n_steps):
+        one(warm + i)
+    e1.record(s_out)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n_steps
+
+
+def _e2e(args, w, host_segs, sets, launch):
+    """Same metric through the C ABI with host buffers: every step copies its inputs from pinned host
+    memory to the device, runs the forward pass and copies the output back, the copies of
+    neighbouring steps overlapping its compute (two device buffer sets)."""
     import torch
 
     B, H, Ts, dv = w.batch, w.heads, w.seqlen, w.dv
     hsegs = [{n: t.pin_memory() for n, t in hs.items()} for hs in host_segs]
-    hout = [torch.empty((B, H, Ts, dv), dtype=w.torch_dtype).pin_memory() for _ in range(w.segments)]
-    h2d = sum(t.numel() * t.element_size() for hs in hsegs for t in hs.values())
-    d2h = sum(t.numel() * t.element_size() for t in hout)
+    hout = [[torch.empty((B, H, Ts, dv), dtype=w.torch_dtype).pin_memory() for _ in range(w.segments)]
+            for _ in range(2)]
+    h2d_bytes = sum(t.numel() * t.element_size() for hs in hsegs for t in hs.values())
+    d2h_bytes = sum(t.numel() * t.element_size() for t in hout[0])
 
-    def step():
+    def h2d(b):
         for s in range(w.segments):
             for n in hsegs[s]:
-                dev_segs[s][n].copy_(hsegs[s][n], non_blocking=True)
-        launch(dev_segs, stream)
-        for s in range(w.segments):
-            hout[s].copy_(dev_segs[s]["out"], non_blocking=True)
+                sets[b][s][n].copy_(hsegs[s][n], non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            step()
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        n = max(3, min(args.steps, 50))
-        e0.record(stream)
-        for _ in range(n):
-            step()
-        e1.record(stream)
-        stream.synchronize()
-    return e0.elapsed_time(e1) / n, h2d, d2h
+    def d2h(b):
+        for s in range(w.segments):
+            hout[b][s].copy_(sets[b][s]["out"], non_blocking=True)
+
+    ms = _pipelined_ms(max(3, min(args.steps, 50)), max(3, args.warmup), h2d, lambda b, st: launch(sets[b], st), d2h)
+    return ms, h2d_bytes, d2h_bytes
 
 
 def run_ours(args, w):
@@ -373,7 +411,7 @@ def run_ours(args, w):
     if args.no_e2e:
         e2e_ms, h2d, d2h = float("nan"), 0, 0
     else:
-        e2e_ms, h2d, d2h = _e2e(args, w, host_segs, sets[0], launch, stream)
+        e2e_ms, h2d, d2h = _e2e(args, w, host_segs, sets, launch)
     total_ms = _barrier_max(dist, total_ms)
     ms_step = total_ms / args.steps
     tokens_step = w.total_tokens
@@ -402,8 +440,10 @@ def run_ours(args, w):
                      "scope": "one falcon_fwd call (all kernels it launches); per-kernel shares in profiles/",
                      "traffic": _traffic(w.name, kernel_id), "peak_source": src,
                      "algorithmic_bytes_per_step": step_bytes, "ms_per_call": mean_launch},
-        "e2e": None if args.no_e2e else {"value": world * tokens_step / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": None if args.no_e2e else {"value": world * tokens_step / (e2e_ms / 1e3), "unit": "tokens/s",
+                                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                                         "pipeline": "copy-in of step i+1 and copy-out of step i-1 overlap the "
+                                                     "compute of step i (two device buffer sets, three streams)"},
         "gpu_launches": args.steps * w.segments * _launches_per_call(w, kernel_id),
         "clocks": clk,
     }
@@ -563,35 +603,29 @@ def run_ours_bwd(args, w):
         total_ms = e0.elapsed_time(e1)
         if F.falcon_device_status(stream.cuda_stream) != 0:
             raise SystemExit("device-side timeout during the timed region")
-        # end to end: pinned host inputs in, every gradient out, per step
+        # end to end: pinned host inputs in, every gradient out, per step (pipelined as in _e2e)
         e2e = None
         if not args.no_e2e:
             hin = {n: host[n].pin_memory() for n in names_in}
             outs = ("dq", "dk", "dv", "dbeta", "dlam", "dS0")
-            hout = {n: torch.empty(sets[0][n].shape, dtype=torch.float32).pin_memory() for n in outs}
-            d = sets[0]
+            hout = [{n: torch.empty(sets[0][n].shape, dtype=torch.float32).pin_memory() for n in outs}
+                    for _ in range(2)]
 
-            def e2e_step():
+            def h2d(b):
                 for n in names_in:
-                    d[n].copy_(hin[n], non_blocking=True)
-                launch(d, stream)
-                for n in outs:
-                    hout[n].copy_(d[n], non_blocking=True)
+                    sets[b][n].copy_(hin[n], non_blocking=True)
 
-            for _ in range(3):
-                e2e_step()
-            stream.synchronize()
-            n_e = max(3, min(args.steps, 20))
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a0.record(stream)
-            for _ in range(n_e):
-                e2e_step()
-            a1.record(stream)
-            stream.synchronize()
-            e2e_ms = _barrier_max(dist, a0.elapsed_time(a1) / n_e)
+            def d2h(b):
+                for n in outs:
+                    hout[b][n].copy_(sets[b][n], non_blocking=True)
+
+            e2e_ms = _barrier_max(dist, _pipelined_ms(max(3, min(args.steps, 20)), 3, h2d,
+                                                      lambda b, st: launch(sets[b], st), d2h))
             e2e = {"value": world * B * T / (e2e_ms / 1e3), "unit": "tokens/s",
                    "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin.values()),
-                   "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout.values())}
+                   "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout[0].values()),
+                   "pipeline": "copy-in of step i+1 and copy-out of step i-1 overlap the compute of step i "
+                               "(two device buffer sets, three streams)"}
     total_ms = _barrier_max(dist, total_ms)
     ms_step = total_ms / args.steps
     value = _job_value(world, B * T, args.steps, total_ms)
