@@ -68,7 +68,7 @@ typedef enum { FALCON_F32 = 0, FALCON_BF16 = 1 } falcon_dtype_t;
 enum {
     FALCON_OK = 0,
     FALCON_ERR_INVALID_ARG = 1,   /* null required pointer, bad variant/window/chunk/dims, tail vs pos, overlap */
-    FALCON_ERR_UNSUPPORTED = 2,   /* a head size, dtype, window or chunk this build has no kernel for */
+    FALCON_ERR_UNSUPPORTED = 2,   /* a head size, dtype, window or chunk with no kernel in the library */
     FALCON_ERR_MISALIGNED = 3,    /* a pointer not aligned as documented below */
     FALCON_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
     FALCON_ERR_DEVICE_TIMEOUT = 5 /* a kernel gave up a bounded wait (see falcon_device_status) */
