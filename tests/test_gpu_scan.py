@@ -128,3 +128,13 @@ def test_scan_path_on_static_scratch():
     ro, rS, _ = run_oracle(F3, inp, window=4, S0=inp["S0"])
     _check("static out", out.cpu(), ro, torch.bfloat16)
     _check("static S", S.cpu(), rS, torch.bfloat16)
+
+
+@pytest.mark.parametrize("variant", [F3, F3A])
+@pytest.mark.parametrize("W,chunk", [(1, 64), (2, 32), (3, 32), (5, 16), (6, 16), (7, 16), (8, 16)])
+def test_scan_path_window_sizes(variant, W, chunk):
+    """Every window size on the scan path: the Falcon-3 block solve takes 16 // W tokens per block, so
+    W = 3, 5, 6, 7 leave a partial last block and W = 1, 2, 8 do not."""
+    w = _wl(variant, "bf16", window=W, chunk=chunk, nonzero_s0=True)
+    inp = I.make_inputs(w, seed=80 + W, seqlen=300, batch=2)
+    _run(w, inp, chunk, S0=inp["S0"], name=f"v{variant} W={W} C={chunk}")
