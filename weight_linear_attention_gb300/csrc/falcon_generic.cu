@@ -247,7 +247,14 @@ __host__ __device__ inline size_t smem_floats(int variant, int dk, int dvs, int 
     };
     take(s ? &s->X : nullptr, size_t(NE) * (dk + 1));  // rows padded: the Gram reads rows across lanes
     take(s ? &s->Q : nullptr, size_t(C) * (dk + 1));
-    take(s ? &s->Y : nullptr, size_t(NE) * dvs);
+    // Y doubles as the Falcon-3 block solve's diagonal-block inverses (16 x 16 per block of 16 / W
+    // tokens) when a CTA takes all 64 columns, so it is at least that large
+    size_t ny = size_t(NE) * dvs;
+    if (variant == kF3 && dvs == 64) {
+        const int tb = 16 / W, nblk = (C + tb - 1) / tb;
+        ny = ny > size_t(nblk) * 256 ? ny : size_t(nblk) * 256;
+    }
+    take(s ? &s->Y : nullptr, ny);
     take(s ? &s->S : nullptr, size_t(dk) * dvs);
     take(s ? &s->G : nullptr, size_t(NE) * NE);
     take(s ? &s->Sc : nullptr, size_t(C) * NE);
@@ -590,7 +597,8 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GPara
                 s.R[c * RS + m] = valid_u(i, a) ? s.Y[pa * DVS + c] - expf(s.Lx[i]) * s.H[pa * DVS + c] : 0.f;
             }
             __syncthreads();
-            // (2) diagonal-block inverses, one warp per block, a lane per column (Y is free now)
+            // (2) diagonal-block inverses, one warp per block, a lane per column (Y is free now, and sized
+            // for them)
             float* Dinv = s.Y;  // [nblk][16][16]
             {
                 const int kb = tid >> 5, col = tid & 31;
