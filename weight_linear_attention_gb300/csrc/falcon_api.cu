@@ -85,7 +85,7 @@ int validate_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail
     a->eps = d->eps;
     a->eps_gamma = d->eps_gamma;
     a->chunk = chunk;
-    if (falcon::generic_smem_bytes(*a, 16) > 200 * 1024 && !falcon::tc_supported(*a)) return FALCON_ERR_UNSUPPORTED;
+    if (falcon::generic_smem_bytes(*a, 16, false) > 200 * 1024 && !falcon::tc_supported(*a)) return FALCON_ERR_UNSUPPORTED;
     return FALCON_OK;
 }
 

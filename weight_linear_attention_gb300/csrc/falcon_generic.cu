@@ -61,6 +61,7 @@ struct GParams {
     //   the first dk those of M and Ao (state e_c, no target), the rest those of U and Bo (zero state,
     //   the targets); the results go to the chunk's workspace block.
     int mode;
+    int staged;       // mode 0: the next chunk's inputs are copied ahead into shared memory
     const float* mu;  // Falcon-3, mode 1: every token's window normaliser, precomputed ([B*H][T])
     float* ws;   // per chunk (sequence-major) [M | U | S | Ao | Bo], each 64 x 64 fp32 (Ao, Bo: C rows used)
     long long N; // chunks per sequence (mode 1)
@@ -235,9 +236,12 @@ __device__ void mm_tiled(float* out, int ldo, const float* a, int lda, const flo
 struct Smem {
     float *X, *Q, *Y, *S, *G, *Sc, *H, *QS, *R, *A, *P;
     float *eta, *L, *Lx, *kap, *w;
+    float* stg;  // mode 0: the next chunk's raw tiles (and per-column gains, ridge terms), copied ahead
 };
 
-__host__ __device__ inline size_t smem_floats(int variant, int dk, int dvs, int C, int W, Smem* s, float* base) {
+// es: bytes per input element; staged: room for the next chunk's raw inputs (mode 0).
+__host__ __device__ inline size_t smem_floats(int variant, int dk, int dvs, int C, int W, Smem* s, float* base,
+                                              int es = 2, bool staged = false) {
     const int NE = C + W - 1;
     const int per_col = per_column(variant) ? dvs : 1;
     size_t off = 0;
@@ -268,7 +272,24 @@ __host__ __device__ inline size_t smem_floats(int variant, int dk, int dvs, int 
     take(s ? &s->Lx : nullptr, size_t(C + 1) * per_col);
     take(s ? &s->kap : nullptr, size_t(C));
     take(s ? &s->w : nullptr, size_t(C + 1) * per_col);
+    if (staged) {
+        const size_t vecs = size_t(NE) * (dk / 8) + size_t(C) * (dk / 8) + size_t(NE) * (dvs / 8);
+        take(s ? &s->stg : nullptr, vecs * 8 * es / 4 + (per_column(variant) ? size_t(C) * dvs : 0) + size_t(C));
+    } else if (s) {
+        s->stg = nullptr;
+    }
     return off;
+}
+
+__device__ __forceinline__ void cp_async16z(void* smem, const void* gmem, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4z(void* smem, const void* gmem, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem), "r"(valid ? 4 : 0)
+                 : "memory");
 }
 
 template <typename Tin, int VAR>
@@ -298,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GPara
     float* wsb = mode != 0 ? p.ws + (bh * p.N + nck) * blk : nullptr;  // this chunk's workspace block
 
     Smem s;
-    smem_floats(VAR, DK, DVS, C, W, &s, smem_raw);
+    smem_floats(VAR, DK, DVS, C, W, &s, smem_raw, (int)sizeof(Tin), p.mode == 0 && p.staged);
 
     const Tin* q = static_cast<const Tin*>(p.q) + bh * T * DK;
     const Tin* k = static_cast<const Tin*>(p.k) + bh * T * DK;
@@ -335,8 +356,48 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GPara
         __syncthreads();  // previous chunk finished with every buffer
         // ---- (1) tiles. Extended row e <-> pair with global index pos + t0 + 2 - W + e. Eight elements
         // per 16-byte load (rows of q, k, v and the tail are 16-byte aligned), every load of a thread
-        // issued before its stores.
-        {
+        // issued before its stores. After the first chunk of a mode-0 walk the tiles were copied ahead
+        // into the staging area (during the previous chunk's compute) and are only widened here.
+        const int KV = DK / 8, VV = DVS / 8;
+        const int nx = NE * KV, nq = C * KV, ny = NE * VV;
+        constexpr int kVecF = 8 * (int)sizeof(Tin) / 4;  // floats of staging per 8-element vector
+        auto tile_dst = [&](int idx) -> float* {
+            if (idx < nx) return s.X + (idx / KV) * XS + 8 * (idx % KV);
+            if (idx < nx + nq) return s.Q + ((idx - nx) / KV) * XS + 8 * ((idx - nx) % KV);
+            return s.Y + ((idx - nx - nq) / VV) * DVS + 8 * ((idx - nx - nq) % VV);
+        };
+        const bool staged = mode == 0 && p.staged && t0 > t_begin;
+        if (staged) {
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            __syncthreads();
+            for (int idx = tid; idx < nx + nq + ny; idx += kThreads) {
+                float v8[8];
+                const float* src = s.stg + idx * kVecF;
+                if (sizeof(Tin) == 2) {
+                    const uint4 u = *reinterpret_cast<const uint4*>(src);
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        v8[2 * h] = __uint_as_float(w4[h] << 16);
+                        v8[2 * h + 1] = __uint_as_float(w4[h] & 0xffff0000u);
+                    }
+                } else {
+#pragma unroll
+                    for (int e8 = 0; e8 < 8; ++e8) v8[e8] = src[e8];
+                }
+                float* dst = tile_dst(idx);
+#pragma unroll
+                for (int e8 = 0; e8 < 8; ++e8) dst[e8] = v8[e8];
+            }
+            if (per_column(VAR)) {
+                const float* sb = s.stg + (nx + nq + ny) * kVecF;
+                for (int idx = tid; idx < C * DVS; idx += kThreads) {
+                    const int i = (idx >> dvs_sh), c = (idx & (DVS - 1));
+                    s.eta[c * CS + i] = sb[idx];
+                }
+                for (int i = tid; i < C; i += kThreads) s.kap[i] = sb[C * DVS + i];
+            }
+        } else {
             const int KV = DK / 8, VV = DVS / 8;
             const int nx = NE * KV, nq = C * KV, ny = NE * VV;
             constexpr int kPer = 4;  // vector loads in flight per thread and round
@@ -370,24 +431,57 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GPara
 #pragma unroll
                 for (int m = 0; m < kPer; ++m) {
                     const int idx = base + m * kThreads;
-                    float* dst = nullptr;
-                    if (idx < nx) dst = s.X + (idx / KV) * XS + 8 * (idx % KV);
-                    else if (idx < nx + nq) dst = s.Q + ((idx - nx) / KV) * XS + 8 * ((idx - nx) % KV);
-                    else if (idx < nx + nq + ny) dst = s.Y + ((idx - nx - nq) / VV) * DVS + 8 * ((idx - nx - nq) % VV);
-                    if (dst)
+                    if (idx < nx + nq + ny) {
+                        float* dst = tile_dst(idx);
 #pragma unroll
                         for (int e8 = 0; e8 < 8; ++e8) dst[e8] = buf[m][e8];
+                    }
                 }
             }
-        }
-        if (per_column(VAR)) {  // the chunk's gains (per column, into eta) and ridge coefficients (into kap)
-            for (int idx = tid; idx < C * DVS; idx += kThreads) {
-                const int i = (idx >> dvs_sh), c = (idx & (DVS - 1));
-                s.eta[c * CS + i] = i < n ? beta[(t0 + i) * DV + c0 + c] : 0.f;
+            if (per_column(VAR)) {  // the chunk's gains (per column, into eta) and ridge coefficients (into kap)
+                for (int idx = tid; idx < C * DVS; idx += kThreads) {
+                    const int i = (idx >> dvs_sh), c = (idx & (DVS - 1));
+                    s.eta[c * CS + i] = i < n ? beta[(t0 + i) * DV + c0 + c] : 0.f;
+                }
+                for (int i = tid; i < C; i += kThreads) s.kap[i] = i < n ? lam[t0 + i] : 0.f;
             }
-            for (int i = tid; i < C; i += kThreads) s.kap[i] = i < n ? lam[t0 + i] : 0.f;
         }
         __syncthreads();
+        if (mode == 0 && p.staged && t0 + C < t_end) {  // copy the next chunk's inputs ahead (all in k, q, v)
+            const long long t1 = t0 + C;
+            const int n1 = (int)min((long long)C, T - t1);
+            for (int idx = tid; idx < nx + nq + ny; idx += kThreads) {
+                const Tin* src;
+                bool ok;
+                if (idx < nx) {
+                    const int e = idx / KV, c8 = 8 * (idx % KV);
+                    ok = e < n1 + W - 1;
+                    src = k + (t1 - W + e) * DK + c8;
+                } else if (idx < nx + nq) {
+                    const int i = (idx - nx) / KV, c8 = 8 * ((idx - nx) % KV);
+                    ok = i < n1;
+                    src = q + (t1 + i) * DK + c8;
+                } else {
+                    const int e = (idx - nx - nq) / VV, c8 = 8 * ((idx - nx - nq) % VV);
+                    ok = e < n1 + W - 1;
+                    src = v + (t1 + 1 - W + e) * DV + vc0 + c8;
+                }
+                if (!ok) src = k;  // not read (zero fill)
+                float* dst = s.stg + idx * kVecF;
+                cp_async16z(dst, src, ok);
+                if (sizeof(Tin) == 4) cp_async16z(dst + 4, reinterpret_cast<const float*>(src) + 4, ok);
+            }
+            if (per_column(VAR)) {
+                float* sb = s.stg + (nx + nq + ny) * kVecF;
+                for (int idx = tid; idx < C * DVS; idx += kThreads) {  // 4-byte copies: beta is 4-byte aligned
+                    const int i = (idx >> dvs_sh), c = (idx & (DVS - 1));
+                    const bool ok = i < n1;
+                    cp_async4z(sb + idx, ok ? beta + (t1 + i) * DV + c0 + c : beta, ok);
+                }
+                for (int i = tid; i < C; i += kThreads) cp_async4z(sb + C * DVS + i, i < n1 ? lam + t1 + i : lam, i < n1);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        }
         // ---- (2) Gram, scores, projected history, Q S
         constexpr bool kMmaGram = std::is_same<Tin, __nv_bfloat16>::value && !windowed(VAR);
         if (kMmaGram && C <= 64 && C % 16 == 0 && DK % 16 == 0) {
@@ -926,15 +1020,15 @@ int choose_dvs(const Launch& a) {
     int dvs = (int)a.dv;
     const int64_t seqs = a.B * a.H;
     while (dvs > 8 && seqs * (a.dv / dvs) < 2 * 152) dvs /= 2;
-    while (dvs > 16 && generic_smem_bytes(a, dvs) > 200 * 1024) dvs /= 2;
+    while (dvs > 16 && generic_smem_bytes(a, dvs, false) > 200 * 1024) dvs /= 2;
     return dvs;
 }
 
 }  // namespace
 
-size_t generic_smem_bytes(const Launch& a, int dvs) {
+size_t generic_smem_bytes(const Launch& a, int dvs, bool staged) {
     const int W = windowed(a.variant) ? a.W : 1;
-    return smem_floats(a.variant, (int)a.dk, dvs, a.chunk, W, nullptr, nullptr) * sizeof(float);
+    return smem_floats(a.variant, (int)a.dk, dvs, a.chunk, W, nullptr, nullptr, a.bf16 ? 2 : 4, staged) * sizeof(float);
 }
 
 int launch_generic(const Launch& a, cudaStream_t st) { return launch_generic_mode(a, 0, nullptr, 0, nullptr, st); }
@@ -997,7 +1091,9 @@ int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const
     gp.mu = mu;
     gp.ws = ws;
     gp.N = N;
-    const size_t smem = generic_smem_bytes(a, dvs);
+    // mode 0 copies each next chunk ahead when the staging area fits beside the tiles
+    gp.staged = mode == 0 && generic_smem_bytes(a, dvs, true) <= 200 * 1024;
+    const size_t smem = generic_smem_bytes(a, dvs, gp.staged != 0);
     const long long slices = (mode == 1 ? a.dk + a.dv : a.dv) / dvs;
     dim3 grid((unsigned)(slices * a.B * a.H * (mode == 0 ? 1 : N)));
     cudaError_t e = a.bf16 ? launch_typed<__nv_bfloat16>(a, gp, grid, smem, st)

@@ -43,7 +43,7 @@ int launch_generic(const Launch& a, cudaStream_t stream);
 int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const float* mu, cudaStream_t stream);
 // Falcon-3: every token's window normaliser into mu[B*H][T] (read by modes 1 and 2 instead of recomputed).
 int launch_window_mu(const Launch& a, float* mu, cudaStream_t stream);
-size_t generic_smem_bytes(const Launch& a, int dvs);
+size_t generic_smem_bytes(const Launch& a, int dvs, bool staged = true);  // staged: mode 0's copy-ahead area
 
 // tcgen05 / TMA chunk kernel (Falcon-1 and 1A, bf16, dk = dv = 64, chunk 64).
 bool tc_supported(const Launch& a);
