@@ -1,0 +1,35 @@
+"""Host-side arithmetic of bench.py (CPU only): the per-step byte and flop counts and the launch
+counts that go into the JSON line."""
+
+import bench
+from weight_linear_attention_gb300 import inputs as I
+
+
+def test_launches_per_call():
+    W = I.WORKLOADS
+    assert bench._launches_per_call(W["f1_b8h12t1024_bf16"], 3) == 3          # split path
+    assert bench._launches_per_call(W["f1_b8h12t1024_bf16"], 2) == 1          # single pass
+    # scan path, Falcon-3 at 8192 tokens per call, chunk 32: normalisers, maps, compose, groups, apply
+    assert bench._launches_per_call(W["f3w4_b2h12t16384_bf16"], 5) == 5
+    assert bench._launches_per_call(W["f3aw4_b2h12t16384_bf16"], 5) == 4     # no normaliser pass
+    assert bench._launches_per_call(W["f3w4_b2h12t16384_bf16"].with_(seqlen=256), 5) == 3  # one group
+
+
+def test_forward_algorithmic_bytes():
+    w = I.WORKLOADS["f1_b8h12t1024_bf16"]
+    tok = 8 * 12 * 1024
+    # q, k, v and out in bf16, beta and lambda fp32, S_final fp32, the tail key
+    expect = tok * (3 * 64 + 64) * 2 + tok * 8 + 96 * 64 * 64 * 4 + 96 * 64 * 2
+    assert bench._algorithmic_bytes(w, 2) == expect
+
+
+def test_backward_counts():
+    w = I.WORKLOADS["f1_bwd_b8h12t1024_bf16"]
+    one = 2 * 64 ** 3
+    assert bench._bwd_flops_per_chunk(w) == one * (10 + 1 / 3 + 2 + 15)
+    assert bench._bwd_flops_per_chunk(I.WORKLOADS["f1a_bwd_b8h12t1024_bf16"]) == one * 13
+    tok = 8 * 12 * 1024
+    # q, k, v, dout (bf16) and beta, lambda read; fp32 dq, dk, dv, dbeta, dlambda written; dS_final, dS0
+    expect = tok * 4 * 64 * 2 + tok * 8 + tok * 3 * 64 * 4 + tok * 8 + 2 * 96 * 64 * 64 * 4
+    assert bench._bwd_bytes(w, 2) == expect
+
