@@ -371,3 +371,64 @@ def chunk_backward(variant, q, k, v, beta, lam, dout, S0=None, dS_final=None, *,
         dk_[:-1] = dx[1:]
     return {"dq": dq, "dk": dk_, "dv": dvv, "dbeta": dbeta, "dlam": dlam,
             "dS0": dS0, "dtail": dx[0] if (T and pos > 0) else None}
+
+
+# --------------------------------------------------------------------------------------
+# 4. scan over chunk maps (Falcon-1, 1A, 3, 3A)
+# --------------------------------------------------------------------------------------
+
+def scan_forward(variant, q, k, v, beta, lam, S0=None, *, C, G=16, pos=0, tail=None, W=1, eps=1e-6, eps_gamma=1e-6):
+    """Falcon-1, 1A and 3 (the variants chunk_forward covers). The scan path's algebra for one sequence, fp64 (paperlayer §H.1: chunk maps compose
+    associatively). Every chunk n acts affinely on its start state, S_{n+1} = M_n S_n + U_n and
+    O_n = Ao_n S_n + Bo_n; the four maps are read off the chunk form run over that chunk alone (its
+    window and shifted-key history passed as a tail): from the unit states e_c without targets (the
+    columns of M_n and Ao_n) and from the zero state with the targets (U_n, Bo_n). The start states
+    are then formed in groups of G chunks: each group's composed map, the group start states, and
+    each chunk's start state from its group's; the outputs come from the output maps.
+    Returns (out [T,dv], S_final [dk,dv])."""
+    q, k, v, beta, lam, S0 = (_np(a) for a in (q, k, v, beta, lam, S0))
+    T, dk = q.shape
+    dv = v.shape[1]
+    key, val = _global_pairs(k, v, pos, tail, W)
+    S = np.zeros((dk, dv)) if S0 is None else S0
+    maps = []
+    for t0 in range(0, T, C):
+        t1 = min(T, t0 + C)
+        P = pos + t0  # tokens before the chunk
+        tl = None
+        if P > 0:
+            tl = (np.stack([key(g) for g in range(P - W + 1, P + 1)]),
+                  np.stack([val(g) for g in range(P - W + 2, P + 1)]) if W > 1 else np.zeros((0, dv)))
+
+        def run(Sst, targets):  # without targets, the window's earlier values are zero too
+            vv = v[t0:t1] if targets else np.zeros((t1 - t0, dv))
+            tt = tl if (targets or tl is None) else (tl[0], np.zeros_like(tl[1]))
+            return chunk_forward(variant, q[t0:t1], k[t0:t1], vv, beta[t0:t1], lam[t0:t1], Sst, C=t1 - t0, pos=P,
+                                 tail=tt, W=W, eps=eps, eps_gamma=eps_gamma)
+
+        M = np.zeros((dk, dk))
+        Ao = np.zeros((t1 - t0, dk))
+        for c in range(dk):  # every value column starts at e_c: the columns of M and Ao
+            Sst = np.zeros((dk, dv))
+            Sst[c, :] = 1.0
+            o, Se = run(Sst, False)
+            M[:, c] = Se[:, 0]
+            Ao[:, c] = o[:, 0]
+        Bo, U = run(np.zeros((dk, dv)), True)
+        maps.append((M, U, Ao, Bo))
+    N = len(maps)
+    starts = []
+    for g0 in range(0, N, G):  # group maps, then the group start states
+        Mg, Ug = np.eye(dk), np.zeros((dk, dv))
+        for n in range(g0, min(N, g0 + G)):
+            Mg, Ug = maps[n][0] @ Mg, maps[n][0] @ Ug + maps[n][1]
+        starts.append(S)
+        S = Mg @ S + Ug
+    out = np.zeros((T, dv))
+    for gi, g0 in enumerate(range(0, N, G)):  # each group's chunks from its start state
+        Sn = starts[gi]
+        for n in range(g0, min(N, g0 + G)):
+            M, U, Ao, Bo = maps[n]
+            out[n * C:n * C + Ao.shape[0]] = Ao @ Sn + Bo
+            Sn = M @ Sn + U
+    return out, S

@@ -377,3 +377,23 @@ def test_inner_product_variants_sentinel_and_arguments():
     assert np.array_equal(S, S0)
     with pytest.raises(AssertionError):
         oracle.falcon_ref_fwd(F2A, q, k, v, beta, lam, S0)  # gains must be per column
+
+
+# ---------------------------------------------------------------- the scan path's algebra
+
+@pytest.mark.parametrize("variant,W,pos", [(F1, 1, 0), (F1A, 1, 0), (F3, 3, 0), (F3, 4, 0), (F1, 1, 5), (F3, 3, 6)])
+@pytest.mark.parametrize("C,G", [(4, 3), (5, 16), (3, 1)])
+def test_scan_over_chunk_maps_is_exact(variant, W, pos, C, G):
+    """Per-chunk affine maps of the state and of the outputs, composed in groups of G chunks, then the
+    outputs from each chunk's start state (the scan path) give the oracle's outputs and final state
+    (paperlayer §H.1: chunk maps compose associatively)."""
+    q, k, v, beta, lam, S0 = _rand(40 + C + G, 1, 1, 29, 5, 4, variant)
+    tail = None
+    if pos > 0:
+        rng = np.random.default_rng(7)
+        tail = (rng.standard_normal((1, 1, W, 5)), rng.standard_normal((1, 1, W - 1, 4)))
+    o, S = forms.scan_forward(variant, q[0, 0], k[0, 0], v[0, 0], beta[0, 0], lam[0, 0], S0[0, 0], C=C, G=G,
+                              pos=pos, tail=None if tail is None else (tail[0][0, 0], tail[1][0, 0]), W=W)
+    ro, rS, _ = oracle.falcon_ref_fwd(variant, q, k, v, beta, lam, S0, tail, pos=pos, window=W)
+    np.testing.assert_allclose(o, ro[0, 0], rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(S, rS[0, 0], rtol=1e-10, atol=1e-10)
