@@ -432,3 +432,31 @@ def scan_forward(variant, q, k, v, beta, lam, S0=None, *, C, G=16, pos=0, tail=N
             out[n * C:n * C + Ao.shape[0]] = Ao @ Sn + Bo
             Sn = M @ Sn + U
     return out, S
+
+
+def chunk_backward_per_column(variant, q, k, v, beta, lam, dout, S0=None, dS_final=None, *, C, pos=0, tail=None,
+                              eps=1e-6, eps_gamma=1e-6):
+    """Falcon-2 / 2A gradients by columns: every value column evolves on its own given the shared keys
+    (its own beta, so its own step sizes, decay and triangular system), so the loss splits into one
+    term per column and each column's term is the Falcon-1 / 1A backward of that column with its beta.
+    The per-column gradients of v, beta, S0 are that column's; those of q, k, lambda and the tail key
+    are summed over the columns. beta [T,dv]."""
+    q, k, v, beta, lam, dout, S0, dS_final = (_np(a) for a in (q, k, v, beta, lam, dout, S0, dS_final))
+    T, dk = q.shape
+    dv = v.shape[1]
+    base = F1 if variant == F2 else F1A
+    acc = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v), "dbeta": np.zeros_like(beta),
+           "dlam": np.zeros_like(lam), "dS0": np.zeros((dk, dv)), "dtail": None if pos == 0 else np.zeros(dk)}
+    for c in range(dv):
+        g = chunk_backward(base, q, k, v[:, c:c + 1], beta[:, c], lam, dout[:, c:c + 1],
+                           None if S0 is None else S0[:, c:c + 1], None if dS_final is None else dS_final[:, c:c + 1],
+                           C=C, pos=pos, tail=tail, eps=eps, eps_gamma=eps_gamma)
+        acc["dq"] += g["dq"]
+        acc["dk"] += g["dk"]
+        acc["dlam"] += g["dlam"]
+        acc["dv"][:, c] = g["dv"][:, 0]
+        acc["dbeta"][:, c] = g["dbeta"]
+        acc["dS0"][:, c] = g["dS0"][:, 0]
+        if pos > 0:
+            acc["dtail"] += g["dtail"]
+    return acc

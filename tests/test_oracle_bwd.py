@@ -151,3 +151,19 @@ def test_chunk_backward_clamped_chunks(variant):
                              c["dout"][0, 0], c["S0"][0, 0], c["dS"][0, 0], C=8)
     for n in ("dq", "dk", "dv", "dbeta", "dlam", "dS0"):
         np.testing.assert_allclose(f[n], g[n][0, 0], rtol=1e-9, atol=1e-9, err_msg=n)
+
+
+@pytest.mark.parametrize("variant", [F2, F2A])
+@pytest.mark.parametrize("C,pos", [(4, 0), (8, 3), (64, 0)])
+def test_per_column_backward_matches_oracle(variant, C, pos):
+    """Falcon-2 / 2A: the gradient split into one Falcon-1 / 1A backward per value column (the columns
+    share only the keys) equals autograd of the per-column recurrence."""
+    c = _case(90 + C, B=1, H=1, T=19, dk=5, dv=3, variant=variant, pos=pos)
+    g = _grads(variant, c)
+    f = forms.chunk_backward_per_column(variant, c["q"][0, 0], c["k"][0, 0], c["v"][0, 0], c["beta"][0, 0],
+                                        c["lam"][0, 0], c["dout"][0, 0], c["S0"][0, 0], c["dS"][0, 0], C=C, pos=pos,
+                                        tail=None if pos == 0 else c["tail"][0, 0])
+    for n in ("dq", "dk", "dv", "dbeta", "dlam", "dS0"):
+        np.testing.assert_allclose(f[n], g[n][0, 0], rtol=1e-9, atol=1e-9, err_msg=n)
+    if pos > 0:
+        np.testing.assert_allclose(f["dtail"], g["dtail"][0, 0], rtol=1e-9, atol=1e-9)
