@@ -51,12 +51,39 @@ def _algorithmic_bytes(w, es):
 
 def _launches_per_call(w, kernel_id):
     """Kernels one falcon_fwd call launches on the path `kernel_id` takes."""
-    if kernel_id == 3:
-        return 3
     if kernel_id == 5:  # [window normalisers,] chunk maps, [compose, groups,] apply
         n = -(-w.seqlen // w.chunk)
         return (1 if w.variant == "falcon3" else 0) + 1 + (2 if n > 16 else 0) + 1
     return 1
+
+
+def _chunk_flops(w):
+    """Flops of the method's chunk algebra per call (each product once, 2 flops per multiply-add, at
+    the workload's own sizes): per (b, h) chunk of C tokens with dk = dv = d, Falcon-1 forms X X^T,
+    Q X^T, X S_n, Q S_n, the triangular solve (C^2 d / 2 multiply-adds), P R and X^T diag(w) R;
+    Falcon-1A forms Q X^T, Q S_n, P Y and X^T diag(w) Y. Other variants: None (not reported)."""
+    C, d = w.chunk, w.dk
+    per = {"falcon1": 2 * (4 * C * C * d + 2 * C * d * d + C * C * d / 2),
+           "falcon1a": 2 * (2 * C * C * d + 2 * C * d * d)}.get(w.variant)
+    if per is None:
+        return None
+    n = -(-w.seqlen // C)
+    return per * w.batch * w.heads * n * w.segments
+
+
+def _cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model", "hardware")):
+                return line.split(":", 1)[1].strip()
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("cpu part"):
+                return "cpu part " + line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
 
 
 def _kernel_digest(files=None):
@@ -203,28 +230,41 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(w, budget_s=12.0):
+def cpu_baseline(w, budget_s=4.0):
+    """The oracle on the host cores: enough batch rows of the first segment that every core has a
+    sequence, each measurement repeating the sample for about `budget_s` seconds; the median of three
+    such measurements with all cores and one with a single thread."""
     import oracle
     from weight_linear_attention_gb300 import inputs as I
 
     oracle.build()
     cores = os.cpu_count() or 1
     inp = I.make_inputs(w, seed=0)
-    bs = 1
+    bs = max(1, min(w.batch, -(-cores // w.heads)))
     x = {n: inp[n][:bs, :, :w.seqlen] for n in ("q", "k", "v", "beta", "lam")}
     S0, tail = _oracle_start(w, inp, bs)
-    runs, t0 = 0, time.perf_counter()
-    while True:
-        oracle.falcon_ref_fwd(w.variant_id, x["q"], x["k"], x["v"], x["beta"], x["lam"], S0, tail, pos=w.pos0,
-                              window=w.window, eps=w.eps, eps_gamma=w.eps_gamma, nthreads=cores)
-        runs += 1
-        if time.perf_counter() - t0 > budget_s or runs >= 100000:
-            break
-    el = time.perf_counter() - t0
-    return {"value": runs * bs * w.seqlen / el, "unit": "tokens/s", "cores": min(cores, bs * w.heads),
-            "kind": "oracle",
-            "sample": f"{runs} runs of batch row 0 ({w.heads} heads x {w.seqlen} tokens, first segment), "
-                      f"{el:.1f} s"}
+
+    def measure(nthreads, rows):
+        xs = {n: t[:rows] for n, t in x.items()}
+        s0 = S0[:rows] if S0 is not None else None
+        tl = (tail[0][:rows], tail[1][:rows]) if tail is not None else None
+        runs, t0 = 0, time.perf_counter()
+        while True:
+            oracle.falcon_ref_fwd(w.variant_id, xs["q"], xs["k"], xs["v"], xs["beta"], xs["lam"], s0, tl,
+                                  pos=w.pos0, window=w.window, eps=w.eps, eps_gamma=w.eps_gamma, nthreads=nthreads)
+            runs += 1
+            if time.perf_counter() - t0 > budget_s or runs >= 100000:
+                break
+        return runs * rows * w.seqlen / (time.perf_counter() - t0)
+
+    threads = min(cores, bs * w.heads)
+    vals = [measure(threads, bs) for _ in range(3)]
+    one = measure(1, 1)
+    return {"value": statistics.median(vals), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "runs": vals, "one_thread": one, "cpu_model": _cpu_model(),
+            "sample": f"batch rows 0..{bs - 1} of {w.batch} ({bs * w.heads} sequences of {w.seqlen} tokens, "
+                      f"first segment) repeated for ~{budget_s:.0f} s per measurement; median of 3 with "
+                      f"{threads} threads; one_thread: batch row 0 with 1 thread"}
 
 
 def _oracle_start(w, inp, bs):
@@ -293,10 +333,15 @@ def _e2e(args, w, host_segs, sets, launch):
 
     B, H, Ts, dv = w.batch, w.heads, w.seqlen, w.dv
     hsegs = [{n: t.pin_memory() for n, t in hs.items()} for hs in host_segs]
+    # every segment's output, and the final state and tail of the last segment (the call's result)
+    last = sets[0][w.segments - 1]
     hout = [[torch.empty((B, H, Ts, dv), dtype=w.torch_dtype).pin_memory() for _ in range(w.segments)]
             for _ in range(2)]
+    hS = [torch.empty_like(last["S"], device="cpu").pin_memory() for _ in range(2)]
+    htail = [torch.empty_like(last["tail_out"], device="cpu").pin_memory() for _ in range(2)]
     h2d_bytes = sum(t.numel() * t.element_size() for hs in hsegs for t in hs.values())
-    d2h_bytes = sum(t.numel() * t.element_size() for t in hout[0])
+    d2h_bytes = sum(t.numel() * t.element_size() for t in hout[0]) + hS[0].numel() * 4 + \
+        htail[0].numel() * htail[0].element_size()
 
     def h2d(b):
         for s in range(w.segments):
@@ -306,6 +351,8 @@ def _e2e(args, w, host_segs, sets, launch):
     def d2h(b):
         for s in range(w.segments):
             hout[b][s].copy_(sets[b][s]["out"], non_blocking=True)
+        hS[b].copy_(sets[b][w.segments - 1]["S"], non_blocking=True)
+        htail[b].copy_(sets[b][w.segments - 1]["tail_out"], non_blocking=True)
 
     ms = _pipelined_ms(max(3, min(args.steps, 50)), max(3, args.warmup), h2d, lambda b, st: launch(sets[b], st), d2h)
     return ms, h2d_bytes, d2h_bytes
@@ -331,8 +378,6 @@ def run_ours(args, w):
     dims = [F.make_dims(B, H, Ts, dk, dv, window=W, dtype=F.FALCON_F32 if w.dtype == "f32" else F.FALCON_BF16,
                         pos=w.pos0 + s * Ts, eps=w.eps, eps_gamma=w.eps_gamma) for s in range(w.segments)]
     kernel_id = F.falcon_kernel_for(w.variant_id, dims[0], w.chunk)
-    if args.single_pass and kernel_id == 3:
-        kernel_id = 2
     step_bytes = _algorithmic_bytes(w, es)
     nsets = max(2, -(-3 * L2_BYTES // step_bytes) + 1)  # rotating sets: > 3x L2 between reuses
     stream = torch.cuda.Stream(device=dev)
@@ -357,8 +402,8 @@ def run_ours(args, w):
             segs.append(d)
         sets.append(segs)
 
-    # one scratch workspace (the split path's M, U and chunk-start states), reused by every step
-    ws = F.workspace_for(w.variant_id, dims[0], w.chunk, dev) if not args.single_pass else None
+    # one scratch workspace (the scan path's chunk maps, where that path runs), reused by every step
+    ws = F.workspace_for(w.variant_id, dims[0], w.chunk, dev)
 
     def launch(segs, strm):
         for s, d in enumerate(segs):
@@ -431,11 +476,10 @@ def run_ours(args, w):
                    "parallelism": f"dp{world} (independent sequences per GPU, no collective)",
                    "l2": f"rotating {nsets} input/output sets of {step_bytes / 1e6:.1f} MB (> L2 between reuses)",
                    "pos0": w.pos0,
-                   "kernel": {1: "cuda-core chunk kernel", 2: "single-pass tcgen05/TMA chunk kernel",
-                              4: "single-token kernel",
-                              3: "split path: tcgen05/TMA prep, chain and output kernels",
+                   "kernel": {1: "cuda-core chunk kernel", 4: "single-token kernel",
                               5: "scan path: chunk maps on the cuda-core kernel, associative scan over them "
-                                 "with the outputs fused"}.get(kernel_id, "?")},
+                                 "with the outputs fused",
+                              6: "fused tcgen05/TMA kernel, one persistent CTA per sequence"}.get(kernel_id, "?")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "scope": "one falcon_fwd call (all kernels it launches); per-kernel shares in profiles/",
                      "traffic": _traffic(w.name, kernel_id), "peak_source": src,
@@ -447,6 +491,13 @@ def run_ours(args, w):
         "gpu_launches": args.steps * w.segments * _launches_per_call(w, kernel_id),
         "clocks": clk,
     }
+    fl = _chunk_flops(w)
+    if fl is not None:  # the same call against the tensor roofline (the method's own flops)
+        tf = fl / (ms_step / 1e3) / 1e12
+        line["roofline"]["tensor"] = {"achieved": tf, "peak": tfl, "unit": "TFLOP/s", "frac": tf / tfl,
+                                      "flops_per_step": fl,
+                                      "note": "chunk-algebra flops, each product once; peak = measured dense "
+                                              "bf16 (the path mixes bf16 and tf32 products)"}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)
@@ -674,7 +725,6 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--seqlen", type=int, default=None, help="override the workload's tokens per call")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
-    ap.add_argument("--single-pass", action="store_true", help="no workspace: time the single-pass kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

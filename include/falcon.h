@@ -26,15 +26,14 @@
  * A call with T = 1 (Falcon-1, 1A, 2, 2A; dk = dv = 64) runs a single-token kernel instead: the recurrent
  * form of the same update, one (batch, head) state per CTA, so a decoding step costs one read and
  * one write of the state ([PL] §3; [AH] Method).
- * Falcon-1 and 1A at bf16, dk = dv = 64, chunk 64 also have a split path that
- * uses a caller-provided workspace: every chunk's state-independent part
- * (the solve and the chunk transition S -> M S + U it implies) is computed for
- * all chunks at once, then a short scan carries the state, then every chunk's
- * reads are formed at once.
- * Falcon-1, 1A, 3 and 3A with dk = dv = 64 over few (batch, head) sequences and no split path have
- * a scan path that also uses the workspace: every chunk's affine maps of the state and of the
- * outputs, then an associative scan over the chunk maps in groups of 16 chunks ([PL] §H.1, §H.2),
- * whose last step also forms every chunk's outputs.
+ * Falcon-1 and 1A at bf16, dk = dv = 64, chunk 64 run a fused tensor-core kernel: one persistent
+ * CTA per (batch, head) sequence walks its chunks with the state on chip, the state-independent
+ * work of two chunks in flight while the state pass of an earlier one runs ([PL] §E.2: parallel
+ * per-chunk work, a short state recurrence, per-chunk reads); it needs no workspace.
+ * Falcon-1, 1A, 3 and 3A with dk = dv = 64 over few (batch, head) sequences and no fused path have
+ * a scan path that uses a caller-provided workspace: every chunk's affine maps of the state and of
+ * the outputs, then an associative scan over the chunk maps in groups of 16 chunks ([PL] §H.1,
+ * §H.2), whose last step also forms every chunk's outputs.
  *
  * Memory: every pointer argument is DEVICE memory owned by the caller; the
  * library keeps no pointer after a call returns and allocates no device memory.
@@ -102,16 +101,17 @@ typedef struct {
  *             <= 0 are zero); this is what tail_out of the previous call holds.
  *             For window 1 it is the pending key k_pos alone ([PL] §C.7, §4.4).
  *   out       [B,H,T,dv] dtype        o_t = S_t^T q_t; must not overlap any input
- *   S_final   fp32 [B,H,dk,dv] or NULL; may be the same pointer as S0
+ *   S_final   fp32 [B,H,dk,dv] or NULL; may be the same pointer as S0, must not overlap any
+ *             other argument
  *   tail_out  NULL or falcon_tail_bytes(dims) bytes: the tail for position pos+T;
- *             must not overlap tail
+ *             must not overlap any other argument
  *   dims      problem description (host pointer)
  *   chunk     chunk length C: 16, 32 or 64; FALCON_3 and 3A need chunk*window <= 128.
  *             The result does not depend on C beyond fp32 rounding.
  *   workspace NULL, or scratch device memory of at least
  *             falcon_workspace_bytes(variant, dims, chunk) bytes that overlaps no other
- *             argument. When that size is nonzero and the workspace is given, the split
- *             path runs; with NULL the single-pass kernels run (same results up to fp32
+ *             argument. When that size is nonzero and the workspace is given, the scan
+ *             path runs; with NULL the CUDA-core chunk kernel runs (same results up to fp32
  *             rounding). Contents on entry are ignored and on return unspecified; calls
  *             that may run at the same time must not share a workspace.
  *   workspace_bytes  size of `workspace` (ignored when workspace is NULL); a given
@@ -126,25 +126,27 @@ int falcon_fwd(int variant, const void* q, const void* k, const void* v, const f
                void* tail_out, const falcon_dims_t* dims, int chunk, void* workspace,
                size_t workspace_bytes, void* stream);
 
-/* Workspace bytes that enable the split path of falcon_fwd for these arguments
- * (B*H*ceil(T/64) * (66 KiB + 8 bytes) for Falcon-1/1A, bf16, dk = dv = 64, chunk 64, T > 1), or
- * the scan path (B*H*(N + ceil(N/16)) * 80 KiB with N = ceil(T/chunk), plus 4*B*H*T bytes for
- * Falcon-3; Falcon-1, 1A, 3, 3A with dk = dv = 64, B*H < 76, N >= 4, no split path); 0 when no path
- * uses a workspace or the arguments are invalid. Host only. */
+/* Workspace bytes that enable the scan path of falcon_fwd for these arguments
+ * (B*H*(N + ceil(N/16)) * 80 KiB with N = ceil(T/chunk), plus 4*B*H*T bytes for Falcon-3;
+ * Falcon-1, 1A, 3, 3A with dk = dv = 64, B*H < 76, N >= 4, no fused path); 0 when no path uses a
+ * workspace (the fused and single-token kernels need none) or the arguments are invalid. Host only. */
 size_t falcon_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk);
 
 /*
  * falcon_fwd_static — falcon_fwd with the library's own scratch instead of a caller workspace.
- * The paper has no counterpart: this is an engineering entry point for callers that must not
- * allocate (for example while building a CUDA graph). Same arguments and results as falcon_fwd
- * with a workspace. The scratch is a fixed FALCON_STATIC_WORKSPACE_BYTES device array inside the
- * library, located once per device on the first call (cudaGetSymbolAddress) and never allocated
- * or freed. Nothing in it needs zeroing: every byte a kernel reads was written earlier in the same
- * call. A shape whose split path needs more than FALCON_STATIC_WORKSPACE_BYTES returns
- * FALCON_ERR_UNSUPPORTED without launching; a shape whose scan path needs more runs the single-pass
- * kernels instead, as does a shape with neither path. Calls that may overlap in time on one device (any streams) race on the scratch and
- * must be serialized by the caller. Make the first call on each device before capturing a stream
- * into a graph, so that the one-time set-up is not inside the capture.
+ * The paper has no counterpart: this entry point is for callers that cannot allocate device memory,
+ * for example code running inside another runtime's memory pool (an extra cudaMalloc bypasses the
+ * pool's accounting and can fail under memory pressure) or a latency-critical loop that must not pay
+ * cudaMalloc's implicit device synchronisation. Same arguments and results as falcon_fwd with a
+ * workspace. The scratch is a fixed FALCON_STATIC_WORKSPACE_BYTES device array inside the library
+ * (every device that loads the library holds it until the process exits), never allocated or freed
+ * per call; every call looks up its device address (cudaGetSymbolAddress, once per device, then
+ * cached), whether or not that call uses it, so the first call on a device does that set-up.
+ * Nothing in the array needs zeroing: every byte a kernel reads was written earlier in the same call.
+ * Only the scan path uses scratch; a shape whose scan path needs more than
+ * FALCON_STATIC_WORKSPACE_BYTES runs the CUDA-core chunk kernel instead, and every other shape (the
+ * fused and single-token kernels) needs none. Calls that may overlap in time on one device (any
+ * streams) race on the scratch and must be serialized by the caller.
  */
 #define FALCON_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
 int falcon_fwd_static(int variant, const void* q, const void* k, const void* v, const float* beta,
@@ -166,11 +168,10 @@ const char* falcon_status_string(int status);
 int falcon_device_status(void* stream);
 
 /* Which kernels falcon_fwd launches for these arguments when it is given
- * falcon_workspace_bytes() of workspace (0 = none/invalid, 1 = CUDA-core chunk
- * kernel, 2 = single-pass tcgen05/TMA chunk kernel, 3 = split path: prep, chain
- * and output kernels, 4 = single-token kernel for T = 1, workspace or not, 5 = scan path:
- * chunk maps on the CUDA-core kernel, then the scan over them).
- * Without a workspace, 3 becomes 2 and 5 becomes 1. Host only, no launch. */
+ * falcon_workspace_bytes() of workspace (0 = none/invalid, 1 = CUDA-core chunk kernel,
+ * 4 = single-token kernel for T = 1, 5 = scan path: chunk maps on the CUDA-core kernel, then the
+ * scan over them, 6 = fused tensor-core kernel; 2 and 3 are retired). Without a workspace, 5
+ * becomes 1. Host only, no launch. */
 int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk);
 
 /*
@@ -210,7 +211,7 @@ int falcon_bwd(int variant, const void* q, const void* k, const void* v, const f
  * state and the chunk-end adjoint, each 64 x 64 fp32); 0 for invalid or unsupported arguments. */
 size_t falcon_bwd_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk);
 
-/* ABI version of this header: 3. */
+/* ABI version of this header: 4. */
 int falcon_abi_version(void);
 
 #ifdef __cplusplus

@@ -7,8 +7,7 @@ from weight_linear_attention_gb300 import inputs as I
 
 def test_launches_per_call():
     W = I.WORKLOADS
-    assert bench._launches_per_call(W["f1_b8h12t1024_bf16"], 3) == 3          # split path
-    assert bench._launches_per_call(W["f1_b8h12t1024_bf16"], 2) == 1          # single pass
+    assert bench._launches_per_call(W["f1_b8h12t1024_bf16"], 6) == 1          # fused kernel
     # scan path, Falcon-3 at 8192 tokens per call, chunk 32: normalisers, maps, compose, groups, apply
     assert bench._launches_per_call(W["f3w4_b2h12t16384_bf16"], 5) == 5
     assert bench._launches_per_call(W["f3aw4_b2h12t16384_bf16"], 5) == 4     # no normaliser pass
@@ -33,3 +32,12 @@ def test_backward_counts():
     expect = tok * 4 * 64 * 2 + tok * 8 + tok * 3 * 64 * 4 + tok * 8 + 2 * 96 * 64 * 64 * 4
     assert bench._bwd_bytes(w, 2) == expect
 
+
+def test_chunk_flops():
+    # Falcon-1 at the 130M shape: per chunk-head 2 (4 C^2 d + 2 C d^2 + C^2 d / 2) with C = d = 64
+    w = I.WORKLOADS["f1_b8h12t1024_bf16"]
+    per = 2 * (4 * 64 ** 3 + 2 * 64 ** 3 + 64 ** 3 / 2)
+    assert bench._chunk_flops(w) == per * 96 * 16
+    assert abs(bench._chunk_flops(w) - 5.2e9) < 0.1e9  # the survey's ~5.2 GFLOP for this config
+    assert bench._chunk_flops(I.WORKLOADS["f1a_b8h12t1024_bf16"]) == 2 * 4 * 64 ** 3 * 96 * 16
+    assert bench._chunk_flops(I.WORKLOADS["f2_b8h12t2048_bf16"]) is None

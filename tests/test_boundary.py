@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(names) == set(F.EXPORTED), names
     for n in names:
         assert hasattr(lib, n), n
-    assert F.falcon_abi_version() == 3
+    assert F.falcon_abi_version() == 4
 
 
 def test_dims_struct_layout():
@@ -137,9 +137,9 @@ def test_unsupported_and_invalid_shapes(lib):
 
 
 @pytest.mark.parametrize("case,expect", [
-    (dict(), 3),                                           # Falcon-1, bf16, 64, chunk 64: split path
-    (dict(variant=F.FALCON_1A), 3),
-    (dict(variant=F.FALCON_1, seqlen=0), 1),          # nothing to split: no workspace, CUDA-core kernel
+    (dict(), 6),                                           # Falcon-1, bf16, 64, chunk 64: fused kernel
+    (dict(variant=F.FALCON_1A), 6),
+    (dict(variant=F.FALCON_1, seqlen=0), 6),          # no tokens: the fused kernel still writes S_final, tail
     (dict(chunk=32), 1),
     (dict(dtype=F.FALCON_F32), 1),
     (dict(variant=F.FALCON_2), 1),
@@ -148,7 +148,7 @@ def test_unsupported_and_invalid_shapes(lib):
     (dict(seqlen=1, variant=F.FALCON_1A, dtype=F.FALCON_F32), 4),
     (dict(seqlen=1, variant=F.FALCON_2), 4),
     (dict(seqlen=1, dk=32, dv=32), 1),
-    (dict(seqlen=2), 3),
+    (dict(seqlen=2), 6),
     (dict(variant=F.FALCON_2A), 1),                      # inner-product variants: CUDA-core kernel
     (dict(variant=F.FALCON_2A, seqlen=1), 4),            # ... and the single-token kernel for 2A
 ])
@@ -160,10 +160,9 @@ def test_kernel_choice(lib, case, expect):
 
 
 def test_workspace_bytes(lib):
-    # B*H*ceil(T/64) chunks of 66 KiB + 8 bytes: M (hi, lo), U, the chunk-start state (hi, lo), T (hi, lo),
-    # scalars, and the 8-byte flag the chain kernel waits on
-    assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(8, 12, 1024, 64, 64), 64) == 8 * 12 * 16 * 67592
-    assert F.falcon_workspace_bytes(F.FALCON_1A, F.make_dims(2, 3, 65, 64, 64), 64) == 2 * 3 * 2 * 67592
+    # the fused kernel (Falcon-1 / 1A, bf16, 64, chunk 64) keeps everything on chip: no workspace
+    assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(8, 12, 1024, 64, 64), 64) == 0
+    assert F.falcon_workspace_bytes(F.FALCON_1A, F.make_dims(2, 3, 65, 64, 64), 64) == 0
     assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 0, 64, 64), 64) == 0
     assert F.falcon_workspace_bytes(F.FALCON_2, F.make_dims(2, 3, 64, 64, 64), 64) == 0
     assert F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 64, 64, 64, dtype=F.FALCON_F32), 64) == 0
@@ -173,14 +172,32 @@ def test_workspace_bytes(lib):
 
 
 def test_workspace_checks(lib):
-    need = F.falcon_workspace_bytes(F.FALCON_1, F.make_dims(2, 2, 64, 64, 64), 64)
+    # Falcon-1 at chunk 32 over 4 sequences of 256 tokens: the scan path, which uses a workspace
+    d = F.make_dims(2, 2, 256, 64, 64)
+    need = F.falcon_workspace_bytes(F.FALCON_1, d, 32)
+    assert need > 0
     W = A + (9 << 30)
-    assert _call(ws=W, ws_bytes=need - 1) == F.FALCON_ERR_INVALID_ARG      # too small
-    assert _call(ws=W + 128, ws_bytes=need) == F.FALCON_ERR_MISALIGNED    # 256-byte alignment
-    assert _call(ws=A + 4096, ws_bytes=need) == F.FALCON_ERR_INVALID_ARG   # overlaps q
-    assert _call(ws=A + (5 << 30) - 4096, ws_bytes=need) == F.FALCON_ERR_INVALID_ARG  # runs into out
+    assert _call(dims=d, chunk=32, ws=W, ws_bytes=need - 1) == F.FALCON_ERR_INVALID_ARG      # too small
+    assert _call(dims=d, chunk=32, ws=W + 128, ws_bytes=need) == F.FALCON_ERR_MISALIGNED    # 256-byte alignment
+    assert _call(dims=d, chunk=32, ws=A + 4096, ws_bytes=need) == F.FALCON_ERR_INVALID_ARG   # overlaps q
+    assert _call(dims=d, chunk=32, ws=A + (5 << 30) - 4096, ws_bytes=need) == F.FALCON_ERR_INVALID_ARG  # runs into out
     # a well-formed workspace with an otherwise invalid call is still rejected before any launch
-    assert _call(ws=W, ws_bytes=need, chunk=24) == F.FALCON_ERR_UNSUPPORTED
+    assert _call(dims=d, chunk=24, ws=W, ws_bytes=need) == F.FALCON_ERR_UNSUPPORTED
+
+
+def test_written_buffers_must_not_overlap_anything(lib):
+    # S_final and tail_out, like out, may overlap no input and no other written buffer (S_final may
+    # only equal S0 exactly: an in-place state update)
+    d = F.make_dims(2, 2, 64, 64, 64, pos=3)
+    tl = A + (7 << 30)
+    assert _call(S_final=A + 4096) == F.FALCON_ERR_INVALID_ARG                       # inside q
+    assert _call(S_final=A + (4 << 30)) == F.FALCON_ERR_INVALID_ARG                  # on lambda
+    assert _call(S_final=A + (5 << 30) + 256) == F.FALCON_ERR_INVALID_ARG            # inside out
+    assert _call(S0=A + (6 << 30), S_final=A + (6 << 30) + 64) == F.FALCON_ERR_INVALID_ARG  # shifted onto S0
+    assert _call(dims=d, tail=tl, tail_out=A + (1 << 30)) == F.FALCON_ERR_INVALID_ARG  # on k
+    assert _call(dims=d, tail=tl, tail_out=A + (5 << 30)) == F.FALCON_ERR_INVALID_ARG  # on out
+    assert _call(dims=d, tail=tl, S_final=A + (8 << 30), tail_out=A + (8 << 30) + 512) == F.FALCON_ERR_INVALID_ARG
+    assert _call(dims=d, tail=tl, S0=A + (8 << 30), tail_out=A + (8 << 30)) == F.FALCON_ERR_INVALID_ARG  # on S0
 
 
 def test_binding_raises_when_library_missing(tmp_path):
@@ -247,5 +264,5 @@ def test_scan_path_choice(lib):
     assert F.falcon_kernel_for(F.FALCON_2, F.make_dims(2, 12, 8192, 64, 64), 64) == 1  # per-column maps: no
     assert F.falcon_kernel_for(F.FALCON_3, F.make_dims(8, 12, 8192, 64, 64, window=4), 32) == 1  # many sequences
     assert F.falcon_kernel_for(F.FALCON_3, F.make_dims(2, 12, 64, 64, 64, window=4), 32) == 1  # two chunks
-    assert F.falcon_kernel_for(F.FALCON_1, F.make_dims(2, 12, 8192, 64, 64), 64) == 3  # bf16 chunk 64: split
+    assert F.falcon_kernel_for(F.FALCON_1, F.make_dims(2, 12, 8192, 64, 64), 64) == 6  # bf16 chunk 64: fused
     assert F.falcon_kernel_for(F.FALCON_1, F.make_dims(2, 12, 8192, 64, 64), 32) == 5

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.gpu_util import rel_err, run_oracle, slice_inputs, tol
+from tests.gpu_util import check, rel_err, run_oracle, slice_inputs, tol
 from weight_linear_attention_gb300 import falcon as F
 from weight_linear_attention_gb300 import inputs as I
 
@@ -21,9 +21,7 @@ def _inputs(variant, dtype, seqlen, batch=3, seed=21):
 
 
 def _check(name, got, ref, dtype):
-    quant = got.dtype == torch.bfloat16
-    e = rel_err(got.float().numpy(), ref, dtype, quantized_bf16=quant)
-    assert np.isfinite(e) and e <= tol(dtype), f"{name}: rel err {e:.3e} > {tol(dtype):.1e}"
+    check(name, got, ref, dtype)
 
 
 def _step(variant, inp, t, dims_pos, S, tail, dt, inplace=False):

@@ -1,19 +1,19 @@
-"""GPU parity of the two tensor-core paths for Falcon-1 / 1A (bf16, dk = dv = 64, chunk 64):
-the split path (prep, chain and output kernels with a workspace) and the single-pass kernel.
+"""GPU parity of the fused tensor-core kernel (Falcon-1 / 1A, bf16, dk = dv = 64, chunk 64): one
+persistent CTA per sequence, state on chip.
 
-Every case runs through the C ABI on both paths and is compared with the fp64 oracle at the
-bf16 bound (max|gpu - ref| / RMS(ref) <= 2e-2, output rounding excluded), covering the branches
-those kernels have and the generic-kernel tests do not reach at chunk 64: a nonzero and an
-aliased initial state, the clamp (total log decay of a chunk below -30, so every factor is
-formed by its own exp), continuation from a tail at every kind of split point, and lengths
-around the chunk boundary.
+Every case runs through the C ABI and is compared with the fp64 oracle at the bf16 bound (both
+checks of tests.gpu_util.check), covering the branches that kernel has: a nonzero and an aliased
+initial state, the clamp (total log decay of a chunk below -30, so every factor is formed by its
+own exp) and chunks where fast and exact exponential forms alternate, continuation from a tail at
+every kind of split point, lengths around the chunk boundary, odd sequence counts, and the
+headline shape.
 """
 
 import numpy as np
 import pytest
 import torch
 
-from tests.gpu_util import rel_err, run_gpu, run_oracle, slice_inputs, tol
+from tests.gpu_util import check, run_gpu, run_oracle, slice_inputs
 from weight_linear_attention_gb300 import falcon as F
 from weight_linear_attention_gb300 import inputs as I
 
@@ -21,7 +21,6 @@ pytestmark = pytest.mark.gpu
 
 F1, F1A = 1, 2
 HEAD = I.HEADLINE
-PATHS = [pytest.param(True, id="split"), pytest.param(False, id="single")]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,50 +34,40 @@ def _lib():
 
 
 def _check(name, gpu, ref, bound=None):
-    quant = gpu.dtype == torch.bfloat16
-    e = rel_err(gpu.float().numpy(), ref, torch.bfloat16, quantized_bf16=quant)
-    b = tol(torch.bfloat16) if bound is None else bound
-    print(f"PARITY {name}: err {e:.3e} bound {b:.1e}")
-    assert np.isfinite(e) and e <= b, f"{name}: rel err {e:.3e} > {b:.1e}"
+    check(name, gpu, ref, torch.bfloat16, bound)
 
 
 def _wl(variant, **kw):
     return I.WORKLOADS[HEAD].with_(variant="falcon1" if variant == F1 else "falcon1a", **kw)
 
 
-def _both(variant, inp, split, name, S0=None, pos=0, tail=None, eps_gamma=1e-6):
+def _fused(variant, inp, S0=None, pos=0, tail=None, eps_gamma=1e-6):
     dims = F.make_dims(*inp["q"].shape[:3], 64, 64, dtype=F.FALCON_BF16, pos=pos)
-    expect = 3 if split else 2
-    if inp["q"].shape[2] == 1:  # one token: the single-token kernel, with or without a workspace
-        assert F.falcon_kernel_for(variant, dims, 64) == 4
-    elif inp["q"].shape[2] > 0:
-        assert (F.falcon_kernel_for(variant, dims, 64) if split else 2) == expect
-    out, S, t = run_gpu(variant, inp, chunk=64, S0=S0, pos=pos, tail=tail, eps_gamma=eps_gamma, split=split)
-    return out, S, t
+    T = inp["q"].shape[2]
+    assert F.falcon_kernel_for(variant, dims, 64) == (4 if T == 1 else 6)
+    assert F.falcon_workspace_bytes(variant, dims, 64) == 0
+    return run_gpu(variant, inp, chunk=64, S0=S0, pos=pos, tail=tail, eps_gamma=eps_gamma)
 
 
-@pytest.mark.parametrize("split", PATHS)
 @pytest.mark.parametrize("variant", [F1, F1A])
-def test_nonzero_initial_state(variant, split):
+def test_nonzero_initial_state(variant):
     w = _wl(variant, nonzero_s0=True)
     inp = I.make_inputs(w, seed=21, seqlen=200, batch=2)
-    out, S, _ = _both(variant, inp, split, "S0", S0=inp["S0"])
+    out, S, _ = _fused(variant, inp, S0=inp["S0"])
     r_out, r_S, _ = run_oracle(variant, inp, S0=inp["S0"])
     _check(f"v{variant} S0 out", out, r_out)
     _check(f"v{variant} S0 S", S, r_S)
 
 
-@pytest.mark.parametrize("split", PATHS)
 @pytest.mark.parametrize("variant", [F1, F1A])
-def test_S_final_may_alias_S0(variant, split):
+def test_S_final_may_alias_S0(variant):
     w = _wl(variant, nonzero_s0=True)
     inp = I.make_inputs(w, seed=22, seqlen=130, batch=2)
     dev = {n: inp[n].cuda() for n in ("q", "k", "v", "beta", "lam")}
     S = inp["S0"].cuda().contiguous()
     out = torch.empty_like(dev["v"])
     d = F.make_dims(2, 12, 130, 64, 64, dtype=F.FALCON_BF16)
-    ws = F.workspace_for(variant, d, 64, "cuda") if split else None
-    st = F.falcon_fwd(variant, dev["q"], dev["k"], dev["v"], dev["beta"], dev["lam"], S, None, out, S, None, d, 64, ws)
+    st = F.falcon_fwd(variant, dev["q"], dev["k"], dev["v"], dev["beta"], dev["lam"], S, None, out, S, None, d, 64)
     assert st == 0
     torch.cuda.synchronize()
     assert F.falcon_device_status() == F.FALCON_OK
@@ -87,43 +76,40 @@ def test_S_final_may_alias_S0(variant, split):
     _check("alias S", S.cpu(), r_S)
 
 
-@pytest.mark.parametrize("split", PATHS)
 @pytest.mark.parametrize("variant", [F1, F1A])
-def test_clamp_stress(variant, split):
+def test_clamp_stress(variant):
     """beta = 1.5, lambda = 1000: alpha = 1 - eps_gamma on every step, log decay ~ -13.8 per token."""
     w = _wl(variant, lam_const=1000.0, lam_shift=None)
     inp = I.make_inputs(w, seed=23, seqlen=150, batch=1)
     inp["beta"] = torch.full_like(inp["beta"], 1.5)
-    out, S, _ = _both(variant, inp, split, "clamp")
+    out, S, _ = _fused(variant, inp)
     r_out, r_S, _ = run_oracle(variant, inp)
     _check(f"clamp v{variant} out", out, r_out)
     _check(f"clamp v{variant} S", S, r_S)
 
 
-@pytest.mark.parametrize("split", PATHS)
 @pytest.mark.parametrize("variant", [F1, F1A])
-def test_mixed_decay_chunks(variant, split):
+def test_mixed_decay_chunks(variant):
     """Strong decay in some chunks only: the fast and the exact exp forms alternate across chunks."""
     w = _wl(variant)
     inp = I.make_inputs(w, seed=24, seqlen=256, batch=1)
     inp["lam"][:, :, 64:128] = 1000.0
     inp["lam"][:, :, 200:210] = 50.0
-    out, S, _ = _both(variant, inp, split, "mixed")
+    out, S, _ = _fused(variant, inp)
     r_out, r_S, _ = run_oracle(variant, inp)
     _check(f"mixed v{variant} out", out, r_out)
     _check(f"mixed v{variant} S", S, r_S)
 
 
-@pytest.mark.parametrize("split", PATHS)
 @pytest.mark.parametrize("variant,cut", [(F1, 1), (F1, 63), (F1, 64), (F1, 100), (F1A, 64), (F1A, 77)])
-def test_segment_continuation(variant, cut, split):
+def test_segment_continuation(variant, cut):
     """Two calls carrying S_final and the tail (pos > 0: the first shifted key comes from the tail)."""
     w = _wl(variant)
     T = 200
     inp = I.make_inputs(w, seed=25, seqlen=T, batch=2)
     a, b = slice_inputs(inp, 0, cut), slice_inputs(inp, cut, T)
-    o1, S1, t1 = run_gpu(variant, a, chunk=64, split=split)
-    o2, S2, t2 = run_gpu(variant, b, chunk=64, pos=cut, S0=S1, tail=t1, split=split)
+    o1, S1, t1 = run_gpu(variant, a, chunk=64)
+    o2, S2, t2 = run_gpu(variant, b, chunk=64, pos=cut, S0=S1, tail=t1)
     ro, rS, rt = run_oracle(variant, inp)
     _check("cont out", torch.cat([o1, o2], dim=2), ro)
     _check("cont S", S2, rS)
@@ -131,12 +117,11 @@ def test_segment_continuation(variant, cut, split):
     np.testing.assert_array_equal(tk.double().numpy(), rt[0])
 
 
-@pytest.mark.parametrize("split", PATHS)
 @pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 128, 129, 1000])
-def test_lengths(T, split):
+def test_lengths(T):
     w = I.WORKLOADS[HEAD]
     inp = I.make_inputs(w, seed=26, seqlen=T, batch=1)
-    out, S, t = _both(F1, inp, split, "len")
+    out, S, t = _fused(F1, inp)
     r_out, r_S, rt = run_oracle(F1, inp)
     _check(f"T={T} out", out, r_out)
     _check(f"T={T} S", S, r_S)
@@ -144,26 +129,25 @@ def test_lengths(T, split):
 
 
 @pytest.mark.parametrize("variant", [F1, F1A])
-def test_both_paths_headline_shape(variant):
-    """Both paths at the headline shape (2 x 12 x 1024) against the oracle."""
+def test_headline_shape_two_batch_rows(variant):
+    """The headline shape's sequences (2 x 12 x 1024) against the oracle, every sequence compared."""
     w = _wl(variant)
     inp = I.make_inputs(w, seed=27, seqlen=1024, batch=2)
     r_out, r_S, _ = run_oracle(variant, inp)
-    for split in (True, False):
-        o, S, _ = run_gpu(variant, inp, split=split)
-        _check(f"{'split' if split else 'single'} out", o, r_out)
-        _check(f"{'split' if split else 'single'} S", S, r_S)
+    o, S, _ = _fused(variant, inp)
+    _check("headline rows out", o, r_out)
+    _check("headline rows S", S, r_S)
 
 
-def test_bad_workspace_call_leaves_outputs():
+def test_rejected_call_leaves_outputs():
     w = I.WORKLOADS[HEAD]
     inp = I.make_inputs(w, seed=28, seqlen=64, batch=1)
     dev = {n: inp[n].cuda() for n in ("q", "k", "v", "beta", "lam")}
     out = torch.full_like(dev["v"], 7.0)
     d = F.make_dims(1, 12, 64, 64, 64, dtype=F.FALCON_BF16)
-    ws = F.workspace_for(F1, d, 64, "cuda")
-    st = F.falcon_fwd(F1, dev["q"], dev["k"], dev["v"], dev["beta"], dev["lam"], None, None, out, None, None, d, 64,
-                      ws, ws.numel() - 256)
+    # S_final over lambda: rejected before any launch
+    st = F.falcon_fwd(F1, dev["q"], dev["k"], dev["v"], dev["beta"], dev["lam"], None, None, out,
+                      dev["lam"].data_ptr(), None, d, 64)
     assert st == F.FALCON_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(out == 7.0)

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.gpu_util import rel_err, run_gpu, run_oracle, slice_inputs, tol
+from tests.gpu_util import check, run_gpu, run_oracle, slice_inputs
 from weight_linear_attention_gb300 import falcon as F
 from weight_linear_attention_gb300 import inputs as I
 
@@ -32,14 +32,7 @@ def _lib():
 
 
 def _check(name, gpu, ref, dtype, bound=None):
-    quant = hasattr(gpu, "dtype") and gpu.dtype == torch.bfloat16
-    g = gpu.float().numpy() if hasattr(gpu, "numpy") else gpu
-    e = rel_err(g, ref, dtype, quantized_bf16=quant)
-    raw = rel_err(g, ref, dtype)
-    b = tol(dtype) if bound is None else bound
-    print(f"PARITY {name}: err {e:.3e} (raw {raw:.3e}) bound {b:.1e}")
-    assert np.isfinite(e) and e <= b, f"{name}: rel err {e:.3e} (raw {raw:.3e}) > {b:.1e}"
-    return e
+    return check(name, gpu, ref, dtype, bound)
 
 
 def _parity(w: I.Workload, inp, *, chunk=None, S0=None, name=""):

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.gpu_util import rel_err, run_gpu, run_oracle, slice_inputs, tol
+from tests.gpu_util import check, rel_err, run_gpu, run_oracle, slice_inputs, tol
 from weight_linear_attention_gb300 import falcon as F
 from weight_linear_attention_gb300 import inputs as I
 
@@ -36,10 +36,7 @@ def _wl(variant, dtype, **kw):
 
 
 def _check(name, gpu, ref, dtype):
-    quant = gpu.dtype == torch.bfloat16
-    e = rel_err(gpu.float().numpy(), ref, dtype, quantized_bf16=quant)
-    print(f"PARITY {name}: err {e:.3e} bound {tol(dtype):.1e}")
-    assert np.isfinite(e) and e <= tol(dtype), f"{name}: {e:.3e}"
+    check(name, gpu, ref, dtype)
 
 
 def _run(w, inp, chunk, S0=None, pos=0, tail=None, rtail=None, name=""):

@@ -48,16 +48,15 @@ size_t tail_bytes_of(const falcon_dims_t* d) {
     return (size_t)d->batch * (size_t)d->heads * per * es;
 }
 
-// Shape/variant/dtype/chunk checks (no pointers). Fills the size fields of `a`.
-// Workspace bytes a call with these (validated) arguments can use: the split path's, unless the
-// single-token kernel runs.
+// Workspace bytes a call with these (validated) arguments can use: the scan path's; 0 for the
+// single-token and fused kernels, which need none.
 size_t workspace_need(const falcon::Launch& a) {
-    if (falcon::decode_supported(a)) return 0;
-    if (falcon::split_supported(a)) return falcon::split_workspace_bytes(a);
+    if (falcon::decode_supported(a) || falcon::fused_supported(a)) return 0;
     if (falcon::scan_supported(a)) return falcon::scan_workspace_bytes(a);
     return 0;
 }
 
+// Shape/variant/dtype/chunk checks (no pointers). Fills the size fields of `a`.
 int validate_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail, falcon::Launch* a) {
     if (!d) return FALCON_ERR_INVALID_ARG;
     if (variant < FALCON_1 || variant > FALCON_3A) return FALCON_ERR_INVALID_ARG;
@@ -85,7 +84,8 @@ int validate_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail
     a->eps = d->eps;
     a->eps_gamma = d->eps_gamma;
     a->chunk = chunk;
-    if (falcon::generic_smem_bytes(*a, 16, false) > 200 * 1024 && !falcon::tc_supported(*a)) return FALCON_ERR_UNSUPPORTED;
+    if (falcon::generic_smem_bytes(*a, 16, false) > 200 * 1024 && !falcon::fused_supported(*a))
+        return FALCON_ERR_UNSUPPORTED;
     return FALCON_OK;
 }
 
@@ -108,41 +108,33 @@ int validate(int variant, const void* q, const void* k, const void* v, const flo
     const size_t ws_need = workspace_need(*a);
     if (ws && ws_need > 0 && ws_bytes < ws_need) return FALCON_ERR_INVALID_ARG;
 
-    // out must not overlap any input; tail_out must not overlap tail; S_final may equal S0 exactly.
-    if (tokens > 0) {
-        const Range ro = range_of(out, (size_t)tokens * d->dv * es);
+    // Every written buffer (out, S_final, tail_out and a used workspace) overlaps no input and no other
+    // written buffer; the one exception is S_final equal to S0 exactly (an in-place state update).
+    {
         const size_t bcols = (variant == FALCON_2 || variant == FALCON_2A) ? (size_t)d->dv : 1;
+        const size_t sbytes = (size_t)BH * d->dk * d->dv * 4;
         const Range ins[] = {
             range_of(q, (size_t)tokens * d->dk * es), range_of(k, (size_t)tokens * d->dk * es),
             range_of(v, (size_t)tokens * d->dv * es), range_of(beta, (size_t)tokens * bcols * 4),
             range_of(lambda, (size_t)tokens * 4),
-            S0 ? range_of(S0, (size_t)BH * d->dk * d->dv * 4) : Range{0, 0},
+            S0 ? range_of(S0, sbytes) : Range{0, 0},
             tail ? range_of(tail, tail_bytes_of(d)) : Range{0, 0},
-            S_final ? range_of(S_final, (size_t)BH * d->dk * d->dv * 4) : Range{0, 0},
-            tail_out ? range_of(tail_out, tail_bytes_of(d)) : Range{0, 0},
         };
-        for (const Range& r : ins)
-            if (overlaps(ro, r)) return FALCON_ERR_INVALID_ARG;
-    }
-    if (tail && tail_out && overlaps(range_of(tail, tail_bytes_of(d)), range_of(tail_out, tail_bytes_of(d))))
-        return FALCON_ERR_INVALID_ARG;
-    if (S0 && S_final && S0 != S_final &&
-        overlaps(range_of(S0, (size_t)BH * d->dk * d->dv * 4), range_of(S_final, (size_t)BH * d->dk * d->dv * 4)))
-        return FALCON_ERR_INVALID_ARG;
-    if (ws && ws_need > 0) {  // the workspace is written by the kernels: it may overlap nothing
-        const size_t bcols = (variant == FALCON_2 || variant == FALCON_2A) ? (size_t)d->dv : 1;
-        const Range rw = range_of(ws, ws_need);
-        const Range all[] = {
-            range_of(q, (size_t)tokens * d->dk * es), range_of(k, (size_t)tokens * d->dk * es),
-            range_of(v, (size_t)tokens * d->dv * es), range_of(beta, (size_t)tokens * bcols * 4),
-            range_of(lambda, (size_t)tokens * 4), range_of(out, (size_t)tokens * d->dv * es),
-            S0 ? range_of(S0, (size_t)BH * d->dk * d->dv * 4) : Range{0, 0},
-            S_final ? range_of(S_final, (size_t)BH * d->dk * d->dv * 4) : Range{0, 0},
-            tail ? range_of(tail, tail_bytes_of(d)) : Range{0, 0},
+        const Range outs[] = {
+            tokens > 0 ? range_of(out, (size_t)tokens * d->dv * es) : Range{0, 0},
+            S_final ? range_of(S_final, sbytes) : Range{0, 0},
             tail_out ? range_of(tail_out, tail_bytes_of(d)) : Range{0, 0},
+            ws && ws_need > 0 ? range_of(ws, ws_need) : Range{0, 0},
         };
-        for (const Range& r : all)
-            if (overlaps(rw, r)) return FALCON_ERR_INVALID_ARG;
+        const int ni = (int)(sizeof(ins) / sizeof(ins[0])), no = (int)(sizeof(outs) / sizeof(outs[0]));
+        for (int o = 0; o < no; ++o) {
+            for (int i = 0; i < ni; ++i) {
+                const bool in_place = o == 1 && i == 5 && S0 == S_final;
+                if (!in_place && overlaps(outs[o], ins[i])) return FALCON_ERR_INVALID_ARG;
+            }
+            for (int o2 = o + 1; o2 < no; ++o2)
+                if (overlaps(outs[o], outs[o2])) return FALCON_ERR_INVALID_ARG;
+        }
     }
 
     a->q = q;
@@ -160,6 +152,15 @@ int validate(int variant, const void* q, const void* k, const void* v, const flo
     return FALCON_OK;
 }
 
+// Launch the kernels for validated arguments (a.ws set only when a path uses it).
+int dispatch(const falcon::Launch& a, cudaStream_t s) {
+    if (a.B * a.H == 0) return FALCON_OK;
+    if (falcon::decode_supported(a)) return falcon::launch_decode(a, s);
+    if (falcon::fused_supported(a)) return falcon::launch_fused(a, s);
+    if (a.ws) return falcon::launch_scan(a, s);
+    return falcon::launch_generic(a, s);
+}
+
 // Shape checks of falcon_bwd on top of validate_shape.
 int validate_bwd_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail, falcon::Launch* a) {
     const int st = validate_shape(variant, d, chunk, has_tail, a);
@@ -171,7 +172,7 @@ int validate_bwd_shape(int variant, const falcon_dims_t* d, int chunk, bool has_
 
 extern "C" {
 
-int falcon_abi_version(void) { return 3; }
+int falcon_abi_version(void) { return 4; }
 
 size_t falcon_tail_bytes(const falcon_dims_t* d) {
     if (!d || d->batch < 0 || d->heads < 0 || d->dk <= 0 || d->dv <= 0 || d->window < 1) return 0;
@@ -194,9 +195,9 @@ int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk) {
     falcon::Launch a = {};
     if (validate_shape(variant, dims, chunk, dims && dims->pos > 0, &a) != FALCON_OK) return 0;
     if (falcon::decode_supported(a)) return 4;
-    if (falcon::split_supported(a) && falcon::split_workspace_bytes(a) > 0) return 3;
+    if (falcon::fused_supported(a)) return 6;
     if (falcon::scan_supported(a)) return 5;
-    return falcon::tc_supported(a) ? 2 : 1;
+    return 1;
 }
 
 size_t falcon_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk) {
@@ -212,29 +213,28 @@ int falcon_fwd(int variant, const void* q, const void* k, const void* v, const f
     const int st = validate(variant, q, k, v, beta, lambda, S0, tail, out, S_final, tail_out, dims, chunk, workspace,
                             workspace_bytes, &a);
     if (st != FALCON_OK) return st;
-    if (a.B * a.H == 0) return FALCON_OK;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (falcon::decode_supported(a)) return falcon::launch_decode(a, s);
-    if (a.ws) return falcon::split_supported(a) ? falcon::launch_split(a, s) : falcon::launch_scan(a, s);
-    if (falcon::tc_supported(a)) return falcon::launch_tc(a, s);
-    return falcon::launch_generic(a, s);
+    return dispatch(a, static_cast<cudaStream_t>(stream));
 }
 
 int falcon_fwd_static(int variant, const void* q, const void* k, const void* v, const float* beta,
                       const float* lambda, const float* S0, const void* tail, void* out, float* S_final,
                       void* tail_out, const falcon_dims_t* dims, int chunk, void* stream) {
-    falcon::Launch shape = {};
-    const int st = validate_shape(variant, dims, chunk, tail != nullptr, &shape);
+    // Every argument is checked as falcon_fwd checks it (without a caller workspace: the library's array
+    // overlaps no caller buffer), before anything touches the device.
+    falcon::Launch a = {};
+    const int st = validate(variant, q, k, v, beta, lambda, S0, tail, out, S_final, tail_out, dims, chunk, nullptr,
+                            0, &a);
     if (st != FALCON_OK) return st;
-    size_t need = workspace_need(shape);
-    if (need > FALCON_STATIC_WORKSPACE_BYTES) {
-        if (falcon::split_supported(shape)) return FALCON_ERR_UNSUPPORTED;
-        need = 0;  // the scan path does not fit: the single-pass kernels run
+    // The array's device address is looked up on every call (once per device, then cached), whether or
+    // not this call uses it, so that the first call on a device always does the set-up.
+    void* const scratch = static_workspace_address();
+    if (!scratch) return FALCON_ERR_CUDA;
+    const size_t need = workspace_need(a);
+    if (need > 0 && need <= FALCON_STATIC_WORKSPACE_BYTES) {  // else the CUDA-core chunk kernel runs
+        a.ws = scratch;
+        a.ws_bytes = FALCON_STATIC_WORKSPACE_BYTES;
     }
-    void* ws = nullptr;
-    if (need > 0 && !(ws = static_workspace_address())) return FALCON_ERR_CUDA;
-    return falcon_fwd(variant, q, k, v, beta, lambda, S0, tail, out, S_final, tail_out, dims, chunk, ws,
-                      ws ? FALCON_STATIC_WORKSPACE_BYTES : 0, stream);
+    return dispatch(a, static_cast<cudaStream_t>(stream));
 }
 
 size_t falcon_bwd_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk) {
@@ -304,10 +304,9 @@ int falcon_bwd(int variant, const void* q, const void* k, const void* v, const f
 
 int falcon_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FALCON_ERR_CUDA;
-    int f1 = 0, f2 = 0;
-    if (falcon::tc_consume_timeout_flag(&f1) != 0 || falcon::split_consume_timeout_flag(&f2) != 0)
-        return FALCON_ERR_CUDA;
-    return f1 || f2 ? FALCON_ERR_DEVICE_TIMEOUT : FALCON_OK;
+    int f = 0;
+    if (falcon::fused_consume_timeout_flag(&f) != 0) return FALCON_ERR_CUDA;
+    return f ? FALCON_ERR_DEVICE_TIMEOUT : FALCON_OK;
 }
 
 }  // extern "C"

@@ -45,24 +45,18 @@ int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const
 int launch_window_mu(const Launch& a, float* mu, cudaStream_t stream);
 size_t generic_smem_bytes(const Launch& a, int dvs, bool staged = true);  // staged: mode 0's copy-ahead area
 
-// tcgen05 / TMA chunk kernel (Falcon-1 and 1A, bf16, dk = dv = 64, chunk 64).
-bool tc_supported(const Launch& a);
-int launch_tc(const Launch& a, cudaStream_t stream);
-// Reads and clears the device-side timeout flag of the tcgen05 kernel (synchronous).
-int tc_consume_timeout_flag(int* flag);
-
-// Split path (Falcon-1 and 1A, bf16, dk = dv = 64, chunk 64): prep, chain and output kernels
-// working through a caller workspace of split_workspace_bytes(a) bytes at a.ws.
-bool split_supported(const Launch& a);
-size_t split_workspace_bytes(const Launch& a);
-int launch_split(const Launch& a, cudaStream_t stream);
-int split_consume_timeout_flag(int* flag);
+// Fused path (Falcon-1 and 1A, bf16, dk = dv = 64, chunk 64, T != 1): one persistent CTA per
+// sequence, TMA + tcgen05, state on chip; no workspace.
+bool fused_supported(const Launch& a);
+int launch_fused(const Launch& a, cudaStream_t stream);
+// Reads and clears the device-side timeout flag of the fused kernel (synchronous).
+int fused_consume_timeout_flag(int* flag);
 
 // Single-token step (T = 1; Falcon-1, 1A, 2 and 2A; dk = dv = 64): one CTA per (batch, head) state.
 bool decode_supported(const Launch& a);
 int launch_decode(const Launch& a, cudaStream_t stream);
 
-// Scan path (Falcon-1, 1A, 3, 3A with dk = dv = 64, few sequences, no split path): chunk maps,
+// Scan path (Falcon-1, 1A, 3, 3A with dk = dv = 64, few sequences, no fused path): chunk maps,
 // an associative scan over them, then the chunks' outputs, through a caller workspace.
 bool scan_supported(const Launch& a);
 size_t scan_workspace_bytes(const Launch& a);

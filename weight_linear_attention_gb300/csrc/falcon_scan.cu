@@ -199,7 +199,7 @@ bool scan_supported(const Launch& a) {
     const bool shared = a.variant == kF1 || a.variant == kF1A || a.variant == kF3 || a.variant == kF3A;
     const long long N = (a.T + a.chunk - 1) / a.chunk;
     // few sequences (the one-CTA-per-slice kernel would leave SMs idle) and enough chunks to split
-    return shared && a.dk == kD && a.dv == kD && a.B * a.H * (kD / 16) < 2 * 152 && N >= 4 && !split_supported(a);
+    return shared && a.dk == kD && a.dv == kD && a.B * a.H * (kD / 16) < 2 * 152 && N >= 4 && !fused_supported(a);
 }
 
 size_t scan_workspace_bytes(const Launch& a) {

@@ -1,6 +1,8 @@
 // Inline-PTX building blocks for sm_103a kernels: shared-memory and instruction descriptors for
-// tcgen05.mma, TMEM loads, mbarriers with bounded waits, TMA tensor copies and stores, flags between
-// kernels that run at the same time, and the warp-level tf32 mma.sync used in the block inversion.
+// tcgen05.mma (kind::f16 and kind::tf32, A from shared or tensor memory), TMEM loads and stores,
+// mbarriers with bounded waits, named barriers, TMA tensor copies, stores and L2 prefetches, flags
+// between kernels that run at the same time, and the warp-level tf32 mma.sync used in the block
+// inversion.
 // Header-only; every function is device-inline.
 #pragma once
 
@@ -261,6 +263,60 @@ __device__ __forceinline__ uint32_t tf32_rn(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
     return r;
+}
+
+
+// ---- kind::tf32 (both operands tf32, fp32 accumulation; tf32 operands must be K-major) and products
+// whose A operand is read from tensor memory (row m of A in lane m, K along the columns: one tf32 or
+// two packed 16-bit elements per column, the lower K index in the low half)
+__host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n"
+                 ::"r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+                 ::"r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
+// ---- TMEM stores: 16 consecutive columns of this thread's lane; tmem_wait_st before anything
+// (an MMA, another thread) reads them
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---- named barriers over a subset of the CTA's warps
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// The same barrier, returning whether any participating thread passed `v` = true.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, %3, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(r) : "r"((uint32_t)v), "r"(id), "r"(nthreads) : "memory");
+    return r != 0;
+}
+
+// ---- TMA: fetch a tile into L2 only (no shared memory, no completion to track)
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* tm, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(tm), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+// ---- 4-byte asynchronous copy global -> shared; `bytes` = 0 writes zero (a row past the end)
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+// Arrive on `bar` once every earlier cp.async of this thread has landed (counted in the
+// barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 }  // namespace ptx
