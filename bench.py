@@ -73,6 +73,13 @@ def _chunk_flops(w):
 
 def _cpu_model():
     try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
         for line in open("/proc/cpuinfo"):
             if line.lower().startswith(("model name", "cpu model", "hardware")):
                 return line.split(":", 1)[1].strip()
