@@ -40,7 +40,7 @@ def _algorithmic_bytes(w, es):
     """Bytes every step must move at least once: inputs read, outputs written."""
     BH = w.batch * w.heads
     tok = BH * w.seqlen
-    per_seg = tok * (2 * w.dk + w.dv) * es + tok * w.dv * es + tok * 4 * (w.dv if w.variant == "falcon2" else 1) \
+    per_seg = tok * (2 * w.dk + w.dv) * es + tok * w.dv * es + tok * 4 * (w.dv if w.variant in ("falcon2", "falcon2a") else 1) \
         + tok * 4 + BH * w.dk * w.dv * 4
     tail = BH * (w.window * w.dk + (w.window - 1) * w.dv) * es
     total = w.segments * (per_seg + tail)
@@ -486,7 +486,8 @@ def run_ours(args, w):
                    "kernel": {1: "cuda-core chunk kernel", 4: "single-token kernel",
                               5: "scan path: chunk maps on the cuda-core kernel, associative scan over them "
                                  "with the outputs fused",
-                              6: "fused tcgen05/TMA kernel, one persistent CTA per sequence"}.get(kernel_id, "?")},
+                              6: "fused tcgen05/TMA kernel, one persistent CTA per sequence",
+                              7: "per-column tcgen05/TMA kernel, one persistent CTA per sequence"}.get(kernel_id, "?")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "scope": "one falcon_fwd call (all kernels it launches); per-kernel shares in profiles/",
                      "traffic": _traffic(w.name, kernel_id), "peak_source": src,

@@ -20,6 +20,12 @@ def test_forward_algorithmic_bytes():
     # q, k, v and out in bf16, beta and lambda fp32, S_final fp32, the tail key
     expect = tok * (3 * 64 + 64) * 2 + tok * 8 + 96 * 64 * 64 * 4 + 96 * 64 * 2
     assert bench._algorithmic_bytes(w, 2) == expect
+    # Falcon-2 and 2A read beta per value column
+    for name in ("f2_b8h12t2048_bf16", "f2a_b8h12t2048_bf16"):
+        w2 = I.WORKLOADS[name]
+        tok2 = 8 * 12 * 2048
+        assert bench._algorithmic_bytes(w2, 2) == tok2 * (3 * 64 + 64) * 2 + tok2 * (64 + 1) * 4 + \
+            96 * 64 * 64 * 4 + 96 * 64 * 2
 
 
 def test_backward_counts():

@@ -142,14 +142,17 @@ def test_unsupported_and_invalid_shapes(lib):
     (dict(variant=F.FALCON_1, seqlen=0), 6),          # no tokens: the fused kernel still writes S_final, tail
     (dict(chunk=32), 1),
     (dict(dtype=F.FALCON_F32), 1),
-    (dict(variant=F.FALCON_2), 1),
+    (dict(variant=F.FALCON_2), 7),                        # Falcon-2 / 2A, bf16, 64, chunk 64: per-column kernel
+    (dict(variant=F.FALCON_2, dtype=F.FALCON_F32), 1),
+    (dict(variant=F.FALCON_2, chunk=32), 1),
     (dict(dk=32, dv=32), 1),
     (dict(seqlen=1), 4),                                  # one token: the single-token kernel
     (dict(seqlen=1, variant=F.FALCON_1A, dtype=F.FALCON_F32), 4),
     (dict(seqlen=1, variant=F.FALCON_2), 4),
     (dict(seqlen=1, dk=32, dv=32), 1),
     (dict(seqlen=2), 6),
-    (dict(variant=F.FALCON_2A), 1),                      # inner-product variants: CUDA-core kernel
+    (dict(variant=F.FALCON_2A), 7),
+    (dict(variant=F.FALCON_2A, seqlen=0), 7),
     (dict(variant=F.FALCON_2A, seqlen=1), 4),            # ... and the single-token kernel for 2A
 ])
 def test_kernel_choice(lib, case, expect):
@@ -261,7 +264,8 @@ def test_scan_path_choice(lib):
     assert F.falcon_workspace_bytes(F.FALCON_3, d, 32) == 24 * (256 + 16) * 5 * 64 * 64 * 4 + 24 * 8192 * 4
     assert F.falcon_workspace_bytes(F.FALCON_3A, d, 32) == 24 * (256 + 16) * 5 * 64 * 64 * 4
     assert F.falcon_kernel_for(F.FALCON_3A, d, 32) == 5
-    assert F.falcon_kernel_for(F.FALCON_2, F.make_dims(2, 12, 8192, 64, 64), 64) == 1  # per-column maps: no
+    assert F.falcon_kernel_for(F.FALCON_2, F.make_dims(2, 12, 8192, 64, 64), 64) == 7  # per-column kernel
+    assert F.falcon_kernel_for(F.FALCON_2, F.make_dims(2, 12, 8192, 64, 64), 32) == 1  # per-column maps: no scan
     assert F.falcon_kernel_for(F.FALCON_3, F.make_dims(8, 12, 8192, 64, 64, window=4), 32) == 1  # many sequences
     assert F.falcon_kernel_for(F.FALCON_3, F.make_dims(2, 12, 64, 64, 64, window=4), 32) == 1  # two chunks
     assert F.falcon_kernel_for(F.FALCON_1, F.make_dims(2, 12, 8192, 64, 64), 64) == 6  # bf16 chunk 64: fused

@@ -119,20 +119,20 @@ def test_zero_beta_steps():
 
 
 @pytest.mark.parametrize("variant", [F1, F1A])
-def test_headline_shape_sampled_sequences(variant):
-    """The bench's workload (8 x 12 x 1024, bf16) in one call; the oracle recomputes a sample of the
-    96 independent sequences (every (b, h) sequence's gradients depend on that sequence alone)."""
+def test_headline_shape_all_sequences(variant):
+    """The bench's workload (8 x 12 x 1024, bf16) in one call; the oracle recomputes all 96 sequences,
+    one batch row (12 heads) at a time to bound its autograd memory."""
     name = "f1_bwd_b8h12t1024_bf16" if variant == F1 else "f1a_bwd_b8h12t1024_bf16"
     w = I.WORKLOADS[name]
     inp = I.make_inputs(w, seed=55)
     inp.update(I.make_adjoints(w, seed=55))
     g = _gpu(variant, inp)
-    for b, h in ((0, 0), (3, 7), (7, 11)):
-        one = {n: (inp[n][b:b + 1, h:h + 1] if inp.get(n) is not None else None)
+    for b in range(inp["q"].shape[0]):
+        one = {n: (inp[n][b:b + 1] if inp.get(n) is not None else None)
                for n in ("q", "k", "v", "beta", "lam", "S0", "dout", "dS_final")}
         r = _ref(variant, one)
-        gs = {n: (g[n][b:b + 1, h:h + 1] if g.get(n) is not None else None) for n in NAMES}
-        _check(f"v{variant} headline ({b},{h})", gs, r)
+        gs = {n: (g[n][b:b + 1] if g.get(n) is not None else None) for n in NAMES}
+        _check(f"v{variant} headline row {b}", gs, r)
 
 
 def test_argument_errors():

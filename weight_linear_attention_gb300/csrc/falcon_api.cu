@@ -49,9 +49,9 @@ size_t tail_bytes_of(const falcon_dims_t* d) {
 }
 
 // Workspace bytes a call with these (validated) arguments can use: the scan path's; 0 for the
-// single-token and fused kernels, which need none.
+// single-token, fused and per-column kernels, which need none.
 size_t workspace_need(const falcon::Launch& a) {
-    if (falcon::decode_supported(a) || falcon::fused_supported(a)) return 0;
+    if (falcon::decode_supported(a) || falcon::fused_supported(a) || falcon::colw_supported(a)) return 0;
     if (falcon::scan_supported(a)) return falcon::scan_workspace_bytes(a);
     return 0;
 }
@@ -84,7 +84,8 @@ int validate_shape(int variant, const falcon_dims_t* d, int chunk, bool has_tail
     a->eps = d->eps;
     a->eps_gamma = d->eps_gamma;
     a->chunk = chunk;
-    if (falcon::generic_smem_bytes(*a, 16, false) > 200 * 1024 && !falcon::fused_supported(*a))
+    if (falcon::generic_smem_bytes(*a, 16, false) > 200 * 1024 && !falcon::fused_supported(*a) &&
+        !falcon::colw_supported(*a))
         return FALCON_ERR_UNSUPPORTED;
     return FALCON_OK;
 }
@@ -157,6 +158,8 @@ int dispatch(const falcon::Launch& a, cudaStream_t s) {
     if (a.B * a.H == 0) return FALCON_OK;
     if (falcon::decode_supported(a)) return falcon::launch_decode(a, s);
     if (falcon::fused_supported(a)) return falcon::launch_fused(a, s);
+    // the per-column kernel loads beta by TMA (16-byte aligned base); otherwise the CUDA-core kernel
+    if (falcon::colw_supported(a) && aligned(a.beta, 16)) return falcon::launch_colw(a, s);
     if (a.ws) return falcon::launch_scan(a, s);
     return falcon::launch_generic(a, s);
 }
@@ -196,6 +199,7 @@ int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk) {
     if (validate_shape(variant, dims, chunk, dims && dims->pos > 0, &a) != FALCON_OK) return 0;
     if (falcon::decode_supported(a)) return 4;
     if (falcon::fused_supported(a)) return 6;
+    if (falcon::colw_supported(a)) return 7;
     if (falcon::scan_supported(a)) return 5;
     return 1;
 }
@@ -304,9 +308,10 @@ int falcon_bwd(int variant, const void* q, const void* k, const void* v, const f
 
 int falcon_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FALCON_ERR_CUDA;
-    int f = 0;
-    if (falcon::fused_consume_timeout_flag(&f) != 0) return FALCON_ERR_CUDA;
-    return f ? FALCON_ERR_DEVICE_TIMEOUT : FALCON_OK;
+    int f = 0, g = 0;
+    if (falcon::fused_consume_timeout_flag(&f) != 0 || falcon::colw_consume_timeout_flag(&g) != 0)
+        return FALCON_ERR_CUDA;
+    return f || g ? FALCON_ERR_DEVICE_TIMEOUT : FALCON_OK;
 }
 
 }  // extern "C"

@@ -782,6 +782,8 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+}  // namespace
+
 // [BH][T][64] bf16, 64 x 64 boxes, 128-byte swizzle
 bool encode_bhtd(CUtensorMap* tm, const void* ptr, long long T, long long BH) {
     EncodeTiledFn fn = encode_fn();
@@ -794,6 +796,20 @@ bool encode_bhtd(CUtensorMap* tm, const void* ptr, long long T, long long BH) {
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// [BH][T][64] fp32, 64 x 64 boxes (256-byte rows), no swizzle
+bool encode_bhtd_f32(CUtensorMap* tm, const void* ptr, long long T, long long BH) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {64 * 4, (cuuint64_t)T * 64 * 4};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 // The opt-in shared-memory limit of the current device, and the kernels' dynamic shared-memory
 // attribute set on it, both once per device.
 constexpr int kMaxDevices = 64;

@@ -2,6 +2,7 @@
 // Not installed; the public interface is include/falcon.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,6 +52,17 @@ bool fused_supported(const Launch& a);
 int launch_fused(const Launch& a, cudaStream_t stream);
 // Reads and clears the device-side timeout flag of the fused kernel (synchronous).
 int fused_consume_timeout_flag(int* flag);
+// TMA maps of a [BH][T][64] tensor with 64 x 64 boxes: bf16 with the 128-byte swizzle, or fp32 with
+// none. False when the driver entry point is missing or refuses the map.
+bool encode_bhtd(CUtensorMap* tm, const void* ptr, long long T, long long BH);
+bool encode_bhtd_f32(CUtensorMap* tm, const void* ptr, long long T, long long BH);
+
+// Per-column path (Falcon-2 and 2A, bf16, dk = dv = 64, chunk 64, T != 1): one persistent CTA per
+// sequence, the shared Gram and scores on tcgen05 one chunk ahead, each value column's merged
+// residual solve on CUDA cores, the state on chip; no workspace.
+bool colw_supported(const Launch& a);
+int launch_colw(const Launch& a, cudaStream_t stream);
+int colw_consume_timeout_flag(int* flag);
 
 // Single-token step (T = 1; Falcon-1, 1A, 2 and 2A; dk = dv = 64): one CTA per (batch, head) state.
 bool decode_supported(const Launch& a);
