@@ -34,9 +34,10 @@
 //               scalars P and u (u over beta in place); and, one chunk behind, the outputs
 //               o_i = P_i (...)_i from TMEM to bf16 and a TMA store (warps 4-5, which share the
 //               columns' lane quadrants)
-// TMEM (512 columns): [0, 64) the state or V as bf16 hi + lo (A operand, 32 columns each); [64, 128)
-// X^T V; two product regions [128, 256) and [320, 448), chunk parity, each Q S (then + masked(Q X^T) V)
-// and X S (then a); [256, 320) the key side's [Q; X] X^T; [448, 512) the state in fp32.
+// TMEM (512 columns): [0, 64) the state and [64, 128) V as bf16 hi + lo (A operands, 32 columns
+// each); [128, 192) X^T V; two product regions [192, 320) and [384, 512), chunk parity, each Q S (then
+// + masked(Q X^T) V) and X S (then a); [320, 384) the key side's [Q; X] X^T. The state itself stays in
+// fp32 registers.
 //
 // Precision: products of the exact bf16 inputs are exact with fp32 sums; the state, V, G and the
 // masked scores enter the tensor cores as bf16 hi + lo pairs (16 significant bits); every sum and
@@ -117,8 +118,8 @@ static_assert(TSLOT + 4 <= 256, "barrier area");
 }  // namespace lay
 
 // TMEM columns
-constexpr uint32_t kSV = 0, kXV = 64, kPD = 256, kSF = 448;
-__device__ __forceinline__ uint32_t region(int n) { return (n & 1) ? 320u : 128u; }  // Q S at +0, X S at +64
+constexpr uint32_t kSV = 0, kVV = 64, kXV = 128, kPD = 320;
+__device__ __forceinline__ uint32_t region(int n) { return (n & 1) ? 384u : 192u; }  // Q S at +0, X S at +64
 
 struct Ctx {
     uint8_t* sm;
@@ -419,7 +420,7 @@ __device__ void state_pass(const ColwParams& p, const Ctx& c, int ct) {
     int issued = 0;
     if (w == 0)
         for (; issued < kStages && issued < p.N; ++issued) issue_load(p, c, issued, lane);
-    float S[64];  // column col of the state (fp32; between chunks in TMEM)
+    float S[64];  // column col of the state (fp32)
     if (p.S0) {
         const float* src = p.S0 + c.bh * 4096 + col;
 #pragma unroll
@@ -428,7 +429,6 @@ __device__ void state_pass(const ColwParams& p, const Ctx& c, int ct) {
 #pragma unroll
         for (int k = 0; k < 64; ++k) S[k] = 0.f;
     }
-    tst64(tl + kSF, S);
     tst_hilo(tl + kSV, S);
     tmem_wait_st();
     tc_fence_before();
@@ -505,8 +505,8 @@ __device__ void state_pass(const ColwParams& p, const Ctx& c, int ct) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         split2(fast ? a[2 * e] : 0.f, fast ? a[2 * e + 1] : 0.f, h[e], l[e]);
-                    tmem_st16(tl + kSV + 16 * bk, h);
-                    tmem_st16(tl + kSV + 32 + 16 * bk, l);
+                    tmem_st16(tl + kVV + 16 * bk, h);
+                    tmem_st16(tl + kVV + 32 + 16 * bk, l);
                 }
                 if (bk == 0) {  // a[32:64] += G[32:64, 0:32] v_0:32: V_hi G_hi, V_lo G_hi, V_hi G_lo
                     tmem_wait_st();
@@ -519,7 +519,7 @@ __device__ void state_pass(const ColwParams& p, const Ctx& c, int ct) {
 #pragma unroll
                         for (int ks = 0; ks < 6; ++ks) {
                             const int kk = ks & 1, part = ks >> 1;
-                            mma_bf16_ta(d, c.tmem + kSV + 8 * kk + (part == 1 ? 32 : 0),
+                            mma_bf16_ta(d, c.tmem + kVV + 8 * kk + (part == 1 ? 32 : 0),
                                         desc_k(pba + (part == 2 ? lay::GL : lay::GH) + 32 * kk), id, 1);
                         }
                         mma_commit(c.bar(lay::M3));
@@ -538,11 +538,10 @@ __device__ void state_pass(const ColwParams& p, const Ctx& c, int ct) {
             float a[64];
 #pragma unroll
             for (int j = 0; j < 64; ++j) a[j] = fast ? ub[j * 64 + col] * ld_bf16(tp + kY + sw128(j, col)) : 0.f;
-            tst_hilo(tl + kSV, a);  // V replaces the state as the A operand (the first product has completed)
+            tst_hilo(tl + kVV, a);
         }
         if (__any_sync(0xffffffffu, !fast)) {  // a slow column's 64 steps one by one, its outputs over Q s
             float o[64];
-            tld64(tl + kSF, S);
             tld64(tl + R, o);
             if (!fast) {
 #pragma unroll 1
@@ -579,7 +578,6 @@ __device__ void state_pass(const ColwParams& p, const Ctx& c, int ct) {
                     for (int e = 0; e < 64; ++e) o[e] = e == i ? oi : o[e];
                 }
             }
-            tst64(tl + kSF, S);
             tst64(tl + R, o);
         }
         tmem_wait_st();
@@ -592,13 +590,13 @@ __device__ void state_pass(const ColwParams& p, const Ctx& c, int ct) {
             constexpr uint32_t idx = idesc_bf16(128, 64, false, true), idk = idesc_bf16(128, 64, false, false);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)  // X^T V: B = X read MN-major, 16 rows (2048 bytes) per K step
-                mma_bf16_ta(c.tmem + kXV, c.tmem + kSV + 8 * (ks & 3) + 32 * (ks >> 2),
+                mma_bf16_ta(c.tmem + kXV, c.tmem + kVV + 8 * (ks & 3) + 32 * (ks >> 2),
                             desc_mn(tiles + kX + 2048 * (ks & 3), kTile), idx, ks > 0);
             mma_commit(c.bar(lay::M2));  // the state update needs only X^T V
 #pragma unroll
             for (int ks = 0; ks < 12; ++ks) {  // V_hi Sc_hi, V_lo Sc_hi, V_hi Sc_lo onto Q S
                 const int kk = ks & 3, part = ks >> 2;
-                mma_bf16_ta(c.tmem + R, c.tmem + kSV + 8 * kk + (part == 1 ? 32 : 0),
+                mma_bf16_ta(c.tmem + R, c.tmem + kVV + 8 * kk + (part == 1 ? 32 : 0),
                             desc_k(pba + (part == 2 ? lay::SCL : lay::SCH) + 32 * kk), idk, 1);
             }
             mma_commit(c.bar(lay::OUTRDY + b));  // the key side forms the outputs from the region
@@ -612,26 +610,16 @@ __device__ void state_pass(const ColwParams& p, const Ctx& c, int ct) {
         // the stage is no longer read: refill it
         if (w == 0 && issued < p.N) issue_load(p, c, issued++, lane);
 
-        // ---- s' = P_63 (s + X^T v) (a slow column's is final already), as fp32 and as the next
-        // product's operand; then that product, once the key side has the next chunk and region
+        // ---- s' = P_63 (s + X^T v) (a slow column's is final already) and as the next product's
+        // operand; then that product, once the key side has the next chunk and region
         {
             float x[64];
-            tld64(tl + kSF, S);
             tld64(tl + kXV, x);
             if (fast) {
 #pragma unroll
                 for (int k = 0; k < 64; ++k) S[k] = gC * (S[k] + x[k]);
             }
         }
-        tst64(tl + kSF, S);
-        // the read product still takes V from the operand columns: wait for it before the state
-        // replaces V there
-        if (ct == 0) bad = !fwait(c, c.bar(lay::OUTRDY + b), (uint32_t)(n >> 1) & 1u);
-        if (named_bar_or(1, 64, bad)) {
-            ok = false;
-            break;
-        }
-        tc_fence_after();
         tst_hilo(tl + kSV, S);
         tmem_wait_st();
         tc_fence_before();
