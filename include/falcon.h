@@ -30,6 +30,11 @@
  * CTA per (batch, head) sequence walks its chunks with the state on chip, the state-independent
  * work of two chunks in flight while the state pass of an earlier one runs ([PL] §E.2: parallel
  * per-chunk work, a short state recurrence, per-chunk reads); it needs no workspace.
+ * Falcon-2 and 2A at bf16, dk = dv = 64, chunk 64 run a per-column tensor-core kernel: one
+ * persistent CTA per sequence; the chunk's Gram and scores, shared by every value column, are formed
+ * one chunk ahead, and each column's merged residual solve runs between two products over all
+ * columns ([PL] §F, §F.2); it needs no workspace. It loads beta by TMA, so it runs when beta is
+ * 16-byte aligned; with a beta aligned to 4 bytes only, the CUDA-core chunk kernel runs instead.
  * Falcon-1, 1A, 3 and 3A with dk = dv = 64 over few (batch, head) sequences and no fused path have
  * a scan path that uses a caller-provided workspace: every chunk's affine maps of the state and of
  * the outputs, then an associative scan over the chunk maps in groups of 16 chunks ([PL] §H.1,
@@ -170,8 +175,8 @@ int falcon_device_status(void* stream);
 /* Which kernels falcon_fwd launches for these arguments when it is given
  * falcon_workspace_bytes() of workspace (0 = none/invalid, 1 = CUDA-core chunk kernel,
  * 4 = single-token kernel for T = 1, 5 = scan path: chunk maps on the CUDA-core kernel, then the
- * scan over them, 6 = fused tensor-core kernel; 2 and 3 are retired). Without a workspace, 5
- * becomes 1. Host only, no launch. */
+ * scan over them, 6 = fused tensor-core kernel, 7 = per-column tensor-core kernel (beta 16-byte
+ * aligned; else 1); 2 and 3 are retired). Without a workspace, 5 becomes 1. Host only, no launch. */
 int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk);
 
 /*
