@@ -13,8 +13,8 @@
 //   v_j = u_j (y_j - d_j a_j),   a_j = (X s)_j + sum_{l<j} G_jl v_l      (one merged residual solve)
 //   s'  = P_63 (s + X^T v),   o_i = P_i ((Q s)_i + sum_{l<=i} (q_i . x_l) v_l).
 // Per chunk the state-dependent work is the products [Q; X] s and [X^T; masked Q X^T] v for all 64
-// columns at once, and the solve, blocked by 16 rows: each diagonal 16 x 16 triangle by forward
-// substitution on the CUDA cores, each block's contribution G[later rows, block] v_block to the
+// columns at once, and the solve, blocked by 32 rows: each diagonal 32 x 32 triangle by forward
+// substitution on the CUDA cores, and the first block's contribution G[32:64, 0:32] v_0:32 to the
 // later rows' a on tcgen05, accumulated in TMEM onto X s. TMEM lane c holds column c: the products
 // are issued with M = 128 and lanes 64-127 carry nothing. Falcon-2A writes the target itself:
 // v = u (.) y, no solve.
@@ -26,7 +26,7 @@
 // Roles (192 threads):
 //   warps 0-1   the state pass, one value column per lane: [Q S | X S] (tcgen05, the state as bf16
 //               hi + lo), the blocked solve, V (bf16 hi + lo) into TMEM, [X^T V | Q S + masked(Q X^T)
-//               V] (tcgen05), the state update (fp32, kept in TMEM), and the next chunk's [Q S | X S]
+//               V] (tcgen05), the state update (fp32 registers), and the next chunk's [Q S | X S]
 //               at once; warp 0 also loads Y, Q, X (bf16) and beta (fp32) by TMA into a 3-stage ring,
 //               lambda by cp.async, with an L2 prefetch
 //   warps 2-5   the key side, one chunk ahead: [Q; X] X^T (tcgen05, bf16), the masked scores and G as
