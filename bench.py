@@ -51,9 +51,11 @@ def _algorithmic_bytes(w, es):
 
 def _launches_per_call(w, kernel_id):
     """Kernels one falcon_fwd call launches on the path `kernel_id` takes."""
-    if kernel_id == 5:  # [window normalisers,] chunk maps, [compose, groups,] apply
+    if kernel_id == 5:  # [window normalisers,] [tensor-core chunk maps,] chunk maps, [compose, groups,] apply
         n = -(-w.seqlen // w.chunk)
-        return (1 if w.variant == "falcon3" else 0) + 1 + (2 if n > 16 else 0) + 1
+        tc = w.variant in ("falcon3", "falcon3a") and w.window == 4 and w.chunk == 32 and w.dtype == "bf16" \
+            and w.dk == 64 and w.dv == 64
+        return (1 if w.variant == "falcon3" else 0) + (1 if tc else 0) + 1 + (2 if n > 16 else 0) + 1
     return 1
 
 

@@ -8,10 +8,12 @@ from weight_linear_attention_gb300 import inputs as I
 def test_launches_per_call():
     W = I.WORKLOADS
     assert bench._launches_per_call(W["f1_b8h12t1024_bf16"], 6) == 1          # fused kernel
-    # scan path, Falcon-3 at 8192 tokens per call, chunk 32: normalisers, maps, compose, groups, apply
-    assert bench._launches_per_call(W["f3w4_b2h12t16384_bf16"], 5) == 5
-    assert bench._launches_per_call(W["f3aw4_b2h12t16384_bf16"], 5) == 4     # no normaliser pass
-    assert bench._launches_per_call(W["f3w4_b2h12t16384_bf16"].with_(seqlen=256), 5) == 3  # one group
+    # scan path, Falcon-3 at 8192 tokens per call, chunk 32: normalisers, tensor-core maps, the CUDA-core
+    # map kernel (strong-decay chunks only), compose, groups, apply
+    assert bench._launches_per_call(W["f3w4_b2h12t16384_bf16"], 5) == 6
+    assert bench._launches_per_call(W["f3aw4_b2h12t16384_bf16"], 5) == 5     # no normaliser pass
+    assert bench._launches_per_call(W["f3w4_b2h12t16384_bf16"].with_(seqlen=256), 5) == 4  # one group
+    assert bench._launches_per_call(W["f3w4_b2h12t16384_bf16"].with_(chunk=16), 5) == 5  # CUDA-core maps only
 
 
 def test_forward_algorithmic_bytes():

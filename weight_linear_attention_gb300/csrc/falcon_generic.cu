@@ -65,6 +65,7 @@ struct GParams {
     const float* mu;  // Falcon-3, mode 1: every token's window normaliser, precomputed ([B*H][T])
     float* ws;   // per chunk (sequence-major) [M | U | S | Ao | Bo], each 64 x 64 fp32 (Ao, Bo: C rows used)
     long long N; // chunks per sequence (mode 1)
+    int skip_marked;  // mode 1: leave the chunks whose block is marked finished (by the tensor-core map kernel)
 };
 
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
@@ -317,6 +318,9 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GPara
     const int vc0 = mode == 1 ? (mpart ? 0 : c0 - DK) : c0;  // first value column of the targets
     const long long blk = 5LL * DK * DK;
     float* wsb = mode != 0 ? p.ws + (bh * p.N + nck) * blk : nullptr;  // this chunk's workspace block
+    // the state slot of a chunk block is free (only group blocks use theirs): a chunk the tensor-core
+    // map kernel finished is marked there with 1, and its maps and the tail are written already
+    if (mode == 1 && p.skip_marked && reinterpret_cast<const int*>(wsb + 2LL * DK * DK)[0] == 1) return;
 
     Smem s;
     smem_floats(VAR, DK, DVS, C, W, &s, smem_raw, (int)sizeof(Tin), p.mode == 0 && p.staged);
@@ -1062,7 +1066,8 @@ int launch_window_mu(const Launch& a, float* mu, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
-int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const float* mu, cudaStream_t st) {
+int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const float* mu, cudaStream_t st,
+                        bool skip_marked) {
     if (a.B * a.H == 0) return 0;
     // map mode: whole 64-column slices (the chunks supply the parallelism, so the key-only work of a
     // chunk is done by two CTAs instead of once per narrow slice)
@@ -1091,6 +1096,7 @@ int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const
     gp.mu = mu;
     gp.ws = ws;
     gp.N = N;
+    gp.skip_marked = skip_marked ? 1 : 0;
     // mode 0 copies each next chunk ahead when the staging area fits beside the tiles
     gp.staged = mode == 0 && generic_smem_bytes(a, dvs, true) <= 200 * 1024;
     const size_t smem = generic_smem_bytes(a, dvs, gp.staged != 0);

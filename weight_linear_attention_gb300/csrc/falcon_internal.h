@@ -41,7 +41,8 @@ struct Launch {
 int launch_generic(const Launch& a, cudaStream_t stream);
 // The same kernel one chunk per CTA (mode 1): every chunk's affine state and output maps into `ws`
 // (the scan path's layout); mode 0 is launch_generic.
-int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const float* mu, cudaStream_t stream);
+int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const float* mu, cudaStream_t stream,
+                        bool skip_marked = false);
 // Falcon-3: every token's window normaliser into mu[B*H][T] (read by modes 1 and 2 instead of recomputed).
 int launch_window_mu(const Launch& a, float* mu, cudaStream_t stream);
 size_t generic_smem_bytes(const Launch& a, int dvs, bool staged = true);  // staged: mode 0's copy-ahead area
@@ -63,6 +64,14 @@ bool encode_bhtd_f32(CUtensorMap* tm, const void* ptr, long long T, long long BH
 bool colw_supported(const Launch& a);
 int launch_colw(const Launch& a, cudaStream_t stream);
 int colw_consume_timeout_flag(int* flag);
+
+// Tensor-core chunk maps for the scan path (Falcon-3 and 3A, bf16, dk = dv = 64, W = 4, chunk 32): every
+// chunk's [M | U | . | Ao | Bo] into the scan workspace, each finished chunk marked in its block's
+// state slot; chunks whose decay is too strong for the factored form stay unmarked for the CUDA-core
+// map kernel (launch_generic_mode with skip_marked).
+bool f3map_supported(const Launch& a);
+int launch_f3map(const Launch& a, float* ws, long long N, const float* mu, cudaStream_t stream);
+int f3map_consume_timeout_flag(int* flag);
 
 // Single-token step (T = 1; Falcon-1, 1A, 2 and 2A; dk = dv = 64): one CTA per (batch, head) state.
 bool decode_supported(const Launch& a);

@@ -6,7 +6,9 @@
 // For Falcon-1, 1A, 3 and 3A every chunk acts on the carried state as S -> M_n S + U_n, and its
 // outputs are O_n = Ao_n S_n + Bo_n, with M_n, U_n, Ao_n, Bo_n fixed by the chunk's inputs alone (the
 // transition is shared by all value columns). With dk = dv = 64:
-//   1. map   (CUDA-core chunk kernel, map mode): every chunk's four maps at once;
+//   1. map   every chunk's four maps at once: for Falcon-3 and 3A at W = 4, chunk 32, bf16 on the
+//            tensor cores (falcon_f3map.cu; a chunk whose decay is too strong for its factored form
+//            is left to the CUDA-core kernel), otherwise the CUDA-core chunk kernel in map mode;
 //   2. scan  (this file), groups of G = 16 chunks:
 //        compose  every group's map (M_g, U_g) = (M_last ... M_first, ...) at once,
 //        groups   per sequence, S_{g+1} = M_g S_g + U_g over the groups,
@@ -216,7 +218,11 @@ int launch_scan(const Launch& a, cudaStream_t st) {
         mu = ws + BH * (N + NG) * kBlk;
         if (launch_window_mu(a, mu, st)) return 4;
     }
-    int e = launch_generic_mode(a, 1, ws, N, mu, st);
+    // chunk maps: on the tensor cores where that kernel applies (the CUDA-core kernel then takes only
+    // the chunks it left unmarked), else on the CUDA cores
+    const bool tc = f3map_supported(a);
+    if (tc && launch_f3map(a, ws, N, mu, st)) return 4;
+    int e = launch_generic_mode(a, 1, ws, N, mu, st, tc);
     if (e) return e;
     static_assert(smem_bytes(64) <= 227 * 1024, "scan kernel shared memory");
     if (cudaFuncSetAttribute(falcon_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(a.chunk)) !=
