@@ -2,6 +2,7 @@
 chunk's affine state map, the associative scan over those maps (groups of 16 chunks), then every
 chunk's outputs, against the fp64 oracle at the same bounds as the other paths (fp32 inputs:
 max|err| / max|ref| <= 1e-4; bf16: max|err| / RMS(ref) <= 2e-2). Cases span one group and several,
+both scan kernels (16-column slices for few groups, one CTA per group over all columns for many),
 ragged chunks, a nonzero initial state, continuation from a tail, the decay clamp, and the aliased
 S_final = S0 call.
 """
@@ -62,6 +63,9 @@ def _run(w, inp, chunk, S0=None, pos=0, tail=None, rtail=None, name=""):
     (F3, "bf16", 32, 1500),
     (F3A, "bf16", 32, 1500),
     (F3, "f32", 16, 600),
+    (F1, "f32", 32, 4096),     # 2 x 12 sequences x 8 groups: one CTA per group over all 64 columns
+    (F3, "bf16", 32, 4096),
+    (F3A, "bf16", 32, 4096),
 ])
 def test_scan_path(variant, dtype, chunk, T):
     w = _wl(variant, dtype, nonzero_s0=True)

@@ -195,6 +195,153 @@ __global__ void __launch_bounds__(kThreads) falcon_scan_kernel(const ScanParams 
         for (int z = 0; z < 4; ++z) dst[(r0 + z) * kD + cg + c] = Sv[b][c][r0 + z];
 }
 
+
+// The same three modes with one CTA per group (mode 1: per sequence) over every state column at once
+// (mode 0: the 64 columns of M_g and the 64 of U_g together), so that each chunk's maps are read from
+// memory once instead of once per 16-column slice. Thread (rg, cg) owns rows 4 rg .. 4 rg + 3 and
+// NCOL / 16 consecutive columns; the state is kept row-major in shared memory; each step's maps arrive
+// through a two-stage ring of 16-byte asynchronous copies issued one step ahead.
+template <int NCOL>
+__global__ void __launch_bounds__(kThreads, 1) falcon_scan_wide_kernel(const ScanParams p) {
+    extern __shared__ __align__(16) float sm[];
+    constexpr int LD = kLdc, SLD = NCOL + 4, CW = NCOL / 16;
+    const int Cr = p.mode == 2 ? p.C : 0;  // output rows fetched per step
+    const int MF = kD * LD, AF = Cr * LD, SF = 2 * MF + 2 * AF;
+    auto Mst = [&](int st) { return sm + st * SF; };
+    auto Ust = [&](int st) { return sm + st * SF + MF; };
+    auto Ast = [&](int st) { return sm + st * SF + 2 * MF; };
+    auto Bst = [&](int st) { return sm + st * SF + 2 * MF + AF; };
+    float* const Sbase = sm + 2 * SF;  // two state buffers [kD][SLD]
+    const int tid = threadIdx.x, rg = tid >> 4, c0 = CW * (tid & 15);
+    const long long bid = blockIdx.x;
+    const long long bh = p.mode == 1 ? bid : bid / p.NG, gi = p.mode == 1 ? 0 : bid % p.NG;
+    float* const chunks = p.ws + bh * p.N * kBlk;
+    float* const groups = p.ws + (p.BH * p.N + bh * p.NG) * kBlk;
+    long long first = 0, nsteps;
+    if (p.mode == 1) nsteps = p.NG;
+    else {
+        first = gi * kGroup;
+        nsteps = min((long long)kGroup, p.N - first);
+    }
+    auto blk = [&](long long j) -> float* { return p.mode == 1 ? groups + j * kBlk : chunks + (first + j) * kBlk; };
+
+    auto issue = [&](long long j) {
+        if (j < nsteps) {
+            const int st = (int)(j & 1);
+            const float* b = blk(j);
+            for (int e = tid; e < 2 * kD * 16; e += kThreads) {  // M and U, 16-byte pieces
+                const int which = e >> 10, row = (e >> 4) & 63, col = 4 * (e & 15);
+                cp_async16((which ? Ust(st) : Mst(st)) + row * LD + col, b + which * kMat + row * kD + col);
+            }
+            for (int e = tid; e < 2 * Cr * 16; e += kThreads) {  // Ao and Bo rows
+                const int which = e / (Cr * 16), r = e % (Cr * 16), row = r >> 4, col = 4 * (r & 15);
+                cp_async16((which ? Bst(st) : Ast(st)) + row * LD + col, b + (3 + which) * kMat + row * kD + col);
+            }
+        }
+        cp_async_commit();
+    };
+
+    // initial state
+    const float* init = nullptr;
+    if (p.mode == 1 || (p.mode == 2 && p.NG == 1)) init = p.S0 ? p.S0 + bh * kMat : nullptr;
+    else if (p.mode == 2) init = groups + gi * kBlk + 2 * kMat;
+    for (int e = tid; e < kD * NCOL; e += kThreads) {
+        const int r = e / NCOL, c = e % NCOL;
+        float x = 0.f;
+        if (p.mode == 0) x = (c < kD && r == c) ? 1.f : 0.f;
+        else if (init) x = init[r * kD + c];
+        Sbase[r * SLD + c] = x;
+    }
+    issue(0);
+    int b = 0;
+    for (long long j = 0; j < nsteps; ++j, b ^= 1) {
+        const int st = (int)(j & 1);
+        issue(j + 1);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncthreads();
+        const float* S = Sbase + b * kD * SLD;
+        if (p.mode == 1) {  // the state entering this group
+            float* so = blk(j) + 2 * kMat;
+            for (int e = tid; e < kD * kD; e += kThreads) so[e] = S[(e >> 6) * SLD + (e & 63)];
+        } else if (p.mode == 2) {  // the chunk's outputs from the state entering it: O = Ao S + Bo
+            const long long t0 = (first + j) * p.C;
+            const int rows = (int)min((long long)p.C, p.T - t0);
+            const float* Ak = Ast(st);
+            const float* Bk = Bst(st);
+            for (int i = rg; i < rows; i += 16) {
+                float o[CW];
+#pragma unroll
+                for (int z = 0; z < CW; ++z) o[z] = Bk[i * LD + c0 + z];
+#pragma unroll 4
+                for (int k = 0; k < kD; ++k) {
+                    const float a = Ak[i * LD + k];
+#pragma unroll
+                    for (int z = 0; z < CW; ++z) o[z] = fmaf(a, S[k * SLD + c0 + z], o[z]);
+                }
+                const long long at = (bh * p.T + t0 + i) * kD + c0;
+#pragma unroll
+                for (int z = 0; z < CW; ++z) {
+                    if (p.bf16) static_cast<__nv_bfloat16*>(p.out)[at + z] = __float2bfloat16_rn(o[z]);
+                    else static_cast<float*>(p.out)[at + z] = o[z];
+                }
+            }
+        }
+        // S' = M S + U (mode 0: + U only on the U part's columns)
+        const float* Mk = Mst(st);
+        const float* Uk = Ust(st);
+        float acc[4][CW];
+#pragma unroll
+        for (int z = 0; z < 4; ++z)
+#pragma unroll
+            for (int y = 0; y < CW; ++y) {
+                const int c = c0 + y;
+                acc[z][y] = p.mode == 0 ? (c >= kD ? Uk[(4 * rg + z) * LD + c - kD] : 0.f) : Uk[(4 * rg + z) * LD + c];
+            }
+#pragma unroll 2
+        for (int k = 0; k < kD; k += 4) {
+            float4 mv[4];
+#pragma unroll
+            for (int z = 0; z < 4; ++z) mv[z] = *reinterpret_cast<const float4*>(Mk + (4 * rg + z) * LD + k);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                float sv[CW];
+#pragma unroll
+                for (int y = 0; y < CW; y += 4) {
+                    const float4 v4 = *reinterpret_cast<const float4*>(S + (k + kk) * SLD + c0 + y);
+                    sv[y] = v4.x, sv[y + 1] = v4.y, sv[y + 2] = v4.z, sv[y + 3] = v4.w;
+                }
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    const float m = kk == 0 ? mv[z].x : kk == 1 ? mv[z].y : kk == 2 ? mv[z].z : mv[z].w;
+#pragma unroll
+                    for (int y = 0; y < CW; ++y) acc[z][y] = fmaf(m, sv[y], acc[z][y]);
+                }
+            }
+        }
+        float* So = Sbase + (b ^ 1) * kD * SLD;
+#pragma unroll
+        for (int z = 0; z < 4; ++z)
+#pragma unroll
+            for (int y = 0; y < CW; y += 4)
+                *reinterpret_cast<float4*>(So + (4 * rg + z) * SLD + c0 + y) =
+                    make_float4(acc[z][y], acc[z][y + 1], acc[z][y + 2], acc[z][y + 3]);
+        __syncthreads();
+    }
+    const float* S = Sbase + b * kD * SLD;  // the result
+    if (p.mode == 0) {
+        float* g = groups + gi * kBlk;
+        for (int e = tid; e < kD * NCOL; e += kThreads) {
+            const int r = e / NCOL, c = e % NCOL;
+            g[(c < kD ? 0 : kMat) + r * kD + (c & 63)] = S[r * SLD + c];
+        }
+    } else if (p.mode == 2 && gi == p.NG - 1 && p.S_final) {
+        for (int e = tid; e < kD * kD; e += kThreads) p.S_final[bh * kMat + e] = S[(e >> 6) * SLD + (e & 63)];
+    }
+}
+template <int NCOL>
+constexpr size_t wide_smem_bytes(int C) {
+    return (size_t)(2 * (2 * kD * kLdc + 2 * C * kLdc) + 2 * kD * (NCOL + 4)) * sizeof(float);
+}
 }  // namespace
 
 bool scan_supported(const Launch& a) {
@@ -229,6 +376,23 @@ int launch_scan(const Launch& a, cudaStream_t st) {
         cudaSuccess)
         return 4;
     ScanParams p{ws, a.S0, a.S_final, a.out, BH, N, NG, a.T, a.chunk, a.bf16, 0};
+    if (BH * NG >= 152) {  // enough groups to fill the GPU with one CTA each: every map read once
+        static_assert(wide_smem_bytes<128>(0) <= 227 * 1024 && wide_smem_bytes<64>(64) <= 227 * 1024, "wide scan");
+        if (cudaFuncSetAttribute(falcon_scan_wide_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)wide_smem_bytes<128>(0)) != cudaSuccess ||
+            cudaFuncSetAttribute(falcon_scan_wide_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)wide_smem_bytes<64>(a.chunk)) != cudaSuccess)
+            return 4;
+        if (NG > 1) {
+            p.mode = 0;
+            falcon_scan_wide_kernel<128><<<(unsigned)(BH * NG), kThreads, wide_smem_bytes<128>(0), st>>>(p);
+            p.mode = 1;
+            falcon_scan_wide_kernel<64><<<(unsigned)BH, kThreads, wide_smem_bytes<64>(0), st>>>(p);
+        }
+        p.mode = 2;
+        falcon_scan_wide_kernel<64><<<(unsigned)(BH * NG), kThreads, wide_smem_bytes<64>(a.chunk), st>>>(p);
+        return cudaGetLastError() == cudaSuccess ? 0 : 4;
+    }
     if (NG > 1) {
         p.mode = 0;
         falcon_scan_kernel<<<(unsigned)(BH * NG * 8), kThreads, smem_bytes(0), st>>>(p);
