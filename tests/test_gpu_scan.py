@@ -1,5 +1,6 @@
 """GPU parity of the scan path (Falcon-1, 1A, 3, 3A with dk = dv = 64 and few sequences): every
-chunk's affine state map, the associative scan over those maps (groups of 16 chunks), then every
+chunk's affine state map, the associative scan over those maps (groups of 16 chunks, or of enough
+chunks that the groups just fill the GPU when there are many), then every
 chunk's outputs, against the fp64 oracle at the same bounds as the other paths (fp32 inputs:
 max|err| / max|ref| <= 1e-4; bf16: max|err| / RMS(ref) <= 2e-2). Cases span one group and several,
 both scan kernels (16-column slices for few groups, one CTA per group over all columns for many),
@@ -66,6 +67,9 @@ def _run(w, inp, chunk, S0=None, pos=0, tail=None, rtail=None, name=""):
     (F1, "f32", 32, 4096),     # 2 x 12 sequences x 8 groups: one CTA per group over all 64 columns
     (F3, "bf16", 32, 4096),
     (F3A, "bf16", 32, 4096),
+    (F1, "f32", 64, 8300),     # the same kernel at chunk 64, 9 groups of 15 chunks, ragged last chunk
+    (F1A, "f32", 16, 2100),    # and at chunk 16
+    (F3, "bf16", 32, 4100),
 ])
 def test_scan_path(variant, dtype, chunk, T):
     w = _wl(variant, dtype, nonzero_s0=True)

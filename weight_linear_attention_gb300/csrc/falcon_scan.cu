@@ -9,7 +9,8 @@
 //   1. map   every chunk's four maps at once: for Falcon-3 and 3A at W = 4, chunk 32, bf16 on the
 //            tensor cores (falcon_f3map.cu; a chunk whose decay is too strong for its factored form
 //            is left to the CUDA-core kernel), otherwise the CUDA-core chunk kernel in map mode;
-//   2. scan  (this file), groups of G = 16 chunks:
+//   2. scan  (this file), groups of G = 16 chunks (with many sequences x groups: enough chunks per
+//            group that one CTA per group fills two slots of every SM):
 //        compose  every group's map (M_g, U_g) = (M_last ... M_first, ...) at once,
 //        groups   per sequence, S_{g+1} = M_g S_g + U_g over the groups,
 //        apply    every group at once, from the group's start state: O_n = Ao_n S_n + Bo_n, then
@@ -32,7 +33,7 @@ constexpr int kCols = 16;     // state columns per CTA
 constexpr int kLdc = 68;      // 16-byte aligned rows
 constexpr int kStages = 3;
 constexpr int kThreads = 256;
-constexpr int kGroup = 16;    // chunks per group
+constexpr int kGroup = 16;    // chunks per group (the workspace holds the group blocks for this size)
 constexpr long long kMat = kD * kD;
 constexpr long long kBlk = 5 * kMat;  // [M | U | S | Ao | Bo]
 // shared floats of one ring stage: M, the offset columns, and (apply) the output maps' rows
@@ -45,6 +46,7 @@ struct ScanParams {
     float* S_final;
     void* out;      // apply: [B*H][T][64] in the input dtype
     long long BH, N, NG, T;
+    long long G;    // chunks per group (compose, apply)
     int C;          // chunk length (apply: rows of Ao, Bo)
     int bf16;
     int mode;  // 0 compose, 1 groups, 2 apply
@@ -95,8 +97,8 @@ __global__ void __launch_bounds__(kThreads) falcon_scan_kernel(const ScanParams 
     long long first = 0, nsteps;
     if (p.mode == 1) nsteps = p.NG;
     else {
-        first = gi * kGroup;
-        nsteps = min((long long)kGroup, p.N - first);
+        first = gi * p.G;
+        nsteps = min(p.G, p.N - first);
     }
     auto blk = [&](long long j) -> float* { return p.mode == 1 ? groups + j * kBlk : chunks + (first + j) * kBlk; };
     const bool has_off = part != 0;
@@ -196,151 +198,141 @@ __global__ void __launch_bounds__(kThreads) falcon_scan_kernel(const ScanParams 
 }
 
 
-// The same three modes with one CTA per group (mode 1: per sequence) over every state column at once
-// (mode 0: the 64 columns of M_g and the 64 of U_g together), so that each chunk's maps are read from
-// memory once instead of once per 16-column slice. Thread (rg, cg) owns rows 4 rg .. 4 rg + 3 and
-// NCOL / 16 consecutive columns; the state is kept row-major in shared memory; each step's maps arrive
-// through a two-stage ring of 16-byte asynchronous copies issued one step ahead.
-template <int NCOL>
-__global__ void __launch_bounds__(kThreads, 1) falcon_scan_wide_kernel(const ScanParams p) {
+// The compose and apply passes with one CTA per group over every state column at once, so that each
+// chunk's maps are read from memory once. A step is one product of stacked operands:
+//   compose  [M_g | U_g] <- M_n [M_g | U_g] + [0 | U_n]      (state 64 x 128, from the group's first map)
+//   apply    [S' ; O_n]  <- [M_n ; Ao_n] S + [U_n ; Bo_n]      (state 64 x 64; 64 + C rows)
+// Thread (rg, cq) owns rows rg + 16 i and columns 4 cq .. 4 cq + 3 of each 64-column half; a warp spans
+// four row groups and eight column quads, so that one read of a state row covers 128 contiguous bytes
+// and one read of the stacked operand touches four rows in four different banks. M and Ao arrive
+// through a two-stage ring of 16-byte asynchronous copies issued one step ahead; U and Bo go straight
+// to registers at the start of the step and are added after the product, which keeps the shared memory
+// low enough for two CTAs per SM. CR = C / 16 output rows per thread (0: compose).
+template <int CR>
+__global__ void __launch_bounds__(kThreads, 2) falcon_scan_wide_kernel(const ScanParams p) {
     extern __shared__ __align__(16) float sm[];
-    constexpr int LD = kLdc, SLD = NCOL + 4, CW = NCOL / 16;
-    const int Cr = p.mode == 2 ? p.C : 0;  // output rows fetched per step
-    const int MF = kD * LD, AF = Cr * LD, SF = 2 * MF + 2 * AF;
-    auto Mst = [&](int st) { return sm + st * SF; };
-    auto Ust = [&](int st) { return sm + st * SF + MF; };
-    auto Ast = [&](int st) { return sm + st * SF + 2 * MF; };
-    auto Bst = [&](int st) { return sm + st * SF + 2 * MF + AF; };
-    float* const Sbase = sm + 2 * SF;  // two state buffers [kD][SLD]
-    const int tid = threadIdx.x, rg = tid >> 4, c0 = CW * (tid & 15);
-    const long long bid = blockIdx.x;
-    const long long bh = p.mode == 1 ? bid : bid / p.NG, gi = p.mode == 1 ? 0 : bid % p.NG;
-    float* const chunks = p.ws + bh * p.N * kBlk;
+    constexpr int NH = CR == 0 ? 2 : 1;   // 64-column halves of the state
+    constexpr int SLD = 64 * NH + 4;      // state row stride (floats)
+    constexpr int NR = 4 + CR;            // operand rows per thread
+    constexpr int SF = (kD + 16 * CR) * kLdc;  // floats of one ring stage
+    float* const S = sm + 2 * SF;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cq = (lane & 7) + 8 * (warp & 1), rg = (lane >> 3) + 4 * (warp >> 1);
+    const long long bh = blockIdx.x / p.NG, gi = blockIdx.x % p.NG;
+    const float* const chunks = p.ws + bh * p.N * kBlk;
     float* const groups = p.ws + (p.BH * p.N + bh * p.NG) * kBlk;
-    long long first = 0, nsteps;
-    if (p.mode == 1) nsteps = p.NG;
-    else {
-        first = gi * kGroup;
-        nsteps = min((long long)kGroup, p.N - first);
-    }
-    auto blk = [&](long long j) -> float* { return p.mode == 1 ? groups + j * kBlk : chunks + (first + j) * kBlk; };
+    const long long first = gi * p.G, nsteps = min(p.G, p.N - first);
 
     auto issue = [&](long long j) {
         if (j < nsteps) {
-            const int st = (int)(j & 1);
-            const float* b = blk(j);
-            for (int e = tid; e < 2 * kD * 16; e += kThreads) {  // M and U, 16-byte pieces
-                const int which = e >> 10, row = (e >> 4) & 63, col = 4 * (e & 15);
-                cp_async16((which ? Ust(st) : Mst(st)) + row * LD + col, b + which * kMat + row * kD + col);
-            }
-            for (int e = tid; e < 2 * Cr * 16; e += kThreads) {  // Ao and Bo rows
-                const int which = e / (Cr * 16), r = e % (Cr * 16), row = r >> 4, col = 4 * (r & 15);
-                cp_async16((which ? Bst(st) : Ast(st)) + row * LD + col, b + (3 + which) * kMat + row * kD + col);
+            const float* b = chunks + (first + j) * kBlk;
+            float* d = sm + (int)(j & 1) * SF;
+#pragma unroll
+            for (int u = 0; u < NR; ++u) {  // rows 0..63: M; rows 64..: Ao (the block's fourth matrix)
+                const int e = tid + u * kThreads, row = e >> 4, col = 4 * (e & 15);
+                cp_async16(d + row * kLdc + col, b + (row < kD ? row * kD : 3 * kMat + (row - kD) * kD) + col);
             }
         }
         cp_async_commit();
     };
 
-    // initial state
-    const float* init = nullptr;
-    if (p.mode == 1 || (p.mode == 2 && p.NG == 1)) init = p.S0 ? p.S0 + bh * kMat : nullptr;
-    else if (p.mode == 2) init = groups + gi * kBlk + 2 * kMat;
-    for (int e = tid; e < kD * NCOL; e += kThreads) {
-        const int r = e / NCOL, c = e % NCOL;
-        float x = 0.f;
-        if (p.mode == 0) x = (c < kD && r == c) ? 1.f : 0.f;
-        else if (init) x = init[r * kD + c];
-        Sbase[r * SLD + c] = x;
-    }
-    issue(0);
-    int b = 0;
-    for (long long j = 0; j < nsteps; ++j, b ^= 1) {
-        const int st = (int)(j & 1);
-        issue(j + 1);
-        asm volatile("cp.async.wait_group 1;" ::: "memory");
-        __syncthreads();
-        const float* S = Sbase + b * kD * SLD;
-        if (p.mode == 1) {  // the state entering this group
-            float* so = blk(j) + 2 * kMat;
-            for (int e = tid; e < kD * kD; e += kThreads) so[e] = S[(e >> 6) * SLD + (e & 63)];
-        } else if (p.mode == 2) {  // the chunk's outputs from the state entering it: O = Ao S + Bo
-            const long long t0 = (first + j) * p.C;
-            const int rows = (int)min((long long)p.C, p.T - t0);
-            const float* Ak = Ast(st);
-            const float* Bk = Bst(st);
-            for (int i = rg; i < rows; i += 16) {
-                float o[CW];
-#pragma unroll
-                for (int z = 0; z < CW; ++z) o[z] = Bk[i * LD + c0 + z];
-#pragma unroll 4
-                for (int k = 0; k < kD; ++k) {
-                    const float a = Ak[i * LD + k];
-#pragma unroll
-                    for (int z = 0; z < CW; ++z) o[z] = fmaf(a, S[k * SLD + c0 + z], o[z]);
-                }
-                const long long at = (bh * p.T + t0 + i) * kD + c0;
-#pragma unroll
-                for (int z = 0; z < CW; ++z) {
-                    if (p.bf16) static_cast<__nv_bfloat16*>(p.out)[at + z] = __float2bfloat16_rn(o[z]);
-                    else static_cast<float*>(p.out)[at + z] = o[z];
-                }
-            }
+    // the state entering the first step: compose starts from the group's first map itself
+    {
+        const float* src = nullptr;
+        if (CR == 0) src = chunks + first * kBlk;
+        else if (p.NG > 1) src = groups + gi * kBlk + 2 * kMat;
+        else if (p.S0) src = p.S0 + bh * kMat;
+        for (int e = tid; e < kD * 64 * NH; e += kThreads) {
+            const int r = e / (64 * NH), c = e % (64 * NH);
+            S[r * SLD + c] = src ? src[(c < kD ? 0 : kMat) + r * kD + (c & 63)] : 0.f;
         }
-        // S' = M S + U (mode 0: + U only on the U part's columns)
-        const float* Mk = Mst(st);
-        const float* Uk = Ust(st);
-        float acc[4][CW];
+    }
+    const long long j0 = CR == 0 ? 1 : 0;
+    issue(j0);
+    for (long long j = j0; j < nsteps; ++j) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();  // this step's operands and the state are in place; the other stage is free
+        issue(j + 1);
+        const float* bj = chunks + (first + j) * kBlk;
+        float4 off[4], bo[CR > 0 ? CR : 1];
 #pragma unroll
-        for (int z = 0; z < 4; ++z)
+        for (int i = 0; i < 4; ++i) off[i] = __ldg(reinterpret_cast<const float4*>(bj + kMat + (rg + 16 * i) * kD) + cq);
 #pragma unroll
-            for (int y = 0; y < CW; ++y) {
-                const int c = c0 + y;
-                acc[z][y] = p.mode == 0 ? (c >= kD ? Uk[(4 * rg + z) * LD + c - kD] : 0.f) : Uk[(4 * rg + z) * LD + c];
-            }
+        for (int i = 0; i < CR; ++i) bo[i] = __ldg(reinterpret_cast<const float4*>(bj + 4 * kMat + (rg + 16 * i) * kD) + cq);
+        const float* A = sm + (int)(j & 1) * SF;
+        float4 acc[NR][NH];
+#pragma unroll
+        for (int i = 0; i < NR; ++i)
+#pragma unroll
+            for (int h = 0; h < NH; ++h) acc[i][h] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 2
         for (int k = 0; k < kD; k += 4) {
-            float4 mv[4];
+            float4 a[NR];
 #pragma unroll
-            for (int z = 0; z < 4; ++z) mv[z] = *reinterpret_cast<const float4*>(Mk + (4 * rg + z) * LD + k);
+            for (int i = 0; i < NR; ++i) a[i] = *reinterpret_cast<const float4*>(A + (rg + 16 * i) * kLdc + k);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                float sv[CW];
+                float4 s[NH];
 #pragma unroll
-                for (int y = 0; y < CW; y += 4) {
-                    const float4 v4 = *reinterpret_cast<const float4*>(S + (k + kk) * SLD + c0 + y);
-                    sv[y] = v4.x, sv[y + 1] = v4.y, sv[y + 2] = v4.z, sv[y + 3] = v4.w;
-                }
+                for (int h = 0; h < NH; ++h) s[h] = *reinterpret_cast<const float4*>(S + (k + kk) * SLD + 64 * h + 4 * cq);
 #pragma unroll
-                for (int z = 0; z < 4; ++z) {
-                    const float m = kk == 0 ? mv[z].x : kk == 1 ? mv[z].y : kk == 2 ? mv[z].z : mv[z].w;
+                for (int i = 0; i < NR; ++i) {
+                    const float m = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
 #pragma unroll
-                    for (int y = 0; y < CW; ++y) acc[z][y] = fmaf(m, sv[y], acc[z][y]);
+                    for (int h = 0; h < NH; ++h) {
+                        acc[i][h].x = fmaf(m, s[h].x, acc[i][h].x);
+                        acc[i][h].y = fmaf(m, s[h].y, acc[i][h].y);
+                        acc[i][h].z = fmaf(m, s[h].z, acc[i][h].z);
+                        acc[i][h].w = fmaf(m, s[h].w, acc[i][h].w);
+                    }
                 }
             }
         }
-        float* So = Sbase + (b ^ 1) * kD * SLD;
+        if constexpr (CR > 0) {  // the chunk's outputs O = Ao S + Bo (the ragged last chunk: rows < T)
+            const long long t0 = (first + j) * p.C;
 #pragma unroll
-        for (int z = 0; z < 4; ++z)
+            for (int i = 0; i < CR; ++i) {
+                const int r = rg + 16 * i;
+                if (t0 + r >= p.T) continue;
+                const float4 o = make_float4(acc[4 + i][0].x + bo[i].x, acc[4 + i][0].y + bo[i].y,
+                                             acc[4 + i][0].z + bo[i].z, acc[4 + i][0].w + bo[i].w);
+                const long long at = (bh * p.T + t0 + r) * kD + 4 * cq;
+                if (p.bf16) {
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+                    uint2 w;
+                    w.x = *reinterpret_cast<uint32_t*>(&lo);
+                    w.y = *reinterpret_cast<uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + at) = w;
+                } else {
+                    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + at) = o;
+                }
+            }
+        }
+        __syncthreads();  // every read of the state is done
 #pragma unroll
-            for (int y = 0; y < CW; y += 4)
-                *reinterpret_cast<float4*>(So + (4 * rg + z) * SLD + c0 + y) =
-                    make_float4(acc[z][y], acc[z][y + 1], acc[z][y + 2], acc[z][y + 3]);
-        __syncthreads();
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                float4 v = acc[i][h];
+                if (h == NH - 1) v.x += off[i].x, v.y += off[i].y, v.z += off[i].z, v.w += off[i].w;
+                *reinterpret_cast<float4*>(S + (rg + 16 * i) * SLD + 64 * h + 4 * cq) = v;
+            }
     }
-    const float* S = Sbase + b * kD * SLD;  // the result
-    if (p.mode == 0) {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    if (CR == 0) {  // the group's map [M_g | U_g]
         float* g = groups + gi * kBlk;
-        for (int e = tid; e < kD * NCOL; e += kThreads) {
-            const int r = e / NCOL, c = e % NCOL;
+        for (int e = tid; e < kD * 128; e += kThreads) {
+            const int r = e >> 7, c = e & 127;
             g[(c < kD ? 0 : kMat) + r * kD + (c & 63)] = S[r * SLD + c];
         }
-    } else if (p.mode == 2 && gi == p.NG - 1 && p.S_final) {
+    } else if (gi == p.NG - 1 && p.S_final) {
         for (int e = tid; e < kD * kD; e += kThreads) p.S_final[bh * kMat + e] = S[(e >> 6) * SLD + (e & 63)];
     }
 }
-template <int NCOL>
-constexpr size_t wide_smem_bytes(int C) {
-    return (size_t)(2 * (2 * kD * kLdc + 2 * C * kLdc) + 2 * kD * (NCOL + 4)) * sizeof(float);
+template <int CR>
+constexpr size_t wide_smem_bytes() {
+    return (size_t)(2 * (kD + 16 * CR) * kLdc + kD * (64 * (CR == 0 ? 2 : 1) + 4)) * sizeof(float);
 }
 }  // namespace
 
@@ -375,22 +367,40 @@ int launch_scan(const Launch& a, cudaStream_t st) {
     if (cudaFuncSetAttribute(falcon_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes(a.chunk)) !=
         cudaSuccess)
         return 4;
-    ScanParams p{ws, a.S0, a.S_final, a.out, BH, N, NG, a.T, a.chunk, a.bf16, 0};
-    if (BH * NG >= 152) {  // enough groups to fill the GPU with one CTA each: every map read once
-        static_assert(wide_smem_bytes<128>(0) <= 227 * 1024 && wide_smem_bytes<64>(64) <= 227 * 1024, "wide scan");
-        if (cudaFuncSetAttribute(falcon_scan_wide_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)wide_smem_bytes<128>(0)) != cudaSuccess ||
-            cudaFuncSetAttribute(falcon_scan_wide_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)wide_smem_bytes<64>(a.chunk)) != cudaSuccess)
+    ScanParams p{ws, a.S0, a.S_final, a.out, BH, N, NG, a.T, kGroup, a.chunk, a.bf16, 0};
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 4;
+    if (BH * NG >= sms) {  // enough groups for one CTA per SM: each map read once, all columns per CTA
+        // the fewest groups that still fill the two CTA slots of every SM (never more groups than the
+        // workspace's blocks for groups of 16)
+        const long long want = max(1LL, min(NG, 2LL * sms / BH));
+        p.G = (N + want - 1) / want;
+        p.NG = (N + p.G - 1) / p.G;
+        const int C = a.chunk;
+        const size_t sm0 = wide_smem_bytes<0>(), sm1 = wide_smem_bytes<1>(), sm2 = wide_smem_bytes<2>(),
+                     sm4 = wide_smem_bytes<4>();
+        static_assert(wide_smem_bytes<4>() <= 113 * 1024, "two wide-scan CTAs per SM");
+        if (cudaFuncSetAttribute(falcon_scan_wide_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm0) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(falcon_scan_wide_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(falcon_scan_wide_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(falcon_scan_wide_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm4) !=
+                cudaSuccess)
             return 4;
-        if (NG > 1) {
+        const unsigned grid = (unsigned)(BH * p.NG);
+        if (p.NG > 1) {
             p.mode = 0;
-            falcon_scan_wide_kernel<128><<<(unsigned)(BH * NG), kThreads, wide_smem_bytes<128>(0), st>>>(p);
-            p.mode = 1;
-            falcon_scan_wide_kernel<64><<<(unsigned)BH, kThreads, wide_smem_bytes<64>(0), st>>>(p);
+            falcon_scan_wide_kernel<0><<<grid, kThreads, sm0, st>>>(p);
+            p.mode = 1;  // the short pass over the groups: 16-column slices
+            falcon_scan_kernel<<<(unsigned)(BH * 4), kThreads, smem_bytes(0), st>>>(p);
         }
         p.mode = 2;
-        falcon_scan_wide_kernel<64><<<(unsigned)(BH * NG), kThreads, wide_smem_bytes<64>(a.chunk), st>>>(p);
+        if (C == 16) falcon_scan_wide_kernel<1><<<grid, kThreads, sm1, st>>>(p);
+        else if (C == 32) falcon_scan_wide_kernel<2><<<grid, kThreads, sm2, st>>>(p);
+        else falcon_scan_wide_kernel<4><<<grid, kThreads, sm4, st>>>(p);
         return cudaGetLastError() == cudaSuccess ? 0 : 4;
     }
     if (NG > 1) {
