@@ -40,7 +40,7 @@ def _sources():
 
 def _digest() -> str:
     h = hashlib.sha256()
-    for p in _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [os.path.join(ROOT, "include", "falcon.h"),
+    for p in _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(ROOT, "include", "falcon.h"),
                                                                           os.path.abspath(__file__)]:
         h.update(p.encode())
         with open(p, "rb") as f:

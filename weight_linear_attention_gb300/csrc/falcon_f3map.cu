@@ -86,8 +86,8 @@ constexpr int G2H = G01L + 12288, G2L = G2H + 4096;    // G[96:128, 64:128], 32 
 constexpr int SCH = G2L + 4096, SCL = SCH + 8192;      // masked Q X_w^T [i][m], two K-atoms of 32 rows
 constexpr int GD = SCL + 8192;                         // four packed diagonal blocks (fp32)
 constexpr int U = GD + 4 * kDBlk * 4;                  // u [128]
-constexpr int GDIAG = U + 512;                         // G_mm [128]
-constexpr int DT = GDIAG + 512, ELT = DT + 128;        // d_i, e^{L_i} [32]
+constexpr int WG = U + 512;                            // G's entries within each token's own window [128][4]
+constexpr int DT = WG + 2048, ELT = DT + 128;          // d_i, e^{L_i} [32]
 constexpr int MISC = ELT + 128;                        // [0] e^{L_C}, [1] fast, [2..] beta, lambda, mu scratch
 constexpr int BAR = MISC + 512;
 constexpr int FULL = 0, MMA = 1, DRAIN = 2, NBAR = 3;
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_f3map_kernel(const __grid_
     const int n = (int)min((long long)kC, p.T - t0);
     float* blk = p.ws + (bh * p.N + nck) * kBlk;
     float* u = reinterpret_cast<float*>(sm + lay::U);
-    float* gdiag = reinterpret_cast<float*>(sm + lay::GDIAG);
+    float* wg = reinterpret_cast<float*>(sm + lay::WG);
     float* dt = reinterpret_cast<float*>(sm + lay::DT);
     float* elt = reinterpret_cast<float*>(sm + lay::ELT);
     float* misc = reinterpret_cast<float*>(sm + lay::MISC);
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_f3map_kernel(const __grid_
     if (ok) {
         tc_fence_after();
         // ---- G row m = tid: the off-diagonal blocks as bf16 hi + lo, this warp's diagonal block (rows
-        // 32 w .. 32 w + 31) packed in fp32, and G_mm
+        // 32 w .. 32 w + 31) packed in fp32, and the row's entries within its own token's window
         {
             const int m = tid, r = lane, f = 4 * ((r >> 2) + 1);
             float* gd = reinterpret_cast<float*>(sm + lay::GD) + warp * kDBlk + dg_off(r) - f;
@@ -276,14 +276,9 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_f3map_kernel(const __grid_
                         for (int q4 = 0; q4 < 8; ++q4) {
                             const float* x = g + 32 * bb + 4 * q4;
                             if (4 * q4 >= f) *reinterpret_cast<float4*>(gd + 4 * q4) = make_float4(x[0], x[1], x[2], x[3]);
+                            if (4 * q4 == f - 4) *reinterpret_cast<float4*>(wg + 4 * m) = make_float4(x[0], x[1], x[2], x[3]);
                         }
                     }
-                }
-                if ((m >> 6) == h) {
-                    float gm = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) gm = e == (m & 63) ? g[e] : gm;
-                    gdiag[m] = gm;
                 }
             }
         }
@@ -307,17 +302,18 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_f3map_kernel(const __grid_
         if (warp == 0) {
             const int i = lane;
             const long long tau = p.pos + t0 + i + 1;
-            int nb = 0;
+            // the window's realised pairs are the slots a < nb; Falcon-3A's window energy sums their
+            // keys' energies G[4 i + a][4 i + a]
+            const int nb = (int)min((long long)kW, max(0LL, tau - 1));
             float en = 0.f;
 #pragma unroll
             for (int a = 0; a < kW; ++a)
-                if (tau - a >= 2) {
-                    ++nb;
-                    en += gdiag[4 * i + a];
-                }
+                if (a < nb) en += wg[4 * (4 * i + a) + a];
             float eta = 0.f, alpha = 0.f, kap = 0.f;
             if (i < n && nb > 0) {
-                const float mu = F3 ? misc[96 + i] : en / (float)nb;  // Falcon-3A: the window's mean key energy
+                // Falcon-3: the window normaliser from the per-token pass; Falcon-3A: the window's mean
+                // key energy
+                const float mu = F3 ? misc[96 + i] : en / (float)nb;
                 const float lm = misc[64 + i];
                 const float den = mu + lm + p.eps;
                 eta = den == 0.f ? 0.f : misc[32 + i] / den;

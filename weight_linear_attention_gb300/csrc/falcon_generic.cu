@@ -30,6 +30,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "falcon_internal.h"
@@ -66,6 +67,8 @@ struct GParams {
     float* ws;   // per chunk (sequence-major) [M | U | S | Ao | Bo], each 64 x 64 fp32 (Ao, Bo: C rows used)
     long long N; // chunks per sequence (mode 1)
     int skip_marked;  // mode 1: leave the chunks whose block is marked finished (by the tensor-core map kernel)
+    long long BH;     // sequences
+    int per_cta;      // skip_marked: items per CTA (at most kThreads)
 };
 
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
@@ -293,8 +296,9 @@ __device__ __forceinline__ void cp_async4z(void* smem, const void* gmem, bool va
                  : "memory");
 }
 
+// One work item: mode 0 a (sequence, column slice), mode 1 a (chunk, column slice).
 template <typename Tin, int VAR>
-__global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GParams p) {
+__device__ __forceinline__ void generic_item(const GParams& p, long long item) {
     extern __shared__ __align__(16) float smem_raw[];
     const int tid = threadIdx.x;
     const int DK = p.dk, DV = p.dv, DVS = p.dvs, C = p.C;
@@ -307,8 +311,8 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GPara
     const long long T = p.T, pos = p.pos;
     const int mode = p.mode;  // 0 or 1
     const int slices = (mode == 1 ? DK + DV : DV) / DVS;
-    const long long nck = mode == 0 ? 0 : (long long)(blockIdx.x % p.N);
-    const long long rest = mode == 0 ? (long long)blockIdx.x : (long long)(blockIdx.x / p.N);
+    const long long nck = mode == 0 ? 0 : item % p.N;
+    const long long rest = mode == 0 ? item : item / p.N;
     const long long bh = rest / slices;
     const int slice = (int)(rest % slices);
     const int c0 = slice * DVS;          // first (virtual) column of this CTA
@@ -318,9 +322,6 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GPara
     const int vc0 = mode == 1 ? (mpart ? 0 : c0 - DK) : c0;  // first value column of the targets
     const long long blk = 5LL * DK * DK;
     float* wsb = mode != 0 ? p.ws + (bh * p.N + nck) * blk : nullptr;  // this chunk's workspace block
-    // the state slot of a chunk block is free (only group blocks use theirs): a chunk the tensor-core
-    // map kernel finished is marked there with 1, and its maps and the tail are written already
-    if (mode == 1 && p.skip_marked && reinterpret_cast<const int*>(wsb + 2LL * DK * DK)[0] == 1) return;
 
     Smem s;
     smem_floats(VAR, DK, DVS, C, W, &s, smem_raw, (int)sizeof(Tin), p.mode == 0 && p.staged);
@@ -948,6 +949,40 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GPara
     }
 }
 
+template <typename Tin, int VAR>
+__global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_kernel(GParams p) {
+    generic_item<Tin, VAR>(p, blockIdx.x);
+}
+
+template <typename Tin, int VAR>
+__global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_left_kernel(GParams p) {
+    // map mode after the tensor-core map kernel: each CTA takes a range of (chunk, slice) items and runs
+    // only those of the chunks that kernel left, so that the launch is about one wave of CTAs when it
+    // finished them all, and as many CTAs per item as before when it finished none. A finished chunk is
+    // marked with 1 in its block's state slot (only group blocks use theirs); its maps and the tail
+    // are written already.
+    const int slices = (p.dk + p.dv) / p.dvs;
+    const long long items = p.BH * p.N * slices, blk = 5LL * p.dk * p.dk;
+    // this CTA's items: a contiguous range of at most kThreads, their marks read by one thread each
+    __shared__ int s_list[kThreads];
+    __shared__ int s_n;
+    const long long first = (long long)blockIdx.x * p.per_cta;
+    if (threadIdx.x == 0) s_n = 0;
+    __syncthreads();
+    const long long me = first + threadIdx.x;
+    if (threadIdx.x < p.per_cta && me < items) {
+        const long long nck = me % p.N, bh = (me / p.N) / slices;
+        if (reinterpret_cast<const int*>(p.ws + (bh * p.N + nck) * blk + 2LL * p.dk * p.dk)[0] != 1)
+            s_list[atomicAdd(&s_n, 1)] = threadIdx.x;
+    }
+    __syncthreads();
+    const int n = s_n;
+    for (int u = 0; u < n; ++u) {
+        generic_item<Tin, VAR>(p, first + s_list[u]);
+        __syncthreads();  // the next item reuses the shared memory
+    }
+}
+
 // Falcon-3: every token's window normaliser mu = lambda_max((1/B) sum_j x_j x_j^T) over the window's
 // realised pairs, one thread per token (the same Gram entries, summed in the same order, and the same
 // Jacobi as the chunk kernel's own), so that chunk kernels running one chunk per CTA read it instead
@@ -1003,7 +1038,13 @@ __global__ void __launch_bounds__(128) falcon_window_mu_kernel(const Tin* k, con
 template <typename Tin>
 cudaError_t launch_typed(const Launch& a, const GParams& gp, dim3 grid, size_t smem, cudaStream_t st) {
     void (*fn)(GParams) = nullptr;
-    switch (a.variant) {
+    if (gp.skip_marked) {  // only the tensor-core map kernel's variants leave chunks unmarked
+        switch (a.variant) {
+            case kF3: fn = falcon_chunk_generic_left_kernel<Tin, kF3>; break;
+            case kF3A: fn = falcon_chunk_generic_left_kernel<Tin, kF3A>; break;
+            default: return cudaErrorInvalidValue;
+        }
+    } else switch (a.variant) {
         case kF1: fn = falcon_chunk_generic_kernel<Tin, kF1>; break;
         case kF1A: fn = falcon_chunk_generic_kernel<Tin, kF1A>; break;
         case kF2: fn = falcon_chunk_generic_kernel<Tin, kF2>; break;
@@ -1101,7 +1142,16 @@ int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const
     gp.staged = mode == 0 && generic_smem_bytes(a, dvs, true) <= 200 * 1024;
     const size_t smem = generic_smem_bytes(a, dvs, gp.staged != 0);
     const long long slices = (mode == 1 ? a.dk + a.dv : a.dv) / dvs;
-    dim3 grid((unsigned)(slices * a.B * a.H * (mode == 0 ? 1 : N)));
+    const long long items = slices * a.B * a.H * (mode == 0 ? 1 : N);
+    gp.BH = a.B * a.H;
+    gp.per_cta = 1;
+    if (skip_marked) {  // about two CTAs per SM, each over a range of items
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 4;
+        gp.per_cta = (int)std::min<long long>(kThreads, std::max<long long>(1, (items + 2LL * sms - 1) / (2LL * sms)));
+    }
+    dim3 grid((unsigned)((items + gp.per_cta - 1) / gp.per_cta));
     cudaError_t e = a.bf16 ? launch_typed<__nv_bfloat16>(a, gp, grid, smem, st)
                            : launch_typed<float>(a, gp, grid, smem, st);
     return e == cudaSuccess ? 0 : 4;
