@@ -3,7 +3,8 @@ chunk's affine state map, the associative scan over those maps (groups of 16 chu
 chunks that the groups just fill the GPU when there are many), then every
 chunk's outputs, against the fp64 oracle at the same bounds as the other paths (fp32 inputs:
 max|err| / max|ref| <= 1e-4; bf16: max|err| / RMS(ref) <= 2e-2). Cases span one group and several,
-both scan kernels (16-column slices for few groups, one CTA per group over all columns for many),
+both scan kernels (16-column slices for few groups; for many, one CTA per group with the state in
+tensor memory and each step a tensor-core product),
 ragged chunks, a nonzero initial state, continuation from a tail, the decay clamp, and the aliased
 S_final = S0 call.
 """
@@ -64,7 +65,7 @@ def _run(w, inp, chunk, S0=None, pos=0, tail=None, rtail=None, name=""):
     (F3, "bf16", 32, 1500),
     (F3A, "bf16", 32, 1500),
     (F3, "f32", 16, 600),
-    (F1, "f32", 32, 4096),     # 2 x 12 sequences x 8 groups: one CTA per group over all 64 columns
+    (F1, "f32", 32, 4096),     # 2 x 12 sequences x 8 groups: the tensor-core steps (fp32 inputs: 1e-4 bound)
     (F3, "bf16", 32, 4096),
     (F3A, "bf16", 32, 4096),
     (F1, "f32", 64, 8300),     # the same kernel at chunk 64, 9 groups of 15 chunks, ragged last chunk

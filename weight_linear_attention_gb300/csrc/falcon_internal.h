@@ -57,6 +57,7 @@ int fused_consume_timeout_flag(int* flag);
 // none. False when the driver entry point is missing or refuses the map.
 bool encode_bhtd(CUtensorMap* tm, const void* ptr, long long T, long long BH);
 bool encode_bhtd_f32(CUtensorMap* tm, const void* ptr, long long T, long long BH);
+bool encode_rows_f32_sw128(CUtensorMap* tm, const void* ptr, long long rows);
 
 // Per-column path (Falcon-2 and 2A, bf16, dk = dv = 64, chunk 64, T != 1): one persistent CTA per
 // sequence, the shared Gram and scores on tcgen05 one chunk ahead, each value column's merged
@@ -82,6 +83,7 @@ int launch_decode(const Launch& a, cudaStream_t stream);
 bool scan_supported(const Launch& a);
 size_t scan_workspace_bytes(const Launch& a);
 int launch_scan(const Launch& a, cudaStream_t stream);
+int scan_tc_consume_timeout_flag(int* flag);
 
 // Backward pass (Falcon-1 and 1A, dk = dv = 64, chunk 64): prep, chain and gradient kernels working
 // through a caller workspace of bwd_workspace_bytes(a) bytes at a.ws. `a` carries the forward inputs.

@@ -10,7 +10,8 @@
 //            tensor cores (falcon_f3map.cu; a chunk whose decay is too strong for its factored form
 //            is left to the CUDA-core kernel), otherwise the CUDA-core chunk kernel in map mode;
 //   2. scan  (this file), groups of G = 16 chunks (with many sequences x groups: enough chunks per
-//            group that one CTA per group fills two slots of every SM):
+//            group that one CTA per group fills two slots of every SM, and compose and apply on the
+//            tensor cores, each map read once):
 //        compose  every group's map (M_g, U_g) = (M_last ... M_first, ...) at once,
 //        groups   per sequence, S_{g+1} = M_g S_g + U_g over the groups,
 //        apply    every group at once, from the group's start state: O_n = Ao_n S_n + Bo_n, then
@@ -20,12 +21,17 @@
 // (Ao, Bo: C rows used; S: a group's start state); for Falcon-3 then every token's window normaliser
 // (computed once by a one-thread-per-token kernel and read by the map pass).
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "falcon_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace falcon {
+
+__device__ int g_scan_tc_timeout_flag = 0;
+
 namespace {
 
 constexpr int kD = 64;
@@ -198,141 +204,268 @@ __global__ void __launch_bounds__(kThreads) falcon_scan_kernel(const ScanParams 
 }
 
 
-// The compose and apply passes with one CTA per group over every state column at once, so that each
-// chunk's maps are read from memory once. A step is one product of stacked operands:
-//   compose  [M_g | U_g] <- M_n [M_g | U_g] + [0 | U_n]      (state 64 x 128, from the group's first map)
-//   apply    [S' ; O_n]  <- [M_n ; Ao_n] S + [U_n ; Bo_n]      (state 64 x 64; 64 + C rows)
-// Thread (rg, cq) owns rows rg + 16 i and columns 4 cq .. 4 cq + 3 of each 64-column half; a warp spans
-// four row groups and eight column quads, so that one read of a state row covers 128 contiguous bytes
-// and one read of the stacked operand touches four rows in four different banks. M and Ao arrive
-// through a two-stage ring of 16-byte asynchronous copies issued one step ahead; U and Bo go straight
-// to registers at the start of the step and are added after the product, which keeps the shared memory
-// low enough for two CTAs per SM. CR = C / 16 output rows per thread (0: compose).
-template <int CR>
-__global__ void __launch_bounds__(kThreads, 2) falcon_scan_wide_kernel(const ScanParams p) {
-    extern __shared__ __align__(16) float sm[];
-    constexpr int NH = CR == 0 ? 2 : 1;   // 64-column halves of the state
-    constexpr int SLD = 64 * NH + 4;      // state row stride (floats)
-    constexpr int NR = 4 + CR;            // operand rows per thread
-    constexpr int SF = (kD + 16 * CR) * kLdc;  // floats of one ring stage
-    float* const S = sm + 2 * SF;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cq = (lane & 7) + 8 * (warp & 1), rg = (lane >> 3) + 4 * (warp >> 1);
+
+// ---------------------------------------------------------------- the same steps on the tensor cores
+// Compose and apply with one CTA of 128 threads per group and the carried state transposed in tensor
+// memory: lane c holds state column c (compose: the 128 columns of [M_g | U_g]; apply: 64, the other
+// lanes zero), TMEM column k its row k. That is the A operand of one product per step,
+//   D = S^T [M_n ; Ao_n]^T   (M = 128, N = 64 + CP, K = 64, kind::tf32),
+// whose first 64 columns are (M_n S)^T and the next CP (apply) (Ao_n S)^T, the chunk's outputs
+// transposed. B = [M_n ; Ao_n] is K-major as stored (row-major maps), loaded by TMA with the 128-byte
+// swizzle, 32 rows x 32 K per load. Each operand x is split into hi = x with its low 13 bits cleared
+// (exact in tf32) and lo = x - hi, and D = A_hi B_hi + A_hi B_lo + A_lo B_hi, so the product has
+// fp32 accuracy (the dropped A_lo B_lo term is below 2^-22 of it). U_n and Bo_n arrive by 16-byte
+// asynchronous copies one step ahead and are added in registers, where each thread also splits its
+// new state column for the next step and (apply) writes its column of the chunk's outputs. Every
+// wait is bounded: on timeout the CTA raises the device flag, drains what it issued and frees its
+// tensor memory.
+constexpr int kTcThreads = 128;
+constexpr uint32_t kTAH = 0, kTAL = 64, kTD = 128;  // TMEM columns: state hi, state lo, product
+constexpr long long kTcTimeout = 4000000000LL;     // ~2 s
+
+template <int CP>  // 0: compose; else apply, output rows rounded up to 32
+struct TcLay {
+    static constexpr int NB = 64 + CP;             // B rows: M_n, then CP rows of Ao_n
+    static constexpr int BHI = 0, BLO = NB * 256;  // each: two K halves of NB rows x 128 bytes
+    static constexpr int UF = (64 + CP) * 64;      // floats of one [U_n ; Bo_n] buffer
+    static constexpr int UB = 2 * NB * 256;        // two such buffers
+    static constexpr int BAR = UB + 2 * UF * 4;
+    static constexpr int BYTES = BAR + 64;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+
+struct ScanTcParams {
+    CUtensorMap tm_ws;  // the workspace as [rows][64] fp32
+    ScanParams s;
+};
+
+__device__ __forceinline__ float hi19(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
+
+__device__ bool tc_wait(uint32_t bar, uint32_t parity) {
+    if (ptx::mbar_try(bar, parity)) return true;
+    const long long t0 = clock64();
+    int spins = 0;
+    while (!ptx::mbar_try(bar, parity)) {
+        if (++spins > 64) __nanosleep(32);
+        if (clock64() - t0 > kTcTimeout) {
+            atomicExch(&g_scan_tc_timeout_flag, 1);
+            return false;
+        }
+    }
+    return true;
+}
+
+// NQ x 16 consecutive TMEM columns of this thread's lane (one wait)
+template <int NQ>
+__device__ __forceinline__ void tc_ld(uint32_t taddr, float* v) {
+    uint32_t r[NQ][16];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) ptx::tmem_ld16(taddr + 16 * q, r[q]);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        ptx::regs_ready(r[q]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[16 * q + e] = __uint_as_float(r[q][e]);
+    }
+}
+
+// this thread's state column into the A operand's hi and lo columns of its lane (no wait)
+__device__ __forceinline__ void put_state(uint32_t tq, const float (&x)[kD]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t h[16], l[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float v = x[16 * q + e], vh = hi19(v);
+            h[e] = __float_as_uint(vh);
+            l[e] = __float_as_uint(v - vh);
+        }
+        ptx::tmem_st16(tq + kTAH + 16 * q, h);
+        ptx::tmem_st16(tq + kTAL + 16 * q, l);
+    }
+}
+
+template <int CP>
+__global__ void __launch_bounds__(kTcThreads, 2) falcon_scan_tc_kernel(const __grid_constant__ ScanTcParams P) {
+    using L = TcLay<CP>;
+    using namespace ptx;
+    constexpr bool kCompose = CP == 0;
+    const ScanParams& p = P.s;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw), base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t bar_full = base + L::BAR, bar_mma = bar_full + 8, bar_drain = bar_full + 16;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BAR + 32);
     const long long bh = blockIdx.x / p.NG, gi = blockIdx.x % p.NG;
+    const long long first = gi * p.G, nsteps = min(p.G, p.N - first);
     const float* const chunks = p.ws + bh * p.N * kBlk;
     float* const groups = p.ws + (p.BH * p.N + bh * p.NG) * kBlk;
-    const long long first = gi * p.G, nsteps = min(p.G, p.N - first);
+    const long long row0 = bh * p.N * (kBlk / kD);  // this sequence's first workspace row of 64 floats
+    if (tid == 0) {
+        mbar_init(bar_full, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_drain, 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot, tq = tmem + ((uint32_t)(32 * warp) << 16);
+    const int c = tid;                     // state column = TMEM lane
+    const bool live = kCompose || c < kD;  // apply: lanes 64..127 hold zeros
 
-    auto issue = [&](long long j) {
+    auto issue_b = [&](long long j) {  // thread 0: [M_n ; Ao_n] of step j by TMA
+        const int r = (int)(row0 + (first + j) * (kBlk / kD));
+        mbar_expect_tx(bar_full, (uint32_t)(L::NB * 256));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t d = base + L::BHI + h * L::NB * 128;
+            tma_load_2d(d, &P.tm_ws, 32 * h, r, bar_full);
+            tma_load_2d(d + 32 * 128, &P.tm_ws, 32 * h, r + 32, bar_full);
+#pragma unroll
+            for (int q = 0; q < CP / 32; ++q) tma_load_2d(d + (64 + 32 * q) * 128, &P.tm_ws, 32 * h, r + 3 * kD + 32 * q, bar_full);
+        }
+    };
+    auto issue_ub = [&](long long j) {  // every thread: U_n (and Bo_n) rows of step j into buffer j & 1
         if (j < nsteps) {
             const float* b = chunks + (first + j) * kBlk;
-            float* d = sm + (int)(j & 1) * SF;
+            float* d = reinterpret_cast<float*>(sm + L::UB) + (int)(j & 1) * L::UF;
 #pragma unroll
-            for (int u = 0; u < NR; ++u) {  // rows 0..63: M; rows 64..: Ao (the block's fourth matrix)
-                const int e = tid + u * kThreads, row = e >> 4, col = 4 * (e & 15);
-                cp_async16(d + row * kLdc + col, b + (row < kD ? row * kD : 3 * kMat + (row - kD) * kD) + col);
+            for (int u = 0; u < L::UF / 4 / kTcThreads; ++u) {
+                const int e = tid + u * kTcThreads, row = e >> 4, col = 4 * (e & 15);
+                cp_async16(d + row * kD + col, b + (row < kD ? kMat + row * kD : 4 * kMat + (row - kD) * kD) + col);
             }
         }
         cp_async_commit();
     };
 
-    // the state entering the first step: compose starts from the group's first map itself
+    // the state entering the first step (compose: the group's first map itself)
+    float s[kD];
     {
         const float* src = nullptr;
-        if (CR == 0) src = chunks + first * kBlk;
-        else if (p.NG > 1) src = groups + gi * kBlk + 2 * kMat;
-        else if (p.S0) src = p.S0 + bh * kMat;
-        for (int e = tid; e < kD * 64 * NH; e += kThreads) {
-            const int r = e / (64 * NH), c = e % (64 * NH);
-            S[r * SLD + c] = src ? src[(c < kD ? 0 : kMat) + r * kD + (c & 63)] : 0.f;
-        }
+        if (kCompose) src = chunks + first * kBlk + (c < kD ? 0 : kMat) + (c & 63);
+        else if (p.NG > 1) src = groups + gi * kBlk + 2 * kMat + c;
+        else if (p.S0) src = p.S0 + bh * kMat + c;
+#pragma unroll
+        for (int r = 0; r < kD; ++r) s[r] = (live && src) ? src[r * kD] : 0.f;
     }
-    const long long j0 = CR == 0 ? 1 : 0;
-    issue(j0);
-    for (long long j = j0; j < nsteps; ++j) {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncthreads();  // this step's operands and the state are in place; the other stage is free
-        issue(j + 1);
-        const float* bj = chunks + (first + j) * kBlk;
-        float4 off[4], bo[CR > 0 ? CR : 1];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) off[i] = __ldg(reinterpret_cast<const float4*>(bj + kMat + (rg + 16 * i) * kD) + cq);
-#pragma unroll
-        for (int i = 0; i < CR; ++i) bo[i] = __ldg(reinterpret_cast<const float4*>(bj + 4 * kMat + (rg + 16 * i) * kD) + cq);
-        const float* A = sm + (int)(j & 1) * SF;
-        float4 acc[NR][NH];
-#pragma unroll
-        for (int i = 0; i < NR; ++i)
-#pragma unroll
-            for (int h = 0; h < NH; ++h) acc[i][h] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-        for (int k = 0; k < kD; k += 4) {
-            float4 a[NR];
-#pragma unroll
-            for (int i = 0; i < NR; ++i) a[i] = *reinterpret_cast<const float4*>(A + (rg + 16 * i) * kLdc + k);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                float4 s[NH];
-#pragma unroll
-                for (int h = 0; h < NH; ++h) s[h] = *reinterpret_cast<const float4*>(S + (k + kk) * SLD + 64 * h + 4 * cq);
-#pragma unroll
-                for (int i = 0; i < NR; ++i) {
-                    const float m = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-#pragma unroll
-                    for (int h = 0; h < NH; ++h) {
-                        acc[i][h].x = fmaf(m, s[h].x, acc[i][h].x);
-                        acc[i][h].y = fmaf(m, s[h].y, acc[i][h].y);
-                        acc[i][h].z = fmaf(m, s[h].z, acc[i][h].z);
-                        acc[i][h].w = fmaf(m, s[h].w, acc[i][h].w);
-                    }
-                }
-            }
-        }
-        if constexpr (CR > 0) {  // the chunk's outputs O = Ao S + Bo (the ragged last chunk: rows < T)
-            const long long t0 = (first + j) * p.C;
-#pragma unroll
-            for (int i = 0; i < CR; ++i) {
-                const int r = rg + 16 * i;
-                if (t0 + r >= p.T) continue;
-                const float4 o = make_float4(acc[4 + i][0].x + bo[i].x, acc[4 + i][0].y + bo[i].y,
-                                             acc[4 + i][0].z + bo[i].z, acc[4 + i][0].w + bo[i].w);
-                const long long at = (bh * p.T + t0 + r) * kD + 4 * cq;
-                if (p.bf16) {
-                    __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
-                    uint2 w;
-                    w.x = *reinterpret_cast<uint32_t*>(&lo);
-                    w.y = *reinterpret_cast<uint32_t*>(&hi);
-                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + at) = w;
-                } else {
-                    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + at) = o;
-                }
-            }
-        }
-        __syncthreads();  // every read of the state is done
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                float4 v = acc[i][h];
-                if (h == NH - 1) v.x += off[i].x, v.y += off[i].y, v.z += off[i].z, v.w += off[i].w;
-                *reinterpret_cast<float4*>(S + (rg + 16 * i) * SLD + 64 * h + 4 * cq) = v;
-            }
+    put_state(tq, s);
+    tmem_wait_st();
+    const long long j0 = kCompose ? 1 : 0;
+    long long pending = -1;  // the step whose B tile is in flight
+    if (j0 < nsteps) {
+        if (tid == 0) issue_b(j0);
+        pending = j0;
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    issue_ub(j0);
+    tc_fence_before();
     __syncthreads();
-    if (CR == 0) {  // the group's map [M_g | U_g]
-        float* g = groups + gi * kBlk;
-        for (int e = tid; e < kD * 128; e += kThreads) {
-            const int r = e >> 7, c = e & 127;
-            g[(c < kD ? 0 : kMat) + r * kD + (c & 63)] = S[r * SLD + c];
+    bool ok = true;
+    constexpr uint32_t id = idesc_tf32(128, (uint32_t)L::NB);
+    for (long long j = j0; j < nsteps; ++j) {
+        const uint32_t ph = (uint32_t)((j - j0) & 1);
+        bool bad = false;
+        if (tid == 0) bad = !tc_wait(bar_full, ph);
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (named_bar_or(1, kTcThreads, bad)) {
+            ok = false;
+            break;
         }
-    } else if (gi == p.NG - 1 && p.S_final) {
-        for (int e = tid; e < kD * kD; e += kThreads) p.S_final[bh * kMat + e] = S[(e >> 6) * SLD + (e & 63)];
+        pending = -1;
+        {  // B: hi (low 13 bits cleared) in place, lo = the rest
+            float4* bh4 = reinterpret_cast<float4*>(sm + L::BHI);
+            float4* bl4 = reinterpret_cast<float4*>(sm + L::BLO);
+#pragma unroll 4
+            for (int e = tid; e < L::NB * 16; e += kTcThreads) {
+                const float4 v = bh4[e];
+                const float4 h = make_float4(hi19(v.x), hi19(v.y), hi19(v.z), hi19(v.w));
+                bh4[e] = h;
+                bl4[e] = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (uint32_t)((ks >> 2) * (L::NB * 128) + 32 * (ks & 3));
+                const uint64_t dh = desc_k(base + L::BHI + off), dl = desc_k(base + L::BLO + off);
+                mma_tf32_ta(tmem + kTD, tmem + kTAH + 8 * ks, dh, id, ks > 0);
+                mma_tf32_ta(tmem + kTD, tmem + kTAH + 8 * ks, dl, id, 1);
+                mma_tf32_ta(tmem + kTD, tmem + kTAL + 8 * ks, dh, id, 1);
+            }
+            mma_commit(bar_mma);
+            bad = !tc_wait(bar_mma, ph);
+            if (!bad && j + 1 < nsteps) issue_b(j + 1);  // the B tile is free again
+        }
+        if (named_bar_or(1, kTcThreads, bad)) {
+            ok = false;
+            break;
+        }
+        if (j + 1 < nsteps) pending = j + 1;
+        issue_ub(j + 1);
+        tc_fence_after();
+        const float* ub = reinterpret_cast<const float*>(sm + L::UB) + (int)(j & 1) * L::UF;
+        {
+            float x[kD];
+            tc_ld<4>(tq + kTD, x);
+#pragma unroll
+            for (int r = 0; r < kD; ++r) {
+                float v = x[r];
+                if (kCompose) v += c >= kD ? ub[r * kD + c - kD] : 0.f;
+                else v = live ? v + ub[r * kD + c] : 0.f;
+                s[r] = v;
+            }
+        }
+        if constexpr (!kCompose) {  // the chunk's outputs O = Ao S + Bo, this thread's column
+            float o[CP];
+            tc_ld<CP / 16>(tq + kTD + kD, o);
+            const long long t0 = (first + j) * p.C;
+            const int rows = (int)min((long long)p.C, p.T - t0);
+            if (live) {
+#pragma unroll
+                for (int i = 0; i < CP; ++i) {
+                    if (i >= rows) break;
+                    const float v = o[i] + ub[(kD + i) * kD + c];
+                    const long long at = (bh * p.T + t0 + i) * kD + c;
+                    if (p.bf16) static_cast<__nv_bfloat16*>(p.out)[at] = __float2bfloat16_rn(v);
+                    else static_cast<float*>(p.out)[at] = v;
+                }
+            }
+        }
+        if (j + 1 < nsteps) put_state(tq, s);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncthreads();
     }
-}
-template <int CR>
-constexpr size_t wide_smem_bytes() {
-    return (size_t)(2 * (kD + 16 * CR) * kLdc + kD * (64 * (CR == 0 ? 2 : 1) + 4)) * sizeof(float);
+    if (ok) {
+        if (kCompose) {  // the group's map [M_g | U_g], column c
+            float* g = groups + gi * kBlk + (c < kD ? 0 : kMat) + (c & 63);
+#pragma unroll
+            for (int r = 0; r < kD; ++r) g[r * kD] = s[r];
+        } else if (gi == p.NG - 1 && p.S_final && live) {
+#pragma unroll
+            for (int r = 0; r < kD; ++r) p.S_final[bh * kMat + r * kD + c] = s[r];
+        }
+    }
+    // drain: copies, a B tile still in flight (only after a timeout), the MMAs; then free TMEM
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (tid == 0 && pending >= 0) mbar_wait_bounded(bar_full, (uint32_t)((pending - j0) & 1), kTcTimeout);
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        mma_commit(bar_drain);
+        mbar_wait_bounded(bar_drain, 0, kTcTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 }  // namespace
 
@@ -371,36 +504,36 @@ int launch_scan(const Launch& a, cudaStream_t st) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 4;
-    if (BH * NG >= sms) {  // enough groups for one CTA per SM: each map read once, all columns per CTA
+    if (BH * NG >= sms) {  // enough groups for a CTA per SM: the tensor-core steps, one CTA per group
         // the fewest groups that still fill the two CTA slots of every SM (never more groups than the
         // workspace's blocks for groups of 16)
         const long long want = max(1LL, min(NG, 2LL * sms / BH));
         p.G = (N + want - 1) / want;
         p.NG = (N + p.G - 1) / p.G;
         const int C = a.chunk;
-        const size_t sm0 = wide_smem_bytes<0>(), sm1 = wide_smem_bytes<1>(), sm2 = wide_smem_bytes<2>(),
-                     sm4 = wide_smem_bytes<4>();
-        static_assert(wide_smem_bytes<4>() <= 113 * 1024, "two wide-scan CTAs per SM");
-        if (cudaFuncSetAttribute(falcon_scan_wide_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm0) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(falcon_scan_wide_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(falcon_scan_wide_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(falcon_scan_wide_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm4) !=
-                cudaSuccess)
-            return 4;
         const unsigned grid = (unsigned)(BH * p.NG);
+        // the workspace as rows of 64 floats for the tensor maps (any workspace that fits in memory has
+        // fewer than 2^31)
+        const long long rows = BH * (N + NG) * (kBlk / kD);
+        ScanTcParams tp{};
+        if (rows >= (1LL << 31) || !encode_rows_f32_sw128(&tp.tm_ws, ws, rows)) return 4;
+        constexpr int a0 = TcLay<0>::ALLOC, a32 = TcLay<32>::ALLOC, a64 = TcLay<64>::ALLOC;
+        static_assert(a64 <= 227 * 1024 && 2 * (a32 + 1024) <= 228 * 1024, "tensor-core scan shared memory");
+        if (cudaFuncSetAttribute(falcon_scan_tc_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, a0) != cudaSuccess ||
+            cudaFuncSetAttribute(falcon_scan_tc_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, a32) != cudaSuccess ||
+            cudaFuncSetAttribute(falcon_scan_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, a64) != cudaSuccess)
+            return 4;
         if (p.NG > 1) {
             p.mode = 0;
-            falcon_scan_wide_kernel<0><<<grid, kThreads, sm0, st>>>(p);
+            tp.s = p;
+            falcon_scan_tc_kernel<0><<<grid, kTcThreads, a0, st>>>(tp);
             p.mode = 1;  // the short pass over the groups: 16-column slices
             falcon_scan_kernel<<<(unsigned)(BH * 4), kThreads, smem_bytes(0), st>>>(p);
         }
         p.mode = 2;
-        if (C == 16) falcon_scan_wide_kernel<1><<<grid, kThreads, sm1, st>>>(p);
-        else if (C == 32) falcon_scan_wide_kernel<2><<<grid, kThreads, sm2, st>>>(p);
-        else falcon_scan_wide_kernel<4><<<grid, kThreads, sm4, st>>>(p);
+        tp.s = p;
+        if (C <= 32) falcon_scan_tc_kernel<32><<<grid, kTcThreads, a32, st>>>(tp);
+        else falcon_scan_tc_kernel<64><<<grid, kTcThreads, a64, st>>>(tp);
         return cudaGetLastError() == cudaSuccess ? 0 : 4;
     }
     if (NG > 1) {
@@ -412,6 +545,14 @@ int launch_scan(const Launch& a, cudaStream_t st) {
     p.mode = 2;
     falcon_scan_kernel<<<(unsigned)(BH * NG * 4), kThreads, smem_bytes(a.chunk), st>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+int scan_tc_consume_timeout_flag(int* flag) {
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_scan_tc_timeout_flag, sizeof(int)) != cudaSuccess) return 1;
+    if (v && cudaMemcpyToSymbol(g_scan_tc_timeout_flag, &zero, sizeof(int)) != cudaSuccess) return 1;
+    *flag = v;
+    return 0;
 }
 
 }  // namespace falcon
