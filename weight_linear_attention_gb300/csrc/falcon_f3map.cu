@@ -18,7 +18,8 @@
 // Per chunk (4 warps; warp w reads TMEM lane quadrant w):
 //   loads     TMA of the key tile (from row t0 - 4), the value tile (from t0 - 3) and the query tile,
 //             a continuation's first rows from the tail; X_w built from the key tile
-//   products  G = X_w X_w^T and Q X_w^T (tcgen05 bf16, exact inputs, fp32 sums)
+//   products  G = X_w X_w^T and Q X_w^T (tcgen05 bf16, exact inputs, fp32 sums); for Falcon-3 then
+//             a = X_w s of every virtual column, [I ; 0] X_w^T, beside the scalars
 //   operands  G's off-diagonal blocks as bf16 hi + lo K-major tiles, its diagonal 32 x 32 blocks in
 //             fp32 (the entries a substitution needs), the masked scores as bf16 hi + lo
 //   scalars   per token eta (window normaliser from the scan path's per-token pass, or for Falcon-3A
@@ -295,9 +296,32 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_f3map_kernel(const __grid_
                     st8_hilo(sm + lay::SCH + 4096 * h, sm + lay::SCL + 4096 * h, sw128(i, 8 * q8), s + 8 * q8);
             }
         }
+        if (F3) {  // the rows of [I ; 0] (lane c < 64: e_c) as a bf16 A operand in RB's first 32 columns
+            // (each warp writes its own lanes, warp 0 after reading its scores there)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t z[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    z[e] = (tid < 64 && (tid >> 1) == 16 * q + e) ? ((tid & 1) ? 0x3F800000u : 0x3F80u) : 0u;
+                tmem_st16(tq + kRB + 16 * q, z);
+            }
+            tmem_wait_st();
+        }
         tc_fence_before();
         fence_async_smem();
         __syncthreads();
+        // ---- Falcon-3: a = X_w s for every virtual column at once, [I ; 0] X_w^T into RA (a unit
+        // column reads X_w's column c, a target column 0), on the tensor cores while warp 0 forms the
+        // per-token scalars
+        if (F3 && tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id = idesc_bf16(128, 128, false, false);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ta(c.tmem + kRA, c.tmem + kRB + 8 * ks, desc_k(base + lay::XW + 32 * ks), id, ks > 0);
+            mma_commit(c.bar(lay::MMA));
+        }
         // ---- per-token scalars (warp 0, token i = lane)
         if (warp == 0) {
             const int i = lane;
@@ -338,24 +362,17 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_f3map_kernel(const __grid_
                 misc[1] = LC >= -kFastL ? 1.f : 0.f;
             }
         }
-        __syncthreads();
+        bool bad = false;
+        if (F3 && tid == 0) bad = !fwait(c, c.bar(lay::MMA), mph & 1u);
+        if (F3) ++mph;
+        ok = !named_bar_or(1, kThreads, bad);
     }
     const bool fast = ok && misc[1] != 0.f;
     if (fast) {
         const int col = tid, cc = col & 63;
         const bool unit = col < 64;  // unit start column e_cc without targets (M, Ao), else targets (U, Bo)
         if (F3) {
-            // a = X_w s: for a unit column the key tile's column cc, else 0
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float a[64];
-#pragma unroll
-                for (int e = 0; e < 64; ++e) a[e] = unit ? ld_bf16(sm + lay::XW + sw128(64 * h + e, cc)) : 0.f;
-                tst<4>(tq + kRA + 64 * h, a);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncthreads();
+            tc_fence_after();  // a = X_w s is in RA
             // ---- v_m = u_m (y_m - d_i a_m) by blocks of 32 rows (8 tokens): the block's a from TMEM,
             // its substitution, v (bf16 hi + lo) into the A operand columns, then G[later rows, block]
             // v_block onto the later rows' a
