@@ -809,20 +809,6 @@ bool encode_bhtd_f32(CUtensorMap* tm, const void* ptr, long long T, long long BH
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][64] fp32, 32 x 32 boxes, 128-byte swizzle: one 32-element K half of 32 rows of a K-major
-// tf32 operand per load
-bool encode_rows_f32_sw128(CUtensorMap* tm, const void* ptr, long long rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {64, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {64 * 4};
-    cuuint32_t box[2] = {32, 32};
-    cuuint32_t es[2] = {1, 1};
-    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 namespace {
 // The opt-in shared-memory limit of the current device, and the kernels' dynamic shared-memory
 // attribute set on it, both once per device.

@@ -57,7 +57,6 @@ int fused_consume_timeout_flag(int* flag);
 // none. False when the driver entry point is missing or refuses the map.
 bool encode_bhtd(CUtensorMap* tm, const void* ptr, long long T, long long BH);
 bool encode_bhtd_f32(CUtensorMap* tm, const void* ptr, long long T, long long BH);
-bool encode_rows_f32_sw128(CUtensorMap* tm, const void* ptr, long long rows);
 
 // Per-column path (Falcon-2 and 2A, bf16, dk = dv = 64, chunk 64, T != 1): one persistent CTA per
 // sequence, the shared Gram and scores on tcgen05 one chunk ahead, each value column's merged
