@@ -61,13 +61,19 @@ def _launches_per_call(w, kernel_id):
 
 def _chunk_flops(w):
     """Flops of the method's chunk algebra per call (each product once, 2 flops per multiply-add, at
-    the workload's own sizes): per (b, h) chunk of C tokens with dk = dv = d, Falcon-1 forms X X^T,
-    Q X^T, X S_n, Q S_n, the triangular solve (C^2 d / 2 multiply-adds), P R and X^T diag(w) R;
-    Falcon-1A forms Q X^T, Q S_n, P Y and X^T diag(w) Y. Other variants: None (not reported)."""
+    the workload's own sizes). Per (b, h) chunk of C tokens with dk = dv = d and R = C W unknown rows
+    (W = 1 but for Falcon-3 / 3A, whose rows are the chunk's (token, window slot) pairs): the solve
+    variants (Falcon-1, 2, 3) form G = X_w X_w^T (R R d), Q X_w^T (C R d), X_w S_n (R d d), Q S_n
+    (C d d), the triangular solve (R R d / 2), P R (C R d) and X_w^T diag(w) R (d R d); the
+    inner-product variants (1A, 2A, 3A) form Q X_w^T, Q S_n, P Y and X_w^T diag(w) Y. Falcon-2's
+    per-column solves and reads add up to the same counts as Falcon-1's."""
     C, d = w.chunk, w.dk
-    per = {"falcon1": 2 * (4 * C * C * d + 2 * C * d * d + C * C * d / 2),
-           "falcon1a": 2 * (2 * C * C * d + 2 * C * d * d)}.get(w.variant)
-    if per is None:
+    R = C * (w.window if w.variant in ("falcon3", "falcon3a") else 1)
+    if w.variant in ("falcon1", "falcon2", "falcon3"):
+        per = 2 * (1.5 * R * R * d + 2 * C * R * d + 2 * R * d * d + C * d * d)
+    elif w.variant in ("falcon1a", "falcon2a", "falcon3a"):
+        per = 2 * (2 * C * R * d + C * d * d + R * d * d)
+    else:
         return None
     n = -(-w.seqlen // C)
     return per * w.batch * w.heads * n * w.segments

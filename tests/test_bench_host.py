@@ -48,4 +48,12 @@ def test_chunk_flops():
     assert bench._chunk_flops(w) == per * 96 * 16
     assert abs(bench._chunk_flops(w) - 5.2e9) < 0.1e9  # the survey's ~5.2 GFLOP for this config
     assert bench._chunk_flops(I.WORKLOADS["f1a_b8h12t1024_bf16"]) == 2 * 4 * 64 ** 3 * 96 * 16
-    assert bench._chunk_flops(I.WORKLOADS["f2_b8h12t2048_bf16"]) is None
+    # Falcon-2 / 2A: the same products at their own length
+    assert bench._chunk_flops(I.WORKLOADS["f2_b8h12t2048_bf16"]) == per * 96 * 32
+    assert bench._chunk_flops(I.WORKLOADS["f2a_b8h12t2048_bf16"]) == 2 * 4 * 64 ** 3 * 96 * 32
+    # Falcon-3 at W = 4, C = 32: R = 128 windowed rows per chunk, 24 sequences x 512 chunks
+    R, C, d = 128, 32, 64
+    per3 = 2 * (1.5 * R * R * d + 2 * C * R * d + 2 * R * d * d + C * d * d)
+    assert bench._chunk_flops(I.WORKLOADS["f3w4_b2h12t16384_bf16"]) == per3 * 24 * 512
+    assert abs(bench._chunk_flops(I.WORKLOADS["f3w4_b2h12t16384_bf16"]) - 80.5e9) < 0.1e9
+    assert bench._chunk_flops(I.WORKLOADS["f3aw4_b2h12t16384_bf16"]) == 2 * (2 * C * R * d + C * d * d + R * d * d) * 24 * 512
