@@ -37,8 +37,11 @@
  * 16-byte aligned; with a beta aligned to 4 bytes only, the CUDA-core chunk kernel runs instead.
  * Falcon-1, 1A, 3 and 3A with dk = dv = 64 over few (batch, head) sequences and no fused path have
  * a scan path that uses a caller-provided workspace: every chunk's affine maps of the state and of
- * the outputs, then an associative scan over the chunk maps in groups of 16 chunks ([PL] §H.1,
- * §H.2), whose last step also forms every chunk's outputs.
+ * the outputs, then an associative scan over the chunk maps in groups of chunks ([PL] §H.1, §H.2),
+ * whose last step also forms every chunk's outputs. For Falcon-3 and 3A at window 4, chunk 32, bf16
+ * the maps are formed on the tensor cores ([PL] §H.3's windowed block system); with enough
+ * sequences x groups to fill the GPU, the scan's compose and apply steps run on the tensor cores
+ * too (tf32 products of split operands, fp32-accurate).
  *
  * Memory: every pointer argument is DEVICE memory owned by the caller; the
  * library keeps no pointer after a call returns and allocates no device memory.
@@ -174,8 +177,9 @@ int falcon_device_status(void* stream);
 
 /* Which kernels falcon_fwd launches for these arguments when it is given
  * falcon_workspace_bytes() of workspace (0 = none/invalid, 1 = CUDA-core chunk kernel,
- * 4 = single-token kernel for T = 1, 5 = scan path: chunk maps on the CUDA-core kernel, then the
- * scan over them, 6 = fused tensor-core kernel, 7 = per-column tensor-core kernel (beta 16-byte
+ * 4 = single-token kernel for T = 1, 5 = scan path: chunk maps (tensor-core kernel for Falcon-3 / 3A
+ * at window 4, chunk 32, bf16; else the CUDA-core kernel), then the scan over them, 6 = fused
+ * tensor-core kernel, 7 = per-column tensor-core kernel (beta 16-byte
  * aligned; else 1); 2 and 3 are retired). Without a workspace, 5 becomes 1. Host only, no launch. */
 int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk);
 
