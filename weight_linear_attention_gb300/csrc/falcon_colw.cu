@@ -494,10 +494,11 @@ __device__ void state_pass(const ColwParams& p, const Ctx& c, int ct) {
 #pragma unroll
                     for (int t0 = d_first(t); t0 < 32; t0 += 4) {
                         const float4 g4 = *reinterpret_cast<const float4*>(gd + d_row(t) + t0 - d_first(t));
-                        if (t0 > t) a[t0] = fmaf(g4.x, vj, a[t0]);
-                        if (t0 + 1 > t) a[t0 + 1] = fmaf(g4.y, vj, a[t0 + 1]);
-                        if (t0 + 2 > t) a[t0 + 2] = fmaf(g4.z, vj, a[t0 + 2]);
-                        a[t0 + 3] = fmaf(g4.w, vj, a[t0 + 3]);
+                        // the later rows in pairs (packed fp32 FMAs; every condition is known at compile time)
+                        if (t0 > t) fma2(a[t0], a[t0 + 1], g4.x, g4.y, vj);
+                        else if (t0 + 1 > t) a[t0 + 1] = fmaf(g4.y, vj, a[t0 + 1]);
+                        if (t0 + 2 > t) fma2(a[t0 + 2], a[t0 + 3], g4.z, g4.w, vj);
+                        else a[t0 + 3] = fmaf(g4.w, vj, a[t0 + 3]);
                     }
                 }
                 {

@@ -399,10 +399,8 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_f3map_kernel(const __grid_
 #pragma unroll
                         for (int r2 = 4 * (t + 1); r2 < 32; r2 += 4) {
                             const float4 g4 = *reinterpret_cast<const float4*>(gd + dg_off(r) + r2 - 4 * (t + 1));
-                            a[r2] = fmaf(g4.x, vr, a[r2]);
-                            a[r2 + 1] = fmaf(g4.y, vr, a[r2 + 1]);
-                            a[r2 + 2] = fmaf(g4.z, vr, a[r2 + 2]);
-                            a[r2 + 3] = fmaf(g4.w, vr, a[r2 + 3]);
+                            fma2(a[r2], a[r2 + 1], g4.x, g4.y, vr);  // packed fp32 FMAs
+                            fma2(a[r2 + 2], a[r2 + 3], g4.z, g4.w, vr);
                         }
                     }
                 }
