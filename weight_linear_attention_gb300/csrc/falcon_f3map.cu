@@ -41,6 +41,7 @@
 #include <stdint.h>
 
 #include "falcon_internal.h"
+#include "sm103_f32x2.cuh"
 #include "sm103_ptx.cuh"
 
 namespace falcon {

@@ -298,14 +298,6 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// ---- packed fp32 pair: (x0, x1) += (g0, g1) * v, one fma.rn.f32x2 (each lane rounded exactly as fmaf)
-__device__ __forceinline__ void fma2(float& x0, float& x1, float g0, float g1, float v) {
-    asm("{\n .reg .b64 a, b, c;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n mov.b64 c, {%4, %4};\n"
-        " fma.rn.f32x2 a, b, c, a;\n mov.b64 {%0, %1}, a;\n}\n"
-        : "+f"(x0), "+f"(x1)
-        : "f"(g0), "f"(g1), "f"(v));
-}
-
 // ---- named barriers over a subset of the CTA's warps
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
