@@ -986,22 +986,37 @@ __global__ void __launch_bounds__(kThreads, 2) falcon_chunk_generic_left_kernel(
 // Falcon-3: every token's window normaliser mu = lambda_max((1/B) sum_j x_j x_j^T) over the window's
 // realised pairs, one thread per token (the same Gram entries, summed in the same order, and the same
 // Jacobi as the chunk kernel's own), so that chunk kernels running one chunk per CTA read it instead
-// of each recomputing it.
+// of each recomputing it. A CTA takes 128 consecutive tokens of one sequence and first copies the
+// 127 + W key rows they use into shared memory with coalesced 16-byte loads (rows padded by 16 bytes,
+// so that neighbouring tokens' rows fall in different banks).
 template <typename Tin, int W>
 __global__ void __launch_bounds__(128) falcon_window_mu_kernel(const Tin* k, const Tin* tail, float* mu, long long BH,
                                                              long long T, long long pos, int DK,
                                                              long long tail_stride) {
-    const long long idx = blockIdx.x * 128LL + threadIdx.x;
-    if (idx >= BH * T) return;
-    const long long bh = idx / T, t = idx % T, tau = pos + t + 1;
-    // the window's realised pairs are a = 0 .. nb - 1 (pair tau - a, key k_{tau - a - 1})
+    extern __shared__ __align__(16) unsigned char mu_sm[];
+    const long long tiles = (T + 127) / 128;
+    const long long bh = blockIdx.x / tiles, t0 = (blockIdx.x % tiles) * 128;
+    const int rb = DK * (int)sizeof(Tin), rs = rb + 16, pieces = rb / 16;
+    // row r holds the key of local index u = t0 - W + r (a negative u: the tail's key u + W)
+    for (int e = threadIdx.x; e < (127 + W) * pieces; e += 128) {
+        const int r = e / pieces, q = e % pieces;
+        const long long u = t0 - W + r;
+        const Tin* src = nullptr;
+        if (u >= 0 && u < T) src = k + (bh * T + u) * DK;
+        else if (u < 0 && tail) src = tail + bh * tail_stride + (u + W) * DK;
+        const uint4 v = src ? reinterpret_cast<const uint4*>(src)[q] : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(mu_sm + r * rs + 16 * q) = v;
+    }
+    __syncthreads();
+    const long long t = t0 + threadIdx.x;
+    if (t >= T) return;
+    const long long tau = pos + t + 1;
+    // the window's realised pairs are a = 0 .. nb - 1 (pair tau - a, key k_{tau - a - 1}: row tid + W - a - 1)
     const int nb = (int)min((long long)W, max(0LL, tau - 1));
     const Tin* rows[W];
 #pragma unroll
-    for (int a = 0; a < W; ++a) {
-        const long long u = t - a - 1;  // local index of the key
-        rows[a] = a >= nb ? nullptr : (u >= 0 ? k + (bh * T + u) * DK : tail + bh * tail_stride + (u + W) * DK);
-    }
+    for (int a = 0; a < W; ++a)
+        rows[a] = a >= nb ? nullptr : reinterpret_cast<const Tin*>(mu_sm + (threadIdx.x + W - a - 1) * rs);
     float g[W][W];
 #pragma unroll
     for (int x = 0; x < W; ++x)
@@ -1032,7 +1047,7 @@ __global__ void __launch_bounds__(128) falcon_window_mu_kernel(const Tin* k, con
             for (int y = 0; y < W; ++y) g[x][y] = (x >= y ? g[x][y] : g[y][x]) * inv;
         m = W == 1 ? g[0][0] * (float)nb : lambda_max_fixed<W>(g);
     }
-    mu[idx] = m;
+    mu[bh * T + t] = m;
 }
 
 template <typename Tin>
@@ -1082,13 +1097,20 @@ int launch_window_mu(const Launch& a, float* mu, cudaStream_t st) {
     const long long n = a.B * a.H * a.T;
     if (n == 0) return 0;
     const long long ts = (long long)a.W * a.dk + (long long)(a.W - 1) * a.dv;
-    const unsigned grid = (unsigned)((n + 127) / 128);
+    const unsigned grid = (unsigned)(a.B * a.H * ((a.T + 127) / 128));
+    bool attr_ok = true;
     auto go = [&](auto tin, auto wc) {
         using Tin = decltype(tin);
         constexpr int W = decltype(wc)::value;
-        falcon_window_mu_kernel<Tin, W><<<grid, 128, 0, st>>>(static_cast<const Tin*>(a.k),
-                                                              static_cast<const Tin*>(a.tail), mu, a.B * a.H, a.T,
-                                                              a.pos, (int)a.dk, ts);
+        const size_t smem = (size_t)(127 + W) * (size_t)(a.dk * sizeof(Tin) + 16);  // at most 71 KB
+        if (cudaFuncSetAttribute(falcon_window_mu_kernel<Tin, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess) {
+            attr_ok = false;
+            return;
+        }
+        falcon_window_mu_kernel<Tin, W><<<grid, 128, smem, st>>>(static_cast<const Tin*>(a.k),
+                                                                 static_cast<const Tin*>(a.tail), mu, a.B * a.H, a.T,
+                                                                 a.pos, (int)a.dk, ts);
     };
     auto by_w = [&](auto tin) {
         switch (a.W) {
@@ -1104,7 +1126,7 @@ int launch_window_mu(const Launch& a, float* mu, cudaStream_t st) {
     };
     if (a.bf16) by_w(__nv_bfloat16{});
     else by_w(float{});
-    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+    return attr_ok && cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
 int launch_generic_mode(const Launch& a, int mode, float* ws, long long N, const float* mu, cudaStream_t st,
