@@ -78,6 +78,15 @@ def test_scan_path(variant, dtype, chunk, T):
     _run(w, inp, chunk, S0=inp["S0"], name=f"v{variant} {dtype} C={chunk} T={T}")
 
 
+@pytest.mark.parametrize("variant,dtype,chunk,T", [(F1, "f32", 16, 3848), (F3, "bf16", 32, 7696)])
+def test_tensor_core_scan_last_group_of_one_chunk(variant, dtype, chunk, T):
+    """12 sequences of 241 chunks: 16 groups of 16, the last group a single ragged chunk (compose
+    takes it as the group's map without a step; apply runs one step from its start state)."""
+    w = _wl(variant, dtype, nonzero_s0=True)
+    inp = I.make_inputs(w, seed=70 + T, seqlen=T, batch=1)
+    _run(w, inp, chunk, S0=inp["S0"], name=f"v{variant} {dtype} C={chunk} T={T} one-chunk group")
+
+
 @pytest.mark.parametrize("variant", [F1, F3])
 def test_scan_continuation(variant):
     """Two calls: the second starts at pos > 0 from the first's S_final and tail."""
