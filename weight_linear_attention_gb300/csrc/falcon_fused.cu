@@ -24,17 +24,18 @@
 // the finished products. Otherwise every factor is one exp of a non-positive argument and s = 1.
 //
 // Roles (384 threads, three warps per SM sub-partition):
-//   warps 0-3, 4-7   two key-side groups; group g takes chunks g, g + 2, ...: [Q; X] X^T and
-//                    [Y^T; X^T] = [Y^T; X^T] I (tcgen05, bf16), the scalars, A (shared) and the
-//                    masked scores (TMEM), T by blocked substitution, E~ (tcgen05, tf32, A operand
-//                    in TMEM), E~ [diag(d) X | Y] (tcgen05, tf32), then [Ao ; -K] back into TMEM
+//   warps 0-3, 4-7   two key-side groups; group g takes chunks g, g + 2, ...: [Q; X] X^T (tcgen05,
+//                    bf16), the scalars, A (shared) and the masked scores (TMEM), T by blocked
+//                    substitution, Y^T and X^T read column by column from the staged tiles into
+//                    E~'s operands, E~ (tcgen05, tf32, A operand in TMEM), E~ [diag(d) X | Y]
+//                    (tcgen05, tf32), then [Ao ; -K] back into TMEM
 //   warps 8-11       the state pass: [Ao ; -K] S (tcgen05, tf32), O = Ao S + Bo to bf16 and a TMA
 //                    store, S' in fp32 registers and as the next product's operand; its first warp
 //                    also loads (TMA of Y, Q and X into a 3-stage ring, beta and lambda by cp.async,
 //                    L2 prefetch): a chunk's stage is refilled once the state pass has received the
 //                    chunk, since the key side is then done reading it
 // TMEM (512 columns): group g owns columns [256g, 256g + 256) as C0 = [0, 64): [Q; X] X^T -> masked
-// scores and X^T (E~'s A operand); C1 = [64, 128): [Y^T; X^T] -> E~ -> the state-pass product;
+// scores and X^T (E~'s A operand); C1 = [64, 128): E~ -> the state-pass product;
 // C2 = [128, 256): [PW | Bo ; K | U] -> [Ao | Bo ; -K | U].
 //
 // Precision: products of the exact bf16 inputs are bf16 (exact, fp32 sums); E~ and everything after
@@ -99,13 +100,11 @@ constexpr int TOP = 0, B3 = 16384, AT = B3, SCAL = B3 + 32768;
 constexpr int GRP_BYTES = SCAL + 3072;
 constexpr int SOP = GRP + 2 * GRP_BYTES;  // S^T as the tf32 B operand of the state pass
 constexpr int OUTS = SOP + 16384;         // two bf16 output staging tiles
-constexpr int IDENT = OUTS + 2 * kTile;   // the 64 x 64 identity (bf16)
-constexpr int CGS = IDENT + kTile;        // per group: the finished chunk's row scales s (128 floats)
+constexpr int CGS = OUTS + 2 * kTile;     // per group: the finished chunk's row scales s (128 floats)
 constexpr int BAR = CGS + 1024;
 constexpr int BYTES = BAR + 256;
 constexpr int ALLOC = BYTES + 1024;
-static_assert(GRP % 1024 == 0 && GRP_BYTES % 1024 == 0 && SOP % 1024 == 0 && OUTS % 1024 == 0 &&
-                  IDENT % 1024 == 0, "layout");
+static_assert(GRP % 1024 == 0 && GRP_BYTES % 1024 == 0 && SOP % 1024 == 0 && OUTS % 1024 == 0, "layout");
 static_assert(64 * kS * 4 <= 32768 && sizeof(FScal) <= 3072, "group area");
 // mbarriers
 constexpr int FULL = 0, MMA = 3, CA = 5, CD = 7, CONS = 9, DRAIN = 11, NBAR = 14;
@@ -270,7 +269,6 @@ __device__ void key_group(const FusedParams& p, const Ctx& c, int g, int gt) {
     const uint32_t grp_a = c.base + lay::GRP + g * lay::GRP_BYTES;
     float* gch = reinterpret_cast<float*>(c.sm + lay::BAR + lay::GCH);
     float* cgs = reinterpret_cast<float*>(c.sm + lay::CGS) + 128 * g;
-    const uint32_t ident = c.base + lay::IDENT;
     uint32_t mph = 0;  // phases of this group's MMA barrier consumed so far
     // thread 0 issues, commits and waits; every thread learns the outcome at the group barrier
     auto wait_mma = [&]() -> bool {
@@ -426,28 +424,25 @@ __device__ void key_group(const FusedParams& p, const Ctx& c, int g, int gt) {
             fence_async_smem();
         }
 
-        // ---- C1 and C2 free (the state pass has read chunk n - 2's): [Y^T; X^T] = [Y^T; X^T] I
-        if (gt == 0 && j > 0) bad = !fwait(c, c.bar(lay::CONS + g), (uint32_t)(j - 1) & 1u);
-        if (named_bar_or(bid, 128, bad)) break;
-        if (gt == 0) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc_bf16(128, 64, true, false);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(Bg + C1, desc_mn(stage + 2048 * ks, kX), desc_k(ident + 32 * ks), id, ks > 0);
-            mma_commit(c.bar(lay::MMA + g));
-        }
-        if (!wait_mma()) break;
-        tc_fence_after();
-        // rows 0-63 (feature c): Y^T row c -> the B operand's rows 64 + c (exact);
-        // rows 64-127 (feature a): X^T row a -> diag(d) folded in, B rows a; and back to C0 as the
-        // bottom of E~'s A operand (factored: as is, Falcon-1A times u_j; otherwise times w_j)
+        // ---- the transposes, each thread its feature's column of the stage's Y or X tile (exact):
+        // rows 0-63 (feature c): Y^T row c -> the B operand's rows 64 + c;
+        // rows 64-127 (feature a): X^T row a -> diag(d) folded in, B rows a; and to C0 as the bottom
+        // of E~'s A operand (factored: as is, Falcon-1A times u_j; otherwise times w_j)
         {
             uint8_t* b3 = grp + lay::B3;
+            const int fc = gt & 63;  // the feature
+            const uint8_t* colb = stg + (gt < 64 ? 0 : kX) + ((fc & 7) << 1);
+            uint32_t xo[8];  // the feature's 16-byte chunk in a swizzled row, per row residue
+#pragma unroll
+            for (int k = 0; k < 8; ++k) xo[k] = (uint32_t)(((fc >> 3) ^ k) << 4);
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 float v[32];
-                tmem_ld32(tq + C1 + 32 * h, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {  // token row 32 h + e of the tile
+                    const int jr = 32 * h + e;
+                    v[e] = __bfloat162float(*reinterpret_cast<const bf16*>(colb + (jr >> 3) * 1024 + (jr & 7) * 128 + xo[jr & 7]));
+                }
                 if (gt < 64) {
 #pragma unroll
                     for (int k4 = 0; k4 < 8; ++k4)
@@ -474,7 +469,9 @@ __device__ void key_group(const FusedParams& p, const Ctx& c, int g, int gt) {
         tmem_wait_st();
         fence_async_smem();
         tc_fence_before();
-        named_bar(bid, 128);
+        // C1 and C2 free (the state pass has read chunk n - 2's)
+        if (gt == 0 && j > 0) bad = !fwait(c, c.bar(lay::CONS + g), (uint32_t)(j - 1) & 1u);
+        if (named_bar_or(bid, 128, bad)) break;
 
         uint32_t ea = C0;  // TMEM columns of E~ (the A operand of the products with X and Y)
         if (f1) {
@@ -737,17 +734,6 @@ __global__ void __launch_bounds__(kThreads, 1) falcon_fused_kernel(const __grid_
         *c.abort = 0;
         mbar_init_fence();
     }
-    for (int e = tid; e < kTile / 16; e += kThreads) {  // the identity, in the bf16 tile layout
-        const int r = e >> 3, q = e & 7;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if ((r >> 3) == q) {
-            const uint32_t one = 0x3F80u << (16 * (r & 1));
-            const int w = (r & 7) >> 1;
-            (w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w) = one;
-        }
-        *reinterpret_cast<uint4*>(sm + lay::IDENT + r * 128 + ((q ^ (r & 7)) << 4)) = v;
-    }
-    fence_async_smem();
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + lay::BAR + lay::TSLOT);
     if (warp == 8) tmem_alloc(smem_u32(tslot), 512);
     tc_fence_before();
