@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include "falcon_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace falcon {
 namespace {
@@ -58,6 +59,11 @@ __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p
     __shared__ float xs[kD], qs[kD], ys[kD], rs[kD], eta_s[kD], gam_s[kD];
     __shared__ float part[kGroups][kD];
     __shared__ float nx_s;
+    // launched with programmatic stream serialisation: wait until the grid before this one in the
+    // stream has finished and its writes are visible (a decode loop's previous step wrote this step's
+    // state), then let the next grid start launching while this one runs
+    ptx::pdl_wait();
+    ptx::pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31;
     const long long bh = blockIdx.x;
     const int cq = tid & 15, rg = tid >> 4, c0 = 4 * cq, r0 = kRows * rg;
@@ -147,15 +153,26 @@ __global__ void __launch_bounds__(kThreads) falcon_decode_kernel(const DParams p
 
 template <typename Tin>
 cudaError_t launch_typed(const Launch& a, const DParams& p, cudaStream_t st) {
-    const unsigned grid = (unsigned)(a.B * a.H);
+    void (*fn)(DParams) = nullptr;
     switch (a.variant) {
-        case kF1: falcon_decode_kernel<Tin, kF1><<<grid, kThreads, 0, st>>>(p); break;
-        case kF1A: falcon_decode_kernel<Tin, kF1A><<<grid, kThreads, 0, st>>>(p); break;
-        case kF2: falcon_decode_kernel<Tin, kF2><<<grid, kThreads, 0, st>>>(p); break;
-        case kF2A: falcon_decode_kernel<Tin, kF2A><<<grid, kThreads, 0, st>>>(p); break;
+        case kF1: fn = falcon_decode_kernel<Tin, kF1>; break;
+        case kF1A: fn = falcon_decode_kernel<Tin, kF1A>; break;
+        case kF2: fn = falcon_decode_kernel<Tin, kF2>; break;
+        case kF2A: fn = falcon_decode_kernel<Tin, kF2A>; break;
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+    // programmatic stream serialisation: consecutive steps overlap one's launch with the other's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.B * a.H));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
 }  // namespace
