@@ -308,11 +308,12 @@ int falcon_bwd(int variant, const void* q, const void* k, const void* v, const f
 
 int falcon_device_status(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FALCON_ERR_CUDA;
-    int f = 0, g = 0, h = 0, k = 0;
+    int f = 0, g = 0, h = 0, k = 0, b = 0;
     if (falcon::fused_consume_timeout_flag(&f) != 0 || falcon::colw_consume_timeout_flag(&g) != 0 ||
-        falcon::f3map_consume_timeout_flag(&h) != 0 || falcon::scan_tc_consume_timeout_flag(&k) != 0)
+        falcon::f3map_consume_timeout_flag(&h) != 0 || falcon::scan_tc_consume_timeout_flag(&k) != 0 ||
+        falcon::bwd_consume_timeout_flag(&b) != 0)
         return FALCON_ERR_CUDA;
-    return f || g || h || k ? FALCON_ERR_DEVICE_TIMEOUT : FALCON_OK;
+    return f || g || h || k || b ? FALCON_ERR_DEVICE_TIMEOUT : FALCON_OK;
 }
 
 }  // extern "C"

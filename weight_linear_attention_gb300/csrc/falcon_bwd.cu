@@ -21,14 +21,17 @@
 //             by definition: a zero denominator or the first step of a fresh sequence).
 // The chunk-start state adjoint is dS = M^T dS' + V with M = e^{L_C} I - X^T diag(w) T diag(e^Lx) X
 // and V = Q^T diag(e^L) dO - X^T diag(e^Lx) T^T P^T dO, so three launches do the whole pass:
-//   falcon_bwd_prep   every chunk at once: T, the forward transition (M, U = X^T diag(w) T Y) and V;
-//   falcon_bwd_chain  per sequence (four CTAs of 16 value columns each): S_{n+1} = M_n S_n + U_n
-//                     forward, then dS_n = M_n^T dS_{n+1} + V_n backward, storing S_n and dS_{n+1};
+//   falcon_bwd_prep   every chunk at once: T, the forward transition (M and M^T, U = X^T diag(w) T Y)
+//                     and V;
+//   falcon_bwd_chain  per sequence (one CTA, the carried matrix in tensor memory, one tcgen05 product
+//                     per step): S_{n+1} = M_n S_n + U_n forward, then dS_n = M_n^T dS_{n+1} + V_n
+//                     backward, storing S_n and dS_{n+1};
 //   falcon_bwd_grad   every chunk at once: all input gradients from S_n and dS_{n+1}.
 // The 64 x 64 x 64 products of prep and grad run on the tensor cores as warp-level tf32 MMAs with
 // every fp32 operand split into a tf32 head and remainder (fp32-accurate); the scans, the scalars
 // and the triangular inverse run on the CUDA cores in fp32.
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -36,6 +39,9 @@
 #include "sm103_ptx.cuh"
 
 namespace falcon {
+
+__device__ int g_bwd_timeout_flag = 0;
+
 namespace {
 
 constexpr int kD = 64;        // dk = dv
@@ -43,11 +49,9 @@ constexpr int kC = 64;        // chunk length
 constexpr int kLd = 68;       // shared-memory row stride (floats): 16-byte rows, tensor-core fragments
 constexpr int kMat = kC * kLd;
 constexpr int kThreads = 512;       // prep and gradient kernels: 16 warps
-constexpr int kChainThreads = 256;  // state scans: 16 x 16 threads
-constexpr int kCols = 16;     // value columns per chain CTA
 constexpr int kWsMat = kD * kD;             // floats per workspace matrix
-constexpr int kWsChunk = 6 * kWsMat;        // M, U, V, T, S_n, dS_{n+1}
-enum { kWsM = 0, kWsU = 1, kWsV = 2, kWsT = 3, kWsS = 4, kWsDS = 5 };
+constexpr int kWsChunk = 7 * kWsMat;        // M, U, V, T, S_n, dS_{n+1}, M^T
+enum { kWsM = 0, kWsU = 1, kWsV = 2, kWsT = 3, kWsS = 4, kWsDS = 5, kWsMT = 6 };
 
 struct BParams {
     const void* q;
@@ -409,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) falcon_bwd_prep(const BParams p) 
         zero(acc2);
         mm<true, false, EX, false>(acc2, Q, dO);
         FOR_TILE(ws[kWsM * kWsMat + i * kD + j] = i == j ? s.eLC : 0.f;
+                 ws[kWsMT * kWsMat + i * kD + j] = i == j ? s.eLC : 0.f;
                  ws[kWsU * kWsMat + i * kD + j] = acc[m][n];
                  ws[kWsV * kWsMat + i * kD + j] = acc2[m][n];)
         return;
@@ -429,7 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1) falcon_bwd_prep(const BParams p) 
     mm<true, false, EX, false>(acc, X, B1);
     zero(acc2);
     mm<true, false, EX, false>(acc2, X, B2);
-    FOR_TILE(ws[kWsM * kWsMat + i * kD + j] = (i == j ? s.eLC : 0.f) - acc[m][n];
+    FOR_TILE(const float mij = (i == j ? s.eLC : 0.f) - acc[m][n];
+             ws[kWsM * kWsMat + i * kD + j] = mij;
+             ws[kWsMT * kWsMat + j * kD + i] = mij;
              ws[kWsU * kWsMat + i * kD + j] = acc2[m][n];
              ws[kWsT * kWsMat + i * kD + j] = Tm[i * kLd + j];)
     zero(acc);
@@ -445,113 +452,229 @@ __global__ void __launch_bounds__(kThreads, 1) falcon_bwd_prep(const BParams p) 
     FOR_TILE(ws[kWsV * kWsMat + i * kD + j] = acc[m][n] - acc2[m][n];)
 }
 
-// --------------------------------------------------------------------------------------------------
-// falcon_bwd_chain: one CTA per (sequence, group of 16 value columns). Thread (r4, c) owns rows
-// 4 r4 .. 4 r4 + 3 of column c. The state slice is kept transposed (column-major) so that a thread reads
-// four consecutive k of its column at once. M_n (row-major) and the column slice of U_n (forward) or
-// V_n (backward) arrive through a three-stage ring of 16-byte asynchronous copies issued two steps
-// ahead of their use.
-constexpr int kLdc = 68;      // 16-byte aligned rows
-constexpr int kStages = 3;
-constexpr size_t kChainSmem = (size_t)kStages * (kD * kLdc + kD * kCols) * sizeof(float) + 2 * kCols * kLdc * sizeof(float);
-
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
                  "l"(gmem)
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kChainThreads) falcon_bwd_chain(const BParams p) {
-    extern __shared__ __align__(16) float smc[];
-    float* Ms = smc;                              // [kStages][kD * kLdc]
-    float* Os = Ms + kStages * kD * kLdc;         // [kStages][kD][kCols]  offsets (U or V columns)
-    float (*Sv)[kCols][kLdc] = reinterpret_cast<float (*)[kCols][kLdc]>(Os + kStages * kD * kCols);  // [2]
-    const long long bh = blockIdx.x / (kD / kCols);
-    const int cg = (int)(blockIdx.x % (kD / kCols)) * kCols;
-    const int c = threadIdx.x & 15, r0 = 4 * (threadIdx.x >> 4);
-    const long long N = p.N;
-    const float* wsq = p.ws + bh * N * kWsChunk;
+// falcon_bwd_chain: one CTA of 128 threads per sequence, the two state scans on the tensor cores.
+// The carried matrix (S forward, dS backward) is kept transposed in tensor memory, lane c = column c
+// (lanes 64-127 zero), as the A operand of one product per step: D = X^T B^T with B = M_n (forward:
+// D = (M_n S)^T) or B = M_n^T (backward: D = (M_n^T dS)^T), both K-major as the prep kernel stores them,
+// loaded by TMA with the 128-byte swizzle. Each operand x is split into hi = x with its low 13 bits
+// cleared (exact in tf32) and lo = x - hi, and D = A_hi B_hi + A_hi B_lo + A_lo B_hi (fp32-accurate).
+// U_n / V_n arrive by 16-byte asynchronous copies one step ahead and are added in registers, where
+// each thread also stores its column of S_n / dS_{n+1} for the gradient kernel. Every wait is bounded:
+// on timeout the CTA raises the device flag, drains what it issued and frees its tensor memory.
+constexpr int kChainT = 128;
+constexpr uint32_t kCAH = 0, kCAL = 64, kCD = 128;  // TMEM columns: carried hi, lo, product
+constexpr long long kTcTimeout = 4000000000LL;     // ~2 s
+namespace chl {
+constexpr int BHI = 0, BLO = 16384;  // B = M_n or M_n^T: two K halves of 64 rows x 128 bytes each
+constexpr int OFS = 32768;           // two offset buffers (U_n or V_n), [64][64] fp32
+constexpr int BAR = OFS + 32768;
+constexpr int BYTES = BAR + 64;
+constexpr int ALLOC = BYTES + 1024;
+}  // namespace chl
 
-    // stage <- (M_n, offset slice `which` of chunk n); an empty group when n is out of range
-    auto issue = [&](long long nck, int which) {
-        if (nck >= 0 && nck < N) {
-            const int st = (int)(((nck % kStages) + kStages) % kStages);
-            const float* m = wsq + nck * kWsChunk + kWsM * kWsMat;
+struct ChainParams {
+    CUtensorMap tm_ws;  // the workspace as [rows][64] fp32, 32 x 32 boxes, 128-byte swizzle
+    BParams p;
+};
+
+__device__ __forceinline__ float hi19(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
+
+__device__ bool chain_wait(uint32_t bar, uint32_t parity) {
+    if (ptx::mbar_try(bar, parity)) return true;
+    const long long t0 = clock64();
+    int spins = 0;
+    while (!ptx::mbar_try(bar, parity)) {
+        if (++spins > 64) __nanosleep(32);
+        if (clock64() - t0 > kTcTimeout) {
+            atomicExch(&g_bwd_timeout_flag, 1);
+            return false;
+        }
+    }
+    return true;
+}
+
+// this thread's carried column into the A operand's hi and lo columns of its lane (no wait)
+__device__ __forceinline__ void chain_put(uint32_t tq, const float (&x)[kD]) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = 4 * (threadIdx.x + u * kChainThreads), row = e >> 6, col = e & 63;
-                cp_async16(Ms + st * kD * kLdc + row * kLdc + col, m + e);
+    for (int q = 0; q < 4; ++q) {
+        uint32_t h[16], l[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float v = x[16 * q + e], vh = hi19(v);
+            h[e] = __float_as_uint(vh);
+            l[e] = __float_as_uint(v - vh);
+        }
+        ptx::tmem_st16(tq + kCAH + 16 * q, h);
+        ptx::tmem_st16(tq + kCAL + 16 * q, l);
+    }
+}
+
+__global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_constant__ ChainParams P) {
+    using namespace ptx;
+    const BParams& p = P.p;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw), base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t bar_full = base + chl::BAR, bar_mma = bar_full + 8, bar_drain = bar_full + 16;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chl::BAR + 32);
+    const long long bh = blockIdx.x, N = p.N;
+    if (tid == 0) {
+        mbar_init(bar_full, 1);
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_drain, 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot, tq = tmem + ((uint32_t)(32 * warp) << 16);
+    const int c = tid;            // carried column = TMEM lane
+    const bool live = c < kD;     // lanes 64-127 hold zeros
+    float* const wsq = p.ws + bh * N * kWsChunk;
+
+    // step k of the 2 N: chunk n, matrix and offset of the pass
+    auto chunk_of = [&](long long k) { return k < N ? k : 2 * N - 1 - k; };
+    auto issue_b = [&](long long k) {  // thread 0: B of step k by TMA
+        const long long n = chunk_of(k);
+        const int r = (int)((bh * N + n) * (kWsChunk / kD) + (k < N ? kWsM : kWsMT) * kD);
+        mbar_expect_tx(bar_full, 16384u);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t d = base + chl::BHI + h * 8192;
+            tma_load_2d(d, &P.tm_ws, 32 * h, r, bar_full);
+            tma_load_2d(d + 4096, &P.tm_ws, 32 * h, r + 32, bar_full);
+        }
+    };
+    auto issue_ofs = [&](long long k) {  // every thread: U_n (forward) or V_n (backward) into buffer k & 1
+        if (k < 2 * N) {
+            const float* src = wsq + chunk_of(k) * kWsChunk + (k < N ? kWsU : kWsV) * kWsMat;
+            float* d = reinterpret_cast<float*>(sm + chl::OFS) + (int)(k & 1) * kWsMat;
+#pragma unroll
+            for (int u = 0; u < kWsMat / 4 / kChainT; ++u) {
+                const int e = 4 * (tid + u * kChainT);
+                cp_async16(d + e, src + e);
             }
-            const int row = threadIdx.x >> 2, q = 4 * (threadIdx.x & 3);
-            cp_async16(Os + (st * kD + row) * kCols + q, wsq + nck * kWsChunk + which * kWsMat + row * kD + cg + q);
         }
         cp_async_commit();
     };
-    // out[r0 + z] = off + sum_k M(r0 + z, k) S(k)   (forward: M(i, k) = Mk[i][k]; backward: M^T, Mk[k][i])
-    auto step = [&](const float* Mk, const float* off, const float* Sc, float* So, bool transpose) {
-        float acc[4] = {off[(r0 + 0) * kCols], off[(r0 + 1) * kCols], off[(r0 + 2) * kCols], off[(r0 + 3) * kCols]};
+
+    float s[kD];
+    auto load_start = [&](const float* src) {
+#pragma unroll
+        for (int r = 0; r < kD; ++r) s[r] = (live && src) ? src[(bh * kD + r) * kD + c] : 0.f;
+        chain_put(tq, s);
+        tmem_wait_st();
+    };
+    load_start(p.S0);
+    long long pending = 0;  // the step whose B is in flight (-1: none)
+    if (tid == 0) issue_b(0);
+    issue_ofs(0);
+    tc_fence_before();
+    __syncthreads();
+    bool ok = true;
+    constexpr uint32_t id = idesc_tf32(128, kD);
+    for (long long k = 0; k < 2 * N; ++k) {
+        const long long n = chunk_of(k);
+        const bool fwd = k < N;
+        if (k == N) {  // the backward scan starts from dS_final
+            load_start(p.dS_final);
+            tc_fence_before();
+            __syncthreads();
+        }
+        bool bad = false;
+        if (tid == 0) bad = !chain_wait(bar_full, (uint32_t)(k & 1));
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (named_bar_or(1, kChainT, bad)) {
+            ok = false;
+            break;
+        }
+        pending = -1;
+        if (live) {  // S_n (forward) / dS_{n+1} (backward) for the gradient kernel, this thread's column
+            float* dst = wsq + n * kWsChunk + (fwd ? kWsS : kWsDS) * kWsMat + c;
+#pragma unroll
+            for (int r = 0; r < kD; ++r) dst[r * kD] = s[r];
+        }
+        {  // B: hi (low 13 bits cleared) in place, lo = the rest
+            float4* bh4 = reinterpret_cast<float4*>(sm + chl::BHI);
+            float4* bl4 = reinterpret_cast<float4*>(sm + chl::BLO);
 #pragma unroll 4
-        for (int k = 0; k < kD; k += 4) {
-            const float4 sv = *reinterpret_cast<const float4*>(Sc + k);
-            const float s4[4] = {sv.x, sv.y, sv.z, sv.w};
-            if (transpose) {
+            for (int e = tid; e < 16384 / 16; e += kChainT) {
+                const float4 v = bh4[e];
+                const float4 h = make_float4(hi19(v.x), hi19(v.y), hi19(v.z), hi19(v.w));
+                bh4[e] = h;
+                bl4[e] = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const float4 mv = *reinterpret_cast<const float4*>(Mk + (k + kk) * kLdc + r0);
-                    acc[0] = fmaf(mv.x, s4[kk], acc[0]);
-                    acc[1] = fmaf(mv.y, s4[kk], acc[1]);
-                    acc[2] = fmaf(mv.z, s4[kk], acc[2]);
-                    acc[3] = fmaf(mv.w, s4[kk], acc[3]);
-                }
-            } else {
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (uint32_t)((ks >> 2) * 8192 + 32 * (ks & 3));
+                const uint64_t dh = desc_k(base + chl::BHI + off), dl = desc_k(base + chl::BLO + off);
+                mma_tf32_ta(tmem + kCD, tmem + kCAH + 8 * ks, dh, id, ks > 0);
+                mma_tf32_ta(tmem + kCD, tmem + kCAH + 8 * ks, dl, id, 1);
+                mma_tf32_ta(tmem + kCD, tmem + kCAL + 8 * ks, dh, id, 1);
+            }
+            mma_commit(bar_mma);
+            bad = !chain_wait(bar_mma, (uint32_t)(k & 1));
+            if (!bad && k + 1 < 2 * N) issue_b(k + 1);  // B is free again
+        }
+        if (named_bar_or(1, kChainT, bad)) {
+            ok = false;
+            break;
+        }
+        if (k + 1 < 2 * N) pending = k + 1;
+        issue_ofs(k + 1);
+        tc_fence_after();
+        {
+            const float* of = reinterpret_cast<const float*>(sm + chl::OFS) + (int)(k & 1) * kWsMat;
+            uint32_t d[4][16];
 #pragma unroll
-                for (int z = 0; z < 4; ++z) {
-                    const float4 mv = *reinterpret_cast<const float4*>(Mk + (r0 + z) * kLdc + k);
-                    acc[z] = fmaf(mv.x, s4[0], fmaf(mv.y, s4[1], fmaf(mv.z, s4[2], fmaf(mv.w, s4[3], acc[z]))));
+            for (int q = 0; q < 4; ++q) tmem_ld16(tq + kCD + 16 * q, d[q]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                regs_ready(d[q]);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int r = 16 * q + e;
+                    s[r] = live ? __uint_as_float(d[q][e]) + of[r * kD + c] : 0.f;
                 }
             }
         }
-        *reinterpret_cast<float4*>(So + r0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    };
-
-    // forward: S_{n+1} = M_n S_n + U_n, storing S_n
-#pragma unroll
-    for (int z = 0; z < 4; ++z) Sv[0][c][r0 + z] = p.S0 ? p.S0[(bh * kD + r0 + z) * kD + cg + c] : 0.f;
-    issue(0, kWsU);
-    issue(1, kWsU);
-    for (long long nck = 0; nck < N; ++nck) {
-        const int b = (int)(nck & 1), st = (int)(nck % kStages);
-        issue(nck + 2, kWsU);
-        cp_async_wait2();
-        __syncthreads();
-        float* wc = p.ws + (bh * N + nck) * kWsChunk + kWsS * kWsMat + cg + c;
-#pragma unroll
-        for (int z = 0; z < 4; ++z) wc[(r0 + z) * kD] = Sv[b][c][r0 + z];
-        step(Ms + st * kD * kLdc, Os + st * kD * kCols + c, Sv[b][c], Sv[b ^ 1][c], false);
+        if (k + 1 < 2 * N && k + 1 != N) chain_put(tq, s);
+        tmem_wait_st();
+        tc_fence_before();
         __syncthreads();
     }
-    // backward: dS_n = M_n^T dS_{n+1} + V_n, storing dS_{n+1}
+    if (ok && p.dS0 && live) {
 #pragma unroll
-    for (int z = 0; z < 4; ++z) Sv[0][c][r0 + z] = p.dS_final ? p.dS_final[(bh * kD + r0 + z) * kD + cg + c] : 0.f;
-    issue(N - 1, kWsV);
-    issue(N - 2, kWsV);
-    int b = 0;
-    for (long long nck = N - 1; nck >= 0; --nck, b ^= 1) {
-        const int st = (int)(nck % kStages);
-        issue(nck - 2, kWsV);
-        cp_async_wait2();
-        __syncthreads();
-        float* wc = p.ws + (bh * N + nck) * kWsChunk + kWsDS * kWsMat + cg + c;
-#pragma unroll
-        for (int z = 0; z < 4; ++z) wc[(r0 + z) * kD] = Sv[b][c][r0 + z];
-        step(Ms + st * kD * kLdc, Os + st * kD * kCols + c, Sv[b][c], Sv[b ^ 1][c], true);
-        __syncthreads();
+        for (int r = 0; r < kD; ++r) p.dS0[(bh * kD + r) * kD + c] = s[r];
     }
-    if (p.dS0)
-#pragma unroll
-        for (int z = 0; z < 4; ++z) p.dS0[(bh * kD + r0 + z) * kD + cg + c] = Sv[b][c][r0 + z];
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (tid == 0 && pending >= 0) mbar_wait_bounded(bar_full, (uint32_t)(pending & 1), kTcTimeout);
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        mma_commit(bar_drain);
+        mbar_wait_bounded(bar_drain, 0, kTcTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // --------------------------------------------------------------------------------------------------
@@ -829,8 +952,12 @@ int launch_typed(const BParams& p, cudaStream_t st) {
     cudaFuncSetAttribute(falcon_bwd_prep<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     cudaFuncSetAttribute(falcon_bwd_grad<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gradSmem(IP));
     falcon_bwd_prep<Tin, IP><<<chunks, kThreads, kPrepSmem, st>>>(p);
-    cudaFuncSetAttribute(falcon_bwd_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
-    falcon_bwd_chain<<<(unsigned)(p.BH * (kD / kCols)), kChainThreads, kChainSmem, st>>>(p);
+    ChainParams cp{};
+    cp.p = p;
+    const long long rows = p.BH * p.N * (kWsChunk / kD);  // the workspace as rows of 64 floats
+    if (rows >= (1LL << 31) || !encode_rows_f32_sw128(&cp.tm_ws, p.ws, rows)) return 4;
+    cudaFuncSetAttribute(falcon_bwd_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chl::ALLOC);
+    falcon_bwd_chain<<<(unsigned)p.BH, kChainT, chl::ALLOC, st>>>(cp);
     falcon_bwd_grad<Tin, IP><<<chunks, kThreads, gradSmem(IP), st>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
@@ -885,6 +1012,14 @@ int launch_bwd(const Launch& a, const BwdArgs& g, cudaStream_t st) {
     const bool ip = a.variant == kF1A;
     if (a.bf16) return ip ? launch_typed<__nv_bfloat16, true>(p, st) : launch_typed<__nv_bfloat16, false>(p, st);
     return ip ? launch_typed<float, true>(p, st) : launch_typed<float, false>(p, st);
+}
+
+int bwd_consume_timeout_flag(int* flag) {
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_bwd_timeout_flag, sizeof(int)) != cudaSuccess) return 1;
+    if (v && cudaMemcpyToSymbol(g_bwd_timeout_flag, &zero, sizeof(int)) != cudaSuccess) return 1;
+    *flag = v;
+    return 0;
 }
 
 }  // namespace falcon

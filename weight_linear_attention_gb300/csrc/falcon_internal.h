@@ -83,6 +83,8 @@ bool scan_supported(const Launch& a);
 size_t scan_workspace_bytes(const Launch& a);
 int launch_scan(const Launch& a, cudaStream_t stream);
 int scan_tc_consume_timeout_flag(int* flag);
+bool encode_rows_f32_sw128(CUtensorMap* tm, const void* ptr, long long rows);  // [rows][64] fp32, 32 x 32 boxes, 128-byte swizzle
+int bwd_consume_timeout_flag(int* flag);
 
 // Backward pass (Falcon-1 and 1A, dk = dv = 64, chunk 64): prep, chain and gradient kernels working
 // through a caller workspace of bwd_workspace_bytes(a) bytes at a.ws. `a` carries the forward inputs.

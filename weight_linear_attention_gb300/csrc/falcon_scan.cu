@@ -468,7 +468,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) falcon_scan_tc_kernel(const __g
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// The workspace as [rows][64] fp32 for TMA: 32 x 32 boxes with the 128-byte swizzle, one 32-element K
+}  // namespace
+
+// A workspace as [rows][64] fp32 for TMA: 32 x 32 boxes with the 128-byte swizzle, one 32-element K
 // half of 32 rows of a K-major tf32 operand per load (cuTensorMapEncodeTiled through the runtime's
 // driver entry point, looked up once).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -494,7 +496,6 @@ bool encode_rows_f32_sw128(CUtensorMap* tm, const void* ptr, long long rows) {
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-}  // namespace
 
 bool scan_supported(const Launch& a) {
     const bool shared = a.variant == kF1 || a.variant == kF1A || a.variant == kF3 || a.variant == kF3A;
