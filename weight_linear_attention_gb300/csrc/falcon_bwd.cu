@@ -27,9 +27,10 @@
 //                     per step): S_{n+1} = M_n S_n + U_n forward, then dS_n = M_n^T dS_{n+1} + V_n
 //                     backward, storing S_n and dS_{n+1};
 //   falcon_bwd_grad   every chunk at once: all input gradients from S_n and dS_{n+1}.
-// The 64 x 64 x 64 products of prep and grad run on the tensor cores as warp-level tf32 MMAs with
-// every fp32 operand split into a tf32 head and remainder (fp32-accurate); the scans, the scalars
-// and the triangular inverse run on the CUDA cores in fp32.
+// prep and grad run one 128-thread CTA per chunk, two per SM, every 64 x 64 x 64 product a tcgen05
+// bf16 product with the fp32 operands split into bf16 hi and lo parts (hi*hi + hi*lo + lo*hi, fp32
+// sums in tensor memory); the scalars, the per-element factors and the triangular inverse run on the
+// CUDA cores in fp32.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -44,11 +45,10 @@ __device__ int g_bwd_timeout_flag = 0;
 
 namespace {
 
+using namespace ptx;
+
 constexpr int kD = 64;        // dk = dv
 constexpr int kC = 64;        // chunk length
-constexpr int kLd = 68;       // shared-memory row stride (floats): 16-byte rows, tensor-core fragments
-constexpr int kMat = kC * kLd;
-constexpr int kThreads = 512;       // prep and gradient kernels: 16 warps
 constexpr int kWsMat = kD * kD;             // floats per workspace matrix
 constexpr int kWsChunk = 7 * kWsMat;        // M, U, V, T, S_n, dS_{n+1}, M^T
 enum { kWsM = 0, kWsU = 1, kWsV = 2, kWsT = 3, kWsS = 4, kWsDS = 5, kWsMT = 6 };
@@ -82,78 +82,190 @@ struct Scal {
     float eLC;
 };
 
-// Tile loads: every thread issues all of its 16-byte loads of the chunk's tiles before it stores
-// any of them to shared memory, so their latencies overlap.
-__device__ __forceinline__ void put(float* d, const uint4& v, const float*) {
-    d[0] = __uint_as_float(v.x);
-    d[1] = __uint_as_float(v.y);
-    d[2] = __uint_as_float(v.z);
-    d[3] = __uint_as_float(v.w);
-}
-__device__ __forceinline__ void put(float* d, const uint4& v, const __nv_bfloat16*) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+
+// ================================================================================================
+// Chunk kernels on the tensor cores: one 128-thread CTA per chunk, thread t reading and writing TMEM
+// lane t (warp w: lanes 32 w .. 32 w + 31). Every operand is a 64 x 64 bf16 tile in shared memory
+// (128-byte rows, the 128-byte swizzle), usable K-major or MN-major, or a 128-row A operand in TMEM.
+// An fp32 operand x enters as two tiles, hi = bf16(x) and lo = bf16(x - hi), and a product as
+// hi*hi + hi*lo + lo*hi with fp32 sums in TMEM: every operand element keeps ~16 significant bits.
+// The inputs of a bf16 call are exact tiles without a lo part. Each product is tcgen05 kind::f16 with
+// M = 128 (two stacked 64-row operands, or one whose second half is read and its result rows unused),
+// N = 64 or 128 and K = 64, issued by one thread; the per-element work between products runs on the
+// row (or column) the thread's lane holds.
+
+constexpr int kCT = 128;                        // threads of a chunk CTA
+constexpr int kTile = 8192;                     // one 64 x 64 bf16 tile
+constexpr int kAS = 68;                         // row stride (floats) of the matrix the inverse works on
+constexpr long long kCTimeout = 4000000000LL;   // ~2 s
+
+struct Opd {  // one operand of a 64-deep product
+    uint32_t addr, lbo;
+    int kind;  // 0: K-major tile(s); 1: MN-major (lbo: bytes to the second 64-wide atom); 2: TMEM A
+};
+__device__ __forceinline__ Opd kmaj(uint32_t a) { return Opd{a, 0u, 0}; }
+__device__ __forceinline__ Opd mnmaj(uint32_t a, uint32_t lbo = kTile) { return Opd{a, lbo, 1}; }
+__device__ __forceinline__ Opd tmem_a(uint32_t col) { return Opd{col, 0u, 2}; }
+
+// d (+)= A B, M = 128, K = 64 (four steps of 16), N = n (64 or 128).
+__device__ __forceinline__ void mma64(uint32_t d, const Opd& a, const Opd& b, uint32_t n, bool acc) {
+    const uint32_t id = idesc_bf16(128, n, a.kind == 1, b.kind == 1);
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        d[2 * h] = __uint_as_float(w[h] << 16);
-        d[2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
+    for (int ks = 0; ks < 4; ++ks) {
+        const uint64_t bd = b.kind == 1 ? desc_mn(b.addr + 2048 * ks, b.lbo) : desc_k(b.addr + 32 * ks);
+        const uint32_t ac = (acc || ks > 0) ? 1u : 0u;
+        if (a.kind == 2)
+            mma_bf16_ta(d, a.addr + 8 * ks, bd, id, ac);
+        else
+            mma_bf16(d, a.kind == 1 ? desc_mn(a.addr + 2048 * ks, a.lbo) : desc_k(a.addr + 32 * ks), bd, id, ac);
     }
 }
 
-// Rows t0 .. t0 + nr - 1 of the [BH, T, 64] tensors k (shifted: x_t = k_{t-1}, row -1 the tail key or
-// zero), q, v and dout into four shared 64 x 64 tiles (zero rows past nr).
+// 16 NQ consecutive TMEM columns of this thread's lane (one wait).
+template <int NQ>
+__device__ __forceinline__ void tld(uint32_t taddr, float* v) {
+    uint32_t r[NQ][16];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) tmem_ld16(taddr + 16 * q, r[q]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        regs_ready(r[q]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[16 * q + e] = __uint_as_float(r[q][e]);
+    }
+}
+// v[0..63] as this lane's row of a bf16 A operand: hi pairs to columns hc .. hc + 31, lo pairs to
+// lc .. lc + 31 (element k in the low half of column k / 2 when k is even). No wait.
+__device__ __forceinline__ void tst_a(uint32_t hc, uint32_t lc, const float* v) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        uint32_t h[16], l[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) split2(v[32 * q + 2 * e], v[32 * q + 2 * e + 1], h[e], l[e]);
+        tmem_st16(hc + 16 * q, h);
+        tmem_st16(lc + 16 * q, l);
+    }
+}
+
+// Eight elements of a row (from byte offset `off` of the tile, an sw128 offset) as fp32; for fp32
+// inputs hi + lo.
+template <bool EX>
+__device__ __forceinline__ void row8(const uint8_t* hi, const uint8_t* lo, uint32_t off, float* v) {
+    unpack8(*reinterpret_cast<const uint4*>(hi + off), v);
+    if (!EX) {
+        float w[8];
+        unpack8(*reinterpret_cast<const uint4*>(lo + off), w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] += w[e];
+    }
+}
+template <bool EX>
+__device__ __forceinline__ float elem(const uint8_t* hi, const uint8_t* lo, uint32_t off) {
+    float x = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(hi + off));
+    if (!EX) x += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(lo + off));
+    return x;
+}
+// Four fp32 values as bf16 hi and lo at `off` of two tiles (8 bytes each).
+__device__ __forceinline__ void put4_hilo(uint8_t* hi, uint8_t* lo, uint32_t off, float4 v) {
+    uint32_t h0, l0, h1, l1;
+    split2(v.x, v.y, h0, l0);
+    split2(v.z, v.w, h1, l1);
+    *reinterpret_cast<uint2*>(hi + off) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(lo + off) = make_uint2(l0, l1);
+}
+
+__device__ __forceinline__ void cp_async16z(uint32_t dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+
+// Rows r < nr of q, k, v and dout for the chunk's tokens t0 + r (k shifted: token t0 + r - 1, the
+// tail key or zero before the first token) into tiles at byte offsets hi[a] (bf16: asynchronous
+// copies, committed as one group for the caller to wait on) or hi[a] and lo[a] (fp32: through
+// registers). An offset < 0 skips the tensor; rows past nr are zero.
 template <typename Tin>
-__device__ void load_inputs(float* X, float* Q, float* Y, float* dO, const BParams& p, long long bh, long long t0,
-                            int nr) {
-    constexpr int vw = 16 / sizeof(Tin), nv = kC * kD / vw / kThreads;
-    const Tin* src[4] = {static_cast<const Tin*>(p.k), static_cast<const Tin*>(p.q), static_cast<const Tin*>(p.v),
+__device__ void load_chunk(const BParams& p, uint8_t* sm, uint32_t base, const int (&hi)[4], const int (&lo)[4],
+                           long long bh, long long t0, int nr) {
+    const Tin* src[4] = {static_cast<const Tin*>(p.q), static_cast<const Tin*>(p.k), static_cast<const Tin*>(p.v),
                          static_cast<const Tin*>(p.dout)};
-    float* dst[4] = {X, Q, Y, dO};
     const Tin* tail = static_cast<const Tin*>(p.tail);
-    uint4 v[4][nv];
+    const int tid = threadIdx.x;
+    auto row = [&](int a, int r) -> const Tin* {
+        if (r >= nr) return nullptr;
+        const long long t = t0 + r - (a == 1 ? 1 : 0);
+        if (t >= 0) return src[a] + (bh * p.T + t) * kD;
+        return tail ? tail + bh * kD : nullptr;
+    };
+    if constexpr (sizeof(Tin) == 2) {
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < 4; ++a) {
+            if (hi[a] < 0) continue;
 #pragma unroll
-        for (int u = 0; u < nv; ++u) {
-            const int e = (threadIdx.x + u * kThreads) * vw, r = e >> 6, c = e & 63;
-            const long long t = t0 + r - (a == 0 ? 1 : 0);
-            const Tin* ptr = nullptr;
-            if (r < nr) ptr = t >= 0 ? src[a] + (bh * p.T + t) * kD + c : (tail ? tail + bh * kD + c : nullptr);
-            v[a][u] = ptr ? *reinterpret_cast<const uint4*>(ptr) : make_uint4(0u, 0u, 0u, 0u);
+            for (int u = 0; u < 4; ++u) {
+                const int e = tid + kCT * u, r = e >> 3, q8 = e & 7;
+                const Tin* ptr = row(a, r);
+                cp_async16z(base + (uint32_t)hi[a] + sw128(r, 8 * q8), ptr ? ptr + 8 * q8 : src[a], ptr ? 16u : 0u);
+            }
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    } else {
+        float4 v[4][8];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+        for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int u = 0; u < nv; ++u) {
-            const int e = (threadIdx.x + u * kThreads) * vw;
-            put(dst[a] + (e >> 6) * kLd + (e & 63), v[a][u], (const Tin*)nullptr);
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + kCT * u, r = e >> 4, c4 = e & 15;
+                const Tin* ptr = hi[a] >= 0 ? row(a, r) : nullptr;
+                v[a][u] = ptr ? *reinterpret_cast<const float4*>(ptr + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            if (hi[a] < 0) continue;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = tid + kCT * u, r = e >> 4, c4 = e & 15;
+                put4_hilo(sm + hi[a], sm + lo[a], sw128(r, 4 * c4), v[a][u]);
+            }
         }
+    }
 }
 
-// NT dense fp32 64 x 64 workspace matrices into shared tiles.
-template <int NT>
-__device__ void load_ws(float* const (&dst)[NT], const float* const (&src)[NT]) {
-    constexpr int nv = kD * kD / 4 / kThreads;
-    uint4 v[NT][nv];
+// A dense fp32 64 x 64 workspace matrix into hi and lo tiles.
+__device__ void ws_tiles(const float* src, uint8_t* hi, uint8_t* lo) {
+    float4 v[8];
 #pragma unroll
-    for (int a = 0; a < NT; ++a)
+    for (int u = 0; u < 8; ++u) v[u] = reinterpret_cast<const float4*>(src)[threadIdx.x + kCT * u];
 #pragma unroll
-        for (int u = 0; u < nv; ++u) v[a][u] = reinterpret_cast<const uint4*>(src[a])[threadIdx.x + u * kThreads];
+    for (int u = 0; u < 8; ++u) {
+        const int e = threadIdx.x + kCT * u;
+        put4_hilo(hi, lo, sw128(e >> 4, 4 * (e & 15)), v[u]);
+    }
+}
+// Two of them, returning this thread's part of sum(a * b).
+__device__ float ws_tiles2(const float* a, const float* b, uint8_t* ah, uint8_t* al, uint8_t* bh, uint8_t* bl) {
+    float4 x[8], y[8];
 #pragma unroll
-    for (int a = 0; a < NT; ++a)
+    for (int u = 0; u < 8; ++u) {
+        x[u] = reinterpret_cast<const float4*>(a)[threadIdx.x + kCT * u];
+        y[u] = reinterpret_cast<const float4*>(b)[threadIdx.x + kCT * u];
+    }
+    float dot = 0.f;
 #pragma unroll
-        for (int u = 0; u < nv; ++u) {
-            const int e = (threadIdx.x + u * kThreads) * 4;
-            put(dst[a] + (e >> 6) * kLd + (e & 63), v[a][u], (const float*)nullptr);
-        }
+    for (int u = 0; u < 8; ++u) {
+        const int e = threadIdx.x + kCT * u;
+        const uint32_t off = sw128(e >> 4, 4 * (e & 15));
+        put4_hilo(ah, al, off, x[u]);
+        put4_hilo(bh, bl, off, y[u]);
+        dot = fmaf(x[u].x, y[u].x, fmaf(x[u].y, y[u].y, fmaf(x[u].z, y[u].z, fmaf(x[u].w, y[u].w, dot))));
+    }
+    return dot;
 }
 
-// Per-row scalars of the chunk from X (shifted keys), beta and lambda; then the chunk-local log prefixes.
-__device__ void chunk_scalars(Scal& s, const float* X, const BParams& p, long long bh, long long t0, int n) {
+// Per-token scalars of the chunk; thread i < 64 passes nx = ||x_i||^2 of its row. Then the
+// chunk-local log prefixes. All threads call it.
+__device__ void chunk_scalars(Scal& s, float nx, const BParams& p, long long bh, long long t0, int n) {
     const int i = threadIdx.x;
     if (i < kC) {
-        float nx = 0.f;
-#pragma unroll 8
-        for (int c = 0; c < kD; ++c) nx = fmaf(X[i * kLd + c], X[i * kLd + c], nx);
         float eta = 0.f, alpha = 0.f, lm = 0.f, den = 0.f;
         int unc = 0, live = 0;
         if (i < n) {
@@ -205,251 +317,914 @@ __device__ void chunk_scalars(Scal& s, const float* X, const BParams& p, long lo
     __syncthreads();
 }
 
-// 64 x 64 x 64 products on the tensor cores: mma.sync m16n8k8 with tf32 operands and fp32
-// accumulation, each fp32 operand split into a tf32 head and a tf32 remainder and the product taken
-// as head*head + head*rem + rem*head (the remainder products carry the bits tf32 drops, so the
-// result has fp32 accuracy). An operand flagged exact (a bf16 input, which tf32 holds without loss)
-// has no remainder and skips its pass.
-// Warp w (of 16) owns output rows 16 (w >> 2) .. + 15 (one m16 tile) and columns 16 (w & 3) .. + 15
-// (two n8 tiles). acc[m][n]: m = the n8 tile, n = the fragment element (2 * row half + column).
-__device__ __forceinline__ int tile_row(int m, int n) {
-    const int lane = threadIdx.x & 31;
-    (void)m;
-    return 16 * (threadIdx.x >> 7) + (lane >> 2) + 8 * (n >> 1);
-}
-__device__ __forceinline__ int tile_col(int m, int n) {
-    const int lane = threadIdx.x & 31;
-    return 16 * ((threadIdx.x >> 5) & 3) + 8 * m + 2 * (lane & 3) + (n & 1);
-}
-
-// x = head + remainder; the remainder goes to the tensor core as its fp32 bits (the unit reads the top
-// 19 bits of a tf32 operand, i.e. truncates the remainder, which costs at most 2^-10 of it).
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-    hi = ptx::tf32_rn(x);
-    lo = __float_as_uint(x - __uint_as_float(hi));
-}
-
-// acc += A B with A(i, k) = a[i][k] (TA: a[k][i]) and B(k, j) = b[k][j] (TB: b[j][k]).
-template <bool TA, bool TB, bool AX = false, bool BX = false>
-__device__ __forceinline__ void mm(float (&acc)[2][4], const float* a, const float* b) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int r = 16 * (threadIdx.x >> 7) + g, cb = 16 * ((threadIdx.x >> 5) & 3);
-    auto A = [&](int i, int k) { return TA ? a[k * kLd + i] : a[i * kLd + k]; };
-    auto B = [&](int k, int j) { return TB ? b[j * kLd + k] : b[k * kLd + j]; };
-    float cr[2][4] = {};
+// ||x_i||^2 of row i of the key tile(s).
+template <bool EX>
+__device__ __forceinline__ float row_norm(const uint8_t* xh, const uint8_t* xl, int i) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k0 = 0; k0 < kD; k0 += 8) {
-        uint32_t ah[4], al[4], bh[2][2], bl[2][2];
-        {
-            const float x[4] = {A(r, k0 + t), A(r + 8, k0 + t), A(r, k0 + t + 4), A(r + 8, k0 + t + 4)};
+    for (int q8 = 0; q8 < 8; ++q8) {
+        float x[8];
+        row8<EX>(xh, xl, sw128(i, 8 * q8), x);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (AX) ah[e] = __float_as_uint(x[e]), al[e] = 0u;
-                else split_tf32(x[e], ah[e], al[e]);
-            }
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int c = cb + 8 * nt + g;
-            const float y[2] = {B(k0 + t, c), B(k0 + t + 4, c)};
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                if (BX) bh[nt][e] = __float_as_uint(y[e]), bl[nt][e] = 0u;
-                else split_tf32(y[e], bh[nt][e], bl[nt][e]);
-            }
-        }
-        // the three passes in turn over the two tiles, remainder terms into their own accumulators
-        if (!AX)
-#pragma unroll
-            for (int q = 0; q < 2; ++q) ptx::mma1688_tf32(cr[q], al[0], al[1], al[2], al[3], bh[q][0], bh[q][1]);
-        if (!BX)
-#pragma unroll
-            for (int q = 0; q < 2; ++q) ptx::mma1688_tf32(cr[q], ah[0], ah[1], ah[2], ah[3], bl[q][0], bl[q][1]);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) ptx::mma1688_tf32(acc[q], ah[0], ah[1], ah[2], ah[3], bh[q][0], bh[q][1]);
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(x[e], x[e], acc[e]);
     }
-    if (!AX || !BX)
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[q][e] += cr[q][e];
+    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
-__device__ __forceinline__ void zero(float (&acc)[2][4]) {
+// Column sums of a warp's 32 rows: v[0..31] holds this lane's row over 32 columns; returns the sum of
+// column `lane` (each step keeps half of the columns and adds the partner lane's copy of that half).
+template <int M, int N>
+__device__ __forceinline__ void colsum_step(float* v, bool up) {
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int n = 0; n < 4; ++n) acc[m][n] = 0.f;
-}
-
-// Runs the body for each accumulator element acc[m][n] of this thread, at output (i, j); ri and ci
-// index the thread's two rows and four columns (for row_add / col_add).
-#define FOR_TILE(...)                                                         \
-    _Pragma("unroll") for (int m = 0; m < 2; ++m) {                           \
-        _Pragma("unroll") for (int n = 0; n < 4; ++n) {                       \
-            const int i = tile_row(m, n), j = tile_col(m, n);                 \
-            const int ri = n >> 1, ci = 2 * m + (n & 1);                      \
-            (void)ri;                                                         \
-            (void)ci;                                                         \
-            __VA_ARGS__                                                       \
-        }                                                                     \
-    }
-
-// arr[i] += sign * scale[i] * (sum over the whole row of this CTA's partial sums v[ri]).
-__device__ __forceinline__ void row_add(float* arr, const float (&v)[2], const float* scale = nullptr,
-                                        float sign = 1.f) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int ri = 0; ri < 2; ++ri) {
-        float x = v[ri];
-        x += __shfl_xor_sync(0xffffffffu, x, 1);
-        x += __shfl_xor_sync(0xffffffffu, x, 2);
-        const int i = tile_row(0, 2 * ri);
-        if ((lane & 3) == 0) atomicAdd(&arr[i], sign * (scale ? scale[i] : 1.f) * x);
+    for (int k = 0; k < N / 2; ++k) {
+        const float send = up ? v[k] : v[k + N / 2];
+        const float keep = up ? v[k + N / 2] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, M);
     }
 }
-// arr[j] += sign * (sum over the whole column of the partial sums v[ci]).
-__device__ __forceinline__ void col_add(float* arr, const float (&v)[4], float sign = 1.f) {
+__device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
     const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int ci = 0; ci < 4; ++ci) {
-        float x = v[ci];
-        x += __shfl_xor_sync(0xffffffffu, x, 4);
-        x += __shfl_xor_sync(0xffffffffu, x, 8);
-        x += __shfl_xor_sync(0xffffffffu, x, 16);
-        if ((lane >> 2) == 0) atomicAdd(&arr[tile_col(ci >> 1, ci & 1)], sign * x);
-    }
+    colsum_step<16, 32>(v, lane & 16);
+    colsum_step<8, 16>(v, lane & 8);
+    colsum_step<4, 8>(v, lane & 4);
+    colsum_step<2, 4>(v, lane & 2);
+    colsum_step<1, 2>(v, lane & 1);
+    return v[0];
 }
 
-// T = (I + A)^-1 for a strictly lower 64 x 64 A: the four 16 x 16 diagonal blocks by forward
-// substitution (one warp each, a lane per column), then two levels of block combination,
-// [L11 0; L21 L22]^-1 = [T11 0; -T22 L21 T11, T22], with 16- and then 32-row blocks.
-// W: scratch of 32 rows.
-__device__ void unit_lower_inverse(float* Tm, const float* A, float* W) {
-    for (int e = threadIdx.x; e < kC * kLd; e += kThreads) Tm[e] = 0.f;
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp < 4 && lane < 16) {
-        const int b0 = 16 * warp, c = b0 + lane;
-        Tm[c * kLd + c] = 1.f;
-        __syncwarp(0xffffu);
-        for (int i = b0 + 1; i < b0 + 16; ++i) {
-            if (c < i) {
-                float a = 0.f;
-                for (int j = c; j < i; ++j) a = fmaf(A[i * kLd + j], Tm[j * kLd + c], a);
-                Tm[i * kLd + c] = -a;
-            }
-            __syncwarp(0xffffu);
+// T = (I + A)^{-1} in place for the strictly lower 64 x 64 A in M (fp32, stride kAS; zero on and above
+// the diagonal on entry, T with its unit diagonal on exit): the four 16 x 16 diagonal blocks by
+// right-looking column substitution (one thread per column), then two levels of block merges,
+// T_ba = -T_bb (A_ba T_aa), through the scratch W (32 x 33 floats). All threads call it.
+__device__ void invert128(float* M, float* W) {
+    const int tid = threadIdx.x;
+    float x[16];
+    if (tid < 64) {
+        const int b = tid >> 4, c = tid & 15;
+        const float* Ab = M + 16 * b * kAS + 16 * b;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = r == c ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 0; r < 15; ++r) {
+            float col[15];
+#pragma unroll
+            for (int s2 = r + 1; s2 < 16; ++s2) col[s2 - r - 1] = Ab[s2 * kAS + r];
+#pragma unroll
+            for (int s2 = r + 1; s2 < 16; ++s2) x[s2] = fmaf(-col[s2 - r - 1], x[r], x[s2]);
         }
     }
     __syncthreads();
-    for (int h = 16; h < kC; h *= 2) {
-        const int nb = kC / (2 * h);
-        for (int e = threadIdx.x; e < nb * h * h; e += kThreads) {  // W = L21 T11 (T11 lower: k >= cc)
+    if (tid < 64) {
+        const int b = tid >> 4, c = tid & 15;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) M[(16 * b + r) * kAS + 16 * b + c] = x[r];
+    }
+    __syncthreads();
+    for (int h = 16; h < 64; h *= 2) {
+        const int nb = 64 / (2 * h);
+        for (int e = tid; e < nb * h * h; e += kCT) {  // W = A_ba T_aa (T_aa lower: k >= cc)
             const int blk = e / (h * h), rr = (e / h) % h, cc = e % h, r0 = 2 * h * blk;
             float a = 0.f;
-            for (int k = cc; k < h; ++k) a = fmaf(A[(r0 + h + rr) * kLd + r0 + k], Tm[(r0 + k) * kLd + r0 + cc], a);
-            W[(blk * h + rr) * kLd + cc] = a;
+            for (int k = cc; k < h; ++k) a = fmaf(M[(r0 + h + rr) * kAS + r0 + k], M[(r0 + k) * kAS + r0 + cc], a);
+            W[(blk * h + rr) * 33 + cc] = a;
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < nb * h * h; e += kThreads) {  // T21 = -T22 W (T22 lower: k <= rr)
+        for (int e = tid; e < nb * h * h; e += kCT) {  // T_ba = -T_bb W (T_bb lower: k <= rr)
             const int blk = e / (h * h), rr = (e / h) % h, cc = e % h, r0 = 2 * h * blk;
             float a = 0.f;
-            for (int k = 0; k <= rr; ++k) a = fmaf(Tm[(r0 + h + rr) * kLd + r0 + h + k], W[(blk * h + k) * kLd + cc], a);
-            Tm[(r0 + h + rr) * kLd + r0 + cc] = -a;
+            for (int k = 0; k <= rr; ++k) a = fmaf(M[(r0 + h + rr) * kAS + r0 + h + k], W[(blk * h + k) * 33 + cc], a);
+            M[(r0 + h + rr) * kAS + r0 + cc] = -a;
         }
         __syncthreads();
     }
+}
+
+// Waits of the chunk kernels: thread 0 waits for the next phase of the MMA barrier (bounded); every
+// thread learns whether it completed.
+struct ChunkSync {
+    uint32_t bar, mph;
+    __device__ bool wait() {
+        bool bad = false;
+        if (threadIdx.x == 0) {
+            bad = !mbar_wait_bounded(bar, mph & 1u, kCTimeout);
+            if (bad) atomicExch(&g_bwd_timeout_flag, 1);
+        }
+        ++mph;
+        const bool any = __syncthreads_or(bad) != 0;
+        tc_fence_after();
+        return !any;
+    }
+    // shared-memory and TMEM writes of every thread are visible to the tensor cores
+    __device__ void publish() {
+        fence_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        __syncthreads();
+    }
+    // nothing issued is still running (waits at most the timeout), then TMEM is freed
+    __device__ void finish(uint32_t tmem, uint32_t cols) {
+        tc_fence_before();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            mma_commit(bar + 8);
+            mbar_wait_bounded(bar + 8, 0, kCTimeout);
+        }
+        __syncthreads();
+        tc_fence_after();
+        if ((threadIdx.x >> 5) == 0) tmem_dealloc(tmem, cols);
+    }
+};
+
+// Shared-memory layout of the chunk kernels (bytes from the 1024-aligned base): 8 KB tile slots, then
+// (prep, Falcon-1) the fp32 matrix of the inverse, the scalars and the barriers.
+template <bool EX, bool IP>
+struct PrepLay {
+    // Falcon-1:  Q X [QL XL] DO [DOL] DXH YH DXL [YL] TH TL AOH AOL   ([..]: fp32 inputs only)
+    // Falcon-1A: WXH Q YH EDH WXL [QL YL] EDL X [XL] DO [DOL]
+    enum : int {
+        Q = IP ? 1 : 0,
+        X = IP ? (EX ? 5 : 8) : 1,
+        QL = EX ? -1 : (IP ? 5 : 2),
+        XL = EX ? -1 : (IP ? 9 : 3),
+        DO = IP ? (EX ? 6 : 10) : (EX ? 2 : 4),
+        DOL = EX ? -1 : (IP ? 11 : 5),
+        DXH = EX ? 3 : 6,
+        YH = IP ? 2 : (EX ? 4 : 7),
+        DXL = EX ? 5 : 8,
+        YL = EX ? -1 : (IP ? 6 : 9),
+        TH = EX ? 6 : 10,
+        TL = TH + 1,
+        AOH = TH + 2,
+        AOL = TH + 3,
+        WXH = 0,
+        EDH = 3,
+        WXL = 4,
+        EDL = 7,
+        NT = IP ? (EX ? 8 : 12) : (EX ? 10 : 14),
+        AT = NT * kTile,                          // Falcon-1: the fp32 matrix of the inverse
+        SCAL = AT + (IP ? 0 : 64 * kAS * 4),
+        BAR = SCAL + (int)(sizeof(Scal) + 15) / 16 * 16,
+        BYTES = BAR + 64,
+        ALLOC = BYTES + 1024,
+        COLS = IP ? 128 : 256                     // TMEM columns
+    };
+};
+template <bool EX, bool IP>
+struct GradLay {
+    // Q X [QL XL] DO [DOL] | YZ ZL PRH SH PRL SL TH TL DSH DSL, then the scalars, the gradient
+    // accumulators and the barriers. Roles of the shared slots over the kernel:
+    //   YZ, ZL   Y (Falcon-1; its lo part in ZL) -> Z -> dR; Falcon-1A: P; then dSc_hi, dGs_hi
+    //   PRH, PRL P -> R (Falcon-1); Falcon-1A: Y
+    //   TH, TL   T (Falcon-1); then dSc_lo, dGs_lo
+    // Adjacent pairs serve as stacked K-major operands: [Q; X], [YZ; ZL], [PRH; SH], [PRL; SL], [TH; TL].
+    enum : int {
+        Q = 0,
+        X = 1,
+        QL = EX ? -1 : 2,
+        XL = EX ? -1 : 3,
+        DO = EX ? 2 : 4,
+        DOL = EX ? -1 : 5,
+        YZ = EX ? 3 : 6,
+        ZL = YZ + 1,
+        PRH = YZ + 2,
+        SH = YZ + 3,
+        PRL = YZ + 4,
+        SL = YZ + 5,
+        TH = YZ + 6,
+        TL = YZ + 7,
+        DSH = YZ + 8,
+        DSL = YZ + 9,
+        NT = YZ + 10,
+        SCAL = NT * kTile,
+        ACC = SCAL + (int)(sizeof(Scal) + 15) / 16 * 16,  // deta dL dLx dw c2 [64], red [4]
+        BAR = ACC + (5 * kC + 4) * 4,
+        BYTES = BAR + 64,
+        ALLOC = BYTES + 1024
+    };
+};
+
+// --------------------------------------------------------------------------------------------------
+// falcon_bwd_prep: per chunk T, the forward transition M (and M^T), U = X^T diag(w) T Y and
+// V = Ao^T dO with Ao = diag(e^L) Q - P T diag(e^Lx) X (the chunk's read of its start state).
+// Falcon-1, as products: [Sc; G] = [Q; X] X^T; P and A from them; T = (I + A)^{-1} on the CUDA cores;
+// E = [P; X^T diag(w)] T; E [diag(e^Lx) X | Y] = [P T diag(e^Lx) X, . ; K, U] with M = e^{L_C} I - K;
+// V = Ao^T dO. Falcon-1A (T = I, K = 0): [U, . ; ., V] = [(diag(w) X)^T ; Q^T] [Y | diag(e^L) dO].
+template <typename Tin, bool IP>
+__global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep(const BParams p) {
+    constexpr bool EX = sizeof(Tin) == 2;
+    using L = PrepLay<EX, IP>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw), base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    auto TP = [&](int slot) { return sm + slot * kTile; };
+    auto TA = [&](int slot) { return base + (uint32_t)(slot * kTile); };
+    const int tid = threadIdx.x, warp = tid >> 5;
+    Scal& s = *reinterpret_cast<Scal*>(sm + L::SCAL);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BAR + 16);
+    ChunkSync cs{base + L::BAR, 0u};
+    const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N, t0 = nck * kC;
+    const int nr = (int)min((long long)kC, p.T - t0);
+    float* ws = p.ws + cid * kWsChunk;
+
+    if (tid == 0) {
+        mbar_init(cs.bar, 1);
+        mbar_init(cs.bar + 8, 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(tslot), L::COLS);
+    {
+        const int hi[4] = {L::Q * kTile, L::X * kTile, L::YH * kTile, L::DO * kTile};
+        const int lo[4] = {L::QL * kTile, L::XL * kTile, L::YL * kTile, L::DOL * kTile};
+        load_chunk<Tin>(p, sm, base, hi, lo, bh, t0, nr);
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    cs.publish();
+    tc_fence_after();
+    const uint32_t tmem = *tslot, tq = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint8_t* xl = EX ? nullptr : TP(L::XL);
+    bool ok = true;
+
+    if constexpr (!IP) {
+        if (tid == 0) {  // [Sc; G] = [Q; X] X^T into columns 0-63
+            tc_fence_after();
+            mma64(tmem, kmaj(TA(L::Q)), kmaj(TA(L::X)), 64, false);
+            if constexpr (!EX) {
+                mma64(tmem, kmaj(TA(L::Q)), kmaj(TA(L::XL)), 64, true);
+                mma64(tmem, kmaj(TA(L::QL)), kmaj(TA(L::X)), 64, true);
+            }
+            mma_commit(cs.bar);
+        }
+        chunk_scalars(s, tid < kC ? row_norm<EX>(TP(L::X), xl, tid) : 0.f, p, bh, t0, nr);
+        ok = cs.wait();
+        float* AT = reinterpret_cast<float*>(sm + L::AT);
+        if (ok) {
+            if (tid < 64) {  // P row i into the A operand (columns 64-127, rows 0-63); diag(e^Lx) X row i
+                const int i = tid;
+                const float li = s.L[i];
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float v[32];
+                    tld<2>(tq + 32 * h, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int j = 32 * h + e;
+                        v[e] = j <= i ? s.eta[j] * expf(fminf(li - s.L[j], 0.f)) * v[e] : 0.f;
+                    }
+                    uint32_t hh[16], ll[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) split2(v[2 * e], v[2 * e + 1], hh[e], ll[e]);
+                    tmem_st16(tq + 64 + 16 * h, hh);
+                    tmem_st16(tq + 96 + 16 * h, ll);
+                }
+                const float di = s.eLx[i];
+#pragma unroll
+                for (int q8 = 0; q8 < 8; ++q8) {
+                    float x[8];
+                    row8<EX>(TP(L::X), xl, sw128(i, 8 * q8), x);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] *= di;
+                    st8_hilo(TP(L::DXH), TP(L::DXL), sw128(i, 8 * q8), x);
+                }
+            } else {  // A row f (fp32, for the inverse); X^T diag(w) row f into the A operand
+                const int f = tid - 64;
+                const float lx = s.Lx[f];
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float v[32];
+                    tld<2>(tq + 32 * h, v);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int j = 32 * h + e;
+                        v[e] = j < f ? s.eta[j] * expf(fminf(lx - s.L[j], 0.f)) * v[e] : 0.f;
+                    }
+                    float4* dst = reinterpret_cast<float4*>(AT + f * kAS + 32 * h);
+#pragma unroll
+                    for (int k4 = 0; k4 < 8; ++k4) dst[k4] = make_float4(v[4 * k4], v[4 * k4 + 1], v[4 * k4 + 2], v[4 * k4 + 3]);
+                }
+                float v[64];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) v[j] = elem<EX>(TP(L::X), xl, sw128(j, f)) * s.w[j];
+                tst_a(tq + 64, tq + 96, v);
+            }
+            cs.publish();
+            invert128(AT, reinterpret_cast<float*>(TP(L::TH)));
+            {  // T to its hi / lo tiles and to the workspace
+                const int r = tid >> 1, c0 = 32 * (tid & 1);
+                float v[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = AT[r * kAS + c0 + e];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st8_hilo(TP(L::TH), TP(L::TL), sw128(r, c0 + 8 * q), v + 8 * q);
+                float4* dst = reinterpret_cast<float4*>(ws + kWsT * kWsMat + r * kD + c0);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+            cs.publish();
+            if (tid == 0) {  // E = [P; X^T diag(w)] T into columns 128-191
+                tc_fence_after();
+                mma64(tmem + 128, tmem_a(tmem + 64), mnmaj(TA(L::TH)), 64, false);
+                mma64(tmem + 128, tmem_a(tmem + 64), mnmaj(TA(L::TL)), 64, true);
+                mma64(tmem + 128, tmem_a(tmem + 96), mnmaj(TA(L::TH)), 64, true);
+                mma_commit(cs.bar);
+            }
+            ok = cs.wait();
+        }
+        if (ok) {
+            {  // E as the next A operand
+                float v[64];
+                tld<4>(tq + 128, v);
+                tst_a(tq + 64, tq + 96, v);
+            }
+            cs.publish();
+            if (tid == 0) {  // E [diag(e^Lx) X | Y] into columns 128-255
+                tc_fence_after();
+                const Opd bh = mnmaj(TA(L::DXH), (uint32_t)((L::YH - L::DXH) * kTile));
+                mma64(tmem + 128, tmem_a(tmem + 64), bh, 128, false);
+                if constexpr (EX)
+                    mma64(tmem + 128, tmem_a(tmem + 64), mnmaj(TA(L::DXL)), 64, true);
+                else
+                    mma64(tmem + 128, tmem_a(tmem + 64), mnmaj(TA(L::DXL), (uint32_t)((L::YL - L::DXL) * kTile)), 128, true);
+                mma64(tmem + 128, tmem_a(tmem + 96), bh, 128, true);
+                mma_commit(cs.bar);
+            }
+            ok = cs.wait();
+        }
+        if (ok) {
+            if (tid < 64) {  // Ao row i = e^{L_i} q_i - (P T diag(e^Lx) X)_i as hi / lo tiles
+                const int i = tid;
+                const float ei = s.eL[i];
+                const uint8_t* ql = EX ? nullptr : TP(L::QL);
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float v[32];
+                    tld<2>(tq + 128 + 32 * h, v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float x[8];
+                        row8<EX>(TP(L::Q), ql, sw128(i, 32 * h + 8 * q), x);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = fmaf(ei, x[e], -v[8 * q + e]);
+                        st8_hilo(TP(L::AOH), TP(L::AOL), sw128(i, 32 * h + 8 * q), x);
+                    }
+                }
+            } else {  // M row f = e^{L_C} e_f - K_f (and M^T column f), U row f
+                const int f = tid - 64;
+                const float gC = s.eLC;
+                float* Mr = ws + kWsM * kWsMat + f * kD;
+                float* MT = ws + kWsMT * kWsMat + f;
+                float* Ur = ws + kWsU * kWsMat + f * kD;
+#pragma unroll 1
+                for (int h = 0; h < 4; ++h) {
+                    float v[32];
+                    tld<2>(tq + 128 + 32 * h, v);
+                    if (h < 2) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int c = 32 * h + e;
+                            v[e] = (c == f ? gC : 0.f) - v[e];
+                            MT[c * kD] = v[e];
+                        }
+                    }
+                    float4* dst = reinterpret_cast<float4*>((h < 2 ? Mr : Ur) + 32 * (h & 1));
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+            }
+            cs.publish();
+            if (tid == 0) {  // V = Ao^T dO into columns 0-63
+                tc_fence_after();
+                mma64(tmem, mnmaj(TA(L::AOH)), mnmaj(TA(L::DO)), 64, false);
+                mma64(tmem, mnmaj(TA(L::AOL)), mnmaj(TA(L::DO)), 64, true);
+                if constexpr (!EX) mma64(tmem, mnmaj(TA(L::AOH)), mnmaj(TA(L::DOL)), 64, true);
+                mma_commit(cs.bar);
+            }
+            ok = cs.wait();
+        }
+        if (ok && tid < 64) {
+            float v[64];
+            tld<4>(tq, v);
+            float4* dst = reinterpret_cast<float4*>(ws + kWsV * kWsMat + tid * kD);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+    } else {
+        chunk_scalars(s, tid < kC ? row_norm<EX>(TP(L::X), xl, tid) : 0.f, p, bh, t0, nr);
+        if (tid < 64) {  // diag(w) X and diag(e^L) dO, row j, as hi / lo tiles
+            const int j = tid;
+            const float wj = s.w[j], ej = s.eL[j];
+            const uint8_t* dl = EX ? nullptr : TP(L::DOL);
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8) {
+                const uint32_t off = sw128(j, 8 * q8);
+                float x[8], d[8];
+                row8<EX>(TP(L::X), xl, off, x);
+                row8<EX>(TP(L::DO), dl, off, d);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    x[e] *= wj;
+                    d[e] *= ej;
+                }
+                st8_hilo(TP(L::WXH), TP(L::WXL), off, x);
+                st8_hilo(TP(L::EDH), TP(L::EDL), off, d);
+            }
+        }
+        cs.publish();
+        if (tid == 0) {  // [U, . ; ., V] = [(diag(w) X)^T ; Q^T] [Y | diag(e^L) dO] into columns 0-127
+            tc_fence_after();
+            const Opd ah = mnmaj(TA(L::WXH), (uint32_t)((L::Q - L::WXH) * kTile));
+            const Opd bh = mnmaj(TA(L::YH), (uint32_t)((L::EDH - L::YH) * kTile));
+            mma64(tmem, ah, bh, 128, false);
+            if constexpr (EX) {
+                mma64(tmem + 64, ah, mnmaj(TA(L::EDL)), 64, true);
+                mma64(tmem, mnmaj(TA(L::WXL)), mnmaj(TA(L::YH)), 64, true);
+            } else {
+                mma64(tmem, ah, mnmaj(TA(L::YL), (uint32_t)((L::EDL - L::YL) * kTile)), 128, true);
+                mma64(tmem, mnmaj(TA(L::WXL), (uint32_t)((L::QL - L::WXL) * kTile)), bh, 128, true);
+            }
+            mma_commit(cs.bar);
+        }
+        ok = cs.wait();
+        if (ok) {
+            const int f = tid & 63;
+            float v[64];
+            tld<4>(tq + (tid < 64 ? 0 : 64), v);
+            float4* dst = reinterpret_cast<float4*>(ws + (tid < 64 ? kWsU : kWsV) * kWsMat + f * kD);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            if (tid < 64) {  // M = M^T = e^{L_C} I
+                float4* m = reinterpret_cast<float4*>(ws + kWsM * kWsMat + f * kD);
+                float4* mt = reinterpret_cast<float4*>(ws + kWsMT * kWsMat + f * kD);
+                const float g = s.eLC;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float4 z = make_float4(4 * q == f ? g : 0.f, 4 * q + 1 == f ? g : 0.f, 4 * q + 2 == f ? g : 0.f,
+                                                 4 * q + 3 == f ? g : 0.f);
+                    m[q] = z;
+                    mt[q] = z;
+                }
+            }
+        }
+    }
+    cs.finish(tmem, L::COLS);
 }
 
 // --------------------------------------------------------------------------------------------------
-// falcon_bwd_prep: one CTA per chunk.
+// falcon_bwd_grad: every input gradient of one chunk from S_n, dS_{n+1} and T. Falcon-1, as products:
+//   [X S | X dS'] and [Sc; G] = [Q; X] X^T; Z = Y - diag(e^Lx) X S and P from them;
+//   R = T Z and P^T dO, so dR = P^T dO + diag(w) X dS'; dZ = T^T dR (= dV);
+//   [dO; dZ] [R^T | S^T] = [dP, dO S^T ; -dA, dZ S^T]; dSc and dG (then dG + dG^T) from dP and dA;
+//   [dSc; dG + dG^T] X, dSc^T Q and R dS'^T; then
+//   dQ = diag(e^L) dO S^T + dSc X,
+//   dX = dSc^T Q + (dG + dG^T) X - diag(e^Lx) dZ S^T + diag(w) R dS'^T + 2 dden x
+// and the scalar gradients (eta, the log prefixes, the clamp, beta, lambda). Falcon-1A: R = Y, no
+// T, Z, dZ, dA. TMEM columns: [0, 128) X S | X dS' -> R -> dZ -> [dP | dO S^T ; -dA | dZ S^T] ->
+// R dS'^T; [128, 192) [Sc; G] -> dSc^T Q; [192, 256) P^T dO -> the [dO; dZ] operand -> [dSc; dGs] X.
 template <typename Tin, bool IP>
-__global__ void __launch_bounds__(kThreads, 1) falcon_bwd_prep(const BParams p) {
-    extern __shared__ __align__(16) float sm[];
-    float* X = sm;
-    float* Q = X + kMat;
-    float* Y = Q + kMat;
-    float* dO = Y + kMat;
-    float* A = dO + kMat;
-    float* Tm = A + kMat;
-    float* P = Tm + kMat;
-    float* DX = P + kMat;
-    float* B1 = DX + kMat;
-    float* B2 = B1 + kMat;
-    Scal& s = *reinterpret_cast<Scal*>(B2 + kMat);
-    constexpr bool EX = sizeof(Tin) == 2;  // bf16 inputs are exact tf32 operands
+__global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad(const BParams p) {
+    constexpr bool EX = sizeof(Tin) == 2;
+    using L = GradLay<EX, IP>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw), base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    auto TP = [&](int slot) { return sm + slot * kTile; };
+    auto TA = [&](int slot) { return base + (uint32_t)(slot * kTile); };
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    Scal& s = *reinterpret_cast<Scal*>(sm + L::SCAL);
+    float* deta = reinterpret_cast<float*>(sm + L::ACC);
+    float* dL = deta + kC;
+    float* dLx = dL + kC;
+    float* dw = dLx + kC;
+    float* c2 = dw + kC;
+    float* red = c2 + kC;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BAR + 16);
+    ChunkSync cs{base + L::BAR, 0u};
+    const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N, t0 = nck * kC;
+    const int nr = (int)min((long long)kC, p.T - t0);
+    const float* ws = p.ws + cid * kWsChunk;
+    const uint8_t* xl = EX ? nullptr : TP(L::XL);
+    const uint8_t* ql = EX ? nullptr : TP(L::QL);
 
-    const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N;
-    const long long t0 = nck * kC;
-    const int nr = (int)min((long long)kC, p.T - t0);  // rows of this chunk
-    load_inputs<Tin>(X, Q, Y, dO, p, bh, t0, nr);
-    __syncthreads();
-    chunk_scalars(s, X, p, bh, t0, nr);
-    float* ws = p.ws + cid * kWsChunk;
-    float acc[2][4], acc2[2][4];
-
-    // Falcon-1: P, A and diag(e^Lx) X
-    if (!IP) {
-        zero(acc);
-        mm<false, true, EX, EX>(acc, Q, X);
-        FOR_TILE(P[i * kLd + j] = j <= i ? s.eta[j] * expf(s.L[i] - s.L[j]) * acc[m][n] : 0.f;)
-        zero(acc);
-        mm<false, true, EX, EX>(acc, X, X);
-        FOR_TILE(A[i * kLd + j] = j < i ? s.eta[j] * expf(s.Lx[i] - s.L[j]) * acc[m][n] : 0.f;
-                 DX[i * kLd + j] = s.eLx[i] * X[i * kLd + j];)
+    if (tid == 0) {
+        mbar_init(cs.bar, 1);
+        mbar_init(cs.bar + 8, 1);
+        mbar_init_fence();
     }
-    __syncthreads();
-    if (IP) {
-        // M = e^{L_C} I, U = X^T diag(w) Y, V = Q^T diag(e^L) dO
-        for (int e = threadIdx.x; e < kC * kD; e += kThreads) {
-            const int r = e >> 6, c = e & 63;
-            B2[r * kLd + c] = s.w[r] * Y[r * kLd + c];
-            dO[r * kLd + c] *= s.eL[r];
+    if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
+    {
+        const int yh = IP ? L::PRH : L::YZ, yl = IP ? L::PRL : L::ZL;
+        const int hi[4] = {L::Q * kTile, L::X * kTile, yh * kTile, L::DO * kTile};
+        const int lo[4] = {L::QL * kTile, L::XL * kTile, yl * kTile, L::DOL * kTile};
+        load_chunk<Tin>(p, sm, base, hi, lo, bh, t0, nr);
+    }
+    {
+        float dot = ws_tiles2(ws + kWsS * kWsMat, ws + kWsDS * kWsMat, TP(L::SH), TP(L::SL), TP(L::DSH), TP(L::DSL));
+        if (!IP) ws_tiles(ws + kWsT * kWsMat, TP(L::TH), TP(L::TL));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (lane == 0) red[warp] = dot;  // <dS_{n+1}, S_n>, per warp
+    }
+    if (tid < kC) {
+        deta[tid] = 0.f;
+        dL[tid] = 0.f;
+        dLx[tid] = 0.f;
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    cs.publish();
+    tc_fence_after();
+    const uint32_t tmem = *tslot, tq = tmem + ((uint32_t)(32 * warp) << 16);
+    bool ok = true;
+
+    if (tid == 0) {
+        tc_fence_after();
+        if constexpr (!IP) {  // [X S | X dS'] into columns 0-127
+            const Opd bh = mnmaj(TA(L::SH), (uint32_t)((L::DSH - L::SH) * kTile));
+            mma64(tmem, kmaj(TA(L::X)), bh, 128, false);
+            mma64(tmem, kmaj(TA(L::X)), mnmaj(TA(L::SL), (uint32_t)((L::DSL - L::SL) * kTile)), 128, true);
+            if constexpr (!EX) mma64(tmem, kmaj(TA(L::XL)), bh, 128, true);
+        } else {  // X dS' into columns 64-127
+            mma64(tmem + 64, kmaj(TA(L::X)), mnmaj(TA(L::DSH)), 64, false);
+            mma64(tmem + 64, kmaj(TA(L::X)), mnmaj(TA(L::DSL)), 64, true);
+            if constexpr (!EX) mma64(tmem + 64, kmaj(TA(L::XL)), mnmaj(TA(L::DSH)), 64, true);
+        }
+        mma64(tmem + 128, kmaj(TA(L::Q)), kmaj(TA(L::X)), 64, false);  // [Sc; G]
+        if constexpr (!EX) {
+            mma64(tmem + 128, kmaj(TA(L::Q)), kmaj(TA(L::XL)), 64, true);
+            mma64(tmem + 128, kmaj(TA(L::QL)), kmaj(TA(L::X)), 64, true);
+        }
+        mma_commit(cs.bar);
+    }
+    chunk_scalars(s, tid < kC ? row_norm<EX>(TP(L::X), xl, tid) : 0.f, p, bh, t0, nr);
+    ok = cs.wait();
+
+    // ---- Z (Falcon-1) and P, row i
+    if (ok) {
+        if (tid < 64) {
+            const int i = tid;
+            if constexpr (!IP) {
+                const float di = s.eLx[i];
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float xs[32];
+                    tld<2>(tq + 32 * h, xs);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t off = sw128(i, 32 * h + 8 * q);
+                        float y[8];
+                        row8<EX>(TP(L::YZ), TP(L::ZL), off, y);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) y[e] = fmaf(-di, xs[8 * q + e], y[e]);
+                        st8_hilo(TP(L::YZ), TP(L::ZL), off, y);
+                    }
+                }
+            }
+            const int ph = IP ? L::YZ : L::PRH, pl = IP ? L::ZL : L::PRL;
+            const float li = s.L[i];
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float v[32];
+                tld<2>(tq + 128 + 32 * h, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int j = 32 * h + e;
+                    v[e] = j <= i ? s.eta[j] * expf(fminf(li - s.L[j], 0.f)) * v[e] : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st8_hilo(TP(ph), TP(pl), sw128(i, 32 * h + 8 * q), v + 8 * q);
+            }
+        }
+        cs.publish();
+        if (tid == 0) {
+            tc_fence_after();
+            if constexpr (!IP) {  // R = T Z into columns 0-63
+                mma64(tmem, kmaj(TA(L::TH)), mnmaj(TA(L::YZ)), 64, false);
+                mma64(tmem, kmaj(TA(L::TH)), mnmaj(TA(L::ZL)), 64, true);
+                mma64(tmem, kmaj(TA(L::TL)), mnmaj(TA(L::YZ)), 64, true);
+            }
+            const int ph = IP ? L::YZ : L::PRH, pl = IP ? L::ZL : L::PRL;  // P^T dO into columns 192-255
+            mma64(tmem + 192, mnmaj(TA(ph)), mnmaj(TA(L::DO)), 64, false);
+            mma64(tmem + 192, mnmaj(TA(pl)), mnmaj(TA(L::DO)), 64, true);
+            if constexpr (!EX) mma64(tmem + 192, mnmaj(TA(ph)), mnmaj(TA(L::DOL)), 64, true);
+            mma_commit(cs.bar);
+        }
+        ok = cs.wait();
+    }
+
+    // ---- R (Falcon-1) to tiles; dR = P^T dO + diag(w) X dS' (Falcon-1: tiles; 1A: dV); dw
+    if (ok) {
+        if (tid < 64) {
+            const int i = tid;
+            const float wi = s.w[i];
+            float dwa = 0.f;
+            const uint8_t* yl = EX ? nullptr : TP(L::PRL);
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float xd[32], r[32], d[32];
+                tld<2>(tq + 64 + 32 * h, xd);
+                tld<2>(tq + 192 + 32 * h, d);
+                if constexpr (!IP) {
+                    tld<2>(tq + 32 * h, r);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) st8_hilo(TP(L::PRH), TP(L::PRL), sw128(i, 32 * h + 8 * q), r + 8 * q);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) row8<EX>(TP(L::PRH), yl, sw128(i, 32 * h + 8 * q), r + 8 * q);
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    dwa = fmaf(xd[e], r[e], dwa);
+                    d[e] = fmaf(wi, xd[e], d[e]);
+                }
+                if constexpr (!IP) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) st8_hilo(TP(L::YZ), TP(L::ZL), sw128(i, 32 * h + 8 * q), d + 8 * q);
+                } else if (i < nr) {
+                    float4* dst = reinterpret_cast<float4*>(p.dv + (bh * p.T + t0 + i) * kD + 32 * h);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) dst[q] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+                }
+            }
+            dw[i] = dwa;
+        }
+        if constexpr (!IP) {
+            cs.publish();
+            if (tid == 0) {  // dZ = T^T dR into columns 0-63, rows 64-127 (A: [any; T^T], MN-major)
+                tc_fence_after();
+                const Opd ah = mnmaj(TA(L::SL), (uint32_t)((L::TH - L::SL) * kTile));
+                const Opd al = mnmaj(TA(L::TH), (uint32_t)((L::TL - L::TH) * kTile));
+                mma64(tmem, ah, mnmaj(TA(L::YZ)), 64, false);
+                mma64(tmem, ah, mnmaj(TA(L::ZL)), 64, true);
+                mma64(tmem, al, mnmaj(TA(L::YZ)), 64, true);
+                mma_commit(cs.bar);
+            }
+            ok = cs.wait();
+        }
+    }
+
+    // ---- the A operand [dO; dZ] (columns 192-255: hi, lo); dV = dZ
+    if (ok) {
+        float v[64];
+        if (tid < 64) {
+            const uint8_t* dl = EX ? nullptr : TP(L::DOL);
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8) row8<EX>(TP(L::DO), dl, sw128(tid, 8 * q8), v + 8 * q8);
+            tst_a(tq + 192, tq + 224, v);
+        } else if (!IP) {
+            const int i = tid - 64;
+            tld<4>(tq, v);
+            if (i < nr) {
+                float4* dst = reinterpret_cast<float4*>(p.dv + (bh * p.T + t0 + i) * kD);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+            tst_a(tq + 192, tq + 224, v);
+        }
+        cs.publish();
+        if (tid == 0) {  // [dO; dZ] [R^T | S^T] into columns 0-127 (B: [R; S] K-major, N = 128)
+            tc_fence_after();
+            const Opd ah = tmem_a(tmem + 192), al = tmem_a(tmem + 224);
+            mma64(tmem, ah, kmaj(TA(L::PRH)), 128, false);
+            if constexpr (IP && EX) {
+                mma64(tmem + 64, ah, kmaj(TA(L::SL)), 64, true);
+            } else {
+                mma64(tmem, ah, kmaj(TA(L::PRL)), 128, true);
+                mma64(tmem, al, kmaj(TA(L::PRH)), 128, true);
+            }
+            mma_commit(cs.bar);
+        }
+        ok = cs.wait();
+    }
+
+    // ---- dP (rows 0-63) and dA (rows 64-127): the score and Gram adjoints, the scalar terms
+    if (ok) {
+        if (tid < 64) {
+            const int i = tid;
+            const float li = s.L[i];
+            float rowL = 0.f;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float d[32], sc[32], cE[32], cL[32];
+                tld<2>(tq + 32 * h, d);
+                tld<2>(tq + 128 + 32 * h, sc);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int j = 32 * h + e;
+                    const bool on = j <= i;
+                    const float f = expf(fminf(li - s.L[j], 0.f)), g = d[e];
+                    const float pp = s.eta[j] * f * sc[e];
+                    cE[e] = on ? g * f * sc[e] : 0.f;
+                    cL[e] = on ? g * pp : 0.f;
+                    rowL += cL[e];
+                    d[e] = on ? g * s.eta[j] * f : 0.f;  // dSc
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st8_hilo(TP(L::YZ), TP(L::TH), sw128(i, 32 * h + 8 * q), d + 8 * q);
+                const float ce = warp_colsum32(cE);
+                const float cl = warp_colsum32(cL);
+                atomicAdd(&deta[32 * h + lane], ce);
+                atomicAdd(&dL[32 * h + lane], -cl);
+            }
+            atomicAdd(&dL[i], rowL);
+        } else if constexpr (!IP) {
+            const int i = tid - 64;
+            const float lx = s.Lx[i];
+            float rowX = 0.f;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float d[32], g[32], cE[32], cL[32];
+                tld<2>(tq + 32 * h, d);
+                tld<2>(tq + 128 + 32 * h, g);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int j = 32 * h + e;
+                    const bool on = j < i;
+                    const float f = expf(fminf(lx - s.L[j], 0.f)), da = -d[e];
+                    const float aa = s.eta[j] * f * g[e] * da;
+                    cE[e] = on ? da * f * g[e] : 0.f;
+                    cL[e] = on ? aa : 0.f;
+                    rowX += cL[e];
+                    d[e] = on ? da * s.eta[j] * f : 0.f;  // dG
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st8_hilo(TP(L::ZL), TP(L::TL), sw128(i, 32 * h + 8 * q), d + 8 * q);
+                const float ce = warp_colsum32(cE);
+                const float cl = warp_colsum32(cL);
+                atomicAdd(&deta[32 * h + lane], ce);
+                atomicAdd(&dL[32 * h + lane], -cl);
+            }
+            atomicAdd(&dLx[i], rowX);
+            named_bar(2, 64);  // every row of the strictly lower dG is in place
+            // dG + dG^T: the upper triangle (i, j > i) takes the stored (j, i); only lower entries are read
+            for (int j = i + 1; j < kC; ++j) {
+                const uint32_t src = sw128(j, i), dst = sw128(i, j);
+                *reinterpret_cast<uint16_t*>(TP(L::ZL) + dst) = *reinterpret_cast<const uint16_t*>(TP(L::ZL) + src);
+                *reinterpret_cast<uint16_t*>(TP(L::TL) + dst) = *reinterpret_cast<const uint16_t*>(TP(L::TL) + src);
+            }
+        }
+        cs.publish();
+        if (tid == 0) {
+            tc_fence_after();
+            // [dSc; dG + dG^T] X into columns 192-255
+            mma64(tmem + 192, kmaj(TA(L::YZ)), mnmaj(TA(L::X)), 64, false);
+            mma64(tmem + 192, kmaj(TA(L::TH)), mnmaj(TA(L::X)), 64, true);
+            if constexpr (!EX) mma64(tmem + 192, kmaj(TA(L::YZ)), mnmaj(TA(L::XL)), 64, true);
+            // dSc^T Q into columns 128-191
+            mma64(tmem + 128, mnmaj(TA(L::YZ)), mnmaj(TA(L::Q)), 64, false);
+            mma64(tmem + 128, mnmaj(TA(L::TH)), mnmaj(TA(L::Q)), 64, true);
+            if constexpr (!EX) mma64(tmem + 128, mnmaj(TA(L::YZ)), mnmaj(TA(L::QL)), 64, true);
+            // R dS'^T into columns 0-63
+            mma64(tmem, kmaj(TA(L::PRH)), kmaj(TA(L::DSH)), 64, false);
+            mma64(tmem, kmaj(TA(L::PRH)), kmaj(TA(L::DSL)), 64, true);
+            if constexpr (!(IP && EX)) mma64(tmem, kmaj(TA(L::PRL)), kmaj(TA(L::DSH)), 64, true);
+            mma_commit(cs.bar);
+        }
+        ok = cs.wait();
+    }
+
+    // ---- dQ; the two halves of dX to shared memory; the scalar gradients; dK
+    if (ok) {
+        float* EA = reinterpret_cast<float*>(TP(L::DSH));  // rows 0-63: dSc^T Q + diag(w) R dS'^T
+        float* EB = reinterpret_cast<float*>(TP(L::YZ));   // rows 64-127: dGs X - diag(e^Lx) dZ S^T
+        if (tid < 64) {
+            const int i = tid;
+            const float ei = s.eL[i], wi = s.w[i];
+            float rowL = 0.f;
+            float* dqo = p.dq + (bh * p.T + t0 + i) * kD;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float a[32], b[32], qv[32];
+                tld<2>(tq + 64 + 32 * h, a);   // dO S^T
+                tld<2>(tq + 192 + 32 * h, b);  // dSc X
+#pragma unroll
+                for (int q = 0; q < 4; ++q) row8<EX>(TP(L::Q), ql, sw128(i, 32 * h + 8 * q), qv + 8 * q);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    rowL = fmaf(qv[e], a[e], rowL);
+                    a[e] = fmaf(ei, a[e], b[e]);
+                }
+                if (i < nr) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        reinterpret_cast<float4*>(dqo + 32 * h)[q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+                }
+                tld<2>(tq + 128 + 32 * h, a);  // dSc^T Q
+                tld<2>(tq + 32 * h, b);        // R dS'^T
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4*>(EA + i * kD)[(8 * h + q) ^ (i & 15)] =
+                        make_float4(fmaf(wi, b[4 * q], a[4 * q]), fmaf(wi, b[4 * q + 1], a[4 * q + 1]),
+                                    fmaf(wi, b[4 * q + 2], a[4 * q + 2]), fmaf(wi, b[4 * q + 3], a[4 * q + 3]));
+            }
+            atomicAdd(&dL[i], ei * rowL);
+        } else if constexpr (!IP) {
+            const int i = tid - 64;
+            const float di = s.eLx[i];
+            float rowX = 0.f;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float a[32], b[32], xv[32];
+                tld<2>(tq + 64 + 32 * h, a);   // dZ S^T
+                tld<2>(tq + 192 + 32 * h, b);  // (dG + dG^T) X
+#pragma unroll
+                for (int q = 0; q < 4; ++q) row8<EX>(TP(L::X), xl, sw128(i, 32 * h + 8 * q), xv + 8 * q);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    rowX = fmaf(xv[e], a[e], rowX);
+                    b[e] = fmaf(-di, a[e], b[e]);
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4*>(EB + i * kD)[(8 * h + q) ^ (i & 15)] =
+                        make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+            }
+            atomicAdd(&dLx[i], -di * rowX);
         }
         __syncthreads();
-        zero(acc);
-        mm<true, false, EX, false>(acc, X, B2);
-        zero(acc2);
-        mm<true, false, EX, false>(acc2, Q, dO);
-        FOR_TILE(ws[kWsM * kWsMat + i * kD + j] = i == j ? s.eLC : 0.f;
-                 ws[kWsMT * kWsMat + i * kD + j] = i == j ? s.eLC : 0.f;
-                 ws[kWsU * kWsMat + i * kD + j] = acc[m][n];
-                 ws[kWsV * kWsMat + i * kD + j] = acc2[m][n];)
-        return;
+        // scalars: d eta and dL from w and the chunk-end decay; d log gamma; the clamp; eta = beta / den
+        if (tid < 32) {
+            const int l = tid;
+            float dwsum = 0.f;
+            float dl[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = 2 * l + h;
+                const float ww = dw[j] * s.w[j];
+                dwsum += ww;
+                deta[j] = fmaf(dw[j], expf(s.L[kC - 1] - s.L[j]), deta[j]);
+                dl[h] = dL[j] - ww + (j + 1 < kC ? dLx[j + 1] : 0.f);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dwsum += __shfl_xor_sync(0xffffffffu, dwsum, o);
+            float dss = 0.f;
+#pragma unroll
+            for (int u = 0; u < kCT / 32; ++u) dss += red[u];
+            if (l == 31) dl[1] += dwsum + s.eLC * dss;
+            // suffix sums: d log gamma_u = sum_{i >= u} dL_i
+            float v = dl[0] + dl[1];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_down_sync(0xffffffffu, v, o);
+                if (l + o < 32) v += u;
+            }
+            const float suf[2] = {v, v - dl[0]};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int u = 2 * l + h;
+                float db = 0.f, dlm = 0.f, cc = 0.f;
+                if (u < nr) {
+                    float de = deta[u];
+                    if (s.unc[u]) {
+                        const float da = -suf[h] / s.gam[u];
+                        de = fmaf(da, s.lam[u], de);
+                        dlm = da * s.eta[u];
+                    }
+                    if (s.live[u]) {
+                        db = de / s.den[u];
+                        const float dden = -de * s.eta[u] / s.den[u];
+                        dlm += dden;
+                        cc = 2.f * dden;
+                    }
+                    p.dbeta[bh * p.T + t0 + u] = db;
+                    p.dlam[bh * p.T + t0 + u] = dlm;
+                }
+                c2[u] = cc;
+            }
+        }
+        __syncthreads();
+        // dX row r = EA + EB + 2 dden x; row r is dk of token t0 + r - 1 (row 0 of the call: the tail key)
+        {
+            const int r = tid >> 1, c0 = 32 * (tid & 1);
+            if (r < nr) {
+                const long long t = t0 + r - 1;
+                float* dst = t >= 0 ? p.dk + (bh * p.T + t) * kD + c0 : (p.dtail ? p.dtail + bh * kD + c0 : nullptr);
+                if (dst) {
+                    const float cr = c2[r];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float x[8];
+                        row8<EX>(TP(L::X), xl, sw128(r, c0 + 8 * q), x);
+#pragma unroll
+                        for (int hq = 0; hq < 2; ++hq) {
+                            const int f4 = ((c0 >> 2) + 2 * q + hq) ^ (r & 15);
+                            float4 a = reinterpret_cast<const float4*>(EA + r * kD)[f4];
+                            if constexpr (!IP) {
+                                const float4 b = reinterpret_cast<const float4*>(EB + r * kD)[f4];
+                                a.x += b.x;
+                                a.y += b.y;
+                                a.z += b.z;
+                                a.w += b.w;
+                            }
+                            reinterpret_cast<float4*>(dst)[2 * q + hq] =
+                                make_float4(fmaf(cr, x[4 * hq], a.x), fmaf(cr, x[4 * hq + 1], a.y),
+                                            fmaf(cr, x[4 * hq + 2], a.z), fmaf(cr, x[4 * hq + 3], a.w));
+                        }
+                    }
+                }
+            }
+            if (t0 + nr == p.T && tid < kD / 4)  // the last key feeds only the next call's tail
+                reinterpret_cast<float4*>(p.dk + (bh * p.T + p.T - 1) * kD)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
-    unit_lower_inverse(Tm, A, B1);
-    // B1 = diag(w) T diag(e^Lx) X, B2 = diag(w) T Y, A <- P^T dO
-    zero(acc);
-    mm<false, false>(acc, Tm, DX);
-    zero(acc2);
-    mm<false, false, false, EX>(acc2, Tm, Y);
-    FOR_TILE(B1[i * kLd + j] = s.w[i] * acc[m][n]; B2[i * kLd + j] = s.w[i] * acc2[m][n];)
-    zero(acc);
-    mm<true, false, false, EX>(acc, P, dO);
-    FOR_TILE(A[i * kLd + j] = acc[m][n];)
-    __syncthreads();
-    // M = e^{L_C} I - X^T B1, U = X^T B2; P <- T^T (P^T dO); dO <- diag(e^L) dO
-    zero(acc);
-    mm<true, false, EX, false>(acc, X, B1);
-    zero(acc2);
-    mm<true, false, EX, false>(acc2, X, B2);
-    FOR_TILE(const float mij = (i == j ? s.eLC : 0.f) - acc[m][n];
-             ws[kWsM * kWsMat + i * kD + j] = mij;
-             ws[kWsMT * kWsMat + j * kD + i] = mij;
-             ws[kWsU * kWsMat + i * kD + j] = acc2[m][n];
-             ws[kWsT * kWsMat + i * kD + j] = Tm[i * kLd + j];)
-    zero(acc);
-    mm<true, false>(acc, Tm, A);
-    __syncthreads();  // every read of P and dO above is done
-    FOR_TILE(P[i * kLd + j] = acc[m][n]; dO[i * kLd + j] *= s.eL[i];)
-    __syncthreads();
-    // V = Q^T diag(e^L) dO - (diag(e^Lx) X)^T T^T P^T dO
-    zero(acc);
-    mm<true, false, EX, false>(acc, Q, dO);
-    zero(acc2);
-    mm<true, false>(acc2, DX, P);
-    FOR_TILE(ws[kWsV * kWsMat + i * kD + j] = acc[m][n] - acc2[m][n];)
+    cs.finish(tmem, 256);
 }
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
@@ -677,288 +1452,22 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// --------------------------------------------------------------------------------------------------
-// falcon_bwd_grad: one CTA per chunk.
-template <typename Tin, bool IP>
-__global__ void __launch_bounds__(kThreads, 1) falcon_bwd_grad(const BParams p) {
-    extern __shared__ __align__(16) float sm[];
-    float* X = sm;
-    float* Q = X + kMat;
-    float* Y = Q + kMat;   // Y; Falcon-1: Z, then P, then the dX accumulator
-    float* dO = Y + kMat;
-    float* S = dO + kMat;
-    float* dS = S + kMat;
-    float* Tm = dS + kMat;  // T (Falcon-1), then dP -> dSc
-    float* b0 = Tm + kMat;  // Falcon-1: R; Falcon-1A: P
-    float* b1 = b0 + kMat;  // X dS', then dR; Falcon-1: dA -> dG + dG^T
-    float* b2 = b1 + kMat;  // Sc
-    float* b3 = b2 + kMat;  // G (Falcon-1); Falcon-1A: the dX accumulator
-    float* b4 = IP ? b3 : b3 + kMat;  // dZ (Falcon-1)
-    Scal& s = *reinterpret_cast<Scal*>(b4 + kMat);
-    float* deta = reinterpret_cast<float*>(&s + 1);
-    float* dL = deta + kC;
-    float* dLx = dL + kC;
-    float* dw = dLx + kC;
-    float* c2 = dw + kC;
-    float* red = c2 + kC;  // [warps] block reduction
-
-    constexpr bool EX = sizeof(Tin) == 2;  // bf16 inputs are exact tf32 operands
-    float* R = IP ? Y : b0;
-    float* P = IP ? b0 : Y;
-    float* DXa = IP ? b3 : Y;
-
-    const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N;
-    const long long t0 = nck * kC;
-    const int nr = (int)min((long long)kC, p.T - t0);  // rows of this chunk
-    const float* ws = p.ws + cid * kWsChunk;
-    load_inputs<Tin>(X, Q, Y, dO, p, bh, t0, nr);
-    if (IP) {
-        float* const d2[2] = {S, dS};
-        const float* const s2[2] = {ws + kWsS * kWsMat, ws + kWsDS * kWsMat};
-        load_ws<2>(d2, s2);
-    } else {
-        float* const d3[3] = {S, dS, Tm};
-        const float* const s3[3] = {ws + kWsS * kWsMat, ws + kWsDS * kWsMat, ws + kWsT * kWsMat};
-        load_ws<3>(d3, s3);
-    }
-    if (threadIdx.x < kC) {
-        deta[threadIdx.x] = 0.f;
-        dL[threadIdx.x] = 0.f;
-        dLx[threadIdx.x] = 0.f;
-    }
-    if (threadIdx.x < kThreads / 32) red[threadIdx.x] = 0.f;
-    __syncthreads();
-    chunk_scalars(s, X, p, bh, t0, nr);
-    const int lane = threadIdx.x & 31;
-    float acc[2][4], acc2[2][4];
-
-    // <dS', S>
-    {
-        float a = 0.f;
-        for (int e = threadIdx.x; e < kD * kD; e += kThreads) {
-            const int rr = e >> 6, cc = e & 63;
-            a = fmaf(dS[rr * kLd + cc], S[rr * kLd + cc], a);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        if (lane == 0) red[threadIdx.x >> 5] = a;
-    }
-    // Z = Y - diag(e^Lx) X S (Falcon-1); X dS'
-    if (!IP) {
-        zero(acc);
-        mm<false, false, EX, false>(acc, X, S);
-        FOR_TILE(Y[i * kLd + j] -= s.eLx[i] * acc[m][n];)
-    }
-    zero(acc);
-    mm<false, false, EX, false>(acc, X, dS);
-    FOR_TILE(b1[i * kLd + j] = acc[m][n];)
-    __syncthreads();
-    // R = T Z (Falcon-1); Sc = Q X^T; G = X X^T (Falcon-1)
-    if (!IP) {
-        zero(acc);
-        mm<false, false>(acc, Tm, Y);
-        FOR_TILE(b0[i * kLd + j] = acc[m][n];)
-        zero(acc);
-        mm<false, true, EX, EX>(acc, X, X);
-        FOR_TILE(b3[i * kLd + j] = acc[m][n];)
-    }
-    zero(acc);
-    mm<false, true, EX, EX>(acc, Q, X);
-    FOR_TILE(b2[i * kLd + j] = acc[m][n];)
-    __syncthreads();
-    // dw_j = x_j^T dS' r_j; P
-    if (threadIdx.x < kC) {
-        const int j = threadIdx.x;
-        float a = 0.f;
-#pragma unroll 8
-        for (int cc = 0; cc < kD; ++cc) a = fmaf(b1[j * kLd + cc], R[j * kLd + cc], a);
-        dw[j] = a;
-    }
-    FOR_TILE(P[i * kLd + j] = j <= i ? s.eta[j] * expf(s.L[i] - s.L[j]) * b2[i * kLd + j] : 0.f;)
-    __syncthreads();
-    // dR = P^T dO + diag(w) X dS'  (Falcon-1A: dV = dR)
-    zero(acc);
-    mm<true, false, false, EX>(acc, P, dO);
-    FOR_TILE(b1[i * kLd + j] = acc[m][n] + s.w[i] * b1[i * kLd + j];)
-    __syncthreads();
-    float* dvo = p.dv + (bh * p.T + t0) * kD;
-    if (!IP) {  // dZ = T^T dR = dV
-        zero(acc);
-        mm<true, false>(acc, Tm, b1);
-        FOR_TILE(b4[i * kLd + j] = acc[m][n]; if (i < nr) dvo[i * kD + j] = acc[m][n];)
-    } else {
-        FOR_TILE(if (i < nr) dvo[i * kD + j] = b1[i * kLd + j];)
-    }
-    __syncthreads();
-    // dP = dO R^T (j <= i) -> d eta, dL; dSc = dP eta_j e^{L_i - L_j}, into Tm
-    zero(acc);
-    mm<false, true, EX, IP && EX>(acc, dO, R);
-    if (!IP) {
-        zero(acc2);
-        mm<false, true>(acc2, b4, R);  // dZ R^T = -dA
-    }
-    __syncthreads();  // Tm (T) and b1 (dR) are read no more
-    {
-        float rowL[2] = {0.f, 0.f}, colE[4] = {0.f, 0.f, 0.f, 0.f}, colL[4] = {0.f, 0.f, 0.f, 0.f};
-        FOR_TILE({
-            float v = 0.f;
-            if (j <= i) {
-                const float f = expf(s.L[i] - s.L[j]), d = acc[m][n];
-                const float pp = P[i * kLd + j];
-                colE[ci] = fmaf(d * f, b2[i * kLd + j], colE[ci]);
-                rowL[ri] = fmaf(d, pp, rowL[ri]);
-                colL[ci] = fmaf(d, pp, colL[ci]);
-                v = d * s.eta[j] * f;
-            }
-            Tm[i * kLd + j] = v;
-        })
-        row_add(dL, rowL);
-        col_add(deta, colE);
-        col_add(dL, colL, -1.f);
-    }
-    if (!IP) {  // dA = -dZ R^T (j < i) -> d eta, dLx, dL; dG = dA eta_j e^{Lx_i - L_j}, into b1
-        float rowX[2] = {0.f, 0.f}, colE[4] = {0.f, 0.f, 0.f, 0.f}, colL[4] = {0.f, 0.f, 0.f, 0.f};
-        FOR_TILE({
-            float v = 0.f;
-            if (j < i) {
-                const float f = expf(s.Lx[i] - s.L[j]), d = -acc2[m][n];
-                const float gv = b3[i * kLd + j];
-                const float aa = s.eta[j] * f * gv * d;
-                colE[ci] = fmaf(d * f, gv, colE[ci]);
-                rowX[ri] += aa;
-                colL[ci] += aa;
-                v = d * s.eta[j] * f;
-            }
-            b1[i * kLd + j] = v;
-        })
-        row_add(dLx, rowX);
-        col_add(deta, colE);
-        col_add(dL, colL, -1.f);
-    }
-    __syncthreads();
-    if (!IP) {  // dG + dG^T: mirror the strict lower triangle into the upper one
-        for (int e = threadIdx.x; e < kC * kC; e += kThreads) {
-            const int i = e >> 6, j = e & 63;
-            if (j > i) b1[i * kLd + j] = b1[j * kLd + i];
-        }
-    }
-    // dX accumulator: diag(w) R dS'^T  (for Falcon-1 it overwrites P, last read before the barrier above)
-    zero(acc);
-    mm<false, true, IP && EX, false>(acc, R, dS);
-    __syncthreads();
-    FOR_TILE(DXa[i * kLd + j] = s.w[i] * acc[m][n];)
-    __syncthreads();
-    // dX += dSc^T Q (+ (dG + dG^T) X - diag(e^Lx) dZ S^T, with dLx_i -= e^Lx_i x_i . (dZ S^T)_i)
-    zero(acc);
-    mm<true, false, false, EX>(acc, Tm, Q);
-    if (!IP) {
-        mm<false, false, false, EX>(acc, b1, X);
-        zero(acc2);
-        mm<false, true>(acc2, b4, S);
-        float rowX[2] = {0.f, 0.f};
-        FOR_TILE(DXa[i * kLd + j] += acc[m][n] - s.eLx[i] * acc2[m][n];
-                 rowX[ri] = fmaf(X[i * kLd + j], acc2[m][n], rowX[ri]);)
-        row_add(dLx, rowX, s.eLx, -1.f);
-    } else {
-        FOR_TILE(DXa[i * kLd + j] += acc[m][n];)
-    }
-    // dQ = diag(e^L) dO S^T + dSc X, with dL_i += e^L_i q_i . (dO S^T)_i
-    zero(acc);
-    mm<false, true, EX, false>(acc, dO, S);
-    zero(acc2);
-    mm<false, false, false, EX>(acc2, Tm, X);
-    {
-        float rowL[2] = {0.f, 0.f};
-        float* dqo = p.dq + (bh * p.T + t0) * kD;
-        FOR_TILE(rowL[ri] = fmaf(Q[i * kLd + j], acc[m][n], rowL[ri]);
-                 if (i < nr) dqo[i * kD + j] = s.eL[i] * acc[m][n] + acc2[m][n];)
-        row_add(dL, rowL, s.eL);
-    }
-    __syncthreads();
-    // scalars: d eta and dL from w and the chunk-end decay; d log gamma; the clamp; eta = beta / den
-    if (threadIdx.x < 32) {
-        const int l = threadIdx.x;
-        float dwsum = 0.f;
-        float dl[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int j = 2 * l + h;
-            const float ww = dw[j] * s.w[j];
-            dwsum += ww;
-            deta[j] = fmaf(dw[j], expf(s.L[kC - 1] - s.L[j]), deta[j]);
-            dl[h] = dL[j] - ww + (j + 1 < kC ? dLx[j + 1] : 0.f);
-        }
-        dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 16);
-        dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 8);
-        dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 4);
-        dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 2);
-        dwsum += __shfl_xor_sync(0xffffffffu, dwsum, 1);
-        float dss = 0.f;
-#pragma unroll
-        for (int u = 0; u < kThreads / 32; ++u) dss += red[u];
-        if (l == 31) dl[1] += dwsum + s.eLC * dss;
-        // suffix sums: d log gamma_u = sum_{i >= u} dL_i
-        float v = dl[0] + dl[1];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_down_sync(0xffffffffu, v, o);
-            if (l + o < 32) v += u;
-        }
-        const float suf[2] = {v, v - dl[0]};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int u = 2 * l + h;
-            float db = 0.f, dlm = 0.f, cc = 0.f;
-            if (u < nr) {
-                float de = deta[u];
-                if (s.unc[u]) {
-                    const float da = -suf[h] / s.gam[u];
-                    de = fmaf(da, s.lam[u], de);
-                    dlm = da * s.eta[u];
-                }
-                if (s.live[u]) {
-                    db = de / s.den[u];
-                    const float dden = -de * s.eta[u] / s.den[u];
-                    dlm += dden;
-                    cc = 2.f * dden;
-                }
-                p.dbeta[bh * p.T + t0 + u] = db;
-                p.dlam[bh * p.T + t0 + u] = dlm;
-            }
-            c2[u] = cc;
-        }
-    }
-    __syncthreads();
-    // dX = accumulator + 2 dden x; row i is dk of token t0 + i - 1 (row 0 of the call: the tail key)
-    for (int e = threadIdx.x; e < kC * kD; e += kThreads) {
-        const int i = e >> 6, j = e & 63;
-        if (i >= nr) continue;
-        const float g = fmaf(c2[i], X[i * kLd + j], DXa[i * kLd + j]);
-        const long long t = t0 + i - 1;
-        if (t >= 0) p.dk[(bh * p.T + t) * kD + j] = g;
-        else if (p.dtail) p.dtail[bh * kD + j] = g;
-    }
-    if (t0 + nr == p.T)  // the last key feeds only the next call's tail
-        for (int j = threadIdx.x; j < kD; j += kThreads) p.dk[(bh * p.T + p.T - 1) * kD + j] = 0.f;
-}
-
-constexpr size_t kScalBytes = sizeof(Scal);
-constexpr size_t kPrepSmem = 10 * kMat * sizeof(float) + kScalBytes;
-constexpr size_t gradSmem(bool ip) { return (ip ? 11 : 12) * kMat * sizeof(float) + kScalBytes + (5 * kC + kThreads / 32) * sizeof(float); }
 
 template <typename Tin, bool IP>
 int launch_typed(const BParams& p, cudaStream_t st) {
+    constexpr bool EX = sizeof(Tin) == 2;
     const unsigned chunks = (unsigned)(p.BH * p.N);
-    cudaFuncSetAttribute(falcon_bwd_prep<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
-    cudaFuncSetAttribute(falcon_bwd_grad<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gradSmem(IP));
-    falcon_bwd_prep<Tin, IP><<<chunks, kThreads, kPrepSmem, st>>>(p);
+    constexpr int prep_smem = PrepLay<EX, IP>::ALLOC, grad_smem = GradLay<EX, IP>::ALLOC;
+    cudaFuncSetAttribute(falcon_bwd_prep<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
+    cudaFuncSetAttribute(falcon_bwd_grad<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, grad_smem);
+    falcon_bwd_prep<Tin, IP><<<chunks, kCT, prep_smem, st>>>(p);
     ChainParams cp{};
     cp.p = p;
     const long long rows = p.BH * p.N * (kWsChunk / kD);  // the workspace as rows of 64 floats
     if (rows >= (1LL << 31) || !encode_rows_f32_sw128(&cp.tm_ws, p.ws, rows)) return 4;
     cudaFuncSetAttribute(falcon_bwd_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chl::ALLOC);
     falcon_bwd_chain<<<(unsigned)p.BH, kChainT, chl::ALLOC, st>>>(cp);
-    falcon_bwd_grad<Tin, IP><<<chunks, kThreads, gradSmem(IP), st>>>(p);
+    falcon_bwd_grad<Tin, IP><<<chunks, kCT, grad_smem, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
