@@ -27,7 +27,7 @@
 //                     per step): S_{n+1} = M_n S_n + U_n forward, then dS_n = M_n^T dS_{n+1} + V_n
 //                     backward, storing S_n and dS_{n+1};
 //   falcon_bwd_grad   every chunk at once: all input gradients from S_n and dS_{n+1}.
-// prep and grad run one 128-thread CTA per chunk, two per SM, every 64 x 64 x 64 product a tcgen05
+// prep and grad run one 256-thread CTA per chunk, two per SM, every 64 x 64 x 64 product a tcgen05
 // bf16 product with the fp32 operands split into bf16 hi and lo parts (hi*hi + hi*lo + lo*hi, fp32
 // sums in tensor memory); the scalars, the per-element factors and the triangular inverse run on the
 // CUDA cores in fp32.
@@ -50,7 +50,8 @@ using namespace ptx;
 constexpr int kD = 64;        // dk = dv
 constexpr int kC = 64;        // chunk length
 constexpr int kWsMat = kD * kD;             // floats per workspace matrix
-constexpr int kWsChunk = 7 * kWsMat;        // M, U, V, T, S_n, dS_{n+1}, M^T
+constexpr int kWsChunk = 7 * kWsMat;        // M, U, V, T, S_n, dS_{n+1}, M^T (T, S_n, dS_{n+1} as bf16
+                                            // hi and lo tiles, the others dense fp32)
 enum { kWsM = 0, kWsU = 1, kWsV = 2, kWsT = 3, kWsS = 4, kWsDS = 5, kWsMT = 6 };
 
 struct BParams {
@@ -84,17 +85,18 @@ struct Scal {
 
 
 // ================================================================================================
-// Chunk kernels on the tensor cores: one 128-thread CTA per chunk, thread t reading and writing TMEM
-// lane t (warp w: lanes 32 w .. 32 w + 31). Every operand is a 64 x 64 bf16 tile in shared memory
-// (128-byte rows, the 128-byte swizzle), usable K-major or MN-major, or a 128-row A operand in TMEM.
-// An fp32 operand x enters as two tiles, hi = bf16(x) and lo = bf16(x - hi), and a product as
-// hi*hi + hi*lo + lo*hi with fp32 sums in TMEM: every operand element keeps ~16 significant bits.
-// The inputs of a bf16 call are exact tiles without a lo part. Each product is tcgen05 kind::f16 with
-// M = 128 (two stacked 64-row operands, or one whose second half is read and its result rows unused),
-// N = 64 or 128 and K = 64, issued by one thread; the per-element work between products runs on the
-// row (or column) the thread's lane holds.
+// Chunk kernels on the tensor cores: one 256-thread CTA per chunk, two per SM. Thread t reads and
+// writes TMEM lane t % 128 (warp w: lanes 32 (w % 4) ..) and takes the columns 32 (t / 128) .. + 31 of
+// that lane's rows. Every operand is a 64 x 64 bf16 tile in shared memory (128-byte rows, the 128-byte
+// swizzle), usable K-major or MN-major, or a 128-row A operand in TMEM. An fp32 operand x enters as
+// two tiles, hi = bf16(x) and lo = bf16(x - hi), and a product as hi*hi + hi*lo + lo*hi with fp32
+// sums in TMEM: every operand element keeps ~16 significant bits. The inputs of a bf16 call are exact
+// tiles without a lo part. Each product is tcgen05 kind::f16 with M = 128 (two stacked 64-row
+// operands, or one whose second half is read and its result rows unused), N = 64 or 128 and K = 64,
+// issued by one thread; a tcgen05 instruction costs about the same for every N up to 256, so
+// products that share an operand are issued as one where the layout allows.
 
-constexpr int kCT = 128;                        // threads of a chunk CTA
+constexpr int kCT = 256;                        // threads of a chunk CTA
 constexpr int kTile = 8192;                     // one 64 x 64 bf16 tile
 constexpr int kAS = 68;                         // row stride (floats) of the matrix the inverse works on
 constexpr long long kCTimeout = 4000000000LL;   // ~2 s
@@ -121,31 +123,29 @@ __device__ __forceinline__ void mma64(uint32_t d, const Opd& a, const Opd& b, ui
     }
 }
 
-// 16 NQ consecutive TMEM columns of this thread's lane (one wait).
-template <int NQ>
-__device__ __forceinline__ void tld(uint32_t taddr, float* v) {
-    uint32_t r[NQ][16];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) tmem_ld16(taddr + 16 * q, r[q]);
+// 32 consecutive TMEM columns of this thread's lane (one wait).
+__device__ __forceinline__ void tld32(uint32_t taddr, float* v) {
+    uint32_t r[2][16];
+    tmem_ld16(taddr, r[0]);
+    tmem_ld16(taddr + 16, r[1]);
     tmem_wait_ld();
+    regs_ready(r[0]);
+    regs_ready(r[1]);
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        regs_ready(r[q]);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[16 * q + e] = __uint_as_float(r[q][e]);
+    for (int e = 0; e < 16; ++e) {
+        v[e] = __uint_as_float(r[0][e]);
+        v[16 + e] = __uint_as_float(r[1][e]);
     }
 }
-// v[0..63] as this lane's row of a bf16 A operand: hi pairs to columns hc .. hc + 31, lo pairs to
-// lc .. lc + 31 (element k in the low half of column k / 2 when k is even). No wait.
-__device__ __forceinline__ void tst_a(uint32_t hc, uint32_t lc, const float* v) {
+// v[0..31] (the K elements 32 h .. 32 h + 31 of this lane's row) into a bf16 A operand in TMEM whose
+// hi part starts at column hc and lo part at lc (element k in the low half of column k / 2 when k is
+// even). No wait.
+__device__ __forceinline__ void tst_a32(uint32_t hc, uint32_t lc, int h, const float* v) {
+    uint32_t hh[16], ll[16];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        uint32_t h[16], l[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) split2(v[32 * q + 2 * e], v[32 * q + 2 * e + 1], h[e], l[e]);
-        tmem_st16(hc + 16 * q, h);
-        tmem_st16(lc + 16 * q, l);
-    }
+    for (int e = 0; e < 16; ++e) split2(v[2 * e], v[2 * e + 1], hh[e], ll[e]);
+    tmem_st16(hc + 16 * h, hh);
+    tmem_st16(lc + 16 * h, ll);
 }
 
 // Eight elements of a row (from byte offset `off` of the tile, an sw128 offset) as fp32; for fp32
@@ -174,6 +174,10 @@ __device__ __forceinline__ void put4_hilo(uint8_t* hi, uint8_t* lo, uint32_t off
     *reinterpret_cast<uint2*>(hi + off) = make_uint2(h0, h1);
     *reinterpret_cast<uint2*>(lo + off) = make_uint2(l0, l1);
 }
+__device__ __forceinline__ void store32(float* dst, const float* v) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
 
 __device__ __forceinline__ void cp_async16z(uint32_t dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
@@ -181,8 +185,8 @@ __device__ __forceinline__ void cp_async16z(uint32_t dst, const void* src, uint3
 
 // Rows r < nr of q, k, v and dout for the chunk's tokens t0 + r (k shifted: token t0 + r - 1, the
 // tail key or zero before the first token) into tiles at byte offsets hi[a] (bf16: asynchronous
-// copies, committed as one group for the caller to wait on) or hi[a] and lo[a] (fp32: through
-// registers). An offset < 0 skips the tensor; rows past nr are zero.
+// copies, left for the caller to commit and wait on) or hi[a] and lo[a] (fp32: through registers).
+// An offset < 0 skips the tensor; rows past nr are zero.
 template <typename Tin>
 __device__ void load_chunk(const BParams& p, uint8_t* sm, uint32_t base, const int (&hi)[4], const int (&lo)[4],
                            long long bh, long long t0, int nr) {
@@ -201,19 +205,19 @@ __device__ void load_chunk(const BParams& p, uint8_t* sm, uint32_t base, const i
         for (int a = 0; a < 4; ++a) {
             if (hi[a] < 0) continue;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 512 / kCT; ++u) {
                 const int e = tid + kCT * u, r = e >> 3, q8 = e & 7;
                 const Tin* ptr = row(a, r);
                 cp_async16z(base + (uint32_t)hi[a] + sw128(r, 8 * q8), ptr ? ptr + 8 * q8 : src[a], ptr ? 16u : 0u);
             }
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
     } else {
-        float4 v[4][8];
+        constexpr int NU = 1024 / kCT;
+        float4 v[4][NU];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < NU; ++u) {
                 const int e = tid + kCT * u, r = e >> 4, c4 = e & 15;
                 const Tin* ptr = hi[a] >= 0 ? row(a, r) : nullptr;
                 v[a][u] = ptr ? *reinterpret_cast<const float4*>(ptr + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -222,43 +226,12 @@ __device__ void load_chunk(const BParams& p, uint8_t* sm, uint32_t base, const i
         for (int a = 0; a < 4; ++a) {
             if (hi[a] < 0) continue;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < NU; ++u) {
                 const int e = tid + kCT * u, r = e >> 4, c4 = e & 15;
                 put4_hilo(sm + hi[a], sm + lo[a], sw128(r, 4 * c4), v[a][u]);
             }
         }
     }
-}
-
-// A dense fp32 64 x 64 workspace matrix into hi and lo tiles.
-__device__ void ws_tiles(const float* src, uint8_t* hi, uint8_t* lo) {
-    float4 v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = reinterpret_cast<const float4*>(src)[threadIdx.x + kCT * u];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int e = threadIdx.x + kCT * u;
-        put4_hilo(hi, lo, sw128(e >> 4, 4 * (e & 15)), v[u]);
-    }
-}
-// Two of them, returning this thread's part of sum(a * b).
-__device__ float ws_tiles2(const float* a, const float* b, uint8_t* ah, uint8_t* al, uint8_t* bh, uint8_t* bl) {
-    float4 x[8], y[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        x[u] = reinterpret_cast<const float4*>(a)[threadIdx.x + kCT * u];
-        y[u] = reinterpret_cast<const float4*>(b)[threadIdx.x + kCT * u];
-    }
-    float dot = 0.f;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int e = threadIdx.x + kCT * u;
-        const uint32_t off = sw128(e >> 4, 4 * (e & 15));
-        put4_hilo(ah, al, off, x[u]);
-        put4_hilo(bh, bl, off, y[u]);
-        dot = fmaf(x[u].x, y[u].x, fmaf(x[u].y, y[u].y, fmaf(x[u].z, y[u].z, fmaf(x[u].w, y[u].w, dot))));
-    }
-    return dot;
 }
 
 // Per-token scalars of the chunk; thread i < 64 passes nx = ||x_i||^2 of its row. Then the
@@ -355,7 +328,45 @@ __device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
 // T = (I + A)^{-1} in place for the strictly lower 64 x 64 A in M (fp32, stride kAS; zero on and above
 // the diagonal on entry, T with its unit diagonal on exit): the four 16 x 16 diagonal blocks by
 // right-looking column substitution (one thread per column), then two levels of block merges,
-// T_ba = -T_bb (A_ba T_aa), through the scratch W (32 x 33 floats). All threads call it.
+// T_ba = -T_bb (A_ba T_aa) through the scratch W (32 x 33 floats), each of 128 threads a column of the
+// block over a quarter of its rows. The triangles' zeros stand in for the bounds of the sums, so every
+// loop has a fixed length. All threads call it.
+template <int H>
+__device__ __forceinline__ void merge_level(float* M, float* W) {
+    constexpr int RQ = H / 4;  // rows per thread
+    const int tid = threadIdx.x;
+    static_assert((64 / (2 * H)) * H * 4 == 128, "one thread per (block, column, row quarter)");
+    if (tid < 128) {
+        const int cc = tid % H, rq = (tid / H) % 4, blk = tid / (4 * H), r0 = 2 * H * blk;
+        float t[H];
+#pragma unroll
+        for (int k = 0; k < H; ++k) t[k] = M[(r0 + k) * kAS + r0 + cc];  // T_aa column cc
+#pragma unroll
+        for (int r = 0; r < RQ; ++r) {
+            const float* a = M + (r0 + H + RQ * rq + r) * kAS + r0;  // A_ba row
+            float x = 0.f;
+#pragma unroll
+            for (int k = 0; k < H; ++k) x = fmaf(a[k], t[k], x);
+            W[(H * blk + RQ * rq + r) * 33 + cc] = x;
+        }
+    }
+    __syncthreads();
+    if (tid < 128) {
+        const int cc = tid % H, rq = (tid / H) % 4, blk = tid / (4 * H), r0 = 2 * H * blk;
+        float w[H];
+#pragma unroll
+        for (int k = 0; k < H; ++k) w[k] = W[(H * blk + k) * 33 + cc];
+#pragma unroll
+        for (int r = 0; r < RQ; ++r) {
+            const float* t = M + (r0 + H + RQ * rq + r) * kAS + r0 + H;  // T_bb row
+            float x = 0.f;
+#pragma unroll
+            for (int k = 0; k < H; ++k) x = fmaf(t[k], w[k], x);
+            M[(r0 + H + RQ * rq + r) * kAS + r0 + cc] = -x;
+        }
+    }
+    __syncthreads();
+}
 __device__ void invert128(float* M, float* W) {
     const int tid = threadIdx.x;
     float x[16];
@@ -380,23 +391,8 @@ __device__ void invert128(float* M, float* W) {
         for (int r = 0; r < 16; ++r) M[(16 * b + r) * kAS + 16 * b + c] = x[r];
     }
     __syncthreads();
-    for (int h = 16; h < 64; h *= 2) {
-        const int nb = 64 / (2 * h);
-        for (int e = tid; e < nb * h * h; e += kCT) {  // W = A_ba T_aa (T_aa lower: k >= cc)
-            const int blk = e / (h * h), rr = (e / h) % h, cc = e % h, r0 = 2 * h * blk;
-            float a = 0.f;
-            for (int k = cc; k < h; ++k) a = fmaf(M[(r0 + h + rr) * kAS + r0 + k], M[(r0 + k) * kAS + r0 + cc], a);
-            W[(blk * h + rr) * 33 + cc] = a;
-        }
-        __syncthreads();
-        for (int e = tid; e < nb * h * h; e += kCT) {  // T_ba = -T_bb W (T_bb lower: k <= rr)
-            const int blk = e / (h * h), rr = (e / h) % h, cc = e % h, r0 = 2 * h * blk;
-            float a = 0.f;
-            for (int k = 0; k <= rr; ++k) a = fmaf(M[(r0 + h + rr) * kAS + r0 + h + k], W[(blk * h + k) * 33 + cc], a);
-            M[(r0 + h + rr) * kAS + r0 + cc] = -a;
-        }
-        __syncthreads();
-    }
+    merge_level<16>(M, W);
+    merge_level<32>(M, W);
 }
 
 // Waits of the chunk kernels: thread 0 waits for the next phase of the MMA barrier (bounded); every
@@ -473,9 +469,9 @@ template <bool EX, bool IP>
 struct GradLay {
     // Q X [QL XL] DO [DOL] | YZ ZL PRH SH PRL SL TH TL DSH DSL, then the scalars, the gradient
     // accumulators and the barriers. Roles of the shared slots over the kernel:
-    //   YZ, ZL   Y (Falcon-1; its lo part in ZL) -> Z -> dR; Falcon-1A: P; then dSc_hi, dGs_hi
+    //   YZ, ZL   Y (Falcon-1; its lo part in ZL) -> Z -> dR; Falcon-1A: P; then dSc_hi, dG_hi
     //   PRH, PRL P -> R (Falcon-1); Falcon-1A: Y
-    //   TH, TL   T (Falcon-1); then dSc_lo, dGs_lo
+    //   TH, TL   T (Falcon-1); then dSc_lo, dG_lo
     // Adjacent pairs serve as stacked K-major operands: [Q; X], [YZ; ZL], [PRH; SH], [PRL; SL], [TH; TL].
     enum : int {
         Q = 0,
@@ -496,8 +492,8 @@ struct GradLay {
         DSL = YZ + 9,
         NT = YZ + 10,
         SCAL = NT * kTile,
-        ACC = SCAL + (int)(sizeof(Scal) + 15) / 16 * 16,  // deta dL dLx dw c2 [64], red [4]
-        BAR = ACC + (5 * kC + 4) * 4,
+        ACC = SCAL + (int)(sizeof(Scal) + 15) / 16 * 16,  // deta dL dLx dw c2 [64], red [8]
+        BAR = ACC + (5 * kC + 8) * 4,
         BYTES = BAR + 64,
         ALLOC = BYTES + 1024
     };
@@ -509,6 +505,8 @@ struct GradLay {
 // Falcon-1, as products: [Sc; G] = [Q; X] X^T; P and A from them; T = (I + A)^{-1} on the CUDA cores;
 // E = [P; X^T diag(w)] T; E [diag(e^Lx) X | Y] = [P T diag(e^Lx) X, . ; K, U] with M = e^{L_C} I - K;
 // V = Ao^T dO. Falcon-1A (T = I, K = 0): [U, . ; ., V] = [(diag(w) X)^T ; Q^T] [Y | diag(e^L) dO].
+// T goes to the workspace as bf16 hi and lo tiles (the gradient kernel's operand), M, M^T, U and V as
+// dense fp32 matrices (the chain's).
 template <typename Tin, bool IP>
 __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep(const BParams p) {
     constexpr bool EX = sizeof(Tin) == 2;
@@ -518,7 +516,7 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
     uint8_t* sm = smem_raw + (base - raw);
     auto TP = [&](int slot) { return sm + slot * kTile; };
     auto TA = [&](int slot) { return base + (uint32_t)(slot * kTile); };
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, ln = tid & 127, hf = tid >> 7;  // TMEM lane, column half
     Scal& s = *reinterpret_cast<Scal*>(sm + L::SCAL);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BAR + 16);
     ChunkSync cs{base + L::BAR, 0u};
@@ -536,12 +534,14 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
         const int hi[4] = {L::Q * kTile, L::X * kTile, L::YH * kTile, L::DO * kTile};
         const int lo[4] = {L::QL * kTile, L::XL * kTile, L::YL * kTile, L::DOL * kTile};
         load_chunk<Tin>(p, sm, base, hi, lo, bh, t0, nr);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
     cs.publish();
     tc_fence_after();
-    const uint32_t tmem = *tslot, tq = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t tmem = *tslot, tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint8_t* xl = EX ? nullptr : TP(L::XL);
+    const int c0 = 32 * hf;  // this thread's columns
     bool ok = true;
 
     if constexpr (!IP) {
@@ -558,66 +558,54 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
         ok = cs.wait();
         float* AT = reinterpret_cast<float*>(sm + L::AT);
         if (ok) {
-            if (tid < 64) {  // P row i into the A operand (columns 64-127, rows 0-63); diag(e^Lx) X row i
-                const int i = tid;
+            float v[32];
+            tld32(tq + c0, v);
+            if (ln < 64) {  // P row i into the A operand (columns 64-127, rows 0-63); diag(e^Lx) X row i
+                const int i = ln;
                 const float li = s.L[i];
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    float v[32];
-                    tld<2>(tq + 32 * h, v);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int j = 32 * h + e;
-                        v[e] = j <= i ? s.eta[j] * expf(fminf(li - s.L[j], 0.f)) * v[e] : 0.f;
-                    }
-                    uint32_t hh[16], ll[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) split2(v[2 * e], v[2 * e + 1], hh[e], ll[e]);
-                    tmem_st16(tq + 64 + 16 * h, hh);
-                    tmem_st16(tq + 96 + 16 * h, ll);
+                for (int e = 0; e < 32; ++e) {
+                    const int j = c0 + e;
+                    v[e] = j <= i ? s.eta[j] * __expf(fminf(li - s.L[j], 0.f)) * v[e] : 0.f;
                 }
+                tst_a32(tq + 64, tq + 96, hf, v);
                 const float di = s.eLx[i];
 #pragma unroll
-                for (int q8 = 0; q8 < 8; ++q8) {
+                for (int q = 0; q < 4; ++q) {
                     float x[8];
-                    row8<EX>(TP(L::X), xl, sw128(i, 8 * q8), x);
+                    row8<EX>(TP(L::X), xl, sw128(i, c0 + 8 * q), x);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] *= di;
-                    st8_hilo(TP(L::DXH), TP(L::DXL), sw128(i, 8 * q8), x);
+                    st8_hilo(TP(L::DXH), TP(L::DXL), sw128(i, c0 + 8 * q), x);
                 }
             } else {  // A row f (fp32, for the inverse); X^T diag(w) row f into the A operand
-                const int f = tid - 64;
+                const int f = ln - 64;
                 const float lx = s.Lx[f];
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    float v[32];
-                    tld<2>(tq + 32 * h, v);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int j = 32 * h + e;
-                        v[e] = j < f ? s.eta[j] * expf(fminf(lx - s.L[j], 0.f)) * v[e] : 0.f;
-                    }
-                    float4* dst = reinterpret_cast<float4*>(AT + f * kAS + 32 * h);
-#pragma unroll
-                    for (int k4 = 0; k4 < 8; ++k4) dst[k4] = make_float4(v[4 * k4], v[4 * k4 + 1], v[4 * k4 + 2], v[4 * k4 + 3]);
+                for (int e = 0; e < 32; ++e) {
+                    const int j = c0 + e;
+                    v[e] = j < f ? s.eta[j] * __expf(fminf(lx - s.L[j], 0.f)) * v[e] : 0.f;
                 }
-                float v[64];
+                float4* dst = reinterpret_cast<float4*>(AT + f * kAS + c0);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) v[j] = elem<EX>(TP(L::X), xl, sw128(j, f)) * s.w[j];
-                tst_a(tq + 64, tq + 96, v);
+                for (int k4 = 0; k4 < 8; ++k4) dst[k4] = make_float4(v[4 * k4], v[4 * k4 + 1], v[4 * k4 + 2], v[4 * k4 + 3]);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = elem<EX>(TP(L::X), xl, sw128(c0 + e, f)) * s.w[c0 + e];
+                tst_a32(tq + 64, tq + 96, hf, v);
             }
             cs.publish();
             invert128(AT, reinterpret_cast<float*>(TP(L::TH)));
-            {  // T to its hi / lo tiles and to the workspace
-                const int r = tid >> 1, c0 = 32 * (tid & 1);
-                float v[32];
+            {  // T to its hi / lo tiles and to the workspace as the same tiles (hi, then lo)
+                const int r = tid >> 2, cq = 16 * (tid & 3);
+                uint8_t* tg = reinterpret_cast<uint8_t*>(ws + kWsT * kWsMat);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = AT[r * kAS + c0 + e];
+                for (int q = 0; q < 2; ++q) {
+                    float x[8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st8_hilo(TP(L::TH), TP(L::TL), sw128(r, c0 + 8 * q), v + 8 * q);
-                float4* dst = reinterpret_cast<float4*>(ws + kWsT * kWsMat + r * kD + c0);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    for (int e = 0; e < 8; ++e) x[e] = AT[r * kAS + cq + 8 * q + e];
+                    st8_hilo(TP(L::TH), TP(L::TL), sw128(r, cq + 8 * q), x);
+                    st8_hilo(tg, tg + kTile, sw128(r, cq + 8 * q), x);
+                }
             }
             cs.publish();
             if (tid == 0) {  // E = [P; X^T diag(w)] T into columns 128-191
@@ -631,9 +619,9 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
         }
         if (ok) {
             {  // E as the next A operand
-                float v[64];
-                tld<4>(tq + 128, v);
-                tst_a(tq + 64, tq + 96, v);
+                float v[32];
+                tld32(tq + 128 + c0, v);
+                tst_a32(tq + 64, tq + 96, hf, v);
             }
             cs.publish();
             if (tid == 0) {  // E [diag(e^Lx) X | Y] into columns 128-255
@@ -650,45 +638,35 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
             ok = cs.wait();
         }
         if (ok) {
-            if (tid < 64) {  // Ao row i = e^{L_i} q_i - (P T diag(e^Lx) X)_i as hi / lo tiles
-                const int i = tid;
+            if (ln < 64) {  // Ao row i = e^{L_i} q_i - (P T diag(e^Lx) X)_i as hi / lo tiles
+                const int i = ln;
                 const float ei = s.eL[i];
                 const uint8_t* ql = EX ? nullptr : TP(L::QL);
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    float v[32];
-                    tld<2>(tq + 128 + 32 * h, v);
+                float v[32];
+                tld32(tq + 128 + c0, v);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float x[8];
-                        row8<EX>(TP(L::Q), ql, sw128(i, 32 * h + 8 * q), x);
+                for (int q = 0; q < 4; ++q) {
+                    float x[8];
+                    row8<EX>(TP(L::Q), ql, sw128(i, c0 + 8 * q), x);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = fmaf(ei, x[e], -v[8 * q + e]);
-                        st8_hilo(TP(L::AOH), TP(L::AOL), sw128(i, 32 * h + 8 * q), x);
-                    }
+                    for (int e = 0; e < 8; ++e) x[e] = fmaf(ei, x[e], -v[8 * q + e]);
+                    st8_hilo(TP(L::AOH), TP(L::AOL), sw128(i, c0 + 8 * q), x);
                 }
             } else {  // M row f = e^{L_C} e_f - K_f (and M^T column f), U row f
-                const int f = tid - 64;
+                const int f = ln - 64;
                 const float gC = s.eLC;
-                float* Mr = ws + kWsM * kWsMat + f * kD;
+                float v[32];
+                tld32(tq + 128 + c0, v);
                 float* MT = ws + kWsMT * kWsMat + f;
-                float* Ur = ws + kWsU * kWsMat + f * kD;
-#pragma unroll 1
-                for (int h = 0; h < 4; ++h) {
-                    float v[32];
-                    tld<2>(tq + 128 + 32 * h, v);
-                    if (h < 2) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int c = 32 * h + e;
-                            v[e] = (c == f ? gC : 0.f) - v[e];
-                            MT[c * kD] = v[e];
-                        }
-                    }
-                    float4* dst = reinterpret_cast<float4*>((h < 2 ? Mr : Ur) + 32 * (h & 1));
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                for (int e = 0; e < 32; ++e) {
+                    const int c = c0 + e;
+                    v[e] = (c == f ? gC : 0.f) - v[e];
+                    MT[c * kD] = v[e];
                 }
+                store32(ws + kWsM * kWsMat + f * kD + c0, v);
+                tld32(tq + 192 + c0, v);
+                store32(ws + kWsU * kWsMat + f * kD + c0, v);
             }
             cs.publish();
             if (tid == 0) {  // V = Ao^T dO into columns 0-63
@@ -700,22 +678,20 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
             }
             ok = cs.wait();
         }
-        if (ok && tid < 64) {
-            float v[64];
-            tld<4>(tq, v);
-            float4* dst = reinterpret_cast<float4*>(ws + kWsV * kWsMat + tid * kD);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        if (ok && ln < 64) {
+            float v[32];
+            tld32(tq + c0, v);
+            store32(ws + kWsV * kWsMat + ln * kD + c0, v);
         }
     } else {
         chunk_scalars(s, tid < kC ? row_norm<EX>(TP(L::X), xl, tid) : 0.f, p, bh, t0, nr);
-        if (tid < 64) {  // diag(w) X and diag(e^L) dO, row j, as hi / lo tiles
-            const int j = tid;
+        if (ln < 64) {  // diag(w) X and diag(e^L) dO, row j, as hi / lo tiles
+            const int j = ln;
             const float wj = s.w[j], ej = s.eL[j];
             const uint8_t* dl = EX ? nullptr : TP(L::DOL);
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) {
-                const uint32_t off = sw128(j, 8 * q8);
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t off = sw128(j, c0 + 8 * q);
                 float x[8], d[8];
                 row8<EX>(TP(L::X), xl, off, x);
                 row8<EX>(TP(L::DO), dl, off, d);
@@ -745,20 +721,19 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
         }
         ok = cs.wait();
         if (ok) {
-            const int f = tid & 63;
-            float v[64];
-            tld<4>(tq + (tid < 64 ? 0 : 64), v);
-            float4* dst = reinterpret_cast<float4*>(ws + (tid < 64 ? kWsU : kWsV) * kWsMat + f * kD);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            if (tid < 64) {  // M = M^T = e^{L_C} I
-                float4* m = reinterpret_cast<float4*>(ws + kWsM * kWsMat + f * kD);
-                float4* mt = reinterpret_cast<float4*>(ws + kWsMT * kWsMat + f * kD);
+            const int f = ln & 63;
+            float v[32];
+            tld32(tq + (ln < 64 ? 0 : 64) + c0, v);
+            store32(ws + (ln < 64 ? kWsU : kWsV) * kWsMat + f * kD + c0, v);
+            if (ln < 64) {  // M = M^T = e^{L_C} I
                 const float g = s.eLC;
+                float4* m = reinterpret_cast<float4*>(ws + kWsM * kWsMat + f * kD + c0);
+                float4* mt = reinterpret_cast<float4*>(ws + kWsMT * kWsMat + f * kD + c0);
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float4 z = make_float4(4 * q == f ? g : 0.f, 4 * q + 1 == f ? g : 0.f, 4 * q + 2 == f ? g : 0.f,
-                                                 4 * q + 3 == f ? g : 0.f);
+                for (int q = 0; q < 8; ++q) {
+                    const int c = c0 + 4 * q;
+                    const float4 z = make_float4(c == f ? g : 0.f, c + 1 == f ? g : 0.f, c + 2 == f ? g : 0.f,
+                                                 c + 3 == f ? g : 0.f);
                     m[q] = z;
                     mt[q] = z;
                 }
@@ -772,13 +747,14 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
 // falcon_bwd_grad: every input gradient of one chunk from S_n, dS_{n+1} and T. Falcon-1, as products:
 //   [X S | X dS'] and [Sc; G] = [Q; X] X^T; Z = Y - diag(e^Lx) X S and P from them;
 //   R = T Z and P^T dO, so dR = P^T dO + diag(w) X dS'; dZ = T^T dR (= dV);
-//   [dO; dZ] [R^T | S^T] = [dP, dO S^T ; -dA, dZ S^T]; dSc and dG (then dG + dG^T) from dP and dA;
-//   [dSc; dG + dG^T] X, dSc^T Q and R dS'^T; then
+//   [dO; dZ] [R^T | S^T] = [dP, dO S^T ; -dA, dZ S^T]; dSc and dG from dP and dA;
+//   [dSc; dG] X, dSc^T Q + dG^T X and R dS'^T; then
 //   dQ = diag(e^L) dO S^T + dSc X,
 //   dX = dSc^T Q + (dG + dG^T) X - diag(e^Lx) dZ S^T + diag(w) R dS'^T + 2 dden x
 // and the scalar gradients (eta, the log prefixes, the clamp, beta, lambda). Falcon-1A: R = Y, no
 // T, Z, dZ, dA. TMEM columns: [0, 128) X S | X dS' -> R -> dZ -> [dP | dO S^T ; -dA | dZ S^T] ->
-// R dS'^T; [128, 192) [Sc; G] -> dSc^T Q; [192, 256) P^T dO -> the [dO; dZ] operand -> [dSc; dGs] X.
+// R dS'^T; [128, 192) [Sc; G] -> dSc^T Q + dG^T X; [192, 256) P^T dO -> the [dO; dZ] operand ->
+// [dSc; dG] X. S_n, dS_{n+1} and T arrive as bf16 hi / lo tiles from the workspace.
 template <typename Tin, bool IP>
 __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad(const BParams p) {
     constexpr bool EX = sizeof(Tin) == 2;
@@ -788,7 +764,8 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
     uint8_t* sm = smem_raw + (base - raw);
     auto TP = [&](int slot) { return sm + slot * kTile; };
     auto TA = [&](int slot) { return base + (uint32_t)(slot * kTile); };
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, ln = tid & 127, hf = tid >> 7;
+    const int c0 = 32 * hf;  // this thread's columns of its lane's row
     Scal& s = *reinterpret_cast<Scal*>(sm + L::SCAL);
     float* deta = reinterpret_cast<float*>(sm + L::ACC);
     float* dL = deta + kC;
@@ -800,7 +777,7 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
     ChunkSync cs{base + L::BAR, 0u};
     const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N, t0 = nck * kC;
     const int nr = (int)min((long long)kC, p.T - t0);
-    const float* ws = p.ws + cid * kWsChunk;
+    const uint8_t* wsb = reinterpret_cast<const uint8_t*>(p.ws + cid * kWsChunk);
     const uint8_t* xl = EX ? nullptr : TP(L::XL);
     const uint8_t* ql = EX ? nullptr : TP(L::QL);
 
@@ -815,23 +792,31 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
         const int hi[4] = {L::Q * kTile, L::X * kTile, yh * kTile, L::DO * kTile};
         const int lo[4] = {L::QL * kTile, L::XL * kTile, yl * kTile, L::DOL * kTile};
         load_chunk<Tin>(p, sm, base, hi, lo, bh, t0, nr);
-    }
-    {
-        float dot = ws_tiles2(ws + kWsS * kWsMat, ws + kWsDS * kWsMat, TP(L::SH), TP(L::SL), TP(L::DSH), TP(L::DSL));
-        if (!IP) ws_tiles(ws + kWsT * kWsMat, TP(L::TH), TP(L::TL));
+        // S_n, dS_{n+1} (and T): their hi and lo tiles as stored, byte for byte
+        constexpr int NM = IP ? 2 : 3;
+        const int src[3] = {kWsS, kWsDS, kWsT};
+        const int dst[3][2] = {{L::SH, L::SL}, {L::DSH, L::DSL}, {L::TH, L::TL}};
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (lane == 0) red[warp] = dot;  // <dS_{n+1}, S_n>, per warp
+        for (int m = 0; m < NM; ++m)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int u = 0; u < 512 / kCT; ++u) {
+                    const int e = tid + kCT * u;
+                    cp_async16z(TA(dst[m][h]) + 16 * e, wsb + (size_t)src[m] * kWsMat * 4 + h * kTile + 16 * e, 16u);
+                }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
     if (tid < kC) {
         deta[tid] = 0.f;
         dL[tid] = 0.f;
         dLx[tid] = 0.f;
+        dw[tid] = 0.f;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     cs.publish();
     tc_fence_after();
-    const uint32_t tmem = *tslot, tq = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t tmem = *tslot, tq = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     bool ok = true;
 
     if (tid == 0) {
@@ -853,44 +838,52 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
         }
         mma_commit(cs.bar);
     }
+    {  // <dS_{n+1}, S_n> per warp, from the tiles, while the products run
+        const int r = tid >> 2, cq = 16 * (tid & 3);
+        float dot = 0.f;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float a[8], b[8];
+            row8<false>(TP(L::SH), TP(L::SL), sw128(r, cq + 8 * q), a);
+            row8<false>(TP(L::DSH), TP(L::DSL), sw128(r, cq + 8 * q), b);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dot = fmaf(a[e], b[e], dot);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (lane == 0) red[warp] = dot;
+    }
     chunk_scalars(s, tid < kC ? row_norm<EX>(TP(L::X), xl, tid) : 0.f, p, bh, t0, nr);
     ok = cs.wait();
 
-    // ---- Z (Falcon-1) and P, row i
+    // ---- Z (Falcon-1) and P: row i = ln < 64, columns c0 ..
     if (ok) {
-        if (tid < 64) {
-            const int i = tid;
+        if (ln < 64) {
+            const int i = ln;
+            float v[32];
             if constexpr (!IP) {
                 const float di = s.eLx[i];
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-                    float xs[32];
-                    tld<2>(tq + 32 * h, xs);
+                tld32(tq + c0, v);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t off = sw128(i, 32 * h + 8 * q);
-                        float y[8];
-                        row8<EX>(TP(L::YZ), TP(L::ZL), off, y);
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t off = sw128(i, c0 + 8 * q);
+                    float y[8];
+                    row8<EX>(TP(L::YZ), TP(L::ZL), off, y);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) y[e] = fmaf(-di, xs[8 * q + e], y[e]);
-                        st8_hilo(TP(L::YZ), TP(L::ZL), off, y);
-                    }
+                    for (int e = 0; e < 8; ++e) y[e] = fmaf(-di, v[8 * q + e], y[e]);
+                    st8_hilo(TP(L::YZ), TP(L::ZL), off, y);
                 }
             }
             const int ph = IP ? L::YZ : L::PRH, pl = IP ? L::ZL : L::PRL;
             const float li = s.L[i];
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float v[32];
-                tld<2>(tq + 128 + 32 * h, v);
+            tld32(tq + 128 + c0, v);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = 32 * h + e;
-                    v[e] = j <= i ? s.eta[j] * expf(fminf(li - s.L[j], 0.f)) * v[e] : 0.f;
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) st8_hilo(TP(ph), TP(pl), sw128(i, 32 * h + 8 * q), v + 8 * q);
+            for (int e = 0; e < 32; ++e) {
+                const int j = c0 + e;
+                v[e] = j <= i ? s.eta[j] * __expf(fminf(li - s.L[j], 0.f)) * v[e] : 0.f;
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st8_hilo(TP(ph), TP(pl), sw128(i, c0 + 8 * q), v + 8 * q);
         }
         cs.publish();
         if (tid == 0) {
@@ -911,39 +904,34 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
 
     // ---- R (Falcon-1) to tiles; dR = P^T dO + diag(w) X dS' (Falcon-1: tiles; 1A: dV); dw
     if (ok) {
-        if (tid < 64) {
-            const int i = tid;
+        if (ln < 64) {
+            const int i = ln;
             const float wi = s.w[i];
-            float dwa = 0.f;
-            const uint8_t* yl = EX ? nullptr : TP(L::PRL);
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float xd[32], r[32], d[32];
-                tld<2>(tq + 64 + 32 * h, xd);
-                tld<2>(tq + 192 + 32 * h, d);
-                if constexpr (!IP) {
-                    tld<2>(tq + 32 * h, r);
+            float xd[32], r[32], d[32];
+            tld32(tq + 64 + c0, xd);
+            tld32(tq + 192 + c0, d);
+            if constexpr (!IP) {
+                tld32(tq + c0, r);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) st8_hilo(TP(L::PRH), TP(L::PRL), sw128(i, 32 * h + 8 * q), r + 8 * q);
-                } else {
+                for (int q = 0; q < 4; ++q) st8_hilo(TP(L::PRH), TP(L::PRL), sw128(i, c0 + 8 * q), r + 8 * q);
+            } else {
+                const uint8_t* yl = EX ? nullptr : TP(L::PRL);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) row8<EX>(TP(L::PRH), yl, sw128(i, 32 * h + 8 * q), r + 8 * q);
-                }
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    dwa = fmaf(xd[e], r[e], dwa);
-                    d[e] = fmaf(wi, xd[e], d[e]);
-                }
-                if constexpr (!IP) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) st8_hilo(TP(L::YZ), TP(L::ZL), sw128(i, 32 * h + 8 * q), d + 8 * q);
-                } else if (i < nr) {
-                    float4* dst = reinterpret_cast<float4*>(p.dv + (bh * p.T + t0 + i) * kD + 32 * h);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) dst[q] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
-                }
+                for (int q = 0; q < 4; ++q) row8<EX>(TP(L::PRH), yl, sw128(i, c0 + 8 * q), r + 8 * q);
             }
-            dw[i] = dwa;
+            float dwa = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                dwa = fmaf(xd[e], r[e], dwa);
+                d[e] = fmaf(wi, xd[e], d[e]);
+            }
+            atomicAdd(&dw[i], dwa);
+            if constexpr (!IP) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st8_hilo(TP(L::YZ), TP(L::ZL), sw128(i, c0 + 8 * q), d + 8 * q);
+            } else if (i < nr) {
+                store32(p.dv + (bh * p.T + t0 + i) * kD + c0, d);
+            }
         }
         if constexpr (!IP) {
             cs.publish();
@@ -962,21 +950,17 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
 
     // ---- the A operand [dO; dZ] (columns 192-255: hi, lo); dV = dZ
     if (ok) {
-        float v[64];
-        if (tid < 64) {
+        float v[32];
+        if (ln < 64) {
             const uint8_t* dl = EX ? nullptr : TP(L::DOL);
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) row8<EX>(TP(L::DO), dl, sw128(tid, 8 * q8), v + 8 * q8);
-            tst_a(tq + 192, tq + 224, v);
+            for (int q = 0; q < 4; ++q) row8<EX>(TP(L::DO), dl, sw128(ln, c0 + 8 * q), v + 8 * q);
+            tst_a32(tq + 192, tq + 224, hf, v);
         } else if (!IP) {
-            const int i = tid - 64;
-            tld<4>(tq, v);
-            if (i < nr) {
-                float4* dst = reinterpret_cast<float4*>(p.dv + (bh * p.T + t0 + i) * kD);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
-            tst_a(tq + 192, tq + 224, v);
+            const int i = ln - 64;
+            tld32(tq + c0, v);
+            if (i < nr) store32(p.dv + (bh * p.T + t0 + i) * kD + c0, v);
+            tst_a32(tq + 192, tq + 224, hf, v);
         }
         cs.publish();
         if (tid == 0) {  // [dO; dZ] [R^T | S^T] into columns 0-127 (B: [R; S] K-major, N = 128)
@@ -996,81 +980,68 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
 
     // ---- dP (rows 0-63) and dA (rows 64-127): the score and Gram adjoints, the scalar terms
     if (ok) {
-        if (tid < 64) {
-            const int i = tid;
+        float d[32], g[32], cE[32], cL[32];
+        tld32(tq + c0, d);
+        tld32(tq + 128 + c0, g);
+        if (ln < 64) {
+            const int i = ln;
             const float li = s.L[i];
             float rowL = 0.f;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float d[32], sc[32], cE[32], cL[32];
-                tld<2>(tq + 32 * h, d);
-                tld<2>(tq + 128 + 32 * h, sc);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = 32 * h + e;
-                    const bool on = j <= i;
-                    const float f = expf(fminf(li - s.L[j], 0.f)), g = d[e];
-                    const float pp = s.eta[j] * f * sc[e];
-                    cE[e] = on ? g * f * sc[e] : 0.f;
-                    cL[e] = on ? g * pp : 0.f;
-                    rowL += cL[e];
-                    d[e] = on ? g * s.eta[j] * f : 0.f;  // dSc
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) st8_hilo(TP(L::YZ), TP(L::TH), sw128(i, 32 * h + 8 * q), d + 8 * q);
-                const float ce = warp_colsum32(cE);
-                const float cl = warp_colsum32(cL);
-                atomicAdd(&deta[32 * h + lane], ce);
-                atomicAdd(&dL[32 * h + lane], -cl);
+            for (int e = 0; e < 32; ++e) {
+                const int j = c0 + e;
+                const bool on = j <= i;
+                const float f = __expf(fminf(li - s.L[j], 0.f)), dp = d[e];
+                const float pp = s.eta[j] * f * g[e];
+                cE[e] = on ? dp * f * g[e] : 0.f;
+                cL[e] = on ? dp * pp : 0.f;
+                rowL += cL[e];
+                d[e] = on ? dp * s.eta[j] * f : 0.f;  // dSc
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st8_hilo(TP(L::YZ), TP(L::TH), sw128(i, c0 + 8 * q), d + 8 * q);
             atomicAdd(&dL[i], rowL);
-        } else if constexpr (!IP) {
-            const int i = tid - 64;
+        } else if (!IP) {
+            const int i = ln - 64;
             const float lx = s.Lx[i];
             float rowX = 0.f;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float d[32], g[32], cE[32], cL[32];
-                tld<2>(tq + 32 * h, d);
-                tld<2>(tq + 128 + 32 * h, g);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = 32 * h + e;
-                    const bool on = j < i;
-                    const float f = expf(fminf(lx - s.L[j], 0.f)), da = -d[e];
-                    const float aa = s.eta[j] * f * g[e] * da;
-                    cE[e] = on ? da * f * g[e] : 0.f;
-                    cL[e] = on ? aa : 0.f;
-                    rowX += cL[e];
-                    d[e] = on ? da * s.eta[j] * f : 0.f;  // dG
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) st8_hilo(TP(L::ZL), TP(L::TL), sw128(i, 32 * h + 8 * q), d + 8 * q);
-                const float ce = warp_colsum32(cE);
-                const float cl = warp_colsum32(cL);
-                atomicAdd(&deta[32 * h + lane], ce);
-                atomicAdd(&dL[32 * h + lane], -cl);
+            for (int e = 0; e < 32; ++e) {
+                const int j = c0 + e;
+                const bool on = j < i;
+                const float f = __expf(fminf(lx - s.L[j], 0.f)), da = -d[e];
+                const float aa = s.eta[j] * f * g[e] * da;
+                cE[e] = on ? da * f * g[e] : 0.f;
+                cL[e] = on ? aa : 0.f;
+                rowX += cL[e];
+                d[e] = on ? da * s.eta[j] * f : 0.f;  // dG
             }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st8_hilo(TP(L::ZL), TP(L::TL), sw128(i, c0 + 8 * q), d + 8 * q);
             atomicAdd(&dLx[i], rowX);
-            named_bar(2, 64);  // every row of the strictly lower dG is in place
-            // dG + dG^T: the upper triangle (i, j > i) takes the stored (j, i); only lower entries are read
-            for (int j = i + 1; j < kC; ++j) {
-                const uint32_t src = sw128(j, i), dst = sw128(i, j);
-                *reinterpret_cast<uint16_t*>(TP(L::ZL) + dst) = *reinterpret_cast<const uint16_t*>(TP(L::ZL) + src);
-                *reinterpret_cast<uint16_t*>(TP(L::TL) + dst) = *reinterpret_cast<const uint16_t*>(TP(L::TL) + src);
-            }
+        }
+        if (ln < 64 || !IP) {
+            const float ce = warp_colsum32(cE);
+            const float cl = warp_colsum32(cL);
+            atomicAdd(&deta[c0 + lane], ce);
+            atomicAdd(&dL[c0 + lane], -cl);
         }
         cs.publish();
         if (tid == 0) {
             tc_fence_after();
-            // [dSc; dG + dG^T] X into columns 192-255
+            // [dSc; dG] X into columns 192-255
             mma64(tmem + 192, kmaj(TA(L::YZ)), mnmaj(TA(L::X)), 64, false);
             mma64(tmem + 192, kmaj(TA(L::TH)), mnmaj(TA(L::X)), 64, true);
             if constexpr (!EX) mma64(tmem + 192, kmaj(TA(L::YZ)), mnmaj(TA(L::XL)), 64, true);
-            // dSc^T Q into columns 128-191
+            // dSc^T Q (+ dG^T X) into columns 128-191, rows 0-63
             mma64(tmem + 128, mnmaj(TA(L::YZ)), mnmaj(TA(L::Q)), 64, false);
             mma64(tmem + 128, mnmaj(TA(L::TH)), mnmaj(TA(L::Q)), 64, true);
             if constexpr (!EX) mma64(tmem + 128, mnmaj(TA(L::YZ)), mnmaj(TA(L::QL)), 64, true);
+            if constexpr (!IP) {
+                mma64(tmem + 128, mnmaj(TA(L::ZL)), mnmaj(TA(L::X)), 64, true);
+                mma64(tmem + 128, mnmaj(TA(L::TL)), mnmaj(TA(L::X)), 64, true);
+                if constexpr (!EX) mma64(tmem + 128, mnmaj(TA(L::ZL)), mnmaj(TA(L::XL)), 64, true);
+            }
             // R dS'^T into columns 0-63
             mma64(tmem, kmaj(TA(L::PRH)), kmaj(TA(L::DSH)), 64, false);
             mma64(tmem, kmaj(TA(L::PRH)), kmaj(TA(L::DSL)), 64, true);
@@ -1082,60 +1053,49 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
 
     // ---- dQ; the two halves of dX to shared memory; the scalar gradients; dK
     if (ok) {
-        float* EA = reinterpret_cast<float*>(TP(L::DSH));  // rows 0-63: dSc^T Q + diag(w) R dS'^T
-        float* EB = reinterpret_cast<float*>(TP(L::YZ));   // rows 64-127: dGs X - diag(e^Lx) dZ S^T
-        if (tid < 64) {
-            const int i = tid;
+        float* EA = reinterpret_cast<float*>(TP(L::DSH));  // rows 0-63: dSc^T Q + dG^T X + diag(w) R dS'^T
+        float* EB = reinterpret_cast<float*>(TP(L::YZ));   // rows 64-127: dG X - diag(e^Lx) dZ S^T
+        if (ln < 64) {
+            const int i = ln;
             const float ei = s.eL[i], wi = s.w[i];
+            float a[32], b[32], qv[32];
+            tld32(tq + 64 + c0, a);   // dO S^T
+            tld32(tq + 192 + c0, b);  // dSc X
+#pragma unroll
+            for (int q = 0; q < 4; ++q) row8<EX>(TP(L::Q), ql, sw128(i, c0 + 8 * q), qv + 8 * q);
             float rowL = 0.f;
-            float* dqo = p.dq + (bh * p.T + t0 + i) * kD;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float a[32], b[32], qv[32];
-                tld<2>(tq + 64 + 32 * h, a);   // dO S^T
-                tld<2>(tq + 192 + 32 * h, b);  // dSc X
 #pragma unroll
-                for (int q = 0; q < 4; ++q) row8<EX>(TP(L::Q), ql, sw128(i, 32 * h + 8 * q), qv + 8 * q);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    rowL = fmaf(qv[e], a[e], rowL);
-                    a[e] = fmaf(ei, a[e], b[e]);
-                }
-                if (i < nr) {
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        reinterpret_cast<float4*>(dqo + 32 * h)[q] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
-                }
-                tld<2>(tq + 128 + 32 * h, a);  // dSc^T Q
-                tld<2>(tq + 32 * h, b);        // R dS'^T
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    reinterpret_cast<float4*>(EA + i * kD)[(8 * h + q) ^ (i & 15)] =
-                        make_float4(fmaf(wi, b[4 * q], a[4 * q]), fmaf(wi, b[4 * q + 1], a[4 * q + 1]),
-                                    fmaf(wi, b[4 * q + 2], a[4 * q + 2]), fmaf(wi, b[4 * q + 3], a[4 * q + 3]));
+            for (int e = 0; e < 32; ++e) {
+                rowL = fmaf(qv[e], a[e], rowL);
+                a[e] = fmaf(ei, a[e], b[e]);
             }
+            if (i < nr) store32(p.dq + (bh * p.T + t0 + i) * kD + c0, a);
             atomicAdd(&dL[i], ei * rowL);
-        } else if constexpr (!IP) {
-            const int i = tid - 64;
+            tld32(tq + 128 + c0, a);  // dSc^T Q + dG^T X
+            tld32(tq + c0, b);        // R dS'^T
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(EA + i * kD)[(8 * hf + q) ^ (i & 15)] =
+                    make_float4(fmaf(wi, b[4 * q], a[4 * q]), fmaf(wi, b[4 * q + 1], a[4 * q + 1]),
+                                fmaf(wi, b[4 * q + 2], a[4 * q + 2]), fmaf(wi, b[4 * q + 3], a[4 * q + 3]));
+        } else if (!IP) {
+            const int i = ln - 64;
             const float di = s.eLx[i];
+            float a[32], b[32], xv[32];
+            tld32(tq + 64 + c0, a);   // dZ S^T
+            tld32(tq + 192 + c0, b);  // dG X
+#pragma unroll
+            for (int q = 0; q < 4; ++q) row8<EX>(TP(L::X), xl, sw128(i, c0 + 8 * q), xv + 8 * q);
             float rowX = 0.f;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float a[32], b[32], xv[32];
-                tld<2>(tq + 64 + 32 * h, a);   // dZ S^T
-                tld<2>(tq + 192 + 32 * h, b);  // (dG + dG^T) X
 #pragma unroll
-                for (int q = 0; q < 4; ++q) row8<EX>(TP(L::X), xl, sw128(i, 32 * h + 8 * q), xv + 8 * q);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    rowX = fmaf(xv[e], a[e], rowX);
-                    b[e] = fmaf(-di, a[e], b[e]);
-                }
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    reinterpret_cast<float4*>(EB + i * kD)[(8 * h + q) ^ (i & 15)] =
-                        make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+            for (int e = 0; e < 32; ++e) {
+                rowX = fmaf(xv[e], a[e], rowX);
+                b[e] = fmaf(-di, a[e], b[e]);
             }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(EB + i * kD)[(8 * hf + q) ^ (i & 15)] =
+                    make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
             atomicAdd(&dLx[i], -di * rowX);
         }
         __syncthreads();
@@ -1190,21 +1150,22 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
             }
         }
         __syncthreads();
-        // dX row r = EA + EB + 2 dden x; row r is dk of token t0 + r - 1 (row 0 of the call: the tail key)
+        // dX row r = EA + EB + 2 dden x, 16 columns per thread; row r is dk of token t0 + r - 1 (row 0 of
+        // the call: the tail key)
         {
-            const int r = tid >> 1, c0 = 32 * (tid & 1);
+            const int r = tid >> 2, cq = 16 * (tid & 3);
             if (r < nr) {
                 const long long t = t0 + r - 1;
-                float* dst = t >= 0 ? p.dk + (bh * p.T + t) * kD + c0 : (p.dtail ? p.dtail + bh * kD + c0 : nullptr);
+                float* dst = t >= 0 ? p.dk + (bh * p.T + t) * kD + cq : (p.dtail ? p.dtail + bh * kD + cq : nullptr);
                 if (dst) {
                     const float cr = c2[r];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 2; ++q) {
                         float x[8];
-                        row8<EX>(TP(L::X), xl, sw128(r, c0 + 8 * q), x);
+                        row8<EX>(TP(L::X), xl, sw128(r, cq + 8 * q), x);
 #pragma unroll
                         for (int hq = 0; hq < 2; ++hq) {
-                            const int f4 = ((c0 >> 2) + 2 * q + hq) ^ (r & 15);
+                            const int f4 = ((cq >> 2) + 2 * q + hq) ^ (r & 15);
                             float4 a = reinterpret_cast<const float4*>(EA + r * kD)[f4];
                             if constexpr (!IP) {
                                 const float4 b = reinterpret_cast<const float4*>(EB + r * kD)[f4];
@@ -1373,10 +1334,16 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
             break;
         }
         pending = -1;
-        if (live) {  // S_n (forward) / dS_{n+1} (backward) for the gradient kernel, this thread's column
-            float* dst = wsq + n * kWsChunk + (fwd ? kWsS : kWsDS) * kWsMat + c;
+        if (live) {  // S_n (forward) / dS_{n+1} (backward) for the gradient kernel: this thread's column of
+            // the bf16 hi and lo tiles the gradient kernel copies in as they are
+            uint8_t* dst = reinterpret_cast<uint8_t*>(wsq + n * kWsChunk + (fwd ? kWsS : kWsDS) * kWsMat);
 #pragma unroll
-            for (int r = 0; r < kD; ++r) dst[r * kD] = s[r];
+            for (int r = 0; r < kD; ++r) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(s[r]);
+                const uint32_t off = sw128(r, c);
+                *reinterpret_cast<__nv_bfloat16*>(dst + off) = h;
+                *reinterpret_cast<__nv_bfloat16*>(dst + kTile + off) = __float2bfloat16_rn(s[r] - __bfloat162float(h));
+            }
         }
         {  // B: hi (low 13 bits cleared) in place, lo = the rest
             float4* bh4 = reinterpret_cast<float4*>(sm + chl::BHI);
