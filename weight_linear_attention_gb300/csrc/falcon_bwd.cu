@@ -1195,22 +1195,25 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
-// falcon_bwd_chain: one CTA of 128 threads per sequence, the two state scans on the tensor cores.
-// The carried matrix (S forward, dS backward) is kept transposed in tensor memory, lane c = column c
-// (lanes 64-127 zero), as the A operand of one product per step: D = X^T B^T with B = M_n (forward:
-// D = (M_n S)^T) or B = M_n^T (backward: D = (M_n^T dS)^T), both K-major as the prep kernel stores them,
-// loaded by TMA with the 128-byte swizzle. Each operand x is split into hi = x with its low 13 bits
-// cleared (exact in tf32) and lo = x - hi, and D = A_hi B_hi + A_hi B_lo + A_lo B_hi (fp32-accurate).
-// U_n / V_n arrive by 16-byte asynchronous copies one step ahead and are added in registers, where
-// each thread also stores its column of S_n / dS_{n+1} for the gradient kernel. Every wait is bounded:
-// on timeout the CTA raises the device flag, drains what it issued and frees its tensor memory.
+// falcon_bwd_chain: two CTAs of 128 threads per sequence, one per state scan, on the tensor cores:
+// the forward scan S_{n+1} = M_n S_n + U_n and the reverse scan dS_n = M_n^T dS_{n+1} + V_n need
+// nothing from each other. The carried matrix (S forward, dS backward) is kept transposed in tensor
+// memory, lane c = column c (lanes 64-127 zero), as the A operand of one product per step: D = X^T B^T
+// with B = M_n (forward: D = (M_n S)^T) or B = M_n^T (backward: D = (M_n^T dS)^T), both K-major as the
+// prep kernel stores them, loaded by TMA with the 128-byte swizzle two steps ahead into one of two
+// raw buffers. Each operand x is split into hi = x with its low 13 bits cleared (exact in tf32) and
+// lo = x - hi, and D = A_hi B_hi + A_hi B_lo + A_lo B_hi (fp32-accurate). U_n / V_n arrive by 16-byte
+// asynchronous copies one step ahead and are added in registers, where each thread also stores its
+// column of S_n / dS_{n+1} for the gradient kernel. Every wait is bounded: on timeout the CTA raises
+// the device flag, drains what it issued and frees its tensor memory.
 constexpr int kChainT = 128;
 constexpr uint32_t kCAH = 0, kCAL = 64, kCD = 128;  // TMEM columns: carried hi, lo, product
 constexpr long long kTcTimeout = 4000000000LL;     // ~2 s
 namespace chl {
 constexpr int BHI = 0, BLO = 16384;  // B = M_n or M_n^T: two K halves of 64 rows x 128 bytes each
 constexpr int OFS = 32768;           // two offset buffers (U_n or V_n), [64][64] fp32
-constexpr int BAR = OFS + 32768;
+constexpr int RAW = OFS + 32768;     // two raw B buffers (TMA destinations), the layout of BHI
+constexpr int BAR = RAW + 32768;
 constexpr int BYTES = BAR + 64;
 constexpr int ALLOC = BYTES + 1024;
 }  // namespace chl
@@ -1259,11 +1262,14 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
     const uint32_t raw = smem_u32(smem_raw), base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const uint32_t bar_full = base + chl::BAR, bar_mma = bar_full + 8, bar_drain = bar_full + 16;
+    const uint32_t bar_full0 = base + chl::BAR, bar_mma = bar_full0 + 16, bar_drain = bar_full0 + 24;  // full: two
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chl::BAR + 32);
-    const long long bh = blockIdx.x, N = p.N;
+    const long long bh = blockIdx.x >> 1, N = p.N;
+    const bool bwd = (blockIdx.x & 1) != 0;  // this CTA's scan
+    const long long k0 = bwd ? N : 0, k1 = k0 + N;  // its steps of the 2 N
     if (tid == 0) {
-        mbar_init(bar_full, 1);
+        mbar_init(bar_full0, 1);
+        mbar_init(bar_full0 + 8, 1);
         mbar_init(bar_mma, 1);
         mbar_init(bar_drain, 1);
         mbar_init_fence();
@@ -1277,21 +1283,22 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
     const bool live = c < kD;     // lanes 64-127 hold zeros
     float* const wsq = p.ws + bh * N * kWsChunk;
 
-    // step k of the 2 N: chunk n, matrix and offset of the pass
+    // step k: chunk n, matrix and offset of the pass
     auto chunk_of = [&](long long k) { return k < N ? k : 2 * N - 1 - k; };
-    auto issue_b = [&](long long k) {  // thread 0: B of step k by TMA
+    auto issue_b = [&](long long k) {  // thread 0: B of step k by TMA into raw buffer (k - k0) & 1
         const long long n = chunk_of(k);
         const int r = (int)((bh * N + n) * (kWsChunk / kD) + (k < N ? kWsM : kWsMT) * kD);
-        mbar_expect_tx(bar_full, 16384u);
+        const uint32_t bar = bar_full0 + 8 * (uint32_t)((k - k0) & 1);
+        mbar_expect_tx(bar, 16384u);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const uint32_t d = base + chl::BHI + h * 8192;
-            tma_load_2d(d, &P.tm_ws, 32 * h, r, bar_full);
-            tma_load_2d(d + 4096, &P.tm_ws, 32 * h, r + 32, bar_full);
+            const uint32_t d = base + chl::RAW + (uint32_t)((k - k0) & 1) * 16384 + h * 8192;
+            tma_load_2d(d, &P.tm_ws, 32 * h, r, bar);
+            tma_load_2d(d + 4096, &P.tm_ws, 32 * h, r + 32, bar);
         }
     };
     auto issue_ofs = [&](long long k) {  // every thread: U_n (forward) or V_n (backward) into buffer k & 1
-        if (k < 2 * N) {
+        if (k < k1) {
             const float* src = wsq + chunk_of(k) * kWsChunk + (k < N ? kWsU : kWsV) * kWsMat;
             float* d = reinterpret_cast<float*>(sm + chl::OFS) + (int)(k & 1) * kWsMat;
 #pragma unroll
@@ -1304,39 +1311,38 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
     };
 
     float s[kD];
-    auto load_start = [&](const float* src) {
+    {
+        const float* src = bwd ? p.dS_final : p.S0;
 #pragma unroll
         for (int r = 0; r < kD; ++r) s[r] = (live && src) ? src[(bh * kD + r) * kD + c] : 0.f;
         chain_put(tq, s);
         tmem_wait_st();
-    };
-    load_start(p.S0);
-    long long pending = 0;  // the step whose B is in flight (-1: none)
-    if (tid == 0) issue_b(0);
-    issue_ofs(0);
+    }
+    long long issued = k0;  // steps whose B has been requested: [k0, issued)
+    if (tid == 0) {
+        for (long long k = k0; k < k1 && k < k0 + 2; ++k) issue_b(k);
+    }
+    issued = k1 < k0 + 2 ? k1 : k0 + 2;
+    issue_ofs(k0);
     tc_fence_before();
     __syncthreads();
     bool ok = true;
+    long long waited = k0;  // steps whose B has landed: [k0, waited)
     constexpr uint32_t id = idesc_tf32(128, kD);
-    for (long long k = 0; k < 2 * N; ++k) {
-        const long long n = chunk_of(k);
-        const bool fwd = k < N;
-        if (k == N) {  // the backward scan starts from dS_final
-            load_start(p.dS_final);
-            tc_fence_before();
-            __syncthreads();
-        }
+    for (long long k = k0; k < k1; ++k) {
+        const long long n = chunk_of(k), i = k - k0;
         bool bad = false;
-        if (tid == 0) bad = !chain_wait(bar_full, (uint32_t)(k & 1));
+        if (tid == 0) bad = !chain_wait(bar_full0 + 8 * (uint32_t)(i & 1), (uint32_t)((i >> 1) & 1));
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         if (named_bar_or(1, kChainT, bad)) {
             ok = false;
             break;
         }
-        pending = -1;
+        waited = k + 1;
+        issue_ofs(k + 1);  // its buffer was last read by the previous step's epilogue
         if (live) {  // S_n (forward) / dS_{n+1} (backward) for the gradient kernel: this thread's column of
             // the bf16 hi and lo tiles the gradient kernel copies in as they are
-            uint8_t* dst = reinterpret_cast<uint8_t*>(wsq + n * kWsChunk + (fwd ? kWsS : kWsDS) * kWsMat);
+            uint8_t* dst = reinterpret_cast<uint8_t*>(wsq + n * kWsChunk + (bwd ? kWsDS : kWsS) * kWsMat);
 #pragma unroll
             for (int r = 0; r < kD; ++r) {
                 const __nv_bfloat16 h = __float2bfloat16_rn(s[r]);
@@ -1345,12 +1351,13 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
                 *reinterpret_cast<__nv_bfloat16*>(dst + kTile + off) = __float2bfloat16_rn(s[r] - __bfloat162float(h));
             }
         }
-        {  // B: hi (low 13 bits cleared) in place, lo = the rest
+        {  // B from its raw buffer: hi (low 13 bits cleared) and lo = the rest
+            const float4* rw = reinterpret_cast<const float4*>(sm + chl::RAW + (int)(i & 1) * 16384);
             float4* bh4 = reinterpret_cast<float4*>(sm + chl::BHI);
             float4* bl4 = reinterpret_cast<float4*>(sm + chl::BLO);
 #pragma unroll 4
             for (int e = tid; e < 16384 / 16; e += kChainT) {
-                const float4 v = bh4[e];
+                const float4 v = rw[e];
                 const float4 h = make_float4(hi19(v.x), hi19(v.y), hi19(v.z), hi19(v.w));
                 bh4[e] = h;
                 bl4[e] = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
@@ -1361,6 +1368,7 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
+            if (k + 2 < k1) issue_b(k + 2);  // the raw buffer has been read
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t off = (uint32_t)((ks >> 2) * 8192 + 32 * (ks & 3));
@@ -1370,15 +1378,13 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
                 mma_tf32_ta(tmem + kCD, tmem + kCAL + 8 * ks, dh, id, 1);
             }
             mma_commit(bar_mma);
-            bad = !chain_wait(bar_mma, (uint32_t)(k & 1));
-            if (!bad && k + 1 < 2 * N) issue_b(k + 1);  // B is free again
+            bad = !chain_wait(bar_mma, (uint32_t)(i & 1));
         }
+        if (k + 2 < k1) issued = k + 3;
         if (named_bar_or(1, kChainT, bad)) {
             ok = false;
             break;
         }
-        if (k + 1 < 2 * N) pending = k + 1;
-        issue_ofs(k + 1);
         tc_fence_after();
         {
             const float* of = reinterpret_cast<const float*>(sm + chl::OFS) + (int)(k & 1) * kWsMat;
@@ -1396,17 +1402,22 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
                 }
             }
         }
-        if (k + 1 < 2 * N && k + 1 != N) chain_put(tq, s);
+        if (k + 1 < k1) chain_put(tq, s);
         tmem_wait_st();
         tc_fence_before();
         __syncthreads();
     }
-    if (ok && p.dS0 && live) {
+    if (ok && bwd && p.dS0 && live) {
 #pragma unroll
         for (int r = 0; r < kD; ++r) p.dS0[(bh * kD + r) * kD + c] = s[r];
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    if (tid == 0 && pending >= 0) mbar_wait_bounded(bar_full, (uint32_t)(pending & 1), kTcTimeout);
+    if (tid == 0) {  // loads still in flight after an early exit
+        for (long long k = waited; k < issued; ++k) {
+            const long long i = k - k0;
+            mbar_wait_bounded(bar_full0 + 8 * (uint32_t)(i & 1), (uint32_t)((i >> 1) & 1), kTcTimeout);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
@@ -1418,7 +1429,6 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
-
 
 template <typename Tin, bool IP>
 int launch_typed(const BParams& p, cudaStream_t st) {
@@ -1433,7 +1443,7 @@ int launch_typed(const BParams& p, cudaStream_t st) {
     const long long rows = p.BH * p.N * (kWsChunk / kD);  // the workspace as rows of 64 floats
     if (rows >= (1LL << 31) || !encode_rows_f32_sw128(&cp.tm_ws, p.ws, rows)) return 4;
     cudaFuncSetAttribute(falcon_bwd_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chl::ALLOC);
-    falcon_bwd_chain<<<(unsigned)p.BH, kChainT, chl::ALLOC, st>>>(cp);
+    falcon_bwd_chain<<<(unsigned)(2 * p.BH), kChainT, chl::ALLOC, st>>>(cp);
     falcon_bwd_grad<Tin, IP><<<chunks, kCT, grad_smem, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
