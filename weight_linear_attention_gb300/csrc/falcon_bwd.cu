@@ -50,9 +50,9 @@ using namespace ptx;
 constexpr int kD = 64;        // dk = dv
 constexpr int kC = 64;        // chunk length
 constexpr int kWsMat = kD * kD;             // floats per workspace matrix
-constexpr int kWsChunk = 7 * kWsMat;        // M, U, V, T, S_n, dS_{n+1}, M^T (T, S_n, dS_{n+1} as bf16
-                                            // hi and lo tiles, the others dense fp32)
-enum { kWsM = 0, kWsU = 1, kWsV = 2, kWsT = 3, kWsS = 4, kWsDS = 5, kWsMT = 6 };
+constexpr int kWsChunk = 6 * kWsMat;        // M, U, V, T, S_n, dS_{n+1}: U and V dense fp32; M, T, S_n and
+                                            // dS_{n+1} as bf16 hi and lo tiles (8 KB each, hi first)
+enum { kWsM = 0, kWsU = 1, kWsV = 2, kWsT = 3, kWsS = 4, kWsDS = 5 };
 
 struct BParams {
     const void* q;
@@ -505,8 +505,8 @@ struct GradLay {
 // Falcon-1, as products: [Sc; G] = [Q; X] X^T; P and A from them; T = (I + A)^{-1} on the CUDA cores;
 // E = [P; X^T diag(w)] T; E [diag(e^Lx) X | Y] = [P T diag(e^Lx) X, . ; K, U] with M = e^{L_C} I - K;
 // V = Ao^T dO. Falcon-1A (T = I, K = 0): [U, . ; ., V] = [(diag(w) X)^T ; Q^T] [Y | diag(e^L) dO].
-// T goes to the workspace as bf16 hi and lo tiles (the gradient kernel's operand), M, M^T, U and V as
-// dense fp32 matrices (the chain's).
+// M and T go to the workspace as bf16 hi and lo tiles (the chain's and the gradient kernel's
+// operands), U and V as dense fp32 matrices.
 template <typename Tin, bool IP>
 __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep(const BParams p) {
     constexpr bool EX = sizeof(Tin) == 2;
@@ -657,14 +657,11 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
                 const float gC = s.eLC;
                 float v[32];
                 tld32(tq + 128 + c0, v);
-                float* MT = ws + kWsMT * kWsMat + f;
+                uint8_t* mg = reinterpret_cast<uint8_t*>(ws + kWsM * kWsMat);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int c = c0 + e;
-                    v[e] = (c == f ? gC : 0.f) - v[e];
-                    MT[c * kD] = v[e];
-                }
-                store32(ws + kWsM * kWsMat + f * kD + c0, v);
+                for (int e = 0; e < 32; ++e) v[e] = (c0 + e == f ? gC : 0.f) - v[e];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st8_hilo(mg, mg + kTile, sw128(f, c0 + 8 * q), v + 8 * q);
                 tld32(tq + 192 + c0, v);
                 store32(ws + kWsU * kWsMat + f * kD + c0, v);
             }
@@ -725,18 +722,13 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
             float v[32];
             tld32(tq + (ln < 64 ? 0 : 64) + c0, v);
             store32(ws + (ln < 64 ? kWsU : kWsV) * kWsMat + f * kD + c0, v);
-            if (ln < 64) {  // M = M^T = e^{L_C} I
-                const float g = s.eLC;
-                float4* m = reinterpret_cast<float4*>(ws + kWsM * kWsMat + f * kD + c0);
-                float4* mt = reinterpret_cast<float4*>(ws + kWsMT * kWsMat + f * kD + c0);
+            if (ln < 64) {  // M = e^{L_C} I
+                uint8_t* mg = reinterpret_cast<uint8_t*>(ws + kWsM * kWsMat);
+                float m[32];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int c = c0 + 4 * q;
-                    const float4 z = make_float4(c == f ? g : 0.f, c + 1 == f ? g : 0.f, c + 2 == f ? g : 0.f,
-                                                 c + 3 == f ? g : 0.f);
-                    m[q] = z;
-                    mt[q] = z;
-                }
+                for (int e = 0; e < 32; ++e) m[e] = c0 + e == f ? s.eLC : 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st8_hilo(mg, mg + kTile, sw128(f, c0 + 8 * q), m + 8 * q);
             }
         }
     }
@@ -1198,38 +1190,31 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 // falcon_bwd_chain: two CTAs of 128 threads per sequence, one per state scan, on the tensor cores:
 // the forward scan S_{n+1} = M_n S_n + U_n and the reverse scan dS_n = M_n^T dS_{n+1} + V_n need
 // nothing from each other. The carried matrix (S forward, dS backward) is kept transposed in tensor
-// memory, lane c = column c (lanes 64-127 zero), as the A operand of one product per step: D = X^T B^T
-// with B = M_n (forward: D = (M_n S)^T) or B = M_n^T (backward: D = (M_n^T dS)^T), both K-major as the
-// prep kernel stores them, loaded by TMA with the 128-byte swizzle two steps ahead into one of two
-// raw buffers. Each operand x is split into hi = x with its low 13 bits cleared (exact in tf32) and
-// lo = x - hi, and D = A_hi B_hi + A_hi B_lo + A_lo B_hi (fp32-accurate). U_n / V_n arrive by 16-byte
-// asynchronous copies one step ahead and are added in registers, where each thread also stores its
-// column of S_n / dS_{n+1} for the gradient kernel. Every wait is bounded: on timeout the CTA raises
+// memory, lane c = column c (lanes 64-127 zero), as the bf16 A operand of one product per step,
+// D = X^T B with B = M_n^T (forward: D = (M_n S)^T; M_n's tile read K-major) or B = M_n (backward:
+// D = (M_n^T dS)^T; the same tile read MN-major). Both operands are split into bf16 hi and lo parts and
+// D = A_hi B_hi + A_hi B_lo + A_lo B_hi (fp32 sums). M_n's hi and lo tiles, as the prep kernel stores
+// them, arrive by one bulk copy two steps ahead into one of two buffers, U_n / V_n by 16-byte
+// asynchronous copies two steps ahead, added in registers; while the product runs each thread stores
+// its column of S_n / dS_{n+1} for the gradient kernel. Every wait is bounded: on timeout the CTA raises
 // the device flag, drains what it issued and frees its tensor memory.
 constexpr int kChainT = 128;
-constexpr uint32_t kCAH = 0, kCAL = 64, kCD = 128;  // TMEM columns: carried hi, lo, product
+constexpr uint32_t kCAH = 0, kCAL = 32, kCD = 64;  // TMEM columns: carried hi, lo (bf16 pairs), product
 constexpr long long kTcTimeout = 4000000000LL;     // ~2 s
 namespace chl {
-constexpr int BHI = 0, BLO = 16384;  // B = M_n or M_n^T: two K halves of 64 rows x 128 bytes each
-constexpr int OFS = 32768;           // two offset buffers (U_n or V_n), [64][64] fp32
-constexpr int RAW = OFS + 32768;     // two raw B buffers (TMA destinations), the layout of BHI
-constexpr int BAR = RAW + 32768;
+constexpr int B = 0;                 // two buffers for M_n: hi tile, lo tile
+constexpr int BSZ = 2 * kTile;
+constexpr int OFS = B + 2 * BSZ;     // two offset buffers (U_n or V_n), [64][64] fp32
+constexpr int BAR = OFS + 32768;
 constexpr int BYTES = BAR + 64;
 constexpr int ALLOC = BYTES + 1024;
 }  // namespace chl
 
-struct ChainParams {
-    CUtensorMap tm_ws;  // the workspace as [rows][64] fp32, 32 x 32 boxes, 128-byte swizzle
-    BParams p;
-};
-
-__device__ __forceinline__ float hi19(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
-
 __device__ bool chain_wait(uint32_t bar, uint32_t parity) {
-    if (ptx::mbar_try(bar, parity)) return true;
+    if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     int spins = 0;
-    while (!ptx::mbar_try(bar, parity)) {
+    while (!mbar_try(bar, parity)) {
         if (++spins > 64) __nanosleep(32);
         if (clock64() - t0 > kTcTimeout) {
             atomicExch(&g_bwd_timeout_flag, 1);
@@ -1242,22 +1227,16 @@ __device__ bool chain_wait(uint32_t bar, uint32_t parity) {
 // this thread's carried column into the A operand's hi and lo columns of its lane (no wait)
 __device__ __forceinline__ void chain_put(uint32_t tq, const float (&x)[kD]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 2; ++q) {
         uint32_t h[16], l[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const float v = x[16 * q + e], vh = hi19(v);
-            h[e] = __float_as_uint(vh);
-            l[e] = __float_as_uint(v - vh);
-        }
-        ptx::tmem_st16(tq + kCAH + 16 * q, h);
-        ptx::tmem_st16(tq + kCAL + 16 * q, l);
+        for (int e = 0; e < 16; ++e) split2(x[32 * q + 2 * e], x[32 * q + 2 * e + 1], h[e], l[e]);
+        tmem_st16(tq + kCAH + 16 * q, h);
+        tmem_st16(tq + kCAL + 16 * q, l);
     }
 }
 
-__global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_constant__ ChainParams P) {
-    using namespace ptx;
-    const BParams& p = P.p;
+__global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const BParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw), base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
@@ -1274,7 +1253,7 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
         mbar_init(bar_drain, 1);
         mbar_init_fence();
     }
-    if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
+    if (warp == 0) tmem_alloc(smem_u32(tslot), 128);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1285,17 +1264,11 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
 
     // step k: chunk n, matrix and offset of the pass
     auto chunk_of = [&](long long k) { return k < N ? k : 2 * N - 1 - k; };
-    auto issue_b = [&](long long k) {  // thread 0: B of step k by TMA into raw buffer (k - k0) & 1
-        const long long n = chunk_of(k);
-        const int r = (int)((bh * N + n) * (kWsChunk / kD) + (k < N ? kWsM : kWsMT) * kD);
+    auto issue_b = [&](long long k) {  // thread 0: M_n's tiles of step k into buffer (k - k0) & 1
         const uint32_t bar = bar_full0 + 8 * (uint32_t)((k - k0) & 1);
-        mbar_expect_tx(bar, 16384u);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t d = base + chl::RAW + (uint32_t)((k - k0) & 1) * 16384 + h * 8192;
-            tma_load_2d(d, &P.tm_ws, 32 * h, r, bar);
-            tma_load_2d(d + 4096, &P.tm_ws, 32 * h, r + 32, bar);
-        }
+        mbar_expect_tx(bar, (uint32_t)chl::BSZ);
+        bulk_load(base + chl::B + (uint32_t)((k - k0) & 1) * chl::BSZ, wsq + chunk_of(k) * kWsChunk + kWsM * kWsMat,
+                  (uint32_t)chl::BSZ, bar);
     };
     auto issue_ofs = [&](long long k) {  // every thread: U_n (forward) or V_n (backward) into buffer k & 1
         if (k < k1) {
@@ -1318,30 +1291,38 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
         chain_put(tq, s);
         tmem_wait_st();
     }
-    long long issued = k0;  // steps whose B has been requested: [k0, issued)
     if (tid == 0) {
         for (long long k = k0; k < k1 && k < k0 + 2; ++k) issue_b(k);
     }
-    issued = k1 < k0 + 2 ? k1 : k0 + 2;
+    long long issued = k1 < k0 + 2 ? k1 : k0 + 2;  // steps whose M has been requested: [k0, issued)
     issue_ofs(k0);
+    issue_ofs(k0 + 1);
     tc_fence_before();
     __syncthreads();
     bool ok = true;
-    long long waited = k0;  // steps whose B has landed: [k0, waited)
-    constexpr uint32_t id = idesc_tf32(128, kD);
+    long long waited = k0;  // steps whose M has landed: [k0, waited)
+    const uint32_t id = idesc_bf16(128, kD, false, bwd);
     for (long long k = k0; k < k1; ++k) {
         const long long n = chunk_of(k), i = k - k0;
+        const uint32_t bb = base + chl::B + (uint32_t)(i & 1) * chl::BSZ;
         bool bad = false;
-        if (tid == 0) bad = !chain_wait(bar_full0 + 8 * (uint32_t)(i & 1), (uint32_t)((i >> 1) & 1));
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        if (named_bar_or(1, kChainT, bad)) {
-            ok = false;
-            break;
+        if (tid == 0) {
+            bad = !chain_wait(bar_full0 + 8 * (uint32_t)(i & 1), (uint32_t)((i >> 1) & 1));
+            if (!bad) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t dh = bwd ? desc_mn(bb + 2048 * ks, kTile) : desc_k(bb + 32 * ks);
+                    const uint64_t dl = bwd ? desc_mn(bb + kTile + 2048 * ks, kTile) : desc_k(bb + kTile + 32 * ks);
+                    mma_bf16_ta(tmem + kCD, tmem + kCAH + 8 * ks, dh, id, ks > 0);
+                    mma_bf16_ta(tmem + kCD, tmem + kCAH + 8 * ks, dl, id, 1);
+                    mma_bf16_ta(tmem + kCD, tmem + kCAL + 8 * ks, dh, id, 1);
+                }
+                mma_commit(bar_mma);
+            }
         }
-        waited = k + 1;
-        issue_ofs(k + 1);  // its buffer was last read by the previous step's epilogue
-        if (live) {  // S_n (forward) / dS_{n+1} (backward) for the gradient kernel: this thread's column of
-            // the bf16 hi and lo tiles the gradient kernel copies in as they are
+        if (live) {  // while the product runs: S_n (forward) / dS_{n+1} (backward) for the gradient kernel,
+            // this thread's column of the bf16 hi and lo tiles the gradient kernel copies in as they are
             uint8_t* dst = reinterpret_cast<uint8_t*>(wsq + n * kWsChunk + (bwd ? kWsDS : kWsS) * kWsMat);
 #pragma unroll
             for (int r = 0; r < kD; ++r) {
@@ -1351,40 +1332,17 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
                 *reinterpret_cast<__nv_bfloat16*>(dst + kTile + off) = __float2bfloat16_rn(s[r] - __bfloat162float(h));
             }
         }
-        {  // B from its raw buffer: hi (low 13 bits cleared) and lo = the rest
-            const float4* rw = reinterpret_cast<const float4*>(sm + chl::RAW + (int)(i & 1) * 16384);
-            float4* bh4 = reinterpret_cast<float4*>(sm + chl::BHI);
-            float4* bl4 = reinterpret_cast<float4*>(sm + chl::BLO);
-#pragma unroll 4
-            for (int e = tid; e < 16384 / 16; e += kChainT) {
-                const float4 v = rw[e];
-                const float4 h = make_float4(hi19(v.x), hi19(v.y), hi19(v.z), hi19(v.w));
-                bh4[e] = h;
-                bl4[e] = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            if (k + 2 < k1) issue_b(k + 2);  // the raw buffer has been read
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (uint32_t)((ks >> 2) * 8192 + 32 * (ks & 3));
-                const uint64_t dh = desc_k(base + chl::BHI + off), dl = desc_k(base + chl::BLO + off);
-                mma_tf32_ta(tmem + kCD, tmem + kCAH + 8 * ks, dh, id, ks > 0);
-                mma_tf32_ta(tmem + kCD, tmem + kCAH + 8 * ks, dl, id, 1);
-                mma_tf32_ta(tmem + kCD, tmem + kCAL + 8 * ks, dh, id, 1);
-            }
-            mma_commit(bar_mma);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");  // this step's offsets (the next step's may fly)
+        if (tid == 0 && !bad) {
             bad = !chain_wait(bar_mma, (uint32_t)(i & 1));
+            if (!bad && k + 2 < k1) issue_b(k + 2);  // the product has read the buffer
         }
-        if (k + 2 < k1) issued = k + 3;
         if (named_bar_or(1, kChainT, bad)) {
             ok = false;
             break;
         }
+        waited = k + 1;
+        if (k + 2 < k1) issued = k + 3;
         tc_fence_after();
         {
             const float* of = reinterpret_cast<const float*>(sm + chl::OFS) + (int)(k & 1) * kWsMat;
@@ -1402,6 +1360,7 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
                 }
             }
         }
+        issue_ofs(k + 2);  // buffer k & 1 has been read
         if (k + 1 < k1) chain_put(tq, s);
         tmem_wait_st();
         tc_fence_before();
@@ -1412,7 +1371,7 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
         for (int r = 0; r < kD; ++r) p.dS0[(bh * kD + r) * kD + c] = s[r];
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    if (tid == 0) {  // loads still in flight after an early exit
+    if (tid == 0) {  // copies still in flight after an early exit
         for (long long k = waited; k < issued; ++k) {
             const long long i = k - k0;
             mbar_wait_bounded(bar_full0 + 8 * (uint32_t)(i & 1), (uint32_t)((i >> 1) & 1), kTcTimeout);
@@ -1427,7 +1386,7 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 template <typename Tin, bool IP>
@@ -1438,12 +1397,8 @@ int launch_typed(const BParams& p, cudaStream_t st) {
     cudaFuncSetAttribute(falcon_bwd_prep<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
     cudaFuncSetAttribute(falcon_bwd_grad<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, grad_smem);
     falcon_bwd_prep<Tin, IP><<<chunks, kCT, prep_smem, st>>>(p);
-    ChainParams cp{};
-    cp.p = p;
-    const long long rows = p.BH * p.N * (kWsChunk / kD);  // the workspace as rows of 64 floats
-    if (rows >= (1LL << 31) || !encode_rows_f32_sw128(&cp.tm_ws, p.ws, rows)) return 4;
     cudaFuncSetAttribute(falcon_bwd_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chl::ALLOC);
-    falcon_bwd_chain<<<(unsigned)(2 * p.BH), kChainT, chl::ALLOC, st>>>(cp);
+    falcon_bwd_chain<<<(unsigned)(2 * p.BH), kChainT, chl::ALLOC, st>>>(p);
     falcon_bwd_grad<Tin, IP><<<chunks, kCT, grad_smem, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
