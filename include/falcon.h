@@ -215,10 +215,10 @@ int falcon_bwd(int variant, const void* q, const void* k, const void* v, const f
                float* dS0, float* dtail, const falcon_dims_t* dims, int chunk, void* workspace,
                size_t workspace_bytes, void* stream);
 
-/* Workspace bytes falcon_bwd needs: B*H*ceil(T/64) * 96 KiB (per chunk six 16 KiB slots: the
+/* Workspace bytes falcon_bwd needs: B*H*ceil(T/64) * 99 KiB (per chunk six 16 KiB slots: the
  * transition's offset and the state-free adjoint term in fp32; the transition, the inverse of the
- * chunk's triangular system, the chunk-start state and the chunk-end adjoint, each as two bf16 parts);
- * 0 for invalid or unsupported arguments. */
+ * chunk's triangular system, the chunk-start state and the chunk-end adjoint, each as two bf16 parts;
+ * and 3 KiB of per-token scalars); 0 for invalid or unsupported arguments. */
 size_t falcon_bwd_workspace_bytes(int variant, const falcon_dims_t* dims, int chunk);
 
 /* ABI version of this header: 4. */

@@ -225,11 +225,11 @@ def _bwd(variant=F.FALCON_1, dims=None, chunk=64, ws=A + (20 << 30), ws_bytes=No
 
 
 def test_bwd_workspace_bytes(lib):
-    # B*H*ceil(T/64) chunks of six 64 x 64 x 4-byte slots: U and V in fp32; M, T, S_n and dS_{n+1}
-    # each as bf16 hi and lo tiles
-    assert F.falcon_bwd_workspace_bytes(F.FALCON_1, F.make_dims(8, 12, 1024, 64, 64), 64) == 8 * 12 * 16 * 98304
+    # B*H*ceil(T/64) chunks of six 64 x 64 x 4-byte slots (U and V in fp32; M, T, S_n and dS_{n+1}
+    # each as bf16 hi and lo tiles) and 3 KiB of the chunk's scalars
+    assert F.falcon_bwd_workspace_bytes(F.FALCON_1, F.make_dims(8, 12, 1024, 64, 64), 64) == 8 * 12 * 16 * 101376
     assert F.falcon_bwd_workspace_bytes(F.FALCON_1A, F.make_dims(2, 3, 65, 64, 64, dtype=F.FALCON_F32), 64) \
-        == 2 * 3 * 2 * 98304
+        == 2 * 3 * 2 * 101376
     assert F.falcon_bwd_workspace_bytes(F.FALCON_1, F.make_dims(2, 3, 0, 64, 64), 64) == 0
     for v in (F.FALCON_2, F.FALCON_2A, F.FALCON_3, F.FALCON_3A):  # no backward kernel for these yet
         assert F.falcon_bwd_workspace_bytes(v, F.make_dims(2, 3, 64, 64, 64, window=2 if v >= 5 else 1), 64) == 0

@@ -50,9 +50,11 @@ using namespace ptx;
 constexpr int kD = 64;        // dk = dv
 constexpr int kC = 64;        // chunk length
 constexpr int kWsMat = kD * kD;             // floats per workspace matrix
-constexpr int kWsChunk = 6 * kWsMat;        // M, U, V, T, S_n, dS_{n+1}: U and V dense fp32; M, T, S_n and
-                                            // dS_{n+1} as bf16 hi and lo tiles (8 KB each, hi first)
-enum { kWsM = 0, kWsU = 1, kWsV = 2, kWsT = 3, kWsS = 4, kWsDS = 5 };
+constexpr int kWsScal = 768;                // floats: the chunk's scalars, as the prep kernel computed them
+constexpr int kWsChunk = 6 * kWsMat + kWsScal;  // M, U, V, T, S_n, dS_{n+1}, the scalars: U and V dense
+                                            // fp32; M, T, S_n and dS_{n+1} as bf16 hi and lo tiles (8 KB
+                                            // each, hi first)
+enum { kWsM = 0, kWsU = 1, kWsV = 2, kWsT = 3, kWsS = 4, kWsDS = 5, kWsSC = 6 };
 
 struct BParams {
     const void* q;
@@ -76,12 +78,14 @@ struct BParams {
     float eps, eps_gamma;
 };
 
-// Scalars of one chunk, recomputed identically by the prep and gradient kernels.
+// Scalars of one chunk: computed by the prep kernel, which stores them for the gradient kernel.
 struct Scal {
     float eta[kC], lam[kC], den[kC], gam[kC], L[kC], Lx[kC], eL[kC], eLx[kC], w[kC];
     int unc[kC], live[kC];  // clamp inactive (alpha differentiable); eta = beta / den differentiable
     float eLC;
 };
+constexpr int kScal16 = (int)(sizeof(Scal) + 15) / 16 * 16;  // bytes, as copied
+static_assert(kScal16 <= kWsScal * 4, "the scalars fit their workspace slot");
 
 
 // ================================================================================================
@@ -181,6 +185,12 @@ __device__ __forceinline__ void store32(float* dst, const float* v) {
 
 __device__ __forceinline__ void cp_async16z(uint32_t dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+// One bulk copy shared -> global (addresses 16-byte aligned, size a multiple of 16) as its own group of
+// this thread; the source is free again after bulk_wait_read, the copy complete after bulk_wait_all.
+__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
 // Rows r < nr of q, k, v and dout for the chunk's tokens t0 + r (k shifted: token t0 + r - 1, the
@@ -287,6 +297,7 @@ __device__ void chunk_scalars(Scal& s, float nx, const BParams& p, long long bh,
         s.w[2 * l] = s.eta[2 * l] * expf(LC - (ex + a));
         s.w[2 * l + 1] = s.eta[2 * l + 1] * expf(LC - v);
     }
+    fence_async_smem();  // the block may leave by a bulk copy
     __syncthreads();
 }
 
@@ -555,6 +566,7 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
             mma_commit(cs.bar);
         }
         chunk_scalars(s, tid < kC ? row_norm<EX>(TP(L::X), xl, tid) : 0.f, p, bh, t0, nr);
+        if (tid == 0) bulk_store(ws + kWsSC * kWsMat, base + L::SCAL, kScal16);
         ok = cs.wait();
         float* AT = reinterpret_cast<float*>(sm + L::AT);
         if (ok) {
@@ -595,20 +607,19 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
             }
             cs.publish();
             invert128(AT, reinterpret_cast<float*>(TP(L::TH)));
-            {  // T to its hi / lo tiles and to the workspace as the same tiles (hi, then lo)
+            {  // T to its hi / lo tiles
                 const int r = tid >> 2, cq = 16 * (tid & 3);
-                uint8_t* tg = reinterpret_cast<uint8_t*>(ws + kWsT * kWsMat);
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = AT[r * kAS + cq + 8 * q + e];
                     st8_hilo(TP(L::TH), TP(L::TL), sw128(r, cq + 8 * q), x);
-                    st8_hilo(tg, tg + kTile, sw128(r, cq + 8 * q), x);
                 }
             }
             cs.publish();
-            if (tid == 0) {  // E = [P; X^T diag(w)] T into columns 128-191
+            if (tid == 0) {  // the T tiles to the workspace as they are; E = [P; X^T diag(w)] T into columns 128-191
+                bulk_store(ws + kWsT * kWsMat, TA(L::TH), 2 * kTile);
                 tc_fence_after();
                 mma64(tmem + 128, tmem_a(tmem + 64), mnmaj(TA(L::TH)), 64, false);
                 mma64(tmem + 128, tmem_a(tmem + 64), mnmaj(TA(L::TL)), 64, true);
@@ -652,21 +663,23 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
                     for (int e = 0; e < 8; ++e) x[e] = fmaf(ei, x[e], -v[8 * q + e]);
                     st8_hilo(TP(L::AOH), TP(L::AOL), sw128(i, c0 + 8 * q), x);
                 }
-            } else {  // M row f = e^{L_C} e_f - K_f (and M^T column f), U row f
+            } else {  // M row f = e^{L_C} e_f - K_f as hi / lo tiles, U row f: staged in slots read no more
                 const int f = ln - 64;
                 const float gC = s.eLC;
                 float v[32];
                 tld32(tq + 128 + c0, v);
-                uint8_t* mg = reinterpret_cast<uint8_t*>(ws + kWsM * kWsMat);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = (c0 + e == f ? gC : 0.f) - v[e];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st8_hilo(mg, mg + kTile, sw128(f, c0 + 8 * q), v + 8 * q);
+                for (int q = 0; q < 4; ++q) st8_hilo(TP(L::DXL), TP(L::X), sw128(f, c0 + 8 * q), v + 8 * q);
                 tld32(tq + 192 + c0, v);
-                store32(ws + kWsU * kWsMat + f * kD + c0, v);
+                store32(reinterpret_cast<float*>(TP(L::DXH)) + f * kD + c0, v);  // DXH, YH: 16 KB
             }
             cs.publish();
-            if (tid == 0) {  // V = Ao^T dO into columns 0-63
+            if (tid == 0) {  // M and U to the workspace; V = Ao^T dO into columns 0-63
+                bulk_store(ws + kWsM * kWsMat, TA(L::DXL), kTile);
+                bulk_store(ws + kWsM * kWsMat + kTile / 4, TA(L::X), kTile);
+                bulk_store(ws + kWsU * kWsMat, TA(L::DXH), 2 * kTile);
                 tc_fence_after();
                 mma64(tmem, mnmaj(TA(L::AOH)), mnmaj(TA(L::DO)), 64, false);
                 mma64(tmem, mnmaj(TA(L::AOL)), mnmaj(TA(L::DO)), 64, true);
@@ -675,13 +688,19 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
             }
             ok = cs.wait();
         }
-        if (ok && ln < 64) {
-            float v[32];
-            tld32(tq + c0, v);
-            store32(ws + kWsV * kWsMat + ln * kD + c0, v);
+        if (ok) {  // V through the Ao slots (read no more) to the workspace
+            if (ln < 64) {
+                float v[32];
+                tld32(tq + c0, v);
+                store32(reinterpret_cast<float*>(TP(L::AOH)) + ln * kD + c0, v);
+            }
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) bulk_store(ws + kWsV * kWsMat, TA(L::AOH), 2 * kTile);
         }
     } else {
         chunk_scalars(s, tid < kC ? row_norm<EX>(TP(L::X), xl, tid) : 0.f, p, bh, t0, nr);
+        if (tid == 0) bulk_store(ws + kWsSC * kWsMat, base + L::SCAL, kScal16);
         if (ln < 64) {  // diag(w) X and diag(e^L) dO, row j, as hi / lo tiles
             const int j = ln;
             const float wj = s.w[j], ej = s.eL[j];
@@ -717,21 +736,28 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
             mma_commit(cs.bar);
         }
         ok = cs.wait();
-        if (ok) {
+        if (ok) {  // U (slots 0, 1), V (slots 2, 3) and the tiles of M = e^{L_C} I (slots 4, 5), then out
             const int f = ln & 63;
             float v[32];
             tld32(tq + (ln < 64 ? 0 : 64) + c0, v);
-            store32(ws + (ln < 64 ? kWsU : kWsV) * kWsMat + f * kD + c0, v);
-            if (ln < 64) {  // M = e^{L_C} I
-                uint8_t* mg = reinterpret_cast<uint8_t*>(ws + kWsM * kWsMat);
+            store32(reinterpret_cast<float*>(TP(ln < 64 ? 0 : 2)) + f * kD + c0, v);
+            if (ln < 64) {
                 float m[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) m[e] = c0 + e == f ? s.eLC : 0.f;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) st8_hilo(mg, mg + kTile, sw128(f, c0 + 8 * q), m + 8 * q);
+                for (int q = 0; q < 4; ++q) st8_hilo(TP(4), TP(5), sw128(f, c0 + 8 * q), m + 8 * q);
+            }
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                bulk_store(ws + kWsU * kWsMat, TA(0), 2 * kTile);
+                bulk_store(ws + kWsV * kWsMat, TA(2), 2 * kTile);
+                bulk_store(ws + kWsM * kWsMat, TA(4), 2 * kTile);
             }
         }
     }
+    if (tid == 0) bulk_wait_all();  // the bulk copies have read their sources before the CTA ends
     cs.finish(tmem, L::COLS);
 }
 
@@ -797,6 +823,8 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
                     const int e = tid + kCT * u;
                     cp_async16z(TA(dst[m][h]) + 16 * e, wsb + (size_t)src[m] * kWsMat * 4 + h * kTile + 16 * e, 16u);
                 }
+        if (tid < kScal16 / 16)  // the chunk's scalars as the prep kernel computed them
+            cp_async16z(base + L::SCAL + 16 * tid, wsb + (size_t)kWsSC * kWsMat * 4 + 16 * tid, 16u);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
     if (tid < kC) {
@@ -845,7 +873,6 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
         for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
         if (lane == 0) red[warp] = dot;
     }
-    chunk_scalars(s, tid < kC ? row_norm<EX>(TP(L::X), xl, tid) : 0.f, p, bh, t0, nr);
     ok = cs.wait();
 
     // ---- Z (Falcon-1) and P: row i = ln < 64, columns c0 ..
@@ -921,8 +948,8 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
             if constexpr (!IP) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) st8_hilo(TP(L::YZ), TP(L::ZL), sw128(i, c0 + 8 * q), d + 8 * q);
-            } else if (i < nr) {
-                store32(p.dv + (bh * p.T + t0 + i) * kD + c0, d);
+            } else {  // dV, staged in the T slots (unused here)
+                store32(reinterpret_cast<float*>(TP(L::TH)) + i * kD + c0, d);
             }
         }
         if constexpr (!IP) {
@@ -948,14 +975,15 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
 #pragma unroll
             for (int q = 0; q < 4; ++q) row8<EX>(TP(L::DO), dl, sw128(ln, c0 + 8 * q), v + 8 * q);
             tst_a32(tq + 192, tq + 224, hf, v);
-        } else if (!IP) {
+        } else if (!IP) {  // dV = dZ, staged in the dR slots (read no more)
             const int i = ln - 64;
             tld32(tq + c0, v);
-            if (i < nr) store32(p.dv + (bh * p.T + t0 + i) * kD + c0, v);
+            store32(reinterpret_cast<float*>(TP(L::YZ)) + i * kD + c0, v);
             tst_a32(tq + 192, tq + 224, hf, v);
         }
         cs.publish();
-        if (tid == 0) {  // [dO; dZ] [R^T | S^T] into columns 0-127 (B: [R; S] K-major, N = 128)
+        if (tid == 0) {  // dV out; [dO; dZ] [R^T | S^T] into columns 0-127 (B: [R; S] K-major, N = 128)
+            bulk_store(p.dv + (bh * p.T + t0) * kD, TA(IP ? L::TH : L::YZ), (uint32_t)nr * kD * 4);
             tc_fence_after();
             const Opd ah = tmem_a(tmem + 192), al = tmem_a(tmem + 224);
             mma64(tmem, ah, kmaj(TA(L::PRH)), 128, false);
@@ -966,6 +994,7 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
                 mma64(tmem, al, kmaj(TA(L::PRH)), 128, true);
             }
             mma_commit(cs.bar);
+            bulk_wait_read<0>();  // the next phase rewrites the slots dV was staged in
         }
         ok = cs.wait();
     }
@@ -1061,7 +1090,7 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
                 rowL = fmaf(qv[e], a[e], rowL);
                 a[e] = fmaf(ei, a[e], b[e]);
             }
-            if (i < nr) store32(p.dq + (bh * p.T + t0 + i) * kD + c0, a);
+            store32(reinterpret_cast<float*>(TP(L::TH)) + i * kD + c0, a);  // dQ, staged in the T slots
             atomicAdd(&dL[i], ei * rowL);
             tld32(tq + 128 + c0, a);  // dSc^T Q + dG^T X
             tld32(tq + c0, b);        // R dS'^T
@@ -1090,7 +1119,9 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
                     make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
             atomicAdd(&dLx[i], -di * rowX);
         }
+        fence_async_smem();
         __syncthreads();
+        if (tid == 0) bulk_store(p.dq + (bh * p.T + t0) * kD, TA(L::TH), (uint32_t)nr * kD * 4);
         // scalars: d eta and dL from w and the chunk-end decay; d log gamma; the clamp; eta = beta / den
         if (tid < 32) {
             const int l = tid;
@@ -1177,6 +1208,7 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
                 reinterpret_cast<float4*>(p.dk + (bh * p.T + p.T - 1) * kD)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    if (tid == 0) bulk_wait_all();  // the bulk copies have read their sources before the CTA ends
     cs.finish(tmem, 256);
 }
 
