@@ -36,6 +36,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "falcon_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -74,7 +76,8 @@ struct BParams {
     float* dS0;
     float* dtail;
     float* ws;
-    long long T, pos, N, BH;  // tokens, position, chunks per sequence, sequences
+    long long T, pos, N, BH;  // tokens, position, chunks per sequence, sequences of this launch
+    long long bh0;            // the first of them
     float eps, eps_gamma;
 };
 
@@ -531,9 +534,9 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
     Scal& s = *reinterpret_cast<Scal*>(sm + L::SCAL);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BAR + 16);
     ChunkSync cs{base + L::BAR, 0u};
-    const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N, t0 = nck * kC;
+    const long long bh = p.bh0 + blockIdx.x / p.N, nck = blockIdx.x % p.N, t0 = nck * kC;
     const int nr = (int)min((long long)kC, p.T - t0);
-    float* ws = p.ws + cid * kWsChunk;
+    float* ws = p.ws + (bh * p.N + nck) * kWsChunk;
 
     if (tid == 0) {
         mbar_init(cs.bar, 1);
@@ -793,9 +796,9 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
     float* red = c2 + kC;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BAR + 16);
     ChunkSync cs{base + L::BAR, 0u};
-    const long long cid = blockIdx.x, bh = cid / p.N, nck = cid % p.N, t0 = nck * kC;
+    const long long bh = p.bh0 + blockIdx.x / p.N, nck = blockIdx.x % p.N, t0 = nck * kC;
     const int nr = (int)min((long long)kC, p.T - t0);
-    const uint8_t* wsb = reinterpret_cast<const uint8_t*>(p.ws + cid * kWsChunk);
+    const uint8_t* wsb = reinterpret_cast<const uint8_t*>(p.ws + (bh * p.N + nck) * kWsChunk);
     const uint8_t* xl = EX ? nullptr : TP(L::XL);
     const uint8_t* ql = EX ? nullptr : TP(L::QL);
 
@@ -1227,7 +1230,7 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 // D = (M_n^T dS)^T; the same tile read MN-major). Both operands are split into bf16 hi and lo parts and
 // D = A_hi B_hi + A_hi B_lo + A_lo B_hi (fp32 sums). M_n's hi and lo tiles, as the prep kernel stores
 // them, arrive by one bulk copy two steps ahead into one of two buffers, U_n / V_n by 16-byte
-// asynchronous copies two steps ahead, added in registers; while the product runs each thread stores
+// asynchronous copies one step ahead, added in registers; while the product runs each thread stores
 // its column of S_n / dS_{n+1} for the gradient kernel. Every wait is bounded: on timeout the CTA raises
 // the device flag, drains what it issued and frees its tensor memory.
 constexpr int kChainT = 128;
@@ -1275,7 +1278,7 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const BParams p) 
     const int tid = threadIdx.x, warp = tid >> 5;
     const uint32_t bar_full0 = base + chl::BAR, bar_mma = bar_full0 + 16, bar_drain = bar_full0 + 24;  // full: two
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + chl::BAR + 32);
-    const long long bh = blockIdx.x >> 1, N = p.N;
+    const long long bh = p.bh0 + (blockIdx.x >> 1), N = p.N;
     const bool bwd = (blockIdx.x & 1) != 0;  // this CTA's scan
     const long long k0 = bwd ? N : 0, k1 = k0 + N;  // its steps of the 2 N
     if (tid == 0) {
@@ -1328,7 +1331,6 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const BParams p) 
     }
     long long issued = k1 < k0 + 2 ? k1 : k0 + 2;  // steps whose M has been requested: [k0, issued)
     issue_ofs(k0);
-    issue_ofs(k0 + 1);
     tc_fence_before();
     __syncthreads();
     bool ok = true;
@@ -1337,6 +1339,7 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const BParams p) 
     for (long long k = k0; k < k1; ++k) {
         const long long n = chunk_of(k), i = k - k0;
         const uint32_t bb = base + chl::B + (uint32_t)(i & 1) * chl::BSZ;
+        issue_ofs(k + 1);  // its buffer was last read before the previous step's closing barrier
         bool bad = false;
         if (tid == 0) {
             bad = !chain_wait(bar_full0 + 8 * (uint32_t)(i & 1), (uint32_t)((i >> 1) & 1));
@@ -1392,7 +1395,6 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const BParams p) 
                 }
             }
         }
-        issue_ofs(k + 2);  // buffer k & 1 has been read
         if (k + 1 < k1) chain_put(tq, s);
         tmem_wait_st();
         tc_fence_before();
@@ -1421,18 +1423,85 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const BParams p) 
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
+// Streams and events of a split call (created once per device; a mutex orders the calls that use them).
+struct BwdStreams {
+    bool ready = false;
+    cudaStream_t half[2], chain;
+    cudaEvent_t fork, prep[2], chained[2], done[2];
+};
+std::mutex g_bwd_mu;
+BwdStreams g_bwd_streams[64];
+
+bool bwd_streams(BwdStreams*& out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    BwdStreams& b = g_bwd_streams[dev];
+    if (!b.ready) {
+        int least = 0, greatest = 0;
+        if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
+        bool ok = cudaStreamCreateWithPriority(&b.half[0], cudaStreamNonBlocking, least) == cudaSuccess &&
+                  cudaStreamCreateWithPriority(&b.half[1], cudaStreamNonBlocking, least) == cudaSuccess &&
+                  cudaStreamCreateWithPriority(&b.chain, cudaStreamNonBlocking, greatest) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&b.fork, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; ok && i < 2; ++i)
+            ok = cudaEventCreateWithFlags(&b.prep[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&b.chained[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&b.done[i], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) return false;
+        b.ready = true;
+    }
+    out = &b;
+    return true;
+}
+
+// Each kernel over the sequences of p, on stream st.
 template <typename Tin, bool IP>
-int launch_typed(const BParams& p, cudaStream_t st) {
+bool enqueue_prep(const BParams& p, cudaStream_t st) {
     constexpr bool EX = sizeof(Tin) == 2;
-    const unsigned chunks = (unsigned)(p.BH * p.N);
-    constexpr int prep_smem = PrepLay<EX, IP>::ALLOC, grad_smem = GradLay<EX, IP>::ALLOC;
+    constexpr int prep_smem = PrepLay<EX, IP>::ALLOC;
     cudaFuncSetAttribute(falcon_bwd_prep<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_smem);
-    cudaFuncSetAttribute(falcon_bwd_grad<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, grad_smem);
-    falcon_bwd_prep<Tin, IP><<<chunks, kCT, prep_smem, st>>>(p);
+    falcon_bwd_prep<Tin, IP><<<(unsigned)(p.BH * p.N), kCT, prep_smem, st>>>(p);
+    return cudaGetLastError() == cudaSuccess;
+}
+bool enqueue_chain(const BParams& p, cudaStream_t st) {
     cudaFuncSetAttribute(falcon_bwd_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, chl::ALLOC);
     falcon_bwd_chain<<<(unsigned)(2 * p.BH), kChainT, chl::ALLOC, st>>>(p);
-    falcon_bwd_grad<Tin, IP><<<chunks, kCT, grad_smem, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+    return cudaGetLastError() == cudaSuccess;
+}
+template <typename Tin, bool IP>
+bool enqueue_grad(const BParams& p, cudaStream_t st) {
+    constexpr bool EX = sizeof(Tin) == 2;
+    constexpr int grad_smem = GradLay<EX, IP>::ALLOC;
+    cudaFuncSetAttribute(falcon_bwd_grad<Tin, IP>, cudaFuncAttributeMaxDynamicSharedMemorySize, grad_smem);
+    falcon_bwd_grad<Tin, IP><<<(unsigned)(p.BH * p.N), kCT, grad_smem, st>>>(p);
+    return cudaGetLastError() == cudaSuccess;
+}
+
+// One call: with at least 4 sequences, two halves of them on two streams, their chains on a
+// high-priority stream, so that one half's chain (a few CTAs per SM) runs beside the other half's
+// chunk kernels; the caller's stream waits for both halves.
+template <typename Tin, bool IP>
+int launch_typed(const BParams& p, cudaStream_t st) {
+    if (p.BH < 4) return enqueue_prep<Tin, IP>(p, st) && enqueue_chain(p, st) && enqueue_grad<Tin, IP>(p, st) ? 0 : 4;
+    std::lock_guard<std::mutex> lock(g_bwd_mu);
+    BwdStreams* b = nullptr;
+    if (!bwd_streams(b)) return 4;
+    BParams h[2] = {p, p};
+    h[0].BH = p.BH / 2;
+    h[1].bh0 = p.bh0 + h[0].BH;
+    h[1].BH = p.BH - h[0].BH;
+    bool ok = cudaEventRecord(b->fork, st) == cudaSuccess;
+    for (int i = 0; ok && i < 2; ++i)
+        ok = cudaStreamWaitEvent(b->half[i], b->fork, 0) == cudaSuccess && enqueue_prep<Tin, IP>(h[i], b->half[i]) &&
+             cudaEventRecord(b->prep[i], b->half[i]) == cudaSuccess;
+    for (int i = 0; ok && i < 2; ++i)
+        ok = cudaStreamWaitEvent(b->chain, b->prep[i], 0) == cudaSuccess && enqueue_chain(h[i], b->chain) &&
+             cudaEventRecord(b->chained[i], b->chain) == cudaSuccess;
+    for (int i = 0; ok && i < 2; ++i)
+        ok = cudaStreamWaitEvent(b->half[i], b->chained[i], 0) == cudaSuccess &&
+             enqueue_grad<Tin, IP>(h[i], b->half[i]) && cudaEventRecord(b->done[i], b->half[i]) == cudaSuccess &&
+             cudaStreamWaitEvent(st, b->done[i], 0) == cudaSuccess;
+    return ok ? 0 : 4;
 }
 
 }  // namespace
@@ -1469,6 +1538,7 @@ int launch_bwd(const Launch& a, const BwdArgs& g, cudaStream_t st) {
     p.pos = a.pos;
     p.N = (a.T + kC - 1) / kC;
     p.BH = a.B * a.H;
+    p.bh0 = 0;
     p.eps = a.eps;
     p.eps_gamma = a.eps_gamma;
     if (p.BH == 0) return 0;
