@@ -1424,10 +1424,11 @@ __global__ void __launch_bounds__(kChainT, 1) falcon_bwd_chain(const BParams p) 
 }
 
 // Streams and events of a split call (created once per device; a mutex orders the calls that use them).
+constexpr int kGroups = 4;
 struct BwdStreams {
     bool ready = false;
-    cudaStream_t half[2], chain;
-    cudaEvent_t fork, prep[2], chained[2], done[2];
+    cudaStream_t group[kGroups], chain[kGroups];
+    cudaEvent_t fork, prep[kGroups], chained[kGroups], done[kGroups];
 };
 std::mutex g_bwd_mu;
 BwdStreams g_bwd_streams[64];
@@ -1439,12 +1440,11 @@ bool bwd_streams(BwdStreams*& out) {
     if (!b.ready) {
         int least = 0, greatest = 0;
         if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
-        bool ok = cudaStreamCreateWithPriority(&b.half[0], cudaStreamNonBlocking, least) == cudaSuccess &&
-                  cudaStreamCreateWithPriority(&b.half[1], cudaStreamNonBlocking, least) == cudaSuccess &&
-                  cudaStreamCreateWithPriority(&b.chain, cudaStreamNonBlocking, greatest) == cudaSuccess &&
-                  cudaEventCreateWithFlags(&b.fork, cudaEventDisableTiming) == cudaSuccess;
-        for (int i = 0; ok && i < 2; ++i)
-            ok = cudaEventCreateWithFlags(&b.prep[i], cudaEventDisableTiming) == cudaSuccess &&
+        bool ok = cudaEventCreateWithFlags(&b.fork, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; ok && i < kGroups; ++i)
+            ok = cudaStreamCreateWithPriority(&b.group[i], cudaStreamNonBlocking, least) == cudaSuccess &&
+                 cudaStreamCreateWithPriority(&b.chain[i], cudaStreamNonBlocking, greatest) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&b.prep[i], cudaEventDisableTiming) == cudaSuccess &&
                  cudaEventCreateWithFlags(&b.chained[i], cudaEventDisableTiming) == cudaSuccess &&
                  cudaEventCreateWithFlags(&b.done[i], cudaEventDisableTiming) == cudaSuccess;
         if (!ok) return false;
@@ -1477,29 +1477,32 @@ bool enqueue_grad(const BParams& p, cudaStream_t st) {
     return cudaGetLastError() == cudaSuccess;
 }
 
-// One call: with at least 4 sequences, two halves of them on two streams, their chains on a
-// high-priority stream, so that one half's chain (a few CTAs per SM) runs beside the other half's
-// chunk kernels; the caller's stream waits for both halves.
+// One call: with at least 4 sequences, 2 (or with 16 and more, 4) groups of them on streams of their
+// own, each group's chain on a high-priority stream, so that a chain launch (a few CTAs per SM) runs
+// beside the other groups' chunk kernels; the caller's stream waits for every group.
 template <typename Tin, bool IP>
 int launch_typed(const BParams& p, cudaStream_t st) {
     if (p.BH < 4) return enqueue_prep<Tin, IP>(p, st) && enqueue_chain(p, st) && enqueue_grad<Tin, IP>(p, st) ? 0 : 4;
     std::lock_guard<std::mutex> lock(g_bwd_mu);
     BwdStreams* b = nullptr;
     if (!bwd_streams(b)) return 4;
-    BParams h[2] = {p, p};
-    h[0].BH = p.BH / 2;
-    h[1].bh0 = p.bh0 + h[0].BH;
-    h[1].BH = p.BH - h[0].BH;
+    const int G = p.BH >= 16 ? kGroups : 2;
+    BParams h[kGroups];
+    for (int i = 0; i < G; ++i) {
+        h[i] = p;
+        h[i].bh0 = p.bh0 + p.BH * i / G;
+        h[i].BH = p.BH * (i + 1) / G - p.BH * i / G;
+    }
     bool ok = cudaEventRecord(b->fork, st) == cudaSuccess;
-    for (int i = 0; ok && i < 2; ++i)
-        ok = cudaStreamWaitEvent(b->half[i], b->fork, 0) == cudaSuccess && enqueue_prep<Tin, IP>(h[i], b->half[i]) &&
-             cudaEventRecord(b->prep[i], b->half[i]) == cudaSuccess;
-    for (int i = 0; ok && i < 2; ++i)
-        ok = cudaStreamWaitEvent(b->chain, b->prep[i], 0) == cudaSuccess && enqueue_chain(h[i], b->chain) &&
-             cudaEventRecord(b->chained[i], b->chain) == cudaSuccess;
-    for (int i = 0; ok && i < 2; ++i)
-        ok = cudaStreamWaitEvent(b->half[i], b->chained[i], 0) == cudaSuccess &&
-             enqueue_grad<Tin, IP>(h[i], b->half[i]) && cudaEventRecord(b->done[i], b->half[i]) == cudaSuccess &&
+    for (int i = 0; ok && i < G; ++i)
+        ok = cudaStreamWaitEvent(b->group[i], b->fork, 0) == cudaSuccess && enqueue_prep<Tin, IP>(h[i], b->group[i]) &&
+             cudaEventRecord(b->prep[i], b->group[i]) == cudaSuccess;
+    for (int i = 0; ok && i < G; ++i)
+        ok = cudaStreamWaitEvent(b->chain[i], b->prep[i], 0) == cudaSuccess && enqueue_chain(h[i], b->chain[i]) &&
+             cudaEventRecord(b->chained[i], b->chain[i]) == cudaSuccess;
+    for (int i = 0; ok && i < G; ++i)
+        ok = cudaStreamWaitEvent(b->group[i], b->chained[i], 0) == cudaSuccess &&
+             enqueue_grad<Tin, IP>(h[i], b->group[i]) && cudaEventRecord(b->done[i], b->group[i]) == cudaSuccess &&
              cudaStreamWaitEvent(st, b->done[i], 0) == cudaSuccess;
     return ok ? 0 : 4;
 }
