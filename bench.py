@@ -522,7 +522,11 @@ def run_ours(args, w):
 # --------------------------------------------------------------------------------------------------
 # backward workloads (falcon_bwd)
 
-TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rates
+
+
+def _bwd_groups(bh):
+    """Groups of sequences one falcon_bwd call runs on streams of their own (three kernels each)."""
+    return 4 if bh >= 16 else (2 if bh >= 4 else 1)
 
 
 def _bwd_flops_per_chunk(w):
@@ -699,10 +703,10 @@ def run_ours_bwd(args, w):
     if rank != 0:
         return
     hbm, bf16_peak, src = _peaks()
-    tf32_peak = bf16_peak * TF32_PER_BF16
     chunks = B * H * (-(-T // w.chunk))
     flops = _bwd_flops_per_chunk(w) * chunks
     achieved = flops / (ms_step / 1e3) / 1e12
+    groups = _bwd_groups(B * H)
     line = {
         "metric": "falcon_bwd_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -711,16 +715,17 @@ def run_ours_bwd(args, w):
         "config": {"workload": w.name, "variant": w.variant, "batch": B, "heads": H, "seq_len": T, "d": dk,
                    "chunk": w.chunk, "parallelism": f"dp{world} (independent sequences per GPU, no collective)",
                    "l2": f"rotating {nsets} input/gradient sets of {step_bytes / 1e6:.1f} MB (> L2 between reuses)",
-                   "kernel": "backward: CUDA-core prep, chain and gradient kernels"},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
-                     "frac": achieved / tf32_peak, "traffic": None,
-                     "scope": "one falcon_bwd call (all three kernels); flops of the chunk algebra, each product "
-                              "counted once (tf32 tensor cores, 1-3 passes per product for fp32 accuracy)",
-                     "peak_source": f"{src} bf16 x nominal tf32/bf16 ratio 1.1/2.25",
+                   "kernel": "backward: prep, chain and gradient kernels, every product tcgen05 bf16 with fp32 "
+                             f"operands split into hi and lo; sequences in {groups} group(s) on their own streams"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": achieved / bf16_peak, "traffic": None,
+                     "scope": "one falcon_bwd call (all its kernels); flops of the chunk algebra, each product "
+                              "counted once (bf16 tensor cores, 1-3 passes per product for fp32 accuracy)",
+                     "peak_source": f"{src} dense bf16",
                      "flops_per_step": flops, "hbm_algorithmic_bytes_per_step": step_bytes,
                      "hbm_frac": step_bytes / (ms_step / 1e3) / 1e9 / hbm, "hbm_peak_source": src},
         "e2e": e2e,
-        "gpu_launches": args.steps * 3,
+        "gpu_launches": args.steps * 3 * groups,
         "clocks": clk,
     }
     if world == 1 and not args.no_cpu_baseline:

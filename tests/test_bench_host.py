@@ -39,6 +39,8 @@ def test_backward_counts():
     # q, k, v, dout (bf16) and beta, lambda read; fp32 dq, dk, dv, dbeta, dlambda written; dS_final, dS0
     expect = tok * 4 * 64 * 2 + tok * 8 + tok * 3 * 64 * 4 + tok * 8 + 2 * 96 * 64 * 64 * 4
     assert bench._bwd_bytes(w, 2) == expect
+    # a call runs its sequences in groups on streams of their own, three kernels each
+    assert [bench._bwd_groups(n) for n in (1, 3, 4, 15, 16, 96)] == [1, 1, 2, 2, 4, 4]
 
 
 def test_chunk_flops():
