@@ -575,14 +575,18 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
         if (ok) {
             float v[32];
             tld32(tq + c0, v);
-            if (ln < 64) {  // P row i into the A operand (columns 64-127, rows 0-63); diag(e^Lx) X row i
-                const int i = ln;
-                const float li = s.L[i];
+            {  // rows 0-63: P_ij = eta_j e^{L_i - L_j} Sc_ij (j <= i); rows 64-127: A_ij = eta_j e^{Lx_i - L_j} G_ij
+               // (j < i)
+                const int side = ln >> 6, i = ln & 63, lim = i + 1 - side;
+                const float base = side ? s.Lx[i] : s.L[i];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int j = c0 + e;
-                    v[e] = j <= i ? s.eta[j] * __expf(fminf(li - s.L[j], 0.f)) * v[e] : 0.f;
+                    v[e] = j < lim ? s.eta[j] * __expf(fminf(base - s.L[j], 0.f)) * v[e] : 0.f;
                 }
+            }
+            if (ln < 64) {  // P row i into the A operand (columns 64-127, rows 0-63); diag(e^Lx) X row i
+                const int i = ln;
                 tst_a32(tq + 64, tq + 96, hf, v);
                 const float di = s.eLx[i];
 #pragma unroll
@@ -595,12 +599,6 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
                 }
             } else {  // A row f (fp32, for the inverse); X^T diag(w) row f into the A operand
                 const int f = ln - 64;
-                const float lx = s.Lx[f];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = c0 + e;
-                    v[e] = j < f ? s.eta[j] * __expf(fminf(lx - s.L[j], 0.f)) * v[e] : 0.f;
-                }
                 float4* dst = reinterpret_cast<float4*>(AT + f * kAS + c0);
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) dst[k4] = make_float4(v[4 * k4], v[4 * k4 + 1], v[4 * k4 + 2], v[4 * k4 + 3]);
@@ -1007,44 +1005,29 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
         float d[32], g[32], cE[32], cL[32];
         tld32(tq + c0, d);
         tld32(tq + 128 + c0, g);
-        if (ln < 64) {
-            const int i = ln;
-            const float li = s.L[i];
-            float rowL = 0.f;
+        // rows 0-63: dP = dO R^T (j <= i) against Sc, giving dSc; rows 64-127 (Falcon-1): -dA = dZ R^T
+        // (j < i) against G, giving dG. One formula with x = dP or dA: the column terms x f g and
+        // x eta_j f g, the row sum of the latter, and the adjoint x eta_j f.
+        const int side = ln >> 6, i = ln & 63;
+        if (!IP || side == 0) {
+            const float base = side ? s.Lx[i] : s.L[i], sgn = side ? -1.f : 1.f;
+            const int lim = i + 1 - side;
+            float rsum = 0.f;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 const int j = c0 + e;
-                const bool on = j <= i;
-                const float f = __expf(fminf(li - s.L[j], 0.f)), dp = d[e];
-                const float pp = s.eta[j] * f * g[e];
-                cE[e] = on ? dp * f * g[e] : 0.f;
-                cL[e] = on ? dp * pp : 0.f;
-                rowL += cL[e];
-                d[e] = on ? dp * s.eta[j] * f : 0.f;  // dSc
+                const bool on = j < lim;
+                const float f = __expf(fminf(base - s.L[j], 0.f)), x = sgn * d[e], ef = s.eta[j] * f;
+                cE[e] = on ? x * f * g[e] : 0.f;
+                cL[e] = on ? x * ef * g[e] : 0.f;
+                rsum += cL[e];
+                d[e] = on ? x * ef : 0.f;
             }
+            uint8_t* th = TP(side ? L::ZL : L::YZ);
+            uint8_t* tl = TP(side ? L::TL : L::TH);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) st8_hilo(TP(L::YZ), TP(L::TH), sw128(i, c0 + 8 * q), d + 8 * q);
-            atomicAdd(&dL[i], rowL);
-        } else if (!IP) {
-            const int i = ln - 64;
-            const float lx = s.Lx[i];
-            float rowX = 0.f;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int j = c0 + e;
-                const bool on = j < i;
-                const float f = __expf(fminf(lx - s.L[j], 0.f)), da = -d[e];
-                const float aa = s.eta[j] * f * g[e] * da;
-                cE[e] = on ? da * f * g[e] : 0.f;
-                cL[e] = on ? aa : 0.f;
-                rowX += cL[e];
-                d[e] = on ? da * s.eta[j] * f : 0.f;  // dG
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) st8_hilo(TP(L::ZL), TP(L::TL), sw128(i, c0 + 8 * q), d + 8 * q);
-            atomicAdd(&dLx[i], rowX);
-        }
-        if (ln < 64 || !IP) {
+            for (int q = 0; q < 4; ++q) st8_hilo(th, tl, sw128(i, c0 + 8 * q), d + 8 * q);
+            atomicAdd(side ? &dLx[i] : &dL[i], rsum);
             const float ce = warp_colsum32(cE);
             const float cl = warp_colsum32(cL);
             atomicAdd(&deta[c0 + lane], ce);
