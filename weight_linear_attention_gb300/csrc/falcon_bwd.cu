@@ -1062,48 +1062,39 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
     if (ok) {
         float* EA = reinterpret_cast<float*>(TP(L::DSH));  // rows 0-63: dSc^T Q + dG^T X + diag(w) R dS'^T
         float* EB = reinterpret_cast<float*>(TP(L::YZ));   // rows 64-127: dG X - diag(e^Lx) dZ S^T
-        if (ln < 64) {
-            const int i = ln;
-            const float ei = s.eL[i], wi = s.w[i];
-            float a[32], b[32], qv[32];
-            tld32(tq + 64 + c0, a);   // dO S^T
-            tld32(tq + 192 + c0, b);  // dSc X
+        // rows 0-63: dQ = e^{L_i} dO S^T + dSc X (staged in the T slots), dL_i += e^{L_i} q_i . (dO S^T)_i;
+        // rows 64-127: dG X - e^{Lx_i} dZ S^T (half of dX), dLx_i -= e^{Lx_i} x_i . (dZ S^T)_i
+        const int side = ln >> 6, i = ln & 63;
+        if (!IP || side == 0) {
+            const float sc = side ? -s.eLx[i] : s.eL[i];
+            float a[32], b[32], rv[32];
+            tld32(tq + 64 + c0, a);   // dO S^T or dZ S^T
+            tld32(tq + 192 + c0, b);  // dSc X or dG X
+            const uint8_t* rh = TP(side ? L::X : L::Q);
+            const uint8_t* rl = side ? xl : ql;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) row8<EX>(TP(L::Q), ql, sw128(i, c0 + 8 * q), qv + 8 * q);
-            float rowL = 0.f;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                rowL = fmaf(qv[e], a[e], rowL);
-                a[e] = fmaf(ei, a[e], b[e]);
-            }
-            store32(reinterpret_cast<float*>(TP(L::TH)) + i * kD + c0, a);  // dQ, staged in the T slots
-            atomicAdd(&dL[i], ei * rowL);
-            tld32(tq + 128 + c0, a);  // dSc^T Q + dG^T X
-            tld32(tq + c0, b);        // R dS'^T
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                reinterpret_cast<float4*>(EA + i * kD)[(8 * hf + q) ^ (i & 15)] =
-                    make_float4(fmaf(wi, b[4 * q], a[4 * q]), fmaf(wi, b[4 * q + 1], a[4 * q + 1]),
-                                fmaf(wi, b[4 * q + 2], a[4 * q + 2]), fmaf(wi, b[4 * q + 3], a[4 * q + 3]));
-        } else if (!IP) {
-            const int i = ln - 64;
-            const float di = s.eLx[i];
-            float a[32], b[32], xv[32];
-            tld32(tq + 64 + c0, a);   // dZ S^T
-            tld32(tq + 192 + c0, b);  // dG X
-#pragma unroll
-            for (int q = 0; q < 4; ++q) row8<EX>(TP(L::X), xl, sw128(i, c0 + 8 * q), xv + 8 * q);
-            float rowX = 0.f;
+            for (int q = 0; q < 4; ++q) row8<EX>(rh, rl, sw128(i, c0 + 8 * q), rv + 8 * q);
+            float rsum = 0.f;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                rowX = fmaf(xv[e], a[e], rowX);
-                b[e] = fmaf(-di, a[e], b[e]);
+                rsum = fmaf(rv[e], a[e], rsum);
+                a[e] = fmaf(sc, a[e], b[e]);
             }
+            float4* dst = reinterpret_cast<float4*>(side ? EB : reinterpret_cast<float*>(TP(L::TH))) + 16 * i;
+            const int sw = side ? (i & 15) : 0;  // EB's rows are swizzled; dQ's staging is the plain image
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                reinterpret_cast<float4*>(EB + i * kD)[(8 * hf + q) ^ (i & 15)] =
-                    make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
-            atomicAdd(&dLx[i], -di * rowX);
+            for (int q = 0; q < 8; ++q) dst[(8 * hf + q) ^ sw] = make_float4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+            atomicAdd(side ? &dLx[i] : &dL[i], sc * rsum);
+            if (side == 0) {  // EA: dSc^T Q + dG^T X + diag(w) R dS'^T
+                const float wi = s.w[i];
+                tld32(tq + 128 + c0, a);
+                tld32(tq + c0, b);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    reinterpret_cast<float4*>(EA + i * kD)[(8 * hf + q) ^ (i & 15)] =
+                        make_float4(fmaf(wi, b[4 * q], a[4 * q]), fmaf(wi, b[4 * q + 1], a[4 * q + 1]),
+                                    fmaf(wi, b[4 * q + 2], a[4 * q + 2]), fmaf(wi, b[4 * q + 3], a[4 * q + 3]));
+            }
         }
         fence_async_smem();
         __syncthreads();
