@@ -355,7 +355,7 @@ __device__ __forceinline__ void merge_level(float* M, float* W) {
         float t[H];
 #pragma unroll
         for (int k = 0; k < H; ++k) t[k] = M[(r0 + k) * kAS + r0 + cc];  // T_aa column cc
-#pragma unroll
+#pragma unroll 1
         for (int r = 0; r < RQ; ++r) {
             const float* a = M + (r0 + H + RQ * rq + r) * kAS + r0;  // A_ba row
             float x = 0.f;
@@ -370,7 +370,7 @@ __device__ __forceinline__ void merge_level(float* M, float* W) {
         float w[H];
 #pragma unroll
         for (int k = 0; k < H; ++k) w[k] = W[(H * blk + k) * 33 + cc];
-#pragma unroll
+#pragma unroll 1
         for (int r = 0; r < RQ; ++r) {
             const float* t = M + (r0 + H + RQ * rq + r) * kAS + r0 + H;  // T_bb row
             float x = 0.f;
