@@ -585,9 +585,8 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
                     v[e] = j < lim ? s.eta[j] * __expf(fminf(base - s.L[j], 0.f)) * v[e] : 0.f;
                 }
             }
-            if (ln < 64) {  // P row i into the A operand (columns 64-127, rows 0-63); diag(e^Lx) X row i
+            if (ln < 64) {  // diag(e^Lx) X row i
                 const int i = ln;
-                tst_a32(tq + 64, tq + 96, hf, v);
                 const float di = s.eLx[i];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
@@ -597,15 +596,15 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
                     for (int e = 0; e < 8; ++e) x[e] *= di;
                     st8_hilo(TP(L::DXH), TP(L::DXL), sw128(i, c0 + 8 * q), x);
                 }
-            } else {  // A row f (fp32, for the inverse); X^T diag(w) row f into the A operand
+            } else {  // A row f (fp32, for the inverse), then X^T diag(w) row f in its place
                 const int f = ln - 64;
                 float4* dst = reinterpret_cast<float4*>(AT + f * kAS + c0);
 #pragma unroll
                 for (int k4 = 0; k4 < 8; ++k4) dst[k4] = make_float4(v[4 * k4], v[4 * k4 + 1], v[4 * k4 + 2], v[4 * k4 + 3]);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = elem<EX>(TP(L::X), xl, sw128(c0 + e, f)) * s.w[c0 + e];
-                tst_a32(tq + 64, tq + 96, hf, v);
             }
+            tst_a32(tq + 64, tq + 96, hf, v);  // [P; X^T diag(w)]: E's A operand (columns 64-127)
             cs.publish();
             invert128(AT, reinterpret_cast<float*>(TP(L::TH)));
             {  // T to its hi / lo tiles
