@@ -135,6 +135,15 @@ def test_headline_shape_all_sequences(variant):
         _check(f"v{variant} headline row {b}", gs, r)
 
 
+@pytest.mark.parametrize("B,H", [(1, 1), (1, 3), (2, 2), (1, 15), (17, 1), (3, 11)])
+def test_sequence_groups(B, H):
+    """A call runs its sequences unsplit (fewer than 4), in two groups (4 to 15) or in four groups
+    (16 and more, here of unequal sizes: 17 and 33 sequences) on streams of their own; every
+    sequence of every group is compared, with a ragged last chunk and a nonzero initial state."""
+    inp = _inputs(F1, 57 + B * H, 150, B=B, H=H)
+    _check(f"groups B={B} H={H}", _gpu(F1, inp), _ref(F1, inp))
+
+
 def test_argument_errors():
     inp = _inputs(F1, 56, 64)
     d = {n: inp[n].cuda() for n in ("q", "k", "v", "beta", "lam", "dout")}
