@@ -718,7 +718,7 @@ def run_ours_bwd(args, w):
                    "kernel": "backward: prep, chain and gradient kernels, every product tcgen05 bf16 with fp32 "
                              f"operands split into hi and lo; sequences in {groups} group(s) on their own streams"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
-                     "frac": achieved / bf16_peak, "traffic": None,
+                     "frac": achieved / bf16_peak, "traffic": _traffic(w.name, "bwd"),
                      "scope": "one falcon_bwd call (all its kernels); flops of the chunk algebra, each product "
                               "counted once (bf16 tensor cores, 1-3 passes per product for fp32 accuracy)",
                      "peak_source": f"{src} dense bf16",
