@@ -342,16 +342,16 @@ __device__ __forceinline__ float warp_colsum32(float (&v)[32]) {
 // T = (I + A)^{-1} in place for the strictly lower 64 x 64 A in M (fp32, stride kAS; zero on and above
 // the diagonal on entry, T with its unit diagonal on exit): the four 16 x 16 diagonal blocks by
 // right-looking column substitution (one thread per column), then two levels of block merges,
-// T_ba = -T_bb (A_ba T_aa) through the scratch W (32 x 33 floats), each of 128 threads a column of the
-// block over a quarter of its rows. The triangles' zeros stand in for the bounds of the sums, so every
+// T_ba = -T_bb (A_ba T_aa) through the scratch W (32 x 33 floats), each thread a column of the block
+// over an eighth of its rows. The triangles' zeros stand in for the bounds of the sums, so every
 // loop has a fixed length. All threads call it.
 template <int H>
 __device__ __forceinline__ void merge_level(float* M, float* W) {
-    constexpr int RQ = H / 4;  // rows per thread
+    constexpr int RQ = H / 8;  // rows per thread
     const int tid = threadIdx.x;
-    static_assert((64 / (2 * H)) * H * 4 == 128, "one thread per (block, column, row quarter)");
-    if (tid < 128) {
-        const int cc = tid % H, rq = (tid / H) % 4, blk = tid / (4 * H), r0 = 2 * H * blk;
+    static_assert((64 / (2 * H)) * H * 8 == kCT, "one thread per (block, column, eighth of the rows)");
+    const int cc = tid % H, rq = (tid / H) % 8, blk = tid / (8 * H), r0 = 2 * H * blk;
+    {
         float t[H];
 #pragma unroll
         for (int k = 0; k < H; ++k) t[k] = M[(r0 + k) * kAS + r0 + cc];  // T_aa column cc
@@ -365,8 +365,7 @@ __device__ __forceinline__ void merge_level(float* M, float* W) {
         }
     }
     __syncthreads();
-    if (tid < 128) {
-        const int cc = tid % H, rq = (tid / H) % 4, blk = tid / (4 * H), r0 = 2 * H * blk;
+    {
         float w[H];
 #pragma unroll
         for (int k = 0; k < H; ++k) w[k] = W[(H * blk + k) * 33 + cc];
