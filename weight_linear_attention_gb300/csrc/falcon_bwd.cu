@@ -85,7 +85,7 @@ struct BParams {
 struct Scal {
     float eta[kC], lam[kC], den[kC], gam[kC], L[kC], Lx[kC], eL[kC], eLx[kC], w[kC];
     int unc[kC], live[kC];  // clamp inactive (alpha differentiable); eta = beta / den differentiable
-    float eLC;
+    float eLC, LC;
 };
 constexpr int kScal16 = (int)(sizeof(Scal) + 15) / 16 * 16;  // bytes, as copied
 static_assert(kScal16 <= kWsScal * 4, "the scalars fit their workspace slot");
@@ -247,11 +247,25 @@ __device__ void load_chunk(const BParams& p, uint8_t* sm, uint32_t base, const i
     }
 }
 
-// Per-token scalars of the chunk; thread i < 64 passes nx = ||x_i||^2 of its row. Then the
-// chunk-local log prefixes. All threads call it.
-__device__ void chunk_scalars(Scal& s, float nx, const BParams& p, long long bh, long long t0, int n) {
-    const int i = threadIdx.x;
-    if (i < kC) {
+// Per-token scalars of the chunk from the key tile(s) (four threads per row share its squared norm),
+// beta and lambda; then the chunk-local log prefixes (one warp) and their exponentials (one thread a
+// row). All threads call it.
+template <bool EX>
+__device__ void chunk_scalars(Scal& s, const uint8_t* xh, const uint8_t* xl, const BParams& p, long long bh,
+                              long long t0, int n) {
+    const int tid = threadIdx.x, r = tid >> 2, q = tid & 3;
+    float nx = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float x[8];
+        row8<EX>(xh, xl, sw128(r, 16 * q + 8 * h), x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) nx = fmaf(x[e], x[e], nx);
+    }
+    nx += __shfl_xor_sync(0xffffffffu, nx, 1);
+    nx += __shfl_xor_sync(0xffffffffu, nx, 2);
+    if (q == 0) {
+        const int i = r;
         float eta = 0.f, alpha = 0.f, lm = 0.f, den = 0.f;
         int unc = 0, live = 0;
         if (i < n) {
@@ -276,8 +290,8 @@ __device__ void chunk_scalars(Scal& s, float nx, const BParams& p, long long bh,
         s.L[i] = log1pf(-alpha);
     }
     __syncthreads();
-    if (threadIdx.x < 32) {  // inclusive prefix over 64 rows: lane l holds rows 2l, 2l + 1
-        const int l = threadIdx.x;
+    if (tid < 32) {  // inclusive prefix over 64 rows: lane l holds rows 2l, 2l + 1
+        const int l = tid;
         const float a = s.L[2 * l], b = s.L[2 * l + 1];
         float v = a + b;
 #pragma unroll
@@ -288,34 +302,21 @@ __device__ void chunk_scalars(Scal& s, float nx, const BParams& p, long long bh,
         const float ex = v - a - b;  // exclusive prefix of row 2l
         s.L[2 * l] = ex + a;
         s.L[2 * l + 1] = v;
-        __syncwarp();
-        const float LC = __shfl_sync(0xffffffffu, v, 31);
-        if (l == 0) s.eLC = expf(LC);
         s.Lx[2 * l] = ex;
         s.Lx[2 * l + 1] = ex + a;
-        s.eL[2 * l] = expf(ex + a);
-        s.eL[2 * l + 1] = expf(v);
-        s.eLx[2 * l] = expf(ex);
-        s.eLx[2 * l + 1] = expf(ex + a);
-        s.w[2 * l] = s.eta[2 * l] * expf(LC - (ex + a));
-        s.w[2 * l + 1] = s.eta[2 * l + 1] * expf(LC - v);
+        if (l == 31) s.LC = v;
+    }
+    __syncthreads();
+    if (tid < kC) {
+        const int i = tid;
+        const float L = s.L[i], LC = s.LC;
+        s.eL[i] = expf(L);
+        s.eLx[i] = expf(s.Lx[i]);
+        s.w[i] = s.eta[i] * expf(LC - L);
+        if (i == 0) s.eLC = expf(LC);
     }
     fence_async_smem();  // the block may leave by a bulk copy
     __syncthreads();
-}
-
-// ||x_i||^2 of row i of the key tile(s).
-template <bool EX>
-__device__ __forceinline__ float row_norm(const uint8_t* xh, const uint8_t* xl, int i) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int q8 = 0; q8 < 8; ++q8) {
-        float x[8];
-        row8<EX>(xh, xl, sw128(i, 8 * q8), x);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(x[e], x[e], acc[e]);
-    }
-    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
 // Column sums of a warp's 32 rows: v[0..31] holds this lane's row over 32 columns; returns the sum of
@@ -567,7 +568,7 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
             }
             mma_commit(cs.bar);
         }
-        chunk_scalars(s, tid < kC ? row_norm<EX>(TP(L::X), xl, tid) : 0.f, p, bh, t0, nr);
+        chunk_scalars<EX>(s, TP(L::X), xl, p, bh, t0, nr);
         if (tid == 0) bulk_store(ws + kWsSC * kWsMat, base + L::SCAL, kScal16);
         ok = cs.wait();
         float* AT = reinterpret_cast<float*>(sm + L::AT);
@@ -698,7 +699,7 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_prep
             if (tid == 0) bulk_store(ws + kWsV * kWsMat, TA(L::AOH), 2 * kTile);
         }
     } else {
-        chunk_scalars(s, tid < kC ? row_norm<EX>(TP(L::X), xl, tid) : 0.f, p, bh, t0, nr);
+        chunk_scalars<EX>(s, TP(L::X), xl, p, bh, t0, nr);
         if (tid == 0) bulk_store(ws + kWsSC * kWsMat, base + L::SCAL, kScal16);
         if (ln < 64) {  // diag(w) X and diag(e^L) dO, row j, as hi / lo tiles
             const int j = ln;
