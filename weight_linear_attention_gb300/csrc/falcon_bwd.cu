@@ -841,15 +841,16 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
 
     if (tid == 0) {
         tc_fence_after();
+        // A = [Q; X]: the rows of X land in lanes 64-127, beside the rows of G
         if constexpr (!IP) {  // [X S | X dS'] into columns 0-127
             const Opd bh = mnmaj(TA(L::SH), (uint32_t)((L::DSH - L::SH) * kTile));
-            mma64(tmem, kmaj(TA(L::X)), bh, 128, false);
-            mma64(tmem, kmaj(TA(L::X)), mnmaj(TA(L::SL), (uint32_t)((L::DSL - L::SL) * kTile)), 128, true);
-            if constexpr (!EX) mma64(tmem, kmaj(TA(L::XL)), bh, 128, true);
+            mma64(tmem, kmaj(TA(L::Q)), bh, 128, false);
+            mma64(tmem, kmaj(TA(L::Q)), mnmaj(TA(L::SL), (uint32_t)((L::DSL - L::SL) * kTile)), 128, true);
+            if constexpr (!EX) mma64(tmem, kmaj(TA(L::QL)), bh, 128, true);
         } else {  // X dS' into columns 64-127
-            mma64(tmem + 64, kmaj(TA(L::X)), mnmaj(TA(L::DSH)), 64, false);
-            mma64(tmem + 64, kmaj(TA(L::X)), mnmaj(TA(L::DSL)), 64, true);
-            if constexpr (!EX) mma64(tmem + 64, kmaj(TA(L::XL)), mnmaj(TA(L::DSH)), 64, true);
+            mma64(tmem + 64, kmaj(TA(L::Q)), mnmaj(TA(L::DSH)), 64, false);
+            mma64(tmem + 64, kmaj(TA(L::Q)), mnmaj(TA(L::DSL)), 64, true);
+            if constexpr (!EX) mma64(tmem + 64, kmaj(TA(L::QL)), mnmaj(TA(L::DSH)), 64, true);
         }
         mma64(tmem + 128, kmaj(TA(L::Q)), kmaj(TA(L::X)), 64, false);  // [Sc; G]
         if constexpr (!EX) {
@@ -875,24 +876,26 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
     }
     ok = cs.wait();
 
-    // ---- Z (Falcon-1) and P: row i = ln < 64, columns c0 ..
+    // ---- P (rows 0-63 of [Sc; G]) and, beside it, Z (Falcon-1; from X S in lanes 64-127): row i, columns c0 ..
     if (ok) {
+        if (ln >= 64 && !IP) {
+            const int i = ln - 64;
+            const float di = s.eLx[i];
+            float v[32];
+            tld32(tq + c0, v);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t off = sw128(i, c0 + 8 * q);
+                float y[8];
+                row8<EX>(TP(L::YZ), TP(L::ZL), off, y);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = fmaf(-di, v[8 * q + e], y[e]);
+                st8_hilo(TP(L::YZ), TP(L::ZL), off, y);
+            }
+        }
         if (ln < 64) {
             const int i = ln;
             float v[32];
-            if constexpr (!IP) {
-                const float di = s.eLx[i];
-                tld32(tq + c0, v);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t off = sw128(i, c0 + 8 * q);
-                    float y[8];
-                    row8<EX>(TP(L::YZ), TP(L::ZL), off, y);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = fmaf(-di, v[8 * q + e], y[e]);
-                    st8_hilo(TP(L::YZ), TP(L::ZL), off, y);
-                }
-            }
             const int ph = IP ? L::YZ : L::PRH, pl = IP ? L::ZL : L::PRL;
             const float li = s.L[i];
             tld32(tq + 128 + c0, v);
@@ -907,24 +910,25 @@ __global__ void __launch_bounds__(kCT, sizeof(Tin) == 2 ? 2 : 1) falcon_bwd_grad
         cs.publish();
         if (tid == 0) {
             tc_fence_after();
+            // both into lanes 64-127 (the A operands start one slot early: their first halves are unused)
             if constexpr (!IP) {  // R = T Z into columns 0-63
-                mma64(tmem, kmaj(TA(L::TH)), mnmaj(TA(L::YZ)), 64, false);
-                mma64(tmem, kmaj(TA(L::TH)), mnmaj(TA(L::ZL)), 64, true);
-                mma64(tmem, kmaj(TA(L::TL)), mnmaj(TA(L::YZ)), 64, true);
+                mma64(tmem, kmaj(TA(L::SL)), mnmaj(TA(L::YZ)), 64, false);
+                mma64(tmem, kmaj(TA(L::SL)), mnmaj(TA(L::ZL)), 64, true);
+                mma64(tmem, kmaj(TA(L::TH)), mnmaj(TA(L::YZ)), 64, true);
             }
             const int ph = IP ? L::YZ : L::PRH, pl = IP ? L::ZL : L::PRL;  // P^T dO into columns 192-255
-            mma64(tmem + 192, mnmaj(TA(ph)), mnmaj(TA(L::DO)), 64, false);
-            mma64(tmem + 192, mnmaj(TA(pl)), mnmaj(TA(L::DO)), 64, true);
-            if constexpr (!EX) mma64(tmem + 192, mnmaj(TA(ph)), mnmaj(TA(L::DOL)), 64, true);
+            mma64(tmem + 192, mnmaj(TA(ph - 1)), mnmaj(TA(L::DO)), 64, false);
+            mma64(tmem + 192, mnmaj(TA(pl - 1)), mnmaj(TA(L::DO)), 64, true);
+            if constexpr (!EX) mma64(tmem + 192, mnmaj(TA(ph - 1)), mnmaj(TA(L::DOL)), 64, true);
             mma_commit(cs.bar);
         }
         ok = cs.wait();
     }
 
-    // ---- R (Falcon-1) to tiles; dR = P^T dO + diag(w) X dS' (Falcon-1: tiles; 1A: dV); dw
+    // ---- R (Falcon-1) to tiles; dR = P^T dO + diag(w) X dS' (Falcon-1: tiles; 1A: dV); dw: lanes 64-127
     if (ok) {
-        if (ln < 64) {
-            const int i = ln;
+        if (ln >= 64) {
+            const int i = ln - 64;
             const float wi = s.w[i];
             float xd[32], r[32], d[32];
             tld32(tq + 64 + c0, xd);
