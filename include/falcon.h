@@ -207,7 +207,11 @@ int falcon_kernel_for(int variant, const falcon_dims_t* dims, int chunk);
  *             nonzero); contents ignored on entry, unspecified on return
  * Every output and the workspace must overlap no other argument. Alignment: q, k, v, tail, dout,
  * S0, dS_final, dq, dk, dv, dS0, dtail 16 bytes; beta, lambda, dbeta, dlambda 4; workspace 256.
- * Shapes other than the above return FALCON_ERR_UNSUPPORTED. Asynchronous on `stream`.
+ * Shapes other than the above return FALCON_ERR_UNSUPPORTED. Asynchronous on `stream`: with 4 or
+ * more sequences (B*H) the call runs them in 2 (16 or more: 4) groups on streams of the library's
+ * own (made once per device, non-blocking), which wait for `stream` first and which `stream` waits
+ * for at the end, so work ordered on `stream` stays ordered and a CUDA graph capture of `stream`
+ * takes them in. Calls from several host threads are serialised while they enqueue.
  */
 int falcon_bwd(int variant, const void* q, const void* k, const void* v, const float* beta,
                const float* lambda, const float* S0, const void* tail, const void* dout,
