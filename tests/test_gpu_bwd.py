@@ -144,6 +144,43 @@ def test_sequence_groups(B, H):
     _check(f"groups B={B} H={H}", _gpu(F1, inp), _ref(F1, inp))
 
 
+def test_graph_capture():
+    """One falcon_bwd call captured into a CUDA graph (two groups of sequences, so the library's own
+    streams join the capture) and replayed on new inputs copied into the same buffers."""
+    B, H, T = 2, 4, 150
+    names = ("q", "k", "v", "beta", "lam", "S0", "dout", "dS_final")
+    a, b = _inputs(F1, 61, T, B=B, H=H), _inputs(F1, 62, T, B=B, H=H)
+    d = {n: a[n].cuda().contiguous() for n in names}
+    f32 = dict(dtype=torch.float32, device="cuda")
+    out = {"dq": torch.empty(B, H, T, 64, **f32), "dk": torch.empty(B, H, T, 64, **f32),
+           "dv": torch.empty(B, H, T, 64, **f32), "dbeta": torch.empty(B, H, T, **f32),
+           "dlam": torch.empty(B, H, T, **f32), "dS0": torch.empty(B, H, 64, 64, **f32)}
+    dims = F.make_dims(B, H, T, 64, 64, dtype=F.FALCON_BF16)
+    ws = torch.empty(F.falcon_bwd_workspace_bytes(F1, dims, 64), dtype=torch.uint8, device="cuda")
+
+    def call():
+        st = F.falcon_bwd(F1, d["q"], d["k"], d["v"], d["beta"], d["lam"], d["S0"], None, d["dout"], d["dS_final"],
+                          out["dq"], out["dk"], out["dv"], out["dbeta"], out["dlam"], out["dS0"], None, dims, 64, ws,
+                          stream=torch.cuda.current_stream().cuda_stream)
+        assert st == 0
+
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        call()  # the library's streams and kernel attributes exist before the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for inp in (a, b):
+        for n in names:
+            d[n].copy_(inp[n])
+        g.replay()
+        torch.cuda.synchronize()
+        got = {n: t.cpu().double().numpy() for n, t in out.items()}
+        got["dtail"] = None
+        _check("graph replay", got, _ref(F1, inp))
+
+
 def test_argument_errors():
     inp = _inputs(F1, 56, 64)
     d = {n: inp[n].cuda() for n in ("q", "k", "v", "beta", "lam", "dout")}
