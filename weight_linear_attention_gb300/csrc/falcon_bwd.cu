@@ -21,16 +21,17 @@
 //             by definition: a zero denominator or the first step of a fresh sequence).
 // The chunk-start state adjoint is dS = M^T dS' + V with M = e^{L_C} I - X^T diag(w) T diag(e^Lx) X
 // and V = Q^T diag(e^L) dO - X^T diag(e^Lx) T^T P^T dO, so three launches do the whole pass:
-//   falcon_bwd_prep   every chunk at once: T, the forward transition (M and M^T, U = X^T diag(w) T Y)
-//                     and V;
-//   falcon_bwd_chain  per sequence (one CTA, the carried matrix in tensor memory, one tcgen05 product
-//                     per step): S_{n+1} = M_n S_n + U_n forward, then dS_n = M_n^T dS_{n+1} + V_n
-//                     backward, storing S_n and dS_{n+1};
+//   falcon_bwd_prep   every chunk at once: T, the forward transition (M, U = X^T diag(w) T Y), the
+//                     chunk's scalars and V;
+//   falcon_bwd_chain  per sequence (two CTAs, one per scan; the carried matrix in tensor memory, one
+//                     tcgen05 product per step): S_{n+1} = M_n S_n + U_n forward and dS_n =
+//                     M_n^T dS_{n+1} + V_n backward, storing S_n and dS_{n+1};
 //   falcon_bwd_grad   every chunk at once: all input gradients from S_n and dS_{n+1}.
 // prep and grad run one 256-thread CTA per chunk, two per SM, every 64 x 64 x 64 product a tcgen05
 // bf16 product with the fp32 operands split into bf16 hi and lo parts (hi*hi + hi*lo + lo*hi, fp32
 // sums in tensor memory); the scalars, the per-element factors and the triangular inverse run on the
-// CUDA cores in fp32.
+// CUDA cores in fp32. With 4 or more sequences a call runs them as 2 or 4 groups, each group's three
+// kernels on a stream of its own (its chain on a high-priority one).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -514,7 +515,7 @@ struct GradLay {
 };
 
 // --------------------------------------------------------------------------------------------------
-// falcon_bwd_prep: per chunk T, the forward transition M (and M^T), U = X^T diag(w) T Y and
+// falcon_bwd_prep: per chunk T, the forward transition M, U = X^T diag(w) T Y and
 // V = Ao^T dO with Ao = diag(e^L) Q - P T diag(e^Lx) X (the chunk's read of its start state).
 // Falcon-1, as products: [Sc; G] = [Q; X] X^T; P and A from them; T = (I + A)^{-1} on the CUDA cores;
 // E = [P; X^T diag(w)] T; E [diag(e^Lx) X | Y] = [P T diag(e^Lx) X, . ; K, U] with M = e^{L_C} I - K;
