@@ -48,7 +48,7 @@ def test_chunk_flops():
     w = I.WORKLOADS["f1_b8h12t1024_bf16"]
     per = 2 * (4 * 64 ** 3 + 2 * 64 ** 3 + 64 ** 3 / 2)
     assert bench._chunk_flops(w) == per * 96 * 16
-    assert abs(bench._chunk_flops(w) - 5.2e9) < 0.1e9  # the survey's ~5.2 GFLOP for this config
+    assert abs(bench._chunk_flops(w) - 5.2e9) < 0.1e9  # ~5.2 GFLOP of chunk algebra for this config
     assert bench._chunk_flops(I.WORKLOADS["f1a_b8h12t1024_bf16"]) == 2 * 4 * 64 ** 3 * 96 * 16
     # Falcon-2 / 2A: the same products at their own length
     assert bench._chunk_flops(I.WORKLOADS["f2_b8h12t2048_bf16"]) == per * 96 * 32
