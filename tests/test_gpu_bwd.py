@@ -135,13 +135,14 @@ def test_headline_shape_all_sequences(variant):
         _check(f"v{variant} headline row {b}", gs, r)
 
 
+@pytest.mark.parametrize("variant,dtype", [(F1, "bf16"), (F1A, "bf16"), (F1, "f32"), (F1A, "f32")])
 @pytest.mark.parametrize("B,H", [(1, 1), (1, 3), (2, 2), (1, 15), (17, 1), (3, 11)])
-def test_sequence_groups(B, H):
+def test_sequence_groups(B, H, variant, dtype):
     """A call runs its sequences unsplit (fewer than 4), in two groups (4 to 15) or in four groups
     (16 and more, here of unequal sizes: 17 and 33 sequences) on streams of their own; every
     sequence of every group is compared, with a ragged last chunk and a nonzero initial state."""
-    inp = _inputs(F1, 57 + B * H, 150, B=B, H=H)
-    _check(f"groups B={B} H={H}", _gpu(F1, inp), _ref(F1, inp))
+    inp = _inputs(variant, 57 + B * H, 150, B=B, H=H, dtype=dtype)
+    _check(f"groups v{variant} {dtype} B={B} H={H}", _gpu(variant, inp), _ref(variant, inp))
 
 
 def test_graph_capture():
